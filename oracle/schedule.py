@@ -1,0 +1,165 @@
+"""Oracle for the tile schedule: mappings F(i) -> (m, n), CTA assignment and Stream-K splits.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, the smoke check and the
+benchmark's CPU-baseline leg, never by the product library.  It shares no code
+with the CUDA path; it restates the pages' definitions as plain Python.
+
+Sources (page title, section):
+  * "Deep dive into DeepGEMM" (blog.kumaling.xyz/posts/deepgemm-sm90), panel
+    "CTA <-> output tile: mapping first, then assignment" and its table of
+    common mapping families (linear N-fast, linear M-fast, grouped-M strip,
+    grouped-N strip).  The panel also fixes that persistent scheduling is not a
+    mapping: it only chooses which linear task i a fixed worker p takes,
+    i = p + iter * P.
+  * "H100 . Kernel Design" (runguoli.com H100 course notes, Lesson 8),
+    section 9.2 (non-persistent: one CTA per tile), 9.3 (persistent), 9.4
+    (wave quantisation: 150 tiles on 132 SMs -> 56.8 %), 10.3 (Stream-K,
+    hybrid "tail only" with the 50 % rule, backward tile iteration).
+  * "H100 . Stream-K scheduling" (same course, Lesson 8.1), sections 2-6:
+    unit of work, split, K_idx = tile_iter_start - output_tile_iter_start,
+    is_final_split <=> K_idx + k_tile_count == k_tiles_per_output_tile, the
+    lock that counts accumulated k-tiles, deterministic left-to-right order.
+
+Readings where the pages leave a step open (each is listed in the design notes):
+  * grouped strips with a ragged last strip use its true height/width
+    gs = min(G, tiles left);
+  * the Stream-K unit u owns global MAC iterations [floor(u W / P),
+    floor((u+1) W / P)), W = T * Kt; the worked example in Lesson 8.1 section 3
+    (3 tiles x 90 k-tiles over 4 units: unit 1 continues tile 0 at K_idx 67
+    with 23 k-tiles) fixes the floor;
+  * Stream-K visits tiles in the mapping's F order (iteration g belongs to
+    linear task g // Kt);
+  * the hybrid schedule runs T - (T mod P) tiles data-parallel and splits only
+    the last T mod P tiles, unless the tail wave is more than half full, in
+    which case it stays fully data-parallel;
+  * backward iteration reverses the order of a unit's splits; k stays
+    ascending inside each split.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+LINEAR_NFAST, LINEAR_MFAST, GROUPED_M, GROUPED_N = 0, 1, 2, 3
+STATIC, PERSISTENT, STREAMK, STREAMK_HYBRID = 0, 1, 2, 3
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def tile_grid(M: int, N: int, K: int, BM: int, BN: int, BK: int):
+    """Output-tile grid: (Mt, Nt, Kt) = (ceil(M/BM), ceil(N/BN), ceil(K/BK))."""
+    return ceil_div(M, BM), ceil_div(N, BN), ceil_div(K, BK)
+
+
+def tile_map(kind: int, group: int, Mt: int, Nt: int, i: int):
+    """F(i) -> (m, n) for linear task i in [0, Mt*Nt)."""
+    if not 0 <= i < Mt * Nt:
+        raise IndexError(i)
+    if kind == LINEAR_NFAST:        # C00 -> C01 -> ... : row-major walk
+        return i // Nt, i % Nt
+    if kind == LINEAR_MFAST:        # C00 -> C10 -> ... : column-major walk
+        return i % Mt, i // Mt
+    if kind == GROUPED_M:           # strips of G tile-rows, M-fast inside a strip
+        strip = i // (group * Nt)
+        r = i % (group * Nt)
+        m0 = strip * group
+        height = min(group, Mt - m0)
+        return m0 + r % height, r // height
+    if kind == GROUPED_N:           # strips of G tile-columns, N-fast inside a strip
+        strip = i // (group * Mt)
+        r = i % (group * Mt)
+        n0 = strip * group
+        width = min(group, Nt - n0)
+        return r // width, n0 + r % width
+    raise ValueError(kind)
+
+
+def wave_efficiency(T: int, P: int) -> float:
+    """Tiles over occupied wave slots: T / (ceil(T/P) * P)."""
+    return T / (ceil_div(T, P) * P)
+
+
+def operand_bands(tiles, BM: int, BN: int, K: int, elt_bytes: int):
+    """Unique A row-bands and B column-bands touched by a set of (m, n) tiles, and
+    their bytes (the DeepGEMM panel's 'A+B logical working set')."""
+    ms = {m for m, _ in tiles}
+    ns = {n for _, n in tiles}
+    return len(ms), len(ns), len(ms) * BM * K * elt_bytes + len(ns) * BN * K * elt_bytes
+
+
+@dataclass(frozen=True)
+class Split:
+    """One unit's contribution to one output tile."""
+    tile: int          # linear task index i (its (m, n) is tile_map(i))
+    k_idx: int         # first k-tile inside the tile
+    k_count: int       # number of k-tiles
+    k_tiles: int       # k-tiles per output tile (Kt)
+
+    @property
+    def is_final(self) -> bool:
+        return self.k_idx + self.k_count == self.k_tiles
+
+    @property
+    def requires_fixup(self) -> bool:
+        return not (self.k_idx == 0 and self.is_final)
+
+    @property
+    def role(self) -> str:
+        if not self.requires_fixup:
+            return "whole"
+        if self.k_idx == 0:
+            return "first"
+        return "final" if self.is_final else "middle"
+
+
+def streamk_unit_range(u: int, P: int, W: int):
+    return (u * W) // P, ((u + 1) * W) // P
+
+
+def streamk_splits(u: int, P: int, T_sk: int, Kt: int, tile_offset: int = 0):
+    """The splits of Stream-K unit u over tiles [tile_offset, tile_offset + T_sk)."""
+    W = T_sk * Kt
+    begin, end = streamk_unit_range(u, P, W)
+    out = []
+    g = begin
+    while g < end:
+        t = g // Kt
+        tile_start = t * Kt                   # output_tile_iter_start
+        k_idx = g - tile_start                # K_idx = tile_iter_start - output_tile_iter_start
+        count = min(end, tile_start + Kt) - g
+        out.append(Split(tile_offset + t, k_idx, count, Kt))
+        g += count
+    return out
+
+
+def hybrid_split_count(T: int, P: int) -> int:
+    """Tiles given to Stream-K under the hybrid rule (0 = fully data-parallel)."""
+    tail = T % P
+    if tail == 0 or 2 * tail > P:
+        return 0
+    return tail
+
+
+def work_items(schedule: int, u: int, P: int, T: int, Kt: int, backward: bool = False):
+    """Ordered work list of worker u: a list of Split (whole tiles have k_idx 0, k_count Kt).
+
+    STATIC: worker u is CTA u of a grid of T CTAs and takes task u.
+    PERSISTENT: worker u takes u, u + P, u + 2P, ...
+    STREAMK: all T tiles are split over P units.
+    STREAMK_HYBRID: data-parallel full waves, then Stream-K over the tail.
+    """
+    if schedule == STATIC:
+        return [Split(u, 0, Kt, Kt)] if u < T else []
+    if schedule == PERSISTENT:
+        return [Split(i, 0, Kt, Kt) for i in range(u, T, P)]
+    if schedule == STREAMK:
+        sk = streamk_splits(u, P, T, Kt)
+        return sk[::-1] if backward else sk
+    if schedule == STREAMK_HYBRID:
+        T_sk = hybrid_split_count(T, P)
+        T_dp = T - T_sk
+        dp = [Split(i, 0, Kt, Kt) for i in range(u, T_dp, P)]
+        sk = streamk_splits(u, P, T_sk, Kt, tile_offset=T_dp) if T_sk else []
+        return dp + (sk[::-1] if backward else sk)
+    raise ValueError(schedule)
