@@ -1,0 +1,382 @@
+"""Benchmark of the tile-scheduled GEMM on GB300: GEMM TFLOPS (2MNK / device time).
+
+One step = one pass of the hot path (plan already built; one gemm_run: TMA
+producer, tcgen05 MMA, epilogue, and for Stream-K schedules the fixup) over one
+batch of seeded synthetic input resident in HBM.  L2 is flushed (a 512 MiB
+write) between timed steps, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Rank 0 prints ONE JSON line.  Under torchrun every rank runs the same problem
+on its own GPU (independent problems, no data-path collective): weak scaling.
+`--impl reference` times the CPU oracle (FP64, all host cores) on a bounded
+row sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import make_gemm_inputs  # noqa: E402
+from synthetic.workloads import WORKLOADS  # noqa: E402
+
+METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
+HEADLINE = "c2_bf16_4096"
+EXTRA = ["c1_bf16_256", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
+         "c5_bf16_epilogue"]
+DESCR = {
+    "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
+    "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 tiles, grouped-M G=8, persistent",
+    "c2x_bf16_8192": "BF16 GEMM 8192^3, N(0,1), BF16 out, grouped-M G=8, persistent",
+    "c3_e4m3_8192": "FP8-e4m3 GEMM 8192^3, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, persistent",
+    "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, Stream-K with fixup",
+    "c4_bf16_persistent": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, grouped-M G=8 persistent",
+    "c5_bf16_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=bf16(ReLU(0.5 acc + bias)), grouped-M G=8",
+}
+L2_FLUSH_BYTES = 512 << 20
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h"]
+
+
+def flops(w):
+    return 2.0 * w["M"] * w["N"] * w["K"]
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tile_scheduled_tensor_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def dram_traffic(name):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(name)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="tst_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names[1:], parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_rate(w, inp, budget_s=10.0, max_rows=None):
+    """Time the oracle (as it stands) on whole output rows until ~budget_s of CPU work."""
+    import oracle
+    rows_done, t_total, r0 = 0, 0.0, 0
+    step = 4
+    while t_total < budget_s and r0 < w["M"] and (max_rows is None or rows_done < max_rows):
+        rows = np.arange(r0, min(r0 + step, w["M"]), dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
+                    relu=w.get("relu", False), rows=rows)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        rows_done += rows.size
+        r0 += rows.size
+        if dt < budget_s / 8:
+            step *= 2
+    fl = 2.0 * rows_done * w["N"] * w["K"]
+    return fl / t_total / 1e12, rows_done, t_total
+
+
+def run_reference(args):
+    world, rank, _ = setup_dist()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build_oracle()
+    w = WORKLOADS[args.workload]
+    inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
+                           bias_dist=w.get("bias_dist"))
+    rows_per_step = 8
+    per_step_flops = 2.0 * rows_per_step * w["N"] * w["K"]
+    for s in range(args.warmup):
+        oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
+                    relu=w.get("relu", False), rows=np.arange(s * rows_per_step, (s + 1) * rows_per_step) % w["M"])
+    times = []
+    for s in range(args.steps):
+        rows = (np.arange(rows_per_step) + (s + args.warmup) * rows_per_step) % w["M"]
+        t0 = time.perf_counter()
+        oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
+                    relu=w.get("relu", False), rows=rows.astype(np.int64))
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = per_step_flops / (ms / 1e3) / 1e12
+    cores = os.cpu_count()
+    sample = (f"{rows_per_step} output rows x {w['N']} columns x K={w['K']} per step of workload "
+              f"{args.workload}; TFLOPS scaled to 2*rows*N*K")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}"}, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = setup_dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    import tile_scheduled_tensor_gb300 as tst
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def prepare(name):
+        w = WORKLOADS[name]
+        inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
+                               bias_dist=w.get("bias_dist"))
+        plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
+                                    schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
+                                    has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
+                                    use_scales=w.get("use_scales", False), bn=w.get("bn", 0))
+        a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
+        b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
+        host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory()}
+        if inp.bias is not None:
+            host["bias"] = torch.from_numpy(inp.bias).pin_memory()
+        if inp.scales is not None:
+            host["scales"] = torch.from_numpy(inp.scales).pin_memory()
+        dev = {k: v.cuda() for k, v in host.items()}
+        cdt = torch.bfloat16 if w["out"] == "bf16" else torch.float32
+        C = torch.empty(w["M"], w["N"], dtype=cdt, device="cuda")
+        return w, inp, plan, host, dev, C
+
+    def launch(plan, dev, C):
+        tst.gemm_run(plan, dev["A"], dev["B"], C, bias=dev.get("bias"), scales=dev.get("scales"),
+                     stream=stream.cuda_stream)
+
+    def time_device(name, steps, warmup, sampler=None):
+        w, inp, plan, host, dev, C = prepare(name)
+        for _ in range(warmup):
+            launch(plan, dev, C)
+        st, word = tst.gemm_status_query(plan)
+        if st != tst.TST_OK:
+            raise RuntimeError(f"{name}: device status {tst.gemm_status_string(st)} {word:#x}")
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.start()
+        times = []
+        t_wall = time.perf_counter()
+        for _ in range(steps):
+            flush_buf.fill_(1.0)        # evict the operands from L2 (outside the timed events)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(plan, dev, C)
+            e1.record(stream)
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+        barrier()
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        ms = [a.elapsed_time(b) for a, b in times]
+        st, word = tst.gemm_status_query(plan)
+        if st != tst.TST_OK:
+            raise RuntimeError(f"{name}: device status {tst.gemm_status_string(st)} {word:#x}")
+        return dict(w=w, inp=inp, plan=plan, host=host, dev=dev, C=C, ms=ms, clocks=clocks, wall=wall)
+
+    def time_e2e(r, steps):
+        """Same metric through the public API with host buffers: pinned H2D of the inputs, the
+        GEMM, D2H of the result, all inside the timed region."""
+        w, plan, host, dev, C = r["w"], r["plan"], r["host"], r["dev"], r["C"]
+        C_host = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = C.numel() * C.element_size()
+        for _ in range(2):
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            launch(plan, dev, C)
+            C_host.copy_(C, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            launch(plan, dev, C)
+            C_host.copy_(C, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        return ms, h2d, d2h
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    peaks, peak_kind = measured_peaks()
+    sampler = ClockSampler(local) if rank == 0 else None
+    head = time_device(args.workload, args.steps, args.warmup, sampler)
+    w = head["w"]
+    ms_mean = max_over_ranks(sum(head["ms"]) / len(head["ms"]))
+    fl = flops(w)
+    value = world * fl / (ms_mean / 1e3) / 1e12
+    is_fp8 = w["dtype"] == "e4m3"
+    peak_tf = peaks["bf16_tflops"] * (2.0 if is_fp8 else 1.0)
+    achieved = fl / (ms_mean / 1e3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e(head, max(3, args.steps // 2))
+    e2e_ms = max_over_ranks(e2e_ms)
+
+    extra = {}
+    if not args.no_extra:
+        for name in EXTRA:
+            if name == args.workload:
+                continue
+            r = time_device(name, max(5, args.steps // 2), 3)
+            ms = sum(r["ms"]) / len(r["ms"])
+            pk = peaks["bf16_tflops"] * (2.0 if r["w"]["dtype"] == "e4m3" else 1.0)
+            tf = flops(r["w"]) / (ms / 1e3) / 1e12
+            extra[name] = {"tflops": round(tf, 1), "ms": round(ms, 4), "frac_of_peak": round(tf / pk, 4),
+                           "tiles": int(r["plan"].info.tiles), "grid": int(r["plan"].info.grid),
+                           "bn": int(r["plan"].info.bn), "describe": DESCR[name]}
+            del r
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, rows, secs = cpu_oracle_rate(w, head["inp"], budget_s=10.0)
+        cpu = {"value": rate, "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{rows} output rows x {w['N']} x K={w['K']} of {args.workload} in {secs:.1f} s "
+                         f"(FP64, OpenMP over rows); TFLOPS scaled to 2*rows*N*K"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3" if is_fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "M": w["M"], "N": w["N"],
+                       "K": w["K"], "tile": f"{head['plan'].info.bm}x{head['plan'].info.bn}x{head['plan'].info.bk}",
+                       "grid": int(head["plan"].info.grid), "stages": int(head["plan"].info.stages),
+                       "l2": "flushed (512 MiB write) between timed steps", "accumulate": "fp32",
+                       "parallelism": f"{world} independent problem(s), one per GPU"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tf, "traffic": dram_traffic(args.workload),
+                         "peak_source": f"{peak_kind} bf16_tflops (burst)" + (" x2 nominal fp8/bf16 ratio" if is_fp8 else ""),
+                         "algorithmic_flops_per_launch": fl},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * fl / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": head["clocks"],
+            "workloads": extra,
+            "kernel_hash": kernel_hash(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

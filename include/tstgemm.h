@@ -1,0 +1,238 @@
+/*
+ * tstgemm.h - C ABI of the tile-scheduled GEMM library (libtstgemm.so).
+ *
+ * One operation: the tiled dense GEMM
+ *
+ *     C[i][j] = out_cast( act( alpha * sA * sB * sum_k A[i][k] * B[j][k] + bias[j] ) )
+ *
+ * with BF16 or FP8-e4m3 inputs and FP32 accumulation, computed on one GPU by
+ * hand-written sm_103a kernels (TMA producer warp, tcgen05.mma issuer with the
+ * accumulator in Tensor Memory, epilogue warps).  The GEMM is cut into output
+ * tiles; a mapping F(i) -> (m, n) says which tile is linear task i, and a
+ * schedule says which tasks (or which k-ranges of them) each CTA takes.
+ *
+ * Sources of the operation and its vocabulary:
+ *   - C = A x B per output tile, the mapping F(i) -> (m,n) and its families
+ *     (linear N-fast, linear M-fast, grouped-M strip, grouped-N strip), and
+ *     "persistent is an assignment, not a mapping": "Deep dive into DeepGEMM"
+ *     (blog.kumaling.xyz/posts/deepgemm-sm90), panel "CTA <-> output tile:
+ *     mapping first, then assignment" and its mapping-family table.
+ *   - Non-persistent, persistent and Stream-K schedules, the hybrid 50 % rule,
+ *     backward tile iteration: "H100 . Kernel Design" (runguoli.com H100 course
+ *     notes, Lesson 8), sections 9.2-9.4 and 10.1-10.3.
+ *   - Stream-K units, splits, K_idx, is_final_split, the fixup lock:
+ *     "H100 . Stream-K scheduling" (same course, Lesson 8.1), sections 2-6.
+ *   - Epilogue order Z = alpha*Acc -> + bias -> activation -> cast:
+ *     "H100 . Kernel Design", section 12.2.
+ *   - FP8 tensor-wise scales: "H100 . WGMMA Part 2" (Lesson 7), section 11.
+ *
+ * Conventions for every call:
+ *   - Pointers named A, B, C, bias, scales are DEVICE pointers owned by the
+ *     caller; they must stay valid until the stream work that uses them ends.
+ *   - A is M x K row-major (K contiguous), B is N x K row-major (K contiguous),
+ *     C is M x N row-major.  BF16 elements are 2 bytes, e4m3 1 byte.
+ *   - Every call returns a tst_status; nothing aborts the process or prints
+ *     (unless the environment variable TST_LOG=1 is set).
+ *   - gemm_run is asynchronous and ordered on the given stream.
+ *   - A plan is not re-entrant: do not run one plan on two streams at once
+ *     (its Stream-K workspace, locks and status word are per plan).
+ */
+#ifndef TSTGEMM_H
+#define TSTGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TST_OK = 0,
+    TST_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum value */
+    TST_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+    TST_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned or K * elt not a multiple of 16 */
+    TST_ERR_OOM = 4,           /* device allocation for the plan's workspace failed */
+    TST_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    TST_ERR_TIMEOUT = 6,       /* a bounded device-side wait ran out (see gemm_status_query) */
+    TST_ERR_DEVICE_CHECK = 7,  /* a device-side consistency check failed */
+    TST_ERR_NO_DEVICE = 8      /* the plan was built host-only, or no GPU is present */
+} tst_status;
+
+/* input element type */
+typedef enum { TST_BF16 = 0, TST_E4M3 = 1 } tst_dtype;
+
+/* output element type */
+typedef enum { TST_OUT_F32 = 0, TST_OUT_BF16 = 1 } tst_out_dtype;
+
+/* A M x K (K contiguous), B N x K (K contiguous), C M x N row-major ("TN").
+ * e4m3 tensor-core operands must be K-major, which this layout is. */
+typedef enum { TST_LAYOUT_A_ROW_B_NK = 0 } tst_layout;
+
+/* Mapping F(i) -> (m, n) over the Mt x Nt grid of scheduled tiles.
+ *   LINEAR_NFAST: m = i / Nt, n = i % Nt              (C00 -> C01 -> ...)
+ *   LINEAR_MFAST: m = i % Mt, n = i / Mt              (C00 -> C10 -> ...)
+ *   GROUPED_M:    strips of `group` tile-rows, M-fast inside a strip
+ *   GROUPED_N:    strips of `group` tile-columns, N-fast inside a strip
+ * A ragged last strip uses its true height / width. */
+typedef enum {
+    TST_MAP_LINEAR_NFAST = 0,
+    TST_MAP_LINEAR_MFAST = 1,
+    TST_MAP_GROUPED_M = 2,
+    TST_MAP_GROUPED_N = 3
+} tst_mapping_kind;
+
+typedef struct {
+    int32_t kind;   /* tst_mapping_kind */
+    int32_t group;  /* strip width G in tiles (>= 1) for the grouped kinds; ignored otherwise */
+} tst_mapping;
+
+/* Assignment of linear tasks to CTAs.
+ *   STATIC:         grid = T CTAs, CTA b computes task b (one tile each).
+ *   PERSISTENT:     grid = P CTAs, CTA p computes tasks p, p + P, p + 2P, ...
+ *   STREAMK:        the T * Kt MAC iterations are cut into P equal ranges
+ *                   (unit u owns [floor(uW/P), floor((u+1)W/P))); partial tiles
+ *                   are combined through a workspace in a deterministic
+ *                   left-to-right order.
+ *   STREAMK_HYBRID: full data-parallel waves, Stream-K over the last T mod P
+ *                   tiles only; stays fully data-parallel when that tail wave is
+ *                   more than half full. */
+typedef enum {
+    TST_STATIC = 0,
+    TST_PERSISTENT = 1,
+    TST_STREAMK = 2,
+    TST_STREAMK_HYBRID = 3
+} tst_schedule;
+
+/* Fused epilogue: out = cast( relu?( alpha * sA * sB * acc + bias[n] ) ). */
+typedef struct {
+    int32_t out_dtype;   /* tst_out_dtype */
+    float alpha;         /* multiplies the FP32 accumulator */
+    int32_t has_bias;    /* 1: bias is an FP32 device vector of length N, added per column */
+    int32_t relu;        /* 1: apply max(z, 0) after the bias */
+    int32_t use_scales;  /* 1: scales is an FP32 device array {sA, sB} folded into alpha */
+} tst_epilogue;
+
+/* Optional plan settings.  Zero-initialise and set what you need. */
+typedef struct {
+    int32_t bn;            /* output tile width: 0 = choose, else 128 or 256 (tile height is 128) */
+    int32_t num_ctas;      /* persistent / Stream-K grid size P: 0 = number of SMs */
+    int32_t sk_backward;   /* 1: a Stream-K unit visits its splits last-first */
+    int32_t host_only;     /* 1: build the schedule without a GPU (gemm_run then fails);
+                              num_sms must be set */
+    int32_t num_sms;       /* SM count to plan for when host_only (else queried) */
+    int32_t reserved0;
+    int64_t timeout_ns;    /* limit of every device-side wait: 0 = 10 s */
+} tst_plan_options;
+
+/* What the plan decided (for logging and tests). */
+typedef struct {
+    int64_t M, N, K;
+    int32_t bm, bn, bk;        /* tile shape (bk = 64 for BF16, 128 for e4m3) */
+    int32_t stages;            /* shared-memory ring depth */
+    int32_t mt, nt, kt;        /* tiles along M, N and k-tiles along K */
+    int64_t tiles;             /* T = mt * nt */
+    int32_t grid;              /* CTAs launched */
+    int32_t num_sms;           /* SMs planned for */
+    int32_t sk_tiles;          /* tiles handled by Stream-K (0 if none) */
+    int32_t dp_tiles;          /* tiles handled whole, data-parallel */
+    int32_t max_items_per_cta; /* longest work list of any CTA */
+    int32_t smem_bytes;        /* dynamic shared memory per CTA */
+    int64_t workspace_bytes;   /* device bytes owned by the plan (Stream-K partials + locks + status) */
+} tst_plan_info;
+
+typedef struct tst_plan tst_plan;
+
+/* One entry of a CTA's work list, as the device enumerates it. */
+typedef struct {
+    int32_t tile;      /* linear task i */
+    int32_t m, n;      /* F(i) */
+    int32_t k_begin;   /* first k-tile of the split (K_idx) */
+    int32_t k_count;   /* k-tiles in the split */
+    int32_t flags;     /* bit 0: final split; bit 1: split needs fixup */
+} tst_work_item;
+
+/* Create a plan for C = A x B with the given shapes and choices.  Validates the
+ * arguments, queries the device (unless opts->host_only), chooses the tile
+ * shape and pipeline depth, builds the schedule, and allocates the plan-owned
+ * device memory (Stream-K partial tiles + one lock per split tile + a status
+ * word).  opts may be NULL.  On error *plan is set to NULL.
+ * Errors: INVALID_ARG (null plan/epi, M/N/K <= 0, sizes beyond int32 tiles,
+ * bad enum or group < 1), ALIGNMENT (K * elt not a multiple of 16 bytes, a
+ * requirement of the TMA descriptor's row stride), UNSUPPORTED (bn not 0/128/256,
+ * layout other than TST_LAYOUT_A_ROW_B_NK, e4m3 with FP32 scales absent is
+ * allowed: scales then default to 1 only if use_scales == 0), OOM, CUDA,
+ * NO_DEVICE. */
+tst_status gemm_plan_create(tst_plan **plan, int64_t M, int64_t N, int64_t K,
+                            tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                            tst_schedule schedule, const tst_epilogue *epi);
+
+/* gemm_plan_create with options (opts may be NULL). */
+tst_status gemm_plan_create_ex(tst_plan **plan, int64_t M, int64_t N, int64_t K,
+                               tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                               tst_schedule schedule, const tst_epilogue *epi,
+                               const tst_plan_options *opts);
+
+/* Launch the GEMM on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * A, B, C: device pointers, 16-byte aligned.  bias: FP32[N] when epi.has_bias,
+ * else ignored.  scales: FP32[2] = {sA, sB} when epi.use_scales, else ignored.
+ * The call enqueues a reset of the plan's status word and Stream-K locks and
+ * one kernel launch, then returns; it does not wait for the GPU.
+ * Errors: INVALID_ARG (null pointers), ALIGNMENT, NO_DEVICE, CUDA (launch
+ * failure).  Device-side failures (a wait that ran out) are reported by
+ * gemm_status_query after the stream has been synchronised. */
+tst_status gemm_run(tst_plan *plan, const void *A, const void *B, void *C,
+                    const float *bias, const float *scales, void *stream);
+
+/* F(i) for linear task i of the plan's tile grid (pure host computation).
+ * Errors: INVALID_ARG (null, i outside [0, T)). */
+tst_status gemm_tile_map(const tst_plan *plan, int64_t i, int32_t *m, int32_t *n);
+
+/* The plan's decisions.  Errors: INVALID_ARG. */
+tst_status gemm_plan_get_info(const tst_plan *plan, tst_plan_info *info);
+
+/* Work list of CTA `cta` in the order the device processes it (pure host
+ * computation from the same schedule code the kernel runs).  Writes at most
+ * `cap` items to `items` and the full count to *count.
+ * Errors: INVALID_ARG (null, cta outside [0, grid)). */
+tst_status gemm_work_items(const tst_plan *plan, int32_t cta, tst_work_item *items,
+                           int64_t cap, int64_t *count);
+
+/* Device-side status of the last gemm_run on this plan: TST_OK, TST_ERR_TIMEOUT
+ * or TST_ERR_DEVICE_CHECK.  Synchronises the stream of the last run first.
+ * The status stays until the next gemm_run resets it.  If `detail` is not NULL
+ * it receives the raw status word (code in bits 0-7, role in bits 8-15, CTA in
+ * bits 16-31). */
+tst_status gemm_status_query(tst_plan *plan, uint32_t *detail);
+
+/* Free the plan and its device memory.  NULL is accepted. */
+tst_status gemm_plan_destroy(tst_plan *plan);
+
+/* Human-readable name of a status code (static storage). */
+const char *gemm_status_string(tst_status s);
+
+/* Debug and test hooks.
+ * flags bit 0 (TST_DEBUG_TRACE): the kernel writes one record per work item
+ *   to trace_buf, a DEVICE buffer of `cap` int32 values; record r of CTA c is
+ *   at offset (c * max_items_per_cta + r) * 8 and holds
+ *   {cta, seq, tile, m, n, k_begin, k_count, flags}.  The call fails with
+ *   INVALID_ARG when cap < grid * max_items_per_cta * 8.
+ * flags bit 1 (TST_DEBUG_FAULT_SKIP_LOAD): the producer skips the TMA loads of
+ *   the first k-tile of its first work item (it still announces them), so the
+ *   MMA issuer's wait runs out: used to test that a bounded wait ends the
+ *   kernel with TST_ERR_TIMEOUT instead of hanging.
+ * flags bit 2 (TST_DEBUG_FAULT_SKIP_LOCK): first Stream-K splits never publish
+ *   their lock, so the later splits' waits run out (TST_ERR_TIMEOUT).
+ * The settings stay on the plan until changed; flags = 0 turns them off. */
+enum {
+    TST_DEBUG_TRACE = 1,
+    TST_DEBUG_FAULT_SKIP_LOAD = 2,
+    TST_DEBUG_FAULT_SKIP_LOCK = 4
+};
+tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, int64_t cap,
+                               int64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSTGEMM_H */

@@ -1,0 +1,250 @@
+"""GPU parity tests: the CUDA path, called through the C ABI, against the oracle.
+
+Bit-exact where the result is exactly representable (small integers, identity,
+one-hot decode probes, schedule traces); within the element-wise error bound
+otherwise; cross-schedule and run-to-run bitwise equality where the method
+fixes the summation order.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import tile_scheduled_tensor_gb300 as tst
+from oracle import schedule as S
+from synthetic.workloads import WORKLOADS
+
+from gemm_check import (assert_close, device_codes, freivalds, host_values, make_inputs, oracle_rows, plan_for,
+                        run_gemm, sample_rows, to_device)
+
+pytestmark = pytest.mark.gpu
+
+MAPPINGS = [("linear_nfast", 1), ("linear_mfast", 1), ("grouped_m", 8), ("grouped_n", 16), ("grouped_m", 3)]
+SCHEDULES = ["static", "persistent", "streamk", "streamk_hybrid"]
+
+
+def _gemm(M, N, K, dtype="bf16", dist="normal", case=11, out="f32", bias_dist=None, **plan_kw):
+    inp = synthetic.make_gemm_inputs(M, N, K, dtype, dist, case=case, bias_dist=bias_dist)
+    w = dict(M=M, N=N, K=K, dtype=dtype, out=out, mapping=plan_kw.pop("mapping", ("linear_nfast", 1)),
+             schedule=plan_kw.pop("schedule", "static"), bn=plan_kw.pop("bn", 128),
+             alpha=plan_kw.pop("alpha", 1.0), relu=plan_kw.pop("relu", False),
+             use_scales=plan_kw.pop("use_scales", dtype == "e4m3"), bias_dist=bias_dist)
+    plan = plan_for(w, **plan_kw)
+    C = run_gemm(plan, inp, out)
+    return inp, w, plan, C
+
+
+def test_single_tile_bf16_small_integers_exact():
+    inp, w, plan, C = _gemm(128, 128, 64, dist="int:4")
+    z, _ = oracle_rows(inp, w)
+    assert np.array_equal(host_values(C), z)
+
+
+def test_identity_gives_b_transpose_exactly():
+    n = 256
+    A = synthetic.bf16_bits(np.eye(n))
+    inp = synthetic.make_gemm_inputs(n, n, n, "bf16", "uniform", case=12)
+    inp.A = A
+    w = dict(M=n, N=n, K=n, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="persistent", bn=128)
+    C = run_gemm(plan_for(w), inp, "f32")
+    assert np.array_equal(host_values(C), oracle.decode(inp.B, "bf16").T)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("mapping", MAPPINGS)
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_small_integers_exact_every_dtype_mapping_schedule(dtype, bn, mapping, schedule):
+    # |partial sums| <= 64 * K < 2^24: every FP32 sum is exact whatever the order
+    M, N, K = 640, 768, 640
+    inp, w, plan, C = _gemm(M, N, K, dtype=dtype, dist="int:8", case=13, mapping=mapping, schedule=schedule,
+                            bn=bn, use_scales=False, num_ctas=37)
+    z, _ = oracle_rows(inp, w)
+    assert np.array_equal(host_values(C), z)
+
+
+def test_small_integers_bf16_output_exact():
+    # |C| <= 4 * 4 * 16 = 256 is exact in BF16
+    inp, w, plan, C = _gemm(384, 256, 16 * 8, dist="int:2", out="bf16", mapping=("grouped_m", 8),
+                            schedule="persistent")
+    z, _ = oracle_rows(inp, w)
+    assert np.abs(z).max() <= 256
+    assert np.array_equal(host_values(C), z)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_decode_probe_every_code_exact(dtype):
+    """Row r of A holds code r at k = 0; B is one-hot on k = 0: C[r, 0] = dec(code r) exactly.
+    Covers subnormals (checks that the tensor core keeps them)."""
+    if dtype == "bf16":
+        codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+        finite = np.isfinite(oracle.decode(codes, "bf16"))
+        # products with 1.0 of FP32-range values stay exact in the FP32 accumulator
+        codes = codes[finite]
+    else:
+        codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+        codes = codes[np.isfinite(oracle.decode(codes, "e4m3"))]
+    M, K, N = codes.size, (64 if dtype == "bf16" else 128), 16
+    A = np.zeros((M, K), dtype=codes.dtype)
+    A[:, 0] = codes
+    B = np.zeros((N, K), dtype=codes.dtype)
+    one = synthetic.bf16_bits(np.array([1.0])) if dtype == "bf16" else synthetic.e4m3_bytes(np.array([1.0], np.float32))
+    B[0, 0] = one[0]
+    inp = synthetic.GemmInputs(M, N, K, dtype, A, B, np.array([1, 1], np.float32) if dtype == "e4m3" else None, None)
+    w = dict(M=M, N=N, K=K, dtype=dtype, out="f32", mapping=("linear_nfast", 1), schedule="persistent", bn=128,
+             use_scales=False)
+    C = host_values(run_gemm(plan_for(w), inp, "f32"))
+    want = oracle.decode(codes, dtype)
+    got = C[:, 0]
+    assert np.array_equal(got, want), f"first mismatch at code {codes[np.argmax(got != want)]:#x}"
+    assert (C[:, 1:] == 0).all()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 8), (1, 300, 64), (300, 1, 64), (200, 136, 72), (129, 257, 520),
+                                   (127, 129, 1000), (1000, 1000, 24)])
+@pytest.mark.parametrize("schedule", ["static", "persistent", "streamk"])
+def test_ragged_shapes_within_bound(shape, schedule):
+    M, N, K = shape
+    inp, w, plan, C = _gemm(M, N, K, dist="normal", case=14, out="bf16", mapping=("grouped_m", 8),
+                            schedule=schedule, alpha=0.75, bias_dist="normal", relu=True, num_ctas=19)
+    z, ad = oracle_rows(inp, w)
+    assert_close(host_values(C), z, ad, "bf16", f"{shape}")
+
+
+def test_e4m3_ragged_with_scales_within_bound():
+    inp, w, plan, C = _gemm(300, 520, 384, dtype="e4m3", dist="normal", case=15, out="f32",
+                            mapping=("grouped_n", 16), schedule="persistent", bn=256)
+    z, ad = oracle_rows(inp, w)
+    assert_close(host_values(C), z, ad, "f32", "e4m3 ragged")
+
+
+def test_cross_schedule_and_mapping_bitwise_identical():
+    """Non-split schedules give every tile the same MMA sequence: identical bits."""
+    M, N, K = 1024, 896, 1536
+    inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=16)
+    dev = to_device(inp)
+    ref = None
+    for mapping in MAPPINGS:
+        for schedule in ("static", "persistent"):
+            w = dict(M=M, N=N, K=K, dtype="bf16", out="f32", mapping=mapping, schedule=schedule, bn=128)
+            C = run_gemm(plan_for(w, num_ctas=29), inp, "f32", dev)
+            if ref is None:
+                ref = C.clone()
+                z, ad = oracle_rows(inp, w)
+                assert_close(host_values(C), z, ad, "f32", "cross-schedule reference")
+            else:
+                assert torch.equal(C, ref), f"{mapping} {schedule} differs"
+
+
+def test_streamk_forward_backward_and_repeat_bitwise():
+    w = WORKLOADS["c4_bf16_streamk"]
+    inp = make_inputs(w)
+    dev = to_device(inp)
+    fwd = run_gemm(plan_for(w), inp, "f32", dev)
+    bwd = run_gemm(plan_for(w, sk_backward=True), inp, "f32", dev)
+    again = run_gemm(plan_for(w), inp, "f32", dev)
+    assert torch.equal(fwd, bwd) and torch.equal(fwd, again)
+    hyb = run_gemm(plan_for(w, schedule="streamk_hybrid"), inp, "f32", dev)
+    per = run_gemm(plan_for(w, schedule="persistent"), inp, "f32", dev)
+    rows = sample_rows(w["M"])
+    z, ad = oracle_rows(inp, w, rows)
+    for name, C in (("streamk", fwd), ("hybrid", hyb), ("persistent", per)):
+        assert_close(host_values(C)[rows], z, ad, "f32", name)
+
+
+def test_device_trace_matches_oracle_enumeration():
+    for sched, kw in (("persistent", {}), ("streamk", {}), ("streamk", {"sk_backward": True}),
+                      ("streamk_hybrid", {}), ("static", {})):
+        w = dict(WORKLOADS["c4_bf16_streamk"], schedule=sched)
+        plan = plan_for(w, **kw)
+        info = plan.info
+        cap = info.grid * info.max_items_per_cta * 8
+        trace = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+        tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TRACE, trace, cap)
+        inp = make_inputs(w)
+        run_gemm(plan, inp, "f32")
+        t = trace.view(info.grid, info.max_items_per_cta, 8).cpu().numpy()
+        P = info.grid
+        for u in range(info.grid):
+            if sched == "static":
+                want = S.work_items(S.STATIC, u, info.tiles, info.tiles, info.kt)
+            else:
+                code = {"persistent": S.PERSISTENT, "streamk": S.STREAMK, "streamk_hybrid": S.STREAMK_HYBRID}[sched]
+                want = S.work_items(code, u, info.num_sms if sched != "persistent" else P, info.tiles, info.kt,
+                                    backward=kw.get("sk_backward", False))
+            got = [tuple(r) for r in t[u] if r[0] != -1]
+            exp = [(u, j, s.tile, *S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, s.tile), s.k_idx, s.k_count,
+                    int(s.is_final) | (2 if s.requires_fixup else 0)) for j, s in enumerate(want)]
+            assert got == exp, f"{sched} cta {u}"
+
+
+@pytest.mark.parametrize("name", ["c1_bf16_256"])
+def test_config_full_compare(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    C = run_gemm(plan_for(w), inp, w["out"])
+    z, ad = oracle_rows(inp, w)
+    assert_close(host_values(C), z, ad, w["out"], name)
+
+
+@pytest.mark.parametrize("name", ["c2_bf16_4096", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk",
+                                  "c4_bf16_persistent", "c5_bf16_epilogue"])
+def test_config_full_size_sampled_rows_and_freivalds(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    C = run_gemm(plan_for(w), inp, w["out"])
+    vals = host_values(C)
+    rows = sample_rows(w["M"], count=24 if w["K"] <= 4096 else 12)
+    z, ad = oracle_rows(inp, w, rows)
+    assert_close(vals[rows], z, ad, w["out"], name)
+    if not w.get("relu", False):
+        freivalds(inp, w, vals)
+    else:
+        assert (vals >= 0).all()
+
+
+def test_timeout_on_missing_load_reports_and_recovers():
+    w = dict(M=512, N=512, K=512, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="persistent", bn=128)
+    inp = synthetic.make_gemm_inputs(512, 512, 512, "bf16", "normal", case=17)
+    plan = plan_for(w)
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOAD, None, 0, timeout_ns=20_000_000)
+    A, B, _, _ = to_device(inp)
+    C = torch.zeros(512, 512, device="cuda")
+    tst.gemm_run(plan, A, B, C)
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_ERR_TIMEOUT, (st, hex(word))
+    # the context is still usable and a normal run is correct
+    tst.gemm_plan_set_debug(plan, 0, None, 0)
+    C2 = run_gemm(plan, inp, "f32")
+    z, ad = oracle_rows(inp, w)
+    assert_close(host_values(C2), z, ad, "f32", "after timeout")
+
+
+def test_timeout_on_unpublished_streamk_lock():
+    w = dict(M=384, N=384, K=2048, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="streamk", bn=128)
+    inp = synthetic.make_gemm_inputs(384, 384, 2048, "bf16", "normal", case=18)
+    plan = plan_for(w, num_ctas=16)
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOCK, None, 0, timeout_ns=20_000_000)
+    A, B, _, _ = to_device(inp)
+    C = torch.zeros(384, 384, device="cuda")
+    tst.gemm_run(plan, A, B, C)
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_ERR_TIMEOUT and ((word >> 8) & 0xFF) == 4, (st, hex(word))
+    tst.gemm_plan_set_debug(plan, 0, None, 0)
+    C2 = run_gemm(plan, inp, "f32")
+    z, ad = oracle_rows(inp, w)
+    assert_close(host_values(C2), z, ad, "f32", "after lock timeout")
+
+
+def test_run_rejects_misaligned_and_null_pointers():
+    w = dict(M=128, N=128, K=64, dtype="bf16", out="f32", mapping=("linear_nfast", 1), schedule="static", bn=128)
+    plan = plan_for(w)
+    buf = torch.zeros(128 * 64 + 8, dtype=torch.int16, device="cuda")
+    C = torch.zeros(128, 128, device="cuda")
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_run(plan, buf.data_ptr() + 2, buf.data_ptr(), C)
+    assert e.value.status == tst.TST_ERR_ALIGNMENT
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_run(plan, 0, buf, C)
+    assert e.value.status == tst.TST_ERR_INVALID_ARG

@@ -1,0 +1,160 @@
+"""CPU tests of the C ABI: the library loads, exports every declared symbol,
+validates arguments, and its host-side schedule (the same code the kernel runs)
+matches the oracle's enumeration bit for bit.  No GPU calls."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tile_scheduled_tensor_gb300 as tst
+from oracle import schedule as S
+from tile_scheduled_tensor_gb300 import _capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MAPS = {"linear_nfast": S.LINEAR_NFAST, "linear_mfast": S.LINEAR_MFAST,
+        "grouped_m": S.GROUPED_M, "grouped_n": S.GROUPED_N}
+SCHEDS = {"static": S.STATIC, "persistent": S.PERSISTENT, "streamk": S.STREAMK,
+          "streamk_hybrid": S.STREAMK_HYBRID}
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                                text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared_functions()
+    assert "gemm_run" in names and "gemm_plan_create" in names and "gemm_tile_map" in names
+    lib = ctypes.CDLL(_capi.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings():
+    assert tst.gemm_status_string(tst.TST_OK) == "TST_OK"
+    assert tst.gemm_status_string(tst.TST_ERR_TIMEOUT) == "TST_ERR_TIMEOUT"
+    assert tst.gemm_status_string(99) == "TST_ERR_UNKNOWN"
+
+
+def _host_plan(M, N, K, **kw):
+    kw.setdefault("host_only", True)
+    kw.setdefault("num_sms", 152)
+    return tst.gemm_plan_create(M, N, K, **kw)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(M=0, N=16, K=16), tst.TST_ERR_INVALID_ARG),
+    (dict(M=16, N=-1, K=16), tst.TST_ERR_INVALID_ARG),
+    (dict(M=16, N=16, K=12), tst.TST_ERR_ALIGNMENT),           # 12 BF16 = 24 bytes per row
+    (dict(M=16, N=16, K=8, dtype="e4m3"), tst.TST_ERR_ALIGNMENT),  # 8 bytes per row
+    (dict(M=16, N=16, K=16, bn=64), tst.TST_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=16, mapping=("grouped_m", 0)), tst.TST_ERR_INVALID_ARG),
+    (dict(M=16, N=16, K=16, num_sms=0), tst.TST_ERR_INVALID_ARG),  # host-only needs an SM count
+    (dict(M=1 << 31, N=16, K=16), tst.TST_ERR_INVALID_ARG),
+])
+def test_plan_argument_errors(args, code):
+    M, N, K = args.pop("M"), args.pop("N"), args.pop("K")
+    with pytest.raises(tst.TstError) as e:
+        _host_plan(M, N, K, **args)
+    assert e.value.status == code
+
+
+def test_raw_abi_null_and_bad_enum():
+    lib = tst.lib
+    h = ctypes.c_void_p()
+    epi = _capi.tst_epilogue(0, 1.0, 0, 0, 0)
+    m = _capi.tst_mapping(0, 1)
+    assert lib.gemm_plan_create(None, 16, 16, 16, 0, 0, m, 0, ctypes.byref(epi)) == tst.TST_ERR_INVALID_ARG
+    assert lib.gemm_plan_create(ctypes.byref(h), 16, 16, 16, 0, 0, m, 0, None) == tst.TST_ERR_INVALID_ARG
+    assert lib.gemm_plan_create(ctypes.byref(h), 16, 16, 16, 7, 0, m, 0, ctypes.byref(epi)) == tst.TST_ERR_INVALID_ARG
+    assert lib.gemm_plan_create(ctypes.byref(h), 16, 16, 16, 0, 3, m, 0, ctypes.byref(epi)) == tst.TST_ERR_UNSUPPORTED
+    assert lib.gemm_plan_create(ctypes.byref(h), 16, 16, 16, 0, 0, _capi.tst_mapping(9, 1), 0,
+                                ctypes.byref(epi)) == tst.TST_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.gemm_plan_destroy(None) == tst.TST_OK
+    assert lib.gemm_tile_map(None, 0, None, None) == tst.TST_ERR_INVALID_ARG
+    assert lib.gemm_run(None, None, None, None, None, None, None) == tst.TST_ERR_INVALID_ARG
+
+
+def test_host_only_plan_cannot_run_and_checks_ranges():
+    p = _host_plan(300, 200, 128, bn=128)
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_run(p, 16, 16, 16, stream=0)
+    assert e.value.status == tst.TST_ERR_NO_DEVICE
+    with pytest.raises(tst.TstError):
+        tst.gemm_tile_map(p, p.info.tiles)
+    with pytest.raises(tst.TstError):
+        tst.gemm_work_items(p, p.info.grid)
+    st, _ = tst.gemm_status_query(p)
+    assert st == tst.TST_ERR_NO_DEVICE
+
+
+def test_tile_grid_and_config():
+    p = _host_plan(1920, 1920, 16384, bn=128, schedule="streamk")
+    i = p.info
+    assert (i.mt, i.nt, i.kt, i.tiles, i.bk) == (15, 15, 256, 225, 64)
+    assert i.grid == 152 and i.sk_tiles == 225 and i.dp_tiles == 0
+    p8 = _host_plan(8192, 8192, 8192, dtype="e4m3", bn=256)
+    assert (p8.info.bk, p8.info.mt, p8.info.nt, p8.info.kt) == (128, 64, 32, 64)
+    # ragged shapes round up
+    pr = _host_plan(129, 257, 72, bn=128)
+    assert (pr.info.mt, pr.info.nt, pr.info.kt) == (2, 3, 2)
+
+
+@pytest.mark.parametrize("kind", list(MAPS))
+def test_tile_map_matches_oracle(kind):
+    for M, N in [(128, 128), (1920, 1920), (4096, 4096), (129, 2049), (5000, 300), (300, 5000)]:
+        for G in (1, 3, 8, 16):
+            p = _host_plan(M, N, 64, mapping=(kind, G), bn=128)
+            Mt, Nt = p.info.mt, p.info.nt
+            for i in range(Mt * Nt):
+                assert tst.gemm_tile_map(p, i) == S.tile_map(MAPS[kind], G, Mt, Nt, i)
+
+
+def _oracle_items(sched, u, P, T, Kt, backward=False):
+    return [(s.tile, s.k_idx, s.k_count, int(s.is_final) | (2 if s.requires_fixup else 0))
+            for s in S.work_items(SCHEDS[sched], u, P, T, Kt, backward)]
+
+
+@pytest.mark.parametrize("sched", list(SCHEDS))
+@pytest.mark.parametrize("shape,sms", [((1920, 1920, 16384), 152), ((1920, 1920, 16384), 148),
+                                       ((256, 256, 256), 152), ((4096, 4096, 4096), 152),
+                                       ((640, 896, 320), 7), ((200, 130, 64), 3)])
+def test_work_lists_match_oracle(sched, shape, sms):
+    M, N, K = shape
+    for backward in (False, True):
+        p = _host_plan(M, N, K, mapping=("grouped_m", 8), schedule=sched, bn=128, num_sms=sms,
+                       sk_backward=backward)
+        i = p.info
+        T = i.tiles
+        P = i.grid if sched != "static" else T
+        seen = 0
+        for u in range(i.grid):
+            got = tst.gemm_work_items(p, u)
+            if sched == "static":
+                want = _oracle_items("static", u, T, T, i.kt)
+            elif sched == "persistent":
+                want = _oracle_items("persistent", u, P, T, i.kt)
+            else:
+                want = _oracle_items(sched, u, sms, T, i.kt, backward)
+            assert [(t, kb, kc, f) for t, _, _, kb, kc, f in got] == want
+            for t, m, n, *_ in got:
+                assert (m, n) == S.tile_map(S.GROUPED_M, 8, i.mt, i.nt, t)
+            assert len(got) <= i.max_items_per_cta
+            seen += sum(kc for *_, kc, _ in got)
+        assert seen == T * i.kt
+
+
+def test_hybrid_plan_matches_rule():
+    p = _host_plan(1920, 1920, 16384, schedule="streamk_hybrid", bn=128, num_sms=152)
+    assert (p.info.dp_tiles, p.info.sk_tiles) == (152, S.hybrid_split_count(225, 152))
+    q = _host_plan(1920, 1920, 16384, schedule="streamk_hybrid", bn=128, num_sms=148)
+    assert q.info.sk_tiles == 0 and q.info.dp_tiles == 225

@@ -1,0 +1,96 @@
+"""ctypes declarations of the C ABI in include/tstgemm.h (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtstgemm.so")
+
+# status codes
+TST_OK = 0
+TST_ERR_INVALID_ARG = 1
+TST_ERR_UNSUPPORTED = 2
+TST_ERR_ALIGNMENT = 3
+TST_ERR_OOM = 4
+TST_ERR_CUDA = 5
+TST_ERR_TIMEOUT = 6
+TST_ERR_DEVICE_CHECK = 7
+TST_ERR_NO_DEVICE = 8
+
+TST_BF16, TST_E4M3 = 0, 1
+TST_OUT_F32, TST_OUT_BF16 = 0, 1
+TST_LAYOUT_A_ROW_B_NK = 0
+TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N = 0, 1, 2, 3
+TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID = 0, 1, 2, 3
+TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK = 1, 2, 4
+
+
+class tst_mapping(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("group", ctypes.c_int32)]
+
+
+class tst_epilogue(ctypes.Structure):
+    _fields_ = [("out_dtype", ctypes.c_int32), ("alpha", ctypes.c_float), ("has_bias", ctypes.c_int32),
+                ("relu", ctypes.c_int32), ("use_scales", ctypes.c_int32)]
+
+
+class tst_plan_options(ctypes.Structure):
+    _fields_ = [("bn", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("sk_backward", ctypes.c_int32),
+                ("host_only", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("timeout_ns", ctypes.c_int64)]
+
+
+class tst_plan_info(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("bm", ctypes.c_int32), ("bn", ctypes.c_int32), ("bk", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("mt", ctypes.c_int32), ("nt", ctypes.c_int32),
+                ("kt", ctypes.c_int32), ("tiles", ctypes.c_int64), ("grid", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("sk_tiles", ctypes.c_int32), ("dp_tiles", ctypes.c_int32),
+                ("max_items_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+class tst_work_item(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int32), ("m", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("k_begin", ctypes.c_int32), ("k_count", ctypes.c_int32), ("flags", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_SIGNATURES = {
+    "gemm_plan_create": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                        ctypes.c_int, ctypes.c_int, tst_mapping, ctypes.c_int,
+                                        ctypes.POINTER(tst_epilogue)]),
+    "gemm_plan_create_ex": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int, ctypes.c_int, tst_mapping, ctypes.c_int,
+                                           ctypes.POINTER(tst_epilogue), ctypes.POINTER(tst_plan_options)]),
+    "gemm_run": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
+    "gemm_tile_map": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_int32)]),
+    "gemm_plan_get_info": (ctypes.c_int, [_P, ctypes.POINTER(tst_plan_info)]),
+    "gemm_work_items": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(tst_work_item), ctypes.c_int64,
+                                       ctypes.POINTER(ctypes.c_int64)]),
+    "gemm_status_query": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "gemm_plan_destroy": (ctypes.c_int, [_P]),
+    "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gemm_plan_set_debug": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int64, ctypes.c_int64]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libtstgemm.so; raises if it has not been built (there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python tile_scheduled_tensor_gb300/build.py` "
+                          f"(or __graft_entry__.build()); this package has no CPU or PyTorch fallback")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib

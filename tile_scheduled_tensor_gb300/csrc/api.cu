@@ -1,0 +1,432 @@
+// Host side of the C ABI declared in include/tstgemm.h: argument checks, tile
+// configuration, schedule construction, plan-owned device memory, TMA
+// descriptor encoding and the kernel launch.
+//
+// The plan follows the pages' split between the mapping F(i) -> (m, n) and the
+// assignment of tasks to CTAs ("Deep dive into DeepGEMM", kumaling.xyz, panel
+// "CTA <-> output tile: mapping first, then assignment"), and sizes the tile
+// grid as ceil(M/BM) x ceil(N/BN) with ceil(K/BK) k-tiles (same page, panel
+// "Kernel Configuration Heuristic", parallelism terms).  The Stream-K
+// workspace holds one FP32 partial tile per split tile with the int locks in
+// the same allocation, zeroed before every launch ("H100 . Stream-K
+// scheduling", runguoli.com Lesson 8.1, section 6).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "kernel_params.h"
+#include "tile_sched.h"
+#include "tstgemm.h"
+
+struct tst_plan {
+  int64_t M = 0, N = 0, K = 0;
+  tst_dtype dtype = TST_BF16;
+  tst_mapping mapping{};
+  tst_schedule schedule = TST_STATIC;
+  tst_epilogue epi{};
+  tst_plan_options opts{};
+  int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
+  int32_t num_sms = 0, max_items = 0;
+  tst::Sched sched{};
+  bool host_only = false;
+  int device = -1;
+  // plan-owned device memory: [status word | locks | workspace]
+  void* dev_block = nullptr;
+  size_t dev_bytes = 0, reset_bytes = 0;
+  uint32_t* d_status = nullptr;
+  int32_t* d_locks = nullptr;
+  float* d_ws = nullptr;
+  // debug
+  int32_t debug_flags = 0;
+  int32_t* trace = nullptr;
+  int64_t trace_cap = 0;
+  uint64_t timeout_ns = 10ull * 1000 * 1000 * 1000;
+  // launch
+  const void* kernel = nullptr;
+  const void* tm_A = nullptr;
+  const void* tm_B = nullptr;
+  CUtensorMap tmap_a{}, tmap_b{};
+  cudaStream_t last_stream = nullptr;
+  bool ran = false;
+};
+
+namespace {
+
+bool log_enabled() {
+  static int v = [] {
+    const char* e = getenv("TST_LOG");
+    return (e && e[0] == '1') ? 1 : 0;
+  }();
+  return v != 0;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D K-major operand: rows x K elements, box = box_k x box_rows, 128-byte swizzle,
+// out-of-bounds elements read as zero (ragged M, N and K tails).
+bool encode_operand(CUtensorMap* map, const void* ptr, tst_dtype dt, int64_t rows, int64_t K, int box_k,
+                    int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const int elt = dt == TST_BF16 ? 2 : 1;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt == TST_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Hybrid rule: split only the tail wave, and only when it is at most half full.
+int64_t hybrid_split_tiles(int64_t T, int64_t P) {
+  const int64_t tail = T % P;
+  if (tail == 0 || 2 * tail > P) return 0;
+  return tail;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(tst_status s) {
+  switch (s) {
+    case TST_OK: return "TST_OK";
+    case TST_ERR_INVALID_ARG: return "TST_ERR_INVALID_ARG";
+    case TST_ERR_UNSUPPORTED: return "TST_ERR_UNSUPPORTED";
+    case TST_ERR_ALIGNMENT: return "TST_ERR_ALIGNMENT";
+    case TST_ERR_OOM: return "TST_ERR_OOM";
+    case TST_ERR_CUDA: return "TST_ERR_CUDA";
+    case TST_ERR_TIMEOUT: return "TST_ERR_TIMEOUT";
+    case TST_ERR_DEVICE_CHECK: return "TST_ERR_DEVICE_CHECK";
+    case TST_ERR_NO_DEVICE: return "TST_ERR_NO_DEVICE";
+  }
+  return "TST_ERR_UNKNOWN";
+}
+
+tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
+                               tst_mapping mapping, tst_schedule schedule, const tst_epilogue* epi,
+                               const tst_plan_options* opts) {
+  if (out == nullptr) return TST_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (epi == nullptr || M <= 0 || N <= 0 || K <= 0) return TST_ERR_INVALID_ARG;
+  if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TST_ERR_INVALID_ARG;
+  if (dtype != TST_BF16 && dtype != TST_E4M3) return TST_ERR_INVALID_ARG;
+  if (mapping.kind < TST_MAP_LINEAR_NFAST || mapping.kind > TST_MAP_GROUPED_N) return TST_ERR_INVALID_ARG;
+  if ((mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N) && mapping.group < 1)
+    return TST_ERR_INVALID_ARG;
+  if (schedule < TST_STATIC || schedule > TST_STREAMK_HYBRID) return TST_ERR_INVALID_ARG;
+  if (epi->out_dtype != TST_OUT_F32 && epi->out_dtype != TST_OUT_BF16) return TST_ERR_INVALID_ARG;
+  if (layout != TST_LAYOUT_A_ROW_B_NK) return TST_ERR_UNSUPPORTED;
+  tst_plan_options o{};
+  if (opts) o = *opts;
+  if (o.bn != 0 && o.bn != 128 && o.bn != 256) return TST_ERR_UNSUPPORTED;
+  if (o.num_ctas < 0 || o.num_sms < 0 || o.timeout_ns < 0) return TST_ERR_INVALID_ARG;
+  const int elt = dtype == TST_BF16 ? 2 : 1;
+  if ((K * elt) % 16 != 0) return TST_ERR_ALIGNMENT;  // TMA row stride must be a multiple of 16 bytes
+
+  tst_plan* p = new (std::nothrow) tst_plan();
+  if (!p) return TST_ERR_OOM;
+  p->M = M; p->N = N; p->K = K;
+  p->dtype = dtype; p->mapping = mapping; p->schedule = schedule; p->epi = *epi; p->opts = o;
+  p->host_only = o.host_only != 0;
+  if (o.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(o.timeout_ns);
+
+  // device properties
+  if (p->host_only) {
+    if (o.num_sms <= 0) { delete p; return TST_ERR_INVALID_ARG; }
+    p->num_sms = o.num_sms;
+  } else {
+    int dev = 0, count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) { cudaGetLastError(); delete p; return TST_ERR_NO_DEVICE; }
+    if (cudaGetDevice(&dev) != cudaSuccess) { delete p; return TST_ERR_CUDA; }
+    int sms = 0, major = 0, minor = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) { delete p; return TST_ERR_UNSUPPORTED; }  // built for sm_103a only
+    p->device = dev;
+    p->num_sms = o.num_sms > 0 ? std::min(o.num_sms, sms) : sms;
+  }
+
+  // tile configuration: 128-row tiles, 128-byte operand rows
+  p->bk = 128 / elt;
+  const int64_t mt = ceil_div(M, p->bm);
+  if (o.bn != 0) {
+    p->bn = o.bn;
+  } else {
+    // wide tiles when they still give at least one full wave
+    p->bn = (N > 128 && mt * ceil_div(N, 256) >= p->num_sms) ? 256 : 128;
+  }
+  const int64_t nt = ceil_div(N, p->bn);
+  const int64_t kt = ceil_div(K, p->bk);
+  const int64_t T = mt * nt;
+  if (T >= (int64_t(1) << 31) || T * kt >= (int64_t(1) << 62)) { delete p; return TST_ERR_INVALID_ARG; }
+  p->stages = tst_kernel_stages(p->bn);
+  p->smem_bytes = tst_kernel_smem_bytes(p->bn);
+
+  // schedule
+  tst::Sched& s = p->sched;
+  s.mt = static_cast<int32_t>(mt);
+  s.nt = static_cast<int32_t>(nt);
+  s.kt = static_cast<int32_t>(kt);
+  s.map_kind = mapping.kind;
+  s.group = (mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N) ? mapping.group : 1;
+  s.backward = o.sk_backward ? 1 : 0;
+  const int64_t P = o.num_ctas > 0 ? o.num_ctas : p->num_sms;
+  switch (schedule) {
+    case TST_STATIC:
+      s.grid = static_cast<int32_t>(T); s.dp_tiles = static_cast<int32_t>(T); s.sk_tiles = 0;
+      break;
+    case TST_PERSISTENT:
+      s.grid = static_cast<int32_t>(std::min(P, T)); s.dp_tiles = static_cast<int32_t>(T); s.sk_tiles = 0;
+      break;
+    case TST_STREAMK:
+      s.grid = static_cast<int32_t>(P); s.dp_tiles = 0; s.sk_tiles = static_cast<int32_t>(T);
+      break;
+    case TST_STREAMK_HYBRID: {
+      const int64_t sk = hybrid_split_tiles(T, P);
+      s.sk_tiles = static_cast<int32_t>(sk);
+      s.dp_tiles = static_cast<int32_t>(T - sk);
+      s.grid = static_cast<int32_t>(sk > 0 ? P : std::min(P, T));
+      break;
+    }
+  }
+  if ((schedule == TST_STREAMK || schedule == TST_STREAMK_HYBRID) && !p->host_only && P > p->num_sms) {
+    // split tiles wait on each other: every CTA must be resident at once
+    delete p;
+    return TST_ERR_UNSUPPORTED;
+  }
+  // longest work list (trace sizing)
+  int32_t max_items = 0;
+  for (int32_t c = 0; c < s.grid; ++c) {
+    tst::WorkIter it;
+    tst::WorkItem w;
+    tst::work_begin(s, c, it);
+    int32_t n = 0;
+    while (tst::work_next(s, it, w)) ++n;
+    max_items = std::max(max_items, n);
+  }
+  p->max_items = max_items;
+
+  // plan-owned device memory
+  const size_t status_bytes = 256;
+  const size_t lock_bytes = ((static_cast<size_t>(s.sk_tiles) * 4 + 255) / 256) * 256;
+  const size_t ws_bytes = static_cast<size_t>(s.sk_tiles) * p->bm * p->bn * sizeof(float);
+  p->reset_bytes = status_bytes + lock_bytes;
+  p->dev_bytes = status_bytes + lock_bytes + ws_bytes;
+  if (!p->host_only) {
+    if (cudaMalloc(&p->dev_block, p->dev_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      delete p;
+      return TST_ERR_OOM;
+    }
+    if (cudaMemset(p->dev_block, 0, p->reset_bytes) != cudaSuccess) {
+      cudaFree(p->dev_block);
+      delete p;
+      return TST_ERR_CUDA;
+    }
+    char* base = static_cast<char*>(p->dev_block);
+    p->d_status = reinterpret_cast<uint32_t*>(base);
+    p->d_locks = reinterpret_cast<int32_t*>(base + status_bytes);
+    p->d_ws = ws_bytes ? reinterpret_cast<float*>(base + status_bytes + lock_bytes) : nullptr;
+    p->kernel = dtype == TST_BF16 ? tst_kernel_bf16(p->bn, epi->out_dtype) : tst_kernel_e4m3(p->bn, epi->out_dtype);
+    if (!p->kernel ||
+        cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(p->dev_block);
+      delete p;
+      return TST_ERR_CUDA;
+    }
+  }
+  if (log_enabled())
+    fprintf(stderr,
+            "[tstgemm] plan M=%lld N=%lld K=%lld dtype=%d tile=%dx%dx%d stages=%d grid=%d (sms=%d) tiles=%lld "
+            "dp=%d sk=%d kt=%d map=%d G=%d sched=%d max_items=%d ws=%zu B\n",
+            (long long)M, (long long)N, (long long)K, (int)dtype, p->bm, p->bn, p->bk, p->stages, s.grid,
+            p->num_sms, (long long)T, s.dp_tiles, s.sk_tiles, s.kt, s.map_kind, s.group, (int)schedule,
+            p->max_items, p->dev_bytes);
+  *out = p;
+  return TST_OK;
+}
+
+tst_status gemm_plan_create(tst_plan** plan, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
+                            tst_mapping mapping, tst_schedule schedule, const tst_epilogue* epi) {
+  return gemm_plan_create_ex(plan, M, N, K, dtype, layout, mapping, schedule, epi, nullptr);
+}
+
+tst_status gemm_plan_destroy(tst_plan* plan) {
+  if (plan == nullptr) return TST_OK;
+  tst_status st = TST_OK;
+  if (plan->dev_block && cudaFree(plan->dev_block) != cudaSuccess) st = TST_ERR_CUDA;
+  delete plan;
+  return st;
+}
+
+tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
+  if (p == nullptr || info == nullptr) return TST_ERR_INVALID_ARG;
+  memset(info, 0, sizeof(*info));
+  info->M = p->M; info->N = p->N; info->K = p->K;
+  info->bm = p->bm; info->bn = p->bn; info->bk = p->bk; info->stages = p->stages;
+  info->mt = p->sched.mt; info->nt = p->sched.nt; info->kt = p->sched.kt;
+  info->tiles = static_cast<int64_t>(p->sched.mt) * p->sched.nt;
+  info->grid = p->sched.grid;
+  info->num_sms = p->num_sms;
+  info->sk_tiles = p->sched.sk_tiles;
+  info->dp_tiles = p->sched.dp_tiles;
+  info->max_items_per_cta = p->max_items;
+  info->smem_bytes = p->smem_bytes;
+  info->workspace_bytes = static_cast<int64_t>(p->dev_bytes);
+  return TST_OK;
+}
+
+tst_status gemm_tile_map(const tst_plan* p, int64_t i, int32_t* m, int32_t* n) {
+  if (p == nullptr || m == nullptr || n == nullptr) return TST_ERR_INVALID_ARG;
+  if (i < 0 || i >= static_cast<int64_t>(p->sched.mt) * p->sched.nt) return TST_ERR_INVALID_ARG;
+  tst::tile_coord(p->sched, static_cast<int32_t>(i), *m, *n);
+  return TST_OK;
+}
+
+tst_status gemm_work_items(const tst_plan* p, int32_t cta, tst_work_item* items, int64_t cap, int64_t* count) {
+  if (p == nullptr || count == nullptr || (cap > 0 && items == nullptr) || cap < 0) return TST_ERR_INVALID_ARG;
+  if (cta < 0 || cta >= p->sched.grid) return TST_ERR_INVALID_ARG;
+  tst::WorkIter it;
+  tst::WorkItem w;
+  tst::work_begin(p->sched, cta, it);
+  int64_t n = 0;
+  while (tst::work_next(p->sched, it, w)) {
+    if (n < cap) {
+      items[n].tile = w.tile; items[n].m = w.m; items[n].n = w.n;
+      items[n].k_begin = w.k_begin; items[n].k_count = w.k_count; items[n].flags = w.flags;
+    }
+    ++n;
+  }
+  *count = n;
+  return TST_OK;
+}
+
+tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int64_t cap, int64_t timeout_ns) {
+  if (p == nullptr || cap < 0 || timeout_ns < 0) return TST_ERR_INVALID_ARG;
+  if (flags & TST_DEBUG_TRACE) {
+    const int64_t need = static_cast<int64_t>(p->sched.grid) * p->max_items * 8;
+    if (trace_buf == nullptr || cap < need) return TST_ERR_INVALID_ARG;
+  }
+  p->debug_flags = flags;
+  p->trace = (flags & TST_DEBUG_TRACE) ? static_cast<int32_t*>(trace_buf) : nullptr;
+  p->trace_cap = cap;
+  if (timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(timeout_ns);
+  else if (p->opts.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(p->opts.timeout_ns);
+  else p->timeout_ns = 10ull * 1000 * 1000 * 1000;
+  return TST_OK;
+}
+
+tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const float* bias, const float* scales,
+                    void* stream_) {
+  if (p == nullptr || A == nullptr || B == nullptr || C == nullptr) return TST_ERR_INVALID_ARG;
+  if (p->host_only || p->kernel == nullptr) return TST_ERR_NO_DEVICE;
+  if (p->epi.has_bias && bias == nullptr) return TST_ERR_INVALID_ARG;
+  if (p->epi.use_scales && scales == nullptr) return TST_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return TST_ERR_ALIGNMENT;
+  if ((p->epi.has_bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
+      (p->epi.use_scales && (reinterpret_cast<uintptr_t>(scales) & 3u)))
+    return TST_ERR_ALIGNMENT;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+  if (A != p->tm_A) {
+    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, p->bk, p->bm)) return TST_ERR_CUDA;
+    p->tm_A = A;
+  }
+  if (B != p->tm_B) {
+    if (!encode_operand(&p->tmap_b, B, p->dtype, p->N, p->K, p->bk, p->bn)) return TST_ERR_CUDA;
+    p->tm_B = B;
+  }
+
+  tst::KernelParams kp = {};
+  kp.tmap_a = p->tmap_a;
+  kp.tmap_b = p->tmap_b;
+  kp.C = C;
+  kp.bias = p->epi.has_bias ? bias : nullptr;
+  kp.scales = p->epi.use_scales ? scales : nullptr;
+  kp.workspace = p->d_ws;
+  kp.locks = p->d_locks;
+  kp.status = p->d_status;
+  kp.trace = p->trace;
+  kp.M = static_cast<int32_t>(p->M);
+  kp.N = static_cast<int32_t>(p->N);
+  kp.K = static_cast<int32_t>(p->K);
+  kp.alpha = p->epi.alpha;
+  kp.sched = p->sched;
+  kp.has_bias = p->epi.has_bias ? 1 : 0;
+  kp.relu = p->epi.relu ? 1 : 0;
+  kp.use_scales = p->epi.use_scales ? 1 : 0;
+  kp.debug_flags = p->debug_flags;
+  kp.max_items = p->max_items;
+  kp.timeout_ns = p->timeout_ns;
+
+  // status word and Stream-K locks start at zero for every launch
+  if (cudaMemsetAsync(p->dev_block, 0, p->reset_bytes, stream) != cudaSuccess) return TST_ERR_CUDA;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid), 1, 1);
+  cfg.blockDim = dim3(tst::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (p->sched.sk_tiles > 0) {
+    // Stream-K splits wait on each other across CTAs: ask for a co-resident grid
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[] = {&kp};
+  if (cudaLaunchKernelExC(&cfg, p->kernel, args) != cudaSuccess) {
+    cudaGetLastError();
+    return TST_ERR_CUDA;
+  }
+  p->last_stream = stream;
+  p->ran = true;
+  return TST_OK;
+}
+
+tst_status gemm_status_query(tst_plan* p, uint32_t* detail) {
+  if (p == nullptr) return TST_ERR_INVALID_ARG;
+  if (detail) *detail = 0;
+  if (p->host_only || p->dev_block == nullptr) return TST_ERR_NO_DEVICE;
+  if (!p->ran) return TST_OK;
+  if (cudaStreamSynchronize(p->last_stream) != cudaSuccess) return TST_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, p->d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TST_ERR_CUDA;
+  if (detail) *detail = word;
+  switch (word & 0xFFu) {
+    case 0: return TST_OK;
+    case tst::ST_TIMEOUT: return TST_ERR_TIMEOUT;
+    default: return TST_ERR_DEVICE_CHECK;
+  }
+}
+
+}  // extern "C"

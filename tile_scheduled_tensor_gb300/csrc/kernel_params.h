@@ -1,0 +1,65 @@
+// Launch parameters of the GEMM kernel (host and device view).
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "tile_sched.h"
+
+namespace tst {
+
+constexpr int kBlockM = 128;        // tile height (one TMEM lane per row)
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kSmemLimit = 232448;  // 227 KiB opt-in dynamic shared memory per CTA
+
+enum DType : int32_t { DT_BF16 = 0, DT_E4M3 = 1 };
+enum OutType : int32_t { OUT_F32 = 0, OUT_BF16 = 1 };
+
+// device status word: code (bits 0-7) | role (8-15) | CTA (16-31)
+enum StatusCode : uint32_t { ST_OK = 0, ST_TIMEOUT = 6, ST_DEVICE_CHECK = 7 };
+enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_LOCK = 4 };
+
+enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4 };
+
+struct KernelParams {
+  CUtensorMap tmap_a;       // A: M x K, K contiguous, box BK x 128, 128-byte swizzle
+  CUtensorMap tmap_b;       // B: N x K, K contiguous, box BK x BN, 128-byte swizzle
+  void* C;                  // M x N row-major, FP32 or BF16
+  const float* bias;        // FP32[N] or null
+  const float* scales;      // FP32[2] = {sA, sB} or null
+  float* workspace;         // Stream-K partial tiles, one BM x BN FP32 slot per split tile
+  int32_t* locks;           // one lock per split tile: k-tiles accumulated so far
+  uint32_t* status;         // device status word
+  int32_t* trace;           // debug trace or null
+  int32_t M, N, K;
+  float alpha;
+  Sched sched;
+  int32_t has_bias, relu, use_scales;
+  int32_t debug_flags;
+  int32_t max_items;        // trace records per CTA
+  int32_t pad_;
+  uint64_t timeout_ns;      // limit of every device-side wait
+};
+
+// Tile configuration for a tile width BN.  Operand rows are always 128 bytes
+// (BK = 64 BF16 or 128 e4m3 elements), matching the 128-byte swizzle span.
+template <int BN>
+struct TileCfg {
+  static constexpr int A_BYTES = kBlockM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int RAW_STAGES = (kSmemLimit - 2048) / STAGE_BYTES;
+  static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
+  static constexpr int NACC = 512 / BN;                 // accumulator buffers in 512 TMEM columns
+  static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
+  static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = 1024 + MISC_OFFSET + 16;  // + slack to align the base to 1024
+};
+
+}  // namespace tst
+
+// Kernel lookup, one per input type (defined in gemm_bf16.cu / gemm_e4m3.cu).
+const void* tst_kernel_bf16(int bn, int out_type);
+const void* tst_kernel_e4m3(int bn, int out_type);
+int tst_kernel_smem_bytes(int bn);
+int tst_kernel_stages(int bn);

@@ -1,0 +1,145 @@
+// Tile schedule shared by the host API and the GPU kernel: the mapping
+// F(i) -> (m, n), and each CTA's ordered work list under the static,
+// persistent, Stream-K and hybrid schedules.  Everything here is a pure
+// function of the plan constants and the CTA index, so the host can enumerate
+// exactly what the device will do.
+//
+// Sources:
+//  * Mapping families and "persistent is an assignment, not a mapping":
+//    "Deep dive into DeepGEMM" (blog.kumaling.xyz/posts/deepgemm-sm90), panel
+//    "CTA <-> output tile: mapping first, then assignment" and its table of
+//    mapping families (linear N-fast / M-fast, grouped-M / grouped-N strips).
+//  * Static (one CTA per tile), persistent (grid-stride over tiles), Stream-K
+//    over a 1-D band of MAC iterations, the hybrid "tail only" variant with
+//    its 50 % rule, backward iteration: "H100 . Kernel Design" (runguoli.com
+//    H100 course notes, Lesson 8), sections 9.2, 9.3, 10.1 and 10.3.
+//  * Split bookkeeping K_idx = tile_iter_start - output_tile_iter_start and
+//    is_final_split <=> K_idx + k_tile_count == k_tiles_per_output_tile:
+//    "H100 . Stream-K scheduling" (Lesson 8.1), sections 2-4.
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define TST_HD __host__ __device__ __forceinline__
+#else
+#define TST_HD inline
+#endif
+
+namespace tst {
+
+enum MapKind : int32_t { MAP_LINEAR_NFAST = 0, MAP_LINEAR_MFAST = 1, MAP_GROUPED_M = 2, MAP_GROUPED_N = 3 };
+enum SchedKind : int32_t { SCHED_STATIC = 0, SCHED_PERSISTENT = 1, SCHED_STREAMK = 2, SCHED_STREAMK_HYBRID = 3 };
+
+enum : int32_t { ITEM_FINAL = 1, ITEM_FIXUP = 2 };
+
+struct Sched {
+  int32_t mt, nt, kt;     // scheduled tiles along M and N, k-tiles along K
+  int32_t map_kind;       // MapKind
+  int32_t group;          // strip width G for grouped mappings
+  int32_t grid;           // CTAs launched
+  int32_t dp_tiles;       // tasks [0, dp_tiles) are computed whole, grid-stride
+  int32_t sk_tiles;       // tasks [dp_tiles, dp_tiles + sk_tiles) are split by Stream-K
+  int32_t backward;       // Stream-K splits of a unit visited last-first
+  int32_t pad_;
+};
+
+struct WorkItem {
+  int32_t tile;     // linear task i
+  int32_t m, n;     // F(i)
+  int32_t k_begin;  // K_idx: first k-tile of the split
+  int32_t k_count;  // k-tiles in the split
+  int32_t flags;    // ITEM_FINAL | ITEM_FIXUP
+};
+
+// F(i) -> (m, n).  Grouped strips: a strip holds G tile-rows (grouped-M) or
+// G tile-columns (grouped-N); the last strip may be thinner.
+TST_HD void tile_coord(const Sched& s, int32_t i, int32_t& m, int32_t& n) {
+  switch (s.map_kind) {
+    case MAP_LINEAR_NFAST:
+      m = i / s.nt;
+      n = i - m * s.nt;
+      return;
+    case MAP_LINEAR_MFAST:
+      n = i / s.mt;
+      m = i - n * s.mt;
+      return;
+    case MAP_GROUPED_M: {
+      const int32_t span = s.group * s.nt;       // tasks per strip
+      const int32_t strip = i / span;
+      const int32_t r = i - strip * span;
+      const int32_t m0 = strip * s.group;
+      const int32_t h = (s.mt - m0) < s.group ? (s.mt - m0) : s.group;
+      n = r / h;
+      m = m0 + (r - n * h);
+      return;
+    }
+    default: {  // MAP_GROUPED_N
+      const int32_t span = s.group * s.mt;
+      const int32_t strip = i / span;
+      const int32_t r = i - strip * span;
+      const int32_t n0 = strip * s.group;
+      const int32_t w = (s.nt - n0) < s.group ? (s.nt - n0) : s.group;
+      m = r / w;
+      n = n0 + (r - m * w);
+      return;
+    }
+  }
+}
+
+// Iterator over one CTA's work list: first its whole (data-parallel) tiles,
+// grid-stride; then its Stream-K range of MAC iterations cut at tile edges.
+struct WorkIter {
+  int32_t next_dp;   // next whole task (>= dp_tiles when exhausted)
+  int32_t pad_;
+  int64_t sk_lo;     // remaining Stream-K iterations [sk_lo, sk_hi)
+  int64_t sk_hi;
+};
+
+TST_HD void work_begin(const Sched& s, int32_t cta, WorkIter& it) {
+  it.next_dp = cta;
+  it.pad_ = 0;
+  if (s.sk_tiles > 0) {
+    // unit u owns [floor(u W / P), floor((u + 1) W / P)), W = sk_tiles * Kt
+    const int64_t W = (int64_t)s.sk_tiles * s.kt;
+    it.sk_lo = (int64_t)cta * W / s.grid;
+    it.sk_hi = (int64_t)(cta + 1) * W / s.grid;
+  } else {
+    it.sk_lo = it.sk_hi = 0;
+  }
+}
+
+TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
+  if (it.next_dp < s.dp_tiles) {
+    w.tile = it.next_dp;
+    w.k_begin = 0;
+    w.k_count = s.kt;
+    w.flags = ITEM_FINAL;
+    it.next_dp += s.grid;
+  } else if (it.sk_lo < it.sk_hi) {
+    int64_t t, start, end;
+    if (!s.backward) {
+      t = it.sk_lo / s.kt;
+      start = it.sk_lo;
+      const int64_t tile_end = (t + 1) * s.kt;
+      end = tile_end < it.sk_hi ? tile_end : it.sk_hi;
+      it.sk_lo = end;
+    } else {
+      t = (it.sk_hi - 1) / s.kt;
+      const int64_t tile_start = t * s.kt;
+      start = tile_start > it.sk_lo ? tile_start : it.sk_lo;
+      end = it.sk_hi;
+      it.sk_hi = start;
+    }
+    w.tile = s.dp_tiles + (int32_t)t;
+    w.k_begin = (int32_t)(start - t * s.kt);          // tile_iter_start - output_tile_iter_start
+    w.k_count = (int32_t)(end - start);
+    const bool final_split = (w.k_begin + w.k_count) == s.kt;
+    w.flags = (final_split ? ITEM_FINAL : 0) | ((w.k_begin == 0 && final_split) ? 0 : ITEM_FIXUP);
+  } else {
+    return false;
+  }
+  tile_coord(s, w.tile, w.m, w.n);
+  return true;
+}
+
+}  // namespace tst
