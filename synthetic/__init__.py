@@ -142,8 +142,9 @@ class GemmInputs:
 
 
 def make_gemm_inputs(M: int, N: int, K: int, dtype: str = "bf16", dist: str = "uniform",
-                     case: int = 1, bias_dist: str | None = None) -> GemmInputs:
-    """Seeded inputs for one GEMM case.  dtype 'bf16' or 'e4m3'."""
+                     case: int = 1, bias_dist: str | None = None, fp8_scaled: bool = True) -> GemmInputs:
+    """Seeded inputs for one GEMM case.  dtype 'bf16' or 'e4m3'.  With fp8_scaled=False the e4m3
+    bytes encode the drawn values directly (no tensor-wise scale; scales is None)."""
     xa = draw(dist, SEED_A + case, M * K).reshape(M, K)
     xb = draw(dist, SEED_B + case, N * K).reshape(N, K)
     bias = None
@@ -151,6 +152,9 @@ def make_gemm_inputs(M: int, N: int, K: int, dtype: str = "bf16", dist: str = "u
         bias = draw(bias_dist, SEED_BIAS + case, N).astype(np.float32)
     if dtype == "bf16":
         return GemmInputs(M, N, K, dtype, bf16_bits(xa), bf16_bits(xb), None, bias)
+    if dtype == "e4m3" and not fp8_scaled:
+        return GemmInputs(M, N, K, dtype, e4m3_bytes(xa.astype(np.float32)), e4m3_bytes(xb.astype(np.float32)),
+                          None, bias)
     if dtype == "e4m3":
         qa, sa = e4m3_quantise(xa)
         qb, sb = e4m3_quantise(xb)

@@ -25,7 +25,8 @@ SCHEDULES = ["static", "persistent", "streamk", "streamk_hybrid"]
 
 
 def _gemm(M, N, K, dtype="bf16", dist="normal", case=11, out="f32", bias_dist=None, **plan_kw):
-    inp = synthetic.make_gemm_inputs(M, N, K, dtype, dist, case=case, bias_dist=bias_dist)
+    scaled = plan_kw.get("use_scales", dtype == "e4m3")
+    inp = synthetic.make_gemm_inputs(M, N, K, dtype, dist, case=case, bias_dist=bias_dist, fp8_scaled=scaled)
     w = dict(M=M, N=N, K=K, dtype=dtype, out=out, mapping=plan_kw.pop("mapping", ("linear_nfast", 1)),
              schedule=plan_kw.pop("schedule", "static"), bn=plan_kw.pop("bn", 128),
              alpha=plan_kw.pop("alpha", 1.0), relu=plan_kw.pop("relu", False),
