@@ -231,6 +231,47 @@ enum {
 tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, int64_t cap,
                                int64_t timeout_ns);
 
+/* Size of the fixed device scratch array used by gemm_streamk_noalloc: 16 MiB,
+ * held by every GPU that loads this library until the process exits. */
+#define TST_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Stream-K GEMM that allocates nothing.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot call cudaMalloc: code whose device memory is owned by another
+ * allocator (an inference engine or a framework's caching allocator that has
+ * already reserved the GPU's memory, where a raw cudaMalloc would fail or break
+ * its accounting), and latency-critical paths where cudaMalloc/cudaFree may
+ * synchronise the device or fail under memory pressure.  gemm_plan_create
+ * allocates the plan's Stream-K workspace with cudaMalloc; this call instead
+ * keeps the partial tiles and locks in a file-scope device array of
+ * TST_NOALLOC_SCRATCH_BYTES bytes, and builds its schedule on the stack.
+ *
+ * Computes the same C as gemm_plan_create + gemm_run with the same arguments
+ * (schedule must be TST_STREAMK or TST_STREAMK_HYBRID; bn and num_ctas as in
+ * tst_plan_options, 0 = choose).  A, B, C, bias, scales: caller-owned device
+ * pointers as for gemm_run.  device_status: optional device pointer to one
+ * uint32 that receives the device-side status word (0 = OK, code in bits 0-7 as
+ * in tst_status, e.g. 6 = a bounded wait ran out); NULL keeps it in the scratch
+ * array, where it cannot be read.  The call enqueues a clear of the locks (and
+ * of *device_status) plus one kernel launch on `stream` and returns.
+ *
+ * Scratch use: 256 bytes + 4 bytes per split tile (rounded up to 256) +
+ * 128 x bn x 4 bytes per split tile.  A problem that needs more than
+ * TST_NOALLOC_SCRATCH_BYTES is rejected with TST_ERR_UNSUPPORTED before any GPU
+ * work.  Every call, from any thread, shares the one array and leaves its last
+ * contents there: calls that can overlap on the GPU (different streams, or
+ * different host threads without ordering) race on it and must be serialised
+ * by the caller.  The first call on each device (with that device current)
+ * looks up the array's device address and sets the kernels' shared-memory
+ * limit; make that first call before any stream capture begins.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, NO_DEVICE, CUDA, as for
+ * gemm_plan_create and gemm_run. */
+tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_mapping mapping,
+                                tst_schedule schedule, const tst_epilogue *epi, int32_t bn, int32_t num_ctas,
+                                const void *A, const void *B, void *C, const float *bias,
+                                const float *scales, uint32_t *device_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,8 @@ from ._capi import (TST_BF16, TST_E4M3, TST_OUT_F32, TST_OUT_BF16, TST_LAYOUT_A_
                     TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID,
                     TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK,
                     TST_OK, TST_ERR_INVALID_ARG, TST_ERR_UNSUPPORTED, TST_ERR_ALIGNMENT, TST_ERR_OOM,
-                    TST_ERR_CUDA, TST_ERR_TIMEOUT, TST_ERR_DEVICE_CHECK, TST_ERR_NO_DEVICE)
+                    TST_ERR_CUDA, TST_ERR_TIMEOUT, TST_ERR_DEVICE_CHECK, TST_ERR_NO_DEVICE,
+                    TST_NOALLOC_SCRATCH_BYTES)
 
 lib = _capi.load()
 
@@ -159,3 +160,20 @@ def gemm_plan_set_debug(plan: Plan, flags: int = 0, trace=None, cap: int = 0, ti
 
 def gemm_plan_destroy(plan: Plan):
     plan.destroy()
+
+
+def gemm_streamk_noalloc(M: int, N: int, K: int, A, B, C, dtype="bf16", mapping=("linear_nfast", 1),
+                         schedule="streamk", out_dtype="f32", alpha: float = 1.0, has_bias: bool = False,
+                         relu: bool = False, use_scales: bool = False, bn: int = 0, num_ctas: int = 0,
+                         bias=None, scales=None, device_status=None, stream=None):
+    """Stream-K GEMM that allocates no device memory: its partial tiles and locks live in the
+    library's fixed scratch array (TST_NOALLOC_SCRATCH_BYTES).  For callers that cannot call
+    cudaMalloc.  Calls that may overlap on the GPU share that array and must be serialised."""
+    kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
+    m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
+    epi = _capi.tst_epilogue(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), int(bool(has_bias)),
+                             int(bool(relu)), int(bool(use_scales)))
+    _check(lib.gemm_streamk_noalloc(int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"), m,
+                                    _enum(_SCHED, schedule, "schedule"), ctypes.byref(epi), int(bn), int(num_ctas),
+                                    _ptr(A), _ptr(B), _ptr(C), _ptr(bias), _ptr(scales), _ptr(device_status),
+                                    _stream(stream)), "gemm_streamk_noalloc")

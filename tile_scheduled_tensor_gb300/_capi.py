@@ -74,7 +74,12 @@ _SIGNATURES = {
     "gemm_plan_destroy": (ctypes.c_int, [_P]),
     "gemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gemm_plan_set_debug": (ctypes.c_int, [_P, ctypes.c_int32, _P, ctypes.c_int64, ctypes.c_int64]),
+    "gemm_streamk_noalloc": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                            tst_mapping, ctypes.c_int, ctypes.POINTER(tst_epilogue),
+                                            ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P]),
 }
+
+TST_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
