@@ -34,11 +34,13 @@ from synthetic.workloads import WORKLOADS  # noqa: E402
 
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
 HEADLINE = "c2_bf16_4096"
-EXTRA = ["c1_bf16_256", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
+EXTRA = ["c1_bf16_256", "c2_bf16_4096_1cta", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
          "c5_bf16_epilogue"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
-    "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 tiles, grouped-M G=8, persistent",
+    "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
+                    "persistent",
+    "c2_bf16_4096_1cta": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 tiles, one CTA each, grouped-M G=8, persistent",
     "c2x_bf16_8192": "BF16 GEMM 8192^3, N(0,1), BF16 out, grouped-M G=8, persistent",
     "c3_e4m3_8192": "FP8-e4m3 GEMM 8192^3, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, persistent",
     "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, Stream-K with fixup",
@@ -84,51 +86,108 @@ def dram_traffic(name):
 
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled DURING the timed region.
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = None
+    Reads NVML (libnvidia-ml, the library nvidia-smi itself uses) from a
+    background thread every ~2 ms; read-only queries, no setting is touched.
+    Falls back to `nvidia-smi --query-gpu=... -lms 20` when NVML cannot be loaded.
+    """
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x40: "sw_thermal_slowdown",
+               0x80: "hw_thermal_slowdown", 0x100: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index):
+        self.cuda_index = cuda_index
+        self.samples = []
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._smi = None
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if nv.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            ok = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(h)) != 0:
+            return False
+        self._nvml, self._handle = nv, h
+        return True
+
+    def _read(self):
+        import ctypes
+        mhz, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(mhz))      # NVML_CLOCK_SM
+        self._nvml.nvmlDeviceGetMaxClockInfo(self._handle, 1, ctypes.byref(mx))
+        fn = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        fn(self._handle, ctypes.byref(rs))
+        return mhz.value, mx.value, rs.value
 
     def start(self):
-        fd, self.path = tempfile.mkstemp(prefix="tst_clocks_", suffix=".csv")
-        os.close(fd)
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except (FileNotFoundError, OSError):
-            self.proc = None
+        import threading
+        self.samples = []
+        if self._nvml is None and not self._open_nvml():
+            fd, self._path = tempfile.mkstemp(prefix="tst_clocks_", suffix=".csv")
+            os.close(fd)
+            q = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+            try:
+                self._smi = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                              "-lms", "20"], stdout=open(self._path, "w"),
+                                             stderr=subprocess.DEVNULL)
+                time.sleep(0.3)
+            except OSError:
+                self._smi = None
+            return
+        self._stop = threading.Event()
+
+        def loop():
+            while not self._stop.is_set():
+                self.samples.append(self._read())
+                time.sleep(0.002)
+        self.samples.append(self._read())
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, smax, reasons = [], None, set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
-                except ValueError:
-                    continue
-                for n, v in zip(names[1:], parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+            self.samples.append(self._read())
+        elif self._smi is not None:
+            self._smi.terminate()
+            self._smi.wait(timeout=5)
+            with open(self._path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    try:
+                        self.samples.append((float(parts[0]), float(parts[1]), int(parts[2], 16)))
+                    except (ValueError, IndexError):
+                        pass
+            os.unlink(self._path)
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"], "samples": 0}
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x[0] for x in self.samples), "sm_max_mhz": self.samples[-1][1],
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "source": "nvml" if self._thread is not None else "nvidia-smi"}
 
 
 def setup_dist():
@@ -232,7 +291,8 @@ def main():
         plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
                                     schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
                                     has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
-                                    use_scales=w.get("use_scales", False), bn=w.get("bn", 0))
+                                    use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
+                                    cta_group=w.get("cta_group", 0))
         a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
         b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
         host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory()}
@@ -340,7 +400,8 @@ def main():
             tf = flops(r["w"]) / (ms / 1e3) / 1e12
             extra[name] = {"tflops": round(tf, 1), "ms": round(ms, 4), "frac_of_peak": round(tf / pk, 4),
                            "tiles": int(r["plan"].info.tiles), "grid": int(r["plan"].info.grid),
-                           "bn": int(r["plan"].info.bn), "describe": DESCR[name]}
+                           "tile": f"{r['plan'].info.bm}x{r['plan'].info.bn}", "cta_group": int(r["plan"].info.cta_group),
+                           "describe": DESCR[name]}
             del r
             torch.cuda.empty_cache()
 
@@ -359,6 +420,7 @@ def main():
             "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "M": w["M"], "N": w["N"],
                        "K": w["K"], "tile": f"{head['plan'].info.bm}x{head['plan'].info.bn}x{head['plan'].info.bk}",
                        "grid": int(head["plan"].info.grid), "stages": int(head["plan"].info.stages),
+                       "cta_group": int(head["plan"].info.cta_group),
                        "l2": "flushed (512 MiB write) between timed steps", "accumulate": "fp32",
                        "parallelism": f"{world} independent problem(s), one per GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",

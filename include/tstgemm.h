@@ -114,30 +114,42 @@ typedef struct {
 
 /* Optional plan settings.  Zero-initialise and set what you need. */
 typedef struct {
-    int32_t bn;            /* output tile width: 0 = choose, else 128 or 256 (tile height is 128) */
-    int32_t num_ctas;      /* persistent / Stream-K grid size P: 0 = number of SMs */
-    int32_t sk_backward;   /* 1: a Stream-K unit visits its splits last-first */
+    int32_t bn;            /* output tile width: 0 = choose, else 128 or 256 */
+    int32_t num_ctas;      /* persistent / Stream-K grid size P in scheduling units (CTAs, or
+                              CTA pairs when cta_group = 2): 0 = as many as can be resident */
+    int32_t sk_forward;    /* Stream-K split order.  0 (default): each unit visits its splits
+                              last-first ("backward tile iteration"), so the split a later unit
+                              waits for is the first one its neighbour computes; 1: first-first,
+                              which makes every fixup wait for the previous unit's whole range */
     int32_t host_only;     /* 1: build the schedule without a GPU (gemm_run then fails);
                               num_sms must be set */
     int32_t num_sms;       /* SM count to plan for when host_only (else queried) */
-    int32_t reserved0;
+    int32_t cta_group;     /* 0 = choose, 1 = one CTA per 128 x bn tile, 2 = CTA pairs sharing one
+                              M = 256 tensor-core MMA per 256 x bn tile (each CTA computes 128 x bn
+                              and loads half of B; the pair is a cluster of 2 CTAs) */
     int64_t timeout_ns;    /* limit of every device-side wait: 0 = 10 s */
+    int32_t stages;        /* shared-memory ring depth: 0 = as deep as shared memory allows,
+                              else 2 .. that maximum (TST_ERR_UNSUPPORTED beyond it) */
+    int32_t reserved1;
 } tst_plan_options;
 
 /* What the plan decided (for logging and tests). */
 typedef struct {
     int64_t M, N, K;
-    int32_t bm, bn, bk;        /* tile shape (bk = 64 for BF16, 128 for e4m3) */
+    int32_t bm, bn, bk;        /* scheduled tile shape: bm = 128 * cta_group; bk = 64 for BF16,
+                                  128 for e4m3 */
     int32_t stages;            /* shared-memory ring depth */
     int32_t mt, nt, kt;        /* tiles along M, N and k-tiles along K */
     int64_t tiles;             /* T = mt * nt */
-    int32_t grid;              /* CTAs launched */
+    int32_t grid;              /* scheduling units launched (CTAs or CTA pairs) */
     int32_t num_sms;           /* SMs planned for */
     int32_t sk_tiles;          /* tiles handled by Stream-K (0 if none) */
     int32_t dp_tiles;          /* tiles handled whole, data-parallel */
     int32_t max_items_per_cta; /* longest work list of any CTA */
     int32_t smem_bytes;        /* dynamic shared memory per CTA */
     int64_t workspace_bytes;   /* device bytes owned by the plan (Stream-K partials + locks + status) */
+    int32_t cta_group;         /* 1 or 2 CTAs per scheduling unit */
+    int32_t ctas;              /* CTAs launched = grid * cta_group */
 } tst_plan_info;
 
 typedef struct tst_plan tst_plan;
@@ -190,7 +202,8 @@ tst_status gemm_tile_map(const tst_plan *plan, int64_t i, int32_t *m, int32_t *n
 /* The plan's decisions.  Errors: INVALID_ARG. */
 tst_status gemm_plan_get_info(const tst_plan *plan, tst_plan_info *info);
 
-/* Work list of CTA `cta` in the order the device processes it (pure host
+/* Work list of scheduling unit `cta` (a CTA, or a CTA pair when the plan's
+ * cta_group is 2) in the order the device processes it (pure host
  * computation from the same schedule code the kernel runs).  Writes at most
  * `cap` items to `items` and the full count to *count.
  * Errors: INVALID_ARG (null, cta outside [0, grid)). */
@@ -212,9 +225,9 @@ const char *gemm_status_string(tst_status s);
 
 /* Debug and test hooks.
  * flags bit 0 (TST_DEBUG_TRACE): the kernel writes one record per work item
- *   to trace_buf, a DEVICE buffer of `cap` int32 values; record r of CTA c is
- *   at offset (c * max_items_per_cta + r) * 8 and holds
- *   {cta, seq, tile, m, n, k_begin, k_count, flags}.  The call fails with
+ *   to trace_buf, a DEVICE buffer of `cap` int32 values; record r of unit c
+ *   (CTA or CTA pair) is at offset (c * max_items_per_cta + r) * 8 and holds
+ *   {unit, seq, tile, m, n, k_begin, k_count, flags}.  The call fails with
  *   INVALID_ARG when cap < grid * max_items_per_cta * 8.
  * flags bit 1 (TST_DEBUG_FAULT_SKIP_LOAD): the producer skips the TMA loads of
  *   the first k-tile of its first work item (it still announces them), so the
@@ -222,11 +235,19 @@ const char *gemm_status_string(tst_status s);
  *   kernel with TST_ERR_TIMEOUT instead of hanging.
  * flags bit 2 (TST_DEBUG_FAULT_SKIP_LOCK): first Stream-K splits never publish
  *   their lock, so the later splits' waits run out (TST_ERR_TIMEOUT).
+ * flags bit 3 (TST_DEBUG_ROLE_CYCLES): per launched CTA the kernel writes 8
+ *   uint64 counters (SM clock cycles) to trace_buf (8-byte aligned, `cap` counted
+ *   in int32 units, at least 16 per CTA): kernel total, producer waiting for a
+ *   free stage, MMA issuer waiting for loaded operands, MMA issuer waiting for a
+ *   free accumulator, epilogue waiting for an accumulator or a Stream-K lock,
+ *   epilogue busy, k-tiles issued, work items finished.  Cannot be combined
+ *   with TST_DEBUG_TRACE (both use trace_buf).
  * The settings stay on the plan until changed; flags = 0 turns them off. */
 enum {
     TST_DEBUG_TRACE = 1,
     TST_DEBUG_FAULT_SKIP_LOAD = 2,
-    TST_DEBUG_FAULT_SKIP_LOCK = 4
+    TST_DEBUG_FAULT_SKIP_LOCK = 4,
+    TST_DEBUG_ROLE_CYCLES = 8
 };
 tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, int64_t cap,
                                int64_t timeout_ns);
@@ -248,8 +269,9 @@ tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, i
  * TST_NOALLOC_SCRATCH_BYTES bytes, and builds its schedule on the stack.
  *
  * Computes the same C as gemm_plan_create + gemm_run with the same arguments
- * (schedule must be TST_STREAMK or TST_STREAMK_HYBRID; bn and num_ctas as in
- * tst_plan_options, 0 = choose).  A, B, C, bias, scales: caller-owned device
+ * and tst_plan_options.cta_group = 1 (one CTA per tile; schedule must be
+ * TST_STREAMK or TST_STREAMK_HYBRID; bn and num_ctas as in tst_plan_options,
+ * 0 = choose).  A, B, C, bias, scales: caller-owned device
  * pointers as for gemm_run.  device_status: optional device pointer to one
  * uint32 that receives the device-side status word (0 = OK, code in bits 0-7 as
  * in tst_status, e.g. 6 = a bounded wait ran out); NULL keeps it in the scratch

@@ -10,24 +10,29 @@ from __future__ import annotations
 WORKLOADS = {
     # 256^3 BF16 -> FP32, U[-1,1], linear N-fast, static (one CTA per tile)
     "c1_bf16_256": dict(M=256, N=256, K=256, dtype="bf16", dist="uniform", case=1, out="f32",
-                        mapping=("linear_nfast", 1), schedule="static", bn=128),
-    # 4096^3 BF16 -> BF16, N(0,1), 128x128 tiles, grouped-M G=8, persistent
+                        mapping=("linear_nfast", 1), schedule="static", bn=128, cta_group=1),
+    # 4096^3 BF16 -> BF16, N(0,1), 128x128 CTA tiles run as 2x1 CTA pairs (256x128 scheduled
+    # tiles), grouped-M G=8 over the pair tiles, persistent
     "c2_bf16_4096": dict(M=4096, N=4096, K=4096, dtype="bf16", dist="normal", case=2, out="bf16",
-                         mapping=("grouped_m", 8), schedule="persistent", bn=128),
+                         mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=2),
+    # the same problem with one CTA per 128x128 tile (no pairing)
+    "c2_bf16_4096_1cta": dict(M=4096, N=4096, K=4096, dtype="bf16", dist="normal", case=2, out="bf16",
+                              mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),
     # 8192^3 BF16 -> BF16, N(0,1), grouped-M G=8, persistent (BF16 target size)
     "c2x_bf16_8192": dict(M=8192, N=8192, K=8192, dtype="bf16", dist="normal", case=2, out="bf16",
-                          mapping=("grouped_m", 8), schedule="persistent", bn=256),
+                          mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2),
     # 8192^3 e4m3 (tensor-wise scales) -> BF16, N(0,1), grouped-N G=16, persistent
     "c3_e4m3_8192": dict(M=8192, N=8192, K=8192, dtype="e4m3", dist="normal", case=3, out="bf16",
-                         mapping=("grouped_n", 16), schedule="persistent", bn=256, use_scales=True),
+                         mapping=("grouped_n", 16), schedule="persistent", bn=256, cta_group=2,
+                         use_scales=True),
     # 1920 x 1920 x 16384 BF16 -> FP32, U[-1,1], 225 tiles of 128x128, Stream-K with fixup
     "c4_bf16_streamk": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
-                            mapping=("grouped_m", 8), schedule="streamk", bn=128),
+                            mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=1),
     # the same problem, grouped-M G=8 persistent (the data-parallel comparison)
     "c4_bf16_persistent": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
-                               mapping=("grouped_m", 8), schedule="persistent", bn=128),
+                               mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),
     # 16384 x 4096 x 4096 BF16 -> bf16(ReLU(0.5 acc + bias)), N(0,0.02), bias N(0,1)
     "c5_bf16_epilogue": dict(M=16384, N=4096, K=4096, dtype="bf16", dist="normal:0.02", case=5, out="bf16",
-                             mapping=("grouped_m", 8), schedule="persistent", bn=256,
+                             mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2,
                              alpha=0.5, bias_dist="normal", relu=True),
 }

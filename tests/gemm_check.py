@@ -56,7 +56,7 @@ def make_inputs(w: dict):
 def plan_for(w: dict, **over):
     kw = dict(dtype=w["dtype"], mapping=w["mapping"], schedule=w["schedule"], out_dtype=w["out"],
               alpha=w.get("alpha", 1.0), has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
-              use_scales=w.get("use_scales", False), bn=w.get("bn", 0))
+              use_scales=w.get("use_scales", False), bn=w.get("bn", 0), cta_group=w.get("cta_group", 0))
     kw.update(over)
     return tst.gemm_plan_create(w["M"], w["N"], w["K"], **kw)
 

@@ -42,6 +42,16 @@ def test_single_tile_bf16_small_integers_exact():
     assert np.array_equal(host_values(C), z)
 
 
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_single_pair_tile_small_integers_exact(bn, dtype):
+    """One CTA pair: a 256 x bn tile from two CTAs sharing one M = 256 MMA."""
+    inp, w, plan, C = _gemm(256, bn, 256, dtype=dtype, dist="int:4", use_scales=False, bn=bn, cta_group=2)
+    assert plan.info.cta_group == 2 and plan.info.ctas == 2
+    z, _ = oracle_rows(inp, w)
+    assert np.array_equal(host_values(C), z)
+
+
 def test_identity_gives_b_transpose_exactly():
     n = 256
     A = synthetic.bf16_bits(np.eye(n))
@@ -52,15 +62,17 @@ def test_identity_gives_b_transpose_exactly():
     assert np.array_equal(host_values(C), oracle.decode(inp.B, "bf16").T)
 
 
+@pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
 @pytest.mark.parametrize("bn", [128, 256])
 @pytest.mark.parametrize("mapping", MAPPINGS)
 @pytest.mark.parametrize("schedule", SCHEDULES)
-def test_small_integers_exact_every_dtype_mapping_schedule(dtype, bn, mapping, schedule):
+def test_small_integers_exact_every_dtype_mapping_schedule(dtype, bn, mapping, schedule, cta_group):
     # |partial sums| <= 64 * K < 2^24: every FP32 sum is exact whatever the order
     M, N, K = 640, 768, 640
     inp, w, plan, C = _gemm(M, N, K, dtype=dtype, dist="int:8", case=13, mapping=mapping, schedule=schedule,
-                            bn=bn, use_scales=False, num_ctas=37)
+                            bn=bn, use_scales=False, num_ctas=37 if cta_group == 1 else 13, cta_group=cta_group)
+    assert plan.info.cta_group == cta_group
     z, _ = oracle_rows(inp, w)
     assert np.array_equal(host_values(C), z)
 
@@ -102,13 +114,15 @@ def test_decode_probe_every_code_exact(dtype):
     assert (C[:, 1:] == 0).all()
 
 
+@pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("shape", [(1, 1, 8), (1, 300, 64), (300, 1, 64), (200, 136, 72), (129, 257, 520),
-                                   (127, 129, 1000), (1000, 1000, 24)])
+                                   (127, 129, 1000), (1000, 1000, 24), (257, 700, 136)])
 @pytest.mark.parametrize("schedule", ["static", "persistent", "streamk"])
-def test_ragged_shapes_within_bound(shape, schedule):
+def test_ragged_shapes_within_bound(shape, schedule, cta_group):
     M, N, K = shape
     inp, w, plan, C = _gemm(M, N, K, dist="normal", case=14, out="bf16", mapping=("grouped_m", 8),
-                            schedule=schedule, alpha=0.75, bias_dist="normal", relu=True, num_ctas=19)
+                            schedule=schedule, alpha=0.75, bias_dist="normal", relu=True, num_ctas=19,
+                            cta_group=cta_group, bn=256 if cta_group == 2 else 128)
     z, ad = oracle_rows(inp, w)
     assert_close(host_values(C), z, ad, "bf16", f"{shape}")
 
@@ -120,7 +134,8 @@ def test_e4m3_ragged_with_scales_within_bound():
     assert_close(host_values(C), z, ad, "f32", "e4m3 ragged")
 
 
-def test_cross_schedule_and_mapping_bitwise_identical():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_cross_schedule_and_mapping_bitwise_identical(cta_group):
     """Non-split schedules give every tile the same MMA sequence: identical bits."""
     M, N, K = 1024, 896, 1536
     inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=16)
@@ -128,8 +143,9 @@ def test_cross_schedule_and_mapping_bitwise_identical():
     ref = None
     for mapping in MAPPINGS:
         for schedule in ("static", "persistent"):
-            w = dict(M=M, N=N, K=K, dtype="bf16", out="f32", mapping=mapping, schedule=schedule, bn=128)
-            C = run_gemm(plan_for(w, num_ctas=29), inp, "f32", dev)
+            w = dict(M=M, N=N, K=K, dtype="bf16", out="f32", mapping=mapping, schedule=schedule, bn=128,
+                     cta_group=cta_group)
+            C = run_gemm(plan_for(w, num_ctas=29 if cta_group == 1 else 11), inp, "f32", dev)
             if ref is None:
                 ref = C.clone()
                 z, ad = oracle_rows(inp, w)
@@ -143,7 +159,7 @@ def test_streamk_forward_backward_and_repeat_bitwise():
     inp = make_inputs(w)
     dev = to_device(inp)
     fwd = run_gemm(plan_for(w), inp, "f32", dev)
-    bwd = run_gemm(plan_for(w, sk_backward=True), inp, "f32", dev)
+    bwd = run_gemm(plan_for(w, sk_forward=True), inp, "f32", dev)
     again = run_gemm(plan_for(w), inp, "f32", dev)
     assert torch.equal(fwd, bwd) and torch.equal(fwd, again)
     hyb = run_gemm(plan_for(w, schedule="streamk_hybrid"), inp, "f32", dev)
@@ -154,10 +170,11 @@ def test_streamk_forward_backward_and_repeat_bitwise():
         assert_close(host_values(C)[rows], z, ad, "f32", name)
 
 
-def test_device_trace_matches_oracle_enumeration():
-    for sched, kw in (("persistent", {}), ("streamk", {}), ("streamk", {"sk_backward": True}),
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_device_trace_matches_oracle_enumeration(cta_group):
+    for sched, kw in (("persistent", {}), ("streamk", {}), ("streamk", {"sk_forward": True}),
                       ("streamk_hybrid", {}), ("static", {})):
-        w = dict(WORKLOADS["c4_bf16_streamk"], schedule=sched)
+        w = dict(WORKLOADS["c4_bf16_streamk"], schedule=sched, cta_group=cta_group)
         plan = plan_for(w, **kw)
         info = plan.info
         cap = info.grid * info.max_items_per_cta * 8
@@ -172,8 +189,8 @@ def test_device_trace_matches_oracle_enumeration():
                 want = S.work_items(S.STATIC, u, info.tiles, info.tiles, info.kt)
             else:
                 code = {"persistent": S.PERSISTENT, "streamk": S.STREAMK, "streamk_hybrid": S.STREAMK_HYBRID}[sched]
-                want = S.work_items(code, u, info.num_sms if sched != "persistent" else P, info.tiles, info.kt,
-                                    backward=kw.get("sk_backward", False))
+                want = S.work_items(code, u, info.grid, info.tiles, info.kt,
+                                    backward=not kw.get("sk_forward", False))
             got = [tuple(r) for r in t[u] if r[0] != -1]
             exp = [(u, j, s.tile, *S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, s.tile), s.k_idx, s.k_count,
                     int(s.is_final) | (2 if s.requires_fixup else 0)) for j, s in enumerate(want)]
@@ -205,8 +222,10 @@ def test_config_full_size_sampled_rows_and_freivalds(name):
         assert (vals >= 0).all()
 
 
-def test_timeout_on_missing_load_reports_and_recovers():
-    w = dict(M=512, N=512, K=512, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="persistent", bn=128)
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_timeout_on_missing_load_reports_and_recovers(cta_group):
+    w = dict(M=512, N=512, K=512, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="persistent", bn=128,
+             cta_group=cta_group)
     inp = synthetic.make_gemm_inputs(512, 512, 512, "bf16", "normal", case=17)
     plan = plan_for(w)
     tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOAD, None, 0, timeout_ns=20_000_000)
@@ -222,10 +241,12 @@ def test_timeout_on_missing_load_reports_and_recovers():
     assert_close(host_values(C2), z, ad, "f32", "after timeout")
 
 
-def test_timeout_on_unpublished_streamk_lock():
-    w = dict(M=384, N=384, K=2048, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="streamk", bn=128)
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_timeout_on_unpublished_streamk_lock(cta_group):
+    w = dict(M=384, N=384, K=2048, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="streamk", bn=128,
+             cta_group=cta_group)
     inp = synthetic.make_gemm_inputs(384, 384, 2048, "bf16", "normal", case=18)
-    plan = plan_for(w, num_ctas=16)
+    plan = plan_for(w, num_ctas=16 if cta_group == 1 else 8)
     tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOCK, None, 0, timeout_ns=20_000_000)
     A, B, _, _ = to_device(inp)
     C = torch.zeros(384, 384, device="cuda")

@@ -47,6 +47,7 @@ def test_status_strings():
 def _host_plan(M, N, K, **kw):
     kw.setdefault("host_only", True)
     kw.setdefault("num_sms", 152)
+    kw.setdefault("cta_group", 1)
     return tst.gemm_plan_create(M, N, K, **kw)
 
 
@@ -132,7 +133,7 @@ def test_work_lists_match_oracle(sched, shape, sms):
     M, N, K = shape
     for backward in (False, True):
         p = _host_plan(M, N, K, mapping=("grouped_m", 8), schedule=sched, bn=128, num_sms=sms,
-                       sk_backward=backward)
+                       sk_forward=not backward)
         i = p.info
         T = i.tiles
         P = i.grid if sched != "static" else T
@@ -158,3 +159,32 @@ def test_hybrid_plan_matches_rule():
     assert (p.info.dp_tiles, p.info.sk_tiles) == (152, S.hybrid_split_count(225, 152))
     q = _host_plan(1920, 1920, 16384, schedule="streamk_hybrid", bn=128, num_sms=148)
     assert q.info.sk_tiles == 0 and q.info.dp_tiles == 225
+
+
+def test_pair_plans_schedule_256_row_tiles_over_pairs():
+    # CTA pairs: the scheduled tile is 256 x bn, and the units are pairs (152 SMs -> 76 pairs)
+    p = _host_plan(4096, 4096, 4096, mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=2)
+    i = p.info
+    assert (i.bm, i.bn, i.mt, i.nt, i.cta_group) == (256, 128, 16, 32, 2)
+    assert i.grid == 76 and i.ctas == 152
+    for u in (0, 5, 75):
+        got = tst.gemm_work_items(p, u)
+        assert [t for t, *_ in got] == list(range(u, 512, 76))
+        for t, m, n, *_ in got:
+            assert (m, n) == S.tile_map(S.GROUPED_M, 8, 16, 32, t)
+    sk = _host_plan(1920, 1920, 16384, schedule="streamk", bn=128, cta_group=2)
+    assert (sk.info.mt, sk.info.nt, sk.info.grid, sk.info.sk_tiles) == (8, 15, 76, 120)
+    want = [(s.tile, s.k_idx, s.k_count) for s in S.work_items(S.STREAMK, 3, 76, 120, 256, backward=True)]
+    assert [(t, kb, kc) for t, _, _, kb, kc, _ in tst.gemm_work_items(sk, 3)] == want
+    # one lock and one 128 x bn partial tile per CTA-half of each split tile
+    assert sk.info.workspace_bytes >= 120 * 2 * 128 * 128 * 4
+
+
+def test_auto_choices():
+    big = tst.gemm_plan_create(8192, 8192, 8192, host_only=True, num_sms=152)
+    assert (big.info.bn, big.info.cta_group) == (256, 2)
+    small = tst.gemm_plan_create(256, 256, 256, host_only=True, num_sms=152)
+    assert (small.info.bn, small.info.cta_group) == (128, 1)
+    with pytest.raises(tst.TstError) as e:
+        _host_plan(256, 256, 256, cta_group=3)
+    assert e.value.status == tst.TST_ERR_UNSUPPORTED

@@ -14,7 +14,7 @@ from . import _capi
 from ._capi import (TST_BF16, TST_E4M3, TST_OUT_F32, TST_OUT_BF16, TST_LAYOUT_A_ROW_B_NK,  # noqa: F401
                     TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N,
                     TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID,
-                    TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK,
+                    TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG_ROLE_CYCLES,
                     TST_OK, TST_ERR_INVALID_ARG, TST_ERR_UNSUPPORTED, TST_ERR_ALIGNMENT, TST_ERR_OOM,
                     TST_ERR_CUDA, TST_ERR_TIMEOUT, TST_ERR_DEVICE_CHECK, TST_ERR_NO_DEVICE,
                     TST_NOALLOC_SCRATCH_BYTES)
@@ -79,14 +79,15 @@ class Plan:
 
 def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfast", 1), schedule="static",
                      out_dtype="f32", alpha: float = 1.0, has_bias: bool = False, relu: bool = False,
-                     use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_backward: bool = False,
-                     host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0) -> Plan:
+                     use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_forward: bool = False,
+                     host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
+                     stages: int = 0) -> Plan:
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     epi = _capi.tst_epilogue(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), int(bool(has_bias)),
                              int(bool(relu)), int(bool(use_scales)))
-    opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_backward)), int(bool(host_only)),
-                                  int(num_sms), 0, int(timeout_ns))
+    opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
+                                  int(num_sms), int(cta_group), int(timeout_ns), int(stages), 0)
     h = ctypes.c_void_p()
     _check(lib.gemm_plan_create_ex(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
                                    TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtstgemm.so")
-SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_e4m3.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_bf16_cg1.cu", "gemm_bf16_cg2.cu", "gemm_e4m3_cg1.cu", "gemm_e4m3_cg2.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-diag-suppress", "177", f"-I{INCLUDE}", f"-I{CSRC}"]

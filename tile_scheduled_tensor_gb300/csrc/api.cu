@@ -31,7 +31,8 @@ struct tst_plan {
   tst_epilogue epi{};
   tst_plan_options opts{};
   int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
-  int32_t num_sms = 0, max_items = 0;
+  int32_t cg = 1;              // CTAs per scheduling unit (2 = CTA pair)
+  int32_t num_sms = 0, max_items = 0, resident_units = 0;
   tst::Sched sched{};
   bool host_only = false;
   int device = -1;
@@ -44,6 +45,7 @@ struct tst_plan {
   // debug
   int32_t debug_flags = 0;
   int32_t* trace = nullptr;
+  unsigned long long* stats = nullptr;
   int64_t trace_cap = 0;
   uint64_t timeout_ns = 10ull * 1000 * 1000 * 1000;
   // launch
@@ -173,21 +175,67 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
     p->num_sms = o.num_sms > 0 ? std::min(o.num_sms, sms) : sms;
   }
 
-  // tile configuration: 128-row tiles, 128-byte operand rows
+  // tile configuration: 128-row CTA tiles (256-row pair tiles), 128-byte operand rows
+  if (o.cta_group != 0 && o.cta_group != 1 && o.cta_group != 2) { delete p; return TST_ERR_UNSUPPORTED; }
   p->bk = 128 / elt;
-  const int64_t mt = ceil_div(M, p->bm);
   if (o.bn != 0) {
     p->bn = o.bn;
   } else {
-    // wide tiles when they still give at least one full wave
-    p->bn = (N > 128 && mt * ceil_div(N, 256) >= p->num_sms) ? 256 : 128;
+    // wide tiles when they still give at least one full wave of CTAs
+    p->bn = (N > 128 && ceil_div(M, 128) * ceil_div(N, 256) >= p->num_sms) ? 256 : 128;
   }
+  if (o.cta_group != 0) {
+    p->cg = o.cta_group;
+  } else {
+    // pairs halve each CTA's share of B; use them when there is a full wave of pair tiles
+    p->cg = (M > 128 && ceil_div(M, 256) * ceil_div(N, p->bn) >= p->num_sms / 2) ? 2 : 1;
+  }
+  p->bm = tst::kBlockM * p->cg;
+  const int64_t mt = ceil_div(M, p->bm);
   const int64_t nt = ceil_div(N, p->bn);
   const int64_t kt = ceil_div(K, p->bk);
   const int64_t T = mt * nt;
-  if (T >= (int64_t(1) << 31) || T * kt >= (int64_t(1) << 62)) { delete p; return TST_ERR_INVALID_ARG; }
-  p->stages = tst_kernel_stages(p->bn);
-  p->smem_bytes = tst_kernel_smem_bytes(p->bn);
+  if (T >= (int64_t(1) << 30) || T * kt >= (int64_t(1) << 62)) { delete p; return TST_ERR_INVALID_ARG; }
+  p->stages = tst_kernel_stages(p->bn, p->cg);
+  if (o.stages != 0) {
+    if (o.stages < 2 || o.stages > p->stages) { delete p; return TST_ERR_UNSUPPORTED; }
+    p->stages = o.stages;
+  }
+  p->smem_bytes = tst_kernel_smem_bytes(p->bn, p->cg);
+  if (!p->host_only) {
+    p->kernel = tst_kernel(dtype, p->bn, epi->out_dtype, p->cg);
+    if (!p->kernel ||
+        cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      delete p;
+      return TST_ERR_CUDA;
+    }
+  }
+
+  // scheduling units that can be resident at once: one CTA per SM, or pairs
+  // of CTAs placed together as clusters of 2
+  int64_t resident = p->num_sms;
+  if (p->cg == 2) {
+    resident = p->num_sms / 2;
+    if (!p->host_only) {
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(static_cast<unsigned>(2 * resident), 1, 1);
+      qc.blockDim = dim3(tst::kThreads, 1, 1);
+      qc.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
+      cudaLaunchAttribute ca[1];
+      ca[0].id = cudaLaunchAttributeClusterDimension;
+      ca[0].val.clusterDim.x = 2;
+      ca[0].val.clusterDim.y = 1;
+      ca[0].val.clusterDim.z = 1;
+      qc.attrs = ca;
+      qc.numAttrs = 1;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, p->kernel, &qc) == cudaSuccess && clusters > 0)
+        resident = std::min<int64_t>(resident, clusters);
+      cudaGetLastError();
+    }
+  }
+  p->resident_units = static_cast<int32_t>(resident);
 
   // schedule
   tst::Sched& s = p->sched;
@@ -196,8 +244,8 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   s.kt = static_cast<int32_t>(kt);
   s.map_kind = mapping.kind;
   s.group = (mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N) ? mapping.group : 1;
-  s.backward = o.sk_backward ? 1 : 0;
-  const int64_t P = o.num_ctas > 0 ? o.num_ctas : p->num_sms;
+  s.backward = o.sk_forward ? 0 : 1;
+  const int64_t P = o.num_ctas > 0 ? o.num_ctas : resident;
   switch (schedule) {
     case TST_STATIC:
       s.grid = static_cast<int32_t>(T); s.dp_tiles = static_cast<int32_t>(T); s.sk_tiles = 0;
@@ -216,8 +264,8 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
       break;
     }
   }
-  if ((schedule == TST_STREAMK || schedule == TST_STREAMK_HYBRID) && !p->host_only && P > p->num_sms) {
-    // split tiles wait on each other: every CTA must be resident at once
+  if ((schedule == TST_STREAMK || schedule == TST_STREAMK_HYBRID) && !p->host_only && P > resident) {
+    // split tiles wait on each other: every unit must be resident at once
     delete p;
     return TST_ERR_UNSUPPORTED;
   }
@@ -233,10 +281,12 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   }
   p->max_items = max_items;
 
-  // plan-owned device memory
+  // plan-owned device memory: status word, then one lock and one 128 x bn FP32
+  // partial tile per CTA-half of each split tile
+  const size_t slots = static_cast<size_t>(s.sk_tiles) * p->cg;
   const size_t status_bytes = 256;
-  const size_t lock_bytes = ((static_cast<size_t>(s.sk_tiles) * 4 + 255) / 256) * 256;
-  const size_t ws_bytes = static_cast<size_t>(s.sk_tiles) * p->bm * p->bn * sizeof(float);
+  const size_t lock_bytes = ((slots * 4 + 255) / 256) * 256;
+  const size_t ws_bytes = slots * tst::kBlockM * p->bn * sizeof(float);
   p->reset_bytes = status_bytes + lock_bytes;
   p->dev_bytes = status_bytes + lock_bytes + ws_bytes;
   if (!p->host_only) {
@@ -254,21 +304,13 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
     p->d_status = reinterpret_cast<uint32_t*>(base);
     p->d_locks = reinterpret_cast<int32_t*>(base + status_bytes);
     p->d_ws = ws_bytes ? reinterpret_cast<float*>(base + status_bytes + lock_bytes) : nullptr;
-    p->kernel = dtype == TST_BF16 ? tst_kernel_bf16(p->bn, epi->out_dtype) : tst_kernel_e4m3(p->bn, epi->out_dtype);
-    if (!p->kernel ||
-        cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(p->dev_block);
-      delete p;
-      return TST_ERR_CUDA;
-    }
   }
   if (log_enabled())
     fprintf(stderr,
-            "[tstgemm] plan M=%lld N=%lld K=%lld dtype=%d tile=%dx%dx%d stages=%d grid=%d (sms=%d) tiles=%lld "
-            "dp=%d sk=%d kt=%d map=%d G=%d sched=%d max_items=%d ws=%zu B\n",
-            (long long)M, (long long)N, (long long)K, (int)dtype, p->bm, p->bn, p->bk, p->stages, s.grid,
-            p->num_sms, (long long)T, s.dp_tiles, s.sk_tiles, s.kt, s.map_kind, s.group, (int)schedule,
+            "[tstgemm] plan M=%lld N=%lld K=%lld dtype=%d tile=%dx%dx%d cta_group=%d stages=%d grid=%d "
+            "(resident %d, sms=%d) tiles=%lld dp=%d sk=%d kt=%d map=%d G=%d sched=%d max_items=%d ws=%zu B\n",
+            (long long)M, (long long)N, (long long)K, (int)dtype, p->bm, p->bn, p->bk, p->cg, p->stages, s.grid,
+            p->resident_units, p->num_sms, (long long)T, s.dp_tiles, s.sk_tiles, s.kt, s.map_kind, s.group, (int)schedule,
             p->max_items, p->dev_bytes);
   *out = p;
   return TST_OK;
@@ -301,6 +343,8 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->max_items_per_cta = p->max_items;
   info->smem_bytes = p->smem_bytes;
   info->workspace_bytes = static_cast<int64_t>(p->dev_bytes);
+  info->cta_group = p->cg;
+  info->ctas = p->sched.grid * p->cg;
   return TST_OK;
 }
 
@@ -331,12 +375,18 @@ tst_status gemm_work_items(const tst_plan* p, int32_t cta, tst_work_item* items,
 
 tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int64_t cap, int64_t timeout_ns) {
   if (p == nullptr || cap < 0 || timeout_ns < 0) return TST_ERR_INVALID_ARG;
+  if ((flags & TST_DEBUG_TRACE) && (flags & TST_DEBUG_ROLE_CYCLES)) return TST_ERR_INVALID_ARG;
   if (flags & TST_DEBUG_TRACE) {
     const int64_t need = static_cast<int64_t>(p->sched.grid) * p->max_items * 8;
     if (trace_buf == nullptr || cap < need) return TST_ERR_INVALID_ARG;
   }
+  if (flags & TST_DEBUG_ROLE_CYCLES) {
+    const int64_t need = static_cast<int64_t>(p->sched.grid) * p->cg * tst::kStatSlots * 2;  // int32 units
+    if (trace_buf == nullptr || cap < need || (reinterpret_cast<uintptr_t>(trace_buf) & 7u)) return TST_ERR_INVALID_ARG;
+  }
   p->debug_flags = flags;
   p->trace = (flags & TST_DEBUG_TRACE) ? static_cast<int32_t*>(trace_buf) : nullptr;
+  p->stats = (flags & TST_DEBUG_ROLE_CYCLES) ? static_cast<unsigned long long*>(trace_buf) : nullptr;
   p->trace_cap = cap;
   if (timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(timeout_ns);
   else if (p->opts.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(p->opts.timeout_ns);
@@ -356,12 +406,14 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
     return TST_ERR_ALIGNMENT;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
+  // TMA boxes are per CTA: 128 rows of A, and bn / cta_group rows of B (a CTA
+  // pair splits the B rows of its 256 x bn tile between its two CTAs)
   if (A != p->tm_A) {
-    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, p->bk, p->bm)) return TST_ERR_CUDA;
+    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, p->bk, tst::kBlockM)) return TST_ERR_CUDA;
     p->tm_A = A;
   }
   if (B != p->tm_B) {
-    if (!encode_operand(&p->tmap_b, B, p->dtype, p->N, p->K, p->bk, p->bn)) return TST_ERR_CUDA;
+    if (!encode_operand(&p->tmap_b, B, p->dtype, p->N, p->K, p->bk, p->bn / p->cg)) return TST_ERR_CUDA;
     p->tm_B = B;
   }
 
@@ -375,6 +427,7 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.locks = p->d_locks;
   kp.status = p->d_status;
   kp.trace = p->trace;
+  kp.stats = p->stats;
   kp.M = static_cast<int32_t>(p->M);
   kp.N = static_cast<int32_t>(p->N);
   kp.K = static_cast<int32_t>(p->K);
@@ -385,18 +438,27 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.use_scales = p->epi.use_scales ? 1 : 0;
   kp.debug_flags = p->debug_flags;
   kp.max_items = p->max_items;
+  kp.stages = p->stages;
   kp.timeout_ns = p->timeout_ns;
 
   // status word and Stream-K locks start at zero for every launch
   if (cudaMemsetAsync(p->dev_block, 0, p->reset_bytes, stream) != cudaSuccess) return TST_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg), 1, 1);
   cfg.blockDim = dim3(tst::kThreads, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  if (p->sched.sk_tiles > 0) {
+  if (p->cg == 2) {
+    // the two CTAs of a pair run as a cluster of 2 (co-scheduled on a pair of SMs)
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  } else if (p->sched.sk_tiles > 0) {
     // Stream-K splits wait on each other across CTAs: ask for a co-resident grid
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;

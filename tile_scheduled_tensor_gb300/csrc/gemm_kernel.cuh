@@ -1,6 +1,6 @@
-// Warp-specialised tcgen05 GEMM kernel for sm_103a.
+// Warp-specialised tcgen05 GEMM kernel for sm_103a, single CTA or CTA pair.
 //
-// One CTA of 192 threads per SM:
+// 192 threads per CTA, one CTA per SM:
 //   warp 0      TMA producer: for each k-tile of each work item, wait EMPTY[s],
 //               announce the stage's bytes on FULL[s], issue the A and B tile
 //               loads (128-byte swizzle, K-major).
@@ -16,6 +16,15 @@
 // 2 x 256), so the MMA of the next work item overlaps the epilogue of the
 // previous one.
 //
+// CG = 2 runs a cluster of two CTAs as one unit (tcgen05 "cta_group::2"): the
+// scheduled tile is 256 x BN; each CTA loads its own 128 rows of A and half of
+// the BN rows of B into its own shared memory, both CTAs' loads complete on the
+// leader's (rank 0) FULL barrier, the leader alone issues the M = 256 MMA and
+// its commits arrive on EMPTY / TMEM_FULL in both CTAs, and each CTA's epilogue
+// drains its own half of the accumulator (its own TMEM) and arrives on the
+// leader's TMEM_EMPTY.  Per CTA this halves the B bytes moved from L2 and read
+// by the tensor core compared with CG = 1 at the same tile width.
+//
 // The FULL/EMPTY two-barrier handshake with a phase bit, the producer and
 // consumer flows and the drain follow "H100 . Kernel Design" (runguoli.com H100
 // course notes, Lesson 8), sections 4-6.  The epilogue order follows section
@@ -23,13 +32,15 @@
 // and sets the lock; a later split waits until the lock equals its K_idx, adds,
 // and either publishes a larger lock or, as the final split, finishes the tile)
 // follows section 10.3 and "H100 . Stream-K scheduling" (Lesson 8.1),
-// sections 5-6, in the deterministic mode.  Where the pages' Hopper designs
-// keep the accumulator in registers (ping-pong / cooperative warpgroups,
-// setmaxnreg), this kernel keeps it in Tensor Memory instead.
+// sections 5-6, in the deterministic mode.  The CTA pair plays the role of the
+// pages' cluster of 2 (Lesson 8, section 10.1 "Cluster and swizzling").  Where
+// the pages' Hopper designs keep the accumulator in registers (ping-pong /
+// cooperative warpgroups, setmaxnreg), this kernel keeps it in Tensor Memory.
 //
-// Every wait is bounded: on expiry the kernel records TIMEOUT in the status
-// word, raises a CTA-wide abort flag, lets each role leave its loop, waits
-// (bounded) for its own copies and MMAs in flight, frees TMEM and returns.
+// Every wait on an mbarrier or a lock is bounded: on expiry the kernel records
+// TIMEOUT in the status word, raises the abort flag of its CTA (and of the
+// peer CTA), lets each role leave its loop, waits (bounded) for its own copies
+// and MMAs in flight, frees TMEM and returns.
 #pragma once
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -41,29 +52,39 @@ namespace tst {
 
 struct SharedCtl {
   uint32_t tmem_base;
-  uint32_t abort;      // set by any role whose wait ran out
+  uint32_t abort;      // set by any role of this CTA (or of the peer) whose wait ran out
   uint32_t ep_ok;      // elected epilogue thread's verdict for the current item
   uint32_t pad;
 };
 
-__device__ __forceinline__ void raise_error(const KernelParams& p, volatile uint32_t* abort, uint32_t code,
-                                            uint32_t role) {
-  *abort = 1u;
+// Per-CTA context shared by the roles.
+struct Ctx {
+  volatile uint32_t* abort;
+  uint32_t peer_abort;  // shared::cluster address of the peer's abort flag (pairs only)
+  uint32_t rank;        // 0 = leader / single CTA, 1 = peer
+  int32_t unit;         // scheduling unit: the CTA (CG = 1) or the CTA pair (CG = 2)
+};
+
+template <int CG>
+__device__ __forceinline__ void raise_error(const KernelParams& p, const Ctx& c, uint32_t code, uint32_t role) {
+  *c.abort = 1u;
+  if (CG == 2) ptx::st_cluster_u32(c.peer_abort, 1u);
   atomicCAS(p.status, 0u, code | (role << 8) | (static_cast<uint32_t>(blockIdx.x) << 16));
 }
 
 // Wait until the phase with `parity` of mbarrier `bar` completes.  Returns false
 // if the CTA is aborting or the wait ran out (which starts the abort).
-__device__ __forceinline__ bool wait_phase(const KernelParams& p, volatile uint32_t* abort, uint32_t bar,
-                                           uint32_t parity, uint32_t role) {
+template <int CG>
+__device__ __forceinline__ bool wait_phase(const KernelParams& p, const Ctx& c, uint32_t bar, uint32_t parity,
+                                           uint32_t role) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t spin = 1;; ++spin) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((spin & 15u) == 0u) {
-      if (*abort) return false;
+      if (*c.abort) return false;
       if (ptx::globaltimer() - t0 > p.timeout_ns) {
-        raise_error(p, abort, ST_TIMEOUT, role);
+        raise_error<CG>(p, c, ST_TIMEOUT, role);
         return false;
       }
     }
@@ -71,17 +92,17 @@ __device__ __forceinline__ bool wait_phase(const KernelParams& p, volatile uint3
 }
 
 // Bounded wait for a Stream-K lock to reach exactly `want` k-tiles.
-__device__ __forceinline__ bool wait_lock(const KernelParams& p, volatile uint32_t* abort, const int32_t* lock,
-                                          int32_t want) {
+template <int CG>
+__device__ __forceinline__ bool wait_lock(const KernelParams& p, const Ctx& c, const int32_t* lock, int32_t want) {
   if (ptx::ld_acquire_gpu(lock) == want) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t spin = 1;; ++spin) {
     __nanosleep(64);
     if (ptx::ld_acquire_gpu(lock) == want) return true;
     if ((spin & 15u) == 0u) {
-      if (*abort) return false;
+      if (*c.abort) return false;
       if (ptx::globaltimer() - t0 > p.timeout_ns) {
-        raise_error(p, abort, ST_TIMEOUT, ROLE_LOCK);
+        raise_error<CG>(p, c, ST_TIMEOUT, ROLE_LOCK);
         return false;
       }
     }
@@ -89,46 +110,61 @@ __device__ __forceinline__ bool wait_lock(const KernelParams& p, volatile uint32
 }
 
 // ------------------------------------------------------------------ producer
-template <int BN, int DT>
-__device__ __forceinline__ void run_producer(const KernelParams& p, uint32_t smem_a, uint32_t smem_b,
-                                             uint32_t bar_full, uint32_t bar_empty, volatile uint32_t* abort) {
-  using Cfg = TileCfg<BN>;
+template <int BN, int DT, int CG>
+__device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c, uint32_t smem_a, uint32_t smem_b,
+                                             uint32_t bar_full, uint32_t bar_empty) {
+  using Cfg = TileCfg<BN, CG>;
   constexpr int BK = DT == DT_BF16 ? 64 : 128;
+  constexpr int BM_UNIT = kBlockM * CG;   // rows of the scheduled tile
+  constexpr int BN_CTA = BN / CG;         // B rows this CTA loads
+  // pairs: both CTAs' loads complete on the leader's FULL barriers
+  const uint32_t full_target = CG == 2 ? ptx::mapa(bar_full, 0) : bar_full;
+  const bool leader = c.rank == 0;
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued = 0, issued_parity = 0;  // per stage: a load was issued / parity of that phase
   bool ok = true;
   WorkIter it;
-  work_begin(p.sched, blockIdx.x, it);
+  work_begin(p.sched, c.unit, it);
   WorkItem w;
   int32_t seq = 0;
+  long long wait_empty = 0;
   while (ok && work_next(p.sched, it, w)) {
-    if (p.trace != nullptr && seq < p.max_items) {
-      int32_t* rec = p.trace + (static_cast<int64_t>(blockIdx.x) * p.max_items + seq) * 8;
-      rec[0] = blockIdx.x; rec[1] = seq; rec[2] = w.tile; rec[3] = w.m;
+    if (p.trace != nullptr && leader && seq < p.max_items) {
+      int32_t* rec = p.trace + (static_cast<int64_t>(c.unit) * p.max_items + seq) * 8;
+      rec[0] = c.unit; rec[1] = seq; rec[2] = w.tile; rec[3] = w.m;
       rec[4] = w.n; rec[5] = w.k_begin; rec[6] = w.k_count; rec[7] = w.flags;
     }
-    const int32_t m0 = w.m * kBlockM;
-    const int32_t n0 = w.n * BN;
+    const int32_t m0 = w.m * BM_UNIT + static_cast<int32_t>(c.rank) * kBlockM;
+    const int32_t n0 = w.n * BN + static_cast<int32_t>(c.rank) * BN_CTA;
     for (int32_t kb = w.k_begin; kb < w.k_begin + w.k_count; ++kb) {
-      if (!wait_phase(p, abort, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
-      const uint32_t full = bar_full + 8 * stage;
-      ptx::mbar_arrive_expect_tx(full, Cfg::STAGE_BYTES);
+      const long long t0 = p.stats ? clock64() : 0;
+      if (!wait_phase<CG>(p, c, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
+      if (p.stats) wait_empty += clock64() - t0;
+      if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * Cfg::STAGE_BYTES);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
-        ptx::tma_load_2d(smem_a + stage * Cfg::A_BYTES, &p.tmap_a, full, kb * BK, m0);
-        ptx::tma_load_2d(smem_b + stage * Cfg::B_BYTES, &p.tmap_b, full, kb * BK, n0);
+        if (CG == 2) {
+          ptx::tma_load_2d_pair(smem_a + stage * Cfg::A_BYTES, &p.tmap_a, full_target + 8 * stage, kb * BK, m0);
+          ptx::tma_load_2d_pair(smem_b + stage * Cfg::B_BYTES, &p.tmap_b, full_target + 8 * stage, kb * BK, n0);
+        } else {
+          ptx::tma_load_2d(smem_a + stage * Cfg::A_BYTES, &p.tmap_a, bar_full + 8 * stage, kb * BK, m0);
+          ptx::tma_load_2d(smem_b + stage * Cfg::B_BYTES, &p.tmap_b, bar_full + 8 * stage, kb * BK, n0);
+        }
       }
       issued |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-      if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1u; }
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     ++seq;
   }
-  if (!ok) {
-    // aborting: wait (bounded) until the loads already issued have landed
+  if (p.stats) p.stats[blockIdx.x * kStatSlots + STAT_PROD_WAIT_EMPTY] = wait_empty;
+  if (!ok && leader) {
+    // aborting: wait (bounded) until the loads already issued have landed.  For a
+    // pair the leader's FULL barrier counts both CTAs' bytes, and the peer stays
+    // alive at the final cluster barrier until the leader gets there.
     const uint64_t t0 = ptx::globaltimer();
-    for (int s = 0; s < Cfg::STAGES; ++s) {
+    for (int s = 0; s < p.stages; ++s) {
       if (!(issued & (1u << s))) continue;
       const uint32_t par = (issued_parity >> s) & 1u;
       while (!ptx::mbar_try_wait(bar_full + 8 * s, par)) {
@@ -138,53 +174,76 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, uint32_t sme
   }
 }
 
-// ------------------------------------------------------------------ MMA issuer
-template <int BN, int DT>
-__device__ __forceinline__ void run_mma(const KernelParams& p, uint32_t tmem_base, uint32_t smem_a,
-                                        uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty,
-                                        uint32_t bar_tfull, uint32_t bar_tempty, uint32_t bar_drain,
-                                        volatile uint32_t* abort) {
-  using Cfg = TileCfg<BN>;
-  constexpr uint32_t kIdesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM, BN);
+// ------------------------------------------------------------------ MMA issuer (leader only)
+template <int BN, int DT, int CG>
+__device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uint32_t tmem_base, uint32_t smem_a,
+                                        uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
+                                        uint32_t bar_tempty, uint32_t bar_drain) {
+  using Cfg = TileCfg<BN, CG>;
+  constexpr uint32_t kIdesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
   bool ok = true;
+  const uint64_t a_desc0 = ptx::sw128_kmajor_desc(smem_a);
+  const uint64_t b_desc0 = ptx::sw128_kmajor_desc(smem_b);
   WorkIter it;
-  work_begin(p.sched, blockIdx.x, it);
+  work_begin(p.sched, c.unit, it);
   WorkItem w;
+  long long wait_full = 0, wait_tempty = 0, kblocks = 0;
   while (ok && work_next(p.sched, it, w)) {
-    if (!wait_phase(p, abort, bar_tempty + 8 * acc, acc_phase ^ 1u, ROLE_MMA)) { ok = false; break; }
+    // pairs: TMEM_EMPTY counts both CTAs' epilogues
+    const long long t0 = p.stats ? clock64() : 0;
+    if (!wait_phase<CG>(p, c, bar_tempty + 8 * acc, acc_phase ^ 1u, ROLE_MMA)) { ok = false; break; }
+    if (p.stats) wait_tempty += clock64() - t0;
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
     for (int32_t i = 0; i < w.k_count; ++i) {
-      if (!wait_phase(p, abort, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
-      ptx::tc_fence_after();
-      const uint64_t a_desc = ptx::sw128_kmajor_desc(smem_a + stage * Cfg::A_BYTES);
-      const uint64_t b_desc = ptx::sw128_kmajor_desc(smem_b + stage * Cfg::B_BYTES);
+      const long long t1 = p.stats ? clock64() : 0;
+      // the stage was filled by TMA and announced on its mbarrier: the wait alone
+      // orders the MMA's shared-memory reads after the copy (no tcgen05 fence)
+      if (!wait_phase<CG>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
+      if (p.stats) { wait_full += clock64() - t1; ++kblocks; }
+      // descriptor start address is in 16-byte units: step to this stage's tiles
+      const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
+      const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         // each step consumes 32 bytes of K (16 BF16 or 32 e4m3): advance start address by 32 B
         const uint64_t off = static_cast<uint64_t>(k * 2);
-        if (DT == DT_BF16)
-          ptx::mma_f16(d_tmem, a_desc + off, b_desc + off, kIdesc, (i | k) != 0);
-        else
-          ptx::mma_f8(d_tmem, a_desc + off, b_desc + off, kIdesc, (i | k) != 0);
+        const uint32_t accumulate = (i | k) != 0;
+        if (CG == 2) {
+          if (DT == DT_BF16) ptx::mma_f16_pair(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
+          else ptx::mma_f8_pair(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
+        } else {
+          if (DT == DT_BF16) ptx::mma_f16(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
+          else ptx::mma_f8(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
+        }
       }
-      ptx::mma_commit(bar_empty + 8 * stage);  // stage free once these MMAs have read it
-      if (++stage == Cfg::STAGES) { stage = 0; phase ^= 1u; }
+      // stage free (in both CTAs of a pair) once these MMAs have read it
+      if (CG == 2) ptx::mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+      else ptx::mma_commit(bar_empty + 8 * stage);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    ptx::mma_commit(bar_tfull + 8 * acc);      // accumulator ready for the epilogue
+    // accumulator ready for the epilogue(s)
+    if (CG == 2) ptx::mma_commit_pair_mc(bar_tfull + 8 * acc, 0x3);
+    else ptx::mma_commit(bar_tfull + 8 * acc);
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
   }
+  if (p.stats) {
+    p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_FULL] = wait_full;
+    p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_TEMPTY] = wait_tempty;
+    p.stats[blockIdx.x * kStatSlots + STAT_KBLOCKS] = kblocks;
+  }
   // every MMA issued above completes before TMEM can be released
-  ptx::mma_commit(bar_drain);
+  if (CG == 2) ptx::mma_commit_pair(bar_drain);
+  else ptx::mma_commit(bar_drain);
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar_drain, 0)) {
     if (ptx::globaltimer() - t0 > p.timeout_ns) {
-      raise_error(p, abort, ST_TIMEOUT, ROLE_MMA);
+      raise_error<CG>(p, c, ST_TIMEOUT, ROLE_MMA);
       break;
     }
   }
@@ -228,94 +287,124 @@ __device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, 
   }
 }
 
-template <int BN, int OUT>
-__device__ __forceinline__ void run_epilogue(const KernelParams& p, uint32_t tmem_base, uint32_t bar_tfull,
-                                             uint32_t bar_tempty, SharedCtl* ctl) {
-  using Cfg = TileCfg<BN>;
-  volatile uint32_t* abort = &ctl->abort;
+template <int BN, int OUT, int CG>
+__device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
+                                             uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
+  using Cfg = TileCfg<BN, CG>;
   volatile uint32_t* ep_ok = &ctl->ep_ok;
   const int ep = threadIdx.x - 64;             // 0..127
   const int quad = (threadIdx.x >> 5) & 3;     // TMEM lane quadrant this warp may access
   const int lane = threadIdx.x & 31;
   const int row_in_tile = quad * 32 + lane;
+  // pairs: arrive on the leader's TMEM_EMPTY barriers
+  const uint32_t tempty_target = CG == 2 ? ptx::mapa(bar_tempty, 0) : bar_tempty;
   float alpha = p.alpha;
   if (p.use_scales) alpha = alpha * __ldg(p.scales) * __ldg(p.scales + 1);
+  const bool bias_vec = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && (p.N & 3) == 0;
 
   int acc = 0;
   uint32_t acc_phase = 0;
   WorkIter it;
-  work_begin(p.sched, blockIdx.x, it);
+  work_begin(p.sched, c.unit, it);
   WorkItem w;
+  long long wait_tfull = 0, busy = 0, items = 0;
   while (work_next(p.sched, it, w)) {
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
     const bool final_split = (w.flags & ITEM_FINAL) != 0;
-    const int32_t slot = w.tile - p.sched.dp_tiles;   // Stream-K slot (valid when fixup)
+    // Stream-K slot of this CTA's half of the tile (valid when fixup)
+    const int32_t slot = (w.tile - p.sched.dp_tiles) * CG + static_cast<int32_t>(c.rank);
     // one elected thread waits; the verdict is broadcast so all 128 threads
     // take the same path through the named barriers below
+    const long long t0 = (p.stats && ep == 0) ? clock64() : 0;
     if (ep == 0) {
-      bool ok = wait_phase(p, abort, bar_tfull + 8 * acc, acc_phase, ROLE_EPILOGUE);
-      if (ok && fixup && w.k_begin > 0) ok = wait_lock(p, abort, p.locks + slot, w.k_begin);
+      bool ok = wait_phase<CG>(p, c, bar_tfull + 8 * acc, acc_phase, ROLE_EPILOGUE);
+      if (ok && fixup && w.k_begin > 0) ok = wait_lock<CG>(p, c, p.locks + slot, w.k_begin);
       *ep_ok = ok ? 1u : 0u;
     }
     ptx::named_bar_sync(1, 128);
     if (*ep_ok == 0u) break;
+    const long long t1 = (p.stats && ep == 0) ? clock64() : 0;
+    if (p.stats && ep == 0) wait_tfull += t1 - t0;
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
     ptx::tc_fence_after();
 
-    const int32_t row = w.m * kBlockM + row_in_tile;
+    const int32_t row = w.m * (kBlockM * CG) + static_cast<int32_t>(c.rank) * kBlockM + row_in_tile;
     const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      float v[32];
-      ptx::tmem_load_32cols(t_row + c * 32, v);
-      // workspace layout per slot: [column][row], so a warp's 32 rows are contiguous
-      float* wsc = ws != nullptr ? ws + (c * 32) * kBlockM + row_in_tile : nullptr;
-      if (fixup && !final_split) {
-        if (w.k_begin == 0) {
+    for (int ch = 0; ch < BN / 64; ++ch) {
+      float v[64];
+      ptx::tmem_load_64cols(t_row + ch * 64, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) __stcg(wsc + j * kBlockM, v[j]);
-        } else {
+      for (int h = 0; h < 2; ++h) {
+        const int c32 = ch * 2 + h;
+        // workspace layout per slot: [column][row], so a warp's 32 rows are contiguous
+        float* wsc = ws != nullptr ? ws + (c32 * 32) * kBlockM + row_in_tile : nullptr;
+        if (fixup && !final_split) {
+          if (w.k_begin == 0) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) __stcg(wsc + j * kBlockM, __ldcg(wsc + j * kBlockM) + v[j]);
+            for (int j = 0; j < 32; ++j) __stcg(wsc + j * kBlockM, v[32 * h + j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) __stcg(wsc + j * kBlockM, __ldcg(wsc + j * kBlockM) + v[32 * h + j]);
+          }
+          continue;
         }
-        continue;
-      }
-      if (fixup) {  // final split: acc = partial sum of the earlier splits + own part
+        if (fixup) {  // final split: acc = partial sum of the earlier splits + own part
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __ldcg(wsc + j * kBlockM) + v[j];
-      }
-      const int32_t col0 = w.n * BN + c * 32;
-      float z[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float t;
+          for (int j = 0; j < 32; ++j) v[32 * h + j] = __ldcg(wsc + j * kBlockM) + v[32 * h + j];
+        }
+        const int32_t col0 = w.n * BN + c32 * 32;
+        float z[32];
         if (p.has_bias) {
-          const float b = (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.0f;
-          t = fmaf(alpha, v[j], b);
+          float b[32];
+          if (bias_vec && col0 + 32 <= p.N) {
+            // 8 vector loads in flight; every lane reads the same 128 bytes (one broadcast)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 t = __ldg(reinterpret_cast<const float4*>(p.bias + col0) + q);
+              b[4 * q] = t.x; b[4 * q + 1] = t.y; b[4 * q + 2] = t.z; b[4 * q + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) b[j] = (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.0f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z[j] = fmaf(alpha, v[32 * h + j], b[j]);
         } else {
-          t = alpha * v[j];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z[j] = alpha * v[32 * h + j];
         }
-        z[j] = p.relu ? fmaxf(t, 0.0f) : t;
+        if (p.relu) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z[j] = fmaxf(z[j], 0.0f);
+        }
+        store_chunk<OUT>(p, row, col0, z);
       }
-      store_chunk<OUT>(p, row, col0, z);
     }
     ptx::tc_fence_before();
     if (fixup && !final_split) __threadfence();  // partials visible GPU-wide before the lock moves
     ptx::named_bar_sync(1, 128);
+    if (p.stats && ep == 0) { busy += clock64() - t1; ++items; }
     if (ep == 0) {
-      ptx::mbar_arrive(bar_tempty + 8 * acc);
+      if (CG == 2) ptx::mbar_arrive_cluster(tempty_target + 8 * acc);
+      else ptx::mbar_arrive(bar_tempty + 8 * acc);
       if (fixup && !final_split && !(p.debug_flags & DBG_SKIP_LOCK))
         ptx::st_release_gpu(p.locks + slot, w.k_begin + w.k_count);
     }
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
   }
+  if (p.stats && ep == 0) {
+    p.stats[blockIdx.x * kStatSlots + STAT_EPI_WAIT_TFULL] = wait_tfull;
+    p.stats[blockIdx.x * kStatSlots + STAT_EPI_BUSY] = busy;
+    p.stats[blockIdx.x * kStatSlots + STAT_ITEMS] = items;
+  }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, int DT, int OUT>
+template <int BN, int DT, int OUT, int CG>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_constant__ KernelParams p) {
-  using Cfg = TileCfg<BN>;
+  using Cfg = TileCfg<BN, CG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t smem_a = ptx::smem_addr(smem);
@@ -328,6 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + Cfg::MISC_OFFSET);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const long long t_start = clock64();
+
+  Ctx c;
+  c.abort = &ctl->abort;
+  c.rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
+  c.peer_abort = CG == 2 ? ptx::mapa(ptx::smem_addr(&ctl->abort), c.rank ^ 1u) : 0u;
+  c.unit = static_cast<int32_t>(blockIdx.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -336,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
     }
     for (int b = 0; b < Cfg::NACC; ++b) {
       ptx::mbar_init(bar_tfull + 8 * b, 1);
-      ptx::mbar_init(bar_tempty + 8 * b, 1);
+      ptx::mbar_init(bar_tempty + 8 * b, CG);   // one arrival per CTA's epilogue
     }
     ptx::mbar_init(bar_drain, 1);
     ctl->abort = 0;
@@ -346,37 +442,47 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
     ptx::prefetch_tmap(&p.tmap_b);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), 512);
-    ptx::tmem_relinquish();
+    if (CG == 2) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(&ctl->tmem_base), 512);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), 512);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CG == 2) ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<BN, DT>(p, smem_a, smem_b, bar_full, bar_empty, &ctl->abort);
+    if (lane == 0) run_producer<BN, DT, CG>(p, c, smem_a, smem_b, bar_full, bar_empty);
   } else if (warp == 1) {
-    if (lane == 0)
-      run_mma<BN, DT>(p, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty, bar_drain,
-                      &ctl->abort);
+    if (lane == 0 && c.rank == 0)
+      run_mma<BN, DT, CG>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty, bar_drain);
   } else {
-    run_epilogue<BN, OUT>(p, tmem_base, bar_tfull, bar_tempty, ctl);
+    run_epilogue<BN, OUT, CG>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (p.stats && threadIdx.x == 0) p.stats[blockIdx.x * kStatSlots + STAT_TOTAL] = clock64() - t_start;
+  // pairs: neither CTA leaves (nor frees TMEM) while the other may still signal
+  // its barriers or the leader's MMAs may still write its TMEM
+  if (CG == 2) ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, 512);
+    if (CG == 2) ptx::tmem_dealloc_pair(tmem_base, 512);
+    else ptx::tmem_dealloc(tmem_base, 512);
   }
 }
 
-template <int BN, int DT>
+template <int BN, int DT, int CG>
 const void* select_kernel(int out_type) {
-  if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16>);
-  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32>);
+  if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16, CG>);
+  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32, CG>);
 }
 
 }  // namespace tst

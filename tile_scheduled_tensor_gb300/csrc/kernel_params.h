@@ -18,7 +18,20 @@ enum OutType : int32_t { OUT_F32 = 0, OUT_BF16 = 1 };
 enum StatusCode : uint32_t { ST_OK = 0, ST_TIMEOUT = 6, ST_DEVICE_CHECK = 7 };
 enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_LOCK = 4 };
 
-enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4 };
+enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8 };
+
+// Role-cycle counters (debug): kStatSlots uint64 per CTA, in SM clock cycles.
+enum StatSlot : int32_t {
+  STAT_TOTAL = 0,            // kernel start to end (thread 0)
+  STAT_PROD_WAIT_EMPTY = 1,  // producer waiting for a free stage
+  STAT_MMA_WAIT_FULL = 2,    // MMA issuer waiting for loaded operands
+  STAT_MMA_WAIT_TEMPTY = 3,  // MMA issuer waiting for a free accumulator
+  STAT_EPI_WAIT_TFULL = 4,   // epilogue waiting for an accumulator (and Stream-K locks)
+  STAT_EPI_BUSY = 5,         // epilogue processing (TMEM loads, math, stores)
+  STAT_KBLOCKS = 6,          // k-tiles issued by the MMA issuer
+  STAT_ITEMS = 7             // work items processed by the epilogue
+};
+constexpr int kStatSlots = 8;
 
 struct KernelParams {
   CUtensorMap tmap_a;       // A: M x K, K contiguous, box BK x 128, 128-byte swizzle
@@ -30,22 +43,25 @@ struct KernelParams {
   int32_t* locks;           // one lock per split tile: k-tiles accumulated so far
   uint32_t* status;         // device status word
   int32_t* trace;           // debug trace or null
+  unsigned long long* stats;  // debug role-cycle counters (kStatSlots per CTA) or null
   int32_t M, N, K;
   float alpha;
   Sched sched;
   int32_t has_bias, relu, use_scales;
   int32_t debug_flags;
   int32_t max_items;        // trace records per CTA
-  int32_t pad_;
+  int32_t stages;           // shared-memory ring depth in use (2 .. TileCfg::STAGES)
   uint64_t timeout_ns;      // limit of every device-side wait
 };
 
-// Tile configuration for a tile width BN.  Operand rows are always 128 bytes
+// Tile configuration for a scheduled tile width BN and a CTA group of CG CTAs
+// (1, or 2 for a CTA pair that shares one M = 256 MMA).  Each CTA holds 128
+// rows of A and BN / CG rows of B per stage.  Operand rows are always 128 bytes
 // (BK = 64 BF16 or 128 e4m3 elements), matching the 128-byte swizzle span.
-template <int BN>
+template <int BN, int CG = 1>
 struct TileCfg {
   static constexpr int A_BYTES = kBlockM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_BYTES = (BN / CG) * 128;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RAW_STAGES = (kSmemLimit - 2048) / STAGE_BYTES;
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
@@ -58,8 +74,23 @@ struct TileCfg {
 
 }  // namespace tst
 
-// Kernel lookup, one per input type (defined in gemm_bf16.cu / gemm_e4m3.cu).
-const void* tst_kernel_bf16(int bn, int out_type);
-const void* tst_kernel_e4m3(int bn, int out_type);
-int tst_kernel_smem_bytes(int bn);
-int tst_kernel_stages(int bn);
+// Kernel lookup (defined in the gemm_<dtype>_cg<n>.cu instantiation units).
+const void* tst_kernel_bf16_cg1(int bn, int out_type);
+const void* tst_kernel_bf16_cg2(int bn, int out_type);
+const void* tst_kernel_e4m3_cg1(int bn, int out_type);
+const void* tst_kernel_e4m3_cg2(int bn, int out_type);
+
+inline const void* tst_kernel(int dtype, int bn, int out_type, int cg) {
+  if (dtype == tst::DT_BF16) return cg == 2 ? tst_kernel_bf16_cg2(bn, out_type) : tst_kernel_bf16_cg1(bn, out_type);
+  return cg == 2 ? tst_kernel_e4m3_cg2(bn, out_type) : tst_kernel_e4m3_cg1(bn, out_type);
+}
+
+inline int tst_kernel_smem_bytes(int bn, int cg) {
+  if (cg == 2) return bn == 256 ? tst::TileCfg<256, 2>::SMEM_BYTES : tst::TileCfg<128, 2>::SMEM_BYTES;
+  return bn == 256 ? tst::TileCfg<256, 1>::SMEM_BYTES : tst::TileCfg<128, 1>::SMEM_BYTES;
+}
+
+inline int tst_kernel_stages(int bn, int cg) {
+  if (cg == 2) return bn == 256 ? tst::TileCfg<256, 2>::STAGES : tst::TileCfg<128, 2>::STAGES;
+  return bn == 256 ? tst::TileCfg<256, 1>::STAGES : tst::TileCfg<128, 1>::STAGES;
+}

@@ -156,7 +156,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   s.kt = static_cast<int32_t>(kt);
   s.map_kind = mapping.kind;
   s.group = grouped ? mapping.group : 1;
-  s.backward = 0;
+  s.backward = 1;  // backward tile iteration, as gemm_plan_create does by default
   if (schedule == TST_STREAMK) {
     s.grid = static_cast<int32_t>(P);
     s.dp_tiles = 0;
@@ -179,9 +179,9 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   float* ws = reinterpret_cast<float*>(base + kStatusBytes + lock_bytes);
 
   // ---- kernel and its shared-memory limit on this device
-  const void* kernel = dtype == TST_BF16 ? tst_kernel_bf16(bn, epi->out_dtype) : tst_kernel_e4m3(bn, epi->out_dtype);
+  const void* kernel = tst_kernel(dtype, bn, epi->out_dtype, 1);
   if (kernel == nullptr) return TST_ERR_UNSUPPORTED;
-  const int smem = tst_kernel_smem_bytes(bn);
+  const int smem = tst_kernel_smem_bytes(bn, 1);
   const uint32_t kbit = 1u << ((dtype == TST_BF16 ? 0 : 4) + (bn == 256 ? 2 : 0) + epi->out_dtype);
   if (!(dev->smem_set & kbit)) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
@@ -202,6 +202,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   kp.locks = locks;
   kp.status = status;
   kp.trace = nullptr;
+  kp.stats = nullptr;
   kp.M = static_cast<int32_t>(M);
   kp.N = static_cast<int32_t>(N);
   kp.K = static_cast<int32_t>(K);
@@ -212,6 +213,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   kp.use_scales = epi->use_scales ? 1 : 0;
   kp.debug_flags = 0;
   kp.max_items = 0;
+  kp.stages = tst_kernel_stages(bn, 1);
   kp.timeout_ns = 10ull * 1000 * 1000 * 1000;
 
   // ---- clear what must start at zero: the status word and the locks
