@@ -252,6 +252,50 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_role_cycles(args):
+    """Per-CTA cycle counters from the kernel's debug mode: where each role waits."""
+    import torch
+    import tile_scheduled_tensor_gb300 as tst
+    names = [args.workload] + ([] if args.no_extra else [n for n in EXTRA if n != args.workload])
+    for name in names:
+        w = WORKLOADS[name]
+        inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
+                               bias_dist=w.get("bias_dist"))
+        plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
+                                    schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
+                                    has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
+                                    use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
+                                    cta_group=w.get("cta_group", 0))
+        info = plan.info
+        a = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
+        b = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
+        A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+        bias = torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None
+        scales = torch.from_numpy(inp.scales).cuda() if inp.scales is not None else None
+        C = torch.empty(w["M"], w["N"], dtype=torch.bfloat16 if w["out"] == "bf16" else torch.float32,
+                        device="cuda")
+        stats = torch.zeros(info.ctas * 8, dtype=torch.int64, device="cuda")
+        for _ in range(args.warmup):
+            tst.gemm_run(plan, A, B, C, bias=bias, scales=scales)
+        tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_ROLE_CYCLES, stats, info.ctas * 16)
+        tst.gemm_run(plan, A, B, C, bias=bias, scales=scales)
+        st, word = tst.gemm_status_query(plan)
+        if st != tst.TST_OK:
+            raise RuntimeError(f"{name}: device status {tst.gemm_status_string(st)} {word:#x}")
+        s = stats.view(info.ctas, 8).cpu().numpy().astype(np.float64)
+        lead = s[0::info.cta_group]
+        tot = s[:, 0]
+        row = {"workload": name, "tile": f"{info.bm}x{info.bn}x{info.bk}", "cta_group": int(info.cta_group),
+               "stages": int(info.stages), "cycles_per_cta": round(float(tot.mean())),
+               "cycles_per_ktile": round(float((lead[:, 0] / np.maximum(lead[:, 6], 1)).mean()), 1),
+               "producer_wait_empty": round(float((s[:, 1] / tot).mean()), 3),
+               "mma_wait_full": round(float((lead[:, 2] / lead[:, 0]).mean()), 3),
+               "mma_wait_tmem_empty": round(float((lead[:, 3] / lead[:, 0]).mean()), 3),
+               "epilogue_wait": round(float((s[:, 4] / tot).mean()), 3),
+               "epilogue_busy": round(float((s[:, 5] / tot).mean()), 3)}
+        print(json.dumps(row), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -261,11 +305,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--role-cycles", action="store_true",
+                    help="instead of timing, print per-role wait/busy cycle fractions (debug counters) "
+                         "for the listed workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.role_cycles:
+        return run_role_cycles(args)
 
     import torch
     import torch.distributed as dist

@@ -130,7 +130,9 @@ typedef struct {
     int64_t timeout_ns;    /* limit of every device-side wait: 0 = 10 s */
     int32_t stages;        /* shared-memory ring depth: 0 = as deep as shared memory allows,
                               else 2 .. that maximum (TST_ERR_UNSUPPORTED beyond it) */
-    int32_t reserved1;
+    int32_t bk;            /* k-tile in elements: 0 = two atoms (BF16 128, e4m3 256); BF16 64 or
+                              128, e4m3 128 or 256 (one or two 128-byte swizzle atoms per operand
+                              row and stage) */
 } tst_plan_options;
 
 /* What the plan decided (for logging and tests). */

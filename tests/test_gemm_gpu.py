@@ -77,6 +77,23 @@ def test_small_integers_exact_every_dtype_mapping_schedule(dtype, bn, mapping, s
     assert np.array_equal(host_values(C), z)
 
 
+@pytest.mark.parametrize("atoms", [1, 2])
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("schedule", ["static", "persistent", "streamk"])
+def test_k_tile_widths_small_integers_exact(dtype, schedule, cta_group, atoms):
+    """k-tiles of one or two 128-byte swizzle atoms (BK = 64/128 BF16, 128/256 e4m3), including a
+    ragged K whose last atom lies entirely beyond K (zero fill)."""
+    bk = (64 if dtype == "bf16" else 128) * atoms
+    for (M, N, K) in [(640, 768, 640), (300, 260, bk + bk // 2 + 16), (256, 256, bk // 2 - 16)]:
+        inp, w, plan, C = _gemm(M, N, K, dtype=dtype, dist="int:8", case=19, mapping=("grouped_m", 8),
+                                schedule=schedule, bn=128 if cta_group == 1 else 256, use_scales=False,
+                                num_ctas=23 if cta_group == 1 else 9, cta_group=cta_group, bk=bk)
+        assert plan.info.bk == bk
+        z, _ = oracle_rows(inp, w)
+        assert np.array_equal(host_values(C), z), (M, N, K)
+
+
 def test_small_integers_bf16_output_exact():
     # |C| <= 4 * 4 * 16 = 256 is exact in BF16
     inp, w, plan, C = _gemm(384, 256, 16 * 8, dist="int:2", out="bf16", mapping=("grouped_m", 8),

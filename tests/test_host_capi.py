@@ -57,6 +57,9 @@ def _host_plan(M, N, K, **kw):
     (dict(M=16, N=16, K=12), tst.TST_ERR_ALIGNMENT),           # 12 BF16 = 24 bytes per row
     (dict(M=16, N=16, K=8, dtype="e4m3"), tst.TST_ERR_ALIGNMENT),  # 8 bytes per row
     (dict(M=16, N=16, K=16, bn=64), tst.TST_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=16, bk=96), tst.TST_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=16, dtype="e4m3", bk=64), tst.TST_ERR_UNSUPPORTED),
+    (dict(M=16, N=16, K=16, stages=9), tst.TST_ERR_UNSUPPORTED),
     (dict(M=16, N=16, K=16, mapping=("grouped_m", 0)), tst.TST_ERR_INVALID_ARG),
     (dict(M=16, N=16, K=16, num_sms=0), tst.TST_ERR_INVALID_ARG),  # host-only needs an SM count
     (dict(M=1 << 31, N=16, K=16), tst.TST_ERR_INVALID_ARG),
@@ -101,13 +104,18 @@ def test_host_only_plan_cannot_run_and_checks_ranges():
 def test_tile_grid_and_config():
     p = _host_plan(1920, 1920, 16384, bn=128, schedule="streamk")
     i = p.info
-    assert (i.mt, i.nt, i.kt, i.tiles, i.bk) == (15, 15, 256, 225, 64)
+    assert (i.mt, i.nt, i.kt, i.tiles, i.bk) == (15, 15, 128, 225, 128)
     assert i.grid == 152 and i.sk_tiles == 225 and i.dp_tiles == 0
     p8 = _host_plan(8192, 8192, 8192, dtype="e4m3", bn=256)
-    assert (p8.info.bk, p8.info.mt, p8.info.nt, p8.info.kt) == (128, 64, 32, 64)
+    assert (p8.info.bk, p8.info.mt, p8.info.nt, p8.info.kt) == (256, 64, 32, 32)
     # ragged shapes round up
-    pr = _host_plan(129, 257, 72, bn=128)
+    pr = _host_plan(129, 257, 72, bn=128, bk=64)
     assert (pr.info.mt, pr.info.nt, pr.info.kt) == (2, 3, 2)
+    # two-atom k-tiles (the default) halve Kt; the ring depth follows the larger stage
+    wide = _host_plan(4096, 4096, 4096, bn=128)
+    narrow = _host_plan(4096, 4096, 4096, bn=128, bk=64)
+    assert (wide.info.bk, wide.info.kt, narrow.info.bk, narrow.info.kt) == (128, 32, 64, 64)
+    assert wide.info.stages < narrow.info.stages
 
 
 @pytest.mark.parametrize("kind", list(MAPS))
@@ -173,8 +181,8 @@ def test_pair_plans_schedule_256_row_tiles_over_pairs():
         for t, m, n, *_ in got:
             assert (m, n) == S.tile_map(S.GROUPED_M, 8, 16, 32, t)
     sk = _host_plan(1920, 1920, 16384, schedule="streamk", bn=128, cta_group=2)
-    assert (sk.info.mt, sk.info.nt, sk.info.grid, sk.info.sk_tiles) == (8, 15, 76, 120)
-    want = [(s.tile, s.k_idx, s.k_count) for s in S.work_items(S.STREAMK, 3, 76, 120, 256, backward=True)]
+    assert (sk.info.mt, sk.info.nt, sk.info.grid, sk.info.sk_tiles, sk.info.kt) == (8, 15, 76, 120, 128)
+    want = [(s.tile, s.k_idx, s.k_count) for s in S.work_items(S.STREAMK, 3, 76, 120, 128, backward=True)]
     assert [(t, kb, kc) for t, _, _, kb, kc, _ in tst.gemm_work_items(sk, 3)] == want
     # one lock and one 128 x bn partial tile per CTA-half of each split tile
     assert sk.info.workspace_bytes >= 120 * 2 * 128 * 128 * 4

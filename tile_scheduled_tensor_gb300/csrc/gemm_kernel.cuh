@@ -110,11 +110,12 @@ __device__ __forceinline__ bool wait_lock(const KernelParams& p, const Ctx& c, c
 }
 
 // ------------------------------------------------------------------ producer
-template <int BN, int DT, int CG>
+template <int BN, int DT, int CG, int KA>
 __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c, uint32_t smem_a, uint32_t smem_b,
                                              uint32_t bar_full, uint32_t bar_empty) {
-  using Cfg = TileCfg<BN, CG>;
-  constexpr int BK = DT == DT_BF16 ? 64 : 128;
+  using Cfg = TileCfg<BN, CG, KA>;
+  constexpr int BK_ATOM = DT == DT_BF16 ? 64 : 128;   // K elements per 128-byte swizzle atom
+  constexpr int BK = BK_ATOM * KA;
   constexpr int BM_UNIT = kBlockM * CG;   // rows of the scheduled tile
   constexpr int BN_CTA = BN / CG;         // B rows this CTA loads
   // pairs: both CTAs' loads complete on the leader's FULL barriers
@@ -144,12 +145,18 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
       if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * Cfg::STAGE_BYTES);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
-        if (CG == 2) {
-          ptx::tma_load_2d_pair(smem_a + stage * Cfg::A_BYTES, &p.tmap_a, full_target + 8 * stage, kb * BK, m0);
-          ptx::tma_load_2d_pair(smem_b + stage * Cfg::B_BYTES, &p.tmap_b, full_target + 8 * stage, kb * BK, n0);
-        } else {
-          ptx::tma_load_2d(smem_a + stage * Cfg::A_BYTES, &p.tmap_a, bar_full + 8 * stage, kb * BK, m0);
-          ptx::tma_load_2d(smem_b + stage * Cfg::B_BYTES, &p.tmap_b, bar_full + 8 * stage, kb * BK, n0);
+#pragma unroll
+        for (int a = 0; a < KA; ++a) {  // one box per swizzle-atom column of K
+          const uint32_t sa = smem_a + stage * Cfg::A_BYTES + a * Cfg::A_SUB;
+          const uint32_t sb = smem_b + stage * Cfg::B_BYTES + a * Cfg::B_SUB;
+          const int32_t kx = kb * BK + a * BK_ATOM;
+          if (CG == 2) {
+            ptx::tma_load_2d_pair(sa, &p.tmap_a, full_target + 8 * stage, kx, m0);
+            ptx::tma_load_2d_pair(sb, &p.tmap_b, full_target + 8 * stage, kx, n0);
+          } else {
+            ptx::tma_load_2d(sa, &p.tmap_a, bar_full + 8 * stage, kx, m0);
+            ptx::tma_load_2d(sb, &p.tmap_b, bar_full + 8 * stage, kx, n0);
+          }
         }
       }
       issued |= 1u << stage;
@@ -175,11 +182,11 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
 }
 
 // ------------------------------------------------------------------ MMA issuer (leader only)
-template <int BN, int DT, int CG>
+template <int BN, int DT, int CG, int KA>
 __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uint32_t tmem_base, uint32_t smem_a,
                                         uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
                                         uint32_t bar_tempty, uint32_t bar_drain) {
-  using Cfg = TileCfg<BN, CG>;
+  using Cfg = TileCfg<BN, CG, KA>;
   constexpr uint32_t kIdesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN);
   int stage = 0;
   uint32_t phase = 0;
@@ -209,16 +216,20 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
       const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
       const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 4 * KA; ++k) {
         // each step consumes 32 bytes of K (16 BF16 or 32 e4m3): advance start address by 32 B
-        const uint64_t off = static_cast<uint64_t>(k * 2);
+        // inside an atom column, and by one sub-tile per atom column
+        const uint64_t off = static_cast<uint64_t>((k & 3) * 2) +
+                             static_cast<uint64_t>(k >> 2) * static_cast<uint64_t>(Cfg::A_SUB >> 4);
+        const uint64_t off_b = static_cast<uint64_t>((k & 3) * 2) +
+                               static_cast<uint64_t>(k >> 2) * static_cast<uint64_t>(Cfg::B_SUB >> 4);
         const uint32_t accumulate = (i | k) != 0;
         if (CG == 2) {
-          if (DT == DT_BF16) ptx::mma_f16_pair(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
-          else ptx::mma_f8_pair(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
+          if (DT == DT_BF16) ptx::mma_f16_pair(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
+          else ptx::mma_f8_pair(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
         } else {
-          if (DT == DT_BF16) ptx::mma_f16(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
-          else ptx::mma_f8(d_tmem, a_desc + off, b_desc + off, kIdesc, accumulate);
+          if (DT == DT_BF16) ptx::mma_f16(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
+          else ptx::mma_f8(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
         }
       }
       // stage free (in both CTAs of a pair) once these MMAs have read it
@@ -287,10 +298,10 @@ __device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, 
   }
 }
 
-template <int BN, int OUT, int CG>
+template <int BN, int OUT, int CG, int KA>
 __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
                                              uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
-  using Cfg = TileCfg<BN, CG>;
+  using Cfg = TileCfg<BN, CG, KA>;
   volatile uint32_t* ep_ok = &ctl->ep_ok;
   const int ep = threadIdx.x - 64;             // 0..127
   const int quad = (threadIdx.x >> 5) & 3;     // TMEM lane quadrant this warp may access
@@ -402,9 +413,9 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, int DT, int OUT, int CG>
+template <int BN, int DT, int OUT, int CG, int KA>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_constant__ KernelParams p) {
-  using Cfg = TileCfg<BN, CG>;
+  using Cfg = TileCfg<BN, CG, KA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t smem_a = ptx::smem_addr(smem);
@@ -457,12 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<BN, DT, CG>(p, c, smem_a, smem_b, bar_full, bar_empty);
+    if (lane == 0) run_producer<BN, DT, CG, KA>(p, c, smem_a, smem_b, bar_full, bar_empty);
   } else if (warp == 1) {
     if (lane == 0 && c.rank == 0)
-      run_mma<BN, DT, CG>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty, bar_drain);
+      run_mma<BN, DT, CG, KA>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty, bar_drain);
   } else {
-    run_epilogue<BN, OUT, CG>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
+    run_epilogue<BN, OUT, CG, KA>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   }
 
   ptx::tc_fence_before();
@@ -479,10 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
   }
 }
 
-template <int BN, int DT, int CG>
+template <int BN, int DT, int CG, int KA>
 const void* select_kernel(int out_type) {
-  if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16, CG>);
-  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32, CG>);
+  if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16, CG, KA>);
+  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32, CG, KA>);
 }
 
 }  // namespace tst

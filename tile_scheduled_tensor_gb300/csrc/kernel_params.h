@@ -54,14 +54,18 @@ struct KernelParams {
   uint64_t timeout_ns;      // limit of every device-side wait
 };
 
-// Tile configuration for a scheduled tile width BN and a CTA group of CG CTAs
-// (1, or 2 for a CTA pair that shares one M = 256 MMA).  Each CTA holds 128
-// rows of A and BN / CG rows of B per stage.  Operand rows are always 128 bytes
-// (BK = 64 BF16 or 128 e4m3 elements), matching the 128-byte swizzle span.
-template <int BN, int CG = 1>
+// Tile configuration for a scheduled tile width BN, a CTA group of CG CTAs
+// (1, or 2 for a CTA pair that shares one M = 256 MMA) and KA swizzle atoms of
+// K per stage.  Each CTA holds 128 rows of A and BN / CG rows of B per stage;
+// a row of one atom is 128 bytes (64 BF16 or 128 e4m3 elements, the 128-byte
+// swizzle span), so a stage covers BK = KA x 64 BF16 (KA x 128 e4m3) of K,
+// stored as KA consecutive atom-column sub-tiles per operand.
+template <int BN, int CG = 1, int KA = 1>
 struct TileCfg {
-  static constexpr int A_BYTES = kBlockM * 128;
-  static constexpr int B_BYTES = (BN / CG) * 128;
+  static constexpr int A_SUB = kBlockM * 128;            // one atom column of A
+  static constexpr int B_SUB = (BN / CG) * 128;          // one atom column of B
+  static constexpr int A_BYTES = A_SUB * KA;
+  static constexpr int B_BYTES = B_SUB * KA;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RAW_STAGES = (kSmemLimit - 2048) / STAGE_BYTES;
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
@@ -74,23 +78,37 @@ struct TileCfg {
 
 }  // namespace tst
 
-// Kernel lookup (defined in the gemm_<dtype>_cg<n>.cu instantiation units).
-const void* tst_kernel_bf16_cg1(int bn, int out_type);
-const void* tst_kernel_bf16_cg2(int bn, int out_type);
-const void* tst_kernel_e4m3_cg1(int bn, int out_type);
-const void* tst_kernel_e4m3_cg2(int bn, int out_type);
+// Kernel lookup (defined in the gemm_<dtype>_cg<n>_ka<k>.cu instantiation units).
+const void* tst_kernel_bf16_cg1_ka1(int bn, int out_type);
+const void* tst_kernel_bf16_cg2_ka1(int bn, int out_type);
+const void* tst_kernel_e4m3_cg1_ka1(int bn, int out_type);
+const void* tst_kernel_e4m3_cg2_ka1(int bn, int out_type);
+const void* tst_kernel_bf16_cg1_ka2(int bn, int out_type);
+const void* tst_kernel_bf16_cg2_ka2(int bn, int out_type);
+const void* tst_kernel_e4m3_cg1_ka2(int bn, int out_type);
+const void* tst_kernel_e4m3_cg2_ka2(int bn, int out_type);
 
-inline const void* tst_kernel(int dtype, int bn, int out_type, int cg) {
-  if (dtype == tst::DT_BF16) return cg == 2 ? tst_kernel_bf16_cg2(bn, out_type) : tst_kernel_bf16_cg1(bn, out_type);
-  return cg == 2 ? tst_kernel_e4m3_cg2(bn, out_type) : tst_kernel_e4m3_cg1(bn, out_type);
+inline const void* tst_kernel(int dtype, int bn, int out_type, int cg, int ka) {
+  if (ka == 2) {
+    if (dtype == tst::DT_BF16)
+      return cg == 2 ? tst_kernel_bf16_cg2_ka2(bn, out_type) : tst_kernel_bf16_cg1_ka2(bn, out_type);
+    return cg == 2 ? tst_kernel_e4m3_cg2_ka2(bn, out_type) : tst_kernel_e4m3_cg1_ka2(bn, out_type);
+  }
+  if (dtype == tst::DT_BF16)
+    return cg == 2 ? tst_kernel_bf16_cg2_ka1(bn, out_type) : tst_kernel_bf16_cg1_ka1(bn, out_type);
+  return cg == 2 ? tst_kernel_e4m3_cg2_ka1(bn, out_type) : tst_kernel_e4m3_cg1_ka1(bn, out_type);
 }
 
-inline int tst_kernel_smem_bytes(int bn, int cg) {
-  if (cg == 2) return bn == 256 ? tst::TileCfg<256, 2>::SMEM_BYTES : tst::TileCfg<128, 2>::SMEM_BYTES;
-  return bn == 256 ? tst::TileCfg<256, 1>::SMEM_BYTES : tst::TileCfg<128, 1>::SMEM_BYTES;
+template <int CG, int KA>
+inline int tst_cfg_value(int bn, bool smem) {
+  if (bn == 256) return smem ? tst::TileCfg<256, CG, KA>::SMEM_BYTES : tst::TileCfg<256, CG, KA>::STAGES;
+  return smem ? tst::TileCfg<128, CG, KA>::SMEM_BYTES : tst::TileCfg<128, CG, KA>::STAGES;
 }
 
-inline int tst_kernel_stages(int bn, int cg) {
-  if (cg == 2) return bn == 256 ? tst::TileCfg<256, 2>::STAGES : tst::TileCfg<128, 2>::STAGES;
-  return bn == 256 ? tst::TileCfg<256, 1>::STAGES : tst::TileCfg<128, 1>::STAGES;
+inline int tst_cfg(int bn, int cg, int ka, bool smem) {
+  if (cg == 2) return ka == 2 ? tst_cfg_value<2, 2>(bn, smem) : tst_cfg_value<2, 1>(bn, smem);
+  return ka == 2 ? tst_cfg_value<1, 2>(bn, smem) : tst_cfg_value<1, 1>(bn, smem);
 }
+
+inline int tst_kernel_smem_bytes(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, true); }
+inline int tst_kernel_stages(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, false); }

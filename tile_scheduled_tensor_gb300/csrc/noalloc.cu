@@ -179,9 +179,9 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   float* ws = reinterpret_cast<float*>(base + kStatusBytes + lock_bytes);
 
   // ---- kernel and its shared-memory limit on this device
-  const void* kernel = tst_kernel(dtype, bn, epi->out_dtype, 1);
+  const void* kernel = tst_kernel(dtype, bn, epi->out_dtype, 1, 1);
   if (kernel == nullptr) return TST_ERR_UNSUPPORTED;
-  const int smem = tst_kernel_smem_bytes(bn, 1);
+  const int smem = tst_kernel_smem_bytes(bn, 1, 1);
   const uint32_t kbit = 1u << ((dtype == TST_BF16 ? 0 : 4) + (bn == 256 ? 2 : 0) + epi->out_dtype);
   if (!(dev->smem_set & kbit)) {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
@@ -213,7 +213,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   kp.use_scales = epi->use_scales ? 1 : 0;
   kp.debug_flags = 0;
   kp.max_items = 0;
-  kp.stages = tst_kernel_stages(bn, 1);
+  kp.stages = tst_kernel_stages(bn, 1, 1);
   kp.timeout_ns = 10ull * 1000 * 1000 * 1000;
 
   // ---- clear what must start at zero: the status word and the locks
