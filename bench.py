@@ -55,6 +55,12 @@ def flops(w):
     return 2.0 * w["M"] * w["N"] * w["K"]
 
 
+def aggregate(flops_per_rank: float, local_ms: float, world: int, max_reduce):
+    """Whole-job throughput: every rank's flops over the slowest rank's time (TFLOPS)."""
+    ms = max_reduce(local_ms)
+    return world * flops_per_rank / (ms / 1e3) / 1e12, ms
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -429,9 +435,8 @@ def main():
     sampler = ClockSampler(local) if rank == 0 else None
     head = time_device(args.workload, args.steps, args.warmup, sampler)
     w = head["w"]
-    ms_mean = max_over_ranks(sum(head["ms"]) / len(head["ms"]))
     fl = flops(w)
-    value = world * fl / (ms_mean / 1e3) / 1e12
+    value, ms_mean = aggregate(fl, sum(head["ms"]) / len(head["ms"]), world, max_over_ranks)
     is_fp8 = w["dtype"] == "e4m3"
     peak_tf = peaks["bf16_tflops"] * (2.0 if is_fp8 else 1.0)
     achieved = fl / (ms_mean / 1e3) / 1e12

@@ -240,6 +240,29 @@ def test_config_full_size_sampled_rows_and_freivalds(name):
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])
+def test_row_shards_reassemble_bitwise(cta_group):
+    """Row shards (B replicated, shard edges on scheduled-tile boundaries) run one after the
+    other on this GPU and put side by side equal the unsharded result bit for bit."""
+    from tile_scheduled_tensor_gb300.shard import m_shard
+    M, N, K = 1600, 768, 1024
+    inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=21)
+    A, B, _, _ = to_device(inp)
+    w = dict(M=M, N=N, K=K, dtype="bf16", out="bf16", mapping=("grouped_m", 8), schedule="persistent", bn=256,
+             cta_group=cta_group)
+    full = run_gemm(plan_for(w), inp, "bf16", (A, B, None, None))
+    align = 128 * cta_group
+    parts = []
+    for r in range(3):
+        lo, hi = m_shard(M, 3, r, align)
+        if hi == lo:
+            continue
+        ws = dict(w, M=hi - lo)
+        shard_inp = synthetic.GemmInputs(hi - lo, N, K, "bf16", inp.A[lo:hi], inp.B, None, None)
+        parts.append(run_gemm(plan_for(ws), shard_inp, "bf16", (A[lo:hi], B, None, None)))
+    assert torch.equal(torch.cat(parts), full)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
 def test_timeout_on_missing_load_reports_and_recovers(cta_group):
     w = dict(M=512, N=512, K=512, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="persistent", bn=128,
              cta_group=cta_group)
