@@ -35,7 +35,7 @@ from synthetic.workloads import WORKLOADS  # noqa: E402
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
 HEADLINE = "c2_bf16_4096"
 EXTRA = ["c1_bf16_256", "c2_bf16_4096_1cta", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
-         "c5_bf16_epilogue"]
+         "c4_bf16_hybrid", "c5_bf16_epilogue"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
     "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
@@ -45,6 +45,7 @@ DESCR = {
     "c3_e4m3_8192": "FP8-e4m3 GEMM 8192^3, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, persistent",
     "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, Stream-K with fixup",
     "c4_bf16_persistent": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, grouped-M G=8 persistent",
+    "c4_bf16_hybrid": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, data-parallel waves + Stream-K tail",
     "c5_bf16_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=bf16(ReLU(0.5 acc + bias)), grouped-M G=8",
 }
 L2_FLUSH_BYTES = 512 << 20
@@ -258,6 +259,85 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def band_model(plan, elt_bytes, K, l2_bytes=64 << 20):
+    """Operand bands per wave of concurrently running tiles under the plan's mapping.
+
+    A wave is `grid` consecutive linear tasks (the persistent assignment runs task
+    i on unit i mod grid).  The unique A row-bands and B column-bands of a wave are
+    its logical working set (the DeepGEMM page's working-set panel).  DRAM traffic
+    is modelled by passing the waves' bands through an LRU cache: a band that is
+    not resident when its wave starts is read from DRAM once.  The default
+    capacity, 64 MiB, is one die's half of GB300's L2; with it the model matched
+    the ncu DRAM bytes of five mappings at 8192^3 within 6 %.
+    """
+    from collections import OrderedDict
+    import tile_scheduled_tensor_gb300 as tst
+    info = plan.info
+    T, P = int(info.tiles), int(info.grid)
+    band = {"A": info.bm * K * elt_bytes, "B": info.bn * K * elt_bytes}
+    lru, used, dram, per_wave = OrderedDict(), 0, 0, []
+    for w0 in range(0, T, P):
+        keys = set()
+        for i in range(w0, min(T, w0 + P)):
+            m, n = tst.gemm_tile_map(plan, i)
+            keys.add(("A", m))
+            keys.add(("B", n))
+        per_wave.append(sum(band[k[0]] for k in keys))
+        for k in sorted(keys):
+            if k in lru:
+                lru.move_to_end(k)
+                continue
+            dram += band[k[0]]
+            lru[k] = band[k[0]]
+            used += band[k[0]]
+            while used > l2_bytes and len(lru) > 1:
+                _, sz = lru.popitem(last=False)
+                used -= sz
+    return {"wave_working_set_mb": round(sum(per_wave) / len(per_wave) / 2**20, 1),
+            "model_dram_operand_mb": round(dram / 2**20, 1)}
+
+
+def run_mapping_study(args):
+    import torch
+    import tile_scheduled_tensor_gb300 as tst
+    base = WORKLOADS[args.workload]
+    inp = make_gemm_inputs(base["M"], base["N"], base["K"], base["dtype"], base["dist"], case=base["case"],
+                           bias_dist=base.get("bias_dist"))
+    a = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
+    b = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
+    A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    bias = torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None
+    scales = torch.from_numpy(inp.scales).cuda() if inp.scales is not None else None
+    C = torch.empty(base["M"], base["N"], dtype=torch.bfloat16 if base["out"] == "bf16" else torch.float32,
+                    device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    elt = 2 if base["dtype"] == "bf16" else 1
+    for mapping in [("linear_nfast", 1), ("linear_mfast", 1), ("grouped_m", 4), ("grouped_m", 8), ("grouped_m", 16),
+                    ("grouped_n", 8), ("grouped_n", 16)]:
+        plan = tst.gemm_plan_create(base["M"], base["N"], base["K"], dtype=base["dtype"], mapping=mapping,
+                                    schedule=base["schedule"], out_dtype=base["out"], alpha=base.get("alpha", 1.0),
+                                    has_bias=base.get("bias_dist") is not None, relu=base.get("relu", False),
+                                    use_scales=base.get("use_scales", False), bn=base.get("bn", 0),
+                                    cta_group=base.get("cta_group", 0))
+        for _ in range(args.warmup):
+            tst.gemm_run(plan, A, B, C, bias=bias, scales=scales)
+        times = []
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            tst.gemm_run(plan, A, B, C, bias=bias, scales=scales)
+            e1.record()
+            times.append((e0, e1))
+        torch.cuda.synchronize()
+        st, _ = tst.gemm_status_query(plan)
+        ms = statistics.median(x.elapsed_time(y) for x, y in times)
+        row = {"workload": args.workload, "mapping": f"{mapping[0]}:{mapping[1]}", "status": int(st),
+               "ms": round(ms, 4), "tflops": round(flops(base) / (ms / 1e3) / 1e12, 1)}
+        row.update(band_model(plan, elt, base["K"]))
+        print(json.dumps(row), flush=True)
+
+
 def run_role_cycles(args):
     """Per-CTA cycle counters from the kernel's debug mode: where each role waits."""
     import torch
@@ -311,6 +391,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--mapping", default=None,
+                    help="override the workload's mapping, e.g. linear_nfast:1 or grouped_m:16")
+    ap.add_argument("--schedule", default=None, help="override the workload's schedule")
+    ap.add_argument("--mapping-study", action="store_true",
+                    help="time every mapping family on the workload and print the operand-band model")
     ap.add_argument("--role-cycles", action="store_true",
                     help="instead of timing, print per-role wait/busy cycle fractions (debug counters) "
                          "for the listed workloads")
@@ -319,8 +404,20 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.mapping or args.schedule:
+        w = dict(WORKLOADS[args.workload])
+        if args.mapping:
+            kind, _, g = args.mapping.partition(":")
+            w["mapping"] = (kind, int(g or 1))
+        if args.schedule:
+            w["schedule"] = args.schedule
+        WORKLOADS[args.workload] = w
+        DESCR[args.workload] = DESCR[args.workload] + f" [mapping {w['mapping'][0]} G={w['mapping'][1]}, " \
+                                                      f"schedule {w['schedule']}]"
     if args.role_cycles:
         return run_role_cycles(args)
+    if args.mapping_study:
+        return run_mapping_study(args)
 
     import torch
     import torch.distributed as dist

@@ -31,6 +31,9 @@ WORKLOADS = {
     # the same problem, grouped-M G=8 persistent (the data-parallel comparison)
     "c4_bf16_persistent": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                                mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),
+    # the same problem, hybrid: full data-parallel waves, Stream-K over the tail wave only
+    "c4_bf16_hybrid": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
+                           mapping=("grouped_m", 8), schedule="streamk_hybrid", bn=128, cta_group=1),
     # 16384 x 4096 x 4096 BF16 -> bf16(ReLU(0.5 acc + bias)), N(0,0.02), bias N(0,1)
     "c5_bf16_epilogue": dict(M=16384, N=4096, K=4096, dtype="bf16", dist="normal:0.02", case=5, out="bf16",
                              mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2,
