@@ -226,7 +226,7 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
     if (!p->host_only) {
       cudaLaunchConfig_t qc = {};
       qc.gridDim = dim3(static_cast<unsigned>(2 * resident), 1, 1);
-      qc.blockDim = dim3(tst::kThreads, 1, 1);
+      qc.blockDim = dim3(tst_kernel_threads(p->bn, p->ka), 1, 1);
       qc.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
       cudaLaunchAttribute ca[1];
       ca[0].id = cudaLaunchAttributeClusterDimension;
@@ -454,7 +454,7 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg), 1, 1);
-  cfg.blockDim = dim3(tst::kThreads, 1, 1);
+  cfg.blockDim = dim3(tst_kernel_threads(p->bn, p->ka), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

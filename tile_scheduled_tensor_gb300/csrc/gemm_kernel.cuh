@@ -182,10 +182,13 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
 }
 
 // ------------------------------------------------------------------ MMA issuer (leader only)
+// Issuer `issuer` of Cfg::ISSUERS: with two issuers, issuer r issues the MMAs of
+// swizzle atom r of every k-tile into its own accumulator (columns r * BN of the
+// buffer); the epilogue adds the two.
 template <int BN, int DT, int CG, int KA>
 __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uint32_t tmem_base, uint32_t smem_a,
                                         uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
-                                        uint32_t bar_tempty, uint32_t bar_drain) {
+                                        uint32_t bar_tempty, uint32_t bar_drain, int issuer) {
   using Cfg = TileCfg<BN, CG, KA>;
   constexpr uint32_t kIdesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN);
   int stage = 0;
@@ -205,7 +208,7 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
     if (!wait_phase<CG>(p, c, bar_tempty + 8 * acc, acc_phase ^ 1u, ROLE_MMA)) { ok = false; break; }
     if (p.stats) wait_tempty += clock64() - t0;
     ptx::tc_fence_after();
-    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS + issuer * BN);
     for (int32_t i = 0; i < w.k_count; ++i) {
       const long long t1 = p.stats ? clock64() : 0;
       // the stage was filled by TMA and announced on its mbarrier: the wait alone
@@ -217,13 +220,14 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
       const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
       for (int k = 0; k < 4 * KA; ++k) {
+        if (Cfg::DUAL && (k >> 2) != issuer) continue;  // the other issuer's atom
         // each step consumes 32 bytes of K (16 BF16 or 32 e4m3): advance start address by 32 B
         // inside an atom column, and by one sub-tile per atom column
         const uint64_t off = static_cast<uint64_t>((k & 3) * 2) +
                              static_cast<uint64_t>(k >> 2) * static_cast<uint64_t>(Cfg::A_SUB >> 4);
         const uint64_t off_b = static_cast<uint64_t>((k & 3) * 2) +
                                static_cast<uint64_t>(k >> 2) * static_cast<uint64_t>(Cfg::B_SUB >> 4);
-        const uint32_t accumulate = (i | k) != 0;
+        const uint32_t accumulate = Cfg::DUAL ? (i | (k & 3)) != 0 : (i | k) != 0;
         if (CG == 2) {
           if (DT == DT_BF16) ptx::mma_f16_pair(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
           else ptx::mma_f8_pair(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
@@ -243,7 +247,7 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
     else ptx::mma_commit(bar_tfull + 8 * acc);
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
   }
-  if (p.stats) {
+  if (p.stats && issuer == 0) {
     p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_FULL] = wait_full;
     p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_TEMPTY] = wait_tempty;
     p.stats[blockIdx.x * kStatSlots + STAT_KBLOCKS] = kblocks;
@@ -340,12 +344,25 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     ptx::tc_fence_after();
 
     const int32_t row = w.m * (kBlockM * CG) + static_cast<int32_t>(c.rank) * kBlockM + row_in_tile;
-    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN);
+    const uint32_t t_row =
+        tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
 #pragma unroll 1
     for (int ch = 0; ch < BN / 64; ++ch) {
       float v[64];
-      ptx::tmem_load_64cols(t_row + ch * 64, v);
+      if (Cfg::DUAL) {
+        // the two issuers' accumulators, columns [0, BN) and [BN, 2 BN): add them
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float pair[64];
+          const uint32_t col = static_cast<uint32_t>(ch * 64 + h * 32);
+          ptx::tmem_load_2x32(t_row + col, t_row + BN + col, pair);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[32 * h + j] = pair[j] + pair[32 + j];
+        }
+      } else {
+        ptx::tmem_load_64cols(t_row + ch * 64, v);
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c32 = ch * 2 + h;
@@ -414,7 +431,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 
 // ------------------------------------------------------------------ kernel
 template <int BN, int DT, int OUT, int CG, int KA>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_constant__ KernelParams p) {
+__global__ void __launch_bounds__(TileCfg<BN, CG, KA>::THREADS, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ KernelParams p) {
   using Cfg = TileCfg<BN, CG, KA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -439,13 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
       ptx::mbar_init(bar_full + 8 * s, 1);
-      ptx::mbar_init(bar_empty + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, Cfg::ISSUERS);   // one commit per MMA issuer
     }
     for (int b = 0; b < Cfg::NACC; ++b) {
-      ptx::mbar_init(bar_tfull + 8 * b, 1);
+      ptx::mbar_init(bar_tfull + 8 * b, Cfg::ISSUERS);
       ptx::mbar_init(bar_tempty + 8 * b, CG);   // one arrival per CTA's epilogue
     }
     ptx::mbar_init(bar_drain, 1);
+    ptx::mbar_init(bar_drain + 8, 1);
     ctl->abort = 0;
     ctl->ep_ok = 0;
     ptx::fence_mbar_init();
@@ -469,9 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tcgen05_kernel(const __grid_
 
   if (warp == 0) {
     if (lane == 0) run_producer<BN, DT, CG, KA>(p, c, smem_a, smem_b, bar_full, bar_empty);
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 6) {  // warp 6 exists only in dual-issue tiles
+    const int issuer = warp == 1 ? 0 : 1;
     if (lane == 0 && c.rank == 0)
-      run_mma<BN, DT, CG, KA>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty, bar_drain);
+      run_mma<BN, DT, CG, KA>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty,
+                              bar_drain + 8 * issuer, issuer);
   } else {
     run_epilogue<BN, OUT, CG, KA>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   }

@@ -9,6 +9,7 @@ namespace tst {
 
 constexpr int kBlockM = 128;        // tile height (one TMEM lane per row)
 constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kThreadsDual = 224;   // + warp 6: second MMA issuer (dual-issue tiles)
 constexpr int kSmemLimit = 232448;  // 227 KiB opt-in dynamic shared memory per CTA
 
 enum DType : int32_t { DT_BF16 = 0, DT_E4M3 = 1 };
@@ -66,12 +67,18 @@ struct TileCfg {
   static constexpr int B_SUB = (BN / CG) * 128;          // one atom column of B
   static constexpr int A_BYTES = A_SUB * KA;
   static constexpr int B_BYTES = B_SUB * KA;
+  // 128-wide tiles with two atoms: two threads issue the MMAs (atom r by issuer r,
+  // each into its own accumulator), since one thread issues a tcgen05.mma about as
+  // fast as a 128 x 128 x 16 MMA computes
+  static constexpr bool DUAL = (BN == 128 && KA == 2);
+  static constexpr int ISSUERS = DUAL ? 2 : 1;
+  static constexpr int THREADS = DUAL ? kThreadsDual : kThreads;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RAW_STAGES = (kSmemLimit - 2048) / STAGE_BYTES;
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
-  static constexpr int NACC = 512 / BN;                 // accumulator buffers in 512 TMEM columns
+  static constexpr int NACC = 512 / (BN * ISSUERS);    // accumulator buffers in 512 TMEM columns
   static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 2;
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = 1024 + MISC_OFFSET + 16;  // + slack to align the base to 1024
 };
@@ -111,4 +118,5 @@ inline int tst_cfg(int bn, int cg, int ka, bool smem) {
 }
 
 inline int tst_kernel_smem_bytes(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, true); }
+inline int tst_kernel_threads(int bn, int ka) { return (bn == 128 && ka == 2) ? tst::kThreadsDual : tst::kThreads; }
 inline int tst_kernel_stages(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, false); }

@@ -224,7 +224,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(s.grid), 1, 1);
-  cfg.blockDim = dim3(tst::kThreads, 1, 1);
+  cfg.blockDim = dim3(tst_kernel_threads(bn, 1), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

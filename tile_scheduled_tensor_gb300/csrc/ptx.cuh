@@ -138,9 +138,9 @@ __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, float (&v)[32])
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 64 consecutive FP32 columns of this thread's TMEM lane (two 32-column loads
-// in flight before one wait).
-__device__ __forceinline__ void tmem_load_64cols(uint32_t taddr, float (&v)[64]) {
+// Two 32-column FP32 loads of this thread's TMEM lane (columns taddr0.. and
+// taddr1..), both in flight before one wait: v[0..31] and v[32..63].
+__device__ __forceinline__ void tmem_load_2x32(uint32_t taddr0, uint32_t taddr1, float (&v)[64]) {
   uint32_t r[64];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -158,10 +158,15 @@ __device__ __forceinline__ void tmem_load_64cols(uint32_t taddr, float (&v)[64])
         "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
         "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
         "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr), "r"(taddr + 32u)
+      : "r"(taddr0), "r"(taddr1)
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 consecutive FP32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_load_64cols(uint32_t taddr, float (&v)[64]) {
+  tmem_load_2x32(taddr, taddr + 32u, v);
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
