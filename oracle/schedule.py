@@ -33,7 +33,12 @@ Readings where the pages leave a step open (each is listed in the design notes):
     the last T mod P tiles, unless the tail wave is more than half full, in
     which case it stays fully data-parallel;
   * backward iteration reverses the order of a unit's splits; k stays
-    ascending inside each split.
+    ascending inside each split;
+  * Stream-K groups ("H100 . Stream-K scheduling", section 7): the Stream-K
+    tiles are dealt to g groups by output_tile_id = id_in_group * g + group;
+    unit u belongs to group u mod g as its member u // g (the pages do not say
+    which units form a group), and each group splits its own tiles' iterations
+    over its own units with the same floor partition as the ungrouped case.
 """
 from __future__ import annotations
 
@@ -133,6 +138,19 @@ def streamk_splits(u: int, P: int, T_sk: int, Kt: int, tile_offset: int = 0):
     return out
 
 
+def streamk_group_splits(u: int, P: int, T_sk: int, Kt: int, groups: int, tile_offset: int = 0):
+    """Splits of unit u when the Stream-K units and tiles are divided into `groups` groups."""
+    g = groups
+    j, member = u % g, u // g
+    units_in_group = len(range(j, P, g))
+    tiles_in_group = len(range(j, T_sk, g))
+    out = []
+    for s in streamk_splits(member, units_in_group, tiles_in_group, Kt):
+        tile_in_group = s.tile
+        out.append(Split(tile_offset + tile_in_group * g + j, s.k_idx, s.k_count, Kt))  # output_tile_id
+    return out
+
+
 def hybrid_split_count(T: int, P: int) -> int:
     """Tiles given to Stream-K under the hybrid rule (0 = fully data-parallel)."""
     tail = T % P
@@ -141,7 +159,7 @@ def hybrid_split_count(T: int, P: int) -> int:
     return tail
 
 
-def work_items(schedule: int, u: int, P: int, T: int, Kt: int, backward: bool = False):
+def work_items(schedule: int, u: int, P: int, T: int, Kt: int, backward: bool = False, groups: int = 1):
     """Ordered work list of worker u: a list of Split (whole tiles have k_idx 0, k_count Kt).
 
     STATIC: worker u is CTA u of a grid of T CTAs and takes task u.
@@ -154,12 +172,12 @@ def work_items(schedule: int, u: int, P: int, T: int, Kt: int, backward: bool = 
     if schedule == PERSISTENT:
         return [Split(i, 0, Kt, Kt) for i in range(u, T, P)]
     if schedule == STREAMK:
-        sk = streamk_splits(u, P, T, Kt)
+        sk = streamk_group_splits(u, P, T, Kt, groups)
         return sk[::-1] if backward else sk
     if schedule == STREAMK_HYBRID:
         T_sk = hybrid_split_count(T, P)
         T_dp = T - T_sk
         dp = [Split(i, 0, Kt, Kt) for i in range(u, T_dp, P)]
-        sk = streamk_splits(u, P, T_sk, Kt, tile_offset=T_dp) if T_sk else []
+        sk = streamk_group_splits(u, P, T_sk, Kt, groups, tile_offset=T_dp) if T_sk else []
         return dp + (sk[::-1] if backward else sk)
     raise ValueError(schedule)

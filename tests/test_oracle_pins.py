@@ -322,3 +322,41 @@ def test_streamk_hybrid_rule():
         assert all(s.tile >= 152 for s in items[1:])
     total = sum(s.k_count for u in range(152) for s in S.work_items(S.STREAMK_HYBRID, u, 152, 225, 256))
     assert total == 225 * 256
+
+
+def test_streamk_groups_reduce_to_ungrouped_and_interleave():
+    # one group is the plain Stream-K partition
+    for u in range(11):
+        assert S.work_items(S.STREAMK, u, 11, 13, 17, groups=1) == S.streamk_splits(u, 11, 13, 17)
+    # every split of a group-j unit lands on an output tile id = id_in_group * g + j
+    for g in (2, 3, 4, 8):
+        P, T, Kt = 152, 225, 128
+        per_tile = {t: [] for t in range(T)}
+        for u in range(P):
+            for s in S.work_items(S.STREAMK, u, P, T, Kt, groups=g):
+                assert s.tile % g == u % g
+                per_tile[s.tile].append(s)
+        for t, lst in per_tile.items():
+            lst.sort(key=lambda s: s.k_idx)
+            assert sum(s.k_count for s in lst) == Kt and lst[0].k_idx == 0
+            assert all(a.k_idx + a.k_count == b.k_idx for a, b in zip(lst, lst[1:]))
+            assert sum(s.is_final for s in lst) == 1
+        # inside a group the units' iteration counts differ by at most one
+        for j in range(g):
+            lens = [sum(s.k_count for s in S.work_items(S.STREAMK, u, P, T, Kt, groups=g)) for u in range(j, P, g)]
+            assert max(lens) - min(lens) <= 1
+
+
+def test_streamk_groups_same_k_slice_of_neighbouring_tiles():
+    # the point of groups: unit members with the same index in different groups start on
+    # neighbouring output tiles at the same K offset (the same wave of the raster order)
+    g, P, T, Kt = 4, 152, 225, 128
+    first = {}
+    for u in range(P):
+        items = S.work_items(S.STREAMK, u, P, T, Kt, groups=g)
+        first[u] = (items[0].tile, items[0].k_idx) if items else None
+    for m in range(P // g):
+        starts = [first[m * g + j] for j in range(g)]
+        tiles = [t for t, _ in starts]
+        assert max(tiles) - min(tiles) < 2 * g
+        assert len({k for _, k in starts}) <= 2
