@@ -52,6 +52,13 @@ L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h"]
 
 
+PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward")
+
+
+def extra_plan_options(w):
+    return {k: w[k] for k in PLAN_OPTION_KEYS if k in w}
+
+
 def flops(w):
     return 2.0 * w["M"] * w["N"] * w["K"]
 
@@ -394,6 +401,8 @@ def main():
     ap.add_argument("--mapping", default=None,
                     help="override the workload's mapping, e.g. linear_nfast:1 or grouped_m:16")
     ap.add_argument("--schedule", default=None, help="override the workload's schedule")
+    ap.add_argument("--opt", action="append", default=[],
+                    help="override a plan option of the workload, e.g. --opt sk_groups=4 --opt bn=256")
     ap.add_argument("--mapping-study", action="store_true",
                     help="time every mapping family on the workload and print the operand-band model")
     ap.add_argument("--role-cycles", action="store_true",
@@ -404,8 +413,11 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
-    if args.mapping or args.schedule:
+    if args.mapping or args.schedule or args.opt:
         w = dict(WORKLOADS[args.workload])
+        for kv in args.opt:
+            k, _, v = kv.partition("=")
+            w[k] = int(v)
         if args.mapping:
             kind, _, g = args.mapping.partition(":")
             w["mapping"] = (kind, int(g or 1))
@@ -413,7 +425,8 @@ def main():
             w["schedule"] = args.schedule
         WORKLOADS[args.workload] = w
         DESCR[args.workload] = DESCR[args.workload] + f" [mapping {w['mapping'][0]} G={w['mapping'][1]}, " \
-                                                      f"schedule {w['schedule']}]"
+                                                      f"schedule {w['schedule']}" + \
+            "".join(f", {kv}" for kv in args.opt) + "]"
     if args.role_cycles:
         return run_role_cycles(args)
     if args.mapping_study:
@@ -444,7 +457,7 @@ def main():
                                     schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
                                     has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
                                     use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
-                                    cta_group=w.get("cta_group", 0))
+                                    cta_group=w.get("cta_group", 0), **extra_plan_options(w))
         a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
         b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
         host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory()}

@@ -133,6 +133,11 @@ typedef struct {
     int32_t bk;            /* k-tile in elements: 0 = two atoms (BF16 128, e4m3 256); BF16 64 or
                               128, e4m3 128 or 256 (one or two 128-byte swizzle atoms per operand
                               row and stage) */
+    int32_t sk_groups;     /* Stream-K groups, 0 or 1 = none, at most 8: the Stream-K tiles are
+                              dealt to groups by output_tile_id = id_in_group * groups + group,
+                              unit u works in group u % groups, and each group splits its own
+                              tiles over its own units ("H100 . Stream-K scheduling" section 7) */
+    int32_t reserved2;
 } tst_plan_options;
 
 /* What the plan decided (for logging and tests). */

@@ -187,6 +187,44 @@ def test_streamk_forward_backward_and_repeat_bitwise():
         assert_close(host_values(C)[rows], z, ad, "f32", name)
 
 
+@pytest.mark.parametrize("groups", [2, 4, 8])
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_streamk_groups_exact_and_traced(groups, cta_group):
+    """Stream-K groups: small integers exact, real inputs within the bound and run-to-run
+    identical, and the device trace equals the oracle's grouped enumeration."""
+    M, N, K = 1920, 1920, 4096
+    inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "int:8", case=22)
+    dev = to_device(inp)
+    w = dict(M=M, N=N, K=K, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="streamk", bn=128,
+             cta_group=cta_group)
+    ref = run_gemm(plan_for(w), inp, "f32", dev)
+    plan = plan_for(dict(w, sk_groups=groups))
+    info = plan.info
+    cap = info.grid * info.max_items_per_cta * 8
+    trace = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TRACE, trace, cap)
+    C = run_gemm(plan, inp, "f32", dev)
+    z, _ = oracle_rows(inp, w, sample_rows(M))
+    assert np.array_equal(host_values(C)[sample_rows(M)], z)
+    t = trace.view(info.grid, info.max_items_per_cta, 8).cpu().numpy()
+    for u in range(info.grid):
+        want = S.work_items(S.STREAMK, u, info.grid, info.tiles, info.kt, backward=True, groups=groups)
+        got = [tuple(r[2:]) for r in t[u] if r[0] != -1]
+        assert got == [(s.tile, *S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, s.tile), s.k_idx, s.k_count,
+                        int(s.is_final) | (2 if s.requires_fixup else 0)) for s in want]
+    # real-valued inputs: groups move the split points inside a tile (so FP32 rounding differs
+    # from the ungrouped run); the result stays within the bound and is deterministic
+    inp2 = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=23)
+    dev2 = to_device(inp2)
+    wg = dict(w, sk_groups=groups)
+    b1 = run_gemm(plan_for(wg), inp2, "f32", dev2)
+    b2 = run_gemm(plan_for(wg), inp2, "f32", dev2)
+    assert torch.equal(b1, b2)
+    rows = sample_rows(M)
+    z2, ad2 = oracle_rows(inp2, w, rows)
+    assert_close(host_values(b1)[rows], z2, ad2, "f32", f"groups={groups}")
+
+
 @pytest.mark.parametrize("cta_group", [1, 2])
 def test_device_trace_matches_oracle_enumeration(cta_group):
     for sched, kw in (("persistent", {}), ("streamk", {}), ("streamk", {"sk_forward": True}),

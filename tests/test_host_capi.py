@@ -196,3 +196,24 @@ def test_auto_choices():
     with pytest.raises(tst.TstError) as e:
         _host_plan(256, 256, 256, cta_group=3)
     assert e.value.status == tst.TST_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("groups", [2, 3, 4, 8])
+@pytest.mark.parametrize("sched", ["streamk", "streamk_hybrid"])
+def test_streamk_group_work_lists_match_oracle(groups, sched):
+    for (M, N, K, sms) in [(1920, 1920, 16384, 152), (640, 896, 320, 7), (4096, 4096, 4096, 152)]:
+        for backward in (False, True):
+            p = _host_plan(M, N, K, mapping=("grouped_m", 8), schedule=sched, bn=128, num_sms=sms,
+                           sk_forward=not backward, sk_groups=groups)
+            i = p.info
+            for u in range(i.grid):
+                got = [(t, kb, kc, f) for t, _, _, kb, kc, f in tst.gemm_work_items(p, u)]
+                want = [(s.tile, s.k_idx, s.k_count, int(s.is_final) | (2 if s.requires_fixup else 0))
+                        for s in S.work_items(SCHEDS[sched], u, sms, i.tiles, i.kt, backward, groups=groups)]
+                assert got == want, (M, N, K, u)
+
+
+def test_streamk_groups_limit():
+    with pytest.raises(tst.TstError) as e:
+        _host_plan(1920, 1920, 16384, schedule="streamk", sk_groups=9)
+    assert e.value.status == tst.TST_ERR_UNSUPPORTED

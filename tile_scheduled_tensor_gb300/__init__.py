@@ -81,13 +81,14 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      out_dtype="f32", alpha: float = 1.0, has_bias: bool = False, relu: bool = False,
                      use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_forward: bool = False,
                      host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
-                     stages: int = 0, bk: int = 0) -> Plan:
+                     stages: int = 0, bk: int = 0, sk_groups: int = 0) -> Plan:
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     epi = _capi.tst_epilogue(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), int(bool(has_bias)),
                              int(bool(relu)), int(bool(use_scales)))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
-                                  int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk))
+                                  int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
+                                  int(sk_groups), 0)
     h = ctypes.c_void_p()
     _check(lib.gemm_plan_create_ex(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
                                    TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),

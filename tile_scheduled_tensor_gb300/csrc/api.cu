@@ -251,6 +251,8 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   s.map_kind = mapping.kind;
   s.group = (mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N) ? mapping.group : 1;
   s.backward = o.sk_forward ? 0 : 1;
+  if (o.sk_groups < 0 || o.sk_groups > 8) { delete p; return TST_ERR_UNSUPPORTED; }  // at most 8 groups
+  s.sk_groups = o.sk_groups > 0 ? o.sk_groups : 1;
   const int64_t P = o.num_ctas > 0 ? o.num_ctas : resident;
   switch (schedule) {
     case TST_STATIC:

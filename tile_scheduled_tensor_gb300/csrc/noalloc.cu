@@ -157,6 +157,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   s.map_kind = mapping.kind;
   s.group = grouped ? mapping.group : 1;
   s.backward = 1;  // backward tile iteration, as gemm_plan_create does by default
+  s.sk_groups = 1;
   if (schedule == TST_STREAMK) {
     s.grid = static_cast<int32_t>(P);
     s.dp_tiles = 0;

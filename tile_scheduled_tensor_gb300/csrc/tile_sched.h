@@ -16,6 +16,10 @@
 //  * Split bookkeeping K_idx = tile_iter_start - output_tile_iter_start and
 //    is_final_split <=> K_idx + k_tile_count == k_tiles_per_output_tile:
 //    "H100 . Stream-K scheduling" (Lesson 8.1), sections 2-4.
+//  * Stream-K groups for L2 locality, output_tile_id = id_in_group * groups +
+//    group: same lesson, section 7.  Unit u is member u / groups of group
+//    u % groups (the lesson does not say which units form a group); each group
+//    splits its own tiles' iterations evenly over its own units.
 #pragma once
 #include <stdint.h>
 
@@ -40,7 +44,7 @@ struct Sched {
   int32_t dp_tiles;       // tasks [0, dp_tiles) are computed whole, grid-stride
   int32_t sk_tiles;       // tasks [dp_tiles, dp_tiles + sk_tiles) are split by Stream-K
   int32_t backward;       // Stream-K splits of a unit visited last-first
-  int32_t pad_;
+  int32_t sk_groups;      // Stream-K groups (1 = none)
 };
 
 struct WorkItem {
@@ -90,19 +94,24 @@ TST_HD void tile_coord(const Sched& s, int32_t i, int32_t& m, int32_t& n) {
 // grid-stride; then its Stream-K range of MAC iterations cut at tile edges.
 struct WorkIter {
   int32_t next_dp;   // next whole task (>= dp_tiles when exhausted)
-  int32_t pad_;
-  int64_t sk_lo;     // remaining Stream-K iterations [sk_lo, sk_hi)
+  int32_t group;     // Stream-K group of this unit
+  int64_t sk_lo;     // remaining Stream-K iterations [sk_lo, sk_hi) within the group
   int64_t sk_hi;
 };
 
 TST_HD void work_begin(const Sched& s, int32_t cta, WorkIter& it) {
   it.next_dp = cta;
-  it.pad_ = 0;
+  const int32_t g = s.sk_groups > 0 ? s.sk_groups : 1;
+  it.group = cta % g;
   if (s.sk_tiles > 0) {
-    // unit u owns [floor(u W / P), floor((u + 1) W / P)), W = sk_tiles * Kt
-    const int64_t W = (int64_t)s.sk_tiles * s.kt;
-    it.sk_lo = (int64_t)cta * W / s.grid;
-    it.sk_hi = (int64_t)(cta + 1) * W / s.grid;
+    // member u of a group of P_g units owns [floor(u W / P_g), floor((u + 1) W / P_g)),
+    // W = (tiles of the group) * Kt; without groups P_g = P and W = sk_tiles * Kt
+    const int32_t member = cta / g;
+    const int64_t units = (s.grid - it.group + g - 1) / g;
+    const int64_t tiles = (s.sk_tiles - it.group + g - 1) / g;
+    const int64_t W = tiles * s.kt;
+    it.sk_lo = units > 0 ? (int64_t)member * W / units : 0;
+    it.sk_hi = units > 0 ? (int64_t)(member + 1) * W / units : 0;
   } else {
     it.sk_lo = it.sk_hi = 0;
   }
@@ -130,7 +139,8 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
       end = it.sk_hi;
       it.sk_hi = start;
     }
-    w.tile = s.dp_tiles + (int32_t)t;
+    const int32_t g = s.sk_groups > 0 ? s.sk_groups : 1;
+    w.tile = s.dp_tiles + (int32_t)t * g + it.group;   // output_tile_id = id_in_group * groups + group
     w.k_begin = (int32_t)(start - t * s.kt);          // tile_iter_start - output_tile_iter_start
     w.k_count = (int32_t)(end - start);
     const bool final_split = (w.k_begin + w.k_count) == s.kt;
