@@ -34,6 +34,15 @@ Readings where the pages leave a step open (each is listed in the design notes):
     which case it stays fully data-parallel;
   * backward iteration reverses the order of a unit's splits; k stays
     ascending inside each split;
+  * Stream-K fixup modes ("H100 . Stream-K scheduling", section 6): the lock
+    counts accumulated k-tiles; deterministic: every later split waits until
+    the lock equals its K_idx; non-deterministic: a middle split only waits for
+    an initialised workspace (lock >= 1) and adds atomically, the final split
+    still waits for lock == K_idx; separate reduction (named in section 6, steps
+    not given): no split waits, each writes its partial to its own slot and a
+    second pass sums the slots of a tile in K order.  The slot of a split is
+    (member index of its unit) - (member index of the unit holding the tile's
+    first k-tile);
   * Stream-K groups ("H100 . Stream-K scheduling", section 7): the Stream-K
     tiles are dealt to g groups by output_tile_id = id_in_group * g + group;
     unit u belongs to group u mod g as its member u // g (the pages do not say
@@ -149,6 +158,31 @@ def streamk_group_splits(u: int, P: int, T_sk: int, Kt: int, groups: int, tile_o
         tile_in_group = s.tile
         out.append(Split(tile_offset + tile_in_group * g + j, s.k_idx, s.k_count, Kt))  # output_tile_id
     return out
+
+
+def streamk_split_slots(P: int, T_sk: int, Kt: int, groups: int = 1):
+    """Per Stream-K tile (0-based within the Stream-K range) its splits in K order as
+    (unit, k_idx, k_count, slot), and the largest slot count any tile needs."""
+    per_tile = {t: [] for t in range(T_sk)}
+    for u in range(P):
+        for s in streamk_group_splits(u, P, T_sk, Kt, groups):
+            per_tile[s.tile].append((u, s.k_idx, s.k_count))
+    out, slots_max = {}, 0
+    for t, lst in per_tile.items():
+        lst.sort(key=lambda x: x[1])
+        first_member = lst[0][0] // groups
+        out[t] = [(u, k, c, u // groups - first_member) for u, k, c in lst]
+        slots_max = max(slots_max, out[t][-1][3] + 1)
+    return out, slots_max
+
+
+def fixup_wait(split: Split, mode: str):
+    """What a split waits for before touching the workspace: (comparison, lock value) or None."""
+    if not split.requires_fixup or split.role == "first" or mode == "separate":
+        return None
+    if mode == "deterministic" or split.role == "final":
+        return ("==", split.k_idx)
+    return (">=", 1)   # non-deterministic middle split
 
 
 def hybrid_split_count(T: int, P: int) -> int:

@@ -360,3 +360,28 @@ def test_streamk_groups_same_k_slice_of_neighbouring_tiles():
         tiles = [t for t, _ in starts]
         assert max(tiles) - min(tiles) < 2 * g
         assert len({k for _, k in starts}) <= 2
+
+
+@pytest.mark.parametrize("P,T,Kt,g", [(152, 225, 128, 1), (152, 225, 128, 4), (4, 3, 90, 1), (152, 4, 4, 1),
+                                      (16, 9, 16, 2), (7, 13, 3, 3)])
+def test_streamk_split_slots(P, T, Kt, g):
+    slots, smax = S.streamk_split_slots(P, T, Kt, g)
+    assert set(slots) == set(range(T))
+    for t, lst in slots.items():
+        ks = [k for _, k, _, _ in lst]
+        assert ks == sorted(ks) and ks[0] == 0 and sum(c for _, _, c, _ in lst) == Kt
+        sl = [s for *_, s in lst]
+        assert sl[0] == 0 and sl == sorted(sl) and len(set(sl)) == len(sl) and sl[-1] < smax
+    # the worked example: tile 0 has unit 0 (slot 0) and unit 1 (slot 1)
+    if (P, T, Kt, g) == (4, 3, 90, 1):
+        assert [(u, k, c, s) for u, k, c, s in slots[0]] == [(0, 0, 67, 0), (1, 67, 23, 1)]
+
+
+def test_fixup_wait_rules_from_the_lock_section():
+    first, middle, final = S.Split(0, 0, 30, 90), S.Split(0, 30, 30, 90), S.Split(0, 60, 30, 90)
+    whole = S.Split(0, 0, 90, 90)
+    assert S.fixup_wait(whole, "deterministic") is None and S.fixup_wait(first, "deterministic") is None
+    assert S.fixup_wait(middle, "deterministic") == ("==", 30)      # strict left-to-right
+    assert S.fixup_wait(middle, "nondeterministic") == (">=", 1)    # workspace initialised
+    assert S.fixup_wait(final, "nondeterministic") == ("==", 60)    # all earlier k-tiles in
+    assert S.fixup_wait(final, "separate") is None
