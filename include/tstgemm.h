@@ -137,8 +137,18 @@ typedef struct {
                               dealt to groups by output_tile_id = id_in_group * groups + group,
                               unit u works in group u % groups, and each group splits its own
                               tiles over its own units ("H100 . Stream-K scheduling" section 7) */
-    int32_t reserved2;
+    int32_t sk_fixup;      /* how split tiles are combined ("H100 . Stream-K scheduling" section 6):
+                              TST_SK_DETERMINISTIC (default): each later split waits until the
+                              lock equals its K_idx, strict left-to-right order, bitwise
+                              repeatable; TST_SK_ATOMIC: middle splits only wait for an
+                              initialised workspace and add atomically (order varies run to run);
+                              TST_SK_SEPARATE: no split waits, every split writes its own
+                              partial slot and a second kernel sums the slots in K order and
+                              applies the epilogue (bitwise repeatable, needs no co-resident
+                              grid, more workspace) */
 } tst_plan_options;
+
+enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2 };
 
 /* What the plan decided (for logging and tests). */
 typedef struct {
@@ -157,6 +167,8 @@ typedef struct {
     int64_t workspace_bytes;   /* device bytes owned by the plan (Stream-K partials + locks + status) */
     int32_t cta_group;         /* 1 or 2 CTAs per scheduling unit */
     int32_t ctas;              /* CTAs launched = grid * cta_group */
+    int32_t kernels_per_run;   /* kernel launches per gemm_run (2 with the separate reduction) */
+    int32_t sk_slots;          /* partial slots per split-tile half (separate reduction), else 1 */
 } tst_plan_info;
 
 typedef struct tst_plan tst_plan;

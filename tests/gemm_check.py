@@ -57,7 +57,7 @@ def plan_for(w: dict, **over):
     kw = dict(dtype=w["dtype"], mapping=w["mapping"], schedule=w["schedule"], out_dtype=w["out"],
               alpha=w.get("alpha", 1.0), has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
               use_scales=w.get("use_scales", False), bn=w.get("bn", 0), cta_group=w.get("cta_group", 0))
-    for k in ("sk_groups", "bk", "stages", "sk_forward"):
+    for k in ("sk_groups", "bk", "stages", "sk_forward", "sk_fixup"):
         if k in w:
             kw[k] = w[k]
     kw.update(over)

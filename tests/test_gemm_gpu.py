@@ -225,6 +225,49 @@ def test_streamk_groups_exact_and_traced(groups, cta_group):
     assert_close(host_values(b1)[rows], z2, ad2, "f32", f"groups={groups}")
 
 
+@pytest.mark.parametrize("fixup", ["atomic", "separate"])
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("schedule,groups", [("streamk", 1), ("streamk", 4), ("streamk_hybrid", 1)])
+def test_streamk_fixup_modes(fixup, cta_group, schedule, groups):
+    """Non-deterministic (atomic) and separate-reduction fixups: small integers exact, real
+    inputs within the bound; the separate reduction is also bitwise repeatable and equal in
+    forward and backward split order (its adds run in K order whatever the timing)."""
+    M, N, K = 1920, 1920, 4096
+    w = dict(M=M, N=N, K=K, dtype="bf16", out="bf16", mapping=("grouped_m", 8), schedule=schedule, bn=128,
+             cta_group=cta_group, sk_groups=groups, sk_fixup=fixup, alpha=0.5, relu=True, bias_dist="normal")
+    ints = synthetic.make_gemm_inputs(M, N, K, "bf16", "int:2", case=24, bias_dist="int:4")
+    C = run_gemm(plan_for(w), ints, "bf16")
+    rows = sample_rows(M)
+    z, _ = oracle_rows(ints, w, rows)   # exact in FP32 (|z| <= 2^13); compare after the BF16 rounding
+    assert np.array_equal(host_values(C)[rows], oracle.decode(oracle.round_bf16(z), "bf16"))
+    inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=25, bias_dist="normal")
+    dev = to_device(inp)
+    a = run_gemm(plan_for(w), inp, "bf16", dev)
+    z, ad = oracle_rows(inp, w, rows)
+    assert_close(host_values(a)[rows], z, ad, "bf16", f"{fixup} {schedule}")
+    if fixup == "separate":
+        b = run_gemm(plan_for(w), inp, "bf16", dev)
+        f = run_gemm(plan_for(dict(w, sk_forward=1)), inp, "bf16", dev)
+        assert torch.equal(a, b) and torch.equal(a, f)
+
+
+def test_atomic_fixup_lock_timeout_reports():
+    w = dict(M=384, N=384, K=2048, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="streamk", bn=128,
+             cta_group=1, sk_fixup="atomic")
+    inp = synthetic.make_gemm_inputs(384, 384, 2048, "bf16", "normal", case=26)
+    plan = plan_for(w, num_ctas=16)
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOCK, None, 0, timeout_ns=20_000_000)
+    A, B, _, _ = to_device(inp)
+    C = torch.zeros(384, 384, device="cuda")
+    tst.gemm_run(plan, A, B, C)
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_ERR_TIMEOUT and ((word >> 8) & 0xFF) == 4, (st, hex(word))
+    tst.gemm_plan_set_debug(plan, 0, None, 0)
+    C2 = run_gemm(plan, inp, "f32")
+    z, ad = oracle_rows(inp, w)
+    assert_close(host_values(C2), z, ad, "f32", "after atomic-mode lock timeout")
+
+
 @pytest.mark.parametrize("cta_group", [1, 2])
 def test_device_trace_matches_oracle_enumeration(cta_group):
     for sched, kw in (("persistent", {}), ("streamk", {}), ("streamk", {"sk_forward": True}),

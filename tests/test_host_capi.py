@@ -217,3 +217,20 @@ def test_streamk_groups_limit():
     with pytest.raises(tst.TstError) as e:
         _host_plan(1920, 1920, 16384, schedule="streamk", sk_groups=9)
     assert e.value.status == tst.TST_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("shape,sms,groups", [((1920, 1920, 16384), 152, 1), ((1920, 1920, 16384), 152, 4),
+                                              ((384, 384, 2048), 16, 1), ((256, 256, 256), 152, 1),
+                                              ((640, 896, 320), 7, 3)])
+def test_separate_reduction_slots_match_oracle(shape, sms, groups):
+    M, N, K = shape
+    p = _host_plan(M, N, K, schedule="streamk", bn=128, num_sms=sms, sk_groups=groups, sk_fixup="separate")
+    i = p.info
+    _, smax = S.streamk_split_slots(i.grid, int(i.tiles), i.kt, groups)
+    assert i.sk_slots == smax and i.kernels_per_run == 2
+    det = _host_plan(M, N, K, schedule="streamk", bn=128, num_sms=sms, sk_groups=groups)
+    assert det.info.sk_slots == 1 and det.info.kernels_per_run == 1
+    assert i.workspace_bytes > det.info.workspace_bytes or smax == 1
+    with pytest.raises(tst.TstError) as e:
+        _host_plan(M, N, K, schedule="streamk", sk_fixup=7)
+    assert e.value.status == tst.TST_ERR_INVALID_ARG

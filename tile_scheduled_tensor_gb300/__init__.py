@@ -15,6 +15,7 @@ from ._capi import (TST_BF16, TST_E4M3, TST_OUT_F32, TST_OUT_BF16, TST_LAYOUT_A_
                     TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N,
                     TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID,
                     TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG_ROLE_CYCLES,
+                    TST_SK_DETERMINISTIC, TST_SK_ATOMIC, TST_SK_SEPARATE,
                     TST_OK, TST_ERR_INVALID_ARG, TST_ERR_UNSUPPORTED, TST_ERR_ALIGNMENT, TST_ERR_OOM,
                     TST_ERR_CUDA, TST_ERR_TIMEOUT, TST_ERR_DEVICE_CHECK, TST_ERR_NO_DEVICE,
                     TST_NOALLOC_SCRATCH_BYTES)
@@ -25,6 +26,7 @@ _DTYPES = {"bf16": TST_BF16, "e4m3": TST_E4M3}
 _OUT = {"f32": TST_OUT_F32, "bf16": TST_OUT_BF16}
 _MAPS = {"linear_nfast": TST_MAP_LINEAR_NFAST, "linear_mfast": TST_MAP_LINEAR_MFAST,
          "grouped_m": TST_MAP_GROUPED_M, "grouped_n": TST_MAP_GROUPED_N}
+_FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separate": TST_SK_SEPARATE}
 _SCHED = {"static": TST_STATIC, "persistent": TST_PERSISTENT, "streamk": TST_STREAMK,
           "streamk_hybrid": TST_STREAMK_HYBRID}
 
@@ -81,14 +83,14 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      out_dtype="f32", alpha: float = 1.0, has_bias: bool = False, relu: bool = False,
                      use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_forward: bool = False,
                      host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
-                     stages: int = 0, bk: int = 0, sk_groups: int = 0) -> Plan:
+                     stages: int = 0, bk: int = 0, sk_groups: int = 0, sk_fixup="deterministic") -> Plan:
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     epi = _capi.tst_epilogue(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), int(bool(has_bias)),
                              int(bool(relu)), int(bool(use_scales)))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
                                   int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
-                                  int(sk_groups), 0)
+                                  int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"))
     h = ctypes.c_void_p()
     _check(lib.gemm_plan_create_ex(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
                                    TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),

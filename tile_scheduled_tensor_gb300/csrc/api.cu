@@ -32,6 +32,9 @@ struct tst_plan {
   tst_plan_options opts{};
   int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
   int32_t cg = 1;              // CTAs per scheduling unit (2 = CTA pair)
+  int32_t sk_mode = 0;         // tst::SkFixup
+  int32_t sk_slots = 1;        // partial slots per split-tile half
+  const void* reduce_kernel = nullptr;
   int32_t ka = 1;              // 128-byte swizzle atoms of K per pipeline stage
   int32_t num_sms = 0, max_items = 0, resident_units = 0;
   tst::Sched sched{};
@@ -253,6 +256,8 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   s.backward = o.sk_forward ? 0 : 1;
   if (o.sk_groups < 0 || o.sk_groups > 8) { delete p; return TST_ERR_UNSUPPORTED; }  // at most 8 groups
   s.sk_groups = o.sk_groups > 0 ? o.sk_groups : 1;
+  if (o.sk_fixup < TST_SK_DETERMINISTIC || o.sk_fixup > TST_SK_SEPARATE) { delete p; return TST_ERR_INVALID_ARG; }
+  p->sk_mode = o.sk_fixup;
   const int64_t P = o.num_ctas > 0 ? o.num_ctas : resident;
   switch (schedule) {
     case TST_STATIC:
@@ -272,10 +277,22 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
       break;
     }
   }
-  if ((schedule == TST_STREAMK || schedule == TST_STREAMK_HYBRID) && !p->host_only && P > resident) {
+  if ((schedule == TST_STREAMK || schedule == TST_STREAMK_HYBRID) && p->sk_mode != TST_SK_SEPARATE &&
+      !p->host_only && P > resident) {
     // split tiles wait on each other: every unit must be resident at once
     delete p;
     return TST_ERR_UNSUPPORTED;
+  }
+  // separate reduction: as many partial slots per split tile as units can touch one tile
+  if (p->sk_mode == TST_SK_SEPARATE) {
+    int32_t most = 1;
+    for (int32_t t = 0; t < s.sk_tiles; ++t) {
+      int32_t grp, first, last;
+      int64_t lo, hi;
+      tst::sk_tile_members(s, s.dp_tiles + t, grp, first, last, lo, hi);
+      most = std::max(most, last - first + 1);
+    }
+    p->sk_slots = most;
   }
   // longest work list (trace sizing)
   int32_t max_items = 0;
@@ -291,7 +308,7 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
 
   // plan-owned device memory: status word, then one lock and one 128 x bn FP32
   // partial tile per CTA-half of each split tile
-  const size_t slots = static_cast<size_t>(s.sk_tiles) * p->cg;
+  const size_t slots = static_cast<size_t>(s.sk_tiles) * p->cg * p->sk_slots;
   const size_t status_bytes = 256;
   const size_t lock_bytes = ((slots * 4 + 255) / 256) * 256;
   const size_t ws_bytes = slots * tst::kBlockM * p->bn * sizeof(float);
@@ -312,6 +329,14 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
     p->d_status = reinterpret_cast<uint32_t*>(base);
     p->d_locks = reinterpret_cast<int32_t*>(base + status_bytes);
     p->d_ws = ws_bytes ? reinterpret_cast<float*>(base + status_bytes + lock_bytes) : nullptr;
+    if (p->sk_mode == TST_SK_SEPARATE && s.sk_tiles > 0) {
+      p->reduce_kernel = tst_reduce_kernel(epi->out_dtype);
+      if (!p->reduce_kernel) {
+        cudaFree(p->dev_block);
+        delete p;
+        return TST_ERR_CUDA;
+      }
+    }
   }
   if (log_enabled())
     fprintf(stderr,
@@ -353,6 +378,8 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->workspace_bytes = static_cast<int64_t>(p->dev_bytes);
   info->cta_group = p->cg;
   info->ctas = p->sched.grid * p->cg;
+  info->kernels_per_run = (p->sk_mode == TST_SK_SEPARATE && p->sched.sk_tiles > 0) ? 2 : 1;
+  info->sk_slots = p->sk_slots;
   return TST_OK;
 }
 
@@ -449,6 +476,8 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.debug_flags = p->debug_flags;
   kp.max_items = p->max_items;
   kp.stages = p->stages;
+  kp.sk_mode = p->sk_mode;
+  kp.sk_slots = p->sk_slots;
   kp.timeout_ns = p->timeout_ns;
 
   // status word and Stream-K locks start at zero for every launch
@@ -468,7 +497,7 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-  } else if (p->sched.sk_tiles > 0) {
+  } else if (p->sched.sk_tiles > 0 && p->sk_mode != TST_SK_SEPARATE) {
     // Stream-K splits wait on each other across CTAs: ask for a co-resident grid
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
@@ -479,6 +508,33 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   if (cudaLaunchKernelExC(&cfg, p->kernel, args) != cudaSuccess) {
     cudaGetLastError();
     return TST_ERR_CUDA;
+  }
+  if (p->reduce_kernel) {
+    // separate reduction: sum each split tile's partial slots in K order, then the epilogue
+    tst::ReduceParams rp = {};
+    rp.workspace = p->d_ws;
+    rp.C = C;
+    rp.bias = kp.bias;
+    rp.scales = kp.scales;
+    rp.alpha = p->epi.alpha;
+    rp.M = kp.M;
+    rp.N = kp.N;
+    rp.bn = p->bn;
+    rp.cg = p->cg;
+    rp.slots = p->sk_slots;
+    rp.has_bias = kp.has_bias;
+    rp.relu = kp.relu;
+    rp.use_scales = kp.use_scales;
+    rp.sched = p->sched;
+    cudaLaunchConfig_t rc = {};
+    rc.gridDim = dim3(static_cast<unsigned>(p->sched.sk_tiles * p->cg * (tst::kBlockM / tst::kReduceRows)), 1, 1);
+    rc.blockDim = dim3(tst::kReduceThreads, 1, 1);
+    rc.stream = stream;
+    void* rargs[] = {&rp};
+    if (cudaLaunchKernelExC(&rc, p->reduce_kernel, rargs) != cudaSuccess) {
+      cudaGetLastError();
+      return TST_ERR_CUDA;
+    }
   }
   p->last_stream = stream;
   p->ran = true;

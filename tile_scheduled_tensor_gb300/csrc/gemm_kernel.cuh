@@ -109,6 +109,26 @@ __device__ __forceinline__ bool wait_lock(const KernelParams& p, const Ctx& c, c
   }
 }
 
+// Bounded wait for a Stream-K lock to reach at least `want` (non-deterministic
+// fixup: the workspace has been initialised by the first split).
+template <int CG>
+__device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const Ctx& c, const int32_t* lock,
+                                                   int32_t want) {
+  if (ptx::ld_acquire_gpu(lock) >= want) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t spin = 1;; ++spin) {
+    __nanosleep(64);
+    if (ptx::ld_acquire_gpu(lock) >= want) return true;
+    if ((spin & 15u) == 0u) {
+      if (*c.abort) return false;
+      if (ptx::globaltimer() - t0 > p.timeout_ns) {
+        raise_error<CG>(p, c, ST_TIMEOUT, ROLE_LOCK);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ producer
 template <int BN, int DT, int CG, int KA>
 __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c, uint32_t smem_a, uint32_t smem_b,
@@ -326,14 +346,29 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   while (work_next(p.sched, it, w)) {
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
     const bool final_split = (w.flags & ITEM_FINAL) != 0;
-    // Stream-K slot of this CTA's half of the tile (valid when fixup)
-    const int32_t slot = (w.tile - p.sched.dp_tiles) * CG + static_cast<int32_t>(c.rank);
+    const bool separate = p.sk_mode == SK_SEPARATE;
+    // Stream-K slot of this CTA's half of the tile (valid when fixup); the separate
+    // reduction gives every split of the half its own slot, indexed by the unit's
+    // member number relative to the tile's first member
+    int32_t slot = (w.tile - p.sched.dp_tiles) * CG + static_cast<int32_t>(c.rank);
+    if (fixup && separate) {
+      int32_t grp, m_first, m_last;
+      int64_t t_lo, t_hi;
+      sk_tile_members(p.sched, w.tile, grp, m_first, m_last, t_lo, t_hi);
+      const int32_t member = c.unit / (p.sched.sk_groups > 0 ? p.sched.sk_groups : 1);
+      slot = slot * p.sk_slots + (member - m_first);
+    }
     // one elected thread waits; the verdict is broadcast so all 128 threads
     // take the same path through the named barriers below
     const long long t0 = (p.stats && ep == 0) ? clock64() : 0;
     if (ep == 0) {
       bool ok = wait_phase<CG>(p, c, bar_tfull + 8 * acc, acc_phase, ROLE_EPILOGUE);
-      if (ok && fixup && w.k_begin > 0) ok = wait_lock<CG>(p, c, p.locks + slot, w.k_begin);
+      if (ok && fixup && !separate && w.k_begin > 0) {
+        // deterministic: every later split waits for exactly K_idx accumulated k-tiles;
+        // non-deterministic: a middle split only needs an initialised workspace
+        if (p.sk_mode == SK_ATOMIC && !final_split) ok = wait_lock_at_least<CG>(p, c, p.locks + slot, 1);
+        else ok = wait_lock<CG>(p, c, p.locks + slot, w.k_begin);
+      }
       *ep_ok = ok ? 1u : 0u;
     }
     ptx::named_bar_sync(1, 128);
@@ -366,12 +401,24 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c32 = ch * 2 + h;
+        if (fixup && separate) {
+          // own slot, row-major [row][column]: the reduction pass reads and writes rows
+          float4* dst = reinterpret_cast<float4*>(ws + row_in_tile * BN + c32 * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            __stcg(dst + q, make_float4(v[32 * h + 4 * q], v[32 * h + 4 * q + 1], v[32 * h + 4 * q + 2],
+                                        v[32 * h + 4 * q + 3]));
+          continue;
+        }
         // workspace layout per slot: [column][row], so a warp's 32 rows are contiguous
         float* wsc = ws != nullptr ? ws + (c32 * 32) * kBlockM + row_in_tile : nullptr;
         if (fixup && !final_split) {
           if (w.k_begin == 0) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) __stcg(wsc + j * kBlockM, v[32 * h + j]);
+          } else if (p.sk_mode == SK_ATOMIC) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) atomicAdd(wsc + j * kBlockM, v[32 * h + j]);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) __stcg(wsc + j * kBlockM, __ldcg(wsc + j * kBlockM) + v[32 * h + j]);
@@ -411,14 +458,17 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
       }
     }
     ptx::tc_fence_before();
-    if (fixup && !final_split) __threadfence();  // partials visible GPU-wide before the lock moves
+    if (fixup && (!final_split || separate)) __threadfence();  // partials visible GPU-wide before the lock moves
     ptx::named_bar_sync(1, 128);
     if (p.stats && ep == 0) { busy += clock64() - t1; ++items; }
     if (ep == 0) {
       if (CG == 2) ptx::mbar_arrive_cluster(tempty_target + 8 * acc);
       else ptx::mbar_arrive(bar_tempty + 8 * acc);
-      if (fixup && !final_split && !(p.debug_flags & DBG_SKIP_LOCK))
-        ptx::st_release_gpu(p.locks + slot, w.k_begin + w.k_count);
+      if (fixup && !final_split && !separate && !(p.debug_flags & DBG_SKIP_LOCK)) {
+        // the lock counts the k-tiles accumulated in the workspace
+        if (p.sk_mode == SK_ATOMIC && w.k_begin > 0) ptx::red_add_release_gpu(p.locks + slot, w.k_count);
+        else ptx::st_release_gpu(p.locks + slot, w.k_begin + w.k_count);
+      }
     }
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
   }

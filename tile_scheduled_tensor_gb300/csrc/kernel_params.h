@@ -19,6 +19,9 @@ enum OutType : int32_t { OUT_F32 = 0, OUT_BF16 = 1 };
 enum StatusCode : uint32_t { ST_OK = 0, ST_TIMEOUT = 6, ST_DEVICE_CHECK = 7 };
 enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_LOCK = 4 };
 
+// Stream-K fixup ("H100 . Stream-K scheduling", section 6)
+enum SkFixup : int32_t { SK_DETERMINISTIC = 0, SK_ATOMIC = 1, SK_SEPARATE = 2 };
+
 enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8 };
 
 // Role-cycle counters (debug): kStatSlots uint64 per CTA, in SM clock cycles.
@@ -52,6 +55,8 @@ struct KernelParams {
   int32_t debug_flags;
   int32_t max_items;        // trace records per CTA
   int32_t stages;           // shared-memory ring depth in use (2 .. TileCfg::STAGES)
+  int32_t sk_mode;          // SkFixup: how split tiles are combined
+  int32_t sk_slots;         // partial-tile slots per split tile half (separate reduction)
   uint64_t timeout_ns;      // limit of every device-side wait
 };
 
@@ -118,5 +123,24 @@ inline int tst_cfg(int bn, int cg, int ka, bool smem) {
 }
 
 inline int tst_kernel_smem_bytes(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, true); }
+namespace tst {
+// Separate-reduction pass of Stream-K (streamk_reduce.cu): sums each split
+// tile's partial slots in K order and applies the epilogue.
+struct ReduceParams {
+  const float* workspace;
+  void* C;
+  const float* bias;
+  const float* scales;
+  float alpha;
+  int32_t M, N;
+  int32_t bn, cg, slots;
+  int32_t has_bias, relu, use_scales;
+  Sched sched;
+};
+constexpr int kReduceThreads = 256;
+constexpr int kReduceRows = 16;  // rows of a 128-row tile half per CTA
+}  // namespace tst
+const void* tst_reduce_kernel(int out_type);
+
 inline int tst_kernel_threads(int bn, int ka) { return (bn == 128 && ka == 2) ? tst::kThreadsDual : tst::kThreads; }
 inline int tst_kernel_stages(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, false); }

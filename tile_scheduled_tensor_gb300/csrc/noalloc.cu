@@ -215,6 +215,8 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   kp.debug_flags = 0;
   kp.max_items = 0;
   kp.stages = tst_kernel_stages(bn, 1, 1);
+  kp.sk_mode = tst::SK_DETERMINISTIC;
+  kp.sk_slots = 1;
   kp.timeout_ns = 10ull * 1000 * 1000 * 1000;
 
   // ---- clear what must start at zero: the status word and the locks

@@ -152,4 +152,33 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
   return true;
 }
 
+// ---- Stream-K member bookkeeping (separate-reduction fixup).  Member m of a
+// group of P_g members owns iterations [floor(m W / P_g), floor((m+1) W / P_g))
+// of the group's W = (group tiles) * Kt iterations.
+TST_HD void sk_group_geometry(const Sched& s, int32_t group, int64_t& units, int64_t& W) {
+  const int32_t g = s.sk_groups > 0 ? s.sk_groups : 1;
+  units = (s.grid - group + g - 1) / g;
+  W = (int64_t)((s.sk_tiles - group + g - 1) / g) * s.kt;
+}
+
+// the member whose range holds iteration x: the largest m with floor(m W / units) <= x
+TST_HD int32_t sk_owner(int64_t x, int64_t units, int64_t W) {
+  return (int32_t)(((x + 1) * units + W - 1) / W - 1);
+}
+
+// group, first and last member touching Stream-K task `tile`, and the tile's
+// iteration range [t_lo, t_hi) inside its group
+TST_HD void sk_tile_members(const Sched& s, int32_t tile, int32_t& group, int32_t& m_first, int32_t& m_last,
+                            int64_t& t_lo, int64_t& t_hi) {
+  const int32_t g = s.sk_groups > 0 ? s.sk_groups : 1;
+  const int32_t t = tile - s.dp_tiles;
+  group = t % g;
+  t_lo = (int64_t)(t / g) * s.kt;
+  t_hi = t_lo + s.kt;
+  int64_t units, W;
+  sk_group_geometry(s, group, units, W);
+  m_first = sk_owner(t_lo, units, W);
+  m_last = sk_owner(t_hi - 1, units, W);
+}
+
 }  // namespace tst
