@@ -23,6 +23,12 @@ Sources (page title, section):
 Readings where the pages leave a step open (each is listed in the design notes):
   * grouped strips with a ragged last strip use its true height/width
     gs = min(G, tiles left);
+  * 2D blocking (the table's "2D Blocking / box" family, Tensile's
+    WorkGroupMapping): square boxes of G x G tiles taken row-major, M-fast
+    inside a box, ragged edge boxes at their true size;
+  * Morton / Z-order (the table's bit-interleave family): tiles in increasing
+    order of the code that interleaves the bits of n (even bit positions) and
+    m (odd positions), codes outside the Mt x Nt grid skipped;
   * the Stream-K unit u owns global MAC iterations [floor(u W / P),
     floor((u+1) W / P)), W = T * Kt; the worked example in Lesson 8.1 section 3
     (3 tiles x 90 k-tiles over 4 units: unit 1 continues tile 0 at K_idx 67
@@ -52,8 +58,9 @@ Readings where the pages leave a step open (each is listed in the design notes):
 from __future__ import annotations
 
 from dataclasses import dataclass
+from functools import lru_cache
 
-LINEAR_NFAST, LINEAR_MFAST, GROUPED_M, GROUPED_N = 0, 1, 2, 3
+LINEAR_NFAST, LINEAR_MFAST, GROUPED_M, GROUPED_N, BLOCK_2D, MORTON = 0, 1, 2, 3, 4, 5
 STATIC, PERSISTENT, STREAMK, STREAMK_HYBRID = 0, 1, 2, 3
 
 
@@ -86,7 +93,35 @@ def tile_map(kind: int, group: int, Mt: int, Nt: int, i: int):
         n0 = strip * group
         width = min(group, Nt - n0)
         return r // width, n0 + r % width
+    if kind == BLOCK_2D:            # G x G boxes, row-major over boxes, M-fast inside
+        return block_2d_order(group, Mt, Nt)[i]
+    if kind == MORTON:
+        return morton_order(Mt, Nt)[i]
     raise ValueError(kind)
+
+
+@lru_cache(maxsize=256)
+def block_2d_order(G: int, Mt: int, Nt: int):
+    out = []   # a tuple is returned so the cached order cannot be modified
+    for m0 in range(0, Mt, G):
+        for n0 in range(0, Nt, G):
+            for n in range(n0, min(n0 + G, Nt)):
+                for m in range(m0, min(m0 + G, Mt)):
+                    out.append((m, n))
+    return tuple(out)
+
+
+def morton_code(m: int, n: int) -> int:
+    z = 0
+    for b in range(16):
+        z |= ((n >> b) & 1) << (2 * b)
+        z |= ((m >> b) & 1) << (2 * b + 1)
+    return z
+
+
+@lru_cache(maxsize=256)
+def morton_order(Mt: int, Nt: int):
+    return tuple(sorted(((m, n) for m in range(Mt) for n in range(Nt)), key=lambda mn: morton_code(*mn)))
 
 
 def wave_efficiency(T: int, P: int) -> float:

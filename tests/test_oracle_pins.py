@@ -209,10 +209,32 @@ def _strip_order_bruteforce(kind, G, Mt, Nt):
             for m in range(Mt):
                 for n in range(n0, min(n0 + G, Nt)):
                     out.append((m, n))
+    elif kind == S.BLOCK_2D:
+        for b in range(S.ceil_div(Mt, G) * S.ceil_div(Nt, G)):       # boxes row-major
+            bm, bn = divmod(b, S.ceil_div(Nt, G))
+            box = [(m, n) for m in range(bm * G, min(bm * G + G, Mt)) for n in range(bn * G, min(bn * G + G, Nt))]
+            out += sorted(box, key=lambda mn: (mn[1], mn[0]))          # M-fast inside the box
+    elif kind == S.MORTON:
+        # walk the padded power-of-two square in Z order (quadrants recursively: TL, TR, BL, BR)
+        side = 1
+        while side < max(Mt, Nt):
+            side *= 2
+
+        def walk(m0, n0, size):
+            if size == 1:
+                if m0 < Mt and n0 < Nt:
+                    out.append((m0, n0))
+                return
+            h = size // 2
+            walk(m0, n0, h)
+            walk(m0, n0 + h, h)
+            walk(m0 + h, n0, h)
+            walk(m0 + h, n0 + h, h)
+        walk(0, 0, side)
     return out
 
 
-@pytest.mark.parametrize("kind", [S.LINEAR_NFAST, S.LINEAR_MFAST, S.GROUPED_M, S.GROUPED_N])
+@pytest.mark.parametrize("kind", [S.LINEAR_NFAST, S.LINEAR_MFAST, S.GROUPED_M, S.GROUPED_N, S.BLOCK_2D, S.MORTON])
 def test_mapping_bijection_and_bruteforce(kind):
     for Mt in list(range(1, 14)) + [31, 40]:
         for Nt in list(range(1, 14)) + [33, 40]:
@@ -236,6 +258,23 @@ def test_mapping_equivalences_stated_on_page():
         assert [S.tile_map(S.GROUPED_M, Mt, Mt, Nt, i) for i in range(T)] == lin_m
         assert [S.tile_map(S.GROUPED_N, 1, Mt, Nt, i) for i in range(T)] == lin_m
         assert [S.tile_map(S.GROUPED_N, Nt + 3, Mt, Nt, i) for i in range(T)] == lin_n
+
+
+def test_block_2d_and_morton_reduce_to_known_orders():
+    for Mt, Nt in [(8, 8), (5, 7), (12, 3)]:
+        T = Mt * Nt
+        lin_n = [S.tile_map(S.LINEAR_NFAST, 1, Mt, Nt, i) for i in range(T)]
+        lin_m = [S.tile_map(S.LINEAR_MFAST, 1, Mt, Nt, i) for i in range(T)]
+        assert [S.tile_map(S.BLOCK_2D, 1, Mt, Nt, i) for i in range(T)] == lin_n
+        assert [S.tile_map(S.BLOCK_2D, max(Mt, Nt), Mt, Nt, i) for i in range(T)] == lin_m
+        # boxes as wide as the grid are grouped-M strips
+        assert [S.tile_map(S.BLOCK_2D, Nt, Mt, Nt, i) for i in range(T)] == \
+            [S.tile_map(S.GROUPED_M, Nt, Mt, Nt, i) for i in range(T)] or Nt > Mt
+    # Z order on a 4 x 4 grid, written out by hand
+    z4 = [(0, 0), (0, 1), (1, 0), (1, 1), (0, 2), (0, 3), (1, 2), (1, 3),
+          (2, 0), (2, 1), (3, 0), (3, 1), (2, 2), (2, 3), (3, 2), (3, 3)]
+    assert [S.tile_map(S.MORTON, 1, 4, 4, i) for i in range(16)] == z4
+    assert S.morton_code(3, 5) == 0b011011
 
 
 def test_working_set_example():
