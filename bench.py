@@ -320,7 +320,7 @@ def run_mapping_study(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     elt = 2 if base["dtype"] == "bf16" else 1
     for mapping in [("linear_nfast", 1), ("linear_mfast", 1), ("grouped_m", 4), ("grouped_m", 8), ("grouped_m", 16),
-                    ("grouped_n", 8), ("grouped_n", 16)]:
+                    ("grouped_n", 8), ("grouped_n", 16), ("block_2d", 4), ("block_2d", 8), ("morton", 1)]:
         plan = tst.gemm_plan_create(base["M"], base["N"], base["K"], dtype=base["dtype"], mapping=mapping,
                                     schedule=base["schedule"], out_dtype=base["out"], alpha=base.get("alpha", 1.0),
                                     has_bias=base.get("bias_dist") is not None, relu=base.get("relu", False),

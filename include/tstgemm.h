@@ -73,17 +73,25 @@ typedef enum { TST_LAYOUT_A_ROW_B_NK = 0 } tst_layout;
  *   LINEAR_MFAST: m = i % Mt, n = i / Mt              (C00 -> C10 -> ...)
  *   GROUPED_M:    strips of `group` tile-rows, M-fast inside a strip
  *   GROUPED_N:    strips of `group` tile-columns, N-fast inside a strip
- * A ragged last strip uses its true height / width. */
+ *   BLOCK_2D:     boxes of group x group tiles taken row-major, M-fast inside a box
+ *                 (the table's "2D blocking / box" family)
+ *   MORTON:       Z order: tiles by the code interleaving the bits of n (even
+ *                 positions) and m (odd positions), codes outside the grid skipped;
+ *                 the plan keeps the order as a table (8 bytes per tile)
+ * A ragged last strip or box uses its true height / width. */
 typedef enum {
     TST_MAP_LINEAR_NFAST = 0,
     TST_MAP_LINEAR_MFAST = 1,
     TST_MAP_GROUPED_M = 2,
-    TST_MAP_GROUPED_N = 3
+    TST_MAP_GROUPED_N = 3,
+    TST_MAP_BLOCK_2D = 4,
+    TST_MAP_MORTON = 5
 } tst_mapping_kind;
 
 typedef struct {
     int32_t kind;   /* tst_mapping_kind */
-    int32_t group;  /* strip width G in tiles (>= 1) for the grouped kinds; ignored otherwise */
+    int32_t group;  /* strip width G in tiles (>= 1) for the grouped kinds and the box side for
+                       BLOCK_2D; ignored otherwise */
 } tst_mapping;
 
 /* Assignment of linear tasks to CTAs.

@@ -20,7 +20,8 @@ from gemm_check import (assert_close, device_codes, freivalds, host_values, make
 
 pytestmark = pytest.mark.gpu
 
-MAPPINGS = [("linear_nfast", 1), ("linear_mfast", 1), ("grouped_m", 8), ("grouped_n", 16), ("grouped_m", 3)]
+MAPPINGS = [("linear_nfast", 1), ("linear_mfast", 1), ("grouped_m", 8), ("grouped_n", 16), ("grouped_m", 3),
+            ("block_2d", 4), ("morton", 1)]
 SCHEDULES = ["static", "persistent", "streamk", "streamk_hybrid"]
 
 

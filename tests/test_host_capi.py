@@ -14,7 +14,7 @@ from tile_scheduled_tensor_gb300 import _capi
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MAPS = {"linear_nfast": S.LINEAR_NFAST, "linear_mfast": S.LINEAR_MFAST,
-        "grouped_m": S.GROUPED_M, "grouped_n": S.GROUPED_N}
+        "grouped_m": S.GROUPED_M, "grouped_n": S.GROUPED_N, "block_2d": S.BLOCK_2D, "morton": S.MORTON}
 SCHEDS = {"static": S.STATIC, "persistent": S.PERSISTENT, "streamk": S.STREAMK,
           "streamk_hybrid": S.STREAMK_HYBRID}
 

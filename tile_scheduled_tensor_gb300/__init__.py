@@ -25,7 +25,8 @@ lib = _capi.load()
 _DTYPES = {"bf16": TST_BF16, "e4m3": TST_E4M3}
 _OUT = {"f32": TST_OUT_F32, "bf16": TST_OUT_BF16}
 _MAPS = {"linear_nfast": TST_MAP_LINEAR_NFAST, "linear_mfast": TST_MAP_LINEAR_MFAST,
-         "grouped_m": TST_MAP_GROUPED_M, "grouped_n": TST_MAP_GROUPED_N}
+         "grouped_m": TST_MAP_GROUPED_M, "grouped_n": TST_MAP_GROUPED_N,
+         "block_2d": _capi.TST_MAP_BLOCK_2D, "morton": _capi.TST_MAP_MORTON}
 _FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separate": TST_SK_SEPARATE}
 _SCHED = {"static": TST_STATIC, "persistent": TST_PERSISTENT, "streamk": TST_STREAMK,
           "streamk_hybrid": TST_STREAMK_HYBRID}

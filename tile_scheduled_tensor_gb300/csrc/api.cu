@@ -15,6 +15,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <vector>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -37,7 +38,9 @@ struct tst_plan {
   const void* reduce_kernel = nullptr;
   int32_t ka = 1;              // 128-byte swizzle atoms of K per pipeline stage
   int32_t num_sms = 0, max_items = 0, resident_units = 0;
-  tst::Sched sched{};
+  tst::Sched sched{};          // order points at order_host; launches swap in d_order
+  std::vector<int32_t> order_host;  // Morton mapping: (m, n) of every task
+  int32_t* d_order = nullptr;
   bool host_only = false;
   int device = -1;
   // plan-owned device memory: [status word | locks | workspace]
@@ -142,8 +145,9 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   if (epi == nullptr || M <= 0 || N <= 0 || K <= 0) return TST_ERR_INVALID_ARG;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TST_ERR_INVALID_ARG;
   if (dtype != TST_BF16 && dtype != TST_E4M3) return TST_ERR_INVALID_ARG;
-  if (mapping.kind < TST_MAP_LINEAR_NFAST || mapping.kind > TST_MAP_GROUPED_N) return TST_ERR_INVALID_ARG;
-  if ((mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N) && mapping.group < 1)
+  if (mapping.kind < TST_MAP_LINEAR_NFAST || mapping.kind > TST_MAP_MORTON) return TST_ERR_INVALID_ARG;
+  if ((mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N || mapping.kind == TST_MAP_BLOCK_2D) &&
+      mapping.group < 1)
     return TST_ERR_INVALID_ARG;
   if (schedule < TST_STATIC || schedule > TST_STREAMK_HYBRID) return TST_ERR_INVALID_ARG;
   if (epi->out_dtype != TST_OUT_F32 && epi->out_dtype != TST_OUT_BF16) return TST_ERR_INVALID_ARG;
@@ -252,7 +256,28 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   s.nt = static_cast<int32_t>(nt);
   s.kt = static_cast<int32_t>(kt);
   s.map_kind = mapping.kind;
-  s.group = (mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N) ? mapping.group : 1;
+  s.group = (mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N ||
+             mapping.kind == TST_MAP_BLOCK_2D) ? mapping.group : 1;
+  s.order = nullptr;
+  if (mapping.kind == TST_MAP_MORTON) {
+    // Z order: tiles by the code interleaving the bits of n (even) and m (odd positions)
+    std::vector<std::pair<uint64_t, int64_t>> codes;
+    codes.reserve(static_cast<size_t>(T));
+    for (int64_t m = 0; m < mt; ++m)
+      for (int64_t n = 0; n < nt; ++n) {
+        uint64_t z = 0;
+        for (int b = 0; b < 31; ++b)
+          z |= (((static_cast<uint64_t>(n) >> b) & 1u) << (2 * b)) | (((static_cast<uint64_t>(m) >> b) & 1u) << (2 * b + 1));
+        codes.emplace_back(z, m * nt + n);
+      }
+    std::sort(codes.begin(), codes.end());
+    p->order_host.resize(static_cast<size_t>(2 * T));
+    for (int64_t i = 0; i < T; ++i) {
+      p->order_host[2 * i] = static_cast<int32_t>(codes[i].second / nt);
+      p->order_host[2 * i + 1] = static_cast<int32_t>(codes[i].second % nt);
+    }
+    s.order = p->order_host.data();
+  }
   s.backward = o.sk_forward ? 0 : 1;
   if (o.sk_groups < 0 || o.sk_groups > 8) { delete p; return TST_ERR_UNSUPPORTED; }  // at most 8 groups
   s.sk_groups = o.sk_groups > 0 ? o.sk_groups : 1;
@@ -329,6 +354,17 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
     p->d_status = reinterpret_cast<uint32_t*>(base);
     p->d_locks = reinterpret_cast<int32_t*>(base + status_bytes);
     p->d_ws = ws_bytes ? reinterpret_cast<float*>(base + status_bytes + lock_bytes) : nullptr;
+    if (!p->order_host.empty()) {
+      const size_t ob = p->order_host.size() * sizeof(int32_t);
+      if (cudaMalloc(&p->d_order, ob) != cudaSuccess ||
+          cudaMemcpy(p->d_order, p->order_host.data(), ob, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        if (p->d_order) cudaFree(p->d_order);
+        cudaFree(p->dev_block);
+        delete p;
+        return TST_ERR_OOM;
+      }
+    }
     if (p->sk_mode == TST_SK_SEPARATE && s.sk_tiles > 0) {
       p->reduce_kernel = tst_reduce_kernel(epi->out_dtype);
       if (!p->reduce_kernel) {
@@ -358,6 +394,7 @@ tst_status gemm_plan_destroy(tst_plan* plan) {
   if (plan == nullptr) return TST_OK;
   tst_status st = TST_OK;
   if (plan->dev_block && cudaFree(plan->dev_block) != cudaSuccess) st = TST_ERR_CUDA;
+  if (plan->d_order && cudaFree(plan->d_order) != cudaSuccess) st = TST_ERR_CUDA;
   delete plan;
   return st;
 }
@@ -470,6 +507,7 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.K = static_cast<int32_t>(p->K);
   kp.alpha = p->epi.alpha;
   kp.sched = p->sched;
+  kp.sched.order = p->d_order;
   kp.has_bias = p->epi.has_bias ? 1 : 0;
   kp.relu = p->epi.relu ? 1 : 0;
   kp.use_scales = p->epi.use_scales ? 1 : 0;
@@ -526,6 +564,7 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
     rp.relu = kp.relu;
     rp.use_scales = kp.use_scales;
     rp.sched = p->sched;
+    rp.sched.order = p->d_order;
     cudaLaunchConfig_t rc = {};
     rc.gridDim = dim3(static_cast<unsigned>(p->sched.sk_tiles * p->cg * (tst::kBlockM / tst::kReduceRows)), 1, 1);
     rc.blockDim = dim3(tst::kReduceThreads, 1, 1);

@@ -122,8 +122,10 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
     return TST_ERR_INVALID_ARG;
   if (dtype != TST_BF16 && dtype != TST_E4M3) return TST_ERR_INVALID_ARG;
   if (schedule != TST_STREAMK && schedule != TST_STREAMK_HYBRID) return TST_ERR_INVALID_ARG;
-  if (mapping.kind < TST_MAP_LINEAR_NFAST || mapping.kind > TST_MAP_GROUPED_N) return TST_ERR_INVALID_ARG;
-  const bool grouped = mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N;
+  if (mapping.kind < TST_MAP_LINEAR_NFAST || mapping.kind > TST_MAP_MORTON) return TST_ERR_INVALID_ARG;
+  if (mapping.kind == TST_MAP_MORTON) return TST_ERR_UNSUPPORTED;  // its order table would need an allocation
+  const bool grouped = mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N ||
+                       mapping.kind == TST_MAP_BLOCK_2D;
   if (grouped && mapping.group < 1) return TST_ERR_INVALID_ARG;
   if (epi->out_dtype != TST_OUT_F32 && epi->out_dtype != TST_OUT_BF16) return TST_ERR_INVALID_ARG;
   if (bn != 0 && bn != 128 && bn != 256) return TST_ERR_UNSUPPORTED;
@@ -158,6 +160,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   s.group = grouped ? mapping.group : 1;
   s.backward = 1;  // backward tile iteration, as gemm_plan_create does by default
   s.sk_groups = 1;
+  s.order = nullptr;
   if (schedule == TST_STREAMK) {
     s.grid = static_cast<int32_t>(P);
     s.dp_tiles = 0;

@@ -31,7 +31,9 @@
 
 namespace tst {
 
-enum MapKind : int32_t { MAP_LINEAR_NFAST = 0, MAP_LINEAR_MFAST = 1, MAP_GROUPED_M = 2, MAP_GROUPED_N = 3 };
+enum MapKind : int32_t {
+  MAP_LINEAR_NFAST = 0, MAP_LINEAR_MFAST = 1, MAP_GROUPED_M = 2, MAP_GROUPED_N = 3, MAP_BLOCK_2D = 4, MAP_MORTON = 5
+};
 enum SchedKind : int32_t { SCHED_STATIC = 0, SCHED_PERSISTENT = 1, SCHED_STREAMK = 2, SCHED_STREAMK_HYBRID = 3 };
 
 enum : int32_t { ITEM_FINAL = 1, ITEM_FIXUP = 2 };
@@ -45,6 +47,7 @@ struct Sched {
   int32_t sk_tiles;       // tasks [dp_tiles, dp_tiles + sk_tiles) are split by Stream-K
   int32_t backward;       // Stream-K splits of a unit visited last-first
   int32_t sk_groups;      // Stream-K groups (1 = none)
+  const int32_t* order;   // MAP_MORTON: (m, n) of every task, 2 ints each (host or device copy)
 };
 
 struct WorkItem {
@@ -77,7 +80,7 @@ TST_HD void tile_coord(const Sched& s, int32_t i, int32_t& m, int32_t& n) {
       m = m0 + (r - n * h);
       return;
     }
-    default: {  // MAP_GROUPED_N
+    case MAP_GROUPED_N: {
       const int32_t span = s.group * s.mt;
       const int32_t strip = i / span;
       const int32_t r = i - strip * span;
@@ -87,6 +90,23 @@ TST_HD void tile_coord(const Sched& s, int32_t i, int32_t& m, int32_t& n) {
       n = n0 + (r - m * w);
       return;
     }
+    case MAP_BLOCK_2D: {
+      // G x G boxes row-major, M-fast inside a box; an edge box keeps its true size
+      // and is always the last of its box row (or column), so plain division finds it
+      const int32_t row = i / (s.group * s.nt);
+      const int32_t o = i - row * (s.group * s.nt);
+      const int32_t m0 = row * s.group;
+      const int32_t h = (s.mt - m0) < s.group ? (s.mt - m0) : s.group;
+      const int32_t col = o / (h * s.group);
+      const int32_t o2 = o - col * (h * s.group);
+      m = m0 + o2 % h;
+      n = col * s.group + o2 / h;
+      return;
+    }
+    default:  // MAP_MORTON: precomputed Z order of the tiles inside the grid
+      m = s.order[2 * i];
+      n = s.order[2 * i + 1];
+      return;
   }
 }
 
