@@ -424,3 +424,28 @@ def test_fixup_wait_rules_from_the_lock_section():
     assert S.fixup_wait(middle, "nondeterministic") == (">=", 1)    # workspace initialised
     assert S.fixup_wait(final, "nondeterministic") == ("==", 60)    # all earlier k-tiles in
     assert S.fixup_wait(final, "separate") is None
+
+
+def test_cost_model_terms_worked_by_hand():
+    from oracle import heuristic as H
+    # M = N = K = 4096, BM = BN = 128, cluster 1 x 1, BF16 in, BF16 out, 152 SMs:
+    #   blocks 32 * 32 = 1024, waves ceil(1024 / 152) = 7, efficiency 1024 / 1064
+    #   bytes_L2_AB = 4096 * (128 + 128) * 2 = 2 097 152 ; bytes_local_AB the same
+    #   bytes_TC = 4096 * (128 + 128) * 2 + 128 * 128 * 2 = 2 129 920 ; bytes_CD = 32 768
+    r = H.score(4096, 4096, 4096, 128, 128, 1, 1, 2, 2, 152)
+    assert (r["num_blocks"], r["num_waves"]) == (1024, 7)
+    assert r["wave_efficiency"] == 1024 / 1064
+    assert (r["bytes_l2_ab"], r["bytes_local_ab"], r["bytes_tc"], r["bytes_cd"]) == (2097152, 2097152, 2129920, 32768)
+    # a cluster of 2 along M halves the B share of the L2-side bytes, not the local ones
+    r2 = H.score(4096, 4096, 4096, 128, 128, 2, 1, 2, 2, 152)
+    assert r2["bytes_l2_ab"] == 4096 * (128 + 64) * 2 and r2["bytes_local_ab"] == r["bytes_local_ab"]
+    # max(64, BM): a 64-row block still pays 64 rows on the tensor-core side
+    assert H.score(4096, 4096, 4096, 64, 128, 1, 1, 2, 2, 152)["bytes_tc"] == 4096 * (64 + 128) * 2 + 64 * 128 * 2
+    # accumulating into C reads C as well
+    assert H.score(4096, 4096, 4096, 128, 128, 1, 1, 2, 2, 152, accumulate=True)["bytes_cd"] == 2 * 32768
+    # the page's trade-off: a wave-quantised grid loses to a full one of the same bytes
+    a = H.score(152 * 128, 128, 4096, 128, 128, 1, 1, 2, 2, 152)       # exactly one wave
+    b = H.score(153 * 128, 128, 4096, 128, 128, 1, 1, 2, 2, 152)       # one block spills to a 2nd wave
+    # 152 blocks fill one wave; 153 need two half-empty ones: same bytes per block, twice the score
+    assert a["wave_efficiency"] == 1.0 and b["wave_efficiency"] == 153 / 304
+    assert abs(b["score"] / a["score"] - 2.0) < 1e-12
