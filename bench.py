@@ -345,6 +345,50 @@ def run_mapping_study(args):
         print(json.dumps(row), flush=True)
 
 
+CONFIG_STUDY_SHAPES = [(8192, 8192, 8192), (4096, 4096, 4096), (2048, 2048, 2048), (16384, 4096, 4096),
+                       (1920, 1920, 16384), (512, 8192, 8192), (8192, 512, 8192), (3000, 700, 1024),
+                       (256, 256, 256)]
+
+
+def run_config_study(args):
+    """Measured TFLOPS of every (tile width, CTA group) candidate per shape, next to the plan's
+    automatic (cost-model) pick: BF16 in, BF16 out, grouped-M G=8, persistent."""
+    import torch
+    import tile_scheduled_tensor_gb300 as tst
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for (M, N, K) in CONFIG_STUDY_SHAPES:
+        inp = make_gemm_inputs(M, N, K, "bf16", "normal", case=2)
+        A = torch.from_numpy(inp.A.view(np.int16)).cuda()
+        B = torch.from_numpy(inp.B.view(np.int16)).cuda()
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        res = {}
+        auto = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent", out_dtype="bf16")
+        pick = (int(auto.info.bn), int(auto.info.cta_group))
+        for bn in (128, 256):
+            for cg in (1, 2):
+                if cg == 2 and M <= 128:
+                    continue
+                plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent",
+                                            out_dtype="bf16", bn=bn, cta_group=cg)
+                for _ in range(args.warmup):
+                    tst.gemm_run(plan, A, B, C)
+                times = []
+                for _ in range(args.steps):
+                    flush.fill_(1.0)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    tst.gemm_run(plan, A, B, C)
+                    e1.record()
+                    times.append((e0, e1))
+                torch.cuda.synchronize()
+                ms = statistics.median(x.elapsed_time(y) for x, y in times)
+                res[f"{bn}x{cg}"] = round(2.0 * M * N * K / (ms / 1e3) / 1e12, 1)
+        best = max(res, key=res.get)
+        print(json.dumps({"shape": [M, N, K], "tflops_by_bn_x_ctagroup": res, "cost_model_pick": f"{pick[0]}x{pick[1]}",
+                          "best": best, "pick_over_best": round(res[f"{pick[0]}x{pick[1]}"] / res[best], 3)}),
+              flush=True)
+
+
 def run_role_cycles(args):
     """Per-CTA cycle counters from the kernel's debug mode: where each role waits."""
     import torch
@@ -405,6 +449,8 @@ def main():
                     help="override a plan option of the workload, e.g. --opt sk_groups=4 --opt bn=256")
     ap.add_argument("--mapping-study", action="store_true",
                     help="time every mapping family on the workload and print the operand-band model")
+    ap.add_argument("--config-study", action="store_true",
+                    help="time every tile width x CTA group on a set of shapes against the cost model's pick")
     ap.add_argument("--role-cycles", action="store_true",
                     help="instead of timing, print per-role wait/busy cycle fractions (debug counters) "
                          "for the listed workloads")
@@ -431,6 +477,8 @@ def main():
         return run_role_cycles(args)
     if args.mapping_study:
         return run_mapping_study(args)
+    if args.config_study:
+        return run_config_study(args)
 
     import torch
     import torch.distributed as dist

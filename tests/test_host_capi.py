@@ -191,8 +191,11 @@ def test_pair_plans_schedule_256_row_tiles_over_pairs():
 def test_auto_choices():
     big = tst.gemm_plan_create(8192, 8192, 8192, host_only=True, num_sms=152)
     assert (big.info.bn, big.info.cta_group) == (256, 2)
+    # 256^3: one wave whatever the tile; the cost model prefers the pair's smaller B share
     small = tst.gemm_plan_create(256, 256, 256, host_only=True, num_sms=152)
-    assert (small.info.bn, small.info.cta_group) == (128, 1)
+    assert (small.info.bn, small.info.cta_group) == (128, 2)
+    single = tst.gemm_plan_create(128, 256, 256, host_only=True, num_sms=152)
+    assert single.info.cta_group == 1   # a pair needs two 128-row blocks
     with pytest.raises(tst.TstError) as e:
         _host_plan(256, 256, 256, cta_group=3)
     assert e.value.status == tst.TST_ERR_UNSUPPORTED
@@ -234,3 +237,18 @@ def test_separate_reduction_slots_match_oracle(shape, sms, groups):
     with pytest.raises(tst.TstError) as e:
         _host_plan(M, N, K, schedule="streamk", sk_fixup=7)
     assert e.value.status == tst.TST_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shape", [(8192, 8192, 8192), (4096, 4096, 4096), (1920, 1920, 16384), (16384, 4096, 4096),
+                                   (256, 256, 256), (128, 4096, 4096), (2048, 2048, 2048), (512, 8192, 8192),
+                                   (3000, 700, 1024), (100, 100, 64)])
+@pytest.mark.parametrize("dtype,out", [("bf16", "bf16"), ("bf16", "f32"), ("e4m3", "bf16")])
+def test_auto_tile_matches_cost_model_oracle(shape, dtype, out):
+    from oracle import heuristic as H
+    M, N, K = shape
+    p = tst.gemm_plan_create(M, N, K, dtype=dtype, out_dtype=out, host_only=True, num_sms=152)
+    want_bn, want_cg = H.choose(M, N, K, 2 if dtype == "bf16" else 1, 4 if out == "f32" else 2, 152)
+    assert (p.info.bn, p.info.cta_group) == (want_bn, want_cg)
+    # fixing one of the two leaves the other to the model
+    q = tst.gemm_plan_create(M, N, K, dtype=dtype, out_dtype=out, host_only=True, num_sms=152, bn=128)
+    assert q.info.bn == 128

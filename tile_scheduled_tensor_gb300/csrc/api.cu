@@ -111,6 +111,58 @@ bool encode_operand(CUtensorMap* map, const void* ptr, tst_dtype dt, int64_t row
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Plan-time tile choice by the DeepGEMM configuration cost model ("Deep dive
+// into DeepGEMM", panel "Kernel Configuration Heuristic", step 2): for every
+// candidate block (BM = 128, BN in {128, 256}) and cluster (cluster_M = 2 is
+// the CTA pair, whose CTAs each load half of B), score =
+// max(cycles_local, cycles_L2) / wave_efficiency with
+//   cycles_L2    = (K (BM / cluster_N + BN / cluster_M) sizeof(AB) + BM BN sizeof(C)) blocks / BW_L2
+//   cycles_local = (K (BM + BN) sizeof(AB) + K (max(64, BM) + BN) sizeof(AB) + 2 BM BN sizeof(C))
+//                  blocks / BW_local
+// and the lowest score wins (ties: the larger block, then the pair).
+// BW_L2 ~ 17 TB/s of TMA reads from L2 at ~1.9 GHz (measured), BW_local =
+// 256 B per SM cycle, both in bytes per cycle for the whole GPU.
+struct TileChoice {
+  int32_t bn, cg;
+};
+
+double cost_model_score(int64_t M, int64_t N, int64_t K, int64_t BN, int64_t cluster_m, int64_t sizeof_ab,
+                        int64_t sizeof_c, int64_t num_sms) {
+  const int64_t BM = 128, cluster_n = 1;
+  const double blocks = static_cast<double>(ceil_div(M, BM) * ceil_div(N, BN));
+  const double waves = static_cast<double>(ceil_div(static_cast<int64_t>(blocks), num_sms));
+  const double wave_efficiency = blocks / (waves * static_cast<double>(num_sms));
+  const double bytes_l2_ab = static_cast<double>(K) * (static_cast<double>(BM) / cluster_n +
+                                                       static_cast<double>(BN) / cluster_m) * sizeof_ab;
+  const double bytes_local_ab = static_cast<double>(K) * (BM + BN) * sizeof_ab;
+  const double bytes_tc = static_cast<double>(K) * (std::max<int64_t>(64, BM) + BN) * sizeof_ab +
+                          static_cast<double>(BM * BN * sizeof_c);
+  const double bytes_cd = static_cast<double>(BM * BN * sizeof_c);
+  const double bw_l2 = 9000.0, bw_local = 256.0 * static_cast<double>(num_sms);
+  const double cycles_l2 = (bytes_l2_ab + bytes_cd) * blocks / bw_l2;
+  const double cycles_local = (bytes_local_ab + bytes_tc + bytes_cd) * blocks / bw_local;
+  return std::max(cycles_local, cycles_l2) / wave_efficiency;
+}
+
+TileChoice choose_tile(int64_t M, int64_t N, int64_t K, int64_t sizeof_ab, int64_t sizeof_c, int64_t num_sms,
+                       int32_t fixed_bn, int32_t fixed_cg) {
+  TileChoice best{128, 1};
+  double best_score = -1.0;
+  for (int32_t bn : {256, 128}) {
+    if (fixed_bn != 0 && bn != fixed_bn) continue;
+    for (int32_t cg : {2, 1}) {
+      if (fixed_cg != 0 && cg != fixed_cg) continue;
+      if (cg == 2 && M <= 128) continue;  // a pair needs two 128-row blocks
+      const double sc = cost_model_score(M, N, K, bn, cg, sizeof_ab, sizeof_c, num_sms);
+      if (best_score < 0 || sc < best_score * (1.0 - 1e-12)) {
+        best_score = sc;
+        best = {bn, cg};
+      }
+    }
+  }
+  return best;
+}
+
 // Hybrid rule: split only the tail wave, and only when it is at most half full.
 int64_t hybrid_split_tiles(int64_t T, int64_t P) {
   const int64_t tail = T % P;
@@ -191,17 +243,12 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   if (o.bk != 0 && o.bk != 128 / elt && o.bk != 256 / elt) { delete p; return TST_ERR_UNSUPPORTED; }
   p->ka = o.bk == 128 / elt ? 1 : 2;
   p->bk = p->ka * 128 / elt;
-  if (o.bn != 0) {
-    p->bn = o.bn;
-  } else {
-    // wide tiles when they still give at least one full wave of CTAs
-    p->bn = (N > 128 && ceil_div(M, 128) * ceil_div(N, 256) >= p->num_sms) ? 256 : 128;
-  }
-  if (o.cta_group != 0) {
-    p->cg = o.cta_group;
-  } else {
-    // pairs halve each CTA's share of B; use them when there is a full wave of pair tiles
-    p->cg = (M > 128 && ceil_div(M, 256) * ceil_div(N, p->bn) >= p->num_sms / 2) ? 2 : 1;
+  // tile width and CTA group: as given, else by the cost model
+  {
+    const TileChoice tc = choose_tile(M, N, K, elt, epi->out_dtype == TST_OUT_F32 ? 4 : 2, p->num_sms, o.bn,
+                                      o.cta_group);
+    p->bn = o.bn != 0 ? o.bn : tc.bn;
+    p->cg = o.cta_group != 0 ? o.cta_group : tc.cg;
   }
   p->bm = tst::kBlockM * p->cg;
   const int64_t mt = ceil_div(M, p->bm);
