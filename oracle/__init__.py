@@ -7,9 +7,12 @@ this package never imports the product: the two share no code.  The seeded
 input generator (`synthetic`) is the only module both sides use.
 
 Parts:
-  * gemm_ref.c  - exact BF16 / e4m3 decode, FP64 GEMM with the fused epilogue,
+  * gemm_ref.c  - exact BF16 / e4m3 / e5m2 decode, FP64 GEMM with the fused epilogue,
                   FP64 -> BF16 round-to-nearest-even (built into liboracle.so
                   by build_oracle(); plain C, OpenMP over rows).
+  * epilogue.py - the extended fused epilogue in the pages' order (alpha, beta*C,
+                  vector scales, row/column bias, ReLU/GELU/SiLU, amax, output
+                  scale, FP8 e4m3 output encoding), FP64 on the raw accumulator.
   * schedule.py - mappings F(i) -> (m, n), static / persistent / Stream-K work
                   lists, wave efficiency, operand band counts.
 Every function cites the passage it follows in its own source file.
@@ -22,14 +25,14 @@ import subprocess
 
 import numpy as np
 
-from . import schedule  # noqa: F401  (re-exported)
+from . import epilogue, schedule  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_ref.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-BF16, E4M3 = 0, 1
+BF16, E4M3, E5M2 = 0, 1, 2
 
 
 def build_oracle(force: bool = False) -> str:
@@ -52,12 +55,14 @@ def _load():
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
         lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_e5m2.restype = ctypes.c_double
+        lib.oracle_decode_e5m2.argtypes = [ctypes.c_uint8]
         lib.oracle_round_bf16.restype = ctypes.c_uint16
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_decode_array.restype = None
         lib.oracle_decode_array.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         lib.oracle_gemm_rows.restype = None
-        lib.oracle_gemm_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+        lib.oracle_gemm_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                          ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
@@ -70,11 +75,13 @@ def _dtype_code(dtype) -> int:
         return BF16
     if dtype in (E4M3, "e4m3"):
         return E4M3
+    if dtype in (E5M2, "e5m2"):
+        return E5M2
     raise ValueError(dtype)
 
 
 def decode(codes: np.ndarray, dtype) -> np.ndarray:
-    """Exact FP64 values of BF16 (uint16) or e4m3 (uint8) codes."""
+    """Exact FP64 values of BF16 (uint16), e4m3 or e5m2 (uint8) codes."""
     d = _dtype_code(dtype)
     want = np.uint16 if d == BF16 else np.uint8
     c = np.ascontiguousarray(codes, dtype=want)
@@ -91,13 +98,17 @@ def round_bf16(z: np.ndarray) -> np.ndarray:
 
 
 def gemm(A: np.ndarray, B: np.ndarray, dtype, alpha: float = 1.0, scales=None, bias=None,
-         relu: bool = False, rows=None):
+         relu: bool = False, rows=None, dtype_b=None):
     """z (FP64, unrounded, after the epilogue) and absdot = |alpha sA sB| * sum_k |a||b|.
 
-    A: (M, K) codes, B: (N, K) codes.  rows: optional row indices to compute.
+    A: (M, K) codes of `dtype`, B: (N, K) codes of `dtype_b` (default: the same;
+    the FP8 formats may be mixed).  rows: optional row indices to compute.
     Returns arrays of shape (len(rows) or M, N).
     """
     d = _dtype_code(dtype)
+    db = d if dtype_b is None else _dtype_code(dtype_b)
+    if (d == BF16) != (db == BF16):
+        raise ValueError("BF16 pairs only with BF16")
     want = np.uint16 if d == BF16 else np.uint8
     A = np.ascontiguousarray(A, dtype=want)
     B = np.ascontiguousarray(B, dtype=want)
@@ -113,7 +124,7 @@ def gemm(A: np.ndarray, B: np.ndarray, dtype, alpha: float = 1.0, scales=None, b
     bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
     z = np.empty((nrows, N), dtype=np.float64)
     ad = np.empty((nrows, N), dtype=np.float64)
-    _load().oracle_gemm_rows(M, N, K, d, A.ctypes.data, B.ctypes.data, rows_ptr, nrows,
+    _load().oracle_gemm_rows(M, N, K, d, db, A.ctypes.data, B.ctypes.data, rows_ptr, nrows,
                              float(alpha), sA, sB,
                              None if bias_arr is None else bias_arr.ctypes.data, int(bool(relu)),
                              z.ctypes.data, ad.ctypes.data)

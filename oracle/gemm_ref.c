@@ -37,7 +37,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORACLE_BF16 = 0, ORACLE_E4M3 = 1 };
+enum { ORACLE_BF16 = 0, ORACLE_E4M3 = 1, ORACLE_E5M2 = 2 };
 
 /* BF16: 1 sign bit, 8 exponent bits (bias 127), 7 mantissa bits.  The upper
  * half of an IEEE binary32. */
@@ -73,8 +73,29 @@ double oracle_decode_e4m3(uint8_t code) {
     return sign ? -v : v;
 }
 
+/* FP8 e5m2: 1 sign bit, 5 exponent bits (bias 15), 2 mantissa bits ("H100 .
+ * WGMMA Part 2", section 9, and the Hopper summary of "H100 . Kernel Design":
+ * wider range, less precision than e4m3).  It keeps the IEEE special values:
+ * exponent field 31 is infinity (mantissa 0) or NaN; largest finite
+ * 1.75 * 2^15 = 57344; subnormals 0.m * 2^-14. */
+double oracle_decode_e5m2(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 2) & 0x1F;
+    int m = code & 0x3;
+    double v;
+    if (e == 0x1F) {
+        v = (m == 0) ? INFINITY : NAN;
+    } else if (e == 0) {
+        v = ldexp((double)m, -14 - 2);
+    } else {
+        v = ldexp(1.0 + (double)m / 4.0, e - 15);
+    }
+    return sign ? -v : v;
+}
+
 static double decode(int dtype, const void *base, int64_t idx) {
     if (dtype == ORACLE_BF16) return oracle_decode_bf16(((const uint16_t *)base)[idx]);
+    if (dtype == ORACLE_E5M2) return oracle_decode_e5m2(((const uint8_t *)base)[idx]);
     return oracle_decode_e4m3(((const uint8_t *)base)[idx]);
 }
 
@@ -106,12 +127,13 @@ uint16_t oracle_round_bf16(double x) {
 }
 
 /*
- * Rows rows[0..nrows) of the GEMM plus epilogue.  z_out and absdot_out are
+ * Rows rows[0..nrows) of the GEMM plus epilogue.  A holds dtype_a codes and B
+ * dtype_b codes (the two FP8 formats may be mixed).  z_out and absdot_out are
  * nrows x N row-major (FP64).  absdot[r][j] = sum_k |alpha sA sB| |a_ik| |b_jk|,
  * the scale the error bound is quoted against.
  * rows == NULL means rows 0..nrows-1.
  */
-void oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int dtype,
+void oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int dtype_a, int dtype_b,
                       const void *A, const void *B,
                       const int64_t *rows, int64_t nrows,
                       double alpha, double sA, double sB,
@@ -121,14 +143,14 @@ void oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int dtype,
     /* exact decode of B once (N x K doubles); A rows decoded as used */
     double *Bd = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
     for (int64_t j = 0; j < N; ++j)
-        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode(dtype, B, j * K + k);
+        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode(dtype_b, B, j * K + k);
     const double scale = alpha * sA * sB;
 
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t r = 0; r < nrows; ++r) {
         int64_t i = rows ? rows[r] : r;
         double *Ad = (double *)malloc(sizeof(double) * (size_t)K);
-        for (int64_t k = 0; k < K; ++k) Ad[k] = decode(dtype, A, i * K + k);
+        for (int64_t k = 0; k < K; ++k) Ad[k] = decode(dtype_a, A, i * K + k);
         for (int64_t j = 0; j < N; ++j) {
             const double *b = Bd + j * K;
             double acc = 0.0, aacc = 0.0;

@@ -31,6 +31,7 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 def splitmix64(seed: int, count: int, offset: int = 0) -> np.ndarray:
@@ -89,42 +90,82 @@ def bf16_bits(x: np.ndarray) -> np.ndarray:
     return rounded.astype(np.uint16)
 
 
+def _fp8_bytes(x32: np.ndarray, mbits: int, ebias: int, vmax: float) -> np.ndarray:
+    """FP32 values -> FP8 codes with `mbits` mantissa bits and exponent bias `ebias`,
+    round-to-nearest-even, saturating to +-vmax (the largest finite value)."""
+    v = np.asarray(x32, dtype=np.float32).astype(np.float64)
+    sign = (v < 0) | ((v == 0) & np.signbit(v))
+    a = np.minimum(np.abs(v), vmax)
+    emin = 1 - ebias                       # exponent of the smallest normal
+    # exponent of a (for a in the normal range); frexp gives a = f * 2^e, f in [0.5, 1)
+    _, e = np.frexp(a)
+    e = e.astype(np.int64) - 1  # a = 1.xxx * 2^e
+    e = np.maximum(e, emin)     # below 2^emin the spacing stays 2^(emin - mbits) (subnormals)
+    step = np.ldexp(1.0, (e - mbits).astype(np.int32))
+    q = np.rint(a / step) * step  # np.rint rounds half to even
+    q = np.minimum(q, vmax)
+    # back to a code
+    _, e2 = np.frexp(q)
+    e2 = e2.astype(np.int64) - 1
+    normal_ = q >= 2.0 ** emin
+    exp_field = np.where(normal_, e2 + ebias, 0)
+    mant = np.where(normal_, q / np.ldexp(1.0, e2.astype(np.int32)) - 1.0, q / 2.0 ** (emin - mbits))
+    mant = np.where(normal_, mant * (1 << mbits), mant)
+    code = (exp_field.astype(np.int64) << mbits) | np.rint(mant).astype(np.int64)
+    code = np.where(q == 0, 0, code)
+    code = code | (sign.astype(np.int64) << 7)
+    return code.astype(np.uint8)
+
+
 def e4m3_bytes(x32: np.ndarray) -> np.ndarray:
     """FP32 values -> e4m3 bytes, round-to-nearest-even, saturating to +-448.
 
     e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field
     0 is subnormal (value m * 2^-9); the all-ones pattern S.1111.111 is NaN.
     """
-    v = np.asarray(x32, dtype=np.float32).astype(np.float64)
-    sign = (v < 0) | ((v == 0) & np.signbit(v))
-    a = np.minimum(np.abs(v), E4M3_MAX)
-    # exponent of a (for a in the normal range); frexp gives a = f * 2^e, f in [0.5, 1)
-    _, e = np.frexp(a)
-    e = e.astype(np.int64) - 1  # a = 1.xxx * 2^e
-    e = np.maximum(e, -6)  # below 2^-6 the spacing stays 2^-9 (subnormals)
-    step = np.ldexp(1.0, (e - 3).astype(np.int32))
-    q = np.rint(a / step) * step  # np.rint rounds half to even
-    q = np.minimum(q, E4M3_MAX)
-    # back to a code
-    _, e2 = np.frexp(q)
-    e2 = e2.astype(np.int64) - 1
-    normal_ = q >= 2.0 ** -6
-    exp_field = np.where(normal_, e2 + 7, 0)
-    mant = np.where(normal_, q / np.ldexp(1.0, e2.astype(np.int32)) - 1.0, q / 2.0 ** -9)
-    mant = np.where(normal_, mant * 8.0, mant)
-    code = (exp_field.astype(np.int64) << 3) | np.rint(mant).astype(np.int64)
-    code = np.where(q == 0, 0, code)
-    code = code | (sign.astype(np.int64) << 7)
-    return code.astype(np.uint8)
+    return _fp8_bytes(x32, 3, 7, E4M3_MAX)
+
+
+def e5m2_bytes(x32: np.ndarray) -> np.ndarray:
+    """FP32 values -> e5m2 bytes, round-to-nearest-even, saturating to +-57344.
+
+    e5m2: 1 sign bit, 5 exponent bits (bias 15), 2 mantissa bits; exponent field
+    0 is subnormal (value m * 2^-16); exponent field 31 holds infinity and NaN,
+    which saturation never produces.
+    """
+    return _fp8_bytes(x32, 2, 15, E5M2_MAX)
+
+
+def _fp8_quantise(x: np.ndarray, encode, vmax: float):
+    x32 = np.asarray(x, dtype=np.float32)
+    amax = float(np.max(np.abs(x32))) if x32.size else 0.0
+    scale = np.float32(amax) / np.float32(vmax) if amax > 0 else np.float32(1.0)
+    scale = np.float32(scale)
+    return encode(x32 / scale), scale
 
 
 def e4m3_quantise(x: np.ndarray):
     """Tensor-wise FP8 quantisation: returns (bytes, scale) with x ~ scale * decode(bytes)."""
-    x32 = np.asarray(x, dtype=np.float32)
-    amax = float(np.max(np.abs(x32))) if x32.size else 0.0
-    scale = np.float32(amax) / np.float32(E4M3_MAX) if amax > 0 else np.float32(1.0)
-    scale = np.float32(scale)
-    return e4m3_bytes(x32 / scale), scale
+    return _fp8_quantise(x, e4m3_bytes, E4M3_MAX)
+
+
+def e5m2_quantise(x: np.ndarray):
+    """Tensor-wise e5m2 quantisation: returns (bytes, scale) with x ~ scale * decode(bytes)."""
+    return _fp8_quantise(x, e5m2_bytes, E5M2_MAX)
+
+
+# input element types: A's and B's format ("e4m3_e5m2" = A e4m3, B e5m2)
+DTYPES = ("bf16", "e4m3", "e5m2", "e4m3_e5m2", "e5m2_e4m3")
+
+
+def operand_types(dtype: str):
+    """(format of A, format of B) for a dtype name."""
+    if dtype not in DTYPES:
+        raise ValueError(dtype)
+    if "_" in dtype:
+        a, b = dtype.split("_")
+        return a, b
+    return dtype, dtype
 
 
 # Seeds per matrix: A = 1000 + c, B = 2000 + c, bias = 3000 + c, c = config number.
@@ -143,7 +184,7 @@ class GemmInputs:
 
 def make_gemm_inputs(M: int, N: int, K: int, dtype: str = "bf16", dist: str = "uniform",
                      case: int = 1, bias_dist: str | None = None, fp8_scaled: bool = True) -> GemmInputs:
-    """Seeded inputs for one GEMM case.  dtype 'bf16' or 'e4m3'.  With fp8_scaled=False the e4m3
+    """Seeded inputs for one GEMM case.  dtype one of DTYPES.  With fp8_scaled=False the e4m3
     bytes encode the drawn values directly (no tensor-wise scale; scales is None)."""
     xa = draw(dist, SEED_A + case, M * K).reshape(M, K)
     xb = draw(dist, SEED_B + case, N * K).reshape(N, K)
@@ -152,11 +193,11 @@ def make_gemm_inputs(M: int, N: int, K: int, dtype: str = "bf16", dist: str = "u
         bias = draw(bias_dist, SEED_BIAS + case, N).astype(np.float32)
     if dtype == "bf16":
         return GemmInputs(M, N, K, dtype, bf16_bits(xa), bf16_bits(xb), None, bias)
-    if dtype == "e4m3" and not fp8_scaled:
-        return GemmInputs(M, N, K, dtype, e4m3_bytes(xa.astype(np.float32)), e4m3_bytes(xb.astype(np.float32)),
+    fa, fb = operand_types(dtype)
+    enc = {"e4m3": (e4m3_bytes, e4m3_quantise), "e5m2": (e5m2_bytes, e5m2_quantise)}
+    if not fp8_scaled:
+        return GemmInputs(M, N, K, dtype, enc[fa][0](xa.astype(np.float32)), enc[fb][0](xb.astype(np.float32)),
                           None, bias)
-    if dtype == "e4m3":
-        qa, sa = e4m3_quantise(xa)
-        qb, sb = e4m3_quantise(xb)
-        return GemmInputs(M, N, K, dtype, qa, qb, np.array([sa, sb], dtype=np.float32), bias)
-    raise ValueError(dtype)
+    qa, sa = enc[fa][1](xa)
+    qb, sb = enc[fb][1](xb)
+    return GemmInputs(M, N, K, dtype, qa, qb, np.array([sa, sb], dtype=np.float32), bias)

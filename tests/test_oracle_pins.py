@@ -60,6 +60,28 @@ def test_e4m3_decode_all_codes_vs_torch_and_page_facts():
     assert d[1] == 2.0 ** -9 and d[0x08] == 2.0 ** -6
 
 
+def test_e5m2_decode_all_codes_vs_torch_and_format():
+    codes = np.arange(256, dtype=np.uint8)
+    d = oracle.decode(codes, "e5m2")
+    t = torch.from_numpy(codes.copy()).view(torch.float8_e5m2).double().numpy()
+    same = (d == t) | (np.isnan(d) & np.isnan(t))
+    assert same.all()
+    # 5 exponent bits (bias 15), 2 mantissa bits: largest finite 1.75 * 2^15, smallest
+    # subnormal 2^-16, smallest normal 2^-14; exponent field 31 is infinity or NaN
+    assert np.nanmax(d[np.isfinite(d)]) == 57344.0
+    assert d[1] == 2.0 ** -16 and d[0x04] == 2.0 ** -14
+    assert np.isinf(d[0x7C]) and np.isnan(d[0x7D:0x80]).all()
+
+
+def test_generator_e5m2_vs_torch_in_range_and_saturation():
+    x = (synthetic.normal(25, 20000) * np.exp(synthetic.uniform(26, 20000) * 9)).astype(np.float32)
+    inr = np.abs(x) < 57344.0
+    ref = torch.from_numpy(x[inr]).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(synthetic.e5m2_bytes(x[inr]), ref)
+    big = synthetic.e5m2_bytes(np.array([1e6, -1e6, 61000.0], dtype=np.float32))
+    assert oracle.decode(big, "e5m2").tolist() == [57344.0, -57344.0, 57344.0]
+
+
 def test_generator_e4m3_saturation_matches_page():
     _, rows = _golden("e4m3_facts.txt")
     for tag, x, want in rows:
@@ -122,16 +144,17 @@ def test_gemm_identity_and_permutation_exact():
     assert np.array_equal(zp, Bd.T[perm])               # row i of C = row perm[i] of B^T
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3", "e5m2", "e4m3_e5m2", "e5m2_e4m3"])
 def test_gemm_small_integers_exact_vs_int64(dtype):
     M, N, K = 37, 29, 131
+    # e5m2 holds every integer up to 8 exactly (2 mantissa bits: 5, 6, 7 = 1.25, 1.5, 1.75 x 4)
     a = synthetic.draw("int:8", 21, M * K).reshape(M, K)
     b = synthetic.draw("int:8", 22, N * K).reshape(N, K)
-    if dtype == "bf16":
-        A, B = synthetic.bf16_bits(a), synthetic.bf16_bits(b)
-    else:
-        A, B = synthetic.e4m3_bytes(a.astype(np.float32)), synthetic.e4m3_bytes(b.astype(np.float32))
-    z, ad = oracle.gemm(A, B, dtype)
+    fa, fb = synthetic.operand_types(dtype)
+    enc = {"bf16": synthetic.bf16_bits, "e4m3": lambda x: synthetic.e4m3_bytes(x.astype(np.float32)),
+           "e5m2": lambda x: synthetic.e5m2_bytes(x.astype(np.float32))}
+    A, B = enc[fa](a), enc[fb](b)
+    z, ad = oracle.gemm(A, B, fa, dtype_b=fb)
     ref = a.astype(np.int64) @ b.astype(np.int64).T
     assert np.array_equal(z, ref.astype(np.float64))
     assert np.array_equal(ad, (np.abs(a).astype(np.int64) @ np.abs(b).astype(np.int64).T).astype(np.float64))
