@@ -119,6 +119,7 @@ uint16_t oracle_round_bf16(double x) {
     if (b < -126) b = -126;
     double step = ldexp(1.0, b - 7);
     double r = nearbyint(a / step) * step;  /* ties to even (default mode) */
+    if (r == 0.0) return sign;              /* below half the smallest subnormal: signed zero */
     if (r >= ldexp(1.0, 128)) return sign | 0x7F80;
     frexp(r, &e);
     b = e - 1;

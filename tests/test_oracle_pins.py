@@ -90,6 +90,18 @@ def test_generator_e4m3_saturation_matches_page():
         assert oracle.decode(code, "e4m3")[0] == float(want)
 
 
+def test_round_bf16_tiny_and_subnormal_vs_torch():
+    # subnormal BF16 spacing is 2^-133; below half of it a value rounds to a signed zero
+    x = np.concatenate([synthetic.uniform(13, 4000) * 2.0 ** -120, synthetic.uniform(14, 1000) * 2.0 ** -133,
+                        np.array([2.0 ** -134, 3 * 2.0 ** -135, 1e-80, -1e-80, -2.0 ** -133, 2.0 ** -126])])
+    x32 = x.astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x32.astype(np.float32)).bfloat16().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.round_bf16(x32), ref)
+    assert oracle.round_bf16(np.array([1e-80]))[0] == 0x0000 and oracle.round_bf16(np.array([-1e-80]))[0] == 0x8000
+    # 2^-134 is halfway between 0 and 2^-133: ties to the even code 0
+    assert oracle.round_bf16(np.array([2.0 ** -134]))[0] == 0x0000
+
+
 def test_round_bf16_vs_torch_and_hand_ties():
     x = synthetic.normal(11, 20000) * np.exp(synthetic.uniform(12, 20000) * 20)
     x32 = x.astype(np.float32).astype(np.float64)  # exactly representable in FP32: torch rounds once
