@@ -5,7 +5,8 @@
  *
  *     C[i][j] = out_cast( act( alpha * sA * sB * sum_k A[i][k] * B[j][k] + bias[j] ) )
  *
- * with BF16 or FP8-e4m3 inputs and FP32 accumulation, computed on one GPU by
+ * (or the extended epilogue of tst_epilogue_ex) with BF16 or FP8 (e4m3, e5m2)
+ * inputs and FP32 accumulation, computed on one GPU by
  * hand-written sm_103a kernels (TMA producer warp, tcgen05.mma issuer with the
  * accumulator in Tensor Memory, epilogue warps).  The GEMM is cut into output
  * tiles; a mapping F(i) -> (m, n) says which tile is linear task i, and a
@@ -22,15 +23,17 @@
  *     notes, Lesson 8), sections 9.2-9.4 and 10.1-10.3.
  *   - Stream-K units, splits, K_idx, is_final_split, the fixup lock:
  *     "H100 . Stream-K scheduling" (same course, Lesson 8.1), sections 2-6.
- *   - Epilogue order Z = alpha*Acc -> + bias -> activation -> cast:
- *     "H100 . Kernel Design", section 12.2.
- *   - FP8 tensor-wise scales: "H100 . WGMMA Part 2" (Lesson 7), section 11.
+ *   - Epilogue operations and order Z = alpha*Acc + beta*C -> + bias ->
+ *     activation -> output scale / amax -> cast: "H100 . Kernel Design",
+ *     sections 12.1-12.2.
+ *   - FP8 formats and tensor-wise / vector-wise scales: "H100 . WGMMA Part 2"
+ *     (Lesson 7), sections 9-11.
  *
  * Conventions for every call:
  *   - Pointers named A, B, C, bias, scales are DEVICE pointers owned by the
  *     caller; they must stay valid until the stream work that uses them ends.
  *   - A is M x K row-major (K contiguous), B is N x K row-major (K contiguous),
- *     C is M x N row-major.  BF16 elements are 2 bytes, e4m3 1 byte.
+ *     C is M x N row-major.  BF16 elements are 2 bytes, FP8 1 byte.
  *   - Every call returns a tst_status; nothing aborts the process or prints
  *     (unless the environment variable TST_LOG=1 is set).
  *   - gemm_run is asynchronous and ordered on the given stream.
@@ -58,11 +61,21 @@ typedef enum {
     TST_ERR_NO_DEVICE = 8      /* the plan was built host-only, or no GPU is present */
 } tst_status;
 
-/* input element type */
-typedef enum { TST_BF16 = 0, TST_E4M3 = 1 } tst_dtype;
+/* input element types of A and B.  The FP8 formats ("H100 . WGMMA Part 2",
+ * sections 9 and 14): e4m3 (4 exponent bits, 3 mantissa bits, largest finite 448,
+ * no infinity) and e5m2 (5 exponent bits, 2 mantissa bits, largest finite 57344);
+ * A and B may hold different FP8 formats.  Every FP8 code is one byte. */
+typedef enum {
+    TST_BF16 = 0,
+    TST_E4M3 = 1,
+    TST_E5M2 = 2,
+    TST_E4M3_E5M2 = 3,   /* A e4m3, B e5m2 */
+    TST_E5M2_E4M3 = 4    /* A e5m2, B e4m3 */
+} tst_dtype;
 
-/* output element type */
-typedef enum { TST_OUT_F32 = 0, TST_OUT_BF16 = 1 } tst_out_dtype;
+/* output element type.  TST_OUT_E4M3 rounds to nearest even and saturates to
+ * +-448 (the clamping mode of "H100 . WGMMA Part 2", section 10). */
+typedef enum { TST_OUT_F32 = 0, TST_OUT_BF16 = 1, TST_OUT_E4M3 = 2 } tst_out_dtype;
 
 /* A M x K (K contiguous), B N x K (K contiguous), C M x N row-major ("TN").
  * e4m3 tensor-core operands must be K-major, which this layout is. */
@@ -119,6 +132,55 @@ typedef struct {
     int32_t relu;        /* 1: apply max(z, 0) after the bias */
     int32_t use_scales;  /* 1: scales is an FP32 device array {sA, sB} folded into alpha */
 } tst_epilogue;
+
+/* Extended fused epilogue, the operations and order of "H100 . Kernel Design"
+ * (Lesson 8), sections 12.1-12.2.  For output element (i, j):
+ *
+ *   Z = alpha * sA * sB * row_scale[i] * col_scale[j] * Acc + beta * C[i][j]
+ *   Z = Z + bias[j]  (TST_BIAS_COL)   or   Z + bias[i]  (TST_BIAS_ROW)
+ *   aux[i][j] = Z                                    (when aux is set)
+ *   Y = activation(Z)
+ *   amax = max over all (i, j) of |Y|                (when amax is set)
+ *   D[i][j] = cast(d_scale * Y)
+ *
+ * Absent factors are 1 and absent terms 0.  activation: identity, ReLU
+ * max(z, 0), GELU z * Phi(z) (Phi the standard normal CDF), SiLU z / (1 + e^-z).
+ * All arithmetic is FP32.  Here C is the page's addend matrix; the result D is
+ * what the other calls name C. */
+typedef enum { TST_ACT_NONE = 0, TST_ACT_RELU = 1, TST_ACT_GELU = 2, TST_ACT_SILU = 3 } tst_activation;
+typedef enum { TST_BIAS_NONE = 0, TST_BIAS_COL = 1, TST_BIAS_ROW = 2 } tst_bias_mode;
+
+typedef struct {
+    int32_t out_dtype;   /* tst_out_dtype of D */
+    float alpha;
+    float beta;          /* multiplies C when has_c */
+    int32_t has_c;       /* 1: add beta * C, C an M x N row-major matrix of c_dtype */
+    int32_t c_dtype;     /* TST_OUT_F32 or TST_OUT_BF16 */
+    int32_t bias_mode;   /* tst_bias_mode: FP32[N] per column or FP32[M] per row */
+    int32_t activation;  /* tst_activation */
+    int32_t use_scales;  /* 1: tensor-wise FP32[2] = {sA, sB} */
+    int32_t row_scale;   /* 1: FP32[M], one scale per row of A ("vector-wise", WGMMA Part 2 s. 11) */
+    int32_t col_scale;   /* 1: FP32[N], one scale per row of B, i.e. per column of D */
+    int32_t d_scale;     /* 1: FP32[1] output scale multiplying Y before the cast */
+    int32_t amax;        /* 1: write max |Y| (before d_scale) to an FP32[1] */
+    int32_t aux;         /* 1: also store Z (before the activation) to an M x N matrix */
+    int32_t aux_dtype;   /* TST_OUT_F32 or TST_OUT_BF16 */
+} tst_epilogue_ex;
+
+/* Run-time operands of the extended epilogue: DEVICE pointers owned by the
+ * caller; NULL where the plan's tst_epilogue_ex does not use them.  c, aux and
+ * every FP32 vector must be 16-byte aligned.  amax is overwritten: the run first
+ * sets it to 0, then every output element max-combines |Y| into it. */
+typedef struct {
+    const void *c;          /* M x N, c_dtype */
+    const float *bias;      /* FP32[N] or FP32[M] */
+    const float *scales;    /* FP32[2] = {sA, sB} */
+    const float *row_scale; /* FP32[M] */
+    const float *col_scale; /* FP32[N] */
+    const float *d_scale;   /* FP32[1] */
+    float *amax;            /* FP32[1], written */
+    void *aux;              /* M x N, aux_dtype, written */
+} tst_epilogue_args;
 
 /* Optional plan settings.  Zero-initialise and set what you need. */
 typedef struct {
@@ -210,6 +272,22 @@ tst_status gemm_plan_create_ex(tst_plan **plan, int64_t M, int64_t N, int64_t K,
                                tst_dtype dtype, tst_layout layout, tst_mapping mapping,
                                tst_schedule schedule, const tst_epilogue *epi,
                                const tst_plan_options *opts);
+
+/* gemm_plan_create_ex with the extended epilogue.  gemm_plan_create_ex is this
+ * call with alpha, a column bias, ReLU and the tensor-wise scales only.
+ * Errors as gemm_plan_create_ex, and INVALID_ARG for an unknown out_dtype,
+ * c_dtype, aux_dtype, bias_mode or activation. */
+tst_status gemm_plan_create_epi(tst_plan **plan, int64_t M, int64_t N, int64_t K,
+                                tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                                tst_schedule schedule, const tst_epilogue_ex *epi,
+                                const tst_plan_options *opts);
+
+/* Launch the GEMM with the extended epilogue's operands (see gemm_run).
+ * Errors: INVALID_ARG (null A, B, D or args, or a NULL pointer the plan's
+ * epilogue needs), ALIGNMENT, NO_DEVICE, CUDA.  gemm_run(plan, A, B, D, bias,
+ * scales, stream) is this call with only bias and scales set. */
+tst_status gemm_run_epi(tst_plan *plan, const void *A, const void *B, void *D,
+                        const tst_epilogue_args *args, void *stream);
 
 /* Launch the GEMM on `stream` (a cudaStream_t; NULL = legacy default stream).
  * A, B, C: device pointers, 16-byte aligned.  bias: FP32[N] when epi.has_bias,

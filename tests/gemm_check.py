@@ -85,8 +85,9 @@ def to_device(inp):
 
 
 def oracle_rows(inp, w, rows=None):
-    return oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
-                       relu=w.get("relu", False), rows=rows)
+    fa, fb = synthetic.operand_types(inp.dtype)
+    return oracle.gemm(inp.A, inp.B, fa, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
+                       relu=w.get("relu", False), rows=rows, dtype_b=fb)
 
 
 def assert_close(out_vals, z, absdot, out, what=""):
@@ -111,8 +112,9 @@ def sample_rows(M: int, BM: int = 128, count: int = 24, seed: int = 5):
 
 def freivalds(inp, w, C_vals: np.ndarray, seed: int = 99):
     """Whole-matrix check: |C x - alpha sA sB A (B^T x) - bias.x| within the sum of element bounds."""
-    a = oracle.decode(inp.A, inp.dtype)
-    b = oracle.decode(inp.B, inp.dtype)
+    fa, fb = synthetic.operand_types(inp.dtype)
+    a = oracle.decode(inp.A, fa)
+    b = oracle.decode(inp.B, fb)
     x = synthetic.uniform(seed, inp.N)
     s = w.get("alpha", 1.0)
     if inp.scales is not None:

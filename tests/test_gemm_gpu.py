@@ -26,12 +26,12 @@ SCHEDULES = ["static", "persistent", "streamk", "streamk_hybrid"]
 
 
 def _gemm(M, N, K, dtype="bf16", dist="normal", case=11, out="f32", bias_dist=None, **plan_kw):
-    scaled = plan_kw.get("use_scales", dtype == "e4m3")
+    scaled = plan_kw.get("use_scales", dtype != "bf16")
     inp = synthetic.make_gemm_inputs(M, N, K, dtype, dist, case=case, bias_dist=bias_dist, fp8_scaled=scaled)
     w = dict(M=M, N=N, K=K, dtype=dtype, out=out, mapping=plan_kw.pop("mapping", ("linear_nfast", 1)),
              schedule=plan_kw.pop("schedule", "static"), bn=plan_kw.pop("bn", 128),
              alpha=plan_kw.pop("alpha", 1.0), relu=plan_kw.pop("relu", False),
-             use_scales=plan_kw.pop("use_scales", dtype == "e4m3"), bias_dist=bias_dist)
+             use_scales=plan_kw.pop("use_scales", dtype != "bf16"), bias_dist=bias_dist)
     plan = plan_for(w, **plan_kw)
     C = run_gemm(plan, inp, out)
     return inp, w, plan, C
@@ -104,32 +104,48 @@ def test_small_integers_bf16_output_exact():
     assert np.array_equal(host_values(C), z)
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3", "e5m2", "e5m2_e4m3", "e4m3_e5m2"])
 def test_decode_probe_every_code_exact(dtype):
     """Row r of A holds code r at k = 0; B is one-hot on k = 0: C[r, 0] = dec(code r) exactly.
-    Covers subnormals (checks that the tensor core keeps them)."""
-    if dtype == "bf16":
+    Covers subnormals (checks that the tensor core keeps them) and, for the mixed FP8
+    types, that A and B are decoded in their own formats."""
+    fa, fb = synthetic.operand_types(dtype)
+    if fa == "bf16":
         codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
         finite = np.isfinite(oracle.decode(codes, "bf16"))
         # products with 1.0 of FP32-range values stay exact in the FP32 accumulator
         codes = codes[finite]
     else:
         codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
-        codes = codes[np.isfinite(oracle.decode(codes, "e4m3"))]
-    M, K, N = codes.size, (64 if dtype == "bf16" else 128), 16
+        codes = codes[np.isfinite(oracle.decode(codes, fa))]
+    M, K, N = codes.size, (64 if fa == "bf16" else 128), 16
     A = np.zeros((M, K), dtype=codes.dtype)
     A[:, 0] = codes
     B = np.zeros((N, K), dtype=codes.dtype)
-    one = synthetic.bf16_bits(np.array([1.0])) if dtype == "bf16" else synthetic.e4m3_bytes(np.array([1.0], np.float32))
-    B[0, 0] = one[0]
-    inp = synthetic.GemmInputs(M, N, K, dtype, A, B, np.array([1, 1], np.float32) if dtype == "e4m3" else None, None)
+    enc = {"bf16": lambda v: synthetic.bf16_bits(np.array([v])),
+           "e4m3": lambda v: synthetic.e4m3_bytes(np.array([v], np.float32)),
+           "e5m2": lambda v: synthetic.e5m2_bytes(np.array([v], np.float32))}
+    B[0, 0] = enc[fb](1.0)[0]
+    inp = synthetic.GemmInputs(M, N, K, dtype, A, B, None if fa == "bf16" else np.array([1, 1], np.float32), None)
     w = dict(M=M, N=N, K=K, dtype=dtype, out="f32", mapping=("linear_nfast", 1), schedule="persistent", bn=128,
              use_scales=False)
     C = host_values(run_gemm(plan_for(w), inp, "f32"))
-    want = oracle.decode(codes, dtype)
+    want = oracle.decode(codes, fa)
     got = C[:, 0]
     assert np.array_equal(got, want), f"first mismatch at code {codes[np.argmax(got != want)]:#x}"
     assert (C[:, 1:] == 0).all()
+    if fa != fb:
+        # the other way round: B's row j holds code j, A is one-hot
+        codes_b = np.arange(256, dtype=np.uint16).astype(np.uint8)
+        codes_b = codes_b[np.isfinite(oracle.decode(codes_b, fb))]
+        A2 = np.zeros((16, K), dtype=np.uint8)
+        A2[0, 0] = enc[fa](1.0)[0]
+        B2 = np.zeros((codes_b.size, K), dtype=np.uint8)
+        B2[:, 0] = codes_b
+        inp2 = synthetic.GemmInputs(16, codes_b.size, K, dtype, A2, B2, np.array([1, 1], np.float32), None)
+        w2 = dict(w, M=16, N=codes_b.size)
+        C2 = host_values(run_gemm(plan_for(w2), inp2, "f32"))
+        assert np.array_equal(C2[0], oracle.decode(codes_b, fb))
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])

@@ -11,7 +11,10 @@ from __future__ import annotations
 import ctypes
 
 from . import _capi
-from ._capi import (TST_BF16, TST_E4M3, TST_OUT_F32, TST_OUT_BF16, TST_LAYOUT_A_ROW_B_NK,  # noqa: F401
+from ._capi import (TST_BF16, TST_E4M3, TST_E5M2, TST_E4M3_E5M2, TST_E5M2_E4M3,  # noqa: F401
+                    TST_OUT_F32, TST_OUT_BF16, TST_OUT_E4M3, TST_LAYOUT_A_ROW_B_NK,
+                    TST_ACT_NONE, TST_ACT_RELU, TST_ACT_GELU, TST_ACT_SILU, TST_BIAS_NONE, TST_BIAS_COL,
+                    TST_BIAS_ROW,
                     TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N,
                     TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID,
                     TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG_ROLE_CYCLES,
@@ -22,8 +25,11 @@ from ._capi import (TST_BF16, TST_E4M3, TST_OUT_F32, TST_OUT_BF16, TST_LAYOUT_A_
 
 lib = _capi.load()
 
-_DTYPES = {"bf16": TST_BF16, "e4m3": TST_E4M3}
-_OUT = {"f32": TST_OUT_F32, "bf16": TST_OUT_BF16}
+_DTYPES = {"bf16": TST_BF16, "e4m3": TST_E4M3, "e5m2": TST_E5M2, "e4m3_e5m2": TST_E4M3_E5M2,
+           "e5m2_e4m3": TST_E5M2_E4M3}
+_OUT = {"f32": TST_OUT_F32, "bf16": TST_OUT_BF16, "e4m3": TST_OUT_E4M3}
+_ACT = {"none": TST_ACT_NONE, "relu": TST_ACT_RELU, "gelu": TST_ACT_GELU, "silu": TST_ACT_SILU}
+_BIAS = {"none": TST_BIAS_NONE, "col": TST_BIAS_COL, "row": TST_BIAS_ROW}
 _MAPS = {"linear_nfast": TST_MAP_LINEAR_NFAST, "linear_mfast": TST_MAP_LINEAR_MFAST,
          "grouped_m": TST_MAP_GROUPED_M, "grouped_n": TST_MAP_GROUPED_N,
          "block_2d": _capi.TST_MAP_BLOCK_2D, "morton": _capi.TST_MAP_MORTON}
@@ -84,18 +90,41 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      out_dtype="f32", alpha: float = 1.0, has_bias: bool = False, relu: bool = False,
                      use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_forward: bool = False,
                      host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
-                     stages: int = 0, bk: int = 0, sk_groups: int = 0, sk_fixup="deterministic") -> Plan:
+                     stages: int = 0, bk: int = 0, sk_groups: int = 0, sk_fixup="deterministic",
+                     beta: float = 0.0, has_c: bool = False, c_dtype="f32", bias_mode=None, activation=None,
+                     row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
+                     amax: bool = False, aux: bool = False, aux_dtype="f32") -> Plan:
+    """Plan C = epilogue(A x B).  The basic epilogue is alpha, a column bias (has_bias),
+    ReLU and the tensor-wise scales; any of beta/has_c, bias_mode='row', activation
+    'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux or out_dtype 'e4m3' selects
+    the extended one (gemm_plan_create_epi)."""
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
-    epi = _capi.tst_epilogue(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), int(bool(has_bias)),
-                             int(bool(relu)), int(bool(use_scales)))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
                                   int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
                                   int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"))
+    bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
+        (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
+    act = _enum(_ACT, activation, "activation") if activation is not None else \
+        (TST_ACT_RELU if relu else TST_ACT_NONE)
+    extended = bool(has_c or bmode == TST_BIAS_ROW or act in (TST_ACT_GELU, TST_ACT_SILU) or row_scale or
+                    col_scale or d_scale or amax or aux)
     h = ctypes.c_void_p()
-    _check(lib.gemm_plan_create_ex(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
-                                   TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),
-                                   ctypes.byref(epi), ctypes.byref(opts)), "gemm_plan_create")
+    if extended:
+        epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), float(beta),
+                                    int(bool(has_c)), _enum(_OUT, c_dtype, "c_dtype"), bmode, act,
+                                    int(bool(use_scales)), int(bool(row_scale)), int(bool(col_scale)),
+                                    int(bool(d_scale)), int(bool(amax)), int(bool(aux)),
+                                    _enum(_OUT, aux_dtype, "aux_dtype"))
+        _check(lib.gemm_plan_create_epi(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
+                                        TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),
+                                        ctypes.byref(epi), ctypes.byref(opts)), "gemm_plan_create_epi")
+    else:
+        epi = _capi.tst_epilogue(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), int(bmode == TST_BIAS_COL),
+                                 int(act == TST_ACT_RELU), int(bool(use_scales)))
+        _check(lib.gemm_plan_create_ex(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
+                                       TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),
+                                       ctypes.byref(epi), ctypes.byref(opts)), "gemm_plan_create")
     info = _capi.tst_plan_info()
     _check(lib.gemm_plan_get_info(h, ctypes.byref(info)), "gemm_plan_get_info")
     return Plan(h.value, info)
@@ -145,10 +174,19 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def gemm_run(plan: Plan, A, B, C, bias=None, scales=None, stream=None):
-    """Enqueue C = epilogue(A x B) on `stream` (default: torch's current stream)."""
-    _check(lib.gemm_run(plan._h, _ptr(A), _ptr(B), _ptr(C), _ptr(bias), _ptr(scales), _stream(stream)),
-           "gemm_run")
+def gemm_run(plan: Plan, A, B, C, bias=None, scales=None, stream=None, c=None, row_scale=None, col_scale=None,
+             d_scale=None, amax=None, aux=None):
+    """Enqueue C = epilogue(A x B) on `stream` (default: torch's current stream).  The
+    extended epilogue's operands (c: the addend of beta * C; row_scale, col_scale,
+    d_scale, amax, aux) go through gemm_run_epi."""
+    if all(x is None for x in (c, row_scale, col_scale, d_scale, amax, aux)):
+        _check(lib.gemm_run(plan._h, _ptr(A), _ptr(B), _ptr(C), _ptr(bias), _ptr(scales), _stream(stream)),
+               "gemm_run")
+        return
+    args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux))
+    _check(lib.gemm_run_epi(plan._h, _ptr(A), _ptr(B), _ptr(C), ctypes.byref(args), _stream(stream)),
+           "gemm_run_epi")
 
 
 def gemm_status_query(plan: Plan):

@@ -18,8 +18,10 @@ TST_ERR_TIMEOUT = 6
 TST_ERR_DEVICE_CHECK = 7
 TST_ERR_NO_DEVICE = 8
 
-TST_BF16, TST_E4M3 = 0, 1
-TST_OUT_F32, TST_OUT_BF16 = 0, 1
+TST_BF16, TST_E4M3, TST_E5M2, TST_E4M3_E5M2, TST_E5M2_E4M3 = 0, 1, 2, 3, 4
+TST_OUT_F32, TST_OUT_BF16, TST_OUT_E4M3 = 0, 1, 2
+TST_ACT_NONE, TST_ACT_RELU, TST_ACT_GELU, TST_ACT_SILU = 0, 1, 2, 3
+TST_BIAS_NONE, TST_BIAS_COL, TST_BIAS_ROW = 0, 1, 2
 TST_LAYOUT_A_ROW_B_NK = 0
 TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N = 0, 1, 2, 3
 TST_MAP_BLOCK_2D, TST_MAP_MORTON = 4, 5
@@ -35,6 +37,20 @@ class tst_mapping(ctypes.Structure):
 class tst_epilogue(ctypes.Structure):
     _fields_ = [("out_dtype", ctypes.c_int32), ("alpha", ctypes.c_float), ("has_bias", ctypes.c_int32),
                 ("relu", ctypes.c_int32), ("use_scales", ctypes.c_int32)]
+
+
+class tst_epilogue_ex(ctypes.Structure):
+    _fields_ = [("out_dtype", ctypes.c_int32), ("alpha", ctypes.c_float), ("beta", ctypes.c_float),
+                ("has_c", ctypes.c_int32), ("c_dtype", ctypes.c_int32), ("bias_mode", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("use_scales", ctypes.c_int32), ("row_scale", ctypes.c_int32),
+                ("col_scale", ctypes.c_int32), ("d_scale", ctypes.c_int32), ("amax", ctypes.c_int32),
+                ("aux", ctypes.c_int32), ("aux_dtype", ctypes.c_int32)]
+
+
+class tst_epilogue_args(ctypes.Structure):
+    _fields_ = [("c", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p), ("d_scale", ctypes.c_void_p),
+                ("amax", ctypes.c_void_p), ("aux", ctypes.c_void_p)]
 
 
 class tst_plan_options(ctypes.Structure):
@@ -68,7 +84,11 @@ _SIGNATURES = {
     "gemm_plan_create_ex": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                            ctypes.c_int, ctypes.c_int, tst_mapping, ctypes.c_int,
                                            ctypes.POINTER(tst_epilogue), ctypes.POINTER(tst_plan_options)]),
+    "gemm_plan_create_epi": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_int, ctypes.c_int, tst_mapping, ctypes.c_int,
+                                            ctypes.POINTER(tst_epilogue_ex), ctypes.POINTER(tst_plan_options)]),
     "gemm_run": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
+    "gemm_run_epi": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(tst_epilogue_args), _P]),
     "gemm_tile_map": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
                                      ctypes.POINTER(ctypes.c_int32)]),
     "gemm_plan_get_info": (ctypes.c_int, [_P, ctypes.POINTER(tst_plan_info)]),

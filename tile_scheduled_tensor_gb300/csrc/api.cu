@@ -29,7 +29,9 @@ struct tst_plan {
   tst_dtype dtype = TST_BF16;
   tst_mapping mapping{};
   tst_schedule schedule = TST_STATIC;
-  tst_epilogue epi{};
+  tst_epilogue_ex epi{};       // the epilogue (the basic one is a special case)
+  bool ext_on = false;         // epilogue needs more than alpha, column bias, ReLU, scales
+  uint32_t fmt_ab = 0;         // FP8 operand formats for the instruction descriptor
   tst_plan_options opts{};
   int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
   int32_t cg = 1;              // CTAs per scheduling unit (2 = CTA pair)
@@ -111,6 +113,9 @@ bool encode_operand(CUtensorMap* map, const void* ptr, tst_dtype dt, int64_t row
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// template output type of the kernel instance a plan launches
+int kernel_out(const tst_plan& p) { return p.epi.out_dtype == TST_OUT_BF16 ? tst::OUT_BF16 : tst::OUT_F32; }
+
 // Plan-time tile choice by the DeepGEMM configuration cost model ("Deep dive
 // into DeepGEMM", panel "Kernel Configuration Heuristic", step 2): for every
 // candidate block (BM = 128, BN in {128, 256}) and cluster (cluster_M = 2 is
@@ -189,20 +194,47 @@ const char* gemm_status_string(tst_status s) {
   return "TST_ERR_UNKNOWN";
 }
 
-tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
-                               tst_mapping mapping, tst_schedule schedule, const tst_epilogue* epi,
-                               const tst_plan_options* opts) {
+}  // extern "C"
+
+namespace {
+
+// element type codes of the extended epilogue's matrices
+bool valid_out(int32_t t) { return t == TST_OUT_F32 || t == TST_OUT_BF16 || t == TST_OUT_E4M3; }
+bool valid_in(int32_t t) { return t == TST_OUT_F32 || t == TST_OUT_BF16; }
+int out_bytes(int32_t t) { return t == TST_OUT_F32 ? 4 : t == TST_OUT_BF16 ? 2 : 1; }
+
+// whether the epilogue needs more than the basic alpha / column bias / ReLU / scales path
+bool needs_ext(const tst_epilogue_ex& e) {
+  return e.out_dtype == TST_OUT_E4M3 || e.has_c || e.bias_mode == TST_BIAS_ROW ||
+         (e.activation != TST_ACT_NONE && e.activation != TST_ACT_RELU) || e.row_scale || e.col_scale ||
+         e.d_scale || e.amax || e.aux;
+}
+
+// FP8 operand formats of a dtype in the instruction descriptor: A bits 7-9, B bits 10-12,
+// 0 = e4m3, 1 = e5m2
+uint32_t fp8_formats(tst_dtype d) {
+  const uint32_t a = (d == TST_E5M2 || d == TST_E5M2_E4M3) ? 1u : 0u;
+  const uint32_t b = (d == TST_E5M2 || d == TST_E4M3_E5M2) ? 1u : 0u;
+  return (a << 7) | (b << 10);
+}
+
+tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
+                       tst_mapping mapping, tst_schedule schedule, const tst_epilogue_ex* epi,
+                       const tst_plan_options* opts) {
   if (out == nullptr) return TST_ERR_INVALID_ARG;
   *out = nullptr;
   if (epi == nullptr || M <= 0 || N <= 0 || K <= 0) return TST_ERR_INVALID_ARG;
   if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return TST_ERR_INVALID_ARG;
-  if (dtype != TST_BF16 && dtype != TST_E4M3) return TST_ERR_INVALID_ARG;
+  if (dtype < TST_BF16 || dtype > TST_E5M2_E4M3) return TST_ERR_INVALID_ARG;
   if (mapping.kind < TST_MAP_LINEAR_NFAST || mapping.kind > TST_MAP_MORTON) return TST_ERR_INVALID_ARG;
   if ((mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N || mapping.kind == TST_MAP_BLOCK_2D) &&
       mapping.group < 1)
     return TST_ERR_INVALID_ARG;
   if (schedule < TST_STATIC || schedule > TST_STREAMK_HYBRID) return TST_ERR_INVALID_ARG;
-  if (epi->out_dtype != TST_OUT_F32 && epi->out_dtype != TST_OUT_BF16) return TST_ERR_INVALID_ARG;
+  if (!valid_out(epi->out_dtype)) return TST_ERR_INVALID_ARG;
+  if ((epi->has_c && !valid_in(epi->c_dtype)) || (epi->aux && !valid_in(epi->aux_dtype))) return TST_ERR_INVALID_ARG;
+  if (epi->bias_mode < TST_BIAS_NONE || epi->bias_mode > TST_BIAS_ROW) return TST_ERR_INVALID_ARG;
+  if (epi->activation < TST_ACT_NONE || epi->activation > TST_ACT_SILU) return TST_ERR_INVALID_ARG;
   if (layout != TST_LAYOUT_A_ROW_B_NK) return TST_ERR_UNSUPPORTED;
   tst_plan_options o{};
   if (opts) o = *opts;
@@ -215,6 +247,8 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   if (!p) return TST_ERR_OOM;
   p->M = M; p->N = N; p->K = K;
   p->dtype = dtype; p->mapping = mapping; p->schedule = schedule; p->epi = *epi; p->opts = o;
+  p->ext_on = needs_ext(*epi);
+  p->fmt_ab = dtype == TST_BF16 ? 0u : fp8_formats(dtype);
   p->host_only = o.host_only != 0;
   if (o.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(o.timeout_ns);
 
@@ -245,8 +279,7 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   p->bk = p->ka * 128 / elt;
   // tile width and CTA group: as given, else by the cost model
   {
-    const TileChoice tc = choose_tile(M, N, K, elt, epi->out_dtype == TST_OUT_F32 ? 4 : 2, p->num_sms, o.bn,
-                                      o.cta_group);
+    const TileChoice tc = choose_tile(M, N, K, elt, out_bytes(epi->out_dtype), p->num_sms, o.bn, o.cta_group);
     p->bn = o.bn != 0 ? o.bn : tc.bn;
     p->cg = o.cta_group != 0 ? o.cta_group : tc.cg;
   }
@@ -263,7 +296,8 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
   }
   p->smem_bytes = tst_kernel_smem_bytes(p->bn, p->cg, p->ka);
   if (!p->host_only) {
-    p->kernel = tst_kernel(dtype, p->bn, epi->out_dtype, p->cg, p->ka);
+    // the extended epilogue stores D through its own typed path, so any instance serves it
+    p->kernel = tst_kernel(dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3, p->bn, kernel_out(*p), p->cg, p->ka);
     if (!p->kernel ||
         cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) != cudaSuccess) {
       cudaGetLastError();
@@ -413,7 +447,7 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
       }
     }
     if (p->sk_mode == TST_SK_SEPARATE && s.sk_tiles > 0) {
-      p->reduce_kernel = tst_reduce_kernel(epi->out_dtype);
+      p->reduce_kernel = tst_reduce_kernel(kernel_out(*p));
       if (!p->reduce_kernel) {
         cudaFree(p->dev_block);
         delete p;
@@ -430,6 +464,31 @@ tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, 
             p->max_items, p->dev_bytes);
   *out = p;
   return TST_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tst_status gemm_plan_create_epi(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
+                                tst_mapping mapping, tst_schedule schedule, const tst_epilogue_ex* epi,
+                                const tst_plan_options* opts) {
+  return create_plan(out, M, N, K, dtype, layout, mapping, schedule, epi, opts);
+}
+
+tst_status gemm_plan_create_ex(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
+                               tst_mapping mapping, tst_schedule schedule, const tst_epilogue* epi,
+                               const tst_plan_options* opts) {
+  if (out == nullptr) return TST_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (epi == nullptr) return TST_ERR_INVALID_ARG;
+  tst_epilogue_ex e{};
+  e.out_dtype = epi->out_dtype;
+  e.alpha = epi->alpha;
+  e.bias_mode = epi->has_bias ? TST_BIAS_COL : TST_BIAS_NONE;
+  e.activation = epi->relu ? TST_ACT_RELU : TST_ACT_NONE;
+  e.use_scales = epi->use_scales;
+  return create_plan(out, M, N, K, dtype, layout, mapping, schedule, &e, opts);
 }
 
 tst_status gemm_plan_create(tst_plan** plan, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
@@ -515,14 +574,34 @@ tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int6
 
 tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const float* bias, const float* scales,
                     void* stream_) {
-  if (p == nullptr || A == nullptr || B == nullptr || C == nullptr) return TST_ERR_INVALID_ARG;
+  tst_epilogue_args a{};
+  a.bias = bias;
+  a.scales = scales;
+  return gemm_run_epi(p, A, B, C, &a, stream_);
+}
+
+tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
+                        void* stream_) {
+  if (p == nullptr || A == nullptr || B == nullptr || C == nullptr || ea == nullptr) return TST_ERR_INVALID_ARG;
   if (p->host_only || p->kernel == nullptr) return TST_ERR_NO_DEVICE;
-  if (p->epi.has_bias && bias == nullptr) return TST_ERR_INVALID_ARG;
-  if (p->epi.use_scales && scales == nullptr) return TST_ERR_INVALID_ARG;
+  const tst_epilogue_ex& e = p->epi;
+  const bool has_bias = e.bias_mode != TST_BIAS_NONE;
+  if ((has_bias && ea->bias == nullptr) || (e.use_scales && ea->scales == nullptr) ||
+      (e.has_c && ea->c == nullptr) || (e.row_scale && ea->row_scale == nullptr) ||
+      (e.col_scale && ea->col_scale == nullptr) || (e.d_scale && ea->d_scale == nullptr) ||
+      (e.amax && ea->amax == nullptr) || (e.aux && ea->aux == nullptr))
+    return TST_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return TST_ERR_ALIGNMENT;
-  if ((p->epi.has_bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
-      (p->epi.use_scales && (reinterpret_cast<uintptr_t>(scales) & 3u)))
+  if ((has_bias && (reinterpret_cast<uintptr_t>(ea->bias) & 3u)) ||
+      (e.use_scales && (reinterpret_cast<uintptr_t>(ea->scales) & 3u)))
     return TST_ERR_ALIGNMENT;
+  if (p->ext_on && ((has_bias && !aligned16(ea->bias)) || (e.has_c && !aligned16(ea->c)) ||
+                    (e.row_scale && !aligned16(ea->row_scale)) || (e.col_scale && !aligned16(ea->col_scale)) ||
+                    (e.d_scale && !aligned16(ea->d_scale)) || (e.amax && !aligned16(ea->amax)) ||
+                    (e.aux && !aligned16(ea->aux))))
+    return TST_ERR_ALIGNMENT;
+  const float* bias = has_bias ? ea->bias : nullptr;
+  const float* scales = e.use_scales ? ea->scales : nullptr;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
 
   // TMA boxes are per CTA and per swizzle atom: 128 bytes of K by 128 rows of A,
@@ -542,8 +621,8 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.tmap_a = p->tmap_a;
   kp.tmap_b = p->tmap_b;
   kp.C = C;
-  kp.bias = p->epi.has_bias ? bias : nullptr;
-  kp.scales = p->epi.use_scales ? scales : nullptr;
+  kp.bias = bias;
+  kp.scales = scales;
   kp.workspace = p->d_ws;
   kp.locks = p->d_locks;
   kp.status = p->d_status;
@@ -552,12 +631,29 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.M = static_cast<int32_t>(p->M);
   kp.N = static_cast<int32_t>(p->N);
   kp.K = static_cast<int32_t>(p->K);
-  kp.alpha = p->epi.alpha;
+  kp.alpha = e.alpha;
   kp.sched = p->sched;
   kp.sched.order = p->d_order;
-  kp.has_bias = p->epi.has_bias ? 1 : 0;
-  kp.relu = p->epi.relu ? 1 : 0;
-  kp.use_scales = p->epi.use_scales ? 1 : 0;
+  kp.has_bias = has_bias ? 1 : 0;
+  kp.relu = e.activation == TST_ACT_RELU ? 1 : 0;
+  kp.use_scales = e.use_scales ? 1 : 0;
+  kp.fmt_ab = p->fmt_ab;
+  if (p->ext_on) {
+    tst::EpiExt& x = kp.ext;
+    x.on = 1;
+    x.out_type = e.out_dtype;
+    x.act = e.activation;
+    x.bias_mode = e.bias_mode;
+    x.c_type = e.c_dtype;
+    x.aux_type = e.aux_dtype;
+    x.beta = e.beta;
+    x.c_in = e.has_c ? ea->c : nullptr;
+    x.row_scale = e.row_scale ? ea->row_scale : nullptr;
+    x.col_scale = e.col_scale ? ea->col_scale : nullptr;
+    x.d_scale = e.d_scale ? ea->d_scale : nullptr;
+    x.amax = e.amax ? ea->amax : nullptr;
+    x.aux = e.aux ? ea->aux : nullptr;
+  }
   kp.debug_flags = p->debug_flags;
   kp.max_items = p->max_items;
   kp.stages = p->stages;
@@ -565,8 +661,9 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   kp.sk_slots = p->sk_slots;
   kp.timeout_ns = p->timeout_ns;
 
-  // status word and Stream-K locks start at zero for every launch
+  // status word and Stream-K locks start at zero for every launch, and so does amax
   if (cudaMemsetAsync(p->dev_block, 0, p->reset_bytes, stream) != cudaSuccess) return TST_ERR_CUDA;
+  if (kp.ext.amax && cudaMemsetAsync(kp.ext.amax, 0, sizeof(float), stream) != cudaSuccess) return TST_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg), 1, 1);
@@ -601,7 +698,8 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
     rp.C = C;
     rp.bias = kp.bias;
     rp.scales = kp.scales;
-    rp.alpha = p->epi.alpha;
+    rp.alpha = e.alpha;
+    rp.ext = kp.ext;
     rp.M = kp.M;
     rp.N = kp.N;
     rp.bn = p->bn;

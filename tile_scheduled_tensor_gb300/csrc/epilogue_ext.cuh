@@ -1,0 +1,231 @@
+// Extended fused epilogue: the operations and order of "H100 . Kernel Design"
+// (runguoli.com H100 course notes, Lesson 8), sections 12.1-12.2, applied to W
+// consecutive accumulator columns of one output row held by one thread:
+//
+//   Z = alpha * sA * sB * s_row[i] * s_col[j] * Acc + beta * C[i][j]   (step 2)
+//   Z += bias[j] or bias[i]                                            (step 3)
+//   aux[i][j] = Z                              (optional, step 6: pre-activation)
+//   Y = act(Z), act in {identity, ReLU, GELU = x Phi(x), SiLU = x sigmoid(x)}
+//   amax = max(amax, |Y|)                                   (step 5, optional)
+//   D[i][j] = cast(d * Y), cast to FP32, BF16 (round to nearest even) or FP8
+//   e4m3 (round to nearest even, saturating to +-448: "H100 . WGMMA Part 2",
+//   section 10's clamping mode)                                       (step 7)
+//
+// All arithmetic is FP32.  Row-major matrices (C, aux, D) use 16-byte vector
+// accesses when the chunk is whole and every row starts 16-byte aligned;
+// per-column FP32 vectors use 16-byte loads that every lane of a warp shares.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kernel_params.h"
+
+namespace tst {
+namespace epi {
+
+// two FP32 values -> two e4m3 codes (first value in the low byte), round to
+// nearest even, saturating to the largest finite magnitude
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float first, float second) {
+  uint16_t r;
+  // cvt packs its first source into the upper byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+  return r;
+}
+
+__device__ __forceinline__ int elt_bytes(int type) { return type == OUT_F32 ? 4 : type == OUT_BF16 ? 2 : 1; }
+
+// whether row-major element (row, col0) of an N-column matrix of `type` starts a 16-byte unit
+__device__ __forceinline__ bool rows_vec_ok(int type, int32_t N) { return ((N * elt_bytes(type)) & 15) == 0; }
+
+template <int W>
+__device__ __forceinline__ void load_row(int type, const void* base, int32_t row, int32_t N, int32_t col0, bool full,
+                                         float* out) {
+  const int64_t off = static_cast<int64_t>(row) * N + col0;
+  if (type == OUT_F32) {
+    const float* src = static_cast<const float*>(base) + off;
+    if (full && rows_vec_ok(type, N)) {
+#pragma unroll
+      for (int q = 0; q < W / 4; ++q) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(src) + q);
+        out[4 * q] = t.x; out[4 * q + 1] = t.y; out[4 * q + 2] = t.z; out[4 * q + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j) out[j] = (col0 + j < N) ? __ldg(src + j) : 0.0f;
+    }
+  } else {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(base) + off;
+    if (full && rows_vec_ok(type, N) && W % 8 == 0) {
+#pragma unroll
+      for (int q = 0; q < W / 8; ++q) {
+        const uint4 t = __ldg(reinterpret_cast<const uint4*>(src) + q);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          out[8 * q + 2 * h] = __uint_as_float(w[h] << 16);
+          out[8 * q + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j) out[j] = (col0 + j < N) ? __bfloat162float(src[j]) : 0.0f;
+    }
+  }
+}
+
+template <int W>
+__device__ __forceinline__ void store_row(int type, void* base, int32_t row, int32_t N, int32_t col0, bool full,
+                                          const float* y) {
+  const int64_t off = static_cast<int64_t>(row) * N + col0;
+  const bool vec = full && rows_vec_ok(type, N);
+  if (type == OUT_F32) {
+    float* dst = static_cast<float*>(base) + off;
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < W / 4; ++q)
+        reinterpret_cast<float4*>(dst)[q] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j)
+        if (col0 + j < N) dst[j] = y[j];
+    }
+  } else if (type == OUT_BF16) {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(base) + off;
+    if (vec && W % 8 == 0) {
+#pragma unroll
+      for (int q = 0; q < W / 8; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          __nv_bfloat162 two = __floats2bfloat162_rn(y[8 * q + 2 * h], y[8 * q + 2 * h + 1]);
+          w[h] = *reinterpret_cast<uint32_t*>(&two);
+        }
+        reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else if (vec && W == 4) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(y[0], y[1]);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(y[2], y[3]);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j)
+        if (col0 + j < N) dst[j] = __float2bfloat16_rn(y[j]);
+    }
+  } else {  // OUT_E4M3
+    uint8_t* dst = static_cast<uint8_t*>(base) + off;
+    if (vec && W % 16 == 0) {
+#pragma unroll
+      for (int q = 0; q < W / 16; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float* s = y + 16 * q + 4 * h;
+          w[h] = static_cast<uint32_t>(cvt_e4m3x2(s[0], s[1])) | (static_cast<uint32_t>(cvt_e4m3x2(s[2], s[3])) << 16);
+        }
+        reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    } else if (full && W == 4 && ((N & 3) == 0)) {
+      *reinterpret_cast<uint32_t*>(dst) =
+          static_cast<uint32_t>(cvt_e4m3x2(y[0], y[1])) | (static_cast<uint32_t>(cvt_e4m3x2(y[2], y[3])) << 16);
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j)
+        if (col0 + j < N) dst[j] = static_cast<uint8_t>(cvt_e4m3x2(y[j], 0.0f) & 0xFFu);
+    }
+  }
+}
+
+// FP32 vector of length `len` (col0 a multiple of 4, base 16-byte aligned)
+template <int W>
+__device__ __forceinline__ void load_vec(const float* base, int32_t len, int32_t col0, bool full, float* out) {
+  if (full) {
+#pragma unroll
+    for (int q = 0; q < W / 4; ++q) {
+      const float4 t = __ldg(reinterpret_cast<const float4*>(base + col0) + q);
+      out[4 * q] = t.x; out[4 * q + 1] = t.y; out[4 * q + 2] = t.z; out[4 * q + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; ++j) out[j] = (col0 + j < len) ? __ldg(base + col0 + j) : 0.0f;
+  }
+}
+
+__device__ __forceinline__ float activate(int act, float z) {
+  switch (act) {
+    case ACT_RELU: return fmaxf(z, 0.0f);
+    case ACT_GELU: return z * normcdff(z);
+    case ACT_SILU: return z / (1.0f + expf(-z));
+    default: return z;
+  }
+}
+
+// Row constants of the extended epilogue: the accumulator scale of row `row`
+// (alpha, tensor-wise and row scales folded) and its row bias (0 without one).
+__device__ __forceinline__ void row_terms(const EpiExt& e, const float* bias, float alpha, int32_t M, int32_t row,
+                                          float& s_row, float& b_row) {
+  s_row = alpha;
+  b_row = 0.0f;
+  if (row < M) {
+    if (e.row_scale) s_row *= __ldg(e.row_scale + row);
+    if (e.bias_mode == BIAS_ROW) b_row = __ldg(bias + row);
+  }
+}
+
+// One chunk: W accumulator values v of row `row`, columns [col0, col0 + W).
+template <int W>
+__device__ __forceinline__ void chunk(const EpiExt& e, const float* bias, float s_row, float b_row, int32_t M,
+                                      int32_t N, int32_t row, int32_t col0, const float* v, void* D, float& amax) {
+  if (row >= M) return;
+  const bool full = col0 + W <= N;
+  float z[W];
+  if (e.col_scale) {
+    float cs[W];
+    load_vec<W>(e.col_scale, N, col0, full, cs);
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = (s_row * cs[j]) * v[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = s_row * v[j];
+  }
+  if (e.c_in != nullptr) {
+    float c[W];
+    load_row<W>(e.c_type, e.c_in, row, N, col0, full, c);
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = fmaf(e.beta, c[j], z[j]);
+  }
+  if (e.bias_mode == BIAS_COL) {
+    float b[W];
+    load_vec<W>(bias, N, col0, full, b);
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] += b[j];
+  } else if (e.bias_mode == BIAS_ROW) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] += b_row;
+  }
+  if (e.aux != nullptr) store_row<W>(e.aux_type, e.aux, row, N, col0, full, z);
+  float y[W];
+#pragma unroll
+  for (int j = 0; j < W; ++j) y[j] = activate(e.act, z[j]);
+  if (e.amax != nullptr) {
+#pragma unroll
+    for (int j = 0; j < W; ++j)
+      if (col0 + j < N) amax = fmaxf(amax, fabsf(y[j]));
+  }
+  if (e.d_scale != nullptr) {
+    const float d = __ldg(e.d_scale);
+#pragma unroll
+    for (int j = 0; j < W; ++j) y[j] *= d;
+  }
+  store_row<W>(e.out_type, D, row, N, col0, full, y);
+}
+
+// Combine a warp's amax into the global one (non-negative FP32 values order like
+// their bit patterns, so an unsigned atomic max is a float max).  The whole warp calls.
+__device__ __forceinline__ void amax_flush(const EpiExt& e, float amax) {
+  if (e.amax == nullptr) return;
+  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax));
+  if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(reinterpret_cast<unsigned int*>(e.amax), m);
+}
+
+}  // namespace epi
+}  // namespace tst

@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "epilogue_ext.cuh"
 #include "kernel_params.h"
 #include "ptx.cuh"
 
@@ -210,7 +211,8 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
                                         uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
                                         uint32_t bar_tempty, uint32_t bar_drain, int issuer) {
   using Cfg = TileCfg<BN, CG, KA>;
-  constexpr uint32_t kIdesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN);
+  // FP8: the operand formats (e4m3 / e5m2, possibly mixed) come from the plan
+  const uint32_t idesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN) | (DT == DT_BF16 ? 0u : p.fmt_ab);
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
@@ -249,11 +251,11 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
                                static_cast<uint64_t>(k >> 2) * static_cast<uint64_t>(Cfg::B_SUB >> 4);
         const uint32_t accumulate = Cfg::DUAL ? (i | (k & 3)) != 0 : (i | k) != 0;
         if (CG == 2) {
-          if (DT == DT_BF16) ptx::mma_f16_pair(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
-          else ptx::mma_f8_pair(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
+          if (DT == DT_BF16) ptx::mma_f16_pair(d_tmem, a_desc + off, b_desc + off_b, idesc, accumulate);
+          else ptx::mma_f8_pair(d_tmem, a_desc + off, b_desc + off_b, idesc, accumulate);
         } else {
-          if (DT == DT_BF16) ptx::mma_f16(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
-          else ptx::mma_f8(d_tmem, a_desc + off, b_desc + off_b, kIdesc, accumulate);
+          if (DT == DT_BF16) ptx::mma_f16(d_tmem, a_desc + off, b_desc + off_b, idesc, accumulate);
+          else ptx::mma_f8(d_tmem, a_desc + off, b_desc + off_b, idesc, accumulate);
         }
       }
       // stage free (in both CTAs of a pair) once these MMAs have read it
@@ -343,6 +345,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   long long wait_tfull = 0, busy = 0, items = 0;
+  float amax = 0.0f;  // extended epilogue: this thread's max |Y|
   while (work_next(p.sched, it, w)) {
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
     const bool final_split = (w.flags & ITEM_FINAL) != 0;
@@ -382,6 +385,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     const uint32_t t_row =
         tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
+    float s_row = alpha, b_row = 0.0f;  // extended epilogue: this row's accumulator scale and bias
+    if (p.ext.on) epi::row_terms(p.ext, p.bias, alpha, p.M, row, s_row, b_row);
 #pragma unroll 1
     for (int ch = 0; ch < BN / 64; ++ch) {
       float v[64];
@@ -430,6 +435,10 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
           for (int j = 0; j < 32; ++j) v[32 * h + j] = __ldcg(wsc + j * kBlockM) + v[32 * h + j];
         }
         const int32_t col0 = w.n * BN + c32 * 32;
+        if (p.ext.on) {
+          epi::chunk<32>(p.ext, p.bias, s_row, b_row, p.M, p.N, row, col0, v + 32 * h, p.C, amax);
+          continue;
+        }
         float z[32];
         if (p.has_bias) {
           float b[32];
@@ -472,6 +481,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
   }
+  // every epilogue thread leaves the loop in the same iteration, so each warp is whole here
+  if (p.ext.on) epi::amax_flush(p.ext, amax);
   if (p.stats && ep == 0) {
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_WAIT_TFULL] = wait_tfull;
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_BUSY] = busy;

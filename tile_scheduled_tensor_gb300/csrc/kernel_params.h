@@ -13,7 +13,29 @@ constexpr int kThreadsDual = 224;   // + warp 6: second MMA issuer (dual-issue t
 constexpr int kSmemLimit = 232448;  // 227 KiB opt-in dynamic shared memory per CTA
 
 enum DType : int32_t { DT_BF16 = 0, DT_E4M3 = 1 };
-enum OutType : int32_t { OUT_F32 = 0, OUT_BF16 = 1 };
+enum OutType : int32_t { OUT_F32 = 0, OUT_BF16 = 1, OUT_E4M3 = 2 };
+enum ActKind : int32_t { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2, ACT_SILU = 3 };
+enum BiasMode : int32_t { BIAS_NONE = 0, BIAS_COL = 1, BIAS_ROW = 2 };
+
+// Extended epilogue ("H100 . Kernel Design", sections 12.1-12.2).  on == 0
+// selects the basic alpha / column bias / ReLU path; otherwise these fields say
+// what the epilogue does (alpha, the tensor-wise scales and the bias pointer
+// stay in the parameter blocks below) and D's type is out_type.
+struct EpiExt {
+  int32_t on;
+  int32_t out_type;          // OutType of D
+  int32_t act;               // ActKind
+  int32_t bias_mode;         // BiasMode (bias FP32[N] per column or FP32[M] per row)
+  int32_t c_type;            // OUT_F32 / OUT_BF16: elements of C in beta * C
+  int32_t aux_type;          // OUT_F32 / OUT_BF16: elements of the aux output
+  float beta;
+  const void* c_in;          // M x N row-major, or null (no beta * C)
+  const float* row_scale;    // FP32[M] or null
+  const float* col_scale;    // FP32[N] or null
+  const float* d_scale;      // FP32[1] or null
+  float* amax;               // FP32[1] or null
+  void* aux;                 // M x N row-major (pre-activation Z), or null
+};
 
 // device status word: code (bits 0-7) | role (8-15) | CTA (16-31)
 enum StatusCode : uint32_t { ST_OK = 0, ST_TIMEOUT = 6, ST_DEVICE_CHECK = 7 };
@@ -58,6 +80,9 @@ struct KernelParams {
   int32_t sk_mode;          // SkFixup: how split tiles are combined
   int32_t sk_slots;         // partial-tile slots per split tile half (separate reduction)
   uint64_t timeout_ns;      // limit of every device-side wait
+  uint32_t fmt_ab;          // FP8 operand formats for the instruction descriptor: A in bits 7-9,
+                            // B in bits 10-12 (0 = e4m3, 1 = e5m2); 0 for BF16
+  EpiExt ext;               // extended epilogue (ext.on == 0: the basic one above)
 };
 
 // Tile configuration for a scheduled tile width BN, a CTA group of CG CTAs
@@ -136,6 +161,7 @@ struct ReduceParams {
   int32_t bn, cg, slots;
   int32_t has_bias, relu, use_scales;
   Sched sched;
+  EpiExt ext;
 };
 constexpr int kReduceThreads = 256;
 constexpr int kReduceRows = 16;  // rows of a 128-row tile half per CTA

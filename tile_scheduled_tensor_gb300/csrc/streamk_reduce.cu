@@ -3,8 +3,8 @@
 // units never wait on each other, each storing its FP32 partial tile in its own
 // slot; this kernel then sums the slots of every split tile in K order (the
 // order of the units' member numbers), applies the epilogue
-// alpha * sA * sB * acc + bias -> ReLU -> cast ("H100 . Kernel Design",
-// section 12.2) and writes C.
+// alpha * sA * sB * acc + bias -> ReLU -> cast, or the extended one
+// ("H100 . Kernel Design", sections 12.1-12.2), and writes C.
 //
 // Memory-bound: per split-tile half it reads its partial slots (128 x BN FP32
 // each) and writes one 128 x BN tile of C.  A CTA of 256 threads covers 16 rows
@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "epilogue_ext.cuh"
 #include "kernel_params.h"
 #include "tile_sched.h"
 
@@ -38,6 +39,7 @@ __global__ void __launch_bounds__(kReduceThreads) streamk_reduce_kernel(const __
   const int q_per_row = p.bn / 4;                       // float4 per row
   const int per_thread = kReduceRows * q_per_row / kReduceThreads;
   const float* base = p.workspace + static_cast<int64_t>(half) * p.slots * (kBlockM * p.bn);
+  float amax = 0.0f;
 
   for (int t = 0; t < per_thread; ++t) {
     const int q = threadIdx.x + t * kReduceThreads;
@@ -56,6 +58,12 @@ __global__ void __launch_bounds__(kReduceThreads) streamk_reduce_kernel(const __
     const int32_t col = n * p.bn + c4 * 4;
     if (row >= p.M) continue;
     float z[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (p.ext.on) {
+      float s_row, b_row;
+      epi::row_terms(p.ext, p.bias, alpha, p.M, row, s_row, b_row);
+      epi::chunk<4>(p.ext, p.bias, s_row, b_row, p.M, p.N, row, col, z, p.C, amax);
+      continue;
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float b = (p.has_bias && col + j < p.N) ? __ldg(p.bias + col + j) : 0.0f;
@@ -86,6 +94,8 @@ __global__ void __launch_bounds__(kReduceThreads) streamk_reduce_kernel(const __
       }
     }
   }
+  // the loop has no early exit, so every warp is whole here
+  if (p.ext.on) epi::amax_flush(p.ext, amax);
 }
 
 }  // namespace tst
