@@ -29,13 +29,13 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import make_gemm_inputs  # noqa: E402
+from synthetic import make_addend, make_gemm_inputs, operand_types  # noqa: E402
 from synthetic.workloads import WORKLOADS  # noqa: E402
 
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
 HEADLINE = "c2_bf16_4096"
 EXTRA = ["c1_bf16_256", "c2_bf16_4096_1cta", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
-         "c4_bf16_hybrid", "c5_bf16_epilogue"]
+         "c4_bf16_hybrid", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
     "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
@@ -47,9 +47,13 @@ DESCR = {
     "c4_bf16_persistent": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, grouped-M G=8 persistent",
     "c4_bf16_hybrid": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, data-parallel waves + Stream-K tail",
     "c5_bf16_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=bf16(ReLU(0.5 acc + bias)), grouped-M G=8",
+    "c6_bf16_fp8_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=e4m3(32 GELU(acc + C + bias)) with amax, "
+                            "C a BF16 N(0,1) addend, grouped-M G=8",
+    "c3m_e4m3_e5m2_8192": "FP8 GEMM 8192^3, A e4m3 x B e5m2, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, "
+                          "persistent",
 }
 L2_FLUSH_BYTES = 512 << 20
-KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h"]
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
 
 
 PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward")
@@ -61,6 +65,38 @@ def extra_plan_options(w):
 
 def flops(w):
     return 2.0 * w["M"] * w["N"] * w["K"]
+
+
+def is_fp8(w):
+    return w["dtype"] != "bf16"
+
+
+def oracle_step(w, inp, rows, addend=None):
+    """The oracle on output rows `rows` of workload w (FP64): the GEMM with its basic
+    epilogue, and for workloads with an extended epilogue its steps on top."""
+    import oracle
+    from oracle import epilogue as E
+    fa, fb = operand_types(inp.dtype)
+    epi = w.get("epi")
+    if epi is None:
+        return oracle.gemm(inp.A, inp.B, fa, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
+                           relu=w.get("relu", False), rows=rows, dtype_b=fb)
+    acc, ad = oracle.gemm(inp.A, inp.B, fa, rows=rows, dtype_b=fb)
+    e = E.Epilogue(alpha=w.get("alpha", 1.0), beta=epi.get("beta", 0.0), scales=inp.scales,
+                   c_in=addend, bias=inp.bias,
+                   bias_mode={"none": E.BIAS_NONE, "col": E.BIAS_COL, "row": E.BIAS_ROW}[epi.get("bias_mode", "none")],
+                   act={"none": E.ACT_NONE, "relu": E.ACT_RELU, "gelu": E.ACT_GELU,
+                        "silu": E.ACT_SILU}[epi.get("activation", "none")],
+                   d_scale=epi.get("d_scale", 1.0))
+    _, _, D, bz = E.apply(acc, ad, e, rows=rows)
+    return D, bz
+
+
+def addend_for(w):
+    epi = w.get("epi") or {}
+    if "c_dtype" not in epi:
+        return None, None
+    return make_addend(w["M"], w["N"], epi["c_dist"], w["case"], epi["c_dtype"])
 
 
 def aggregate(flops_per_rank: float, local_ms: float, world: int, max_reduce):
@@ -211,16 +247,14 @@ def setup_dist():
     return world, rank, local
 
 
-def cpu_oracle_rate(w, inp, budget_s=10.0, max_rows=None):
+def cpu_oracle_rate(w, inp, budget_s=10.0, max_rows=None, addend=None):
     """Time the oracle (as it stands) on whole output rows until ~budget_s of CPU work."""
-    import oracle
     rows_done, t_total, r0 = 0, 0.0, 0
     step = 4
     while t_total < budget_s and r0 < w["M"] and (max_rows is None or rows_done < max_rows):
         rows = np.arange(r0, min(r0 + step, w["M"]), dtype=np.int64)
         t0 = time.perf_counter()
-        oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
-                    relu=w.get("relu", False), rows=rows)
+        oracle_step(w, inp, rows, addend)
         dt = time.perf_counter() - t0
         t_total += dt
         rows_done += rows.size
@@ -240,17 +274,17 @@ def run_reference(args):
     w = WORKLOADS[args.workload]
     inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
                            bias_dist=w.get("bias_dist"))
+    _, addend = addend_for(w)
     rows_per_step = 8
     per_step_flops = 2.0 * rows_per_step * w["N"] * w["K"]
     for s in range(args.warmup):
-        oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
-                    relu=w.get("relu", False), rows=np.arange(s * rows_per_step, (s + 1) * rows_per_step) % w["M"])
+        oracle_step(w, inp, (np.arange(s * rows_per_step, (s + 1) * rows_per_step) % w["M"]).astype(np.int64),
+                    addend)
     times = []
     for s in range(args.steps):
         rows = (np.arange(rows_per_step) + (s + args.warmup) * rows_per_step) % w["M"]
         t0 = time.perf_counter()
-        oracle.gemm(inp.A, inp.B, inp.dtype, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
-                    relu=w.get("relu", False), rows=rows.astype(np.int64))
+        oracle_step(w, inp, rows.astype(np.int64), addend)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     value = per_step_flops / (ms / 1e3) / 1e12
@@ -501,11 +535,17 @@ def main():
         w = WORKLOADS[name]
         inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
                                bias_dist=w.get("bias_dist"))
+        epi = dict(w.get("epi") or {})
+        epi_plan = {k: epi[k] for k in ("beta", "c_dtype", "bias_mode", "activation", "amax") if k in epi}
+        if "c_dtype" in epi:
+            epi_plan["has_c"] = True
+        if "d_scale" in epi:
+            epi_plan["d_scale"] = True
         plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
                                     schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
                                     has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
                                     use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
-                                    cta_group=w.get("cta_group", 0), **extra_plan_options(w))
+                                    cta_group=w.get("cta_group", 0), **extra_plan_options(w), **epi_plan)
         a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
         b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
         host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory()}
@@ -513,14 +553,21 @@ def main():
             host["bias"] = torch.from_numpy(inp.bias).pin_memory()
         if inp.scales is not None:
             host["scales"] = torch.from_numpy(inp.scales).pin_memory()
+        if "c_dtype" in epi:
+            arr, _ = addend_for(w)
+            host["c"] = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr).pin_memory()
+        if "d_scale" in epi:
+            host["d_scale"] = torch.tensor([epi["d_scale"]], dtype=torch.float32).pin_memory()
         dev = {k: v.cuda() for k, v in host.items()}
-        cdt = torch.bfloat16 if w["out"] == "bf16" else torch.float32
+        if epi.get("amax"):
+            dev["amax"] = torch.zeros(4, dtype=torch.float32, device="cuda")
+        cdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8}[w["out"]]
         C = torch.empty(w["M"], w["N"], dtype=cdt, device="cuda")
         return w, inp, plan, host, dev, C
 
     def launch(plan, dev, C):
         tst.gemm_run(plan, dev["A"], dev["B"], C, bias=dev.get("bias"), scales=dev.get("scales"),
-                     stream=stream.cuda_stream)
+                     stream=stream.cuda_stream, c=dev.get("c"), d_scale=dev.get("d_scale"), amax=dev.get("amax"))
 
     def time_device(name, steps, warmup, sampler=None):
         w, inp, plan, host, dev, C = prepare(name)
@@ -595,8 +642,8 @@ def main():
     w = head["w"]
     fl = flops(w)
     value, ms_mean = aggregate(fl, sum(head["ms"]) / len(head["ms"]), world, max_over_ranks)
-    is_fp8 = w["dtype"] == "e4m3"
-    peak_tf = peaks["bf16_tflops"] * (2.0 if is_fp8 else 1.0)
+    fp8 = is_fp8(w)
+    peak_tf = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
     achieved = fl / (ms_mean / 1e3) / 1e12
     e2e_ms, h2d, d2h = time_e2e(head, max(3, args.steps // 2))
     e2e_ms = max_over_ranks(e2e_ms)
@@ -608,7 +655,7 @@ def main():
                 continue
             r = time_device(name, max(5, args.steps // 2), 3)
             ms = sum(r["ms"]) / len(r["ms"])
-            pk = peaks["bf16_tflops"] * (2.0 if r["w"]["dtype"] == "e4m3" else 1.0)
+            pk = peaks["bf16_tflops"] * (2.0 if is_fp8(r["w"]) else 1.0)
             tf = flops(r["w"]) / (ms / 1e3) / 1e12
             extra[name] = {"tflops": round(tf, 1), "ms": round(ms, 4), "frac_of_peak": round(tf / pk, 4),
                            "tiles": int(r["plan"].info.tiles), "grid": int(r["plan"].info.grid),
@@ -619,7 +666,7 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu:
-        rate, rows, secs = cpu_oracle_rate(w, head["inp"], budget_s=10.0)
+        rate, rows, secs = cpu_oracle_rate(w, head["inp"], budget_s=10.0, addend=addend_for(w)[1])
         cpu = {"value": rate, "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{rows} output rows x {w['N']} x K={w['K']} of {args.workload} in {secs:.1f} s "
                          f"(FP64, OpenMP over rows); TFLOPS scaled to 2*rows*N*K"}
@@ -628,7 +675,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e4m3" if is_fp8 else "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "M": w["M"], "N": w["N"],
                        "K": w["K"], "tile": f"{head['plan'].info.bm}x{head['plan'].info.bn}x{head['plan'].info.bk}",
                        "grid": int(head["plan"].info.grid), "stages": int(head["plan"].info.stages),
@@ -637,12 +684,12 @@ def main():
                        "parallelism": f"{world} independent problem(s), one per GPU"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                          "frac": achieved / peak_tf, "traffic": dram_traffic(args.workload),
-                         "peak_source": f"{peak_kind} bf16_tflops (burst)" + (" x2 nominal fp8/bf16 ratio" if is_fp8 else ""),
+                         "peak_source": f"{peak_kind} bf16_tflops (burst)" + (" x2 nominal fp8/bf16 ratio" if fp8 else ""),
                          "algorithmic_flops_per_launch": fl},
             "cpu_baseline": cpu,
             "e2e": {"value": world * fl / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * int(head["plan"].info.kernels_per_run),
             "clocks": head["clocks"],
             "workloads": extra,
             "kernel_hash": kernel_hash(),

@@ -168,8 +168,22 @@ def operand_types(dtype: str):
     return dtype, dtype
 
 
-# Seeds per matrix: A = 1000 + c, B = 2000 + c, bias = 3000 + c, c = config number.
-SEED_A, SEED_B, SEED_BIAS = 1000, 2000, 3000
+# Seeds per matrix: A = 1000 + c, B = 2000 + c, bias = 3000 + c, the epilogue's addend
+# matrix (beta * C) = 4000 + c, c = config number.
+SEED_A, SEED_B, SEED_BIAS, SEED_C = 1000, 2000, 3000, 4000
+
+
+def make_addend(M: int, N: int, dist: str, case: int, dtype: str = "bf16"):
+    """Seeded M x N addend matrix for beta * C: (array to upload, its FP64 values).
+    dtype 'bf16' gives BF16 bit patterns (uint16), 'f32' FP32 values."""
+    x = draw(dist, SEED_C + case, M * N).reshape(M, N)
+    if dtype == "bf16":
+        bits = bf16_bits(x)
+        return bits, (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if dtype == "f32":
+        x32 = x.astype(np.float32)
+        return x32, x32.astype(np.float64)
+    raise ValueError(dtype)
 
 
 class GemmInputs:

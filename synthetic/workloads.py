@@ -38,4 +38,15 @@ WORKLOADS = {
     "c5_bf16_epilogue": dict(M=16384, N=4096, K=4096, dtype="bf16", dist="normal:0.02", case=5, out="bf16",
                              mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2,
                              alpha=0.5, bias_dist="normal", relu=True),
+    # the same GEMM with the FP8 forward epilogue: Z = acc + 1.0 * C (BF16 addend, N(0,1)),
+    # + column bias N(0,1), GELU, amax, D = e4m3(32 * Y)
+    "c6_bf16_fp8_epilogue": dict(M=16384, N=4096, K=4096, dtype="bf16", dist="normal:0.02", case=6, out="e4m3",
+                                 mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2,
+                                 bias_dist="normal",
+                                 epi=dict(beta=1.0, c_dtype="bf16", c_dist="normal", bias_mode="col",
+                                          activation="gelu", amax=True, d_scale=32.0)),
+    # 8192^3 with mixed FP8 formats: A e4m3, B e5m2 (tensor-wise scales) -> BF16, grouped-N G=16
+    "c3m_e4m3_e5m2_8192": dict(M=8192, N=8192, K=8192, dtype="e4m3_e5m2", dist="normal", case=3, out="bf16",
+                               mapping=("grouped_n", 16), schedule="persistent", bn=256, cta_group=2,
+                               use_scales=True),
 }

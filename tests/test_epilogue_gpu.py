@@ -18,7 +18,8 @@ import synthetic
 import tile_scheduled_tensor_gb300 as tst
 from oracle import epilogue as E
 
-from gemm_check import device_codes, host_values
+from gemm_check import device_codes, host_values, sample_rows
+from synthetic.workloads import WORKLOADS
 
 pytestmark = pytest.mark.gpu
 
@@ -265,3 +266,45 @@ def test_run_epi_rejects_missing_and_misaligned_operands():
     tst.gemm_run(plan, A, B, D, c=C, amax=amax)
     assert tst.gemm_status_query(plan)[0] == tst.TST_OK
     assert float(amax[0]) == 0.0 and (D == 0).all()
+
+
+def test_fp8_forward_epilogue_full_size_sampled_rows():
+    """The 16384 x 4096 x 4096 workload with the FP8 forward epilogue, in the launch
+    configuration the benchmark times: D on sampled rows against the oracle, and amax
+    against the device's own full output (rounding to e4m3 moves a value by at most 1/16 of
+    it in the normal range and by at most 2^-10 among the subnormals)."""
+    w = WORKLOADS["c6_bf16_fp8_epilogue"]
+    epi = w["epi"]
+    M, N, K = w["M"], w["N"], w["K"]
+    inp = synthetic.make_gemm_inputs(M, N, K, w["dtype"], w["dist"], case=w["case"], bias_dist=w["bias_dist"])
+    c_arr, c_vals = synthetic.make_addend(M, N, epi["c_dist"], w["case"], epi["c_dtype"])
+    plan = tst.gemm_plan_create(M, N, K, dtype=w["dtype"], mapping=w["mapping"], schedule=w["schedule"],
+                                out_dtype=w["out"], bn=w["bn"], cta_group=w["cta_group"], has_c=True,
+                                c_dtype=epi["c_dtype"], beta=epi["beta"], bias_mode=epi["bias_mode"],
+                                activation=epi["activation"], d_scale=True, amax=True)
+    D = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+    amax = torch.zeros(4, device="cuda")
+    tst.gemm_run(plan, device_codes(inp.A), device_codes(inp.B), D, bias=torch.from_numpy(inp.bias).cuda(),
+                 c=device_codes(c_arr), d_scale=torch.tensor([epi["d_scale"]], device="cuda"), amax=amax)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    dq = E.decode_e4m3(D.cpu().numpy())
+    rows = sample_rows(M, count=16)
+    acc, ad = oracle.gemm(inp.A, inp.B, "bf16", rows=rows)
+    e = E.Epilogue(beta=epi["beta"], c_in=c_vals, bias=inp.bias.astype(np.float64), bias_mode=E.BIAS_COL,
+                   act=E.ACT_GELU, d_scale=epi["d_scale"])
+    Z, Y, Dp, tol_z, tol_y = _bounds_rows(e, acc, ad, rows)
+    _assert_bracket(dq[rows], Dp, epi["d_scale"] * tol_y + 2 * FP32_EPS * np.abs(Dp), "e4m3", "D")
+    a = float(amax[0])
+    m = float(np.max(np.abs(dq))) / epi["d_scale"]
+    slack = 2.0 ** -10 / epi["d_scale"]
+    assert m < 448.0 / epi["d_scale"]                     # nothing saturated: the bounds below hold
+    assert m / (1 + 1 / 16) - slack <= a <= m / (1 - 1 / 16) + slack
+    assert a >= float(np.max(np.abs(Y) - tol_y))
+
+
+def _bounds_rows(e, acc, ad, rows):
+    Z, Y, Dp, bz = E.apply(acc, ad, e, rows=rows)
+    extra = np.abs(e.beta * np.asarray(e.c_in, np.float64)[rows]) + np.abs(e.bias)[None, :]
+    tol_z = 4e-3 * bz + 1e-6 + 8 * FP32_EPS * (np.abs(Z) + extra + bz)
+    tol_y = E.LIPSCHITZ[e.act] * tol_z + 8 * FP32_EPS * np.abs(Y)
+    return Z, Y, Dp, tol_z, tol_y
