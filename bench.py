@@ -92,6 +92,47 @@ def oracle_step(w, inp, rows, addend=None):
     return D, bz
 
 
+def setup_workload(w, tst, torch):
+    """Plan, pinned host inputs, device copies and the output tensor of workload w."""
+    inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
+                           bias_dist=w.get("bias_dist"))
+    epi = dict(w.get("epi") or {})
+    epi_plan = {k: epi[k] for k in ("beta", "c_dtype", "bias_mode", "activation", "amax") if k in epi}
+    if "c_dtype" in epi:
+        epi_plan["has_c"] = True
+    if "d_scale" in epi:
+        epi_plan["d_scale"] = True
+    plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
+                                schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
+                                has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
+                                use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
+                                cta_group=w.get("cta_group", 0), **extra_plan_options(w), **epi_plan)
+    a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
+    b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
+    host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory()}
+    if inp.bias is not None:
+        host["bias"] = torch.from_numpy(inp.bias).pin_memory()
+    if inp.scales is not None:
+        host["scales"] = torch.from_numpy(inp.scales).pin_memory()
+    if "c_dtype" in epi:
+        arr, _ = addend_for(w)
+        host["c"] = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr).pin_memory()
+    if "d_scale" in epi:
+        host["d_scale"] = torch.tensor([epi["d_scale"]], dtype=torch.float32).pin_memory()
+    dev = {k: v.cuda() for k, v in host.items()}
+    if epi.get("amax"):
+        dev["amax"] = torch.zeros(4, dtype=torch.float32, device="cuda")
+    cdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8}[w["out"]]
+    C = torch.empty(w["M"], w["N"], dtype=cdt, device="cuda")
+    return inp, plan, host, dev, C
+
+
+def run_args(dev):
+    """Keyword arguments of gemm_run for the device operands of setup_workload."""
+    return dict(bias=dev.get("bias"), scales=dev.get("scales"), c=dev.get("c"), d_scale=dev.get("d_scale"),
+                amax=dev.get("amax"))
+
+
 def addend_for(w):
     epi = w.get("epi") or {}
     if "c_dtype" not in epi:
@@ -430,26 +471,13 @@ def run_role_cycles(args):
     names = [args.workload] + ([] if args.no_extra else [n for n in EXTRA if n != args.workload])
     for name in names:
         w = WORKLOADS[name]
-        inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
-                               bias_dist=w.get("bias_dist"))
-        plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
-                                    schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
-                                    has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
-                                    use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
-                                    cta_group=w.get("cta_group", 0))
+        inp, plan, host, dev, C = setup_workload(w, tst, torch)
         info = plan.info
-        a = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
-        b = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
-        A, B = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
-        bias = torch.from_numpy(inp.bias).cuda() if inp.bias is not None else None
-        scales = torch.from_numpy(inp.scales).cuda() if inp.scales is not None else None
-        C = torch.empty(w["M"], w["N"], dtype=torch.bfloat16 if w["out"] == "bf16" else torch.float32,
-                        device="cuda")
         stats = torch.zeros(info.ctas * 8, dtype=torch.int64, device="cuda")
         for _ in range(args.warmup):
-            tst.gemm_run(plan, A, B, C, bias=bias, scales=scales)
+            tst.gemm_run(plan, dev["A"], dev["B"], C, **run_args(dev))
         tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_ROLE_CYCLES, stats, info.ctas * 16)
-        tst.gemm_run(plan, A, B, C, bias=bias, scales=scales)
+        tst.gemm_run(plan, dev["A"], dev["B"], C, **run_args(dev))
         st, word = tst.gemm_status_query(plan)
         if st != tst.TST_OK:
             raise RuntimeError(f"{name}: device status {tst.gemm_status_string(st)} {word:#x}")
@@ -533,41 +561,11 @@ def main():
 
     def prepare(name):
         w = WORKLOADS[name]
-        inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
-                               bias_dist=w.get("bias_dist"))
-        epi = dict(w.get("epi") or {})
-        epi_plan = {k: epi[k] for k in ("beta", "c_dtype", "bias_mode", "activation", "amax") if k in epi}
-        if "c_dtype" in epi:
-            epi_plan["has_c"] = True
-        if "d_scale" in epi:
-            epi_plan["d_scale"] = True
-        plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], dtype=w["dtype"], mapping=w["mapping"],
-                                    schedule=w["schedule"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
-                                    has_bias=w.get("bias_dist") is not None, relu=w.get("relu", False),
-                                    use_scales=w.get("use_scales", False), bn=w.get("bn", 0),
-                                    cta_group=w.get("cta_group", 0), **extra_plan_options(w), **epi_plan)
-        a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
-        b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
-        host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory()}
-        if inp.bias is not None:
-            host["bias"] = torch.from_numpy(inp.bias).pin_memory()
-        if inp.scales is not None:
-            host["scales"] = torch.from_numpy(inp.scales).pin_memory()
-        if "c_dtype" in epi:
-            arr, _ = addend_for(w)
-            host["c"] = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr).pin_memory()
-        if "d_scale" in epi:
-            host["d_scale"] = torch.tensor([epi["d_scale"]], dtype=torch.float32).pin_memory()
-        dev = {k: v.cuda() for k, v in host.items()}
-        if epi.get("amax"):
-            dev["amax"] = torch.zeros(4, dtype=torch.float32, device="cuda")
-        cdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8}[w["out"]]
-        C = torch.empty(w["M"], w["N"], dtype=cdt, device="cuda")
+        inp, plan, host, dev, C = setup_workload(w, tst, torch)
         return w, inp, plan, host, dev, C
 
     def launch(plan, dev, C):
-        tst.gemm_run(plan, dev["A"], dev["B"], C, bias=dev.get("bias"), scales=dev.get("scales"),
-                     stream=stream.cuda_stream, c=dev.get("c"), d_scale=dev.get("d_scale"), amax=dev.get("amax"))
+        tst.gemm_run(plan, dev["A"], dev["B"], C, stream=stream.cuda_stream, **run_args(dev))
 
     def time_device(name, steps, warmup, sampler=None):
         w, inp, plan, host, dev, C = prepare(name)

@@ -296,8 +296,9 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   }
   p->smem_bytes = tst_kernel_smem_bytes(p->bn, p->cg, p->ka);
   if (!p->host_only) {
-    // the extended epilogue stores D through its own typed path, so any instance serves it
-    p->kernel = tst_kernel(dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3, p->bn, kernel_out(*p), p->cg, p->ka);
+    // the extended epilogue has its own instance (two epilogue warpgroups, typed stores of D)
+    const int kdt = dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3;
+    p->kernel = p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka) : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka);
     if (!p->kernel ||
         cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) != cudaSuccess) {
       cudaGetLastError();
@@ -314,7 +315,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     if (!p->host_only) {
       cudaLaunchConfig_t qc = {};
       qc.gridDim = dim3(static_cast<unsigned>(2 * resident), 1, 1);
-      qc.blockDim = dim3(tst_kernel_threads(p->bn, p->ka), 1, 1);
+      qc.blockDim = dim3(tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
       qc.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
       cudaLaunchAttribute ca[1];
       ca[0].id = cudaLaunchAttributeClusterDimension;
@@ -667,7 +668,7 @@ tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, cons
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg), 1, 1);
-  cfg.blockDim = dim3(tst_kernel_threads(p->bn, p->ka), 1, 1);
+  cfg.blockDim = dim3(tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

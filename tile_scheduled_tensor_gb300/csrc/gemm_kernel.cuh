@@ -324,14 +324,23 @@ __device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, 
   }
 }
 
-template <int BN, int OUT, int CG, int KA>
+// ACT and DOUT (activation and D's type) specialise the extended epilogue (OUT == OUT_EXT)
+template <int BN, int OUT, int CG, int KA, int ACT = ACT_NONE, int DOUT = OUT_F32>
 __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
                                              uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
   using Cfg = TileCfg<BN, CG, KA>;
+  constexpr bool EXT = OUT == OUT_EXT;          // extended epilogue instance
+  constexpr int EW = EXT ? 2 : 1;               // epilogue warpgroups
+  constexpr int EP_THREADS = 128 * EW;
+  constexpr int CHUNKS = BN / 64 / EW;          // 64-column TMEM loads per warpgroup and tile
   volatile uint32_t* ep_ok = &ctl->ep_ok;
-  const int ep = threadIdx.x - 64;             // 0..127
-  const int quad = (threadIdx.x >> 5) & 3;     // TMEM lane quadrant this warp may access
+  const int warp = threadIdx.x >> 5;
+  // epilogue warps 2-5, then 6-9 (7-10 when warp 6 is the second MMA issuer)
+  const int ew_idx = warp < 6 ? warp - 2 : warp - (Cfg::DUAL ? 3 : 2);
+  const int group = ew_idx >> 2;               // which half of the columns (EW = 2)
   const int lane = threadIdx.x & 31;
+  const int ep = ew_idx * 32 + lane;           // 0 .. EP_THREADS - 1
+  const int quad = warp & 3;                   // TMEM lane quadrant this warp may access
   const int row_in_tile = quad * 32 + lane;
   // pairs: arrive on the leader's TMEM_EMPTY barriers
   const uint32_t tempty_target = CG == 2 ? ptx::mapa(bar_tempty, 0) : bar_tempty;
@@ -361,7 +370,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
       const int32_t member = c.unit / (p.sched.sk_groups > 0 ? p.sched.sk_groups : 1);
       slot = slot * p.sk_slots + (member - m_first);
     }
-    // one elected thread waits; the verdict is broadcast so all 128 threads
+    // one elected thread waits; the verdict is broadcast so all epilogue threads
     // take the same path through the named barriers below
     const long long t0 = (p.stats && ep == 0) ? clock64() : 0;
     if (ep == 0) {
@@ -374,7 +383,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
       }
       *ep_ok = ok ? 1u : 0u;
     }
-    ptx::named_bar_sync(1, 128);
+    ptx::named_bar_sync(1, EP_THREADS);
     if (*ep_ok == 0u) break;
     const long long t1 = (p.stats && ep == 0) ? clock64() : 0;
     if (p.stats && ep == 0) wait_tfull += t1 - t0;
@@ -386,9 +395,9 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
         tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
     float s_row = alpha, b_row = 0.0f;  // extended epilogue: this row's accumulator scale and bias
-    if (p.ext.on) epi::row_terms(p.ext, p.bias, alpha, p.M, row, s_row, b_row);
+    if (EXT) epi::row_terms(p.ext, p.bias, alpha, p.M, row, s_row, b_row);
 #pragma unroll 1
-    for (int ch = 0; ch < BN / 64; ++ch) {
+    for (int ch = group * CHUNKS; ch < (group + 1) * CHUNKS; ++ch) {
       float v[64];
       if (Cfg::DUAL) {
         // the two issuers' accumulators, columns [0, BN) and [BN, 2 BN): add them
@@ -435,8 +444,9 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
           for (int j = 0; j < 32; ++j) v[32 * h + j] = __ldcg(wsc + j * kBlockM) + v[32 * h + j];
         }
         const int32_t col0 = w.n * BN + c32 * 32;
-        if (p.ext.on) {
-          epi::chunk<32>(p.ext, p.bias, s_row, b_row, p.M, p.N, row, col0, v + 32 * h, p.C, amax);
+        if constexpr (EXT) {
+          amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, p.M, p.N, row, col0, v + 32 * h, p.C,
+                                             amax);
           continue;
         }
         float z[32];
@@ -468,7 +478,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     ptx::tc_fence_before();
     if (fixup && (!final_split || separate)) __threadfence();  // partials visible GPU-wide before the lock moves
-    ptx::named_bar_sync(1, 128);
+    ptx::named_bar_sync(1, EP_THREADS);
     if (p.stats && ep == 0) { busy += clock64() - t1; ++items; }
     if (ep == 0) {
       if (CG == 2) ptx::mbar_arrive_cluster(tempty_target + 8 * acc);
@@ -482,7 +492,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
   }
   // every epilogue thread leaves the loop in the same iteration, so each warp is whole here
-  if (p.ext.on) epi::amax_flush(p.ext, amax);
+  if (EXT) epi::amax_flush(p.ext, amax);
   if (p.stats && ep == 0) {
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_WAIT_TFULL] = wait_tfull;
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_BUSY] = busy;
@@ -490,9 +500,32 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   }
 }
 
+// The extended epilogue with its activation and D's type fixed: one specialised copy
+// of the epilogue loop per combination, picked once per launch.
+template <int BN, int CG, int KA, int ACT>
+__device__ __forceinline__ void run_epilogue_ext_act(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
+                                                     uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
+  switch (p.ext.out_type) {
+    case OUT_BF16: run_epilogue<BN, OUT_EXT, CG, KA, ACT, OUT_BF16>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    case OUT_E4M3: run_epilogue<BN, OUT_EXT, CG, KA, ACT, OUT_E4M3>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    default: run_epilogue<BN, OUT_EXT, CG, KA, ACT, OUT_F32>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+  }
+}
+
+template <int BN, int CG, int KA>
+__device__ __forceinline__ void run_epilogue_ext(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
+                                                 uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
+  switch (p.ext.act) {
+    case ACT_RELU: run_epilogue_ext_act<BN, CG, KA, ACT_RELU>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    case ACT_GELU: run_epilogue_ext_act<BN, CG, KA, ACT_GELU>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    case ACT_SILU: run_epilogue_ext_act<BN, CG, KA, ACT_SILU>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    default: run_epilogue_ext_act<BN, CG, KA, ACT_NONE>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <int BN, int DT, int OUT, int CG, int KA>
-__global__ void __launch_bounds__(TileCfg<BN, CG, KA>::THREADS, 1)
+__global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EXT ? 2 : 1), 1)
     gemm_tcgen05_kernel(const __grid_constant__ KernelParams p) {
   using Cfg = TileCfg<BN, CG, KA>;
   extern __shared__ uint8_t smem_raw[];
@@ -549,11 +582,13 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) run_producer<BN, DT, CG, KA>(p, c, smem_a, smem_b, bar_full, bar_empty);
-  } else if (warp == 1 || warp == 6) {  // warp 6 exists only in dual-issue tiles
+  } else if (warp == 1 || (Cfg::DUAL && warp == 6)) {  // warp 6: second issuer of dual-issue tiles
     const int issuer = warp == 1 ? 0 : 1;
     if (lane == 0 && c.rank == 0)
       run_mma<BN, DT, CG, KA>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty,
                               bar_drain + 8 * issuer, issuer);
+  } else if constexpr (OUT == OUT_EXT) {
+    run_epilogue_ext<BN, CG, KA>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   } else {
     run_epilogue<BN, OUT, CG, KA>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   }
@@ -576,6 +611,11 @@ template <int BN, int DT, int CG, int KA>
 const void* select_kernel(int out_type) {
   if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16, CG, KA>);
   return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32, CG, KA>);
+}
+
+template <int BN, int DT, int CG, int KA>
+const void* select_ext_kernel() {
+  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_EXT, CG, KA>);
 }
 
 }  // namespace tst

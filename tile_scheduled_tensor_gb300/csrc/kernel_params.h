@@ -14,6 +14,9 @@ constexpr int kSmemLimit = 232448;  // 227 KiB opt-in dynamic shared memory per 
 
 enum DType : int32_t { DT_BF16 = 0, DT_E4M3 = 1 };
 enum OutType : int32_t { OUT_F32 = 0, OUT_BF16 = 1, OUT_E4M3 = 2 };
+// Kernel instance for the extended epilogue: two epilogue warpgroups (each takes half
+// of the accumulator's columns) and only the extended path; D's type is EpiExt::out_type.
+constexpr int OUT_EXT = 3;
 enum ActKind : int32_t { ACT_NONE = 0, ACT_RELU = 1, ACT_GELU = 2, ACT_SILU = 3 };
 enum BiasMode : int32_t { BIAS_NONE = 0, BIAS_COL = 1, BIAS_ROW = 2 };
 
@@ -103,6 +106,9 @@ struct TileCfg {
   static constexpr bool DUAL = (BN == 128 && KA == 2);
   static constexpr int ISSUERS = DUAL ? 2 : 1;
   static constexpr int THREADS = DUAL ? kThreadsDual : kThreads;
+  // threads with `ew` epilogue warpgroups: warps 0-1 (+ warp 6 for the second issuer),
+  // epilogue warps 2-5 and, for ew = 2, 6-9 (7-10 with the second issuer)
+  static constexpr int threads_for(int ew) { return THREADS + 128 * (ew - 1); }
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int RAW_STAGES = (kSmemLimit - 2048) / STAGE_BYTES;
   static constexpr int STAGES = RAW_STAGES > 8 ? 8 : RAW_STAGES;
@@ -124,6 +130,25 @@ const void* tst_kernel_bf16_cg1_ka2(int bn, int out_type);
 const void* tst_kernel_bf16_cg2_ka2(int bn, int out_type);
 const void* tst_kernel_e4m3_cg1_ka2(int bn, int out_type);
 const void* tst_kernel_e4m3_cg2_ka2(int bn, int out_type);
+
+const void* tst_kernel_ext_bf16_cg1_ka1(int bn);
+const void* tst_kernel_ext_bf16_cg2_ka1(int bn);
+const void* tst_kernel_ext_e4m3_cg1_ka1(int bn);
+const void* tst_kernel_ext_e4m3_cg2_ka1(int bn);
+const void* tst_kernel_ext_bf16_cg1_ka2(int bn);
+const void* tst_kernel_ext_bf16_cg2_ka2(int bn);
+const void* tst_kernel_ext_e4m3_cg1_ka2(int bn);
+const void* tst_kernel_ext_e4m3_cg2_ka2(int bn);
+
+// The extended-epilogue instance (gemm_ext_<dtype>_cg<n>_ka<k>.cu)
+inline const void* tst_kernel_ext(int dtype, int bn, int cg, int ka) {
+  if (ka == 2) {
+    if (dtype == tst::DT_BF16) return cg == 2 ? tst_kernel_ext_bf16_cg2_ka2(bn) : tst_kernel_ext_bf16_cg1_ka2(bn);
+    return cg == 2 ? tst_kernel_ext_e4m3_cg2_ka2(bn) : tst_kernel_ext_e4m3_cg1_ka2(bn);
+  }
+  if (dtype == tst::DT_BF16) return cg == 2 ? tst_kernel_ext_bf16_cg2_ka1(bn) : tst_kernel_ext_bf16_cg1_ka1(bn);
+  return cg == 2 ? tst_kernel_ext_e4m3_cg2_ka1(bn) : tst_kernel_ext_e4m3_cg1_ka1(bn);
+}
 
 inline const void* tst_kernel(int dtype, int bn, int out_type, int cg, int ka) {
   if (ka == 2) {
@@ -168,5 +193,7 @@ constexpr int kReduceRows = 16;  // rows of a 128-row tile half per CTA
 }  // namespace tst
 const void* tst_reduce_kernel(int out_type);
 
-inline int tst_kernel_threads(int bn, int ka) { return (bn == 128 && ka == 2) ? tst::kThreadsDual : tst::kThreads; }
+inline int tst_kernel_threads(int bn, int ka, bool ext = false) {
+  return ((bn == 128 && ka == 2) ? tst::kThreadsDual : tst::kThreads) + (ext ? 128 : 0);
+}
 inline int tst_kernel_stages(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, false); }
