@@ -15,6 +15,8 @@ Parts:
                   scale, FP8 e4m3 output encoding), FP64 on the raw accumulator.
   * schedule.py - mappings F(i) -> (m, n), static / persistent / Stream-K work
                   lists, wave efficiency, operand band counts.
+  * grouped.py  - the grouped (many-GEMM) persistent schedule: concatenated
+                  tile sequence, the warp-level speculative group search.
 Every function cites the passage it follows in its own source file.
 """
 from __future__ import annotations
@@ -25,7 +27,7 @@ import subprocess
 
 import numpy as np
 
-from . import epilogue, schedule  # noqa: F401  (re-exported)
+from . import epilogue, grouped, schedule  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_ref.c")
