@@ -289,6 +289,43 @@ tst_status gemm_plan_create_epi(tst_plan **plan, int64_t M, int64_t N, int64_t K
 tst_status gemm_run_epi(tst_plan *plan, const void *A, const void *B, void *D,
                         const tst_epilogue_args *args, void *stream);
 
+/* Grouped GEMM: `groups` independent GEMMs in one persistent launch ("H100 .
+ * Kernel Design", section 10.2, Grouped Persistent Scheduling).  The groups
+ * share N and K; group g has M_g rows, M_g read from device memory at run time
+ * (so a previous kernel may produce it, with no host synchronisation):
+ *
+ *   D[r_g + i][j] = epilogue( sum_k A[r_g + i][k] * B[g N + j][k] ),
+ *   0 <= i < M_g, r_g = M_0 + ... + M_(g-1),
+ *
+ * i.e. A holds the groups' rows one after another (at most M rows in all), B
+ * holds one N x K matrix per group (groups * N rows), D has A's rows.  The
+ * groups' tiles form one linear sequence that the persistent CTAs walk; a CTA
+ * finds the group of its next tile by the section's warp-level speculative
+ * search.  The epilogue is per element as in gemm_plan_create_epi (a row bias or
+ * row scale is indexed by the row of A / D).  The schedule is persistent; the
+ * mapping orders each group's tiles (any kind but TST_MAP_MORTON).
+ * Errors as gemm_plan_create_epi; INVALID_ARG for groups < 1; UNSUPPORTED for
+ * TST_MAP_MORTON. */
+tst_status gemm_grouped_plan_create(tst_plan **plan, int32_t groups, int64_t M, int64_t N, int64_t K,
+                                    tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                                    const tst_epilogue_ex *epi, const tst_plan_options *opts);
+
+/* Launch a grouped GEMM.  group_rows: DEVICE int32[groups] holding M_g (negative
+ * counts are taken as 0).  A: M x K, B: (groups * N) x K, D: M x N, as in
+ * gemm_grouped_plan_create; args as in gemm_run_epi.  If the M_g add up to more
+ * than M rows, rows past M are not computed and gemm_status_query reports
+ * TST_ERR_DEVICE_CHECK after the run completes.  Errors as gemm_run_epi, and
+ * INVALID_ARG for a plan that is not grouped or a NULL group_rows. */
+tst_status gemm_grouped_run(tst_plan *plan, const int32_t *group_rows, const void *A, const void *B,
+                            void *D, const tst_epilogue_args *args, void *stream);
+
+/* The work list of scheduling unit `cta` of a grouped plan for the HOST array
+ * group_rows (the device's walk for those group sizes; pure host computation).
+ * Items as gemm_work_items: tile = index in the concatenated sequence, (m, n)
+ * inside the item's group.  gemm_work_items rejects grouped plans. */
+tst_status gemm_grouped_work_items(const tst_plan *plan, const int32_t *group_rows, int32_t cta,
+                                   tst_work_item *items, int64_t cap, int64_t *count);
+
 /* Launch the GEMM on `stream` (a cudaStream_t; NULL = legacy default stream).
  * A, B, C: device pointers, 16-byte aligned.  bias: FP32[N] when epi.has_bias,
  * else ignored.  scales: FP32[2] = {sA, sB} when epi.use_scales, else ignored.

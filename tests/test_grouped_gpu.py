@@ -1,0 +1,186 @@
+"""GPU parity of the grouped GEMM (many GEMMs sharing N and K in one persistent
+launch, group sizes read from device memory) against the oracle, group by group.
+
+Exact with small integers (every FP32 sum exact); within the element bound with
+random inputs; the device's walk over the groups (producer trace) equals the
+oracle's enumeration; rows past the groups' total are left untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import tile_scheduled_tensor_gb300 as tst
+from oracle import epilogue as E
+from oracle import grouped as GR
+from oracle import schedule as S
+
+from gemm_check import assert_close, device_codes, host_values
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(seed, G, hi, zero_every=4):
+    r = (synthetic.splitmix64(seed, G) % np.uint64(hi + 1)).astype(np.int64)
+    r[1::zero_every] = 0
+    return [int(x) for x in r]
+
+
+def _inputs(rows, N, K, dtype, dist, case):
+    M = sum(rows)
+    fa, fb = synthetic.operand_types(dtype)
+    enc = {"bf16": synthetic.bf16_bits, "e4m3": lambda x: synthetic.e4m3_bytes(x.astype(np.float32)),
+           "e5m2": lambda x: synthetic.e5m2_bytes(x.astype(np.float32))}
+    A = enc[fa](synthetic.draw(dist, 1000 + case, max(M, 1) * K).reshape(max(M, 1), K))
+    B = enc[fb](synthetic.draw(dist, 2000 + case, len(rows) * N * K).reshape(len(rows) * N, K))
+    return A, B
+
+
+def _oracle_groups(A, B, rows, N, dtype, **kw):
+    """FP64 result and absdot, group by group (each group an ordinary GEMM)."""
+    fa, fb = synthetic.operand_types(dtype)
+    M = sum(rows)
+    z = np.zeros((M, N))
+    ad = np.zeros((M, N))
+    r0 = 0
+    for g, r in enumerate(rows):
+        if r:
+            zg, adg = oracle.gemm(A[r0:r0 + r], B[g * N:(g + 1) * N], fa, dtype_b=fb, **kw)
+            z[r0:r0 + r], ad[r0:r0 + r] = zg, adg
+        r0 += r
+    return z, ad
+
+
+def _run(plan, rows, A, B, M_cap, N, out="f32", fill=float("nan"), **args):
+    gr = torch.tensor(rows, dtype=torch.int32, device="cuda")
+    Ad = torch.zeros(M_cap, A.shape[1], dtype=torch.int16 if A.dtype == np.uint16 else torch.uint8, device="cuda")
+    Ad[:A.shape[0]] = device_codes(A)
+    D = torch.full((M_cap, N), fill, dtype=torch.float32, device="cuda") if out == "f32" else \
+        torch.full((M_cap, N), fill, dtype=torch.bfloat16, device="cuda")
+    tst.gemm_grouped_run(plan, gr, Ad, device_codes(B), D, **args)
+    st, word = tst.gemm_status_query(plan)
+    return st, word, D
+
+
+@pytest.mark.parametrize("cta_group,bn,dtype", [(1, 128, "bf16"), (2, 256, "bf16"), (2, 128, "e4m3"),
+                                                (1, 256, "e5m2_e4m3")])
+@pytest.mark.parametrize("G,hi", [(5, 700), (40, 300), (100, 60)])
+def test_grouped_small_integers_exact(cta_group, bn, dtype, G, hi):
+    rows = _rows(G * 7 + hi, G, hi)
+    N, K = 384, 256
+    A, B = _inputs(rows, N, K, dtype, "int:8", case=31)
+    M_cap = sum(rows) + 64
+    plan = tst.gemm_grouped_plan_create(G, M_cap, N, K, dtype=dtype, mapping=("grouped_m", 8), out_dtype="f32",
+                                        cta_group=cta_group, bn=bn, num_ctas=19)
+    st, word, D = _run(plan, rows, A, B, M_cap, N)
+    assert st == tst.TST_OK, hex(word)
+    z, _ = _oracle_groups(A, B, rows, N, dtype)
+    got = host_values(D)
+    M = sum(rows)
+    assert np.array_equal(got[:M], z)
+    assert np.isnan(got[M:]).all()                  # rows past the groups are never written
+
+
+def test_group_sizes_change_without_replanning():
+    """One plan, several runs with different device group sizes (a previous kernel could
+    have written them): every run matches its own oracle."""
+    G, N, K = 12, 256, 128
+    M_cap = 12 * 400
+    plan = tst.gemm_grouped_plan_create(G, M_cap, N, K, mapping=("linear_nfast", 1), out_dtype="f32", cta_group=1,
+                                        bn=128)
+    for seed in (1, 2, 3):
+        rows = _rows(seed, G, 400)
+        A, B = _inputs(rows, N, K, "bf16", "int:8", case=32 + seed)
+        st, word, D = _run(plan, rows, A, B, M_cap, N)
+        assert st == tst.TST_OK
+        z, _ = _oracle_groups(A, B, rows, N, "bf16")
+        assert np.array_equal(host_values(D)[:sum(rows)], z)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_grouped_random_bf16_out_within_bound(cta_group):
+    rows = _rows(77, 9, 900)
+    N, K = 520, 1024
+    A, B = _inputs(rows, N, K, "bf16", "normal", case=33)
+    bias = synthetic.normal(3033, N).astype(np.float32)
+    M_cap = sum(rows)
+    plan = tst.gemm_grouped_plan_create(9, M_cap, N, K, mapping=("grouped_m", 8), out_dtype="bf16", alpha=0.5,
+                                        has_bias=True, relu=True, cta_group=cta_group, bn=256 if cta_group == 2 else 128)
+    st, word, D = _run(plan, rows, A, B, M_cap, N, out="bf16", bias=torch.from_numpy(bias).cuda())
+    assert st == tst.TST_OK
+    z, ad = _oracle_groups(A, B, rows, N, "bf16", alpha=0.5, bias=bias, relu=True)
+    assert_close(host_values(D), z, ad, "bf16", "grouped")
+
+
+def test_grouped_extended_epilogue_row_bias_gelu_amax():
+    """Row-indexed operands follow the row of A / D across the groups; amax covers only the
+    groups' rows."""
+    rows = _rows(78, 20, 300)
+    N, K = 256, 512
+    A, B = _inputs(rows, N, K, "bf16", "normal", case=34)
+    M = sum(rows)
+    M_cap = M + 200
+    row_bias = synthetic.normal(3034, M_cap).astype(np.float32)
+    rs = (0.5 + synthetic.uniform01(3035, M_cap)).astype(np.float32)
+    plan = tst.gemm_grouped_plan_create(20, M_cap, N, K, mapping=("grouped_m", 4), out_dtype="f32",
+                                        bias_mode="row", activation="gelu", row_scale=True, amax=True, cta_group=2,
+                                        bn=256)
+    amax = torch.zeros(4, device="cuda")
+    st, word, D = _run(plan, rows, A, B, M_cap, N, bias=torch.from_numpy(row_bias).cuda(),
+                       row_scale=torch.from_numpy(rs).cuda(), amax=amax)
+    assert st == tst.TST_OK
+    acc, ad = _oracle_groups(A, B, rows, N, "bf16")
+    e = E.Epilogue(row_scale=rs.astype(np.float64)[:M], bias=row_bias.astype(np.float64)[:M], bias_mode=E.BIAS_ROW,
+                   act=E.ACT_GELU)
+    Z, Y, Dp, bz = E.apply(acc, ad, e)
+    tol_z = 4e-3 * bz + 1e-6 + 8 * 2.0 ** -23 * (np.abs(Z) + np.abs(e.bias)[:, None] + bz)
+    tol = E.LIPSCHITZ[E.ACT_GELU] * tol_z + 16 * 2.0 ** -23 * np.abs(Y) + 2e-7 * np.maximum(1, np.abs(Z))
+    got = host_values(D)
+    assert (np.abs(got[:M] - Y) <= tol).all()
+    assert np.isnan(got[M:]).all()
+    a = float(amax[0])
+    assert float(np.max(np.abs(Y) - tol)) <= a <= float(np.max(np.abs(Y) + tol))
+
+
+def test_grouped_device_walk_matches_oracle_trace():
+    rows = _rows(79, 45, 250)
+    N, K = 384, 128
+    A, B = _inputs(rows, N, K, "bf16", "int:4", case=35)
+    M_cap = sum(rows) + 1
+    plan = tst.gemm_grouped_plan_create(45, M_cap, N, K, mapping=("grouped_n", 2), out_dtype="f32", cta_group=1,
+                                        bn=128, num_ctas=13)
+    info = plan.info
+    trace = torch.full((info.grid * info.max_items_per_cta * 8,), -1, dtype=torch.int32, device="cuda")
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TRACE, trace, trace.numel())
+    st, word, D = _run(plan, rows, A, B, M_cap, N)
+    assert st == tst.TST_OK
+    t = trace.view(info.grid, info.max_items_per_cta, 8).cpu().numpy()
+    Nt = -(-N // 128)
+    for u in range(info.grid):
+        got = [(int(r[2]), int(r[3]), int(r[4])) for r in t[u] if r[0] != -1]
+        want = [(it.tile, it.m, it.n) for it in GR.grouped_work_items(u, info.grid, rows, 128, Nt, S.GROUPED_N, 2)]
+        assert got == want
+        assert got == [(a, b, c) for a, b, c, *_ in tst.gemm_grouped_work_items(plan, rows, u)]
+
+
+def test_grouped_rows_past_capacity_report_device_check():
+    rows = [300, 300]
+    N, K = 256, 64
+    A, B = _inputs(rows, N, K, "bf16", "int:4", case=36)
+    plan = tst.gemm_grouped_plan_create(2, 500, N, K, out_dtype="f32", cta_group=1, bn=128)
+    st, word, D = _run(plan, rows, A[:500], B, 500, N)
+    assert st == tst.TST_ERR_DEVICE_CHECK
+    z, _ = _oracle_groups(A, B, rows, N, "bf16")
+    assert np.array_equal(host_values(D), z[:500])   # every row that fits is still computed
+    # the next run on the same plan with sizes that fit is clean
+    st, word, D = _run(plan, [200, 300], A[:500], B, 500, N)
+    assert st == tst.TST_OK
+
+
+def test_grouped_all_empty():
+    plan = tst.gemm_grouped_plan_create(8, 256, 128, 64, out_dtype="f32", cta_group=1, bn=128)
+    A, B = _inputs([1], 128, 64, "bf16", "int:4", case=37)
+    B = np.concatenate([B] * 8)
+    st, word, D = _run(plan, [0] * 8, A, B, 256, 128)
+    assert st == tst.TST_OK and np.isnan(host_values(D)).all()

@@ -130,6 +130,62 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
     return Plan(h.value, info)
 
 
+def gemm_grouped_plan_create(groups: int, M: int, N: int, K: int, dtype="bf16", mapping=("grouped_m", 8),
+                             out_dtype="bf16", alpha: float = 1.0, beta: float = 0.0, has_c: bool = False,
+                             c_dtype="f32", has_bias: bool = False, bias_mode=None, relu: bool = False,
+                             activation=None, use_scales: bool = False, row_scale: bool = False,
+                             col_scale: bool = False, d_scale: bool = False, amax: bool = False, aux: bool = False,
+                             aux_dtype="f32", bn: int = 0, num_ctas: int = 0, host_only: bool = False,
+                             num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0, stages: int = 0,
+                             bk: int = 0) -> Plan:
+    """Plan `groups` GEMMs sharing N and K in one persistent launch: A holds the groups'
+    rows one after another (at most M in all), B one N x K matrix per group; the row
+    counts are given to gemm_grouped_run as a device int32 array."""
+    kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
+    m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
+    opts = _capi.tst_plan_options(int(bn), int(num_ctas), 0, int(bool(host_only)), int(num_sms), int(cta_group),
+                                  int(timeout_ns), int(stages), int(bk), 0, 0)
+    bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
+        (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
+    act = _enum(_ACT, activation, "activation") if activation is not None else \
+        (TST_ACT_RELU if relu else TST_ACT_NONE)
+    epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), float(beta), int(bool(has_c)),
+                                _enum(_OUT, c_dtype, "c_dtype"), bmode, act, int(bool(use_scales)),
+                                int(bool(row_scale)), int(bool(col_scale)), int(bool(d_scale)), int(bool(amax)),
+                                int(bool(aux)), _enum(_OUT, aux_dtype, "aux_dtype"))
+    h = ctypes.c_void_p()
+    _check(lib.gemm_grouped_plan_create(ctypes.byref(h), int(groups), int(M), int(N), int(K),
+                                        _enum(_DTYPES, dtype, "dtype"), TST_LAYOUT_A_ROW_B_NK, m, ctypes.byref(epi),
+                                        ctypes.byref(opts)), "gemm_grouped_plan_create")
+    info = _capi.tst_plan_info()
+    _check(lib.gemm_plan_get_info(h, ctypes.byref(info)), "gemm_plan_get_info")
+    return Plan(h.value, info)
+
+
+def gemm_grouped_run(plan: Plan, group_rows, A, B, D, bias=None, scales=None, c=None, row_scale=None,
+                     col_scale=None, d_scale=None, amax=None, aux=None, stream=None):
+    """Enqueue a grouped GEMM; group_rows is a CUDA int32 tensor of the groups' row counts."""
+    if hasattr(group_rows, "dtype") and str(group_rows.dtype) != "torch.int32":
+        raise ValueError("group_rows must be an int32 CUDA tensor")
+    args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux))
+    _check(lib.gemm_grouped_run(plan._h, _ptr(group_rows), _ptr(A), _ptr(B), _ptr(D), ctypes.byref(args),
+                                _stream(stream)), "gemm_grouped_run")
+
+
+def gemm_grouped_work_items(plan: Plan, group_rows, cta: int):
+    """[(tile, m, n, k_begin, k_count, flags), ...] of one CTA of a grouped plan for the given
+    host row counts, in device order."""
+    rows = (ctypes.c_int32 * max(len(group_rows), 1))(*[int(r) for r in group_rows])
+    count = ctypes.c_int64()
+    _check(lib.gemm_grouped_work_items(plan._h, rows, int(cta), None, 0, ctypes.byref(count)),
+           "gemm_grouped_work_items")
+    arr = (_capi.tst_work_item * max(count.value, 1))()
+    _check(lib.gemm_grouped_work_items(plan._h, rows, int(cta), arr, count.value, ctypes.byref(count)),
+           "gemm_grouped_work_items")
+    return [(w.tile, w.m, w.n, w.k_begin, w.k_count, w.flags) for w in arr[:count.value]]
+
+
 def gemm_plan_get_info(plan: Plan):
     info = _capi.tst_plan_info()
     _check(lib.gemm_plan_get_info(plan._h, ctypes.byref(info)), "gemm_plan_get_info")

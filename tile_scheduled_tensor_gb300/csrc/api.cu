@@ -31,6 +31,8 @@ struct tst_plan {
   tst_schedule schedule = TST_STATIC;
   tst_epilogue_ex epi{};       // the epilogue (the basic one is a special case)
   bool ext_on = false;         // epilogue needs more than alpha, column bias, ReLU, scales
+  int32_t groups = 0;          // grouped GEMM: number of groups (0 = one GEMM)
+  int64_t b_rows = 0;          // rows of B: N, or groups * N
   uint32_t fmt_ab = 0;         // FP8 operand formats for the instruction descriptor
   tst_plan_options opts{};
   int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
@@ -220,7 +222,7 @@ uint32_t fp8_formats(tst_dtype d) {
 
 tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
                        tst_mapping mapping, tst_schedule schedule, const tst_epilogue_ex* epi,
-                       const tst_plan_options* opts) {
+                       const tst_plan_options* opts, int32_t groups = 0) {
   if (out == nullptr) return TST_ERR_INVALID_ARG;
   *out = nullptr;
   if (epi == nullptr || M <= 0 || N <= 0 || K <= 0) return TST_ERR_INVALID_ARG;
@@ -231,6 +233,10 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
       mapping.group < 1)
     return TST_ERR_INVALID_ARG;
   if (schedule < TST_STATIC || schedule > TST_STREAMK_HYBRID) return TST_ERR_INVALID_ARG;
+  if (groups < 0 || groups >= (1 << 24)) return TST_ERR_INVALID_ARG;
+  // grouped GEMM: persistent over the groups' tiles, and a mapping that needs no per-grid table
+  if (groups > 0 && (schedule != TST_PERSISTENT || mapping.kind == TST_MAP_MORTON)) return TST_ERR_UNSUPPORTED;
+  if (groups > 0 && static_cast<int64_t>(groups) * N >= (int64_t(1) << 31)) return TST_ERR_INVALID_ARG;
   if (!valid_out(epi->out_dtype)) return TST_ERR_INVALID_ARG;
   if ((epi->has_c && !valid_in(epi->c_dtype)) || (epi->aux && !valid_in(epi->aux_dtype))) return TST_ERR_INVALID_ARG;
   if (epi->bias_mode < TST_BIAS_NONE || epi->bias_mode > TST_BIAS_ROW) return TST_ERR_INVALID_ARG;
@@ -248,6 +254,8 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   p->M = M; p->N = N; p->K = K;
   p->dtype = dtype; p->mapping = mapping; p->schedule = schedule; p->epi = *epi; p->opts = o;
   p->ext_on = needs_ext(*epi);
+  p->groups = groups;
+  p->b_rows = groups > 0 ? static_cast<int64_t>(groups) * N : N;
   p->fmt_ab = dtype == TST_BF16 ? 0u : fp8_formats(dtype);
   p->host_only = o.host_only != 0;
   if (o.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(o.timeout_ns);
@@ -287,7 +295,8 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   const int64_t mt = ceil_div(M, p->bm);
   const int64_t nt = ceil_div(N, p->bn);
   const int64_t kt = ceil_div(K, p->bk);
-  const int64_t T = mt * nt;
+  // grouped: at most ceil(M / bm) + groups tile rows over all groups, whatever the split
+  const int64_t T = (groups > 0 ? mt + groups : mt) * nt;
   if (T >= (int64_t(1) << 30) || T * kt >= (int64_t(1) << 62)) { delete p; return TST_ERR_INVALID_ARG; }
   p->stages = tst_kernel_stages(p->bn, p->cg, p->ka);
   if (o.stages != 0) {
@@ -341,6 +350,12 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   s.group = (mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N ||
              mapping.kind == TST_MAP_BLOCK_2D) ? mapping.group : 1;
   s.order = nullptr;
+  s.rows = static_cast<int32_t>(M);
+  s.bm = p->bm;
+  s.bn = p->bn;
+  s.groups = groups;
+  s.group_rows = nullptr;   // the run supplies the device array of group sizes
+  s.group_b_rows = static_cast<int32_t>(N);
   if (mapping.kind == TST_MAP_MORTON) {
     // Z order: tiles by the code interleaving the bits of n (even) and m (odd positions)
     std::vector<std::pair<uint64_t, int64_t>> codes;
@@ -401,9 +416,9 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     }
     p->sk_slots = most;
   }
-  // longest work list (trace sizing)
-  int32_t max_items = 0;
-  for (int32_t c = 0; c < s.grid; ++c) {
+  // longest work list (trace sizing); a grouped plan knows only the bound on its tiles
+  int32_t max_items = groups > 0 ? static_cast<int32_t>(ceil_div(T, s.grid)) : 0;
+  for (int32_t c = 0; c < s.grid && groups == 0; ++c) {
     tst::WorkIter it;
     tst::WorkItem w;
     tst::work_begin(s, c, it);
@@ -536,7 +551,7 @@ tst_status gemm_tile_map(const tst_plan* p, int64_t i, int32_t* m, int32_t* n) {
 
 tst_status gemm_work_items(const tst_plan* p, int32_t cta, tst_work_item* items, int64_t cap, int64_t* count) {
   if (p == nullptr || count == nullptr || (cap > 0 && items == nullptr) || cap < 0) return TST_ERR_INVALID_ARG;
-  if (cta < 0 || cta >= p->sched.grid) return TST_ERR_INVALID_ARG;
+  if (cta < 0 || cta >= p->sched.grid || p->groups > 0) return TST_ERR_INVALID_ARG;
   tst::WorkIter it;
   tst::WorkItem w;
   tst::work_begin(p->sched, cta, it);
@@ -581,9 +596,15 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
   return gemm_run_epi(p, A, B, C, &a, stream_);
 }
 
-tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
-                        void* stream_) {
+}  // extern "C"
+
+namespace {
+
+tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
+                  const int32_t* group_rows, void* stream_) {
   if (p == nullptr || A == nullptr || B == nullptr || C == nullptr || ea == nullptr) return TST_ERR_INVALID_ARG;
+  if ((p->groups > 0) != (group_rows != nullptr)) return TST_ERR_INVALID_ARG;
+  if (group_rows != nullptr && (reinterpret_cast<uintptr_t>(group_rows) & 3u)) return TST_ERR_ALIGNMENT;
   if (p->host_only || p->kernel == nullptr) return TST_ERR_NO_DEVICE;
   const tst_epilogue_ex& e = p->epi;
   const bool has_bias = e.bias_mode != TST_BIAS_NONE;
@@ -614,7 +635,7 @@ tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, cons
     p->tm_A = A;
   }
   if (B != p->tm_B) {
-    if (!encode_operand(&p->tmap_b, B, p->dtype, p->N, p->K, box_k, p->bn / p->cg)) return TST_ERR_CUDA;
+    if (!encode_operand(&p->tmap_b, B, p->dtype, p->b_rows, p->K, box_k, p->bn / p->cg)) return TST_ERR_CUDA;
     p->tm_B = B;
   }
 
@@ -635,6 +656,7 @@ tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, cons
   kp.alpha = e.alpha;
   kp.sched = p->sched;
   kp.sched.order = p->d_order;
+  kp.sched.group_rows = group_rows;
   kp.has_bias = has_bias ? 1 : 0;
   kp.relu = e.activation == TST_ACT_RELU ? 1 : 0;
   kp.use_scales = e.use_scales ? 1 : 0;
@@ -723,6 +745,51 @@ tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, cons
   }
   p->last_stream = stream;
   p->ran = true;
+  return TST_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tst_status gemm_run_epi(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
+                        void* stream) {
+  return launch(p, A, B, C, ea, nullptr, stream);
+}
+
+tst_status gemm_grouped_plan_create(tst_plan** plan, int32_t groups, int64_t M, int64_t N, int64_t K,
+                                    tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                                    const tst_epilogue_ex* epi, const tst_plan_options* opts) {
+  if (plan != nullptr) *plan = nullptr;
+  if (groups < 1) return TST_ERR_INVALID_ARG;
+  return create_plan(plan, M, N, K, dtype, layout, mapping, TST_PERSISTENT, epi, opts, groups);
+}
+
+tst_status gemm_grouped_run(tst_plan* p, const int32_t* group_rows, const void* A, const void* B, void* D,
+                            const tst_epilogue_args* args, void* stream) {
+  if (p == nullptr || group_rows == nullptr || p->groups == 0) return TST_ERR_INVALID_ARG;
+  return launch(p, A, B, D, args, group_rows, stream);
+}
+
+tst_status gemm_grouped_work_items(const tst_plan* p, const int32_t* group_rows, int32_t cta,
+                                   tst_work_item* items, int64_t cap, int64_t* count) {
+  if (p == nullptr || group_rows == nullptr || count == nullptr || (cap > 0 && items == nullptr) || cap < 0)
+    return TST_ERR_INVALID_ARG;
+  if (p->groups == 0 || cta < 0 || cta >= p->sched.grid) return TST_ERR_INVALID_ARG;
+  tst::Sched s = p->sched;
+  s.group_rows = group_rows;
+  tst::WorkIter it;
+  tst::WorkItem w;
+  tst::work_begin(s, cta, it);
+  int64_t n = 0;
+  while (tst::work_next(s, it, w)) {
+    if (n < cap) {
+      items[n].tile = w.tile; items[n].m = w.m; items[n].n = w.n;
+      items[n].k_begin = w.k_begin; items[n].k_count = w.k_count; items[n].flags = w.flags;
+    }
+    ++n;
+  }
+  *count = n;
   return TST_OK;
 }
 

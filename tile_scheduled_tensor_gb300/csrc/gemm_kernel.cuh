@@ -157,8 +157,12 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
       rec[0] = c.unit; rec[1] = seq; rec[2] = w.tile; rec[3] = w.m;
       rec[4] = w.n; rec[5] = w.k_begin; rec[6] = w.k_count; rec[7] = w.flags;
     }
-    const int32_t m0 = w.m * BM_UNIT + static_cast<int32_t>(c.rank) * kBlockM;
-    const int32_t n0 = w.n * BN + static_cast<int32_t>(c.rank) * BN_CTA;
+    // grouped GEMM: the group sizes add up to more rows than the output holds; the rows past
+    // it are never stored, and the run reports a device check (once, without stopping)
+    if ((w.flags & ITEM_CLAMPED) && leader)
+      atomicCAS(p.status, 0u, ST_DEVICE_CHECK | (ROLE_PRODUCER << 8) | (static_cast<uint32_t>(blockIdx.x) << 16));
+    const int32_t m0 = w.row0 + static_cast<int32_t>(c.rank) * kBlockM;    // row of A
+    const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * BN_CTA;   // row of B
     for (int32_t kb = w.k_begin; kb < w.k_begin + w.k_count; ++kb) {
       const long long t0 = p.stats ? clock64() : 0;
       if (!wait_phase<CG>(p, c, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
@@ -288,8 +292,9 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
 
 // ------------------------------------------------------------------ epilogue
 template <int OUT>
-__device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, int32_t col0, const float (&z)[32]) {
-  if (row >= p.M) return;
+__device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, int32_t row_end, int32_t col0,
+                                            const float (&z)[32]) {
+  if (row >= row_end) return;
   const int64_t base = static_cast<int64_t>(row) * p.N + col0;
   if (OUT == OUT_BF16) {
     __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + base;
@@ -355,7 +360,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   WorkItem w;
   long long wait_tfull = 0, busy = 0, items = 0;
   float amax = 0.0f;  // extended epilogue: this thread's max |Y|
-  while (work_next(p.sched, it, w)) {
+  while (work_next_warp(p.sched, it, w)) {   // every epilogue warp runs the iterator whole
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
     const bool final_split = (w.flags & ITEM_FINAL) != 0;
     const bool separate = p.sk_mode == SK_SEPARATE;
@@ -390,12 +395,12 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
     ptx::tc_fence_after();
 
-    const int32_t row = w.m * (kBlockM * CG) + static_cast<int32_t>(c.rank) * kBlockM + row_in_tile;
+    const int32_t row = w.row0 + static_cast<int32_t>(c.rank) * kBlockM + row_in_tile;
     const uint32_t t_row =
         tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
     float s_row = alpha, b_row = 0.0f;  // extended epilogue: this row's accumulator scale and bias
-    if (EXT) epi::row_terms(p.ext, p.bias, alpha, p.M, row, s_row, b_row);
+    if (EXT) epi::row_terms(p.ext, p.bias, alpha, w.row_end, row, s_row, b_row);
 #pragma unroll 1
     for (int ch = group * CHUNKS; ch < (group + 1) * CHUNKS; ++ch) {
       float v[64];
@@ -445,8 +450,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
         }
         const int32_t col0 = w.n * BN + c32 * 32;
         if constexpr (EXT) {
-          amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, p.M, p.N, row, col0, v + 32 * h, p.C,
-                                             amax);
+          amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, w.row_end, p.N, row, col0, v + 32 * h,
+                                             p.C, amax);
           continue;
         }
         float z[32];
@@ -473,7 +478,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = fmaxf(z[j], 0.0f);
         }
-        store_chunk<OUT>(p, row, col0, z);
+        store_chunk<OUT>(p, row, w.row_end, col0, z);
       }
     }
     ptx::tc_fence_before();

@@ -161,6 +161,9 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   s.backward = 1;  // backward tile iteration, as gemm_plan_create does by default
   s.sk_groups = 1;
   s.order = nullptr;
+  s.rows = static_cast<int32_t>(M);
+  s.bm = tst::kBlockM;
+  s.bn = static_cast<int32_t>(bn);
   if (schedule == TST_STREAMK) {
     s.grid = static_cast<int32_t>(P);
     s.dp_tiles = 0;

@@ -20,6 +20,15 @@
 //    group: same lesson, section 7.  Unit u is member u / groups of group
 //    u % groups (the lesson does not say which units form a group); each group
 //    splits its own tiles' iterations evenly over its own units.
+//  * Grouped GEMM (many problems in one persistent launch): "H100 . Kernel
+//    Design", section 10.2 "Grouped Persistent Scheduling".  The groups' tiles
+//    form one linear sequence; a unit keeps its current group (id, first linear
+//    index, tile count) and, when its index leaves that group, finds the next
+//    one: by a plain scan in single-thread roles, by the section's warp-level
+//    speculative search (32 groups per step, vote + find-first-set + shuffle)
+//    in whole warps.  The groups share N and K and differ in their rows M_g
+//    (read from device memory at run time); the mapping orders the tiles inside
+//    each group's own ceil(M_g / bm) x nt grid.
 #pragma once
 #include <stdint.h>
 
@@ -36,7 +45,7 @@ enum MapKind : int32_t {
 };
 enum SchedKind : int32_t { SCHED_STATIC = 0, SCHED_PERSISTENT = 1, SCHED_STREAMK = 2, SCHED_STREAMK_HYBRID = 3 };
 
-enum : int32_t { ITEM_FINAL = 1, ITEM_FIXUP = 2 };
+enum : int32_t { ITEM_FINAL = 1, ITEM_FIXUP = 2, ITEM_CLAMPED = 4 };
 
 struct Sched {
   int32_t mt, nt, kt;     // scheduled tiles along M and N, k-tiles along K
@@ -48,14 +57,25 @@ struct Sched {
   int32_t backward;       // Stream-K splits of a unit visited last-first
   int32_t sk_groups;      // Stream-K groups (1 = none)
   const int32_t* order;   // MAP_MORTON: (m, n) of every task, 2 ints each (host or device copy)
+  int32_t rows;           // rows of A and of the output: every tile's row bound
+  int32_t bm, bn;         // scheduled tile shape
+  // grouped GEMM (groups > 0): group g has group_rows[g] rows, stored after the previous
+  // groups' rows in A and the output, and its own group_b_rows x K block of B
+  int32_t groups;
+  const int32_t* group_rows;  // host or device copy, read as the schedule advances
+  int32_t group_b_rows;
 };
 
 struct WorkItem {
   int32_t tile;     // linear task i
-  int32_t m, n;     // F(i)
+  int32_t m, n;     // F(i) (inside the item's group for a grouped GEMM)
   int32_t k_begin;  // K_idx: first k-tile of the split
   int32_t k_count;  // k-tiles in the split
-  int32_t flags;    // ITEM_FINAL | ITEM_FIXUP
+  int32_t flags;    // ITEM_FINAL | ITEM_FIXUP | ITEM_CLAMPED (group rows cut at `rows`)
+  int32_t group;    // grouped GEMM: the item's group (0 otherwise)
+  int32_t row0;     // first row of the tile in A and the output
+  int32_t row_end;  // rows at or past this are not results of this item
+  int32_t b_row0;   // first row of the tile's block of B
 };
 
 // F(i) -> (m, n).  Grouped strips: a strip holds G tile-rows (grouped-M) or
@@ -117,10 +137,21 @@ struct WorkIter {
   int32_t group;     // Stream-K group of this unit
   int64_t sk_lo;     // remaining Stream-K iterations [sk_lo, sk_hi) within the group
   int64_t sk_hi;
+  // grouped GEMM: the current group, its first linear index, tiles, first row and rows
+  int32_t g;
+  int32_t g_tiles;
+  int64_t g_start;
+  int64_t g_row;
+  int64_t g_rows;
 };
 
 TST_HD void work_begin(const Sched& s, int32_t cta, WorkIter& it) {
   it.next_dp = cta;
+  it.g = -1;
+  it.g_tiles = 0;
+  it.g_start = 0;
+  it.g_row = 0;
+  it.g_rows = 0;
   const int32_t g = s.sk_groups > 0 ? s.sk_groups : 1;
   it.group = cta % g;
   if (s.sk_tiles > 0) {
@@ -137,7 +168,52 @@ TST_HD void work_begin(const Sched& s, int32_t cta, WorkIter& it) {
   }
 }
 
+// rows of group g as the schedule uses them: negative counts are 0, and no group
+// is taken to be longer than the whole output
+TST_HD int64_t group_row_count(const Sched& s, int32_t g) {
+  const int64_t r = s.group_rows[g];
+  return r < 0 ? 0 : (r > s.rows ? s.rows : r);
+}
+
+TST_HD int32_t group_tile_count(const Sched& s, int64_t rows) {
+  return static_cast<int32_t>((rows + s.bm - 1) / s.bm) * s.nt;
+}
+
+// the item for linear index i of the current group of `it`
+TST_HD void grouped_item(const Sched& s, const WorkIter& it, int64_t i, WorkItem& w) {
+  Sched sg = s;
+  sg.mt = static_cast<int32_t>((it.g_rows + s.bm - 1) / s.bm);
+  w.tile = static_cast<int32_t>(i);
+  tile_coord(sg, static_cast<int32_t>(i - it.g_start), w.m, w.n);   // local offset k = i - start
+  w.k_begin = 0;
+  w.k_count = s.kt;
+  w.flags = ITEM_FINAL;
+  w.group = it.g;
+  const int64_t row0 = it.g_row + static_cast<int64_t>(w.m) * s.bm;
+  const int64_t end = it.g_row + it.g_rows;
+  if (end > s.rows) w.flags |= ITEM_CLAMPED;
+  w.row0 = static_cast<int32_t>(row0 < s.rows ? row0 : s.rows);
+  w.row_end = static_cast<int32_t>(end < s.rows ? end : s.rows);
+  w.b_row0 = it.g * s.group_b_rows + w.n * s.bn;
+}
+
 TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
+  if (s.groups > 0) {
+    // grouped: persistent over the concatenated tiles; a unit's indices only grow, so
+    // its current group advances by a plain scan
+    if (it.g >= s.groups) return false;
+    const int64_t i = it.next_dp;
+    while (it.g < 0 || i >= it.g_start + it.g_tiles) {
+      it.g_start += it.g_tiles;
+      it.g_row += it.g_rows;
+      if (++it.g >= s.groups) return false;
+      it.g_rows = group_row_count(s, it.g);
+      it.g_tiles = group_tile_count(s, it.g_rows);
+    }
+    it.next_dp += s.grid;
+    grouped_item(s, it, i, w);
+    return true;
+  }
   if (it.next_dp < s.dp_tiles) {
     w.tile = it.next_dp;
     w.k_begin = 0;
@@ -169,8 +245,66 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
     return false;
   }
   tile_coord(s, w.tile, w.m, w.n);
+  w.group = 0;
+  w.row0 = w.m * s.bm;
+  w.row_end = s.rows;
+  w.b_row0 = w.n * s.bn;
   return true;
 }
+
+#if defined(__CUDACC__)
+// work_next for a whole warp (all 32 lanes call it together and get the same item).
+// A grouped GEMM finds the group of a new index by the warp-level speculative search:
+// lane l loads group base + l and computes its tiles, inclusive warp scans give each
+// lane's range, a vote picks the lane whose range holds the index and shuffles
+// broadcast its group; with no hit the warp moves on by 32 groups.
+__device__ __forceinline__ bool work_next_warp(const Sched& s, WorkIter& it, WorkItem& w) {
+  if (s.groups == 0) return work_next(s, it, w);
+  if (it.g >= s.groups) return false;
+  const int64_t i = it.next_dp;
+  if (it.g < 0 || i >= it.g_start + it.g_tiles) {
+    const int lane = threadIdx.x & 31;
+    int32_t base = it.g + 1;
+    int64_t start = it.g_start + it.g_tiles;
+    int64_t row = it.g_row + it.g_rows;
+    bool found = false;
+    while (base < s.groups) {
+      const int32_t gl = base + lane;
+      const int64_t r = gl < s.groups ? group_row_count(s, gl) : 0;
+      const int64_t t = group_tile_count(s, r);
+      int64_t incl_t = t, incl_r = r;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t ot = __shfl_up_sync(0xFFFFFFFFu, incl_t, d);
+        const int64_t orow = __shfl_up_sync(0xFFFFFFFFu, incl_r, d);
+        if (lane >= d) { incl_t += ot; incl_r += orow; }
+      }
+      const bool hit = t > 0 && start + incl_t - t <= i && i < start + incl_t;
+      const uint32_t vote = __ballot_sync(0xFFFFFFFFu, hit);
+      if (vote != 0u) {
+        const int l = __ffs(vote) - 1;
+        it.g = base + l;
+        it.g_tiles = static_cast<int32_t>(__shfl_sync(0xFFFFFFFFu, t, l));
+        it.g_rows = __shfl_sync(0xFFFFFFFFu, r, l);
+        it.g_start = start + __shfl_sync(0xFFFFFFFFu, incl_t, l) - it.g_tiles;
+        it.g_row = row + __shfl_sync(0xFFFFFFFFu, incl_r, l) - it.g_rows;
+        found = true;
+        break;
+      }
+      start += __shfl_sync(0xFFFFFFFFu, incl_t, 31);
+      row += __shfl_sync(0xFFFFFFFFu, incl_r, 31);
+      base += 32;
+    }
+    if (!found) {
+      it.g = s.groups;
+      return false;
+    }
+  }
+  it.next_dp += s.grid;
+  grouped_item(s, it, i, w);
+  return true;
+}
+#endif
 
 // ---- Stream-K member bookkeeping (separate-reduction fixup).  Member m of a
 // group of P_g members owns iterations [floor(m W / P_g), floor((m+1) W / P_g))
