@@ -29,13 +29,13 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import make_addend, make_gemm_inputs, operand_types  # noqa: E402
+from synthetic import make_addend, make_gemm_inputs, make_group_rows, operand_types  # noqa: E402
 from synthetic.workloads import WORKLOADS  # noqa: E402
 
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
 HEADLINE = "c2_bf16_4096"
 EXTRA = ["c1_bf16_256", "c2_bf16_4096_1cta", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
-         "c4_bf16_hybrid", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192"]
+         "c4_bf16_hybrid", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "g1_bf16_grouped"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
     "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
@@ -51,6 +51,8 @@ DESCR = {
                             "C a BF16 N(0,1) addend, grouped-M G=8",
     "c3m_e4m3_e5m2_8192": "FP8 GEMM 8192^3, A e4m3 x B e5m2, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, "
                           "persistent",
+    "g1_bf16_grouped": "grouped BF16 GEMM: 16 groups, N=K=4096, group rows summing to 16384 (uneven, seeded), "
+                       "BF16 out, one persistent launch",
 }
 L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
@@ -73,10 +75,22 @@ def is_fp8(w):
 
 def oracle_step(w, inp, rows, addend=None):
     """The oracle on output rows `rows` of workload w (FP64): the GEMM with its basic
-    epilogue, and for workloads with an extended epilogue its steps on top."""
+    epilogue, and for workloads with an extended epilogue its steps on top; a grouped
+    workload multiplies each row by its own group's block of B."""
     import oracle
     from oracle import epilogue as E
     fa, fb = operand_types(inp.dtype)
+    if "groups" in w:
+        edges = np.cumsum([0] + make_group_rows(w["groups"], w["M"], w["case"]))
+        rows = np.asarray(rows, dtype=np.int64)
+        gid = np.searchsorted(edges, rows, side="right") - 1
+        z = np.empty((rows.size, w["N"]))
+        ad = np.empty((rows.size, w["N"]))
+        for g in np.unique(gid):
+            sel = gid == g
+            z[sel], ad[sel] = oracle.gemm(inp.A, inp.B[g * w["N"]:(g + 1) * w["N"]], fa, alpha=w.get("alpha", 1.0),
+                                          rows=rows[sel], dtype_b=fb)
+        return z, ad
     epi = w.get("epi")
     if epi is None:
         return oracle.gemm(inp.A, inp.B, fa, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
@@ -92,10 +106,27 @@ def oracle_step(w, inp, rows, addend=None):
     return D, bz
 
 
+def make_inputs_for(w):
+    """Seeded inputs of workload w (a grouped workload's B holds one N x K block per group)."""
+    n_b = w["N"] * w.get("groups", 1)
+    return make_gemm_inputs(w["M"], n_b, w["K"], w["dtype"], w["dist"], case=w["case"], bias_dist=w.get("bias_dist"))
+
+
 def setup_workload(w, tst, torch):
     """Plan, pinned host inputs, device copies and the output tensor of workload w."""
-    inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
-                           bias_dist=w.get("bias_dist"))
+    inp = make_inputs_for(w)
+    if "groups" in w:
+        plan = tst.gemm_grouped_plan_create(w["groups"], w["M"], w["N"], w["K"], dtype=w["dtype"],
+                                            mapping=w["mapping"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
+                                            bn=w.get("bn", 0), cta_group=w.get("cta_group", 0))
+        a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
+        b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
+        host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory(),
+                "group_rows": torch.tensor(make_group_rows(w["groups"], w["M"], w["case"]),
+                                           dtype=torch.int32).pin_memory()}
+        dev = {k: v.cuda() for k, v in host.items()}
+        cdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8}[w["out"]]
+        return inp, plan, host, dev, torch.empty(w["M"], w["N"], dtype=cdt, device="cuda")
     epi = dict(w.get("epi") or {})
     epi_plan = {k: epi[k] for k in ("beta", "c_dtype", "bias_mode", "activation", "amax") if k in epi}
     if "c_dtype" in epi:
@@ -131,6 +162,14 @@ def run_args(dev):
     """Keyword arguments of gemm_run for the device operands of setup_workload."""
     return dict(bias=dev.get("bias"), scales=dev.get("scales"), c=dev.get("c"), d_scale=dev.get("d_scale"),
                 amax=dev.get("amax"))
+
+
+def run_once(tst, plan, dev, C, stream=None):
+    """One launch of the workload through the public API."""
+    if "group_rows" in dev:
+        tst.gemm_grouped_run(plan, dev["group_rows"], dev["A"], dev["B"], C, stream=stream, **run_args(dev))
+    else:
+        tst.gemm_run(plan, dev["A"], dev["B"], C, stream=stream, **run_args(dev))
 
 
 def addend_for(w):
@@ -313,8 +352,7 @@ def run_reference(args):
     import oracle
     oracle.build_oracle()
     w = WORKLOADS[args.workload]
-    inp = make_gemm_inputs(w["M"], w["N"], w["K"], w["dtype"], w["dist"], case=w["case"],
-                           bias_dist=w.get("bias_dist"))
+    inp = make_inputs_for(w)
     _, addend = addend_for(w)
     rows_per_step = 8
     per_step_flops = 2.0 * rows_per_step * w["N"] * w["K"]
@@ -464,6 +502,61 @@ def run_config_study(args):
               flush=True)
 
 
+CHAIN_STUDY = [(1024, 16), (2048, 16), (4096, 8)]   # (n, chain length): n x n x n BF16 GEMMs
+
+
+def run_chain_study(args):
+    """A chain of dependent GEMMs (each reads the previous output as A), launched one by one
+    and as one captured CUDA graph, with and without programmatic dependent launch."""
+    import torch
+    import tile_scheduled_tensor_gb300 as tst
+    stream = torch.cuda.Stream()
+    for n, L in CHAIN_STUDY:
+        g = torch.Generator(device="cuda").manual_seed(n)
+        X0 = torch.randn(n, n, device="cuda", generator=g).bfloat16()
+        Ws = [(torch.randn(n, n, device="cuda", generator=g) / n ** 0.5).bfloat16() for _ in range(L)]
+        outs = [torch.empty(n, n, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+        row = {"study": "dependent chain", "n": n, "length": L}
+        for pdl in (False, True):
+            plans = [tst.gemm_plan_create(n, n, n, mapping=("grouped_m", 8), schedule="persistent", out_dtype="bf16",
+                                          pdl=pdl) for _ in range(L)]
+
+            def chain():
+                x = X0
+                for plan, W, out in zip(plans, Ws, outs):
+                    tst.gemm_run(plan, x, W, out, stream=stream.cuda_stream)
+                    x = out
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    chain()
+                stream.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    chain()
+                for _ in range(args.warmup):
+                    graph.replay()
+                stream.synchronize()
+            for mode, fn in (("stream", chain), ("graph", graph.replay)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    for _ in range(args.steps):
+                        fn()
+                    e1.record(stream)
+                stream.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / (args.steps * L)
+                row[f"{mode}{'_pdl' if pdl else ''}_us_per_gemm"] = round(us, 2)
+                row[f"{mode}{'_pdl' if pdl else ''}_tflops"] = round(2.0 * n ** 3 / us / 1e6, 1)
+            for plan in plans:
+                st, word = tst.gemm_status_query(plan)
+                if st != tst.TST_OK:
+                    raise RuntimeError(f"chain n={n}: device status {tst.gemm_status_string(st)} {word:#x}")
+            del graph
+        row["tile"] = f"{plans[0].info.bm}x{plans[0].info.bn}"
+        row["grid"] = int(plans[0].info.grid)
+        print(json.dumps(row), flush=True)
+
+
 def run_role_cycles(args):
     """Per-CTA cycle counters from the kernel's debug mode: where each role waits."""
     import torch
@@ -475,9 +568,9 @@ def run_role_cycles(args):
         info = plan.info
         stats = torch.zeros(info.ctas * 8, dtype=torch.int64, device="cuda")
         for _ in range(args.warmup):
-            tst.gemm_run(plan, dev["A"], dev["B"], C, **run_args(dev))
+            run_once(tst, plan, dev, C)
         tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_ROLE_CYCLES, stats, info.ctas * 16)
-        tst.gemm_run(plan, dev["A"], dev["B"], C, **run_args(dev))
+        run_once(tst, plan, dev, C)
         st, word = tst.gemm_status_query(plan)
         if st != tst.TST_OK:
             raise RuntimeError(f"{name}: device status {tst.gemm_status_string(st)} {word:#x}")
@@ -513,6 +606,8 @@ def main():
                     help="time every mapping family on the workload and print the operand-band model")
     ap.add_argument("--config-study", action="store_true",
                     help="time every tile width x CTA group on a set of shapes against the cost model's pick")
+    ap.add_argument("--chain-study", action="store_true",
+                    help="time chains of dependent GEMMs with and without programmatic dependent launch")
     ap.add_argument("--role-cycles", action="store_true",
                     help="instead of timing, print per-role wait/busy cycle fractions (debug counters) "
                          "for the listed workloads")
@@ -537,6 +632,8 @@ def main():
             "".join(f", {kv}" for kv in args.opt) + "]"
     if args.role_cycles:
         return run_role_cycles(args)
+    if args.chain_study:
+        return run_chain_study(args)
     if args.mapping_study:
         return run_mapping_study(args)
     if args.config_study:
@@ -565,7 +662,7 @@ def main():
         return w, inp, plan, host, dev, C
 
     def launch(plan, dev, C):
-        tst.gemm_run(plan, dev["A"], dev["B"], C, stream=stream.cuda_stream, **run_args(dev))
+        run_once(tst, plan, dev, C, stream.cuda_stream)
 
     def time_device(name, steps, warmup, sampler=None):
         w, inp, plan, host, dev, C = prepare(name)

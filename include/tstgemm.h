@@ -216,6 +216,17 @@ typedef struct {
                               partial slot and a second kernel sums the slots in K order and
                               applies the epilogue (bitwise repeatable, needs no co-resident
                               grid, more workspace) */
+    int32_t pdl;           /* 1: programmatic dependent launch ("H100 . Kernel Launch", sections
+                              4-8): the run is launched so that it may start while the previous
+                              kernel on the stream is still finishing; its threads do their
+                              setup (barriers, Tensor Memory, descriptor prefetch, an L2
+                              prefetch of the first B tiles) and then wait with
+                              griddepcontrol.wait until that kernel has completed and its
+                              memory is visible, before touching any other global memory.  Each
+                              CTA signals griddepcontrol.launch_dependents once its last loads
+                              are issued, so the next kernel (launched the same way) may start
+                              early too.  Not with Stream-K fixups that need a co-resident grid
+                              (TST_ERR_UNSUPPORTED). */
 } tst_plan_options;
 
 enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2 };

@@ -173,6 +173,17 @@ def operand_types(dtype: str):
 SEED_A, SEED_B, SEED_BIAS, SEED_C = 1000, 2000, 3000, 4000
 
 
+def make_group_rows(groups: int, total: int, case: int, spread: float = 0.5):
+    """Seeded row counts of `groups` groups adding up to `total`: each group's share is
+    (1 - spread) / groups + spread * w_g / sum(w), w_g uniform in [0, 1) (seed 5000 + c),
+    rounded down, and the remainder goes to the last group."""
+    w = uniform01(5000 + case, groups)
+    share = (1.0 - spread) / groups + spread * w / w.sum()
+    rows = np.floor(share * total).astype(np.int64)
+    rows[-1] += total - rows.sum()
+    return [int(r) for r in rows]
+
+
 def make_addend(M: int, N: int, dist: str, case: int, dtype: str = "bf16"):
     """Seeded M x N addend matrix for beta * C: (array to upload, its FP64 values).
     dtype 'bf16' gives BF16 bit patterns (uint16), 'f32' FP32 values."""

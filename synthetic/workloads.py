@@ -45,6 +45,10 @@ WORKLOADS = {
                                  bias_dist="normal",
                                  epi=dict(beta=1.0, c_dtype="bf16", c_dist="normal", bias_mode="col",
                                           activation="gelu", amax=True, d_scale=32.0)),
+    # grouped GEMM (a mixture-of-experts layer): 16 groups sharing N = K = 4096, group rows
+    # summing to 16384 (seeded, uneven), BF16 -> BF16, grouped-M G=8 inside each group
+    "g1_bf16_grouped": dict(M=16384, N=4096, K=4096, dtype="bf16", dist="normal", case=7, out="bf16",
+                            mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2, groups=16),
     # 8192^3 with mixed FP8 formats: A e4m3, B e5m2 (tensor-wise scales) -> BF16, grouped-N G=16
     "c3m_e4m3_e5m2_8192": dict(M=8192, N=8192, K=8192, dtype="e4m3_e5m2", dist="normal", case=3, out="bf16",
                                mapping=("grouped_n", 16), schedule="persistent", bn=256, cta_group=2,

@@ -184,3 +184,29 @@ def test_grouped_all_empty():
     B = np.concatenate([B] * 8)
     st, word, D = _run(plan, [0] * 8, A, B, 256, 128)
     assert st == tst.TST_OK and np.isnan(host_values(D)).all()
+
+
+def test_grouped_workload_full_size_sampled_rows():
+    """The 16-group workload (N = K = 4096, 16384 rows) in the launch configuration the
+    benchmark times: sampled rows of every group against the oracle."""
+    from gemm_check import assert_close, sample_rows
+    from synthetic.workloads import WORKLOADS
+    w = WORKLOADS["g1_bf16_grouped"]
+    G, M, N, K = w["groups"], w["M"], w["N"], w["K"]
+    rows = synthetic.make_group_rows(G, M, w["case"])
+    inp = synthetic.make_gemm_inputs(M, G * N, K, w["dtype"], w["dist"], case=w["case"])
+    plan = tst.gemm_grouped_plan_create(G, M, N, K, dtype=w["dtype"], mapping=w["mapping"], out_dtype=w["out"],
+                                        bn=w["bn"], cta_group=w["cta_group"])
+    D = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    tst.gemm_grouped_run(plan, torch.tensor(rows, dtype=torch.int32, device="cuda"), device_codes(inp.A),
+                         device_codes(inp.B), D)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    edges = np.cumsum([0] + rows)
+    sample = set(sample_rows(M, count=16).tolist()) | {int(e) for e in edges[1:-1]} | {int(e) - 1 for e in edges[1:]}
+    got = host_values(D)
+    for g in range(G):
+        rs = np.array(sorted(r for r in sample if edges[g] <= r < edges[g + 1]), dtype=np.int64)
+        if rs.size == 0:
+            continue
+        z, ad = oracle.gemm(inp.A, inp.B[g * N:(g + 1) * N], "bf16", rows=rs)
+        assert_close(got[rs], z, ad, "bf16", f"group {g}")

@@ -101,3 +101,16 @@ def test_fp8_format_dtypes_plan_on_the_host():
     with pytest.raises(tst.TstError) as ei:
         tst.gemm_plan_create(512, 512, 8, dtype="e5m2", host_only=True, num_sms=148)
     assert ei.value.status == tst.TST_ERR_ALIGNMENT
+
+
+def test_pdl_option_validation():
+    plan = tst.gemm_plan_create(1024, 1024, 256, host_only=True, num_sms=148, cta_group=1, schedule="persistent",
+                                pdl=True)
+    assert plan.info.grid > 0
+    # a Stream-K grid whose CTAs wait on each other cannot be a dependent launch
+    with pytest.raises(tst.TstError) as ei:
+        tst.gemm_plan_create(1920, 1920, 4096, host_only=True, num_sms=148, cta_group=1, schedule="streamk", pdl=True)
+    assert ei.value.status == tst.TST_ERR_UNSUPPORTED
+    ok = tst.gemm_plan_create(1920, 1920, 4096, host_only=True, num_sms=148, cta_group=1, schedule="streamk",
+                              sk_fixup="separate", pdl=True)
+    assert ok.info.kernels_per_run == 2

@@ -90,7 +90,7 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      out_dtype="f32", alpha: float = 1.0, has_bias: bool = False, relu: bool = False,
                      use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_forward: bool = False,
                      host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
-                     stages: int = 0, bk: int = 0, sk_groups: int = 0, sk_fixup="deterministic",
+                     stages: int = 0, bk: int = 0, sk_groups: int = 0, sk_fixup="deterministic", pdl: bool = False,
                      beta: float = 0.0, has_c: bool = False, c_dtype="f32", bias_mode=None, activation=None,
                      row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
                      amax: bool = False, aux: bool = False, aux_dtype="f32") -> Plan:
@@ -102,7 +102,7 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
                                   int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
-                                  int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"))
+                                  int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"), int(bool(pdl)))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \
@@ -137,14 +137,14 @@ def gemm_grouped_plan_create(groups: int, M: int, N: int, K: int, dtype="bf16", 
                              col_scale: bool = False, d_scale: bool = False, amax: bool = False, aux: bool = False,
                              aux_dtype="f32", bn: int = 0, num_ctas: int = 0, host_only: bool = False,
                              num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0, stages: int = 0,
-                             bk: int = 0) -> Plan:
+                             bk: int = 0, pdl: bool = False) -> Plan:
     """Plan `groups` GEMMs sharing N and K in one persistent launch: A holds the groups'
     rows one after another (at most M in all), B one N x K matrix per group; the row
     counts are given to gemm_grouped_run as a device int32 array."""
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), 0, int(bool(host_only)), int(num_sms), int(cta_group),
-                                  int(timeout_ns), int(stages), int(bk), 0, 0)
+                                  int(timeout_ns), int(stages), int(bk), 0, 0, int(bool(pdl)))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \

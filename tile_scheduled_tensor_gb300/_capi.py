@@ -57,7 +57,7 @@ class tst_plan_options(ctypes.Structure):
     _fields_ = [("bn", ctypes.c_int32), ("num_ctas", ctypes.c_int32), ("sk_forward", ctypes.c_int32),
                 ("host_only", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_int64), ("stages", ctypes.c_int32), ("bk", ctypes.c_int32),
-                ("sk_groups", ctypes.c_int32), ("sk_fixup", ctypes.c_int32)]
+                ("sk_groups", ctypes.c_int32), ("sk_fixup", ctypes.c_int32), ("pdl", ctypes.c_int32)]
 
 
 class tst_plan_info(ctypes.Structure):

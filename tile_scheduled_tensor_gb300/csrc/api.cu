@@ -50,8 +50,9 @@ struct tst_plan {
   // plan-owned device memory: [status word | locks | workspace]
   void* dev_block = nullptr;
   size_t dev_bytes = 0, reset_bytes = 0;
-  uint32_t* d_status = nullptr;
-  int32_t* d_locks = nullptr;
+  unsigned long long* d_status = nullptr;   // (run_id << 32) | status of that run
+  unsigned long long* d_locks = nullptr;
+  uint32_t run_id = 0;                      // id of the last launch (tags status and locks)
   float* d_ws = nullptr;
   // debug
   int32_t debug_flags = 0;
@@ -245,7 +246,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   tst_plan_options o{};
   if (opts) o = *opts;
   if (o.bn != 0 && o.bn != 128 && o.bn != 256) return TST_ERR_UNSUPPORTED;
-  if (o.num_ctas < 0 || o.num_sms < 0 || o.timeout_ns < 0) return TST_ERR_INVALID_ARG;
+  if (o.num_ctas < 0 || o.num_sms < 0 || o.timeout_ns < 0 || o.pdl < 0 || o.pdl > 1) return TST_ERR_INVALID_ARG;
   const int elt = dtype == TST_BF16 ? 2 : 1;
   if ((K * elt) % 16 != 0) return TST_ERR_ALIGNMENT;  // TMA row stride must be a multiple of 16 bytes
 
@@ -405,6 +406,8 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     delete p;
     return TST_ERR_UNSUPPORTED;
   }
+  // dependent launch and a grid whose CTAs wait on each other do not mix
+  if (o.pdl && s.sk_tiles > 0 && p->sk_mode != TST_SK_SEPARATE) { delete p; return TST_ERR_UNSUPPORTED; }
   // separate reduction: as many partial slots per split tile as units can touch one tile
   if (p->sk_mode == TST_SK_SEPARATE) {
     int32_t most = 1;
@@ -432,7 +435,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   // partial tile per CTA-half of each split tile
   const size_t slots = static_cast<size_t>(s.sk_tiles) * p->cg * p->sk_slots;
   const size_t status_bytes = 256;
-  const size_t lock_bytes = ((slots * 4 + 255) / 256) * 256;
+  const size_t lock_bytes = ((slots * 8 + 255) / 256) * 256;
   const size_t ws_bytes = slots * tst::kBlockM * p->bn * sizeof(float);
   p->reset_bytes = status_bytes + lock_bytes;
   p->dev_bytes = status_bytes + lock_bytes + ws_bytes;
@@ -448,8 +451,8 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
       return TST_ERR_CUDA;
     }
     char* base = static_cast<char*>(p->dev_block);
-    p->d_status = reinterpret_cast<uint32_t*>(base);
-    p->d_locks = reinterpret_cast<int32_t*>(base + status_bytes);
+    p->d_status = reinterpret_cast<unsigned long long*>(base);
+    p->d_locks = reinterpret_cast<unsigned long long*>(base + status_bytes);
     p->d_ws = ws_bytes ? reinterpret_cast<float*>(base + status_bytes + lock_bytes) : nullptr;
     if (!p->order_host.empty()) {
       const size_t ob = p->order_host.size() * sizeof(int32_t);
@@ -661,6 +664,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.relu = e.activation == TST_ACT_RELU ? 1 : 0;
   kp.use_scales = e.use_scales ? 1 : 0;
   kp.fmt_ab = p->fmt_ab;
+  kp.pdl = p->opts.pdl;
   if (p->ext_on) {
     tst::EpiExt& x = kp.ext;
     x.on = 1;
@@ -684,8 +688,11 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.sk_slots = p->sk_slots;
   kp.timeout_ns = p->timeout_ns;
 
-  // status word and Stream-K locks start at zero for every launch, and so does amax
-  if (cudaMemsetAsync(p->dev_block, 0, p->reset_bytes, stream) != cudaSuccess) return TST_ERR_CUDA;
+  // the status word and the Stream-K locks need no clearing: this launch's run id tags
+  // what it writes, and values tagged with an earlier id never match (0 is never used)
+  if (++p->run_id == 0) p->run_id = 1;
+  kp.run_id = p->run_id;
+  // amax starts at zero for every launch
   if (kp.ext.amax && cudaMemsetAsync(kp.ext.amax, 0, sizeof(float), stream) != cudaSuccess) return TST_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
@@ -693,22 +700,30 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   cfg.blockDim = dim3(tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (p->cg == 2) {
     // the two CTAs of a pair run as a cluster of 2 (co-scheduled on a pair of SMs)
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   } else if (p->sched.sk_tiles > 0 && p->sk_mode != TST_SK_SEPARATE) {
     // Stream-K splits wait on each other across CTAs: ask for a co-resident grid
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
   }
+  if (p->opts.pdl) {
+    // may start while the previous kernel on the stream finishes (the kernel waits with
+    // griddepcontrol.wait before its dependent accesses)
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   void* args[] = {&kp};
   if (cudaLaunchKernelExC(&cfg, p->kernel, args) != cudaSuccess) {
     cudaGetLastError();
@@ -799,8 +814,10 @@ tst_status gemm_status_query(tst_plan* p, uint32_t* detail) {
   if (p->host_only || p->dev_block == nullptr) return TST_ERR_NO_DEVICE;
   if (!p->ran) return TST_OK;
   if (cudaStreamSynchronize(p->last_stream) != cudaSuccess) return TST_ERR_CUDA;
-  uint32_t word = 0;
-  if (cudaMemcpy(&word, p->d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return TST_ERR_CUDA;
+  unsigned long long tagged = 0;
+  if (cudaMemcpy(&tagged, p->d_status, sizeof(tagged), cudaMemcpyDeviceToHost) != cudaSuccess) return TST_ERR_CUDA;
+  // a word tagged with another run id was left by an earlier launch: the last one recorded nothing
+  const uint32_t word = (tagged >> 32) == p->run_id ? static_cast<uint32_t>(tagged) : 0u;
   if (detail) *detail = word;
   switch (word & 0xFFu) {
     case 0: return TST_OK;

@@ -66,11 +66,29 @@ struct Ctx {
   int32_t unit;         // scheduling unit: the CTA (CG = 1) or the CTA pair (CG = 2)
 };
 
+// Record `code` in the status word unless this launch has recorded one already (a word
+// tagged with another launch's run id is stale and is replaced).
+__device__ __forceinline__ void record_status(const KernelParams& p, uint32_t code, uint32_t role) {
+  const unsigned long long mine = (static_cast<unsigned long long>(p.run_id) << 32) | code | (role << 8) |
+                                  (static_cast<unsigned long long>(blockIdx.x) << 16);
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(p.status);
+  while ((old >> 32) != p.run_id) {
+    const unsigned long long seen = atomicCAS(p.status, old, mine);
+    if (seen == old) break;
+    old = seen;
+  }
+}
+
 template <int CG>
 __device__ __forceinline__ void raise_error(const KernelParams& p, const Ctx& c, uint32_t code, uint32_t role) {
   *c.abort = 1u;
   if (CG == 2) ptx::st_cluster_u32(c.peer_abort, 1u);
-  atomicCAS(p.status, 0u, code | (role << 8) | (static_cast<uint32_t>(blockIdx.x) << 16));
+  record_status(p, code, role);
+}
+
+// a lock value of this launch
+__device__ __forceinline__ unsigned long long lock_value(const KernelParams& p, int32_t k_tiles) {
+  return (static_cast<unsigned long long>(p.run_id) << 32) | static_cast<uint32_t>(k_tiles);
 }
 
 // Wait until the phase with `parity` of mbarrier `bar` completes.  Returns false
@@ -92,14 +110,16 @@ __device__ __forceinline__ bool wait_phase(const KernelParams& p, const Ctx& c, 
   }
 }
 
-// Bounded wait for a Stream-K lock to reach exactly `want` k-tiles.
+// Bounded wait for a Stream-K lock of this launch to reach exactly `want` k-tiles.
 template <int CG>
-__device__ __forceinline__ bool wait_lock(const KernelParams& p, const Ctx& c, const int32_t* lock, int32_t want) {
-  if (ptx::ld_acquire_gpu(lock) == want) return true;
+__device__ __forceinline__ bool wait_lock(const KernelParams& p, const Ctx& c, const unsigned long long* lock,
+                                          int32_t want) {
+  const unsigned long long target = lock_value(p, want);
+  if (ptx::ld_acquire_gpu_u64(lock) == target) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t spin = 1;; ++spin) {
     __nanosleep(64);
-    if (ptx::ld_acquire_gpu(lock) == want) return true;
+    if (ptx::ld_acquire_gpu_u64(lock) == target) return true;
     if ((spin & 15u) == 0u) {
       if (*c.abort) return false;
       if (ptx::globaltimer() - t0 > p.timeout_ns) {
@@ -110,16 +130,19 @@ __device__ __forceinline__ bool wait_lock(const KernelParams& p, const Ctx& c, c
   }
 }
 
-// Bounded wait for a Stream-K lock to reach at least `want` (non-deterministic
-// fixup: the workspace has been initialised by the first split).
+// Bounded wait for a Stream-K lock of this launch to reach at least `want`
+// (non-deterministic fixup: the workspace has been initialised by the first split).
 template <int CG>
-__device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const Ctx& c, const int32_t* lock,
-                                                   int32_t want) {
-  if (ptx::ld_acquire_gpu(lock) >= want) return true;
+__device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const Ctx& c,
+                                                   const unsigned long long* lock, int32_t want) {
+  auto reached = [&](unsigned long long v) {
+    return (v >> 32) == p.run_id && static_cast<uint32_t>(v) >= static_cast<uint32_t>(want);
+  };
+  if (reached(ptx::ld_acquire_gpu_u64(lock))) return true;
   const uint64_t t0 = ptx::globaltimer();
   for (uint32_t spin = 1;; ++spin) {
     __nanosleep(64);
-    if (ptx::ld_acquire_gpu(lock) >= want) return true;
+    if (reached(ptx::ld_acquire_gpu_u64(lock))) return true;
     if ((spin & 15u) == 0u) {
       if (*c.abort) return false;
       if (ptx::globaltimer() - t0 > p.timeout_ns) {
@@ -160,7 +183,7 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     // grouped GEMM: the group sizes add up to more rows than the output holds; the rows past
     // it are never stored, and the run reports a device check (once, without stopping)
     if ((w.flags & ITEM_CLAMPED) && leader)
-      atomicCAS(p.status, 0u, ST_DEVICE_CHECK | (ROLE_PRODUCER << 8) | (static_cast<uint32_t>(blockIdx.x) << 16));
+      record_status(p, ST_DEVICE_CHECK, ROLE_PRODUCER);
     const int32_t m0 = w.row0 + static_cast<int32_t>(c.rank) * kBlockM;    // row of A
     const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * BN_CTA;   // row of B
     for (int32_t kb = w.k_begin; kb < w.k_begin + w.k_count; ++kb) {
@@ -190,6 +213,8 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     }
     ++seq;
   }
+  // every load of this CTA is issued: a dependent grid may be scheduled
+  if (p.pdl) ptx::griddep_launch_dependents();
   if (p.stats) p.stats[blockIdx.x * kStatSlots + STAT_PROD_WAIT_EMPTY] = wait_empty;
   if (!ok && leader) {
     // aborting: wait (bounded) until the loads already issued have landed.  For a
@@ -490,8 +515,10 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
       else ptx::mbar_arrive(bar_tempty + 8 * acc);
       if (fixup && !final_split && !separate && !(p.debug_flags & DBG_SKIP_LOCK)) {
         // the lock counts the k-tiles accumulated in the workspace
-        if (p.sk_mode == SK_ATOMIC && w.k_begin > 0) ptx::red_add_release_gpu(p.locks + slot, w.k_count);
-        else ptx::st_release_gpu(p.locks + slot, w.k_begin + w.k_count);
+        if (p.sk_mode == SK_ATOMIC && w.k_begin > 0)
+          ptx::red_add_release_gpu_u64(p.locks + slot, static_cast<unsigned long long>(w.k_count));
+        else
+          ptx::st_release_gpu_u64(p.locks + slot, lock_value(p, w.k_begin + w.k_count));
       }
     }
     if (++acc == Cfg::NACC) { acc = 0; acc_phase ^= 1u; }
@@ -584,6 +611,25 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
   if (CG == 2) ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+
+  if (p.pdl) {
+    // launched while the previous kernel may still run: before waiting for it, pull the
+    // first B tiles of this unit's first item (B does not depend on it, typically weights)
+    // into L2; then every thread waits before touching other global memory
+    if (warp == 0 && lane == 0 && p.sched.groups == 0) {
+      WorkIter it;
+      WorkItem w;
+      work_begin(p.sched, c.unit, it);
+      if (work_next(p.sched, it, w)) {
+        constexpr int BK = (DT == DT_BF16 ? 64 : 128) * KA;
+        const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (BN / CG);
+        const int32_t kend = w.k_begin + (w.k_count < p.stages ? w.k_count : p.stages);
+        for (int32_t kb = w.k_begin; kb < kend; ++kb)
+          for (int a = 0; a < KA; ++a) ptx::tma_prefetch_l2_2d(&p.tmap_b, kb * BK + a * (BK / KA), n0);
+      }
+    }
+    ptx::griddep_wait();
+  }
 
   if (warp == 0) {
     if (lane == 0) run_producer<BN, DT, CG, KA>(p, c, smem_a, smem_b, bar_full, bar_empty);

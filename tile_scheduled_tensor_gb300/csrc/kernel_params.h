@@ -69,8 +69,8 @@ struct KernelParams {
   const float* bias;        // FP32[N] or null
   const float* scales;      // FP32[2] = {sA, sB} or null
   float* workspace;         // Stream-K partial tiles, one BM x BN FP32 slot per split tile
-  int32_t* locks;           // one lock per split tile: k-tiles accumulated so far
-  uint32_t* status;         // device status word
+  unsigned long long* locks;   // one lock per split tile: (run_id << 32) | k-tiles accumulated so far
+  unsigned long long* status;  // device status word: (run_id << 32) | code | role << 8 | CTA << 16
   int32_t* trace;           // debug trace or null
   unsigned long long* stats;  // debug role-cycle counters (kStatSlots per CTA) or null
   int32_t M, N, K;
@@ -86,6 +86,9 @@ struct KernelParams {
   uint32_t fmt_ab;          // FP8 operand formats for the instruction descriptor: A in bits 7-9,
                             // B in bits 10-12 (0 = e4m3, 1 = e5m2); 0 for BF16
   EpiExt ext;               // extended epilogue (ext.on == 0: the basic one above)
+  int32_t pdl;              // launched as a programmatic dependent: wait before global accesses
+  uint32_t run_id;          // tags the status word and the locks of this launch (never 0), so
+                            // that values left by earlier launches need no clearing
 };
 
 // Tile configuration for a scheduled tile width BN, a CTA group of CG CTAs

@@ -177,12 +177,12 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   }
 
   // ---- scratch layout: [status | locks | partial tiles]; reject what does not fit
-  const size_t lock_bytes = ((static_cast<size_t>(s.sk_tiles) * 4 + 255) / 256) * 256;
+  const size_t lock_bytes = ((static_cast<size_t>(s.sk_tiles) * 8 + 255) / 256) * 256;
   const size_t ws_bytes = static_cast<size_t>(s.sk_tiles) * tst::kBlockM * bn * sizeof(float);
   if (kStatusBytes + lock_bytes + ws_bytes > kScratchBytes) return TST_ERR_UNSUPPORTED;
   char* base = static_cast<char*>(dev->scratch);
-  uint32_t* status = device_status ? device_status : reinterpret_cast<uint32_t*>(base);
-  int32_t* locks = reinterpret_cast<int32_t*>(base + kStatusBytes);
+  auto* status = reinterpret_cast<unsigned long long*>(base);   // (run_id << 32) | status
+  auto* locks = reinterpret_cast<unsigned long long*>(base + kStatusBytes);
   float* ws = reinterpret_cast<float*>(base + kStatusBytes + lock_bytes);
 
   // ---- kernel and its shared-memory limit on this device
@@ -224,11 +224,10 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   kp.sk_mode = tst::SK_DETERMINISTIC;
   kp.sk_slots = 1;
   kp.timeout_ns = 10ull * 1000 * 1000 * 1000;
+  kp.run_id = 1;   // the status word and the locks are cleared below for every call
 
   // ---- clear what must start at zero: the status word and the locks
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (device_status && cudaMemsetAsync(device_status, 0, sizeof(uint32_t), stream) != cudaSuccess)
-    return TST_ERR_CUDA;
   if (cudaMemsetAsync(base, 0, kStatusBytes + lock_bytes, stream) != cudaSuccess) return TST_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
@@ -248,5 +247,9 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
     cudaGetLastError();
     return TST_ERR_CUDA;
   }
+  // the caller's status word: the low half of this call's tagged word (code | role | CTA)
+  if (device_status &&
+      cudaMemcpyAsync(device_status, base, sizeof(uint32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return TST_ERR_CUDA;
   return TST_OK;
 }
