@@ -49,6 +49,12 @@ Readings where the pages leave a step open (each is listed in the design notes):
     second pass sums the slots of a tile in K order.  The slot of a split is
     (member index of its unit) - (member index of the unit holding the tile's
     first k-tile);
+  * HyTiS ("H100 . Stream-K scheduling", section 8: heterogeneous tile sizes
+    in one launch, large tiles for the full waves, smaller ones for the partial
+    wave, no reduction): the first T - (T mod P) tasks run whole; each of the
+    last T mod P tasks is split along N into two half-width tiles, and the
+    grid stride continues over those 2 (T mod P) half tiles.  The page's
+    example shrinks both dimensions; only N is halved here;
   * Stream-K groups ("H100 . Stream-K scheduling", section 7): the Stream-K
     tiles are dealt to g groups by output_tile_id = id_in_group * g + group;
     unit u belongs to group u mod g as its member u // g (the pages do not say
@@ -61,7 +67,7 @@ from dataclasses import dataclass
 from functools import lru_cache
 
 LINEAR_NFAST, LINEAR_MFAST, GROUPED_M, GROUPED_N, BLOCK_2D, MORTON = 0, 1, 2, 3, 4, 5
-STATIC, PERSISTENT, STREAMK, STREAMK_HYBRID = 0, 1, 2, 3
+STATIC, PERSISTENT, STREAMK, STREAMK_HYBRID, HYTIS = 0, 1, 2, 3, 4
 
 
 def ceil_div(a: int, b: int) -> int:
@@ -226,6 +232,31 @@ def hybrid_split_count(T: int, P: int) -> int:
     if tail == 0 or 2 * tail > P:
         return 0
     return tail
+
+
+@dataclass(frozen=True)
+class Half:
+    """Half of task `tile` along N (HyTiS partial wave): half 0 holds the tile's first
+    BN/2 columns, half 1 the rest."""
+    tile: int
+    half: int
+
+
+def hytis_split(T: int, P: int):
+    """(whole tasks, half tiles) of the HyTiS schedule: the partial wave's T mod P tasks
+    are split in two along N."""
+    tail = T % P
+    return T - tail, 2 * tail
+
+
+def hytis_items(u: int, P: int, T: int):
+    """Worker u's list: whole tasks u, u + P, ... below T - (T mod P), then, continuing the
+    same stride over the half tiles, Half(T - tail + j // 2, j % 2)."""
+    dp, halves = hytis_split(T, P)
+    out = []
+    for x in range(u, dp + halves, P):
+        out.append(x if x < dp else Half(dp + (x - dp) // 2, (x - dp) % 2))
+    return out
 
 
 def work_items(schedule: int, u: int, P: int, T: int, Kt: int, backward: bool = False, groups: int = 1):

@@ -484,3 +484,42 @@ def test_cost_model_terms_worked_by_hand():
     # 152 blocks fill one wave; 153 need two half-empty ones: same bytes per block, twice the score
     assert a["wave_efficiency"] == 1.0 and b["wave_efficiency"] == 153 / 304
     assert abs(b["score"] / a["score"] - 2.0) < 1e-12
+
+
+# ---------------------------------------------------------------- HyTiS
+
+@pytest.mark.parametrize("T,P", [(225, 148), (512, 74), (148, 148), (10, 148), (300, 7), (1, 1)])
+def test_hytis_covers_every_column_once(T, P):
+    """Every task's columns are covered exactly once: whole, or by its two halves."""
+    dp, halves = S.hytis_split(T, P)
+    assert dp + halves // 2 == T and dp % P == 0 and halves // 2 < P
+    seen = {}
+    for u in range(P):
+        for it in S.hytis_items(u, P, T):
+            if isinstance(it, S.Half):
+                key = (it.tile, it.half)
+                assert it.tile >= dp and key not in seen and (it.tile, "whole") not in seen
+            else:
+                key = (it, "whole")
+                assert it < dp and key not in seen
+            seen[key] = u
+    for t in range(T):
+        whole = (t, "whole") in seen
+        halves_t = [(t, h) in seen for h in (0, 1)]
+        assert whole != all(halves_t) and (whole or all(halves_t)) and not (whole and any(halves_t))
+
+
+def test_hytis_reduces_to_persistent_without_a_tail():
+    for u in range(74):
+        assert S.hytis_items(u, 74, 74 * 6) == list(range(u, 74 * 6, 74))
+
+
+def test_hytis_c4_example_by_hand():
+    # 225 tasks on 148 workers: one full wave, 77 tasks split in two = 154 half tiles; worker 0
+    # takes task 0, then half-tile index 148 - 148 = 0 -> Half(148, 0); worker 5 takes task 5 and
+    # Half(150, 1) (index 153 - 148 = 5 -> task 148 + 2, half 1); workers 0-5 take a second half
+    # tile 148 indices later: worker 0 -> index 296 - 148 = 148 -> Half(148 + 74, 0)
+    assert S.hytis_split(225, 148) == (148, 154)
+    assert S.hytis_items(0, 148, 225) == [0, S.Half(148, 0), S.Half(222, 0)]
+    assert S.hytis_items(5, 148, 225) == [5, S.Half(150, 1), S.Half(224, 1)]
+    assert S.hytis_items(6, 148, 225) == [6, S.Half(151, 0)]
