@@ -35,7 +35,7 @@ from synthetic.workloads import WORKLOADS  # noqa: E402
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
 HEADLINE = "c2_bf16_4096"
 EXTRA = ["c1_bf16_256", "c2_bf16_4096_1cta", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
-         "c4_bf16_hybrid", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "g1_bf16_grouped"]
+         "c4_bf16_hybrid", "c4_bf16_hytis", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "g1_bf16_grouped"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
     "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
@@ -46,6 +46,8 @@ DESCR = {
     "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, Stream-K with fixup",
     "c4_bf16_persistent": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, grouped-M G=8 persistent",
     "c4_bf16_hybrid": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, data-parallel waves + Stream-K tail",
+    "c4_bf16_hytis": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, HyTiS: 148 tiles of 128x128 whole, the other 77 "
+                     "as 154 tiles of 128x64",
     "c5_bf16_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=bf16(ReLU(0.5 acc + bias)), grouped-M G=8",
     "c6_bf16_fp8_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=e4m3(32 GELU(acc + C + bias)) with amax, "
                             "C a BF16 N(0,1) addend, grouped-M G=8",

@@ -116,12 +116,20 @@ typedef struct {
  *                   left-to-right order.
  *   STREAMK_HYBRID: full data-parallel waves, Stream-K over the last T mod P
  *                   tiles only; stays fully data-parallel when that tail wave is
- *                   more than half full. */
+ *                   more than half full.
+ *   HYTIS:          two tile sizes in one launch ("H100 . Stream-K scheduling",
+ *                   section 8): the first T - (T mod P) tasks run whole as in
+ *                   PERSISTENT, and each of the last T mod P tasks (the partial
+ *                   wave) is split along N into two tiles of bn / 2 columns, which
+ *                   the grid stride takes after the whole ones; no reduction, no
+ *                   workspace.  Work items of a half tile carry flag bit 3, and bit
+ *                   4 for its second half. */
 typedef enum {
     TST_STATIC = 0,
     TST_PERSISTENT = 1,
     TST_STREAMK = 2,
-    TST_STREAMK_HYBRID = 3
+    TST_STREAMK_HYBRID = 3,
+    TST_HYTIS = 4
 } tst_schedule;
 
 /* Fused epilogue: out = cast( relu?( alpha * sA * sB * acc + bias[n] ) ). */

@@ -31,6 +31,9 @@ WORKLOADS = {
     # the same problem, grouped-M G=8 persistent (the data-parallel comparison)
     "c4_bf16_persistent": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                                mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),
+    # the same problem, HyTiS: full waves of 128x128 tiles, the partial wave as 128x64 tiles
+    "c4_bf16_hytis": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
+                          mapping=("grouped_m", 8), schedule="hytis", bn=128, cta_group=1),
     # the same problem, hybrid: full data-parallel waves, Stream-K over the tail wave only
     "c4_bf16_hybrid": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                            mapping=("grouped_m", 8), schedule="streamk_hybrid", bn=128, cta_group=1),

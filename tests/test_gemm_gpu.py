@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 MAPPINGS = [("linear_nfast", 1), ("linear_mfast", 1), ("grouped_m", 8), ("grouped_n", 16), ("grouped_m", 3),
             ("block_2d", 4), ("morton", 1)]
-SCHEDULES = ["static", "persistent", "streamk", "streamk_hybrid"]
+SCHEDULES = ["static", "persistent", "streamk", "streamk_hybrid", "hytis"]
 
 
 def _gemm(M, N, K, dtype="bf16", dist="normal", case=11, out="f32", bias_dist=None, **plan_kw):
@@ -310,6 +310,34 @@ def test_device_trace_matches_oracle_enumeration(cta_group):
             exp = [(u, j, s.tile, *S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, s.tile), s.k_idx, s.k_count,
                     int(s.is_final) | (2 if s.requires_fixup else 0)) for j, s in enumerate(want)]
             assert got == exp, f"{sched} cta {u}"
+
+
+@pytest.mark.parametrize("cta_group,bn", [(1, 128), (1, 256), (2, 128), (2, 256)])
+def test_hytis_trace_and_exact(cta_group, bn):
+    """HyTiS: the device walks the oracle's list (whole tiles, then half-width tiles of the
+    partial wave), and small integers come out exact (the half tiles' N = bn / 2 MMAs and
+    half-height B loads cover every column once)."""
+    w = dict(WORKLOADS["c4_bf16_streamk"], schedule="hytis", cta_group=cta_group, bn=bn, dist="int:8", K=2048)
+    plan = plan_for(w)
+    info = plan.info
+    cap = info.grid * info.max_items_per_cta * 8
+    trace = torch.full((cap,), -1, dtype=torch.int32, device="cuda")
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TRACE, trace, cap)
+    inp = make_inputs(w)
+    C = run_gemm(plan, inp, "f32")
+    z, _ = oracle_rows(inp, w)
+    assert np.array_equal(host_values(C), z)
+    t = trace.view(info.grid, info.max_items_per_cta, 8).cpu().numpy()
+    halves_seen = 0
+    for u in range(info.grid):
+        got = [tuple(int(x) for x in r[2:]) for r in t[u] if r[0] != -1]
+        want = []
+        for it in S.hytis_items(u, info.grid, info.tiles):
+            tile, fl = (it.tile, 1 | 8 | (16 if it.half else 0)) if isinstance(it, S.Half) else (it, 1)
+            want.append((tile, *S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, tile), 0, info.kt, fl))
+            halves_seen += isinstance(it, S.Half)
+        assert got == want, u
+    assert halves_seen == 2 * (info.tiles % info.grid)
 
 
 @pytest.mark.parametrize("name", ["c1_bf16_256"])

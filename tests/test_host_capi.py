@@ -252,3 +252,24 @@ def test_auto_tile_matches_cost_model_oracle(shape, dtype, out):
     # fixing one of the two leaves the other to the model
     q = tst.gemm_plan_create(M, N, K, dtype=dtype, out_dtype=out, host_only=True, num_sms=152, bn=128)
     assert q.info.bn == 128
+
+
+@pytest.mark.parametrize("M,N,K,bn,cg,P", [(1920, 1920, 4096, 128, 1, 148), (4096, 4096, 512, 128, 2, 74),
+                                           (1000, 3000, 256, 256, 1, 37), (300, 200, 128, 128, 1, 148)])
+def test_hytis_work_items_match_oracle(M, N, K, bn, cg, P):
+    plan = _host_plan(M, N, K, mapping=("grouped_m", 8), schedule="hytis", bn=bn, cta_group=cg, num_ctas=P)
+    info = plan.info
+    T = info.tiles
+    dp, halves = S.hytis_split(T, P)
+    assert info.dp_tiles == dp and info.sk_tiles == 0
+    for u in range(info.grid):
+        got = tst.gemm_work_items(plan, u)
+        want = []
+        for it in S.hytis_items(u, info.grid if info.grid < P else P, T):
+            if isinstance(it, S.Half):
+                m, n = S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, it.tile)
+                want.append((it.tile, m, n, 0, info.kt, 1 | 8 | (16 if it.half else 0)))
+            else:
+                m, n = S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, it)
+                want.append((it, m, n, 0, info.kt, 1))
+        assert got == want, u

@@ -16,7 +16,7 @@ from ._capi import (TST_BF16, TST_E4M3, TST_E5M2, TST_E4M3_E5M2, TST_E5M2_E4M3, 
                     TST_ACT_NONE, TST_ACT_RELU, TST_ACT_GELU, TST_ACT_SILU, TST_BIAS_NONE, TST_BIAS_COL,
                     TST_BIAS_ROW,
                     TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N,
-                    TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID,
+                    TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID, TST_HYTIS,
                     TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG_ROLE_CYCLES,
                     TST_SK_DETERMINISTIC, TST_SK_ATOMIC, TST_SK_SEPARATE,
                     TST_OK, TST_ERR_INVALID_ARG, TST_ERR_UNSUPPORTED, TST_ERR_ALIGNMENT, TST_ERR_OOM,
@@ -35,7 +35,7 @@ _MAPS = {"linear_nfast": TST_MAP_LINEAR_NFAST, "linear_mfast": TST_MAP_LINEAR_MF
          "block_2d": _capi.TST_MAP_BLOCK_2D, "morton": _capi.TST_MAP_MORTON}
 _FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separate": TST_SK_SEPARATE}
 _SCHED = {"static": TST_STATIC, "persistent": TST_PERSISTENT, "streamk": TST_STREAMK,
-          "streamk_hybrid": TST_STREAMK_HYBRID}
+          "streamk_hybrid": TST_STREAMK_HYBRID, "hytis": TST_HYTIS}
 
 
 class TstError(RuntimeError):

@@ -64,7 +64,7 @@ struct tst_plan {
   const void* kernel = nullptr;
   const void* tm_A = nullptr;
   const void* tm_B = nullptr;
-  CUtensorMap tmap_a{}, tmap_b{};
+  CUtensorMap tmap_a{}, tmap_b{}, tmap_b_half{};
   cudaStream_t last_stream = nullptr;
   bool ran = false;
 };
@@ -233,7 +233,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if ((mapping.kind == TST_MAP_GROUPED_M || mapping.kind == TST_MAP_GROUPED_N || mapping.kind == TST_MAP_BLOCK_2D) &&
       mapping.group < 1)
     return TST_ERR_INVALID_ARG;
-  if (schedule < TST_STATIC || schedule > TST_STREAMK_HYBRID) return TST_ERR_INVALID_ARG;
+  if (schedule < TST_STATIC || schedule > TST_HYTIS) return TST_ERR_INVALID_ARG;
   if (groups < 0 || groups >= (1 << 24)) return TST_ERR_INVALID_ARG;
   // grouped GEMM: persistent over the groups' tiles, and a mapping that needs no per-grid table
   if (groups > 0 && (schedule != TST_PERSISTENT || mapping.kind == TST_MAP_MORTON)) return TST_ERR_UNSUPPORTED;
@@ -392,6 +392,15 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     case TST_STREAMK:
       s.grid = static_cast<int32_t>(P); s.dp_tiles = 0; s.sk_tiles = static_cast<int32_t>(T);
       break;
+    case TST_HYTIS: {
+      // the partial wave's tasks become two half-width tiles each
+      const int64_t tail = T % P;
+      s.dp_tiles = static_cast<int32_t>(T - tail);
+      s.narrow_tiles = static_cast<int32_t>(2 * tail);
+      s.sk_tiles = 0;
+      s.grid = static_cast<int32_t>(std::min(P, T - tail + 2 * tail));
+      break;
+    }
     case TST_STREAMK_HYBRID: {
       const int64_t sk = hybrid_split_tiles(T, P);
       s.sk_tiles = static_cast<int32_t>(sk);
@@ -639,12 +648,17 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   }
   if (B != p->tm_B) {
     if (!encode_operand(&p->tmap_b, B, p->dtype, p->b_rows, p->K, box_k, p->bn / p->cg)) return TST_ERR_CUDA;
+    // HyTiS half-width tiles read half of the B rows per stage
+    if (p->sched.narrow_tiles > 0 &&
+        !encode_operand(&p->tmap_b_half, B, p->dtype, p->b_rows, p->K, box_k, p->bn / (2 * p->cg)))
+      return TST_ERR_CUDA;
     p->tm_B = B;
   }
 
   tst::KernelParams kp = {};
   kp.tmap_a = p->tmap_a;
   kp.tmap_b = p->tmap_b;
+  kp.tmap_b_half = p->tmap_b_half;
   kp.C = C;
   kp.bias = bias;
   kp.scales = scales;

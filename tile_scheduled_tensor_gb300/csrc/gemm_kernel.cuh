@@ -184,13 +184,16 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     // it are never stored, and the run reports a device check (once, without stopping)
     if ((w.flags & ITEM_CLAMPED) && leader)
       record_status(p, ST_DEVICE_CHECK, ROLE_PRODUCER);
+    const bool narrow = (w.flags & ITEM_NARROW) != 0;   // half-width tile: half of B per stage
     const int32_t m0 = w.row0 + static_cast<int32_t>(c.rank) * kBlockM;    // row of A
-    const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * BN_CTA;   // row of B
+    const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (narrow ? BN_CTA / 2 : BN_CTA);   // row of B
+    const CUtensorMap* tmap_b = narrow ? &p.tmap_b_half : &p.tmap_b;
+    const uint32_t stage_bytes = narrow ? Cfg::A_BYTES + Cfg::B_BYTES / 2 : Cfg::STAGE_BYTES;
     for (int32_t kb = w.k_begin; kb < w.k_begin + w.k_count; ++kb) {
       const long long t0 = p.stats ? clock64() : 0;
       if (!wait_phase<CG>(p, c, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
       if (p.stats) wait_empty += clock64() - t0;
-      if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * Cfg::STAGE_BYTES);
+      if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * stage_bytes);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
 #pragma unroll
@@ -200,10 +203,10 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
           const int32_t kx = kb * BK + a * BK_ATOM;
           if (CG == 2) {
             ptx::tma_load_2d_pair(sa, &p.tmap_a, full_target + 8 * stage, kx, m0);
-            ptx::tma_load_2d_pair(sb, &p.tmap_b, full_target + 8 * stage, kx, n0);
+            ptx::tma_load_2d_pair(sb, tmap_b, full_target + 8 * stage, kx, n0);
           } else {
             ptx::tma_load_2d(sa, &p.tmap_a, bar_full + 8 * stage, kx, m0);
-            ptx::tma_load_2d(sb, &p.tmap_b, bar_full + 8 * stage, kx, n0);
+            ptx::tma_load_2d(sb, tmap_b, bar_full + 8 * stage, kx, n0);
           }
         }
       }
@@ -241,7 +244,10 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
                                         uint32_t bar_tempty, uint32_t bar_drain, int issuer) {
   using Cfg = TileCfg<BN, CG, KA>;
   // FP8: the operand formats (e4m3 / e5m2, possibly mixed) come from the plan
-  const uint32_t idesc = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN) | (DT == DT_BF16 ? 0u : p.fmt_ab);
+  const uint32_t fmt = DT == DT_BF16 ? 0u : p.fmt_ab;
+  const uint32_t idesc_full = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN) | fmt;
+  // HyTiS half-width tiles: N = BN / 2 over the first half of the B stage (a prefix of rows)
+  const uint32_t idesc_half = ptx::make_idesc(DT == DT_BF16 ? 1u : 0u, kBlockM * CG, BN / 2) | fmt;
   int stage = 0;
   uint32_t phase = 0;
   int acc = 0;
@@ -260,6 +266,7 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
     if (p.stats) wait_tempty += clock64() - t0;
     ptx::tc_fence_after();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS + issuer * BN);
+    const uint32_t idesc = (w.flags & ITEM_NARROW) ? idesc_half : idesc_full;
     for (int32_t i = 0; i < w.k_count; ++i) {
       const long long t1 = p.stats ? clock64() : 0;
       // the stage was filled by TMA and announced on its mbarrier: the wait alone
@@ -426,8 +433,11 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
     float s_row = alpha, b_row = 0.0f;  // extended epilogue: this row's accumulator scale and bias
     if (EXT) epi::row_terms(p.ext, p.bias, alpha, w.row_end, row, s_row, b_row);
+    // 64-column TMEM loads of this item (a half-width tile has half of them), dealt to the
+    // epilogue warpgroups in turn
+    const int nchunks = (w.flags & ITEM_NARROW) ? BN / 128 : BN / 64;
 #pragma unroll 1
-    for (int ch = group * CHUNKS; ch < (group + 1) * CHUNKS; ++ch) {
+    for (int ch = group; ch < nchunks; ch += EW) {
       float v[64];
       if (Cfg::DUAL) {
         // the two issuers' accumulators, columns [0, BN) and [BN, 2 BN): add them
@@ -473,7 +483,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[32 * h + j] = __ldcg(wsc + j * kBlockM) + v[32 * h + j];
         }
-        const int32_t col0 = w.n * BN + c32 * 32;
+        const int32_t col0 = w.col0 + c32 * 32;
         if constexpr (EXT) {
           amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, w.row_end, p.N, row, col0, v + 32 * h,
                                              p.C, amax);

@@ -65,6 +65,7 @@ constexpr int kStatSlots = 8;
 struct KernelParams {
   CUtensorMap tmap_a;       // A: M x K, K contiguous, box BK x 128, 128-byte swizzle
   CUtensorMap tmap_b;       // B: N x K, K contiguous, box BK x BN, 128-byte swizzle
+  CUtensorMap tmap_b_half;  // the same B with half-height boxes (HyTiS half-width tiles)
   void* C;                  // M x N row-major, FP32 or BF16
   const float* bias;        // FP32[N] or null
   const float* scales;      // FP32[2] = {sA, sB} or null

@@ -20,6 +20,11 @@
 //    group: same lesson, section 7.  Unit u is member u / groups of group
 //    u % groups (the lesson does not say which units form a group); each group
 //    splits its own tiles' iterations evenly over its own units.
+//  * HyTiS ("H100 . Stream-K scheduling", section 8): tile sizes mixed in one
+//    launch, whole tiles for the full waves and smaller ones for the partial
+//    wave, with no reduction.  Tasks [0, dp_tiles) run whole; each of the
+//    following narrow_tiles / 2 tasks is split along N into two half-width
+//    tiles, which the grid stride walks after the whole ones.
 //  * Grouped GEMM (many problems in one persistent launch): "H100 . Kernel
 //    Design", section 10.2 "Grouped Persistent Scheduling".  The groups' tiles
 //    form one linear sequence; a unit keeps its current group (id, first linear
@@ -43,9 +48,12 @@ namespace tst {
 enum MapKind : int32_t {
   MAP_LINEAR_NFAST = 0, MAP_LINEAR_MFAST = 1, MAP_GROUPED_M = 2, MAP_GROUPED_N = 3, MAP_BLOCK_2D = 4, MAP_MORTON = 5
 };
-enum SchedKind : int32_t { SCHED_STATIC = 0, SCHED_PERSISTENT = 1, SCHED_STREAMK = 2, SCHED_STREAMK_HYBRID = 3 };
+enum SchedKind : int32_t {
+  SCHED_STATIC = 0, SCHED_PERSISTENT = 1, SCHED_STREAMK = 2, SCHED_STREAMK_HYBRID = 3, SCHED_HYTIS = 4
+};
 
-enum : int32_t { ITEM_FINAL = 1, ITEM_FIXUP = 2, ITEM_CLAMPED = 4 };
+// ITEM_NARROW: a half-width tile (HyTiS partial wave); ITEM_HALF1: its second half of the columns
+enum : int32_t { ITEM_FINAL = 1, ITEM_FIXUP = 2, ITEM_CLAMPED = 4, ITEM_NARROW = 8, ITEM_HALF1 = 16 };
 
 struct Sched {
   int32_t mt, nt, kt;     // scheduled tiles along M and N, k-tiles along K
@@ -54,6 +62,7 @@ struct Sched {
   int32_t grid;           // CTAs launched
   int32_t dp_tiles;       // tasks [0, dp_tiles) are computed whole, grid-stride
   int32_t sk_tiles;       // tasks [dp_tiles, dp_tiles + sk_tiles) are split by Stream-K
+  int32_t narrow_tiles;   // HyTiS: half-width tiles after the whole ones (2 per split task)
   int32_t backward;       // Stream-K splits of a unit visited last-first
   int32_t sk_groups;      // Stream-K groups (1 = none)
   const int32_t* order;   // MAP_MORTON: (m, n) of every task, 2 ints each (host or device copy)
@@ -76,6 +85,7 @@ struct WorkItem {
   int32_t row0;     // first row of the tile in A and the output
   int32_t row_end;  // rows at or past this are not results of this item
   int32_t b_row0;   // first row of the tile's block of B
+  int32_t col0;     // first output column of the tile
 };
 
 // F(i) -> (m, n).  Grouped strips: a strip holds G tile-rows (grouped-M) or
@@ -189,6 +199,7 @@ TST_HD void grouped_item(const Sched& s, const WorkIter& it, int64_t i, WorkItem
   w.k_count = s.kt;
   w.flags = ITEM_FINAL;
   w.group = it.g;
+  w.col0 = w.n * s.bn;
   const int64_t row0 = it.g_row + static_cast<int64_t>(w.m) * s.bm;
   const int64_t end = it.g_row + it.g_rows;
   if (end > s.rows) w.flags |= ITEM_CLAMPED;
@@ -214,11 +225,21 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
     grouped_item(s, it, i, w);
     return true;
   }
+  int32_t half_col = 0;   // HyTiS: column offset of a half-width tile inside its task
   if (it.next_dp < s.dp_tiles) {
     w.tile = it.next_dp;
     w.k_begin = 0;
     w.k_count = s.kt;
     w.flags = ITEM_FINAL;
+    it.next_dp += s.grid;
+  } else if (it.next_dp < s.dp_tiles + s.narrow_tiles) {
+    // the stride continues over the half tiles: j -> task dp_tiles + j / 2, half j % 2
+    const int32_t j = it.next_dp - s.dp_tiles;
+    w.tile = s.dp_tiles + j / 2;
+    w.k_begin = 0;
+    w.k_count = s.kt;
+    w.flags = ITEM_FINAL | ITEM_NARROW | ((j & 1) ? ITEM_HALF1 : 0);
+    half_col = (j & 1) * (s.bn / 2);
     it.next_dp += s.grid;
   } else if (it.sk_lo < it.sk_hi) {
     int64_t t, start, end;
@@ -248,7 +269,8 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
   w.group = 0;
   w.row0 = w.m * s.bm;
   w.row_end = s.rows;
-  w.b_row0 = w.n * s.bn;
+  w.col0 = w.n * s.bn + half_col;
+  w.b_row0 = w.col0;
   return true;
 }
 
