@@ -223,7 +223,10 @@ typedef struct {
                               TST_SK_SEPARATE: no split waits, every split writes its own
                               partial slot and a second kernel sums the slots in K order and
                               applies the epilogue (bitwise repeatable, needs no co-resident
-                              grid, more workspace) */
+                              grid, more workspace); TST_SK_TMA: the non-deterministic protocol
+                              with each partial chunk staged in shared memory and stored or
+                              added into the workspace by a TMA bulk tensor copy
+                              (cp.async.bulk.tensor / cp.reduce.async.bulk.tensor .add) */
     int32_t pdl;           /* 1: programmatic dependent launch ("H100 . Kernel Launch", sections
                               4-8): the run is launched so that it may start while the previous
                               kernel on the stream is still finishing; its threads do their
@@ -237,7 +240,7 @@ typedef struct {
                               (TST_ERR_UNSUPPORTED). */
 } tst_plan_options;
 
-enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2 };
+enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2, TST_SK_TMA = 3 };
 
 /* What the plan decided (for logging and tests). */
 typedef struct {

@@ -242,7 +242,7 @@ def test_streamk_groups_exact_and_traced(groups, cta_group):
     assert_close(host_values(b1)[rows], z2, ad2, "f32", f"groups={groups}")
 
 
-@pytest.mark.parametrize("fixup", ["atomic", "separate"])
+@pytest.mark.parametrize("fixup", ["atomic", "separate", "tma"])
 @pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("schedule,groups", [("streamk", 1), ("streamk", 4), ("streamk_hybrid", 1)])
 def test_streamk_fixup_modes(fixup, cta_group, schedule, groups):
@@ -268,9 +268,10 @@ def test_streamk_fixup_modes(fixup, cta_group, schedule, groups):
         assert torch.equal(a, b) and torch.equal(a, f)
 
 
-def test_atomic_fixup_lock_timeout_reports():
+@pytest.mark.parametrize("fixup", ["atomic", "tma"])
+def test_nondeterministic_fixup_lock_timeout_reports(fixup):
     w = dict(M=384, N=384, K=2048, dtype="bf16", out="f32", mapping=("grouped_m", 8), schedule="streamk", bn=128,
-             cta_group=1, sk_fixup="atomic")
+             cta_group=1, sk_fixup=fixup)
     inp = synthetic.make_gemm_inputs(384, 384, 2048, "bf16", "normal", case=26)
     plan = plan_for(w, num_ctas=16)
     tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOCK, None, 0, timeout_ns=20_000_000)
@@ -282,7 +283,7 @@ def test_atomic_fixup_lock_timeout_reports():
     tst.gemm_plan_set_debug(plan, 0, None, 0)
     C2 = run_gemm(plan, inp, "f32")
     z, ad = oracle_rows(inp, w)
-    assert_close(host_values(C2), z, ad, "f32", "after atomic-mode lock timeout")
+    assert_close(host_values(C2), z, ad, "f32", f"after a {fixup}-mode lock timeout")
 
 
 @pytest.mark.parametrize("cta_group", [1, 2])
@@ -436,3 +437,41 @@ def test_run_rejects_misaligned_and_null_pointers():
     with pytest.raises(tst.TstError) as e:
         tst.gemm_run(plan, 0, buf, C)
     assert e.value.status == tst.TST_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("cta_group,bn", [(1, 128), (1, 256), (2, 128), (2, 256)])
+def test_tma_fixup_exact_and_within_bound(cta_group, bn):
+    """Stream-K with the TMA fixup (partial chunks stored / added into the workspace by bulk
+    tensor copies): small integers exact (every FP32 sum exact in any order), random inputs
+    within the bound, repeated runs on one plan (the run-tagged locks need no clearing)."""
+    w = dict(WORKLOADS["c4_bf16_streamk"], cta_group=cta_group, bn=bn, sk_fixup="tma", dist="int:8", K=4096)
+    plan = plan_for(w)
+    inp = make_inputs(w)
+    z, _ = oracle_rows(inp, w)
+    dev = to_device(inp)
+    for _ in range(3):
+        assert np.array_equal(host_values(run_gemm(plan, inp, "f32", dev)), z)
+    wr = dict(WORKLOADS["c4_bf16_streamk"], cta_group=cta_group, bn=bn, sk_fixup="tma")
+    inp = make_inputs(wr)
+    C = run_gemm(plan_for(wr), inp, "f32")
+    z, ad = oracle_rows(inp, wr, rows=sample_rows(wr["M"]))
+    assert_close(host_values(C)[sample_rows(wr["M"])], z, ad, "f32", "tma fixup")
+
+
+def test_tma_fixup_extended_epilogue():
+    """TMA fixup with the extended-epilogue kernel (two epilogue warpgroups, one staging
+    buffer each)."""
+    from oracle import epilogue as E
+    w = dict(WORKLOADS["c4_bf16_streamk"], K=2048, dist="int:8")
+    inp = make_inputs(w)
+    plan = tst.gemm_plan_create(w["M"], w["N"], w["K"], mapping=w["mapping"], schedule="streamk", out_dtype="f32",
+                                bn=128, cta_group=1, sk_fixup="tma", bias_mode="row", amax=True)
+    bias = torch.arange(w["M"], dtype=torch.float32, device="cuda") % 7
+    amax = torch.zeros(4, device="cuda")
+    C = torch.empty(w["M"], w["N"], device="cuda")
+    A, B, _, _ = to_device(inp)
+    tst.gemm_run(plan, A, B, C, bias=bias, amax=amax)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    acc, ad = oracle.gemm(inp.A, inp.B, "bf16")
+    Z, Y, _, _ = E.apply(acc, ad, E.Epilogue(bias=bias.cpu().numpy().astype(np.float64), bias_mode=E.BIAS_ROW))
+    assert np.array_equal(host_values(C), Y) and float(amax[0]) == E.amax(Y)

@@ -33,7 +33,8 @@ _BIAS = {"none": TST_BIAS_NONE, "col": TST_BIAS_COL, "row": TST_BIAS_ROW}
 _MAPS = {"linear_nfast": TST_MAP_LINEAR_NFAST, "linear_mfast": TST_MAP_LINEAR_MFAST,
          "grouped_m": TST_MAP_GROUPED_M, "grouped_n": TST_MAP_GROUPED_N,
          "block_2d": _capi.TST_MAP_BLOCK_2D, "morton": _capi.TST_MAP_MORTON}
-_FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separate": TST_SK_SEPARATE}
+_FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separate": TST_SK_SEPARATE,
+          "tma": _capi.TST_SK_TMA}
 _SCHED = {"static": TST_STATIC, "persistent": TST_PERSISTENT, "streamk": TST_STREAMK,
           "streamk_hybrid": TST_STREAMK_HYBRID, "hytis": TST_HYTIS}
 

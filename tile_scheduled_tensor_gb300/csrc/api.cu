@@ -64,7 +64,7 @@ struct tst_plan {
   const void* kernel = nullptr;
   const void* tm_A = nullptr;
   const void* tm_B = nullptr;
-  CUtensorMap tmap_a{}, tmap_b{}, tmap_b_half{};
+  CUtensorMap tmap_a{}, tmap_b{}, tmap_b_half{}, tmap_ws{};
   cudaStream_t last_stream = nullptr;
   bool ran = false;
 };
@@ -310,7 +310,8 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     const int kdt = dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3;
     p->kernel = p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka) : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka);
     if (!p->kernel ||
-        cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, p->smem_bytes) != cudaSuccess) {
+        // the largest size any plan of this kernel asks for (the attribute is per kernel)
+        cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tst::kSmemLimit) != cudaSuccess) {
       cudaGetLastError();
       delete p;
       return TST_ERR_CUDA;
@@ -379,7 +380,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   s.backward = o.sk_forward ? 0 : 1;
   if (o.sk_groups < 0 || o.sk_groups > 8) { delete p; return TST_ERR_UNSUPPORTED; }  // at most 8 groups
   s.sk_groups = o.sk_groups > 0 ? o.sk_groups : 1;
-  if (o.sk_fixup < TST_SK_DETERMINISTIC || o.sk_fixup > TST_SK_SEPARATE) { delete p; return TST_ERR_INVALID_ARG; }
+  if (o.sk_fixup < TST_SK_DETERMINISTIC || o.sk_fixup > TST_SK_TMA) { delete p; return TST_ERR_INVALID_ARG; }
   p->sk_mode = o.sk_fixup;
   const int64_t P = o.num_ctas > 0 ? o.num_ctas : resident;
   switch (schedule) {
@@ -414,6 +415,12 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     // split tiles wait on each other: every unit must be resident at once
     delete p;
     return TST_ERR_UNSUPPORTED;
+  }
+  // TMA fixup: the kernel stages each partial chunk in shared memory past its ring
+  if (p->sk_mode == TST_SK_TMA && s.sk_tiles > 0) {
+    const int tma_smem = tst_kernel_smem_bytes_tma(p->bn, p->cg, p->ka, p->ext_on ? 2 : 1);
+    if (tma_smem > tst::kSmemLimit) { delete p; return TST_ERR_UNSUPPORTED; }
+    p->smem_bytes = tma_smem;
   }
   // dependent launch and a grid whose CTAs wait on each other do not mix
   if (o.pdl && s.sk_tiles > 0 && p->sk_mode != TST_SK_SEPARATE) { delete p; return TST_ERR_UNSUPPORTED; }
@@ -463,6 +470,22 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     p->d_status = reinterpret_cast<unsigned long long*>(base);
     p->d_locks = reinterpret_cast<unsigned long long*>(base + status_bytes);
     p->d_ws = ws_bytes ? reinterpret_cast<float*>(base + status_bytes + lock_bytes) : nullptr;
+    if (p->sk_mode == TST_SK_TMA && s.sk_tiles > 0) {
+      // the partial tiles as one 128 x (slots * bn) FP32 tensor ([column][row] per slot),
+      // written in 128 x 32 boxes
+      EncodeTiledFn fn = encode_fn();
+      cuuint64_t dims[2] = {static_cast<cuuint64_t>(tst::kBlockM), static_cast<cuuint64_t>(slots * p->bn)};
+      cuuint64_t strides[1] = {static_cast<cuuint64_t>(tst::kBlockM) * sizeof(float)};
+      cuuint32_t box[2] = {static_cast<cuuint32_t>(tst::kBlockM), 32};
+      cuuint32_t estr[2] = {1, 1};
+      if (!fn || fn(&p->tmap_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p->d_ws, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        cudaFree(p->dev_block);
+        delete p;
+        return TST_ERR_CUDA;
+      }
+    }
     if (!p->order_host.empty()) {
       const size_t ob = p->order_host.size() * sizeof(int32_t);
       if (cudaMalloc(&p->d_order, ob) != cudaSuccess ||
@@ -659,6 +682,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.tmap_a = p->tmap_a;
   kp.tmap_b = p->tmap_b;
   kp.tmap_b_half = p->tmap_b_half;
+  kp.tmap_ws = p->tmap_ws;
   kp.C = C;
   kp.bias = bias;
   kp.scales = scales;

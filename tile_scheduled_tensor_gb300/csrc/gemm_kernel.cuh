@@ -381,6 +381,13 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   const int row_in_tile = quad * 32 + lane;
   // pairs: arrive on the leader's TMEM_EMPTY barriers
   const uint32_t tempty_target = CG == 2 ? ptx::mapa(bar_tempty, 0) : bar_tempty;
+  // SK_TMA: this warpgroup's staging buffer for one 128 x 32 FP32 chunk ([column][row]), and
+  // the thread that issues its bulk copies
+  const bool tma_fixup = p.sk_mode == SK_TMA;
+  uint8_t* const smem_base = reinterpret_cast<uint8_t*>(ctl) - Cfg::MISC_OFFSET;
+  float* const staging = reinterpret_cast<float*>(smem_base + Cfg::STAGING_OFFSET + group * kStagingBytes);
+  const uint32_t staging_addr = ptx::smem_addr(staging);
+  const bool group_leader = (ep & 127) == 0;
   float alpha = p.alpha;
   if (p.use_scales) alpha = alpha * __ldg(p.scales) * __ldg(p.scales + 1);
   const bool bias_vec = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && (p.N & 3) == 0;
@@ -415,7 +422,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
       if (ok && fixup && !separate && w.k_begin > 0) {
         // deterministic: every later split waits for exactly K_idx accumulated k-tiles;
         // non-deterministic: a middle split only needs an initialised workspace
-        if (p.sk_mode == SK_ATOMIC && !final_split) ok = wait_lock_at_least<CG>(p, c, p.locks + slot, 1);
+        if ((p.sk_mode == SK_ATOMIC || p.sk_mode == SK_TMA) && !final_split)
+          ok = wait_lock_at_least<CG>(p, c, p.locks + slot, 1);
         else ok = wait_lock<CG>(p, c, p.locks + slot, w.k_begin);
       }
       *ep_ok = ok ? 1u : 0u;
@@ -466,6 +474,23 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
         }
         // workspace layout per slot: [column][row], so a warp's 32 rows are contiguous
         float* wsc = ws != nullptr ? ws + (c32 * 32) * kBlockM + row_in_tile : nullptr;
+        if (fixup && !final_split && tma_fixup) {
+          // stage the chunk, then one thread stores it (first split) or adds it (later
+          // splits) into the workspace with a bulk tensor copy
+#pragma unroll
+          for (int j = 0; j < 32; ++j) staging[j * kBlockM + row_in_tile] = v[32 * h + j];
+          ptx::fence_proxy_async_smem();
+          ptx::named_bar_sync(2 + group, 128);
+          if (group_leader) {
+            const int32_t y = slot * BN + c32 * 32;   // workspace column of the chunk
+            if (w.k_begin == 0) ptx::tma_store_2d(&p.tmap_ws, staging_addr, 0, y);
+            else ptx::tma_reduce_add_2d(&p.tmap_ws, staging_addr, 0, y);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read_all();   // the buffer may be refilled
+          }
+          ptx::named_bar_sync(2 + group, 128);
+          continue;
+        }
         if (fixup && !final_split) {
           if (w.k_begin == 0) {
 #pragma unroll
@@ -518,6 +543,10 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     ptx::tc_fence_before();
     if (fixup && (!final_split || separate)) __threadfence();  // partials visible GPU-wide before the lock moves
+    if (tma_fixup && fixup && !final_split && group_leader) {
+      ptx::bulk_wait_all();               // this warpgroup's bulk writes have landed ...
+      ptx::fence_proxy_async_global();    // ... and are ordered before the lock's release
+    }
     ptx::named_bar_sync(1, EP_THREADS);
     if (p.stats && ep == 0) { busy += clock64() - t1; ++items; }
     if (ep == 0) {
@@ -525,7 +554,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
       else ptx::mbar_arrive(bar_tempty + 8 * acc);
       if (fixup && !final_split && !separate && !(p.debug_flags & DBG_SKIP_LOCK)) {
         // the lock counts the k-tiles accumulated in the workspace
-        if (p.sk_mode == SK_ATOMIC && w.k_begin > 0)
+        if ((p.sk_mode == SK_ATOMIC || p.sk_mode == SK_TMA) && w.k_begin > 0)
           ptx::red_add_release_gpu_u64(p.locks + slot, static_cast<unsigned long long>(w.k_count));
         else
           ptx::st_release_gpu_u64(p.locks + slot, lock_value(p, w.k_begin + w.k_count));

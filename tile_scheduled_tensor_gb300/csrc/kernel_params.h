@@ -44,8 +44,10 @@ struct EpiExt {
 enum StatusCode : uint32_t { ST_OK = 0, ST_TIMEOUT = 6, ST_DEVICE_CHECK = 7 };
 enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_LOCK = 4 };
 
-// Stream-K fixup ("H100 . Stream-K scheduling", section 6)
-enum SkFixup : int32_t { SK_DETERMINISTIC = 0, SK_ATOMIC = 1, SK_SEPARATE = 2 };
+// Stream-K fixup ("H100 . Stream-K scheduling", section 6); SK_TMA: the non-deterministic
+// protocol with the partial tiles stored / added by TMA bulk copies from shared memory
+enum SkFixup : int32_t { SK_DETERMINISTIC = 0, SK_ATOMIC = 1, SK_SEPARATE = 2, SK_TMA = 3 };
+constexpr int kStagingBytes = kBlockM * 32 * 4;   // one 128 x 32 FP32 chunk per epilogue warpgroup
 
 enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8 };
 
@@ -66,6 +68,7 @@ struct KernelParams {
   CUtensorMap tmap_a;       // A: M x K, K contiguous, box BK x 128, 128-byte swizzle
   CUtensorMap tmap_b;       // B: N x K, K contiguous, box BK x BN, 128-byte swizzle
   CUtensorMap tmap_b_half;  // the same B with half-height boxes (HyTiS half-width tiles)
+  CUtensorMap tmap_ws;      // SK_TMA: the partial tiles as a 128 x (slots * BN) FP32 tensor, box 128 x 32
   void* C;                  // M x N row-major, FP32 or BF16
   const float* bias;        // FP32[N] or null
   const float* scales;      // FP32[2] = {sA, sB} or null
@@ -121,6 +124,9 @@ struct TileCfg {
   static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 2;
   static constexpr int MISC_OFFSET = BAR_OFFSET + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = 1024 + MISC_OFFSET + 16;  // + slack to align the base to 1024
+  // SK_TMA staging: one kStagingBytes buffer per epilogue warpgroup after the control block
+  static constexpr int STAGING_OFFSET = ((MISC_OFFSET + 16 + 1023) / 1024) * 1024;
+  static constexpr int smem_bytes_tma(int ew) { return 1024 + STAGING_OFFSET + ew * kStagingBytes; }
 };
 
 }  // namespace tst
@@ -177,6 +183,17 @@ inline int tst_cfg(int bn, int cg, int ka, bool smem) {
 }
 
 inline int tst_kernel_smem_bytes(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, true); }
+
+template <int CG, int KA>
+inline int tst_tma_smem_value(int bn, int ew) {
+  return bn == 256 ? tst::TileCfg<256, CG, KA>::smem_bytes_tma(ew) : tst::TileCfg<128, CG, KA>::smem_bytes_tma(ew);
+}
+
+// dynamic shared memory with the SK_TMA staging buffers (ew epilogue warpgroups)
+inline int tst_kernel_smem_bytes_tma(int bn, int cg, int ka, int ew) {
+  if (cg == 2) return ka == 2 ? tst_tma_smem_value<2, 2>(bn, ew) : tst_tma_smem_value<2, 1>(bn, ew);
+  return ka == 2 ? tst_tma_smem_value<1, 2>(bn, ew) : tst_tma_smem_value<1, 1>(bn, ew);
+}
 namespace tst {
 // Separate-reduction pass of Stream-K (streamk_reduce.cu): sums each split
 // tile's partial slots in K order and applies the epilogue.
