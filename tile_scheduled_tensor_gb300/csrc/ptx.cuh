@@ -82,7 +82,8 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 // Bulk tensor store / add-reduce from shared memory into global memory (bulk-group
-// completion), and the group waits and proxy fences around them
+// completion; the reduction offloaded to TMA, "H100 . cp.async.bulk" section 14), and
+// the group waits and proxy fences around them
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
                "r"(c0), "r"(c1), "r"(src)
