@@ -188,10 +188,16 @@ def aggregate(flops_per_rank: float, local_ms: float, world: int, max_reduce):
 
 
 def kernel_hash():
+    """Hash of the kernel sources' code (comments and blank space removed, so that a
+    comment edit does not invalidate a capture taken on the same code)."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "tile_scheduled_tensor_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tile_scheduled_tensor_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
