@@ -475,3 +475,14 @@ def test_tma_fixup_extended_epilogue():
     acc, ad = oracle.gemm(inp.A, inp.B, "bf16")
     Z, Y, _, _ = E.apply(acc, ad, E.Epilogue(bias=bias.cpu().numpy().astype(np.float64), bias_mode=E.BIAS_ROW))
     assert np.array_equal(host_values(C), Y) and float(amax[0]) == E.amax(Y)
+
+
+def test_plan_workspace_too_large_is_oom():
+    """A Stream-K plan whose partial tiles cannot fit on the device (about 2 TB for 16.7 M
+    split tiles) fails with TST_ERR_OOM at plan creation and leaves the device usable."""
+    with pytest.raises(tst.TstError) as ei:
+        tst.gemm_plan_create(524288, 524288, 64, schedule="streamk", sk_fixup="separate", bn=128, cta_group=1)
+    assert ei.value.status == tst.TST_ERR_OOM
+    inp, w, plan, C = _gemm(128, 128, 64, dist="int:4")
+    z, _ = oracle_rows(inp, w)
+    assert np.array_equal(host_values(C), z)

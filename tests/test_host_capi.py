@@ -273,3 +273,21 @@ def test_hytis_work_items_match_oracle(M, N, K, bn, cg, P):
                 m, n = S.tile_map(S.GROUPED_M, 8, info.mt, info.nt, it)
                 want.append((it, m, n, 0, info.kt, 1))
         assert got == want, u
+
+
+def test_tile_map_every_grid_up_to_40x40():
+    """The product's F(i) against the oracle on every tile grid from 1x1 to 40x40; the
+    mapping kind and G rotate over the grids so that every (kind, G) pair meets many shapes."""
+    kinds = list(MAPS)
+    groups = (1, 2, 3, 8, 16, 64)
+    case = 0
+    for Mt in range(1, 41):
+        for Nt in range(1, 41):
+            kind = kinds[case % len(kinds)]
+            G = groups[(case // len(kinds)) % len(groups)]
+            case += 1
+            p = _host_plan(Mt * 128, Nt * 128, 64, mapping=(kind, G), bn=128)
+            assert (p.info.mt, p.info.nt) == (Mt, Nt)
+            got = [tst.gemm_tile_map(p, i) for i in range(Mt * Nt)]
+            assert got == [S.tile_map(MAPS[kind], G, Mt, Nt, i) for i in range(Mt * Nt)], (kind, G, Mt, Nt)
+            assert len(set(got)) == Mt * Nt
