@@ -7,9 +7,12 @@
 // "CTA <-> output tile: mapping first, then assignment"), and sizes the tile
 // grid as ceil(M/BM) x ceil(N/BN) with ceil(K/BK) k-tiles (same page, panel
 // "Kernel Configuration Heuristic", parallelism terms).  The Stream-K
-// workspace holds one FP32 partial tile per split tile with the int locks in
-// the same allocation, zeroed before every launch ("H100 . Stream-K
-// scheduling", runguoli.com Lesson 8.1, section 6).
+// workspace holds one FP32 partial tile per split tile with the locks in the
+// same allocation ("H100 . Stream-K scheduling", runguoli.com Lesson 8.1,
+// section 6); the locks and the status word carry the launch's run id, so
+// they are zeroed once, when the plan is made, and a launch is one kernel
+// (two with the separate Stream-K reduction).  Grouped GEMMs, HyTiS, the
+// extended epilogue and dependent launches are plan options handled here too.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -1,17 +1,22 @@
 // Warp-specialised tcgen05 GEMM kernel for sm_103a, single CTA or CTA pair.
 //
-// 192 threads per CTA, one CTA per SM:
+// One CTA per SM, 192 threads (224 with a second MMA issuer, +128 with the
+// extended epilogue's second warpgroup):
 //   warp 0      TMA producer: for each k-tile of each work item, wait EMPTY[s],
 //               announce the stage's bytes on FULL[s], issue the A and B tile
 //               loads (128-byte swizzle, K-major).
 //   warp 1      MMA issuer (one thread) and TMEM owner: wait FULL[s], issue
-//               4 tcgen05.mma into the FP32 accumulator in Tensor Memory, then
-//               tcgen05.commit -> EMPTY[s] to hand the stage back; after a work
-//               item's last k-tile, commit -> TMEM_FULL[b].
+//               the k-tile's tcgen05.mma into the FP32 accumulator in Tensor
+//               Memory, then tcgen05.commit -> EMPTY[s] to hand the stage back;
+//               after a work item's last k-tile, commit -> TMEM_FULL[b].
+//   warp 6      (128-wide two-atom tiles) a second MMA issuer taking the second
+//               swizzle atom of every k-tile into its own accumulator.
 //   warps 2-5   epilogue (128 threads = 128 TMEM lanes = 128 tile rows): wait
 //               TMEM_FULL[b], load the accumulator, apply the Stream-K fixup,
-//               alpha * sA * sB * acc + bias -> ReLU -> cast, store, and release
-//               the buffer with TMEM_EMPTY[b].
+//               the epilogue (alpha * sA * sB * acc + bias -> ReLU -> cast, or the
+//               extended one), store, and release the buffer with TMEM_EMPTY[b];
+//               the extended-epilogue instance adds warps 6-9 (7-10) as a second
+//               warpgroup taking every other 64-column chunk.
 // The accumulator is multi-buffered in TMEM (512 columns = 4 x 128 or
 // 2 x 256), so the MMA of the next work item overlaps the epilogue of the
 // previous one.
@@ -25,6 +30,11 @@
 // leader's TMEM_EMPTY.  Per CTA this halves the B bytes moved from L2 and read
 // by the tensor core compared with CG = 1 at the same tile width.
 //
+// Work items come from the schedule iterator (tile_sched.h): whole tiles,
+// Stream-K splits, HyTiS half-width tiles (N halved: half-height B boxes and an
+// N / 2 instruction descriptor) or grouped-GEMM tiles (row base and row bound
+// per item).
+//
 // The FULL/EMPTY two-barrier handshake with a phase bit, the producer and
 // consumer flows and the drain follow "H100 . Kernel Design" (runguoli.com H100
 // course notes, Lesson 8), sections 4-6.  The epilogue order follows section
@@ -32,10 +42,14 @@
 // and sets the lock; a later split waits until the lock equals its K_idx, adds,
 // and either publishes a larger lock or, as the final split, finishes the tile)
 // follows section 10.3 and "H100 . Stream-K scheduling" (Lesson 8.1),
-// sections 5-6, in the deterministic mode.  The CTA pair plays the role of the
-// pages' cluster of 2 (Lesson 8, section 10.1 "Cluster and swizzling").  Where
-// the pages' Hopper designs keep the accumulator in registers (ping-pong /
-// cooperative warpgroups, setmaxnreg), this kernel keeps it in Tensor Memory.
+// sections 5-6; the non-deterministic, separate-reduction and TMA bulk-reduce
+// variants are options.  The CTA pair plays the role of the pages' cluster of 2
+// (Lesson 8, section 10.1 "Cluster and swizzling").  Where the pages' Hopper
+// designs keep the accumulator in registers (ping-pong / cooperative
+// warpgroups, setmaxnreg), this kernel keeps it in Tensor Memory.  A launch may
+// be a programmatic dependent ("H100 . Kernel Launch"): it then waits with
+// griddepcontrol.wait after its setup and signals launch_dependents after its
+// last loads.
 //
 // Every wait on an mbarrier or a lock is bounded: on expiry the kernel records
 // TIMEOUT in the status word, raises the abort flag of its CTA (and of the
