@@ -46,8 +46,8 @@ DESCR = {
     "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, Stream-K with fixup",
     "c4_bf16_persistent": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, grouped-M G=8 persistent",
     "c4_bf16_hybrid": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles, data-parallel waves + Stream-K tail",
-    "c4_bf16_hytis": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, HyTiS: 148 tiles of 128x128 whole, the other 77 "
-                     "as 154 tiles of 128x64",
+    "c4_bf16_hytis": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, HyTiS: one wave (P) of 128x128 tiles whole, "
+                     "the other 225 - P split into 128x64 tiles",
     "c5_bf16_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=bf16(ReLU(0.5 acc + bias)), grouped-M G=8",
     "c6_bf16_fp8_epilogue": "BF16 GEMM 16384x4096x4096, N(0,0.02), out=e4m3(32 GELU(acc + C + bias)) with amax, "
                             "C a BF16 N(0,1) addend, grouped-M G=8",
