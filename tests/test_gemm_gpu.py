@@ -351,7 +351,8 @@ def test_config_full_compare(name):
 
 
 @pytest.mark.parametrize("name", ["c2_bf16_4096", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk",
-                                  "c4_bf16_persistent", "c5_bf16_epilogue", "c3m_e4m3_e5m2_8192"])
+                                  "c4_bf16_persistent", "c4_bf16_hybrid", "c4_bf16_hytis", "c5_bf16_epilogue",
+                                  "c3m_e4m3_e5m2_8192"])
 def test_config_full_size_sampled_rows_and_freivalds(name):
     w = WORKLOADS[name]
     inp = make_inputs(w)
