@@ -487,3 +487,24 @@ def test_plan_workspace_too_large_is_oom():
     inp, w, plan, C = _gemm(128, 128, 64, dist="int:4")
     z, _ = oracle_rows(inp, w)
     assert np.array_equal(host_values(C), z)
+
+
+@pytest.mark.parametrize("dtype,bk", [("e4m3", 128), ("bf16", 64)])
+def test_tma_fixup_staging_in_the_ring(dtype, bk):
+    """One-atom k-tiles fill shared memory with ring stages: the TMA fixup's staging buffers
+    then take the last stages' A regions (the plan runs with fewer stages); exact result."""
+    M, N, K = 1920, 1920, 2048
+    A = synthetic.draw("int:8", 1071, M * K).reshape(M, K)
+    B = synthetic.draw("int:8", 2071, N * K).reshape(N, K)
+    enc = synthetic.bf16_bits if dtype == "bf16" else (lambda x: synthetic.e4m3_bytes(x.astype(np.float32)))
+    A, B = enc(A), enc(B)
+    full = plan_for(dict(M=M, N=N, K=K, dtype=dtype, out="f32", mapping=("grouped_m", 8), schedule="streamk",
+                         bn=128, cta_group=1, bk=bk))
+    plan = plan_for(dict(M=M, N=N, K=K, dtype=dtype, out="f32", mapping=("grouped_m", 8), schedule="streamk",
+                         bn=128, cta_group=1, bk=bk, sk_fixup="tma"), row_scale=True)
+    assert plan.info.stages < full.info.stages
+    C = torch.empty(M, N, device="cuda")
+    tst.gemm_run(plan, device_codes(A), device_codes(B), C, row_scale=torch.ones(M, device="cuda"))
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    z, _ = oracle.gemm(A, B, dtype)
+    assert np.array_equal(host_values(C), z)

@@ -41,6 +41,7 @@ struct tst_plan {
   int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
   int32_t cg = 1;              // CTAs per scheduling unit (2 = CTA pair)
   int32_t sk_mode = 0;         // tst::SkFixup
+  int32_t staging_offset = 0;  // SK_TMA staging buffers in shared memory
   int32_t sk_slots = 1;        // partial slots per split-tile half
   const void* reduce_kernel = nullptr;
   int32_t ka = 1;              // 128-byte swizzle atoms of K per pipeline stage
@@ -421,9 +422,14 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   }
   // TMA fixup: the kernel stages each partial chunk in shared memory past its ring
   if (p->sk_mode == TST_SK_TMA && s.sk_tiles > 0) {
-    const int tma_smem = tst_kernel_smem_bytes_tma(p->bn, p->cg, p->ka, p->ext_on ? 2 : 1);
-    if (tma_smem > tst::kSmemLimit) { delete p; return TST_ERR_UNSUPPORTED; }
-    p->smem_bytes = tma_smem;
+    int offset = 0, smem = 0, max_stages = 0;
+    if (!tst_tma_staging(p->bn, p->cg, p->ka, p->ext_on ? 2 : 1, &offset, &smem, &max_stages)) {
+      delete p;
+      return TST_ERR_UNSUPPORTED;
+    }
+    p->staging_offset = offset;
+    p->smem_bytes = smem;
+    p->stages = std::min(p->stages, max_stages);   // stages whose A region holds the staging stay unused
   }
   // dependent launch and a grid whose CTAs wait on each other do not mix
   if (o.pdl && s.sk_tiles > 0 && p->sk_mode != TST_SK_SEPARATE) { delete p; return TST_ERR_UNSUPPORTED; }
@@ -705,6 +711,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.relu = e.activation == TST_ACT_RELU ? 1 : 0;
   kp.use_scales = e.use_scales ? 1 : 0;
   kp.fmt_ab = p->fmt_ab;
+  kp.staging_offset = p->staging_offset;
   kp.pdl = p->opts.pdl;
   if (p->ext_on) {
     tst::EpiExt& x = kp.ext;

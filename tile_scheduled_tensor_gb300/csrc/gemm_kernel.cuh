@@ -399,7 +399,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   // the thread that issues its bulk copies
   const bool tma_fixup = p.sk_mode == SK_TMA;
   uint8_t* const smem_base = reinterpret_cast<uint8_t*>(ctl) - Cfg::MISC_OFFSET;
-  float* const staging = reinterpret_cast<float*>(smem_base + Cfg::STAGING_OFFSET + group * kStagingBytes);
+  float* const staging = reinterpret_cast<float*>(smem_base + p.staging_offset + group * kStagingBytes);
   const uint32_t staging_addr = ptx::smem_addr(staging);
   const bool group_leader = (ep & 127) == 0;
   float alpha = p.alpha;

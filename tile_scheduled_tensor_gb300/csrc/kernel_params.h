@@ -91,6 +91,7 @@ struct KernelParams {
                             // B in bits 10-12 (0 = e4m3, 1 = e5m2); 0 for BF16
   EpiExt ext;               // extended epilogue (ext.on == 0: the basic one above)
   int32_t pdl;              // launched as a programmatic dependent: wait before global accesses
+  int32_t staging_offset;   // SK_TMA: byte offset of the staging buffers from the aligned shared base
   uint32_t run_id;          // tags the status word and the locks of this launch (never 0), so
                             // that values left by earlier launches need no clearing
 };
@@ -184,15 +185,36 @@ inline int tst_cfg(int bn, int cg, int ka, bool smem) {
 
 inline int tst_kernel_smem_bytes(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, true); }
 
-template <int CG, int KA>
-inline int tst_tma_smem_value(int bn, int ew) {
-  return bn == 256 ? tst::TileCfg<256, CG, KA>::smem_bytes_tma(ew) : tst::TileCfg<128, CG, KA>::smem_bytes_tma(ew);
+// Where the SK_TMA staging buffers (one per epilogue warpgroup) go: past the control
+// block when shared memory has room, else in the A regions of the ring's last stages,
+// which the plan then leaves unused.  Returns false when neither fits.
+template <int BN, int CG, int KA>
+inline bool tst_tma_staging_cfg(int ew, int* offset, int* smem_bytes, int* max_stages) {
+  using Cfg = tst::TileCfg<BN, CG, KA>;
+  if (Cfg::smem_bytes_tma(ew) <= tst::kSmemLimit) {
+    *offset = Cfg::STAGING_OFFSET;
+    *smem_bytes = Cfg::smem_bytes_tma(ew);
+    *max_stages = Cfg::STAGES;
+    return true;
+  }
+  const int need = (ew * tst::kStagingBytes + Cfg::A_BYTES - 1) / Cfg::A_BYTES;
+  *offset = (Cfg::STAGES - need) * Cfg::A_BYTES;
+  *smem_bytes = Cfg::SMEM_BYTES;
+  *max_stages = Cfg::STAGES - need;
+  return *max_stages >= 2;
 }
 
-// dynamic shared memory with the SK_TMA staging buffers (ew epilogue warpgroups)
-inline int tst_kernel_smem_bytes_tma(int bn, int cg, int ka, int ew) {
-  if (cg == 2) return ka == 2 ? tst_tma_smem_value<2, 2>(bn, ew) : tst_tma_smem_value<2, 1>(bn, ew);
-  return ka == 2 ? tst_tma_smem_value<1, 2>(bn, ew) : tst_tma_smem_value<1, 1>(bn, ew);
+inline bool tst_tma_staging(int bn, int cg, int ka, int ew, int* offset, int* smem_bytes, int* max_stages) {
+  if (bn == 256) {
+    if (cg == 2) return ka == 2 ? tst_tma_staging_cfg<256, 2, 2>(ew, offset, smem_bytes, max_stages)
+                                : tst_tma_staging_cfg<256, 2, 1>(ew, offset, smem_bytes, max_stages);
+    return ka == 2 ? tst_tma_staging_cfg<256, 1, 2>(ew, offset, smem_bytes, max_stages)
+                   : tst_tma_staging_cfg<256, 1, 1>(ew, offset, smem_bytes, max_stages);
+  }
+  if (cg == 2) return ka == 2 ? tst_tma_staging_cfg<128, 2, 2>(ew, offset, smem_bytes, max_stages)
+                              : tst_tma_staging_cfg<128, 2, 1>(ew, offset, smem_bytes, max_stages);
+  return ka == 2 ? tst_tma_staging_cfg<128, 1, 2>(ew, offset, smem_bytes, max_stages)
+                 : tst_tma_staging_cfg<128, 1, 1>(ew, offset, smem_bytes, max_stages);
 }
 namespace tst {
 // Separate-reduction pass of Stream-K (streamk_reduce.cu): sums each split
