@@ -115,3 +115,60 @@ def grouped_work_items(u: int, P: int, rows, BM: int, Nt: int, kind: int = 0, G:
         m, n = tile_map(kind, G, Mt, Nt, i - start)     # local offset k = i - start
         out.append(GroupedItem(i, g, m, n, row + m * BM, row + int(rows[g])))
     return out
+
+
+# ---------------------------------------------------------------- groups of different shapes
+#
+# Reading (listed in the design notes): with per-group shapes (M_g, N_g, K_g) each group
+# has its own ceil(M_g / BM) x ceil(N_g / BN) grid and ceil(K_g / BK) k-tiles; the
+# concatenated sequence and the search are as above, with a group's tile count
+# computed from its own shape (the page's "each lane loads one group's shape and
+# computes its tile count").
+
+def shape_tiles(shapes, BM: int, BN: int):
+    """Tiles of each group (M_g, N_g, K_g): ceil(M_g / BM) * ceil(N_g / BN) (0 if M_g or N_g is 0)."""
+    return [ceil_div(int(m), BM) * ceil_div(int(n), BN) for m, n, _ in shapes]
+
+
+def shaped_search(i: int, tiles, st: SearchState, lanes: int = 32):
+    """The speculative search over per-group tile counts: (group, first index) of linear
+    index i, or None past the last group.  `st` carries the current group between calls."""
+    if st.group >= 0 and st.start <= i < st.start + st.tiles:
+        return st
+    G = len(tiles)
+    base, start = st.group + 1, st.start + st.tiles
+    while base < G:
+        lane_tiles = [int(tiles[base + l]) if base + l < G else 0 for l in range(lanes)]
+        incl, acc = [], 0
+        for t in lane_tiles:
+            acc += t
+            incl.append(acc)
+        hits = [lane_tiles[l] > 0 and start + incl[l] - lane_tiles[l] <= i < start + incl[l] for l in range(lanes)]
+        if any(hits):
+            l = hits.index(True)
+            return SearchState(base + l, start + incl[l] - lane_tiles[l], lane_tiles[l], 0, 0)
+        start += incl[-1]
+        base += lanes
+    return None
+
+
+@dataclass(frozen=True)
+class ShapedItem:
+    tile: int          # linear index in the concatenated sequence
+    group: int
+    m: int             # tile row inside the group
+    n: int             # tile column inside the group
+    k_tiles: int       # ceil(K_g / BK)
+
+
+def shaped_work_items(u: int, P: int, shapes, BM: int, BN: int, BK: int, kind: int = 0, G: int = 1):
+    """Persistent worker u's list over groups of different shapes: indices u, u + P, ..."""
+    tiles = shape_tiles(shapes, BM, BN)
+    out, st = [], SearchState()
+    for i in range(u, sum(tiles), P):
+        st = shaped_search(i, tiles, st)
+        g = st.group
+        Mg, Ng, Kg = (int(x) for x in shapes[g])
+        m, n = tile_map(kind, G, ceil_div(Mg, BM), ceil_div(Ng, BN), i - st.start)
+        out.append(ShapedItem(i, g, m, n, ceil_div(Kg, BK)))
+    return out

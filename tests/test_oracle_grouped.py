@@ -94,3 +94,54 @@ def test_empty_groups_and_no_work():
     assert GR.speculative_search(0, [0, 0], 128, 3, GR.SearchState()) is None
     items = GR.grouped_work_items(0, 1, [0, 5, 0, 0, 130], 128, 1)
     assert [(it.group, it.m, it.row0, it.row_end) for it in items] == [(1, 0, 0, 5), (4, 0, 5, 135), (4, 1, 133, 135)]
+
+
+# ---------------------------------------------------------------- groups of different shapes
+
+def _shapes(seed, G):
+    r = synthetic.splitmix64(seed, 3 * G) % np.uint64(700)
+    shapes = [(int(r[3 * g]), int(r[3 * g + 1]) + 1, 64 * (int(r[3 * g + 2]) % 9 + 1)) for g in range(G)]
+    return [(0, n, k) if g % 5 == 3 else (m, n, k) for g, (m, n, k) in enumerate(shapes)]
+
+
+@pytest.mark.parametrize("G", [1, 9, 40, 75])
+def test_shaped_search_equals_prefix_scan(G):
+    shapes = _shapes(G, G)
+    tiles = GR.shape_tiles(shapes, 128, 256)
+    edges = np.cumsum([0] + tiles)
+    for P in (1, 7, 152):
+        st = GR.SearchState()
+        for i in range(0, int(edges[-1]) + P, P):
+            st = GR.shaped_search(i, tiles, st)
+            if i >= edges[-1]:
+                assert st is None
+                break
+            g = int(np.searchsorted(edges, i, side="right")) - 1
+            assert (st.group, st.start) == (g, int(edges[g]))
+
+
+@pytest.mark.parametrize("kind,Gm", [(S.LINEAR_NFAST, 1), (S.GROUPED_M, 8), (S.BLOCK_2D, 2)])
+def test_shaped_items_cover_every_group_once(kind, Gm):
+    shapes = _shapes(77, 23)
+    BM, BN, BK = 128, 128, 64
+    seen = {}
+    for u in range(13):
+        for it in GR.shaped_work_items(u, 13, shapes, BM, BN, BK, kind, Gm):
+            key = (it.group, it.m, it.n)
+            assert key not in seen
+            seen[key] = u
+            assert it.k_tiles == -(-shapes[it.group][2] // BK)
+    for g, (m, n, _) in enumerate(shapes):
+        want = {(g, a, b) for a in range(-(-m // BM)) for b in range(-(-n // BN))}
+        assert want == {k for k in seen if k[0] == g}
+
+
+def test_shared_n_k_shapes_reduce_to_the_row_grouped_schedule():
+    rows = [300, 0, 1000, 57, 640]
+    N, K, BM, BN = 520, 256, 128, 128
+    shapes = [(r, N, K) for r in rows]
+    Nt = -(-N // BN)
+    for u in range(5):
+        a = [(it.tile, it.group, it.m, it.n) for it in GR.shaped_work_items(u, 5, shapes, BM, BN, 64, S.GROUPED_M, 8)]
+        b = [(it.tile, it.group, it.m, it.n) for it in GR.grouped_work_items(u, 5, rows, BM, Nt, S.GROUPED_M, 8)]
+        assert a == b
