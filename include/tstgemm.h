@@ -249,7 +249,7 @@ typedef struct {
                                   128 for e4m3 */
     int32_t stages;            /* shared-memory ring depth */
     int32_t mt, nt, kt;        /* tiles along M, N and k-tiles along K */
-    int64_t tiles;             /* T = mt * nt */
+    int64_t tiles;             /* T = mt * nt (groups of different shapes: the sum of their grids) */
     int32_t grid;              /* scheduling units launched (CTAs or CTA pairs) */
     int32_t num_sms;           /* SMs planned for */
     int32_t sk_tiles;          /* tiles handled by Stream-K (0 if none) */
@@ -340,6 +340,34 @@ tst_status gemm_grouped_plan_create(tst_plan **plan, int32_t groups, int64_t M, 
  * INVALID_ARG for a plan that is not grouped or a NULL group_rows. */
 tst_status gemm_grouped_run(tst_plan *plan, const int32_t *group_rows, const void *A, const void *B,
                             void *D, const tst_epilogue_args *args, void *stream);
+
+/* Grouped GEMM over groups of different shapes ("H100 . Kernel Design", section
+ * 10.2: each group's tile count comes from its own shape): group g is the GEMM
+ *
+ *   D_g[i][j] = epilogue( sum_k A_g[i][k] * B_g[j][k] ),  A_g M[g] x K[g], B_g N[g] x K[g],
+ *
+ * with its own matrices (row-major, K contiguous; D_g M[g] x N[g]).  The shapes are
+ * HOST arrays read here (M[g], N[g] >= 0, K[g] > 0, K[g] * elt a multiple of 16 bytes);
+ * the groups' tiles, ceil(M[g] / bm) x ceil(N[g] / bn) each, form one linear sequence
+ * walked by persistent CTAs as in gemm_grouped_plan_create, and each tile takes
+ * ceil(K[g] / bk) k-tiles.  The epilogue may use alpha, the tensor-wise scales, the
+ * activation, the output scale, amax and the output type; per-element operands (bias,
+ * C, row / column scales, aux) are TST_ERR_UNSUPPORTED.  gemm_work_items enumerates a
+ * unit's list (the shapes are known on the host). */
+tst_status gemm_grouped_array_plan_create(tst_plan **plan, int32_t groups, const int64_t *M, const int64_t *N,
+                                          const int64_t *K, tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                                          const tst_epilogue_ex *epi, const tst_plan_options *opts);
+
+/* Launch a grouped GEMM of different shapes.  A, B, D: HOST arrays of `groups`
+ * DEVICE pointers (16-byte aligned; NULL allowed for a group with M[g] or N[g] = 0).
+ * When the pointers differ from the previous run the call writes one A and one B
+ * tensor map per group and the output pointers to plan-owned device memory, with
+ * copies ordered on `stream` (the host waits for the stream's earlier work first);
+ * a run with the same pointers launches at once.  args as in gemm_run_epi.
+ * Errors: INVALID_ARG (a plan not made by gemm_grouped_array_plan_create, NULL
+ * arrays or pointers of non-empty groups), ALIGNMENT, NO_DEVICE, CUDA. */
+tst_status gemm_grouped_array_run(tst_plan *plan, const void *const *A, const void *const *B, void *const *D,
+                                  const tst_epilogue_args *args, void *stream);
 
 /* The work list of scheduling unit `cta` of a grouped plan for the HOST array
  * group_rows (the device's walk for those group sizes; pure host computation).

@@ -210,3 +210,69 @@ def test_grouped_workload_full_size_sampled_rows():
             continue
         z, ad = oracle.gemm(inp.A, inp.B[g * N:(g + 1) * N], "bf16", rows=rs)
         assert_close(got[rs], z, ad, "bf16", f"group {g}")
+
+
+# ---------------------------------------------------------------- groups of different shapes
+
+def _array_case(seed, G, dtype):
+    r = synthetic.splitmix64(seed, 3 * G) % np.uint64(600)
+    k_unit = 64 if dtype == "bf16" else 128
+    shapes = [(0 if g % 5 == 2 else int(r[3 * g]) + 1, int(r[3 * g + 1]) + 1, k_unit * (int(r[3 * g + 2]) % 6 + 1))
+              for g in range(G)]
+    fa, fb = synthetic.operand_types(dtype)
+    enc = {"bf16": synthetic.bf16_bits, "e4m3": lambda x: synthetic.e4m3_bytes(x.astype(np.float32)),
+           "e5m2": lambda x: synthetic.e5m2_bytes(x.astype(np.float32))}
+    As, Bs = [], []
+    for g, (m, n, k) in enumerate(shapes):
+        As.append(enc[fa](synthetic.draw("int:8", 4100 + 7 * seed + g, max(m, 1) * k).reshape(max(m, 1), k))[:m])
+        Bs.append(enc[fb](synthetic.draw("int:8", 4600 + 7 * seed + g, n * k).reshape(n, k)))
+    return shapes, As, Bs, fa, fb
+
+
+def _array_run(plan, shapes, As, Bs, out, **args):
+    dA = [device_codes(a) if m and n else None for (m, n, _), a in zip(shapes, As)]
+    dB = [device_codes(b) if m and n else None for (m, n, _), b in zip(shapes, Bs)]
+    dD = [torch.full((m, n), float("nan"), dtype=out, device="cuda") if m and n else None for m, n, _ in shapes]
+    tst.gemm_grouped_array_run(plan, dA, dB, dD, **args)
+    return dD
+
+
+@pytest.mark.parametrize("cta_group,bn,dtype", [(1, 128, "bf16"), (2, 256, "bf16"), (1, 256, "e4m3"),
+                                                (2, 128, "e4m3_e5m2")])
+def test_grouped_array_small_integers_exact(cta_group, bn, dtype):
+    shapes, As, Bs, fa, fb = _array_case(3 + bn, 17, dtype)
+    plan = tst.gemm_grouped_array_plan_create(shapes, dtype=dtype, mapping=("grouped_m", 4), out_dtype="f32",
+                                              cta_group=cta_group, bn=bn, num_ctas=23)
+    for _ in range(2):   # the second run keeps the uploaded maps (same pointers are new tensors here)
+        dD = _array_run(plan, shapes, As, Bs, torch.float32)
+        assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+        for g, (m, n, k) in enumerate(shapes):
+            if m and n:
+                z, _ = oracle.gemm(As[g], Bs[g], fa, dtype_b=fb)
+                assert np.array_equal(host_values(dD[g]), z), g
+
+
+def test_grouped_array_fp8_output_epilogue_and_trace():
+    shapes, As, Bs, fa, fb = _array_case(11, 40, "bf16")
+    plan = tst.gemm_grouped_array_plan_create(shapes, mapping=("block_2d", 2), out_dtype="e4m3", activation="relu",
+                                              d_scale=True, amax=True, cta_group=1, bn=128, num_ctas=31)
+    info = plan.info
+    trace = torch.full((info.grid * info.max_items_per_cta * 8,), -1, dtype=torch.int32, device="cuda")
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TRACE, trace, trace.numel())
+    amax = torch.zeros(4, device="cuda")
+    dD = _array_run(plan, shapes, As, Bs, torch.uint8, d_scale=torch.tensor([0.125], device="cuda"), amax=amax)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    ys = []
+    for g, (m, n, k) in enumerate(shapes):
+        if m and n:
+            acc, ad = oracle.gemm(As[g], Bs[g], fa, dtype_b=fb)
+            _, Y, Dp, _ = E.apply(acc, ad, E.Epilogue(act=E.ACT_RELU, d_scale=0.125))
+            assert np.array_equal(E.decode_e4m3(dD[g].cpu().numpy()), E.decode_e4m3(E.encode_e4m3(Dp))), g
+            ys.append(E.amax(Y))
+    assert float(amax[0]) == max(ys)
+    t = trace.view(info.grid, info.max_items_per_cta, 8).cpu().numpy()
+    for u in range(info.grid):
+        got = [(int(r[2]), int(r[3]), int(r[4]), int(r[6])) for r in t[u] if r[0] != -1]
+        want = [(it.tile, it.m, it.n, it.k_tiles) for it in
+                GR.shaped_work_items(u, info.grid, shapes, 128, 128, info.bk, S.BLOCK_2D, 2)]
+        assert got == want, u

@@ -114,3 +114,37 @@ def test_pdl_option_validation():
     ok = tst.gemm_plan_create(1920, 1920, 4096, host_only=True, num_sms=148, cta_group=1, schedule="streamk",
                               sk_fixup="separate", pdl=True)
     assert ok.info.kernels_per_run == 2
+
+
+# ---------------------------------------------------------------- groups of different shapes
+
+def _shapes(seed, G):
+    r = synthetic.splitmix64(seed, 3 * G) % np.uint64(700)
+    return [(0 if g % 6 == 4 else int(r[3 * g]), int(r[3 * g + 1]) + 1, 64 * (int(r[3 * g + 2]) % 9 + 1))
+            for g in range(G)]
+
+
+@pytest.mark.parametrize("mapping", [("linear_nfast", 1), ("grouped_m", 8), ("block_2d", 2)])
+@pytest.mark.parametrize("cta_group,bn", [(1, 128), (2, 256)])
+@pytest.mark.parametrize("G", [1, 13, 70])
+def test_grouped_array_schedule_matches_oracle(mapping, cta_group, bn, G):
+    shapes = _shapes(G * 3 + bn, G)
+    plan = tst.gemm_grouped_array_plan_create(shapes, mapping=mapping, cta_group=cta_group, bn=bn, num_ctas=19,
+                                              host_only=True, num_sms=148)
+    info = plan.info
+    tiles = sum(GR.shape_tiles(shapes, info.bm, bn))
+    assert info.tiles == tiles and info.grid == min(19, tiles)
+    for u in range(info.grid):
+        got = [(t, m, n, kc) for t, m, n, kb, kc, fl in tst.gemm_work_items(plan, u)]
+        want = [(it.tile, it.m, it.n, it.k_tiles) for it in
+                GR.shaped_work_items(u, info.grid, shapes, info.bm, bn, info.bk, MAPS[mapping[0]], mapping[1])]
+        assert got == want, u
+
+
+@pytest.mark.parametrize("kw,code", [(dict(K=[64, 0]), tst.TST_ERR_INVALID_ARG), (dict(K=[64, 12]), tst.TST_ERR_ALIGNMENT),
+                                     (dict(M=[-1, 5]), tst.TST_ERR_INVALID_ARG)])
+def test_grouped_array_shape_errors(kw, code):
+    M, N, K = kw.get("M", [100, 5]), kw.get("N", [64, 64]), kw.get("K", [64, 64])
+    with pytest.raises(tst.TstError) as ei:
+        tst.gemm_grouped_array_plan_create(list(zip(M, N, K)), host_only=True, num_sms=148)
+    assert ei.value.status == code

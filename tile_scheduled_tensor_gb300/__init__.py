@@ -174,6 +174,44 @@ def gemm_grouped_run(plan: Plan, group_rows, A, B, D, bias=None, scales=None, c=
                                 _stream(stream)), "gemm_grouped_run")
 
 
+def gemm_grouped_array_plan_create(shapes, dtype="bf16", mapping=("grouped_m", 8), out_dtype="bf16",
+                                   alpha: float = 1.0, relu: bool = False, activation=None, use_scales: bool = False,
+                                   d_scale: bool = False, amax: bool = False, bn: int = 0, num_ctas: int = 0,
+                                   host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
+                                   stages: int = 0, bk: int = 0, pdl: bool = False) -> Plan:
+    """Plan a grouped GEMM over groups of different shapes: `shapes` is a list of
+    (M_g, N_g, K_g); each group has its own A, B and D (gemm_grouped_array_run)."""
+    G = len(shapes)
+    Ms = (ctypes.c_int64 * max(G, 1))(*[int(m) for m, _, _ in shapes])
+    Ns = (ctypes.c_int64 * max(G, 1))(*[int(n) for _, n, _ in shapes])
+    Ks = (ctypes.c_int64 * max(G, 1))(*[int(k) for _, _, k in shapes])
+    kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
+    m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
+    opts = _capi.tst_plan_options(int(bn), int(num_ctas), 0, int(bool(host_only)), int(num_sms), int(cta_group),
+                                  int(timeout_ns), int(stages), int(bk), 0, 0, int(bool(pdl)))
+    act = _enum(_ACT, activation, "activation") if activation is not None else \
+        (TST_ACT_RELU if relu else TST_ACT_NONE)
+    epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), 0.0, 0, 0, TST_BIAS_NONE, act,
+                                int(bool(use_scales)), 0, 0, int(bool(d_scale)), int(bool(amax)), 0, 0)
+    h = ctypes.c_void_p()
+    _check(lib.gemm_grouped_array_plan_create(ctypes.byref(h), G, Ms, Ns, Ks, _enum(_DTYPES, dtype, "dtype"),
+                                              TST_LAYOUT_A_ROW_B_NK, m, ctypes.byref(epi), ctypes.byref(opts)),
+           "gemm_grouped_array_plan_create")
+    info = _capi.tst_plan_info()
+    _check(lib.gemm_plan_get_info(h, ctypes.byref(info)), "gemm_plan_get_info")
+    return Plan(h.value, info)
+
+
+def gemm_grouped_array_run(plan: Plan, A, B, D, scales=None, d_scale=None, amax=None, stream=None):
+    """Enqueue a grouped GEMM of different shapes; A, B, D are lists of CUDA tensors (or None
+    for groups without rows or columns)."""
+    def arr(xs):
+        return (ctypes.c_void_p * max(len(xs), 1))(*[_ptr(x) for x in xs])
+    args = _capi.tst_epilogue_args(None, None, _ptr(scales), None, None, _ptr(d_scale), _ptr(amax), None)
+    _check(lib.gemm_grouped_array_run(plan._h, arr(A), arr(B), arr(D), ctypes.byref(args), _stream(stream)),
+           "gemm_grouped_array_run")
+
+
 def gemm_grouped_work_items(plan: Plan, group_rows, cta: int):
     """[(tile, m, n, k_begin, k_count, flags), ...] of one CTA of a grouped plan for the given
     host row counts, in device order."""

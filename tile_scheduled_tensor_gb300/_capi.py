@@ -93,6 +93,13 @@ _SIGNATURES = {
                                                 ctypes.c_int64, ctypes.c_int, ctypes.c_int, tst_mapping,
                                                 ctypes.POINTER(tst_epilogue_ex), ctypes.POINTER(tst_plan_options)]),
     "gemm_grouped_run": (ctypes.c_int, [_P, _P, _P, _P, _P, ctypes.POINTER(tst_epilogue_args), _P]),
+    "gemm_grouped_array_plan_create": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int32, ctypes.POINTER(ctypes.c_int64),
+                                                      ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                                      ctypes.c_int, ctypes.c_int, tst_mapping,
+                                                      ctypes.POINTER(tst_epilogue_ex),
+                                                      ctypes.POINTER(tst_plan_options)]),
+    "gemm_grouped_array_run": (ctypes.c_int, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                              ctypes.POINTER(tst_epilogue_args), _P]),
     "gemm_grouped_work_items": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                                ctypes.POINTER(tst_work_item), ctypes.c_int64,
                                                ctypes.POINTER(ctypes.c_int64)]),

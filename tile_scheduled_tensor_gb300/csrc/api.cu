@@ -35,6 +35,16 @@ struct tst_plan {
   tst_epilogue_ex epi{};       // the epilogue (the basic one is a special case)
   bool ext_on = false;         // epilogue needs more than alpha, column bias, ReLU, scales
   int32_t groups = 0;          // grouped GEMM: number of groups (0 = one GEMM)
+  // groups of different shapes: (M, N, K, 0) per group on the host and on the device, one
+  // A/B tensor-map pair and one output pointer per group on the device (filled per run)
+  std::vector<int32_t> shapes_host;
+  int64_t shaped_tiles = 0;    // the groups' tiles, sum of their own grids
+  void* dev_groups = nullptr;
+  int32_t* d_shapes = nullptr;
+  CUtensorMap* d_tmaps = nullptr;
+  void** d_outs = nullptr;
+  std::vector<CUtensorMap> tmaps_host;
+  std::vector<const void*> last_ptrs;   // A, B, D of every group at the last upload
   int64_t b_rows = 0;          // rows of B: N, or groups * N
   uint32_t fmt_ab = 0;         // FP8 operand formats for the instruction descriptor
   tst_plan_options opts{};
@@ -227,7 +237,7 @@ uint32_t fp8_formats(tst_dtype d) {
 
 tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtype dtype, tst_layout layout,
                        tst_mapping mapping, tst_schedule schedule, const tst_epilogue_ex* epi,
-                       const tst_plan_options* opts, int32_t groups = 0) {
+                       const tst_plan_options* opts, int32_t groups = 0, const int32_t* shapes = nullptr) {
   if (out == nullptr) return TST_ERR_INVALID_ARG;
   *out = nullptr;
   if (epi == nullptr || M <= 0 || N <= 0 || K <= 0) return TST_ERR_INVALID_ARG;
@@ -300,8 +310,14 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   const int64_t mt = ceil_div(M, p->bm);
   const int64_t nt = ceil_div(N, p->bn);
   const int64_t kt = ceil_div(K, p->bk);
-  // grouped: at most ceil(M / bm) + groups tile rows over all groups, whatever the split
-  const int64_t T = (groups > 0 ? mt + groups : mt) * nt;
+  // grouped: at most ceil(M / bm) + groups tile rows over all groups, whatever the split;
+  // groups of different shapes: exactly the sum of their own grids
+  int64_t T = (groups > 0 ? mt + groups : mt) * nt;
+  if (shapes) {
+    T = 0;
+    for (int32_t g = 0; g < groups; ++g)
+      T += ceil_div(shapes[4 * g], p->bm) * ceil_div(shapes[4 * g + 1], p->bn);
+  }
   if (T >= (int64_t(1) << 30) || T * kt >= (int64_t(1) << 62)) { delete p; return TST_ERR_INVALID_ARG; }
   p->stages = tst_kernel_stages(p->bn, p->cg, p->ka);
   if (o.stages != 0) {
@@ -362,6 +378,14 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   s.groups = groups;
   s.group_rows = nullptr;   // the run supplies the device array of group sizes
   s.group_b_rows = static_cast<int32_t>(N);
+  s.cols = static_cast<int32_t>(N);
+  s.bk = p->bk;
+  if (shapes) {
+    // the host copy serves host enumeration; launches swap in the device copy
+    p->shapes_host.assign(shapes, shapes + 4 * static_cast<size_t>(groups));
+    p->shaped_tiles = T;
+    s.group_shapes = p->shapes_host.data();
+  }
   if (mapping.kind == TST_MAP_MORTON) {
     // Z order: tiles by the code interleaving the bits of n (even) and m (odd positions)
     std::vector<std::pair<uint64_t, int64_t>> codes;
@@ -445,8 +469,9 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     p->sk_slots = most;
   }
   // longest work list (trace sizing); a grouped plan knows only the bound on its tiles
-  int32_t max_items = groups > 0 ? static_cast<int32_t>(ceil_div(T, s.grid)) : 0;
-  for (int32_t c = 0; c < s.grid && groups == 0; ++c) {
+  const bool enumerable = groups == 0 || shapes != nullptr;
+  int32_t max_items = enumerable ? 0 : static_cast<int32_t>(ceil_div(T, s.grid));
+  for (int32_t c = 0; c < s.grid && enumerable; ++c) {
     tst::WorkIter it;
     tst::WorkItem w;
     tst::work_begin(s, c, it);
@@ -506,6 +531,30 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
         return TST_ERR_OOM;
       }
     }
+    if (shapes) {
+      // [shapes | 2 tensor maps per group | one output pointer per group]
+      const size_t shape_bytes = ((16 * static_cast<size_t>(groups) + 127) / 128) * 128;
+      const size_t map_bytes = 2 * sizeof(CUtensorMap) * static_cast<size_t>(groups);
+      if (cudaMalloc(&p->dev_groups, shape_bytes + map_bytes + sizeof(void*) * groups) != cudaSuccess) {
+        cudaGetLastError();
+        if (p->d_order) cudaFree(p->d_order);
+        cudaFree(p->dev_block);
+        delete p;
+        return TST_ERR_OOM;
+      }
+      char* g = static_cast<char*>(p->dev_groups);
+      p->d_shapes = reinterpret_cast<int32_t*>(g);
+      p->d_tmaps = reinterpret_cast<CUtensorMap*>(g + shape_bytes);
+      p->d_outs = reinterpret_cast<void**>(g + shape_bytes + map_bytes);
+      p->tmaps_host.assign(2 * static_cast<size_t>(groups), CUtensorMap{});
+      if (cudaMemcpy(p->d_shapes, shapes, 16 * static_cast<size_t>(groups), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaFree(p->dev_groups);
+        if (p->d_order) cudaFree(p->d_order);
+        cudaFree(p->dev_block);
+        delete p;
+        return TST_ERR_CUDA;
+      }
+    }
     if (p->sk_mode == TST_SK_SEPARATE && s.sk_tiles > 0) {
       p->reduce_kernel = tst_reduce_kernel(kernel_out(*p));
       if (!p->reduce_kernel) {
@@ -561,6 +610,7 @@ tst_status gemm_plan_destroy(tst_plan* plan) {
   tst_status st = TST_OK;
   if (plan->dev_block && cudaFree(plan->dev_block) != cudaSuccess) st = TST_ERR_CUDA;
   if (plan->d_order && cudaFree(plan->d_order) != cudaSuccess) st = TST_ERR_CUDA;
+  if (plan->dev_groups && cudaFree(plan->dev_groups) != cudaSuccess) st = TST_ERR_CUDA;
   delete plan;
   return st;
 }
@@ -571,7 +621,7 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->M = p->M; info->N = p->N; info->K = p->K;
   info->bm = p->bm; info->bn = p->bn; info->bk = p->bk; info->stages = p->stages;
   info->mt = p->sched.mt; info->nt = p->sched.nt; info->kt = p->sched.kt;
-  info->tiles = static_cast<int64_t>(p->sched.mt) * p->sched.nt;
+  info->tiles = p->shapes_host.empty() ? static_cast<int64_t>(p->sched.mt) * p->sched.nt : p->shaped_tiles;
   info->grid = p->sched.grid;
   info->num_sms = p->num_sms;
   info->sk_tiles = p->sched.sk_tiles;
@@ -595,7 +645,7 @@ tst_status gemm_tile_map(const tst_plan* p, int64_t i, int32_t* m, int32_t* n) {
 
 tst_status gemm_work_items(const tst_plan* p, int32_t cta, tst_work_item* items, int64_t cap, int64_t* count) {
   if (p == nullptr || count == nullptr || (cap > 0 && items == nullptr) || cap < 0) return TST_ERR_INVALID_ARG;
-  if (cta < 0 || cta >= p->sched.grid || p->groups > 0) return TST_ERR_INVALID_ARG;
+  if (cta < 0 || cta >= p->sched.grid || (p->groups > 0 && p->shapes_host.empty())) return TST_ERR_INVALID_ARG;
   tst::WorkIter it;
   tst::WorkItem w;
   tst::work_begin(p->sched, cta, it);
@@ -646,8 +696,11 @@ namespace {
 
 tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
                   const int32_t* group_rows, void* stream_) {
-  if (p == nullptr || A == nullptr || B == nullptr || C == nullptr || ea == nullptr) return TST_ERR_INVALID_ARG;
-  if ((p->groups > 0) != (group_rows != nullptr)) return TST_ERR_INVALID_ARG;
+  if (p == nullptr || ea == nullptr) return TST_ERR_INVALID_ARG;
+  // groups of different shapes bring their own operands (uploaded by gemm_grouped_array_run)
+  const bool array_mode = !p->shapes_host.empty();
+  if (!array_mode && (A == nullptr || B == nullptr || C == nullptr)) return TST_ERR_INVALID_ARG;
+  if (!array_mode && (p->groups > 0) != (group_rows != nullptr)) return TST_ERR_INVALID_ARG;
   if (group_rows != nullptr && (reinterpret_cast<uintptr_t>(group_rows) & 3u)) return TST_ERR_ALIGNMENT;
   if (p->host_only || p->kernel == nullptr) return TST_ERR_NO_DEVICE;
   const tst_epilogue_ex& e = p->epi;
@@ -657,7 +710,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
       (e.col_scale && ea->col_scale == nullptr) || (e.d_scale && ea->d_scale == nullptr) ||
       (e.amax && ea->amax == nullptr) || (e.aux && ea->aux == nullptr))
     return TST_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return TST_ERR_ALIGNMENT;
+  if (!array_mode && (!aligned16(A) || !aligned16(B) || !aligned16(C))) return TST_ERR_ALIGNMENT;
   if ((has_bias && (reinterpret_cast<uintptr_t>(ea->bias) & 3u)) ||
       (e.use_scales && (reinterpret_cast<uintptr_t>(ea->scales) & 3u)))
     return TST_ERR_ALIGNMENT;
@@ -674,11 +727,11 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   // and by bn / cta_group rows of B (a CTA pair splits the B rows of its
   // 256 x bn tile between its two CTAs)
   const int box_k = p->bk / p->ka;
-  if (A != p->tm_A) {
+  if (!array_mode && A != p->tm_A) {
     if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, box_k, tst::kBlockM)) return TST_ERR_CUDA;
     p->tm_A = A;
   }
-  if (B != p->tm_B) {
+  if (!array_mode && B != p->tm_B) {
     if (!encode_operand(&p->tmap_b, B, p->dtype, p->b_rows, p->K, box_k, p->bn / p->cg)) return TST_ERR_CUDA;
     // HyTiS half-width tiles read half of the B rows per stage
     if (p->sched.narrow_tiles > 0 &&
@@ -707,6 +760,11 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.sched = p->sched;
   kp.sched.order = p->d_order;
   kp.sched.group_rows = group_rows;
+  if (array_mode) {
+    kp.sched.group_shapes = p->d_shapes;
+    kp.group_tmaps = p->d_tmaps;
+    kp.group_d = p->d_outs;
+  }
   kp.has_bias = has_bias ? 1 : 0;
   kp.relu = e.activation == TST_ACT_RELU ? 1 : 0;
   kp.use_scales = e.use_scales ? 1 : 0;
@@ -832,6 +890,79 @@ tst_status gemm_grouped_run(tst_plan* p, const int32_t* group_rows, const void* 
                             const tst_epilogue_args* args, void* stream) {
   if (p == nullptr || group_rows == nullptr || p->groups == 0) return TST_ERR_INVALID_ARG;
   return launch(p, A, B, D, args, group_rows, stream);
+}
+
+tst_status gemm_grouped_array_plan_create(tst_plan** plan, int32_t groups, const int64_t* M, const int64_t* N,
+                                          const int64_t* K, tst_dtype dtype, tst_layout layout, tst_mapping mapping,
+                                          const tst_epilogue_ex* epi, const tst_plan_options* opts) {
+  if (plan != nullptr) *plan = nullptr;
+  if (plan == nullptr || groups < 1 || M == nullptr || N == nullptr || K == nullptr || epi == nullptr)
+    return TST_ERR_INVALID_ARG;
+  if (dtype < TST_BF16 || dtype > TST_E5M2_E4M3) return TST_ERR_INVALID_ARG;
+  // only epilogue operations without per-element operands: each group has its own output
+  if (epi->bias_mode != TST_BIAS_NONE || epi->has_c || epi->row_scale || epi->col_scale || epi->aux)
+    return TST_ERR_UNSUPPORTED;
+  const int elt = dtype == TST_BF16 ? 2 : 1;
+  std::vector<int32_t> shapes(4 * static_cast<size_t>(groups), 0);
+  int64_t rows = 0, cols = 1, depth = 1;
+  for (int32_t g = 0; g < groups; ++g) {
+    if (M[g] < 0 || N[g] < 0 || K[g] <= 0) return TST_ERR_INVALID_ARG;
+    if (M[g] >= (int64_t(1) << 31) || N[g] >= (int64_t(1) << 31) || K[g] >= (int64_t(1) << 31))
+      return TST_ERR_INVALID_ARG;
+    if ((K[g] * elt) % 16 != 0) return TST_ERR_ALIGNMENT;   // every group's rows feed a TMA map
+    shapes[4 * g] = static_cast<int32_t>(M[g]);
+    shapes[4 * g + 1] = static_cast<int32_t>(N[g]);
+    shapes[4 * g + 2] = static_cast<int32_t>(K[g]);
+    rows += M[g];
+    cols = std::max(cols, N[g]);
+    depth = std::max(depth, K[g]);
+  }
+  // the tile choice and the plan's bounds see the whole batch: all rows, the widest and deepest group
+  return create_plan(plan, std::max<int64_t>(rows, 1), cols, depth, dtype, layout, mapping, TST_PERSISTENT, epi,
+                     opts, groups, shapes.data());
+}
+
+tst_status gemm_grouped_array_run(tst_plan* p, const void* const* A, const void* const* B, void* const* D,
+                                  const tst_epilogue_args* args, void* stream) {
+  if (p == nullptr || p->shapes_host.empty() || A == nullptr || B == nullptr || D == nullptr || args == nullptr)
+    return TST_ERR_INVALID_ARG;
+  if (p->host_only || p->kernel == nullptr) return TST_ERR_NO_DEVICE;
+  const int32_t G = p->groups;
+  bool changed = p->last_ptrs.size() != 3 * static_cast<size_t>(G);
+  for (int32_t g = 0; g < G; ++g) {
+    if (p->shapes_host[4 * g] == 0 || p->shapes_host[4 * g + 1] == 0) continue;   // no tiles, never read
+    if (A[g] == nullptr || B[g] == nullptr || D[g] == nullptr) return TST_ERR_INVALID_ARG;
+    if (!aligned16(A[g]) || !aligned16(B[g]) || !aligned16(D[g])) return TST_ERR_ALIGNMENT;
+    if (!changed && (p->last_ptrs[3 * g] != A[g] || p->last_ptrs[3 * g + 1] != B[g] || p->last_ptrs[3 * g + 2] != D[g]))
+      changed = true;
+  }
+  if (changed) {
+    // one A and one B tensor map per group, and the output pointers, to the device (the
+    // copy is ordered after earlier launches of the plan on this stream)
+    const int box_k = p->bk / p->ka;
+    std::vector<void*> outs(static_cast<size_t>(G), nullptr);
+    p->last_ptrs.assign(3 * static_cast<size_t>(G), nullptr);
+    for (int32_t g = 0; g < G; ++g) {
+      const int64_t Mg = p->shapes_host[4 * g], Ng = p->shapes_host[4 * g + 1], Kg = p->shapes_host[4 * g + 2];
+      if (Mg == 0 || Ng == 0) continue;
+      if (!encode_operand(&p->tmaps_host[2 * g], A[g], p->dtype, Mg, Kg, box_k, tst::kBlockM) ||
+          !encode_operand(&p->tmaps_host[2 * g + 1], B[g], p->dtype, Ng, Kg, box_k, p->bn / p->cg))
+        return TST_ERR_CUDA;
+      outs[g] = D[g];
+      p->last_ptrs[3 * g] = A[g];
+      p->last_ptrs[3 * g + 1] = B[g];
+      p->last_ptrs[3 * g + 2] = D[g];
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(p->d_tmaps, p->tmaps_host.data(), sizeof(CUtensorMap) * 2 * G, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(p->d_outs, outs.data(), sizeof(void*) * G, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+      cudaGetLastError();
+      p->last_ptrs.clear();
+      return TST_ERR_CUDA;
+    }
+  }
+  return launch(p, nullptr, nullptr, nullptr, args, nullptr, stream);
 }
 
 tst_status gemm_grouped_work_items(const tst_plan* p, const int32_t* group_rows, int32_t cta,

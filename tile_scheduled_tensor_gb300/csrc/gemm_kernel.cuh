@@ -201,7 +201,14 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     const bool narrow = (w.flags & ITEM_NARROW) != 0;   // half-width tile: half of B per stage
     const int32_t m0 = w.row0 + static_cast<int32_t>(c.rank) * kBlockM;    // row of A
     const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (narrow ? BN_CTA / 2 : BN_CTA);   // row of B
-    const CUtensorMap* tmap_b = narrow ? &p.tmap_b_half : &p.tmap_b;
+    // groups of different shapes: the item's group has its own tensor maps (A at 2g, B at 2g + 1)
+    const bool own_maps = p.sched.group_shapes != nullptr;
+    const CUtensorMap* tmap_a = own_maps ? p.group_tmaps + 2 * w.group : &p.tmap_a;
+    const CUtensorMap* tmap_b = own_maps ? p.group_tmaps + 2 * w.group + 1 : (narrow ? &p.tmap_b_half : &p.tmap_b);
+    if (own_maps) {
+      ptx::fence_tensormap_acquire(tmap_a);
+      ptx::fence_tensormap_acquire(tmap_b);
+    }
     const uint32_t stage_bytes = narrow ? Cfg::A_BYTES + Cfg::B_BYTES / 2 : Cfg::STAGE_BYTES;
     for (int32_t kb = w.k_begin; kb < w.k_begin + w.k_count; ++kb) {
       const long long t0 = p.stats ? clock64() : 0;
@@ -216,10 +223,10 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
           const uint32_t sb = smem_b + stage * Cfg::B_BYTES + a * Cfg::B_SUB;
           const int32_t kx = kb * BK + a * BK_ATOM;
           if (CG == 2) {
-            ptx::tma_load_2d_pair(sa, &p.tmap_a, full_target + 8 * stage, kx, m0);
+            ptx::tma_load_2d_pair(sa, tmap_a, full_target + 8 * stage, kx, m0);
             ptx::tma_load_2d_pair(sb, tmap_b, full_target + 8 * stage, kx, n0);
           } else {
-            ptx::tma_load_2d(sa, &p.tmap_a, bar_full + 8 * stage, kx, m0);
+            ptx::tma_load_2d(sa, tmap_a, bar_full + 8 * stage, kx, m0);
             ptx::tma_load_2d(sb, tmap_b, bar_full + 8 * stage, kx, n0);
           }
         }
@@ -338,13 +345,13 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
 
 // ------------------------------------------------------------------ epilogue
 template <int OUT>
-__device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, int32_t row_end, int32_t col0,
+__device__ __forceinline__ void store_chunk(void* out, int32_t ncols, int32_t row, int32_t row_end, int32_t col0,
                                             const float (&z)[32]) {
   if (row >= row_end) return;
-  const int64_t base = static_cast<int64_t>(row) * p.N + col0;
+  const int64_t base = static_cast<int64_t>(row) * ncols + col0;
   if (OUT == OUT_BF16) {
-    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.C) + base;
-    if (col0 + 32 <= p.N && (p.N & 7) == 0) {
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(out) + base;
+    if (col0 + 32 <= ncols && (ncols & 7) == 0) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint4 pk;
@@ -359,18 +366,18 @@ __device__ __forceinline__ void store_chunk(const KernelParams& p, int32_t row, 
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (col0 + j < p.N) dst[j] = __float2bfloat16_rn(z[j]);
+        if (col0 + j < ncols) dst[j] = __float2bfloat16_rn(z[j]);
     }
   } else {
-    float* dst = reinterpret_cast<float*>(p.C) + base;
-    if (col0 + 32 <= p.N && (p.N & 3) == 0) {
+    float* dst = reinterpret_cast<float*>(out) + base;
+    if (col0 + 32 <= ncols && (ncols & 3) == 0) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (col0 + j < p.N) dst[j] = z[j];
+        if (col0 + j < ncols) dst[j] = z[j];
     }
   }
 }
@@ -453,6 +460,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     const uint32_t t_row =
         tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
+    // the output of this item: a group of its own shape writes its own matrix
+    void* const out = p.sched.group_shapes ? p.group_d[w.group] : p.C;
     float s_row = alpha, b_row = 0.0f;  // extended epilogue: this row's accumulator scale and bias
     if (EXT) epi::row_terms(p.ext, p.bias, alpha, w.row_end, row, s_row, b_row);
     // 64-column TMEM loads of this item (a half-width tile has half of them), dealt to the
@@ -524,14 +533,14 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
         }
         const int32_t col0 = w.col0 + c32 * 32;
         if constexpr (EXT) {
-          amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, w.row_end, p.N, row, col0, v + 32 * h,
-                                             p.C, amax);
+          amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, w.row_end, w.col_end, row, col0,
+                                             v + 32 * h, out, amax);
           continue;
         }
         float z[32];
         if (p.has_bias) {
           float b[32];
-          if (bias_vec && col0 + 32 <= p.N) {
+          if (bias_vec && col0 + 32 <= w.col_end) {
             // 8 vector loads in flight; every lane reads the same 128 bytes (one broadcast)
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -540,7 +549,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) b[j] = (col0 + j < p.N) ? __ldg(p.bias + col0 + j) : 0.0f;
+            for (int j = 0; j < 32; ++j) b[j] = (col0 + j < w.col_end) ? __ldg(p.bias + col0 + j) : 0.0f;
           }
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = fmaf(alpha, v[32 * h + j], b[j]);
@@ -552,7 +561,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = fmaxf(z[j], 0.0f);
         }
-        store_chunk<OUT>(p, row, w.row_end, col0, z);
+        store_chunk<OUT>(out, w.col_end, row, w.row_end, col0, z);
       }
     }
     ptx::tc_fence_before();

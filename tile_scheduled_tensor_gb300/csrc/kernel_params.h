@@ -69,6 +69,8 @@ struct KernelParams {
   CUtensorMap tmap_b;       // B: N x K, K contiguous, box BK x BN, 128-byte swizzle
   CUtensorMap tmap_b_half;  // the same B with half-height boxes (HyTiS half-width tiles)
   CUtensorMap tmap_ws;      // SK_TMA: the partial tiles as a 128 x (slots * BN) FP32 tensor, box 128 x 32
+  const CUtensorMap* group_tmaps;  // groups of different shapes: A_g and B_g maps at 2g, 2g + 1 (device)
+  void* const* group_d;            // ... and their outputs (device array of pointers)
   void* C;                  // M x N row-major, FP32 or BF16
   const float* bias;        // FP32[N] or null
   const float* scales;      // FP32[2] = {sA, sB} or null

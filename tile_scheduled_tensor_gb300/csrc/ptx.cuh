@@ -67,6 +67,12 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32
                : "memory");
 }
 
+// order a tensor map written to global memory through the generic proxy (a copy before
+// the launch) before this thread's TMA reads of it, so no stale descriptor is used
+__device__ __forceinline__ void fence_tensormap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -73,6 +73,11 @@ struct Sched {
   int32_t groups;
   const int32_t* group_rows;  // host or device copy, read as the schedule advances
   int32_t group_b_rows;
+  // groups of different shapes (group_shapes != null): group g is its own GEMM of
+  // group_shapes[4g .. 4g+2] = (M_g, N_g, K_g) with its own A, B and output
+  const int32_t* group_shapes;
+  int32_t cols;           // columns of the output (N) of a single or shared-N grouped GEMM
+  int32_t bk;             // k-tile in elements (k-tiles of a group of its own shape)
 };
 
 struct WorkItem {
@@ -86,6 +91,7 @@ struct WorkItem {
   int32_t row_end;  // rows at or past this are not results of this item
   int32_t b_row0;   // first row of the tile's block of B
   int32_t col0;     // first output column of the tile
+  int32_t col_end;  // columns at or past this are not results (and the output's row length)
 };
 
 // F(i) -> (m, n).  Grouped strips: a strip holds G tile-rows (grouped-M) or
@@ -181,18 +187,22 @@ TST_HD void work_begin(const Sched& s, int32_t cta, WorkIter& it) {
 // rows of group g as the schedule uses them: negative counts are 0, and no group
 // is taken to be longer than the whole output
 TST_HD int64_t group_row_count(const Sched& s, int32_t g) {
+  if (s.group_shapes) return s.group_shapes[4 * g];
   const int64_t r = s.group_rows[g];
   return r < 0 ? 0 : (r > s.rows ? s.rows : r);
 }
 
-TST_HD int32_t group_tile_count(const Sched& s, int64_t rows) {
-  return static_cast<int32_t>((rows + s.bm - 1) / s.bm) * s.nt;
+// tiles of group g with `rows` rows: its own column count for groups of different shapes
+TST_HD int32_t group_tile_count(const Sched& s, int32_t g, int64_t rows) {
+  const int32_t nt = s.group_shapes ? (s.group_shapes[4 * g + 1] + s.bn - 1) / s.bn : s.nt;
+  return static_cast<int32_t>((rows + s.bm - 1) / s.bm) * nt;
 }
 
 // the item for linear index i of the current group of `it`
 TST_HD void grouped_item(const Sched& s, const WorkIter& it, int64_t i, WorkItem& w) {
   Sched sg = s;
   sg.mt = static_cast<int32_t>((it.g_rows + s.bm - 1) / s.bm);
+  if (s.group_shapes) sg.nt = (s.group_shapes[4 * it.g + 1] + s.bn - 1) / s.bn;
   w.tile = static_cast<int32_t>(i);
   tile_coord(sg, static_cast<int32_t>(i - it.g_start), w.m, w.n);   // local offset k = i - start
   w.k_begin = 0;
@@ -200,6 +210,16 @@ TST_HD void grouped_item(const Sched& s, const WorkIter& it, int64_t i, WorkItem
   w.flags = ITEM_FINAL;
   w.group = it.g;
   w.col0 = w.n * s.bn;
+  if (s.group_shapes) {
+    // a GEMM of its own: its own A, B and output, rows and columns from 0
+    w.k_count = (s.group_shapes[4 * it.g + 2] + s.bk - 1) / s.bk;
+    w.row0 = w.m * s.bm;
+    w.row_end = static_cast<int32_t>(it.g_rows);
+    w.col_end = s.group_shapes[4 * it.g + 1];
+    w.b_row0 = w.col0;
+    return;
+  }
+  w.col_end = s.cols;
   const int64_t row0 = it.g_row + static_cast<int64_t>(w.m) * s.bm;
   const int64_t end = it.g_row + it.g_rows;
   if (end > s.rows) w.flags |= ITEM_CLAMPED;
@@ -219,7 +239,7 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
       it.g_row += it.g_rows;
       if (++it.g >= s.groups) return false;
       it.g_rows = group_row_count(s, it.g);
-      it.g_tiles = group_tile_count(s, it.g_rows);
+      it.g_tiles = group_tile_count(s, it.g, it.g_rows);
     }
     it.next_dp += s.grid;
     grouped_item(s, it, i, w);
@@ -269,6 +289,7 @@ TST_HD bool work_next(const Sched& s, WorkIter& it, WorkItem& w) {
   w.group = 0;
   w.row0 = w.m * s.bm;
   w.row_end = s.rows;
+  w.col_end = s.cols;
   w.col0 = w.n * s.bn + half_col;
   w.b_row0 = w.col0;
   return true;
@@ -293,7 +314,7 @@ __device__ __forceinline__ bool work_next_warp(const Sched& s, WorkIter& it, Wor
     while (base < s.groups) {
       const int32_t gl = base + lane;
       const int64_t r = gl < s.groups ? group_row_count(s, gl) : 0;
-      const int64_t t = group_tile_count(s, r);
+      const int64_t t = gl < s.groups ? group_tile_count(s, gl, r) : 0;
       int64_t incl_t = t, incl_r = r;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
