@@ -232,7 +232,8 @@ def _array_case(seed, G, dtype):
 def _array_run(plan, shapes, As, Bs, out, **args):
     dA = [device_codes(a) if m and n else None for (m, n, _), a in zip(shapes, As)]
     dB = [device_codes(b) if m and n else None for (m, n, _), b in zip(shapes, Bs)]
-    dD = [torch.full((m, n), float("nan"), dtype=out, device="cuda") if m and n else None for m, n, _ in shapes]
+    fill = 0x7F if out == torch.uint8 else float("nan")     # the e4m3 NaN code for byte outputs
+    dD = [torch.full((m, n), fill, dtype=out, device="cuda") if m and n else None for m, n, _ in shapes]
     tst.gemm_grouped_array_run(plan, dA, dB, dD, **args)
     return dD
 
