@@ -29,13 +29,14 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import make_addend, make_gemm_inputs, make_group_rows, operand_types  # noqa: E402
+from synthetic import make_addend, make_gemm_inputs, make_group_rows, make_group_shapes, operand_types  # noqa: E402
 from synthetic.workloads import WORKLOADS  # noqa: E402
 
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
 HEADLINE = "c2_bf16_4096"
 EXTRA = ["c1_bf16_256", "c2_bf16_4096_1cta", "c2x_bf16_8192", "c3_e4m3_8192", "c4_bf16_streamk", "c4_bf16_persistent",
-         "c4_bf16_hybrid", "c4_bf16_hytis", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "g1_bf16_grouped"]
+         "c4_bf16_hybrid", "c4_bf16_hytis", "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "g1_bf16_grouped",
+         "g2_bf16_grouped_shapes"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
     "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
@@ -53,6 +54,9 @@ DESCR = {
                             "C a BF16 N(0,1) addend, grouped-M G=8",
     "c3m_e4m3_e5m2_8192": "FP8 GEMM 8192^3, A e4m3 x B e5m2, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, "
                           "persistent",
+    "g2_bf16_grouped_shapes": "grouped BF16 GEMM over 12 problems of different shapes (seeded M_g in [256, 4096], "
+                              "N_g, K_g in {1024..8192}; 0.68 TFLOP), each with its own A, B, D; BF16 out, "
+                              "grouped-M G=8 inside each group, one persistent launch",
     "g1_bf16_grouped": "grouped BF16 GEMM: 16 groups, N=K=4096, group rows summing to 16384 (uneven, seeded), "
                        "BF16 out, one persistent launch",
 }
@@ -67,7 +71,31 @@ def extra_plan_options(w):
     return {k: w[k] for k in PLAN_OPTION_KEYS if k in w}
 
 
+def group_shapes(w):
+    """(M_g, N_g, K_g) of a workload over groups of different shapes, else None."""
+    return make_group_shapes(w["shape_groups"], w["case"]) if "shape_groups" in w else None
+
+
+def total_rows(w):
+    shapes = group_shapes(w)
+    return sum(m for m, _, _ in shapes) if shapes else w["M"]
+
+
+def row_flops(w, rows):
+    """2 * N * K per output row (rows of a shaped workload count in their group's N_g * K_g;
+    its rows are numbered group after group)."""
+    shapes = group_shapes(w)
+    if not shapes:
+        return 2.0 * len(rows) * w["N"] * w["K"]
+    edges = np.cumsum([0] + [m for m, _, _ in shapes])
+    gid = np.searchsorted(edges, np.asarray(rows), side="right") - 1
+    return float(sum(2.0 * shapes[g][1] * shapes[g][2] for g in gid))
+
+
 def flops(w):
+    shapes = group_shapes(w)
+    if shapes:
+        return float(sum(2.0 * m * n * k for m, n, k in shapes))
     return 2.0 * w["M"] * w["N"] * w["K"]
 
 
@@ -81,6 +109,18 @@ def oracle_step(w, inp, rows, addend=None):
     workload multiplies each row by its own group's block of B."""
     import oracle
     from oracle import epilogue as E
+    shapes = group_shapes(w)
+    if shapes:
+        # rows numbered group after group; group g's rows multiply its own A_g, B_g
+        fa, fb = operand_types(w["dtype"])
+        edges = np.cumsum([0] + [m for m, _, _ in shapes])
+        rows = np.asarray(rows, dtype=np.int64)
+        gid = np.searchsorted(edges, rows, side="right") - 1
+        out = []
+        for g in np.unique(gid):
+            local = rows[gid == g] - edges[g]
+            out.append(oracle.gemm(inp[g].A, inp[g].B, fa, alpha=w.get("alpha", 1.0), rows=local, dtype_b=fb))
+        return out
     fa, fb = operand_types(inp.dtype)
     if "groups" in w:
         edges = np.cumsum([0] + make_group_rows(w["groups"], w["M"], w["case"]))
@@ -109,7 +149,12 @@ def oracle_step(w, inp, rows, addend=None):
 
 
 def make_inputs_for(w):
-    """Seeded inputs of workload w (a grouped workload's B holds one N x K block per group)."""
+    """Seeded inputs of workload w (a grouped workload's B holds one N x K block per group;
+    a workload over groups of different shapes has one input set per group, case 100 c + g)."""
+    shapes = group_shapes(w)
+    if shapes:
+        return [make_gemm_inputs(m, n, k, w["dtype"], w["dist"], case=100 * w["case"] + g)
+                for g, (m, n, k) in enumerate(shapes)]
     n_b = w["N"] * w.get("groups", 1)
     return make_gemm_inputs(w["M"], n_b, w["K"], w["dtype"], w["dist"], case=w["case"], bias_dist=w.get("bias_dist"))
 
@@ -117,6 +162,22 @@ def make_inputs_for(w):
 def setup_workload(w, tst, torch):
     """Plan, pinned host inputs, device copies and the output tensor of workload w."""
     inp = make_inputs_for(w)
+    cdt = {"bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.uint8}[w["out"]]
+    shapes = group_shapes(w)
+    if shapes:
+        plan = tst.gemm_grouped_array_plan_create(shapes, dtype=w["dtype"], mapping=w["mapping"], out_dtype=w["out"],
+                                                  alpha=w.get("alpha", 1.0), bn=w.get("bn", 0),
+                                                  cta_group=w.get("cta_group", 0))
+        host = {}
+        for g, x in enumerate(inp):
+            host[f"A{g}"] = torch.from_numpy(x.A.view(np.int16) if x.A.dtype == np.uint16 else x.A).pin_memory()
+            host[f"B{g}"] = torch.from_numpy(x.B.view(np.int16) if x.B.dtype == np.uint16 else x.B).pin_memory()
+        dev = {k: v.cuda() for k, v in host.items()}
+        # one output buffer; group g's D is the (M_g, N_g) view at its offset
+        C = torch.empty(sum(m * n for m, n, _ in shapes), dtype=cdt, device="cuda")
+        offs = np.cumsum([0] + [m * n for m, n, _ in shapes])
+        dev["shaped"] = (len(shapes), [C[offs[g]:offs[g + 1]].view(m, n) for g, (m, n, _) in enumerate(shapes)])
+        return inp, plan, host, dev, C
     if "groups" in w:
         plan = tst.gemm_grouped_plan_create(w["groups"], w["M"], w["N"], w["K"], dtype=w["dtype"],
                                             mapping=w["mapping"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
@@ -168,7 +229,11 @@ def run_args(dev):
 
 def run_once(tst, plan, dev, C, stream=None):
     """One launch of the workload through the public API."""
-    if "group_rows" in dev:
+    if "shaped" in dev:
+        G, views = dev["shaped"]
+        tst.gemm_grouped_array_run(plan, [dev[f"A{g}"] for g in range(G)], [dev[f"B{g}"] for g in range(G)], views,
+                                   stream=stream)
+    elif "group_rows" in dev:
         tst.gemm_grouped_run(plan, dev["group_rows"], dev["A"], dev["B"], C, stream=stream, **run_args(dev))
     else:
         tst.gemm_run(plan, dev["A"], dev["B"], C, stream=stream, **run_args(dev))
@@ -337,19 +402,20 @@ def setup_dist():
 
 def cpu_oracle_rate(w, inp, budget_s=10.0, max_rows=None, addend=None):
     """Time the oracle (as it stands) on whole output rows until ~budget_s of CPU work."""
-    rows_done, t_total, r0 = 0, 0.0, 0
+    rows_done, t_total, r0, fl = 0, 0.0, 0, 0.0
     step = 4
-    while t_total < budget_s and r0 < w["M"] and (max_rows is None or rows_done < max_rows):
-        rows = np.arange(r0, min(r0 + step, w["M"]), dtype=np.int64)
+    M = total_rows(w)
+    while t_total < budget_s and r0 < M and (max_rows is None or rows_done < max_rows):
+        rows = np.arange(r0, min(r0 + step, M), dtype=np.int64)
         t0 = time.perf_counter()
         oracle_step(w, inp, rows, addend)
         dt = time.perf_counter() - t0
         t_total += dt
         rows_done += rows.size
+        fl += row_flops(w, rows)
         r0 += rows.size
         if dt < budget_s / 8:
             step *= 2
-    fl = 2.0 * rows_done * w["N"] * w["K"]
     return fl / t_total / 1e12, rows_done, t_total
 
 
@@ -363,18 +429,18 @@ def run_reference(args):
     inp = make_inputs_for(w)
     _, addend = addend_for(w)
     rows_per_step = 8
-    per_step_flops = 2.0 * rows_per_step * w["N"] * w["K"]
+    M = total_rows(w)
     for s in range(args.warmup):
-        oracle_step(w, inp, (np.arange(s * rows_per_step, (s + 1) * rows_per_step) % w["M"]).astype(np.int64),
-                    addend)
-    times = []
+        oracle_step(w, inp, (np.arange(s * rows_per_step, (s + 1) * rows_per_step) % M).astype(np.int64), addend)
+    times, fl = [], 0.0
     for s in range(args.steps):
-        rows = (np.arange(rows_per_step) + (s + args.warmup) * rows_per_step) % w["M"]
+        rows = ((np.arange(rows_per_step) + (s + args.warmup) * rows_per_step) % M).astype(np.int64)
         t0 = time.perf_counter()
-        oracle_step(w, inp, rows.astype(np.int64), addend)
+        oracle_step(w, inp, rows, addend)
         times.append(time.perf_counter() - t0)
+        fl += row_flops(w, rows)
     ms = 1e3 * sum(times) / len(times)
-    value = per_step_flops / (ms / 1e3) / 1e12
+    value = fl / (sum(times)) / 1e12
     cores = os.cpu_count()
     sample = (f"{rows_per_step} output rows x {w['N']} columns x K={w['K']} per step of workload "
               f"{args.workload}; TFLOPS scaled to 2*rows*N*K")
@@ -771,8 +837,8 @@ def main():
     if rank == 0 and not args.no_cpu:
         rate, rows, secs = cpu_oracle_rate(w, head["inp"], budget_s=10.0, addend=addend_for(w)[1])
         cpu = {"value": rate, "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"{rows} output rows x {w['N']} x K={w['K']} of {args.workload} in {secs:.1f} s "
-                         f"(FP64, OpenMP over rows); TFLOPS scaled to 2*rows*N*K"}
+               "sample": f"{rows} output rows x {w['N'] or 'N_g'} x K={w['K'] or 'K_g'} of {args.workload} in "
+                         f"{secs:.1f} s (FP64, OpenMP over rows); TFLOPS scaled to 2*rows*N*K"}
 
     if rank == 0:
         line = {
@@ -780,7 +846,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_mean, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w["dtype"], "data": "synthetic",
             "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "M": w["M"], "N": w["N"],
-                       "K": w["K"], "tile": f"{head['plan'].info.bm}x{head['plan'].info.bn}x{head['plan'].info.bk}",
+                       "K": w["K"], **({"group_shapes": group_shapes(w)} if "shape_groups" in w else {}),
+                       "tile": f"{head['plan'].info.bm}x{head['plan'].info.bn}x{head['plan'].info.bk}",
                        "grid": int(head["plan"].info.grid), "stages": int(head["plan"].info.stages),
                        "cta_group": int(head["plan"].info.cta_group),
                        "l2": "flushed (512 MiB write) between timed steps", "accumulate": "fp32",

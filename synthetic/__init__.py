@@ -184,6 +184,19 @@ def make_group_rows(groups: int, total: int, case: int, spread: float = 0.5):
     return [int(r) for r in rows]
 
 
+def make_group_shapes(groups: int, case: int, m_range=(256, 4096), n_choices=(1024, 2048, 4096, 8192),
+                      k_choices=(1024, 2048, 4096, 8192)):
+    """Seeded (M_g, N_g, K_g) of `groups` GEMMs of different shapes (seed 6000 + c):
+    M_g uniform in m_range rounded to 8, N_g and K_g drawn from the choices."""
+    r = splitmix64(6000 + case, 3 * groups)
+    out = []
+    for g in range(groups):
+        m = m_range[0] + int(r[3 * g] % np.uint64(m_range[1] - m_range[0] + 1))
+        out.append((m - m % 8, int(n_choices[int(r[3 * g + 1] % np.uint64(len(n_choices)))]),
+                    int(k_choices[int(r[3 * g + 2] % np.uint64(len(k_choices)))])))
+    return out
+
+
 def make_addend(M: int, N: int, dist: str, case: int, dtype: str = "bf16"):
     """Seeded M x N addend matrix for beta * C: (array to upload, its FP64 values).
     dtype 'bf16' gives BF16 bit patterns (uint16), 'f32' FP32 values."""

@@ -52,6 +52,11 @@ WORKLOADS = {
     # summing to 16384 (seeded, uneven), BF16 -> BF16, grouped-M G=8 inside each group
     "g1_bf16_grouped": dict(M=16384, N=4096, K=4096, dtype="bf16", dist="normal", case=7, out="bf16",
                             mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2, groups=16),
+    # grouped GEMM over 12 problems of different shapes (seeded M in [256, 4096], N and K in
+    # {1024, 2048, 4096, 8192}), each with its own A, B, D; BF16 -> BF16, one persistent launch
+    "g2_bf16_grouped_shapes": dict(M=0, N=0, K=0, dtype="bf16", dist="normal", case=8, out="bf16",
+                                   mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2,
+                                   shape_groups=12),
     # 8192^3 with mixed FP8 formats: A e4m3, B e5m2 (tensor-wise scales) -> BF16, grouped-N G=16
     "c3m_e4m3_e5m2_8192": dict(M=8192, N=8192, K=8192, dtype="e4m3_e5m2", dist="normal", case=3, out="bf16",
                                mapping=("grouped_n", 16), schedule="persistent", bn=256, cta_group=2,

@@ -277,3 +277,22 @@ def test_grouped_array_fp8_output_epilogue_and_trace():
         want = [(it.tile, it.m, it.n, it.k_tiles) for it in
                 GR.shaped_work_items(u, info.grid, shapes, 128, 128, info.bk, S.BLOCK_2D, 2)]
         assert got == want, u
+
+
+def test_grouped_shapes_workload_full_size_sampled_rows():
+    """The 12-problem workload of different shapes in the launch configuration the
+    benchmark times: sampled rows (first, last and random) of every group against the oracle."""
+    from gemm_check import assert_close, sample_rows
+    from synthetic.workloads import WORKLOADS
+    w = WORKLOADS["g2_bf16_grouped_shapes"]
+    shapes = synthetic.make_group_shapes(w["shape_groups"], w["case"])
+    inps = [synthetic.make_gemm_inputs(m, n, k, w["dtype"], w["dist"], case=100 * w["case"] + g)
+            for g, (m, n, k) in enumerate(shapes)]
+    plan = tst.gemm_grouped_array_plan_create(shapes, dtype=w["dtype"], mapping=w["mapping"], out_dtype=w["out"],
+                                              bn=w["bn"], cta_group=w["cta_group"])
+    dD = _array_run(plan, shapes, [x.A for x in inps], [x.B for x in inps], torch.bfloat16)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    for g, (m, n, k) in enumerate(shapes):
+        rows = sample_rows(m, count=4)
+        z, ad = oracle.gemm(inps[g].A, inps[g].B, "bf16", rows=rows)
+        assert_close(host_values(dD[g])[rows], z, ad, "bf16", f"group {g} {shapes[g]}")
