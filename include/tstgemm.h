@@ -238,9 +238,19 @@ typedef struct {
                               are issued, so the next kernel (launched the same way) may start
                               early too.  Not with Stream-K fixups that need a co-resident grid
                               (TST_ERR_UNSUPPORTED). */
+    int32_t l2_hint;       /* L2 eviction priority of the operand loads ("H100 . cp.async.bulk",
+                              section 6, cache hints: data that is read again is kept with
+                              evict_last; the TMA loads carry an L2 cache policy made by
+                              createpolicy): TST_L2_NONE (default): plain loads; TST_L2_KEEP_A:
+                              A's boxes evict_last, B's evict_normal (a band of A rows is re-read
+                              by every tile of its row strip: linear N-fast, grouped-M);
+                              TST_L2_KEEP_B: the reverse (linear M-fast, grouped-N); TST_L2_AUTO:
+                              KEEP_B for linear M-fast and grouped-N, KEEP_A otherwise.  Hints
+                              change where data is cached, never the results. */
 } tst_plan_options;
 
 enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2, TST_SK_TMA = 3 };
+enum { TST_L2_NONE = 0, TST_L2_KEEP_A = 1, TST_L2_KEEP_B = 2, TST_L2_AUTO = 3 };
 
 /* What the plan decided (for logging and tests). */
 typedef struct {
@@ -261,6 +271,7 @@ typedef struct {
     int32_t ctas;              /* CTAs launched = grid * cta_group */
     int32_t kernels_per_run;   /* kernel launches per gemm_run (2 with the separate reduction) */
     int32_t sk_slots;          /* partial slots per split-tile half (separate reduction), else 1 */
+    int32_t l2_hint;           /* the operand cache hint in use: TST_L2_NONE, _KEEP_A or _KEEP_B */
 } tst_plan_info;
 
 typedef struct tst_plan tst_plan;

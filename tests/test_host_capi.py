@@ -291,3 +291,23 @@ def test_tile_map_every_grid_up_to_40x40():
             got = [tst.gemm_tile_map(p, i) for i in range(Mt * Nt)]
             assert got == [S.tile_map(MAPS[kind], G, Mt, Nt, i) for i in range(Mt * Nt)], (kind, G, Mt, Nt)
             assert len(set(got)) == Mt * Nt
+
+
+@pytest.mark.parametrize("mapping,want", [(("linear_nfast", 1), "keep_a"), (("grouped_m", 8), "keep_a"),
+                                          (("block_2d", 2), "keep_a"), (("morton", 1), "keep_a"),
+                                          (("linear_mfast", 1), "keep_b"), (("grouped_n", 16), "keep_b")])
+def test_l2_hint_auto_keeps_the_strip_operand(mapping, want):
+    codes = {"none": _capi.TST_L2_NONE, "keep_a": _capi.TST_L2_KEEP_A, "keep_b": _capi.TST_L2_KEEP_B}
+    plan = tst.gemm_plan_create(4096, 4096, 4096, mapping=mapping, schedule="persistent", host_only=True,
+                                num_sms=152, l2_hint="auto")
+    assert plan.info.l2_hint == codes[want]
+    for explicit in ("none", "keep_a", "keep_b"):
+        p = tst.gemm_plan_create(4096, 4096, 4096, mapping=mapping, host_only=True, num_sms=152, l2_hint=explicit)
+        assert p.info.l2_hint == codes[explicit]
+
+
+def test_l2_hint_out_of_range_is_rejected():
+    for bad in (-1, 4):
+        with pytest.raises(tst.TstError) as e:
+            tst.gemm_plan_create(256, 256, 256, host_only=True, num_sms=152, l2_hint=bad)
+        assert e.value.status == tst.TST_ERR_INVALID_ARG

@@ -261,6 +261,10 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (opts) o = *opts;
   if (o.bn != 0 && o.bn != 128 && o.bn != 256) return TST_ERR_UNSUPPORTED;
   if (o.num_ctas < 0 || o.num_sms < 0 || o.timeout_ns < 0 || o.pdl < 0 || o.pdl > 1) return TST_ERR_INVALID_ARG;
+  if (o.l2_hint < TST_L2_NONE || o.l2_hint > TST_L2_AUTO) return TST_ERR_INVALID_ARG;
+  if (o.l2_hint == TST_L2_AUTO)   // keep the operand whose band the mapping's strips re-read
+    o.l2_hint = (mapping.kind == TST_MAP_LINEAR_MFAST || mapping.kind == TST_MAP_GROUPED_N) ? TST_L2_KEEP_B
+                                                                                            : TST_L2_KEEP_A;
   const int elt = dtype == TST_BF16 ? 2 : 1;
   if ((K * elt) % 16 != 0) return TST_ERR_ALIGNMENT;  // TMA row stride must be a multiple of 16 bytes
 
@@ -633,6 +637,7 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->ctas = p->sched.grid * p->cg;
   info->kernels_per_run = (p->sk_mode == TST_SK_SEPARATE && p->sched.sk_tiles > 0) ? 2 : 1;
   info->sk_slots = p->sk_slots;
+  info->l2_hint = p->opts.l2_hint;
   return TST_OK;
 }
 
@@ -771,6 +776,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.fmt_ab = p->fmt_ab;
   kp.staging_offset = p->staging_offset;
   kp.pdl = p->opts.pdl;
+  kp.l2_hint = p->opts.l2_hint;
   if (p->ext_on) {
     tst::EpiExt& x = kp.ext;
     x.on = 1;

@@ -188,6 +188,15 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
   WorkItem w;
   int32_t seq = 0;
   long long wait_empty = 0;
+  // operand cache hints: the operand the mapping's strips re-read longest is kept
+  // (evict_last), the other loaded at normal priority
+  const bool hint = p.l2_hint != 0;
+  uint64_t pol_a = 0, pol_b = 0;
+  if (hint) {
+    const uint64_t keep = ptx::l2_policy_evict_last(), normal = ptx::l2_policy_evict_normal();
+    pol_a = p.l2_hint == 1 ? keep : normal;
+    pol_b = p.l2_hint == 1 ? normal : keep;
+  }
   while (ok && work_next(p.sched, it, w)) {
     if (p.trace != nullptr && leader && seq < p.max_items) {
       int32_t* rec = p.trace + (static_cast<int64_t>(c.unit) * p.max_items + seq) * 8;
@@ -222,9 +231,15 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
           const uint32_t sa = smem_a + stage * Cfg::A_BYTES + a * Cfg::A_SUB;
           const uint32_t sb = smem_b + stage * Cfg::B_BYTES + a * Cfg::B_SUB;
           const int32_t kx = kb * BK + a * BK_ATOM;
-          if (CG == 2) {
+          if (CG == 2 && hint) {
+            ptx::tma_load_2d_pair_hint(sa, tmap_a, full_target + 8 * stage, kx, m0, pol_a);
+            ptx::tma_load_2d_pair_hint(sb, tmap_b, full_target + 8 * stage, kx, n0, pol_b);
+          } else if (CG == 2) {
             ptx::tma_load_2d_pair(sa, tmap_a, full_target + 8 * stage, kx, m0);
             ptx::tma_load_2d_pair(sb, tmap_b, full_target + 8 * stage, kx, n0);
+          } else if (hint) {
+            ptx::tma_load_2d_hint(sa, tmap_a, bar_full + 8 * stage, kx, m0, pol_a);
+            ptx::tma_load_2d_hint(sb, tmap_b, bar_full + 8 * stage, kx, n0, pol_b);
           } else {
             ptx::tma_load_2d(sa, tmap_a, bar_full + 8 * stage, kx, m0);
             ptx::tma_load_2d(sb, tmap_b, bar_full + 8 * stage, kx, n0);
