@@ -64,7 +64,7 @@ L2_FLUSH_BYTES = 512 << 20
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
 
 
-PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint")
+PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint", "tma_boxes")
 
 
 def extra_plan_options(w):
@@ -167,7 +167,8 @@ def setup_workload(w, tst, torch):
     if shapes:
         plan = tst.gemm_grouped_array_plan_create(shapes, dtype=w["dtype"], mapping=w["mapping"], out_dtype=w["out"],
                                                   alpha=w.get("alpha", 1.0), bn=w.get("bn", 0),
-                                                  cta_group=w.get("cta_group", 0), l2_hint=w.get("l2_hint", 0))
+                                                  cta_group=w.get("cta_group", 0), l2_hint=w.get("l2_hint", 0),
+                                                  tma_boxes=w.get("tma_boxes", 0))
         host = {}
         for g, x in enumerate(inp):
             host[f"A{g}"] = torch.from_numpy(x.A.view(np.int16) if x.A.dtype == np.uint16 else x.A).pin_memory()
@@ -182,7 +183,7 @@ def setup_workload(w, tst, torch):
         plan = tst.gemm_grouped_plan_create(w["groups"], w["M"], w["N"], w["K"], dtype=w["dtype"],
                                             mapping=w["mapping"], out_dtype=w["out"], alpha=w.get("alpha", 1.0),
                                             bn=w.get("bn", 0), cta_group=w.get("cta_group", 0),
-                                            l2_hint=w.get("l2_hint", 0))
+                                            l2_hint=w.get("l2_hint", 0), tma_boxes=w.get("tma_boxes", 0))
         a_np = inp.A.view(np.int16) if inp.A.dtype == np.uint16 else inp.A
         b_np = inp.B.view(np.int16) if inp.B.dtype == np.uint16 else inp.B
         host = {"A": torch.from_numpy(a_np).pin_memory(), "B": torch.from_numpy(b_np).pin_memory(),

@@ -247,10 +247,19 @@ typedef struct {
                               TST_L2_KEEP_B: the reverse (linear M-fast, grouped-N); TST_L2_AUTO:
                               KEEP_B for linear M-fast and grouped-N, KEEP_A otherwise.  Hints
                               change where data is cached, never the results. */
+    int32_t tma_boxes;     /* how a stage's operand tiles are requested from TMA: one 2-D box per
+                              128-byte atom of K, or one 3-D box per operand and stage (the
+                              operand viewed as atom elements x rows x atoms), which needs a
+                              k-tile of two atoms and K a whole number of atoms (every group's
+                              K_g, for groups of different shapes).  The shared-memory image is
+                              the same either way.  TST_BOXES_2D: always 2-D; TST_BOXES_3D: 3-D
+                              wherever possible; TST_BOXES_AUTO (default): 3-D for 128-column CTA
+                              pair tiles, where it measured faster, else 2-D. */
 } tst_plan_options;
 
 enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2, TST_SK_TMA = 3 };
 enum { TST_L2_NONE = 0, TST_L2_KEEP_A = 1, TST_L2_KEEP_B = 2, TST_L2_AUTO = 3 };
+enum { TST_BOXES_AUTO = 0, TST_BOXES_2D = 1, TST_BOXES_3D = 2 };
 
 /* What the plan decided (for logging and tests). */
 typedef struct {
@@ -272,6 +281,7 @@ typedef struct {
     int32_t kernels_per_run;   /* kernel launches per gemm_run (2 with the separate reduction) */
     int32_t sk_slots;          /* partial slots per split-tile half (separate reduction), else 1 */
     int32_t l2_hint;           /* the operand cache hint in use: TST_L2_NONE, _KEEP_A or _KEEP_B */
+    int32_t box3d;             /* 1: one 3-D TMA box per operand and stage, 0: 2-D boxes per atom */
 } tst_plan_info;
 
 typedef struct tst_plan tst_plan;

@@ -311,3 +311,30 @@ def test_l2_hint_out_of_range_is_rejected():
         with pytest.raises(tst.TstError) as e:
             tst.gemm_plan_create(256, 256, 256, host_only=True, num_sms=152, l2_hint=bad)
         assert e.value.status == tst.TST_ERR_INVALID_ARG
+
+
+def test_tma_box_shape_choice():
+    """3-D boxes need two atoms per k-tile and K (every K_g) a whole number of atoms; by
+    default only 128-column pair tiles take them."""
+    def box3d(M, N, K, **kw):
+        kw.setdefault("tma_boxes", "3d")
+        return tst.gemm_plan_create(M, N, K, host_only=True, num_sms=152, schedule="persistent", **kw).info.box3d
+    assert box3d(4096, 4096, 4096) == 1
+    assert box3d(4096, 4096, 4096, bk=64) == 0                 # one atom per stage: nothing to merge
+    assert box3d(4096, 4096, 4104) == 0                        # K not a whole number of 64-element atoms
+    assert box3d(1000, 904, 4160) == 1                         # K tail inside the last k-tile, whole atoms
+    assert box3d(4096, 4096, 4096, tma_boxes="2d") == 0
+    assert box3d(4096, 4096, 4096, dtype="e4m3") == 1
+    assert box3d(4096, 4096, 4160, dtype="e4m3") == 0          # 128-element FP8 atoms
+    # default: 128-column CTA pairs only
+    assert box3d(4096, 4096, 4096, tma_boxes="auto", bn=128, cta_group=2) == 1
+    assert box3d(4096, 4096, 4096, tma_boxes="auto", bn=256, cta_group=2) == 0
+    assert box3d(4096, 4096, 4096, tma_boxes="auto", bn=128, cta_group=1) == 0
+    ok = tst.gemm_grouped_array_plan_create([(100, 200, 256), (50, 64, 512)], host_only=True, num_sms=152,
+                                            tma_boxes="3d")
+    ragged = tst.gemm_grouped_array_plan_create([(100, 200, 256), (50, 64, 520)], host_only=True, num_sms=152,
+                                                tma_boxes="3d")
+    assert ok.info.box3d == 1 and ragged.info.box3d == 0
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_plan_create(256, 256, 256, host_only=True, num_sms=152, tma_boxes=3)
+    assert e.value.status == tst.TST_ERR_INVALID_ARG

@@ -37,6 +37,7 @@ _FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separ
           "tma": _capi.TST_SK_TMA}
 _L2 = {"none": _capi.TST_L2_NONE, "keep_a": _capi.TST_L2_KEEP_A, "keep_b": _capi.TST_L2_KEEP_B,
        "auto": _capi.TST_L2_AUTO}
+_BOXES = {"auto": _capi.TST_BOXES_AUTO, "2d": _capi.TST_BOXES_2D, "3d": _capi.TST_BOXES_3D}
 _SCHED = {"static": TST_STATIC, "persistent": TST_PERSISTENT, "streamk": TST_STREAMK,
           "streamk_hybrid": TST_STREAMK_HYBRID, "hytis": TST_HYTIS}
 
@@ -94,7 +95,8 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      use_scales: bool = False, bn: int = 0, num_ctas: int = 0, sk_forward: bool = False,
                      host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
                      stages: int = 0, bk: int = 0, sk_groups: int = 0, sk_fixup="deterministic", pdl: bool = False,
-                     l2_hint="none", beta: float = 0.0, has_c: bool = False, c_dtype="f32", bias_mode=None, activation=None,
+                     l2_hint="none", tma_boxes="auto", beta: float = 0.0, has_c: bool = False, c_dtype="f32",
+                     bias_mode=None, activation=None,
                      row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
                      amax: bool = False, aux: bool = False, aux_dtype="f32") -> Plan:
     """Plan C = epilogue(A x B).  The basic epilogue is alpha, a column bias (has_bias),
@@ -106,7 +108,8 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
                                   int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
                                   int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"), int(bool(pdl)),
-                                  _enum(_L2, l2_hint, "l2_hint"))
+                                  _enum(_L2, l2_hint, "l2_hint"),
+                                  _enum(_BOXES, tma_boxes, "tma_boxes"))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \
@@ -141,7 +144,7 @@ def gemm_grouped_plan_create(groups: int, M: int, N: int, K: int, dtype="bf16", 
                              col_scale: bool = False, d_scale: bool = False, amax: bool = False, aux: bool = False,
                              aux_dtype="f32", bn: int = 0, num_ctas: int = 0, host_only: bool = False,
                              num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0, stages: int = 0,
-                             bk: int = 0, pdl: bool = False, l2_hint="none") -> Plan:
+                             bk: int = 0, pdl: bool = False, l2_hint="none", tma_boxes="auto") -> Plan:
     """Plan `groups` GEMMs sharing N and K in one persistent launch: A holds the groups'
     rows one after another (at most M in all), B one N x K matrix per group; the row
     counts are given to gemm_grouped_run as a device int32 array."""
@@ -149,7 +152,8 @@ def gemm_grouped_plan_create(groups: int, M: int, N: int, K: int, dtype="bf16", 
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), 0, int(bool(host_only)), int(num_sms), int(cta_group),
                                   int(timeout_ns), int(stages), int(bk), 0, 0, int(bool(pdl)),
-                                  _enum(_L2, l2_hint, "l2_hint"))
+                                  _enum(_L2, l2_hint, "l2_hint"),
+                                  _enum(_BOXES, tma_boxes, "tma_boxes"))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \
@@ -182,7 +186,8 @@ def gemm_grouped_array_plan_create(shapes, dtype="bf16", mapping=("grouped_m", 8
                                    alpha: float = 1.0, relu: bool = False, activation=None, use_scales: bool = False,
                                    d_scale: bool = False, amax: bool = False, bn: int = 0, num_ctas: int = 0,
                                    host_only: bool = False, num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0,
-                                   stages: int = 0, bk: int = 0, pdl: bool = False, l2_hint="none") -> Plan:
+                                   stages: int = 0, bk: int = 0, pdl: bool = False, l2_hint="none",
+                                   tma_boxes="auto") -> Plan:
     """Plan a grouped GEMM over groups of different shapes: `shapes` is a list of
     (M_g, N_g, K_g); each group has its own A, B and D (gemm_grouped_array_run)."""
     G = len(shapes)
@@ -193,7 +198,8 @@ def gemm_grouped_array_plan_create(shapes, dtype="bf16", mapping=("grouped_m", 8
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), 0, int(bool(host_only)), int(num_sms), int(cta_group),
                                   int(timeout_ns), int(stages), int(bk), 0, 0, int(bool(pdl)),
-                                  _enum(_L2, l2_hint, "l2_hint"))
+                                  _enum(_L2, l2_hint, "l2_hint"),
+                                  _enum(_BOXES, tma_boxes, "tma_boxes"))
     act = _enum(_ACT, activation, "activation") if activation is not None else \
         (TST_ACT_RELU if relu else TST_ACT_NONE)
     epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), 0.0, 0, 0, TST_BIAS_NONE, act,

@@ -55,6 +55,7 @@ struct tst_plan {
   int32_t sk_slots = 1;        // partial slots per split-tile half
   const void* reduce_kernel = nullptr;
   int32_t ka = 1;              // 128-byte swizzle atoms of K per pipeline stage
+  bool box3d = false;          // operand maps are 3-D: one box per operand and stage
   int32_t num_sms = 0, max_items = 0, resident_units = 0;
   tst::Sched sched{};          // order points at order_host; launches swap in d_order
   std::vector<int32_t> order_host;  // Morton mapping: (m, n) of every task
@@ -111,20 +112,37 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D K-major operand: rows x K elements, box = box_k x box_rows, 128-byte swizzle,
-// out-of-bounds elements read as zero (ragged M, N and K tails).
+// K-major operand of rows x K elements, 128-byte swizzle, out-of-bounds elements read as
+// zero (ragged M, N and K tails).  atoms == 0: a 2-D map, box = box_k (one 128-byte atom)
+// x box_rows.  atoms > 0: a 3-D view (box_k elements of one atom, rows, K / box_k atoms;
+// the atom stride, 128 bytes, is below the row stride) with box box_k x box_rows x atoms,
+// whose image is `atoms` consecutive box_rows x 128-byte sub-tiles, as `atoms` 2-D boxes
+// give; K must be a whole number of atoms (a partial last atom would read the next row).
 bool encode_operand(CUtensorMap* map, const void* ptr, tst_dtype dt, int64_t rows, int64_t K, int box_k,
-                    int box_rows) {
+                    int box_rows, int atoms = 0) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int elt = dt == TST_BF16 ? 2 : 1;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * elt};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, dt == TST_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType type = dt == TST_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r;
+  if (atoms == 0) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * elt};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(map, type, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    if (K % box_k != 0) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(box_k), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(K / box_k)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * elt, static_cast<cuuint64_t>(box_k) * elt};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows),
+                         static_cast<cuuint32_t>(atoms)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(map, type, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS;
 }
 
@@ -304,6 +322,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (o.bk != 0 && o.bk != 128 / elt && o.bk != 256 / elt) { delete p; return TST_ERR_UNSUPPORTED; }
   p->ka = o.bk == 128 / elt ? 1 : 2;
   p->bk = p->ka * 128 / elt;
+  if (o.tma_boxes < TST_BOXES_AUTO || o.tma_boxes > TST_BOXES_3D) { delete p; return TST_ERR_INVALID_ARG; }
   // tile width and CTA group: as given, else by the cost model
   {
     const TileChoice tc = choose_tile(M, N, K, elt, out_bytes(epi->out_dtype), p->num_sms, o.bn, o.cta_group);
@@ -311,6 +330,14 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     p->cg = o.cta_group != 0 ? o.cta_group : tc.cg;
   }
   p->bm = tst::kBlockM * p->cg;
+  // one 3-D box per operand and stage: needs two atoms per k-tile and K (every group's K_g)
+  // a whole number of 128-byte atoms; chosen by default for 128-column pair tiles only
+  // (measured: +3 % there, 1-4 % slower on the other tile shapes)
+  p->box3d = p->ka > 1 && (K * elt) % 128 == 0 &&
+             (o.tma_boxes == TST_BOXES_3D || (o.tma_boxes == TST_BOXES_AUTO && p->bn == 128 && p->cg == 2));
+  if (shapes)
+    for (int32_t g = 0; g < groups; ++g)
+      if ((static_cast<int64_t>(shapes[4 * g + 2]) * elt) % 128 != 0) p->box3d = false;
   const int64_t mt = ceil_div(M, p->bm);
   const int64_t nt = ceil_div(N, p->bn);
   const int64_t kt = ceil_div(K, p->bk);
@@ -638,6 +665,7 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->kernels_per_run = (p->sk_mode == TST_SK_SEPARATE && p->sched.sk_tiles > 0) ? 2 : 1;
   info->sk_slots = p->sk_slots;
   info->l2_hint = p->opts.l2_hint;
+  info->box3d = p->box3d ? 1 : 0;
   return TST_OK;
 }
 
@@ -733,11 +761,13 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   // 256 x bn tile between its two CTAs)
   const int box_k = p->bk / p->ka;
   if (!array_mode && A != p->tm_A) {
-    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, box_k, tst::kBlockM)) return TST_ERR_CUDA;
+    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, box_k, tst::kBlockM, p->box3d ? p->ka : 0))
+      return TST_ERR_CUDA;
     p->tm_A = A;
   }
   if (!array_mode && B != p->tm_B) {
-    if (!encode_operand(&p->tmap_b, B, p->dtype, p->b_rows, p->K, box_k, p->bn / p->cg)) return TST_ERR_CUDA;
+    if (!encode_operand(&p->tmap_b, B, p->dtype, p->b_rows, p->K, box_k, p->bn / p->cg, p->box3d ? p->ka : 0))
+      return TST_ERR_CUDA;
     // HyTiS half-width tiles read half of the B rows per stage
     if (p->sched.narrow_tiles > 0 &&
         !encode_operand(&p->tmap_b_half, B, p->dtype, p->b_rows, p->K, box_k, p->bn / (2 * p->cg)))
@@ -777,6 +807,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.staging_offset = p->staging_offset;
   kp.pdl = p->opts.pdl;
   kp.l2_hint = p->opts.l2_hint;
+  kp.box3d = p->box3d ? 1 : 0;
   if (p->ext_on) {
     tst::EpiExt& x = kp.ext;
     x.on = 1;
@@ -951,8 +982,9 @@ tst_status gemm_grouped_array_run(tst_plan* p, const void* const* A, const void*
     for (int32_t g = 0; g < G; ++g) {
       const int64_t Mg = p->shapes_host[4 * g], Ng = p->shapes_host[4 * g + 1], Kg = p->shapes_host[4 * g + 2];
       if (Mg == 0 || Ng == 0) continue;
-      if (!encode_operand(&p->tmaps_host[2 * g], A[g], p->dtype, Mg, Kg, box_k, tst::kBlockM) ||
-          !encode_operand(&p->tmaps_host[2 * g + 1], B[g], p->dtype, Ng, Kg, box_k, p->bn / p->cg))
+      const int atoms = p->box3d ? p->ka : 0;
+      if (!encode_operand(&p->tmaps_host[2 * g], A[g], p->dtype, Mg, Kg, box_k, tst::kBlockM, atoms) ||
+          !encode_operand(&p->tmaps_host[2 * g + 1], B[g], p->dtype, Ng, Kg, box_k, p->bn / p->cg, atoms))
         return TST_ERR_CUDA;
       outs[g] = D[g];
       p->last_ptrs[3 * g] = A[g];

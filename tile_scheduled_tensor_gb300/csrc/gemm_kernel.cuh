@@ -226,23 +226,37 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
       if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * stage_bytes);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
+        // a pair's loads complete on the leader's FULL barrier
+        const uint32_t bar = CG == 2 ? full_target + 8 * stage : bar_full + 8 * stage;
+        auto load2 = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, uint64_t pol) {
+          if (CG == 2 && hint) ptx::tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+          else if (CG == 2) ptx::tma_load_2d_pair(dst, map, bar, x, y);
+          else if (hint) ptx::tma_load_2d_hint(dst, map, bar, x, y, pol);
+          else ptx::tma_load_2d(dst, map, bar, x, y);
+        };
+        auto load3 = [&](uint32_t dst, const CUtensorMap* map, int32_t y, int32_t z, uint64_t pol) {
+          if (CG == 2 && hint) ptx::tma_load_3d_pair_hint(dst, map, bar, 0, y, z, pol);
+          else if (CG == 2) ptx::tma_load_3d_pair(dst, map, bar, 0, y, z);
+          else if (hint) ptx::tma_load_3d_hint(dst, map, bar, 0, y, z, pol);
+          else ptx::tma_load_3d(dst, map, bar, 0, y, z);
+        };
+        const uint32_t sa = smem_a + stage * Cfg::A_BYTES;
+        const uint32_t sb = smem_b + stage * Cfg::B_BYTES;
+        if (KA > 1 && p.box3d) {
+          // one 3-D box per operand: the KA atom columns land at KA consecutive sub-tiles,
+          // the same image as KA 2-D boxes, in fewer requests.  A half-width B (HyTiS)
+          // keeps its 2-D boxes at the full-width sub-tile stride.
+          load3(sa, tmap_a, m0, kb * KA, pol_a);
+          if (!narrow) load3(sb, tmap_b, n0, kb * KA, pol_b);
+          else
 #pragma unroll
-        for (int a = 0; a < KA; ++a) {  // one box per swizzle-atom column of K
-          const uint32_t sa = smem_a + stage * Cfg::A_BYTES + a * Cfg::A_SUB;
-          const uint32_t sb = smem_b + stage * Cfg::B_BYTES + a * Cfg::B_SUB;
-          const int32_t kx = kb * BK + a * BK_ATOM;
-          if (CG == 2 && hint) {
-            ptx::tma_load_2d_pair_hint(sa, tmap_a, full_target + 8 * stage, kx, m0, pol_a);
-            ptx::tma_load_2d_pair_hint(sb, tmap_b, full_target + 8 * stage, kx, n0, pol_b);
-          } else if (CG == 2) {
-            ptx::tma_load_2d_pair(sa, tmap_a, full_target + 8 * stage, kx, m0);
-            ptx::tma_load_2d_pair(sb, tmap_b, full_target + 8 * stage, kx, n0);
-          } else if (hint) {
-            ptx::tma_load_2d_hint(sa, tmap_a, bar_full + 8 * stage, kx, m0, pol_a);
-            ptx::tma_load_2d_hint(sb, tmap_b, bar_full + 8 * stage, kx, n0, pol_b);
-          } else {
-            ptx::tma_load_2d(sa, tmap_a, bar_full + 8 * stage, kx, m0);
-            ptx::tma_load_2d(sb, tmap_b, bar_full + 8 * stage, kx, n0);
+            for (int a = 0; a < KA; ++a) load2(sb + a * Cfg::B_SUB, tmap_b, kb * BK + a * BK_ATOM, n0, pol_b);
+        } else {
+#pragma unroll
+          for (int a = 0; a < KA; ++a) {  // one box per swizzle-atom column of K
+            const int32_t kx = kb * BK + a * BK_ATOM;
+            load2(sa + a * Cfg::A_SUB, tmap_a, kx, m0, pol_a);
+            load2(sb + a * Cfg::B_SUB, tmap_b, kx, n0, pol_b);
           }
         }
       }
@@ -701,8 +715,11 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
         constexpr int BK = (DT == DT_BF16 ? 64 : 128) * KA;
         const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (BN / CG);
         const int32_t kend = w.k_begin + (w.k_count < p.stages ? w.k_count : p.stages);
-        for (int32_t kb = w.k_begin; kb < kend; ++kb)
-          for (int a = 0; a < KA; ++a) ptx::tma_prefetch_l2_2d(&p.tmap_b, kb * BK + a * (BK / KA), n0);
+        for (int32_t kb = w.k_begin; kb < kend; ++kb) {
+          if (p.box3d && KA > 1) ptx::tma_prefetch_l2_3d(&p.tmap_b, 0, n0, kb * KA);
+          else
+            for (int a = 0; a < KA; ++a) ptx::tma_prefetch_l2_2d(&p.tmap_b, kb * BK + a * (BK / KA), n0);
+        }
       }
     }
     ptx::griddep_wait();
