@@ -332,6 +332,27 @@ tst_status gemm_plan_create_epi(tst_plan **plan, int64_t M, int64_t N, int64_t K
 tst_status gemm_run_epi(tst_plan *plan, const void *A, const void *B, void *D,
                         const tst_epilogue_args *args, void *stream);
 
+/* The GEMM end to end on HOST buffers: A (M x K), B (N x K) and D (M x N) in host
+ * memory, laid out as for gemm_run; args as in gemm_run_epi (DEVICE pointers, or
+ * NULL when the plan's epilogue needs none).  No counterpart on the pages: the
+ * host-level analogue of the kernel's overlap of loads with MMAs.  The call copies
+ * B to a plan-owned device buffer, then A in row panels (a whole number of
+ * scheduled tile rows each, `panels` of them, 0 = about 8, at most 64); each
+ * panel's GEMM runs on `stream` as soon as its rows have landed, and its rows of D
+ * are copied back while later panels are still arriving.  Two plan-owned copy
+ * streams carry the transfers, ordered after earlier work on `stream`, and
+ * `stream` waits for the last copy, so the call is asynchronous and stream-ordered
+ * like gemm_run; D is complete once `stream` is.  Host buffers should be pinned
+ * (cudaHostAlloc / cudaHostRegister) for the copies to overlap; pageable ones are
+ * copied synchronously.  The first call allocates the device buffers (M K + N K
+ * input elements, M N outputs), the streams and one plan per panel height; later
+ * calls reuse them (with the same `panels`).  amax, if set, covers all panels.
+ * gemm_status_query reports the panels' device status.  Errors: INVALID_ARG (a
+ * NULL operand, panels outside 0..64), UNSUPPORTED (grouped plans), NO_DEVICE,
+ * OOM, CUDA, and those of gemm_run_epi; after an error D is unspecified. */
+tst_status gemm_run_host(tst_plan *plan, const void *A_host, const void *B_host, void *D_host,
+                         const tst_epilogue_args *args, int32_t panels, void *stream);
+
 /* Grouped GEMM: `groups` independent GEMMs in one persistent launch ("H100 .
  * Kernel Design", section 10.2, Grouped Persistent Scheduling).  The groups
  * share N and K; group g has M_g rows, M_g read from device memory at run time

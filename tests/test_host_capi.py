@@ -338,3 +338,26 @@ def test_tma_box_shape_choice():
     with pytest.raises(tst.TstError) as e:
         tst.gemm_plan_create(256, 256, 256, host_only=True, num_sms=152, tma_boxes=3)
     assert e.value.status == tst.TST_ERR_INVALID_ARG
+
+
+def test_run_host_argument_errors():
+    import torch
+    plan = tst.gemm_plan_create(512, 256, 256, host_only=True, num_sms=152)
+    A = torch.zeros(512, 256, dtype=torch.bfloat16)
+    B = torch.zeros(256, 256, dtype=torch.bfloat16)
+    D = torch.zeros(512, 256)
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_run_host(plan, A, B, D, stream=0)
+    assert e.value.status == tst.TST_ERR_NO_DEVICE
+    for panels in (-1, 65):
+        with pytest.raises(tst.TstError) as e:
+            tst.gemm_run_host(plan, A, B, D, panels=panels, stream=0)
+        assert e.value.status == tst.TST_ERR_INVALID_ARG
+    lib = tst.lib
+    args = _capi.tst_epilogue_args()
+    assert lib.gemm_run_host(plan._h, None, B.data_ptr(), D.data_ptr(), ctypes.byref(args), 0, None) == \
+        tst.TST_ERR_INVALID_ARG
+    assert lib.gemm_run_host(None, A.data_ptr(), B.data_ptr(), D.data_ptr(), ctypes.byref(args), 0, None) == \
+        tst.TST_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        tst.gemm_run_host(plan, A, B, [1], stream=0)

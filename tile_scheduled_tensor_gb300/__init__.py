@@ -295,6 +295,25 @@ def gemm_run(plan: Plan, A, B, C, bias=None, scales=None, stream=None, c=None, r
            "gemm_run_epi")
 
 
+def _host_ptr(x):
+    if not hasattr(x, "data_ptr") or x.is_cuda:
+        raise ValueError("gemm_run_host takes host (CPU) tensors; pinned ones overlap the copies")
+    if not x.is_contiguous():
+        raise ValueError("tensors passed to the GEMM must be contiguous")
+    return x.data_ptr()
+
+
+def gemm_run_host(plan: Plan, A, B, D, panels: int = 0, stream=None, bias=None, scales=None, c=None,
+                  row_scale=None, col_scale=None, d_scale=None, amax=None, aux=None):
+    """End to end on host tensors A, B, D (CPU, contiguous; pinned for the copies to
+    overlap the computation): row panels of A stream in, each panel's GEMM runs as soon as
+    it has landed, its rows of D stream back.  Epilogue operands are CUDA tensors."""
+    args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux))
+    _check(lib.gemm_run_host(plan._h, _host_ptr(A), _host_ptr(B), _host_ptr(D), ctypes.byref(args), int(panels),
+                             _stream(stream)), "gemm_run_host")
+
+
 def gemm_status_query(plan: Plan):
     """(status, raw status word) of the last run; synchronises that run's stream."""
     word = ctypes.c_uint32()

@@ -93,6 +93,7 @@ _SIGNATURES = {
                                             ctypes.POINTER(tst_epilogue_ex), ctypes.POINTER(tst_plan_options)]),
     "gemm_run": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "gemm_run_epi": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(tst_epilogue_args), _P]),
+    "gemm_run_host": (ctypes.c_int, [_P, _P, _P, _P, ctypes.POINTER(tst_epilogue_args), ctypes.c_int32, _P]),
     "gemm_grouped_plan_create": (ctypes.c_int, [ctypes.POINTER(_P), ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
                                                 ctypes.c_int64, ctypes.c_int, ctypes.c_int, tst_mapping,
                                                 ctypes.POINTER(tst_epilogue_ex), ctypes.POINTER(tst_plan_options)]),

@@ -27,6 +27,19 @@
 #include "tile_sched.h"
 #include "tstgemm.h"
 
+// gemm_run_host's state: device copies of the operands and of D, the two copy streams,
+// events ([start, done, then one per panel for its inputs and one for its GEMM]) and
+// the plans of the (at most two) panel heights
+struct HostRun {
+  void* dA = nullptr;
+  void* dB = nullptr;
+  void* dD = nullptr;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  std::vector<cudaEvent_t> events;
+  tst_plan* panel_plan[2] = {nullptr, nullptr};
+  int64_t panel_rows[2] = {0, 0};
+};
+
 struct tst_plan {
   int64_t M = 0, N = 0, K = 0;
   tst_dtype dtype = TST_BF16;
@@ -82,9 +95,14 @@ struct tst_plan {
   CUtensorMap tmap_a{}, tmap_b{}, tmap_b_half{}, tmap_ws{};
   cudaStream_t last_stream = nullptr;
   bool ran = false;
+  HostRun* host_run = nullptr;   // gemm_run_host state (created by its first call)
+  bool last_run_host = false;    // the last run was gemm_run_host: its panel plans hold the status
 };
 
 namespace {
+
+constexpr int32_t kMaxHostPanels = 64;      // gemm_run_host: most row panels per call
+constexpr int32_t kDefaultHostPanels = 8;   // and how many it aims for by default
 
 bool log_enabled() {
   static int v = [] {
@@ -639,6 +657,17 @@ tst_status gemm_plan_create(tst_plan** plan, int64_t M, int64_t N, int64_t K, ts
 tst_status gemm_plan_destroy(tst_plan* plan) {
   if (plan == nullptr) return TST_OK;
   tst_status st = TST_OK;
+  if (HostRun* h = plan->host_run) {
+    for (cudaEvent_t e : h->events)
+      if (cudaEventDestroy(e) != cudaSuccess) st = TST_ERR_CUDA;
+    for (cudaStream_t s : {h->s_in, h->s_out})
+      if (s && cudaStreamDestroy(s) != cudaSuccess) st = TST_ERR_CUDA;
+    for (void* b : {h->dA, h->dB, h->dD})
+      if (b && cudaFree(b) != cudaSuccess) st = TST_ERR_CUDA;
+    for (tst_plan* c : h->panel_plan)
+      if (gemm_plan_destroy(c) != TST_OK) st = TST_ERR_CUDA;
+    delete h;
+  }
   if (plan->dev_block && cudaFree(plan->dev_block) != cudaSuccess) st = TST_ERR_CUDA;
   if (plan->d_order && cudaFree(plan->d_order) != cudaSuccess) st = TST_ERR_CUDA;
   if (plan->dev_groups && cudaFree(plan->dev_groups) != cudaSuccess) st = TST_ERR_CUDA;
@@ -728,7 +757,7 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
 namespace {
 
 tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
-                  const int32_t* group_rows, void* stream_) {
+                  const int32_t* group_rows, void* stream_, bool keep_amax = false) {
   if (p == nullptr || ea == nullptr) return TST_ERR_INVALID_ARG;
   // groups of different shapes bring their own operands (uploaded by gemm_grouped_array_run)
   const bool array_mode = !p->shapes_host.empty();
@@ -836,7 +865,8 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   if (++p->run_id == 0) p->run_id = 1;
   kp.run_id = p->run_id;
   // amax starts at zero for every launch
-  if (kp.ext.amax && cudaMemsetAsync(kp.ext.amax, 0, sizeof(float), stream) != cudaSuccess) return TST_ERR_CUDA;
+  if (kp.ext.amax && !keep_amax && cudaMemsetAsync(kp.ext.amax, 0, sizeof(float), stream) != cudaSuccess)
+    return TST_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg), 1, 1);
@@ -903,6 +933,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   }
   p->last_stream = stream;
   p->ran = true;
+  p->last_run_host = false;
   return TST_OK;
 }
 
@@ -1003,6 +1034,132 @@ tst_status gemm_grouped_array_run(tst_plan* p, const void* const* A, const void*
   return launch(p, nullptr, nullptr, nullptr, args, nullptr, stream);
 }
 
+tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, const tst_epilogue_args* args,
+                         int32_t panels, void* stream_) {
+  if (p == nullptr || A == nullptr || B == nullptr || D == nullptr || panels < 0 || panels > kMaxHostPanels)
+    return TST_ERR_INVALID_ARG;
+  if (p->host_only || p->kernel == nullptr) return TST_ERR_NO_DEVICE;
+  if (p->groups > 0) return TST_ERR_UNSUPPORTED;
+  const tst_epilogue_args none{};
+  const tst_epilogue_args* ea = args ? args : &none;
+  const tst_epilogue_ex& e = p->epi;
+  const int64_t M = p->M, N = p->N, K = p->K;
+  const int64_t elt = p->dtype == TST_BF16 ? 2 : 1;
+  const int64_t out_elt = e.out_dtype == TST_OUT_F32 ? 4 : e.out_dtype == TST_OUT_BF16 ? 2 : 1;
+  // panel height: a whole number of scheduled tile rows (so every offset below keeps the
+  // 16-byte alignment of its base); default about M / 8
+  const int64_t want = panels == 0 ? kDefaultHostPanels : panels;
+  const int64_t R = std::max<int64_t>(ceil_div(ceil_div(M, want), p->bm) * p->bm, p->bm);
+  const int64_t P = ceil_div(M, R);
+
+  HostRun* h = p->host_run;
+  if (h == nullptr) {
+    h = new (std::nothrow) HostRun();
+    if (h == nullptr) return TST_ERR_OOM;
+    p->host_run = h;
+  }
+  if (h->dA == nullptr) {
+    if (cudaMalloc(&h->dA, M * K * elt) != cudaSuccess || cudaMalloc(&h->dB, N * K * elt) != cudaSuccess ||
+        cudaMalloc(&h->dD, M * N * out_elt) != cudaSuccess) {
+      cudaGetLastError();
+      for (void** b : {&h->dA, &h->dB, &h->dD}) {
+        if (*b) cudaFree(*b);
+        *b = nullptr;
+      }
+      return TST_ERR_OOM;
+    }
+  }
+  if (h->s_in == nullptr && (cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) != cudaSuccess ||
+                             cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) != cudaSuccess))
+    return TST_ERR_CUDA;
+  while (static_cast<int64_t>(h->events.size()) < 2 + 2 * P) {
+    cudaEvent_t ev;
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return TST_ERR_CUDA;
+    h->events.push_back(ev);
+  }
+  // the plan of a panel height: the parent's tile, CTA group, k-tile and options
+  auto panel_plan = [&](int64_t rows, tst_plan** out) -> tst_status {
+    for (int i = 0; i < 2; ++i)
+      if (h->panel_plan[i] && h->panel_rows[i] == rows) { *out = h->panel_plan[i]; return TST_OK; }
+    int slot = h->panel_plan[0] == nullptr ? 0 : h->panel_plan[1] == nullptr ? 1 : -1;
+    if (slot < 0) {   // another panel count than before: start over
+      for (int i = 0; i < 2; ++i) {
+        gemm_plan_destroy(h->panel_plan[i]);
+        h->panel_plan[i] = nullptr;
+      }
+      slot = 0;
+    }
+    tst_plan_options o = p->opts;
+    o.bn = p->bn;
+    o.cta_group = p->cg;
+    o.bk = p->bk;
+    tst_plan* c = nullptr;
+    const tst_status st = create_plan(&c, rows, N, K, p->dtype, TST_LAYOUT_A_ROW_B_NK, p->mapping, p->schedule,
+                                      &p->epi, &o);
+    if (st != TST_OK) return st;
+    c->timeout_ns = p->timeout_ns;
+    h->panel_plan[slot] = c;
+    h->panel_rows[slot] = rows;
+    *out = c;
+    return TST_OK;
+  };
+  // the row-dependent epilogue operands of a panel starting at row r0
+  auto panel_args = [&](int64_t r0) {
+    tst_epilogue_args a = *ea;
+    if (a.c) a.c = static_cast<const char*>(a.c) + r0 * N * (e.c_dtype == TST_OUT_F32 ? 4 : 2);
+    if (a.bias && e.bias_mode == TST_BIAS_ROW) a.bias += r0;
+    if (a.row_scale) a.row_scale += r0;
+    if (a.aux) a.aux = static_cast<char*>(a.aux) + r0 * N * (e.aux_dtype == TST_OUT_F32 ? 4 : 2);
+    return a;
+  };
+  // every panel plan exists before anything is enqueued
+  tst_plan* plans[kMaxHostPanels];
+  for (int64_t q = 0; q < P; ++q) {
+    const tst_status st = panel_plan(std::min(R, M - q * R), &plans[q]);
+    if (st != TST_OK) return st;
+  }
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream_);
+  cudaEvent_t* ev = h->events.data();
+  const char* hA = static_cast<const char*>(A);
+  char* dA = static_cast<char*>(h->dA);
+  char* dD = static_cast<char*>(h->dD);
+  bool ok = cudaEventRecord(ev[0], s) == cudaSuccess && cudaStreamWaitEvent(h->s_in, ev[0], 0) == cudaSuccess &&
+            cudaStreamWaitEvent(h->s_out, ev[0], 0) == cudaSuccess;
+  // inputs: B whole, then A panel by panel
+  ok = ok && cudaMemcpyAsync(h->dB, B, N * K * elt, cudaMemcpyHostToDevice, h->s_in) == cudaSuccess;
+  for (int64_t q = 0; ok && q < P; ++q) {
+    const int64_t r0 = q * R, rows = std::min(R, M - r0);
+    ok = cudaMemcpyAsync(dA + r0 * K * elt, hA + r0 * K * elt, rows * K * elt, cudaMemcpyHostToDevice, h->s_in) ==
+             cudaSuccess &&
+         cudaEventRecord(ev[2 + q], h->s_in) == cudaSuccess;
+  }
+  if (!ok) return TST_ERR_CUDA;
+  // the panels' GEMMs on the caller's stream, each after its rows of A have landed
+  for (int64_t q = 0; q < P; ++q) {
+    const int64_t r0 = q * R;
+    if (cudaStreamWaitEvent(s, ev[2 + q], 0) != cudaSuccess) return TST_ERR_CUDA;
+    const tst_epilogue_args a = panel_args(r0);
+    const tst_status st = launch(plans[q], dA + r0 * K * elt, h->dB, dD + r0 * N * out_elt, &a, nullptr, s, q > 0);
+    if (st != TST_OK) return st;
+    if (cudaEventRecord(ev[2 + P + q], s) != cudaSuccess) return TST_ERR_CUDA;
+  }
+  // outputs: each panel's D as soon as its GEMM is done
+  char* hD = static_cast<char*>(D);
+  for (int64_t q = 0; ok && q < P; ++q) {
+    const int64_t r0 = q * R, rows = std::min(R, M - r0);
+    ok = cudaStreamWaitEvent(h->s_out, ev[2 + P + q], 0) == cudaSuccess &&
+         cudaMemcpyAsync(hD + r0 * N * out_elt, dD + r0 * N * out_elt, rows * N * out_elt, cudaMemcpyDeviceToHost,
+                         h->s_out) == cudaSuccess;
+  }
+  ok = ok && cudaEventRecord(ev[1], h->s_out) == cudaSuccess && cudaStreamWaitEvent(s, ev[1], 0) == cudaSuccess;
+  if (!ok) return TST_ERR_CUDA;
+  p->last_stream = s;
+  p->ran = true;
+  p->last_run_host = true;
+  return TST_OK;
+}
+
 tst_status gemm_grouped_work_items(const tst_plan* p, const int32_t* group_rows, int32_t cta,
                                    tst_work_item* items, int64_t cap, int64_t* count) {
   if (p == nullptr || group_rows == nullptr || count == nullptr || (cap > 0 && items == nullptr) || cap < 0)
@@ -1029,6 +1186,15 @@ tst_status gemm_status_query(tst_plan* p, uint32_t* detail) {
   if (p == nullptr) return TST_ERR_INVALID_ARG;
   if (detail) *detail = 0;
   if (p->host_only || p->dev_block == nullptr) return TST_ERR_NO_DEVICE;
+  if (p->last_run_host && p->host_run) {
+    // the panels ran on the panel plans: the first one that recorded something decides
+    for (tst_plan* c : p->host_run->panel_plan) {
+      if (c == nullptr) continue;
+      const tst_status st = gemm_status_query(c, detail);
+      if (st != TST_OK) return st;
+    }
+    return TST_OK;
+  }
   if (!p->ran) return TST_OK;
   if (cudaStreamSynchronize(p->last_stream) != cudaSuccess) return TST_ERR_CUDA;
   unsigned long long tagged = 0;
