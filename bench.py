@@ -874,6 +874,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": world * fl / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "call": e2e_path},
+            "timing": {"mean_ms": ms_mean, "median_ms": statistics.median(head["ms"]), "min_ms": min(head["ms"]),
+                       "max_ms": max(head["ms"]), "steps": len(head["ms"])},
             "gpu_launches": args.steps * int(head["plan"].info.kernels_per_run),
             "clocks": head["clocks"],
             "workloads": extra,

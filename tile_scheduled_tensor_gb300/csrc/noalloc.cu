@@ -162,8 +162,10 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   s.sk_groups = 1;
   s.order = nullptr;
   s.rows = static_cast<int32_t>(M);
+  s.cols = static_cast<int32_t>(N);   // the epilogue stores columns below this bound
   s.bm = tst::kBlockM;
   s.bn = static_cast<int32_t>(bn);
+  s.bk = static_cast<int32_t>(bk);
   if (schedule == TST_STREAMK) {
     s.grid = static_cast<int32_t>(P);
     s.dp_tiles = 0;
