@@ -122,8 +122,8 @@ def grouped_work_items(u: int, P: int, rows, BM: int, Nt: int, kind: int = 0, G:
 # Reading (listed in the design notes): with per-group shapes (M_g, N_g, K_g) each group
 # has its own ceil(M_g / BM) x ceil(N_g / BN) grid and ceil(K_g / BK) k-tiles; the
 # concatenated sequence and the search are as above, with a group's tile count
-# computed from its own shape (the page's "each lane loads one group's shape and
-# computes its tile count").
+# computed from its own shape (on the page each lane of the searching warp reads one
+# group's shape and derives that group's tile count from it).
 
 def shape_tiles(shapes, BM: int, BN: int):
     """Tiles of each group (M_g, N_g, K_g): ceil(M_g / BM) * ceil(N_g / BN) (0 if M_g or N_g is 0)."""
