@@ -167,6 +167,11 @@ __device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const 
   }
 }
 
+// start of this CTA's block in the debug timeline (3 stamps per k-tile slot, 2 per item slot)
+__device__ __forceinline__ int64_t tl_base(const KernelParams& p) {
+  return static_cast<int64_t>(blockIdx.x) * (3 * p.tl_kslots + 2 * p.tl_islots);
+}
+
 // ------------------------------------------------------------------ producer
 template <int BN, int DT, int CG, int KA>
 __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c, uint32_t smem_a, uint32_t smem_b,
@@ -187,6 +192,7 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   int32_t seq = 0;
+  int32_t kseq = 0;   // k-tiles issued by this CTA (timeline slot)
   long long wait_empty = 0;
   // operand cache hints: the operand the mapping's strips re-read longest is kept
   // (evict_last), the other loaded at normal priority
@@ -223,6 +229,8 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
       const long long t0 = p.stats ? clock64() : 0;
       if (!wait_phase<CG>(p, c, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
       if (p.stats) wait_empty += clock64() - t0;
+      if (p.timeline && kseq < p.tl_kslots) p.timeline[tl_base(p) + 3 * kseq] = clock64();
+      ++kseq;
       if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * stage_bytes);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
@@ -318,11 +326,16 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS + issuer * BN);
     const uint32_t idesc = (w.flags & ITEM_NARROW) ? idesc_half : idesc_full;
     for (int32_t i = 0; i < w.k_count; ++i) {
-      const long long t1 = p.stats ? clock64() : 0;
+      const long long t1 = (p.stats || p.timeline) ? clock64() : 0;
       // the stage was filled by TMA and announced on its mbarrier: the wait alone
       // orders the MMA's shared-memory reads after the copy (no tcgen05 fence)
       if (!wait_phase<CG>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
-      if (p.stats) { wait_full += clock64() - t1; ++kblocks; }
+      if (p.stats) wait_full += clock64() - t1;
+      if (p.timeline && issuer == 0 && kblocks < p.tl_kslots) {
+        p.timeline[tl_base(p) + 3 * kblocks + 1] = t1;
+        p.timeline[tl_base(p) + 3 * kblocks + 2] = clock64();
+      }
+      ++kblocks;
       // descriptor start address is in 16-byte units: step to this stage's tiles
       const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
       const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
@@ -448,6 +461,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   long long wait_tfull = 0, busy = 0, items = 0;
+  int32_t tl_items = 0;   // work items finished (timeline slot)
   float amax = 0.0f;  // extended epilogue: this thread's max |Y|
   while (work_next_warp(p.sched, it, w)) {   // every epilogue warp runs the iterator whole
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
@@ -480,8 +494,10 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     ptx::named_bar_sync(1, EP_THREADS);
     if (*ep_ok == 0u) break;
-    const long long t1 = (p.stats && ep == 0) ? clock64() : 0;
+    const long long t1 = ((p.stats || p.timeline) && ep == 0) ? clock64() : 0;
     if (p.stats && ep == 0) wait_tfull += t1 - t0;
+    if (p.timeline && ep == 0 && tl_items < p.tl_islots)
+      p.timeline[tl_base(p) + 3 * p.tl_kslots + 2 * tl_items] = t1;
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
     ptx::tc_fence_after();
 
@@ -601,6 +617,9 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     ptx::named_bar_sync(1, EP_THREADS);
     if (p.stats && ep == 0) { busy += clock64() - t1; ++items; }
+    if (p.timeline && ep == 0 && tl_items < p.tl_islots)
+      p.timeline[tl_base(p) + 3 * p.tl_kslots + 2 * tl_items + 1] = clock64();
+    ++tl_items;
     if (ep == 0) {
       if (CG == 2) ptx::mbar_arrive_cluster(tempty_target + 8 * acc);
       else ptx::mbar_arrive(bar_tempty + 8 * acc);
