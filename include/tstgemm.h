@@ -486,13 +486,24 @@ const char *gemm_status_string(tst_status s);
  *   the accumulator, [3K + 2i + 1] = the epilogue is done with it.  Stamps a
  *   role never takes stay as the caller left them.  One of TRACE, ROLE_CYCLES,
  *   TIMELINE at a time (they share trace_buf); UNSUPPORTED when K >= 2^24.
+ * flags bit 5 (TST_DEBUG_CHECKS): every role checks each work item before using
+ *   it -- tile coordinates inside the grid, the k-range inside K, the group inside
+ *   the groups, rows and columns inside the output -- and skips an item that fails
+ *   (all roles alike), recording TST_ERR_DEVICE_CHECK (role in the status word).
+ *   A skipped Stream-K split leaves the other splits of its tile waiting: they end
+ *   with TST_ERR_TIMEOUT after the plan's timeout, the device check recorded first.
+ * flags bit 6 (TST_DEBUG_FAULT_BAD_ITEM): fault injection for the checks: the
+ *   first work item of unit 0 is moved past the output's columns, which the checks
+ *   catch before any access; INVALID_ARG without TST_DEBUG_CHECKS.
  * The settings stay on the plan until changed; flags = 0 turns them off. */
 enum {
     TST_DEBUG_TRACE = 1,
     TST_DEBUG_FAULT_SKIP_LOAD = 2,
     TST_DEBUG_FAULT_SKIP_LOCK = 4,
     TST_DEBUG_ROLE_CYCLES = 8,
-    TST_DEBUG_TIMELINE = 16
+    TST_DEBUG_TIMELINE = 16,
+    TST_DEBUG_CHECKS = 32,
+    TST_DEBUG_FAULT_BAD_ITEM = 64
 };
 tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, int64_t cap,
                                int64_t timeout_ns);

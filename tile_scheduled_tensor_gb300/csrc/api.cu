@@ -731,6 +731,8 @@ tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int6
   const int buffer_modes = !!(flags & TST_DEBUG_TRACE) + !!(flags & TST_DEBUG_ROLE_CYCLES) +
                            !!(flags & TST_DEBUG_TIMELINE);
   if (buffer_modes > 1) return TST_ERR_INVALID_ARG;
+  // the injected bad item is only ever handed to kernels that check and skip it
+  if ((flags & TST_DEBUG_FAULT_BAD_ITEM) && !(flags & TST_DEBUG_CHECKS)) return TST_ERR_INVALID_ARG;
   // timeline: a slot per k-tile a unit can see (its items times Kt) and per item
   const int64_t tl_k = static_cast<int64_t>(p->max_items) * p->sched.kt, tl_i = p->max_items;
   if (flags & TST_DEBUG_TIMELINE) {

@@ -167,6 +167,44 @@ __device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const 
   }
 }
 
+// Debug checks (DBG_CHECKS): whatever a role may touch for item w lies inside the plan's
+// grid and buffers -- tile coordinates, k-range, group, rows and columns.
+__device__ __forceinline__ bool item_in_bounds(const KernelParams& p, const WorkItem& w) {
+  const Sched& s = p.sched;
+  if (w.k_begin < 0 || w.k_count < 1 || w.m < 0 || w.n < 0 || w.row0 < 0 || w.col0 < 0) return false;
+  if (w.col0 >= w.col_end) return false;
+  if (s.group_shapes != nullptr) {            // groups of different shapes: the group's own GEMM
+    if (w.group < 0 || w.group >= s.groups) return false;
+    const int32_t* g = s.group_shapes + 4 * w.group;
+    return w.row0 < w.row_end && w.row_end <= g[0] && w.col_end <= g[1] && w.k_begin == 0 &&
+           w.k_count == (g[2] + s.bk - 1) / s.bk && w.b_row0 == w.col0;
+  }
+  if (w.col_end != s.cols || w.k_begin + w.k_count > s.kt) return false;
+  if (s.groups > 0)                           // shared N and K: rows of the concatenated A
+    return w.group >= 0 && w.group < s.groups && w.row0 <= w.row_end && w.row_end <= s.rows &&
+           w.b_row0 >= 0 && w.b_row0 < (w.group + 1) * s.group_b_rows;
+  return w.m < s.mt && w.n < s.nt && w.row0 < w.row_end && w.row_end == s.rows && w.b_row0 == w.col0;
+}
+
+// The next work item of a role.  With DBG_CHECKS an item outside the bounds is recorded as a
+// device check and skipped -- by every role alike, the verdict being a function of the item.
+template <bool WARP>
+__device__ __forceinline__ bool next_item(const KernelParams& p, const Ctx& c, WorkIter& it, WorkItem& w,
+                                          int32_t& taken, uint32_t role) {
+  for (;;) {
+    if constexpr (WARP) {
+      if (!work_next_warp(p.sched, it, w)) return false;
+    } else {
+      if (!work_next(p.sched, it, w)) return false;
+    }
+    if (!(p.debug_flags & DBG_CHECKS)) return true;
+    if ((p.debug_flags & DBG_FAULT_BAD_ITEM) && c.unit == 0 && taken == 0) w.col0 = w.col_end;
+    ++taken;
+    if (item_in_bounds(p, w)) return true;
+    record_status(p, ST_DEVICE_CHECK, role);
+  }
+}
+
 // start of this CTA's block in the debug timeline (3 stamps per k-tile slot, 2 per item slot)
 __device__ __forceinline__ int64_t tl_base(const KernelParams& p) {
   return static_cast<int64_t>(blockIdx.x) * (3 * p.tl_kslots + 2 * p.tl_islots);
@@ -203,7 +241,8 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     pol_a = p.l2_hint == 1 ? keep : normal;
     pol_b = p.l2_hint == 1 ? normal : keep;
   }
-  while (ok && work_next(p.sched, it, w)) {
+  int32_t taken = 0;
+  while (ok && next_item<false>(p, c, it, w, taken, ROLE_PRODUCER)) {
     if (p.trace != nullptr && leader && seq < p.max_items) {
       int32_t* rec = p.trace + (static_cast<int64_t>(c.unit) * p.max_items + seq) * 8;
       rec[0] = c.unit; rec[1] = seq; rec[2] = w.tile; rec[3] = w.m;
@@ -317,7 +356,8 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   long long wait_full = 0, wait_tempty = 0, kblocks = 0;
-  while (ok && work_next(p.sched, it, w)) {
+  int32_t taken = 0;
+  while (ok && next_item<false>(p, c, it, w, taken, ROLE_MMA)) {
     // pairs: TMEM_EMPTY counts both CTAs' epilogues
     const long long t0 = p.stats ? clock64() : 0;
     if (!wait_phase<CG>(p, c, bar_tempty + 8 * acc, acc_phase ^ 1u, ROLE_MMA)) { ok = false; break; }
@@ -463,7 +503,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   long long wait_tfull = 0, busy = 0, items = 0;
   int32_t tl_items = 0;   // work items finished (timeline slot)
   float amax = 0.0f;  // extended epilogue: this thread's max |Y|
-  while (work_next_warp(p.sched, it, w)) {   // every epilogue warp runs the iterator whole
+  int32_t taken = 0;
+  while (next_item<true>(p, c, it, w, taken, ROLE_EPILOGUE)) {   // every epilogue warp runs the iterator whole
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
     const bool final_split = (w.flags & ITEM_FINAL) != 0;
     const bool separate = p.sk_mode == SK_SEPARATE;
@@ -730,7 +771,8 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
       WorkIter it;
       WorkItem w;
       work_begin(p.sched, c.unit, it);
-      if (work_next(p.sched, it, w)) {
+      int32_t taken = 0;
+      if (next_item<false>(p, c, it, w, taken, ROLE_PRODUCER)) {
         constexpr int BK = (DT == DT_BF16 ? 64 : 128) * KA;
         const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (BN / CG);
         const int32_t kend = w.k_begin + (w.k_count < p.stages ? w.k_count : p.stages);

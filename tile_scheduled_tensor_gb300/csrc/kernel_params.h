@@ -49,7 +49,11 @@ enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_
 enum SkFixup : int32_t { SK_DETERMINISTIC = 0, SK_ATOMIC = 1, SK_SEPARATE = 2, SK_TMA = 3 };
 constexpr int kStagingBytes = kBlockM * 32 * 4;   // one 128 x 32 FP32 chunk per epilogue warpgroup
 
-enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8, DBG_TIMELINE = 16 };
+enum DebugFlags : int32_t {
+  DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8, DBG_TIMELINE = 16,
+  DBG_CHECKS = 32,          // every role checks each work item's bounds before using it
+  DBG_FAULT_BAD_ITEM = 64   // (with DBG_CHECKS) unit 0's first item is moved past its columns
+};
 
 // Role-cycle counters (debug): kStatSlots uint64 per CTA, in SM clock cycles.
 enum StatSlot : int32_t {
