@@ -664,50 +664,6 @@ def run_role_cycles(args):
         print(json.dumps(row), flush=True)
 
 
-def run_timeline(args):
-    """SM-clock stamps per k-tile and per work item from the kernel's debug timeline:
-    the MMA issuer's k-tile period, how long it waits for a stage, how long after the
-    producer's issue the stage is ready, and the epilogue's time per item (medians over the
-    leader CTAs' steady state, the first and last two k-tiles of each CTA left out)."""
-    import torch
-    import tile_scheduled_tensor_gb300 as tst
-    names = [args.workload] + ([] if args.no_extra else [n for n in EXTRA if n != args.workload])
-    for name in names:
-        w = WORKLOADS[name]
-        inp, plan, host, dev, C = setup_workload(w, tst, torch)
-        info = plan.info
-        K, I = info.max_items_per_cta * info.kt, info.max_items_per_cta
-        S = 3 * K + 2 * I
-        buf = torch.zeros(info.ctas * S, dtype=torch.int64, device="cuda")
-        for _ in range(args.warmup):
-            run_once(tst, plan, dev, C)
-        tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TIMELINE, buf, info.ctas * S * 2)
-        run_once(tst, plan, dev, C)
-        st, word = tst.gemm_status_query(plan)
-        if st != tst.TST_OK:
-            raise RuntimeError(f"{name}: device status {tst.gemm_status_string(st)} {word:#x}")
-        t = buf.view(info.ctas, S).cpu().numpy().astype(np.float64)
-        period, starve, ready, lead, epi = [], [], [], [], []
-        for b in range(0, info.ctas, info.cta_group):    # leader CTAs run the MMA issuer
-            k = t[b, :3 * K].reshape(K, 3)
-            k = k[(k > 0).all(axis=1)]
-            if len(k) > 4:
-                k = k[2:-2]
-                period += list(np.diff(k[:, 2]))
-                starve += list(k[:, 2] - k[:, 1])
-                ready += list(k[:, 2] - k[:, 0])
-                lead += list(k[:, 1] - k[:, 0])
-            it = t[b, 3 * K:].reshape(I, 2)
-            it = it[(it > 0).all(axis=1)]
-            epi += list(it[:, 1] - it[:, 0])
-        med = (lambda x: round(float(np.median(x)), 1) if len(x) else None)
-        row = {"workload": name, "tile": f"{info.bm}x{info.bn}x{info.bk}", "cta_group": int(info.cta_group),
-               "stages": int(info.stages), "ktile_period_cycles": med(period), "mma_wait_per_ktile": med(starve),
-               "issue_to_ready_cycles": med(ready), "producer_lead_cycles": med(lead),
-               "epilogue_cycles_per_item": med(epi), "ktiles_sampled": len(period)}
-        print(json.dumps(row), flush=True)
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -728,9 +684,6 @@ def main():
                     help="time every tile width x CTA group on a set of shapes against the cost model's pick")
     ap.add_argument("--chain-study", action="store_true",
                     help="time chains of dependent GEMMs with and without programmatic dependent launch")
-    ap.add_argument("--timeline", action="store_true",
-                    help="instead of timing, print k-tile and work-item timing medians from the kernel's debug "
-                         "timeline for the listed workloads")
     ap.add_argument("--role-cycles", action="store_true",
                     help="instead of timing, print per-role wait/busy cycle fractions (debug counters) "
                          "for the listed workloads")
@@ -755,8 +708,6 @@ def main():
             "".join(f", {kv}" for kv in args.opt) + "]"
     if args.role_cycles:
         return run_role_cycles(args)
-    if args.timeline:
-        return run_timeline(args)
     if args.chain_study:
         return run_chain_study(args)
     if args.mapping_study:

@@ -476,34 +476,12 @@ const char *gemm_status_string(tst_status s);
  *   free accumulator, epilogue waiting for an accumulator or a Stream-K lock,
  *   epilogue busy, k-tiles issued, work items finished.  Cannot be combined
  *   with TST_DEBUG_TRACE (both use trace_buf).
- * flags bit 4 (TST_DEBUG_TIMELINE): per launched CTA b the kernel writes SM-clock
- *   stamps (uint64, the CTA's own SM clock) to trace_buf (8-byte aligned, `cap` in
- *   int32 units), in a block of S = 3 * K + 2 * I values starting at b * S, with
- *   K = max_items_per_cta * kt and I = max_items_per_cta: for the j-th k-tile
- *   this CTA loads, [3j] = its producer issues the loads (after the stage was
- *   free), [3j + 1] and [3j + 2] = the MMA issuer (leader CTA) starts and ends
- *   waiting for that stage; for the i-th work item, [3K + 2i] = the epilogue has
- *   the accumulator, [3K + 2i + 1] = the epilogue is done with it.  Stamps a
- *   role never takes stay as the caller left them.  One of TRACE, ROLE_CYCLES,
- *   TIMELINE at a time (they share trace_buf); UNSUPPORTED when K >= 2^24.
- * flags bit 5 (TST_DEBUG_CHECKS): every role checks each work item before using
- *   it -- tile coordinates inside the grid, the k-range inside K, the group inside
- *   the groups, rows and columns inside the output -- and skips an item that fails
- *   (all roles alike), recording TST_ERR_DEVICE_CHECK (role in the status word).
- *   A skipped Stream-K split leaves the other splits of its tile waiting: they end
- *   with TST_ERR_TIMEOUT after the plan's timeout, the device check recorded first.
- * flags bit 6 (TST_DEBUG_FAULT_BAD_ITEM): fault injection for the checks: the
- *   first work item of unit 0 is moved past the output's columns, which the checks
- *   catch before any access; INVALID_ARG without TST_DEBUG_CHECKS.
  * The settings stay on the plan until changed; flags = 0 turns them off. */
 enum {
     TST_DEBUG_TRACE = 1,
     TST_DEBUG_FAULT_SKIP_LOAD = 2,
     TST_DEBUG_FAULT_SKIP_LOCK = 4,
-    TST_DEBUG_ROLE_CYCLES = 8,
-    TST_DEBUG_TIMELINE = 16,
-    TST_DEBUG_CHECKS = 32,
-    TST_DEBUG_FAULT_BAD_ITEM = 64
+    TST_DEBUG_ROLE_CYCLES = 8
 };
 tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, int64_t cap,
                                int64_t timeout_ns);

@@ -521,107 +521,3 @@ def test_tma_fixup_staging_in_the_ring(dtype, bk):
     assert tst.gemm_status_query(plan)[0] == tst.TST_OK
     z, _ = oracle.gemm(A, B, dtype)
     assert np.array_equal(host_values(C), z)
-
-
-@pytest.mark.parametrize("cta_group,bn,schedule", [(2, 128, "persistent"), (1, 128, "streamk")])
-def test_debug_timeline_stamps_are_ordered(cta_group, bn, schedule):
-    """The debug timeline: every k-tile the leader's MMA issuer takes was issued by the
-    producer before the wait for it ended, waits end after they begin, stamps of
-    consecutive k-tiles increase, every item's epilogue ends after it starts, and the
-    result is the oracle's (the stamps do not disturb the computation)."""
-    M, N, K = 1024, 768, 2048
-    A = synthetic.bf16_bits(synthetic.draw("int:8", 9100, M * K).reshape(M, K))
-    B = synthetic.bf16_bits(synthetic.draw("int:8", 9200, N * K).reshape(N, K))
-    plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule=schedule, out_dtype="f32",
-                                cta_group=cta_group, bn=bn)
-    info = plan.info
-    Kslots, Islots = info.max_items_per_cta * info.kt, info.max_items_per_cta
-    S = 3 * Kslots + 2 * Islots
-    buf = torch.zeros(info.ctas * S, dtype=torch.int64, device="cuda")
-    with pytest.raises(tst.TstError):       # too small a buffer is refused
-        tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TIMELINE, buf, info.ctas * S * 2 - 1)
-    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_TIMELINE, buf, info.ctas * S * 2)
-    D = torch.full((M, N), float("nan"), device="cuda")
-    tst.gemm_run(plan, device_codes(A), device_codes(B), D)
-    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
-    want, _ = oracle.gemm(A, B, "bf16")
-    assert np.array_equal(host_values(D), want)
-    t = buf.view(info.ctas, S).cpu().numpy()
-    taken = 0
-    for b in range(0, info.ctas, info.cta_group):
-        k = t[b, :3 * Kslots].reshape(Kslots, 3)
-        k = k[k[:, 2] > 0]
-        taken += len(k)
-        assert (k[:, 0] > 0).all() and (k[:, 0] <= k[:, 2]).all() and (k[:, 1] <= k[:, 2]).all()
-        assert (np.diff(k[:, 2]) > 0).all() and (np.diff(k[:, 0]) > 0).all()
-        it = t[b, 3 * Kslots:].reshape(Islots, 2)
-        it = it[it[:, 0] > 0]
-        assert (it[:, 1] >= it[:, 0]).all()
-    # every k-tile of the problem was taken by some leader's MMA issuer
-    assert taken == info.tiles * info.kt
-
-
-@pytest.mark.parametrize("schedule,cta_group,bn", [("persistent", 2, 128), ("static", 1, 256), ("streamk", 1, 128),
-                                                   ("streamk_hybrid", 2, 256), ("hytis", 1, 128)])
-def test_debug_checks_pass_every_real_item(schedule, cta_group, bn):
-    """TST_DEBUG_CHECKS never fires on a plan's own items: the run is OK and exact."""
-    M, N, K = 1100, 1000, 1536
-    A = synthetic.bf16_bits(synthetic.draw("int:8", 9300, M * K).reshape(M, K))
-    B = synthetic.bf16_bits(synthetic.draw("int:8", 9400, N * K).reshape(N, K))
-    plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule=schedule, out_dtype="f32",
-                                cta_group=cta_group, bn=bn)
-    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_CHECKS, None, 0)
-    D = torch.full((M, N), float("nan"), device="cuda")
-    tst.gemm_run(plan, device_codes(A), device_codes(B), D)
-    st, word = tst.gemm_status_query(plan)
-    assert st == tst.TST_OK, hex(word)
-    want, _ = oracle.gemm(A, B, "bf16")
-    assert np.array_equal(host_values(D), want)
-
-
-def test_debug_checks_catch_an_injected_bad_item():
-    """The injected item (unit 0's first, moved past the output's columns) is caught by
-    every role before any access: the run reports a device check, exactly that tile is
-    left unwritten, and every other element is the oracle's."""
-    M, N, K = 1024, 1024, 1024
-    A = synthetic.bf16_bits(synthetic.draw("int:8", 9500, M * K).reshape(M, K))
-    B = synthetic.bf16_bits(synthetic.draw("int:8", 9600, N * K).reshape(N, K))
-    plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent", out_dtype="f32",
-                                cta_group=2, bn=128)
-    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_CHECKS | tst.TST_DEBUG_FAULT_BAD_ITEM, None, 0)
-    D = torch.full((M, N), float("nan"), device="cuda")
-    tst.gemm_run(plan, device_codes(A), device_codes(B), D)
-    st, word = tst.gemm_status_query(plan)
-    assert st == tst.TST_ERR_DEVICE_CHECK, hex(word)
-    got = host_values(D)
-    _, m, n, _, _, _ = tst.gemm_work_items(plan, 0)[0]
-    bm, bnn = plan.info.bm, plan.info.bn
-    skipped = np.zeros((M, N), dtype=bool)
-    skipped[m * bm:(m + 1) * bm, n * bnn:(n + 1) * bnn] = True
-    assert np.isnan(got[skipped]).all()
-    want, _ = oracle.gemm(A, B, "bf16")
-    assert np.array_equal(got[~skipped], want[~skipped])
-    tst.gemm_plan_set_debug(plan, 0, None, 0)
-    tst.gemm_run(plan, device_codes(A), device_codes(B), D)
-    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
-    assert np.array_equal(host_values(D), want)
-
-
-def test_debug_checks_pass_grouped_items():
-    G, N, K = 4, 520, 512
-    rows = [300, 0, 513, 129]
-    M = sum(rows)
-    A = synthetic.bf16_bits(synthetic.draw("int:8", 9700, M * K).reshape(M, K))
-    B = synthetic.bf16_bits(synthetic.draw("int:8", 9800, G * N * K).reshape(G * N, K))
-    plan = tst.gemm_grouped_plan_create(G, M, N, K, out_dtype="f32", cta_group=2, bn=256)
-    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_CHECKS, None, 0)
-    D = torch.full((M, N), float("nan"), device="cuda")
-    tst.gemm_grouped_run(plan, torch.tensor(rows, dtype=torch.int32, device="cuda"), device_codes(A),
-                         device_codes(B), D)
-    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
-    edges = np.cumsum([0] + rows)
-    got = host_values(D)
-    for g in range(G):
-        if rows[g]:
-            z, _ = oracle.gemm(A[edges[g]:edges[g + 1]], B[g * N:(g + 1) * N], "bf16")
-            assert np.array_equal(got[edges[g]:edges[g + 1]], z), g

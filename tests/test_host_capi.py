@@ -361,11 +361,3 @@ def test_run_host_argument_errors():
         tst.TST_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         tst.gemm_run_host(plan, A, B, [1], stream=0)
-
-
-def test_injected_bad_item_needs_the_checks():
-    plan = tst.gemm_plan_create(512, 512, 512, host_only=True, num_sms=152)
-    with pytest.raises(tst.TstError) as e:
-        tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_BAD_ITEM, None, 0)
-    assert e.value.status == tst.TST_ERR_INVALID_ARG
-    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_CHECKS | tst.TST_DEBUG_FAULT_BAD_ITEM, None, 0)

@@ -18,7 +18,6 @@ from ._capi import (TST_BF16, TST_E4M3, TST_E5M2, TST_E4M3_E5M2, TST_E5M2_E4M3, 
                     TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N,
                     TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID, TST_HYTIS,
                     TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG_ROLE_CYCLES,
-                    TST_DEBUG_TIMELINE, TST_DEBUG_CHECKS, TST_DEBUG_FAULT_BAD_ITEM,
                     TST_SK_DETERMINISTIC, TST_SK_ATOMIC, TST_SK_SEPARATE,
                     TST_OK, TST_ERR_INVALID_ARG, TST_ERR_UNSUPPORTED, TST_ERR_ALIGNMENT, TST_ERR_OOM,
                     TST_ERR_CUDA, TST_ERR_TIMEOUT, TST_ERR_DEVICE_CHECK, TST_ERR_NO_DEVICE,

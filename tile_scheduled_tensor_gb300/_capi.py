@@ -27,7 +27,6 @@ TST_MAP_LINEAR_NFAST, TST_MAP_LINEAR_MFAST, TST_MAP_GROUPED_M, TST_MAP_GROUPED_N
 TST_MAP_BLOCK_2D, TST_MAP_MORTON = 4, 5
 TST_STATIC, TST_PERSISTENT, TST_STREAMK, TST_STREAMK_HYBRID, TST_HYTIS = 0, 1, 2, 3, 4
 TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG_ROLE_CYCLES = 1, 2, 4, 8
-TST_DEBUG_TIMELINE, TST_DEBUG_CHECKS, TST_DEBUG_FAULT_BAD_ITEM = 16, 32, 64
 TST_SK_DETERMINISTIC, TST_SK_ATOMIC, TST_SK_SEPARATE, TST_SK_TMA = 0, 1, 2, 3
 TST_L2_NONE, TST_L2_KEEP_A, TST_L2_KEEP_B, TST_L2_AUTO = 0, 1, 2, 3
 TST_BOXES_AUTO, TST_BOXES_2D, TST_BOXES_3D = 0, 1, 2

@@ -86,8 +86,6 @@ struct tst_plan {
   int32_t debug_flags = 0;
   int32_t* trace = nullptr;
   unsigned long long* stats = nullptr;
-  unsigned long long* timeline = nullptr;
-  int32_t tl_kslots = 0, tl_islots = 0;
   int64_t trace_cap = 0;
   uint64_t timeout_ns = 10ull * 1000 * 1000 * 1000;
   // launch
@@ -727,19 +725,7 @@ tst_status gemm_work_items(const tst_plan* p, int32_t cta, tst_work_item* items,
 
 tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int64_t cap, int64_t timeout_ns) {
   if (p == nullptr || cap < 0 || timeout_ns < 0) return TST_ERR_INVALID_ARG;
-  // the trace, the role-cycle counters and the timeline share trace_buf: one at a time
-  const int buffer_modes = !!(flags & TST_DEBUG_TRACE) + !!(flags & TST_DEBUG_ROLE_CYCLES) +
-                           !!(flags & TST_DEBUG_TIMELINE);
-  if (buffer_modes > 1) return TST_ERR_INVALID_ARG;
-  // the injected bad item is only ever handed to kernels that check and skip it
-  if ((flags & TST_DEBUG_FAULT_BAD_ITEM) && !(flags & TST_DEBUG_CHECKS)) return TST_ERR_INVALID_ARG;
-  // timeline: a slot per k-tile a unit can see (its items times Kt) and per item
-  const int64_t tl_k = static_cast<int64_t>(p->max_items) * p->sched.kt, tl_i = p->max_items;
-  if (flags & TST_DEBUG_TIMELINE) {
-    if (tl_k >= (int64_t(1) << 24)) return TST_ERR_UNSUPPORTED;
-    const int64_t need = static_cast<int64_t>(p->sched.grid) * p->cg * (3 * tl_k + 2 * tl_i) * 2;  // int32 units
-    if (trace_buf == nullptr || cap < need || (reinterpret_cast<uintptr_t>(trace_buf) & 7u)) return TST_ERR_INVALID_ARG;
-  }
+  if ((flags & TST_DEBUG_TRACE) && (flags & TST_DEBUG_ROLE_CYCLES)) return TST_ERR_INVALID_ARG;
   if (flags & TST_DEBUG_TRACE) {
     const int64_t need = static_cast<int64_t>(p->sched.grid) * p->max_items * 8;
     if (trace_buf == nullptr || cap < need) return TST_ERR_INVALID_ARG;
@@ -751,9 +737,6 @@ tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int6
   p->debug_flags = flags;
   p->trace = (flags & TST_DEBUG_TRACE) ? static_cast<int32_t*>(trace_buf) : nullptr;
   p->stats = (flags & TST_DEBUG_ROLE_CYCLES) ? static_cast<unsigned long long*>(trace_buf) : nullptr;
-  p->timeline = (flags & TST_DEBUG_TIMELINE) ? static_cast<unsigned long long*>(trace_buf) : nullptr;
-  p->tl_kslots = p->timeline ? static_cast<int32_t>(tl_k) : 0;
-  p->tl_islots = p->timeline ? static_cast<int32_t>(tl_i) : 0;
   p->trace_cap = cap;
   if (timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(timeout_ns);
   else if (p->opts.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(p->opts.timeout_ns);
@@ -834,9 +817,6 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.status = p->d_status;
   kp.trace = p->trace;
   kp.stats = p->stats;
-  kp.timeline = p->timeline;
-  kp.tl_kslots = p->tl_kslots;
-  kp.tl_islots = p->tl_islots;
   kp.M = static_cast<int32_t>(p->M);
   kp.N = static_cast<int32_t>(p->N);
   kp.K = static_cast<int32_t>(p->K);

@@ -167,49 +167,6 @@ __device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const 
   }
 }
 
-// Debug checks (DBG_CHECKS): whatever a role may touch for item w lies inside the plan's
-// grid and buffers -- tile coordinates, k-range, group, rows and columns.
-__device__ __forceinline__ bool item_in_bounds(const KernelParams& p, const WorkItem& w) {
-  const Sched& s = p.sched;
-  if (w.k_begin < 0 || w.k_count < 1 || w.m < 0 || w.n < 0 || w.row0 < 0 || w.col0 < 0) return false;
-  if (w.col0 >= w.col_end) return false;
-  if (s.group_shapes != nullptr) {            // groups of different shapes: the group's own GEMM
-    if (w.group < 0 || w.group >= s.groups) return false;
-    const int32_t* g = s.group_shapes + 4 * w.group;
-    return w.row0 < w.row_end && w.row_end <= g[0] && w.col_end <= g[1] && w.k_begin == 0 &&
-           w.k_count == (g[2] + s.bk - 1) / s.bk && w.b_row0 == w.col0;
-  }
-  if (w.col_end != s.cols || w.k_begin + w.k_count > s.kt) return false;
-  if (s.groups > 0)                           // shared N and K: rows of the concatenated A
-    return w.group >= 0 && w.group < s.groups && w.row0 <= w.row_end && w.row_end <= s.rows &&
-           w.b_row0 >= 0 && w.b_row0 < (w.group + 1) * s.group_b_rows;
-  return w.m < s.mt && w.n < s.nt && w.row0 < w.row_end && w.row_end == s.rows && w.b_row0 == w.col0;
-}
-
-// The next work item of a role.  With DBG_CHECKS an item outside the bounds is recorded as a
-// device check and skipped -- by every role alike, the verdict being a function of the item.
-template <bool WARP>
-__device__ __forceinline__ bool next_item(const KernelParams& p, const Ctx& c, WorkIter& it, WorkItem& w,
-                                          int32_t& taken, uint32_t role) {
-  for (;;) {
-    if constexpr (WARP) {
-      if (!work_next_warp(p.sched, it, w)) return false;
-    } else {
-      if (!work_next(p.sched, it, w)) return false;
-    }
-    if (!(p.debug_flags & DBG_CHECKS)) return true;
-    if ((p.debug_flags & DBG_FAULT_BAD_ITEM) && c.unit == 0 && taken == 0) w.col0 = w.col_end;
-    ++taken;
-    if (item_in_bounds(p, w)) return true;
-    record_status(p, ST_DEVICE_CHECK, role);
-  }
-}
-
-// start of this CTA's block in the debug timeline (3 stamps per k-tile slot, 2 per item slot)
-__device__ __forceinline__ int64_t tl_base(const KernelParams& p) {
-  return static_cast<int64_t>(blockIdx.x) * (3 * p.tl_kslots + 2 * p.tl_islots);
-}
-
 // ------------------------------------------------------------------ producer
 template <int BN, int DT, int CG, int KA>
 __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c, uint32_t smem_a, uint32_t smem_b,
@@ -230,7 +187,6 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   int32_t seq = 0;
-  int32_t kseq = 0;   // k-tiles issued by this CTA (timeline slot)
   long long wait_empty = 0;
   // operand cache hints: the operand the mapping's strips re-read longest is kept
   // (evict_last), the other loaded at normal priority
@@ -241,8 +197,7 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     pol_a = p.l2_hint == 1 ? keep : normal;
     pol_b = p.l2_hint == 1 ? normal : keep;
   }
-  int32_t taken = 0;
-  while (ok && next_item<false>(p, c, it, w, taken, ROLE_PRODUCER)) {
+  while (ok && work_next(p.sched, it, w)) {
     if (p.trace != nullptr && leader && seq < p.max_items) {
       int32_t* rec = p.trace + (static_cast<int64_t>(c.unit) * p.max_items + seq) * 8;
       rec[0] = c.unit; rec[1] = seq; rec[2] = w.tile; rec[3] = w.m;
@@ -268,8 +223,6 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
       const long long t0 = p.stats ? clock64() : 0;
       if (!wait_phase<CG>(p, c, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
       if (p.stats) wait_empty += clock64() - t0;
-      if (p.timeline && kseq < p.tl_kslots) p.timeline[tl_base(p) + 3 * kseq] = clock64();
-      ++kseq;
       if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * stage_bytes);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
@@ -356,8 +309,7 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   long long wait_full = 0, wait_tempty = 0, kblocks = 0;
-  int32_t taken = 0;
-  while (ok && next_item<false>(p, c, it, w, taken, ROLE_MMA)) {
+  while (ok && work_next(p.sched, it, w)) {
     // pairs: TMEM_EMPTY counts both CTAs' epilogues
     const long long t0 = p.stats ? clock64() : 0;
     if (!wait_phase<CG>(p, c, bar_tempty + 8 * acc, acc_phase ^ 1u, ROLE_MMA)) { ok = false; break; }
@@ -366,16 +318,11 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS + issuer * BN);
     const uint32_t idesc = (w.flags & ITEM_NARROW) ? idesc_half : idesc_full;
     for (int32_t i = 0; i < w.k_count; ++i) {
-      const long long t1 = (p.stats || p.timeline) ? clock64() : 0;
+      const long long t1 = p.stats ? clock64() : 0;
       // the stage was filled by TMA and announced on its mbarrier: the wait alone
       // orders the MMA's shared-memory reads after the copy (no tcgen05 fence)
       if (!wait_phase<CG>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
-      if (p.stats) wait_full += clock64() - t1;
-      if (p.timeline && issuer == 0 && kblocks < p.tl_kslots) {
-        p.timeline[tl_base(p) + 3 * kblocks + 1] = t1;
-        p.timeline[tl_base(p) + 3 * kblocks + 2] = clock64();
-      }
-      ++kblocks;
+      if (p.stats) { wait_full += clock64() - t1; ++kblocks; }
       // descriptor start address is in 16-byte units: step to this stage's tiles
       const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
       const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
@@ -501,10 +448,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   work_begin(p.sched, c.unit, it);
   WorkItem w;
   long long wait_tfull = 0, busy = 0, items = 0;
-  int32_t tl_items = 0;   // work items finished (timeline slot)
   float amax = 0.0f;  // extended epilogue: this thread's max |Y|
-  int32_t taken = 0;
-  while (next_item<true>(p, c, it, w, taken, ROLE_EPILOGUE)) {   // every epilogue warp runs the iterator whole
+  while (work_next_warp(p.sched, it, w)) {   // every epilogue warp runs the iterator whole
     const bool fixup = (w.flags & ITEM_FIXUP) != 0;
     const bool final_split = (w.flags & ITEM_FINAL) != 0;
     const bool separate = p.sk_mode == SK_SEPARATE;
@@ -535,10 +480,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     ptx::named_bar_sync(1, EP_THREADS);
     if (*ep_ok == 0u) break;
-    const long long t1 = ((p.stats || p.timeline) && ep == 0) ? clock64() : 0;
+    const long long t1 = (p.stats && ep == 0) ? clock64() : 0;
     if (p.stats && ep == 0) wait_tfull += t1 - t0;
-    if (p.timeline && ep == 0 && tl_items < p.tl_islots)
-      p.timeline[tl_base(p) + 3 * p.tl_kslots + 2 * tl_items] = t1;
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
     ptx::tc_fence_after();
 
@@ -658,9 +601,6 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     }
     ptx::named_bar_sync(1, EP_THREADS);
     if (p.stats && ep == 0) { busy += clock64() - t1; ++items; }
-    if (p.timeline && ep == 0 && tl_items < p.tl_islots)
-      p.timeline[tl_base(p) + 3 * p.tl_kslots + 2 * tl_items + 1] = clock64();
-    ++tl_items;
     if (ep == 0) {
       if (CG == 2) ptx::mbar_arrive_cluster(tempty_target + 8 * acc);
       else ptx::mbar_arrive(bar_tempty + 8 * acc);
@@ -771,8 +711,7 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
       WorkIter it;
       WorkItem w;
       work_begin(p.sched, c.unit, it);
-      int32_t taken = 0;
-      if (next_item<false>(p, c, it, w, taken, ROLE_PRODUCER)) {
+      if (work_next(p.sched, it, w)) {
         constexpr int BK = (DT == DT_BF16 ? 64 : 128) * KA;
         const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (BN / CG);
         const int32_t kend = w.k_begin + (w.k_count < p.stages ? w.k_count : p.stages);

@@ -49,11 +49,7 @@ enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_
 enum SkFixup : int32_t { SK_DETERMINISTIC = 0, SK_ATOMIC = 1, SK_SEPARATE = 2, SK_TMA = 3 };
 constexpr int kStagingBytes = kBlockM * 32 * 4;   // one 128 x 32 FP32 chunk per epilogue warpgroup
 
-enum DebugFlags : int32_t {
-  DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8, DBG_TIMELINE = 16,
-  DBG_CHECKS = 32,          // every role checks each work item's bounds before using it
-  DBG_FAULT_BAD_ITEM = 64   // (with DBG_CHECKS) unit 0's first item is moved past its columns
-};
+enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8 };
 
 // Role-cycle counters (debug): kStatSlots uint64 per CTA, in SM clock cycles.
 enum StatSlot : int32_t {
@@ -83,11 +79,6 @@ struct KernelParams {
   unsigned long long* status;  // device status word: (run_id << 32) | code | role << 8 | CTA << 16
   int32_t* trace;           // debug trace or null
   unsigned long long* stats;  // debug role-cycle counters (kStatSlots per CTA) or null
-  // debug timeline or null: per CTA, SM-clock stamps of tl_kslots k-tiles (producer issue,
-  // MMA wait begin, MMA wait end) and tl_islots work items (epilogue has the accumulator,
-  // epilogue done); stamps past the slots are dropped
-  unsigned long long* timeline;
-  int32_t tl_kslots, tl_islots;
   int32_t M, N, K;
   float alpha;
   Sched sched;
