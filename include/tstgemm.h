@@ -52,7 +52,7 @@ extern "C" {
 typedef enum {
     TST_OK = 0,
     TST_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum value */
-    TST_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement */
+    TST_ERR_UNSUPPORTED = 2,   /* a valid request the library does not implement */
     TST_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned or K * elt not a multiple of 16 */
     TST_ERR_OOM = 4,           /* device allocation for the plan's workspace failed */
     TST_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
