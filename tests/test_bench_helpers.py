@@ -1,0 +1,51 @@
+"""Host-side helpers of the benchmark for workloads over groups of different shapes: the
+seeded shapes, the FLOP counts (whole and per output row) and the oracle step, checked on
+small shapes against direct oracle calls."""
+import numpy as np
+
+import bench
+import oracle
+import synthetic
+
+
+def test_group_shapes_are_seeded_and_in_range():
+    a = synthetic.make_group_shapes(12, 8)
+    assert a == synthetic.make_group_shapes(12, 8)
+    assert a != synthetic.make_group_shapes(12, 9)
+    for m, n, k in a:
+        assert 256 <= m <= 4096 and m % 8 == 0
+        assert n in (1024, 2048, 4096, 8192) and k in (1024, 2048, 4096, 8192)
+
+
+def _small_workload():
+    return dict(M=0, N=0, K=0, dtype="bf16", dist="int:8", case=3, out="f32", mapping=("grouped_m", 2),
+                schedule="persistent", bn=128, cta_group=1, shape_groups=3)
+
+
+def test_flops_add_up_over_rows(monkeypatch):
+    shapes = [(24, 40, 64), (8, 16, 32), (16, 8, 128)]
+    monkeypatch.setattr(bench, "make_group_shapes", lambda g, c: shapes)
+    w = _small_workload()
+    assert bench.total_rows(w) == 48
+    assert bench.flops(w) == sum(2.0 * m * n * k for m, n, k in shapes)
+    assert bench.row_flops(w, np.arange(48)) == bench.flops(w)
+    # row 23 is group 0's last, rows 24 and 31 are group 1's first and last, row 32 group 2's first
+    assert bench.row_flops(w, np.array([23, 24, 31, 32])) == 2 * (40 * 64) + 2 * 2 * (16 * 32) + 2 * (8 * 128)
+    plain = dict(M=10, N=20, K=30)
+    assert bench.flops(plain) == 2.0 * 10 * 20 * 30 and bench.row_flops(plain, [1, 2]) == 2.0 * 2 * 20 * 30
+
+
+def test_oracle_step_numbers_rows_group_after_group(monkeypatch):
+    shapes = [(24, 40, 64), (8, 16, 32), (16, 8, 128)]
+    monkeypatch.setattr(bench, "make_group_shapes", lambda g, c: shapes)
+    w = _small_workload()
+    inp = bench.make_inputs_for(w)
+    assert [(x.M, x.N, x.K) for x in inp] == shapes
+    rows = np.array([0, 23, 24, 31, 32, 47])
+    out = bench.oracle_step(w, inp, rows)
+    # one (z, absdot) pair per group touched, in group order, rows local to the group
+    want_groups = [(0, [0, 23]), (1, [0, 7]), (2, [0, 15])]
+    assert len(out) == len(want_groups)
+    for (z, _), (g, local) in zip(out, want_groups):
+        zz, _ = oracle.gemm(inp[g].A, inp[g].B, "bf16", rows=np.array(local))
+        assert np.array_equal(z, zz)
