@@ -90,3 +90,23 @@ def test_run_host_refuses_grouped_plans():
         tst.gemm_run_host(plan, torch.zeros(256, 128, dtype=torch.bfloat16),
                           torch.zeros(256, 128, dtype=torch.bfloat16), torch.zeros(256, 128, dtype=torch.bfloat16))
     assert e.value.status == tst.TST_ERR_UNSUPPORTED
+
+
+def test_run_host_panel_counts_change_between_calls():
+    """One plan, the panel count changing from call to call (the cached plans of the
+    panel heights are replaced without freeing one a call still uses): every call equals
+    the device run."""
+    M, N, K = 1300, 520, 1024
+    A = synthetic.bf16_bits(synthetic.draw("int:8", 8150, M * K).reshape(M, K))
+    B = synthetic.bf16_bits(synthetic.draw("int:8", 8250, N * K).reshape(N, K))
+    plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent", out_dtype="f32",
+                                cta_group=2, bn=128)
+    Dd = torch.empty(M, N, device="cuda")
+    tst.gemm_run(plan, device_codes(A), device_codes(B), Dd)
+    want = Dd.cpu()
+    Ah, Bh = _host(A), _host(B)
+    for panels in (8, 3, 5, 3, 0, 1, 6, 2):
+        Dh = torch.full((M, N), float("nan")).pin_memory()
+        tst.gemm_run_host(plan, Ah, Bh, Dh, panels=panels)
+        assert tst.gemm_status_query(plan)[0] == tst.TST_OK, panels
+        assert torch.equal(Dh, want), panels

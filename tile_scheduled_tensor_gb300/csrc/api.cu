@@ -1077,18 +1077,21 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
     if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return TST_ERR_CUDA;
     h->events.push_back(ev);
   }
+  // the panels have at most two heights, R and the last panel's; plans cached for other
+  // heights (an earlier call with another panel count) are freed before any is created, so
+  // no plan this call uses is ever freed by it
+  const int64_t last_rows = M - (P - 1) * R;
+  for (int i = 0; i < 2; ++i)
+    if (h->panel_plan[i] && h->panel_rows[i] != R && h->panel_rows[i] != last_rows) {
+      gemm_plan_destroy(h->panel_plan[i]);   // (cudaFree inside waits for its earlier work)
+      h->panel_plan[i] = nullptr;
+      h->panel_rows[i] = 0;
+    }
   // the plan of a panel height: the parent's tile, CTA group, k-tile and options
   auto panel_plan = [&](int64_t rows, tst_plan** out) -> tst_status {
     for (int i = 0; i < 2; ++i)
       if (h->panel_plan[i] && h->panel_rows[i] == rows) { *out = h->panel_plan[i]; return TST_OK; }
-    int slot = h->panel_plan[0] == nullptr ? 0 : h->panel_plan[1] == nullptr ? 1 : -1;
-    if (slot < 0) {   // another panel count than before: start over
-      for (int i = 0; i < 2; ++i) {
-        gemm_plan_destroy(h->panel_plan[i]);
-        h->panel_plan[i] = nullptr;
-      }
-      slot = 0;
-    }
+    const int slot = h->panel_plan[0] == nullptr ? 0 : 1;   // a free slot exists (see above)
     tst_plan_options o = p->opts;
     o.bn = p->bn;
     o.cta_group = p->cg;
@@ -1115,8 +1118,10 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // every panel plan exists before anything is enqueued
   tst_plan* plans[kMaxHostPanels];
   for (int64_t q = 0; q < P; ++q) {
-    const tst_status st = panel_plan(std::min(R, M - q * R), &plans[q]);
+    const int64_t rows = std::min(R, M - q * R);
+    const tst_status st = panel_plan(rows, &plans[q]);
     if (st != TST_OK) return st;
+    if (plans[q] == nullptr || plans[q]->M != rows || plans[q]->N != N || plans[q]->K != K) return TST_ERR_CUDA;
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream_);
