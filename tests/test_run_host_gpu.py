@@ -96,7 +96,7 @@ def test_run_host_panel_counts_change_between_calls():
     """One plan, the panel count changing from call to call (the cached plans of the
     panel heights are replaced without freeing one a call still uses): every call equals
     the device run."""
-    M, N, K = 1300, 520, 1024
+    M, N, K = 1736, 520, 1024      # last panels of 200 rows or more for every count below
     A = synthetic.bf16_bits(synthetic.draw("int:8", 8150, M * K).reshape(M, K))
     B = synthetic.bf16_bits(synthetic.draw("int:8", 8250, N * K).reshape(N, K))
     plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent", out_dtype="f32",
