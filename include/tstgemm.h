@@ -337,7 +337,8 @@ tst_status gemm_run_epi(tst_plan *plan, const void *A, const void *B, void *D,
  * NULL when the plan's epilogue needs none).  No counterpart on the pages: the
  * host-level analogue of the kernel's overlap of loads with MMAs.  The call copies
  * B to a plan-owned device buffer, then A in row panels (a whole number of
- * scheduled tile rows each, `panels` of them, 0 = about 8, at most 64); each
+ * scheduled tile rows each, `panels` of them, 0 = about 8, at most 64; a last
+ * panel shorter than half the others joins the one before it); each
  * panel's GEMM runs on `stream` as soon as its rows have landed, and its rows of D
  * are copied back while later panels are still arriving.  Two plan-owned copy
  * streams carry the transfers, ordered after earlier work on `stream`, and

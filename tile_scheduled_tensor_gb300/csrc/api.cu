@@ -1050,7 +1050,10 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // 16-byte alignment of its base); default about M / 8
   const int64_t want = panels == 0 ? kDefaultHostPanels : panels;
   const int64_t R = std::max<int64_t>(ceil_div(ceil_div(M, want), p->bm) * p->bm, p->bm);
-  const int64_t P = ceil_div(M, R);
+  int64_t P = ceil_div(M, R);
+  // a last panel shorter than half a panel joins the one before it (a GEMM of a few rows
+  // costs nearly a full panel's time); the panels keep at most two heights
+  if (P > 1 && M - (P - 1) * R < R / 2) --P;
 
   HostRun* h = p->host_run;
   if (h == nullptr) {
@@ -1080,7 +1083,8 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // the panels have at most two heights, R and the last panel's; plans cached for other
   // heights (an earlier call with another panel count) are freed before any is created, so
   // no plan this call uses is ever freed by it
-  const int64_t last_rows = M - (P - 1) * R;
+  const int64_t last_rows = M - (P - 1) * R;   // up to R, or up to 1.5 R after a merge
+  auto rows_of = [&](int64_t q) { return q + 1 < P ? R : last_rows; };
   for (int i = 0; i < 2; ++i)
     if (h->panel_plan[i] && h->panel_rows[i] != R && h->panel_rows[i] != last_rows) {
       gemm_plan_destroy(h->panel_plan[i]);   // (cudaFree inside waits for its earlier work)
@@ -1118,7 +1122,7 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // every panel plan exists before anything is enqueued
   tst_plan* plans[kMaxHostPanels];
   for (int64_t q = 0; q < P; ++q) {
-    const int64_t rows = std::min(R, M - q * R);
+    const int64_t rows = rows_of(q);
     const tst_status st = panel_plan(rows, &plans[q]);
     if (st != TST_OK) return st;
     if (plans[q] == nullptr || plans[q]->M != rows || plans[q]->N != N || plans[q]->K != K) return TST_ERR_CUDA;
@@ -1134,7 +1138,7 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // inputs: B whole, then A panel by panel
   ok = ok && cudaMemcpyAsync(h->dB, B, N * K * elt, cudaMemcpyHostToDevice, h->s_in) == cudaSuccess;
   for (int64_t q = 0; ok && q < P; ++q) {
-    const int64_t r0 = q * R, rows = std::min(R, M - r0);
+    const int64_t r0 = q * R, rows = rows_of(q);
     ok = cudaMemcpyAsync(dA + r0 * K * elt, hA + r0 * K * elt, rows * K * elt, cudaMemcpyHostToDevice, h->s_in) ==
              cudaSuccess &&
          cudaEventRecord(ev[2 + q], h->s_in) == cudaSuccess;
@@ -1152,7 +1156,7 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // outputs: each panel's D as soon as its GEMM is done
   char* hD = static_cast<char*>(D);
   for (int64_t q = 0; ok && q < P; ++q) {
-    const int64_t r0 = q * R, rows = std::min(R, M - r0);
+    const int64_t r0 = q * R, rows = rows_of(q);
     ok = cudaStreamWaitEvent(h->s_out, ev[2 + P + q], 0) == cudaSuccess &&
          cudaMemcpyAsync(hD + r0 * N * out_elt, dD + r0 * N * out_elt, rows * N * out_elt, cudaMemcpyDeviceToHost,
                          h->s_out) == cudaSuccess;
