@@ -188,6 +188,36 @@ def apply(acc: np.ndarray, absdot: np.ndarray, e: Epilogue, rows=None):
     return Z, Y, D_pre, np.abs(scale) * np.asarray(absdot, dtype=np.float64)
 
 
+# ------------------------------------------------- block scale factor generation
+#
+# "H100 . Kernel Design" section 12.1 lists block scale factor generation among the
+# epilogue operations, and "H100 . WGMMA Part 2" section 11 describes block-wise scaling
+# (MXFP8, microscaling): the matrix is cut into small tiles (its examples: 16 x 16 or
+# 32 x 32), one scale per tile.  Reading (listed in the design notes): the output Y is cut
+# into br x bc tiles (32 x 32 by default, ragged at the edges); each tile gets a
+# power-of-two scale X = 2^E, E = floor(log2(amax)) - 8 with amax = max |Y| over the tile
+# (8 = the exponent of e4m3's largest power of two, as the microscaling format derives its
+# shared exponent), E = 0 for an all-zero tile; the tile's codes are e4m3(Y / X), rounded
+# to nearest even and saturated to +-448.  X is exact, so Y / X is too.
+
+def block_scale_e4m3(Y: np.ndarray, block=(32, 32)):
+    """(codes, E): e4m3 codes of Y (its shape) and the int exponents E of each tile's
+    scale 2^E, shape (ceil(rows / br), ceil(cols / bc))."""
+    Y = np.asarray(Y, dtype=np.float64)
+    br, bc = block
+    R, C = Y.shape
+    E = np.zeros((-(-R // br), -(-C // bc)), dtype=np.int64)
+    codes = np.zeros(Y.shape, dtype=np.uint8)
+    for i in range(E.shape[0]):
+        for j in range(E.shape[1]):
+            t = Y[i * br:(i + 1) * br, j * bc:(j + 1) * bc]
+            m = float(np.max(np.abs(t)))
+            e = math.floor(math.log2(m)) - 8 if m > 0 else 0
+            E[i, j] = e
+            codes[i * br:(i + 1) * br, j * bc:(j + 1) * bc] = encode_e4m3(t / 2.0 ** e)
+    return codes, E
+
+
 def amax(Y: np.ndarray) -> float:
     """max |Y| over the output (0 for an empty output)."""
     return float(np.max(np.abs(Y))) if np.size(Y) else 0.0

@@ -200,3 +200,64 @@ def test_rows_selection_matches_full():
 def test_amax():
     assert E.amax(np.zeros((0, 4))) == 0.0
     assert E.amax(np.array([[-3.0, 2.0], [1.0, 0.5]])) == 3.0
+
+
+# ------------------------------------------------- block scale factor generation
+
+E_ = E   # the module (E names the tiles' exponents below)
+
+def test_block_scales_hand_worked():
+    # one 2 x 2 tile: amax 300 -> E = floor(log2 300) - 8 = 0, X = 1; 300 lies between
+    # the e4m3 values 288 and 320 and rounds to 288; -1, 0.5 and 2 are exact
+    codes, E = E_.block_scale_e4m3(np.array([[300.0, -1.0], [0.5, 2.0]]), block=(2, 2))
+    assert E.tolist() == [[0]]
+    assert E_.decode_e4m3(codes).tolist() == [[288.0, -1.0], [0.5, 2.0]]
+    # amax 1000 -> E = 9 - 8 = 1, X = 2: 1000 / 2 = 500 saturates to 448; 3 / 2 = 1.5 exact
+    codes, E = E_.block_scale_e4m3(np.array([[1000.0, 3.0]]), block=(1, 2))
+    assert E.tolist() == [[1]] and E_.decode_e4m3(codes).tolist() == [[448.0, 1.5]]
+    # tiny values: amax 0.01 -> floor(log2 0.01) = -7, E = -15, X = 2^-15; 0.01 * 2^15 = 327.68 -> 320
+    codes, E = E_.block_scale_e4m3(np.array([[0.01]]), block=(1, 1))
+    assert E.tolist() == [[-15]] and E_.decode_e4m3(codes).tolist() == [[320.0]]
+    # an all-zero tile keeps X = 1 and zero codes
+    codes, E = E_.block_scale_e4m3(np.zeros((3, 3)), block=(2, 2))
+    assert (E == 0).all() and (codes == 0).all()
+
+
+def test_block_scales_tiles_ragged_and_independent():
+    rng = np.random.default_rng(5)
+    Y = rng.normal(size=(70, 45)) * np.exp(rng.normal(size=(70, 45)) * 3)
+    codes, E = E_.block_scale_e4m3(Y)
+    assert E.shape == (3, 2) and codes.shape == Y.shape
+    Yd = E_.decode_e4m3(codes)
+    for i in range(3):
+        for j in range(2):
+            sl = (slice(32 * i, 32 * i + 32), slice(32 * j, 32 * j + 32))
+            m = np.abs(Y[sl]).max()
+            # the tile's largest magnitude lands in [256, 512) of the scaled range; none exceeds 448
+            assert 256 <= m / 2.0 ** E[i, j] < 512
+            assert np.abs(Yd[sl]).max() <= 448
+            # reconstruction within half an e4m3 step (3 mantissa bits: 2^-4 relative), or the
+            # saturation at 448 X, or the smallest subnormal step for tiny values
+            X = 2.0 ** E[i, j]
+            err = np.abs(Yd[sl] * X - Y[sl])
+            tol = np.maximum(np.abs(Y[sl]) * 2.0 ** -4, 2.0 ** -10 * X)
+            sat = np.abs(Y[sl]) >= 448 * X
+            assert (err[~sat] <= tol[~sat]).all()
+            assert (np.abs(Yd[sl][sat]) == 448).all()
+    # changing one tile leaves the others' codes and scales alone
+    Y2 = Y.copy()
+    Y2[:32, :32] *= 1000.0
+    codes2, E2 = E_.block_scale_e4m3(Y2)
+    assert (E2[0, 0] == E[0, 0] + 9 or E2[0, 0] == E[0, 0] + 10)
+    mask = np.ones(Y.shape, dtype=bool)
+    mask[:32, :32] = False
+    assert np.array_equal(codes2[mask], codes[mask]) and (E2.ravel()[1:] == E.ravel()[1:]).all()
+
+
+def test_block_scales_follow_powers_of_two():
+    rng = np.random.default_rng(6)
+    Y = rng.normal(size=(40, 40))
+    codes, E = E_.block_scale_e4m3(Y, block=(16, 16))
+    for k in (-5, 3, 11):
+        c2, e2 = E_.block_scale_e4m3(Y * 2.0 ** k, block=(16, 16))
+        assert np.array_equal(c2, codes) and np.array_equal(e2, E + k)
