@@ -17,6 +17,7 @@ Parts:
                   lists, wave efficiency, operand band counts.
   * grouped.py  - the grouped (many-GEMM) persistent schedule: concatenated
                   tile sequence, the warp-level speculative group search.
+  * blockscale.py - block-scaled operands (one scale per tile of A and of B).
 Every function cites the passage it follows in its own source file.
 """
 from __future__ import annotations
@@ -27,7 +28,7 @@ import subprocess
 
 import numpy as np
 
-from . import epilogue, grouped, schedule  # noqa: F401  (re-exported)
+from . import blockscale, epilogue, grouped, schedule  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_ref.c")

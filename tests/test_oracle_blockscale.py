@@ -1,0 +1,58 @@
+"""Pins for the block-scaled operand oracle (oracle/blockscale.py): brute force on tiny
+shapes, the reduction to the plain GEMM, uniform scales factoring out, and a single
+tile's scale acting only on that tile's partial sums."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from oracle import blockscale as BS
+
+
+def test_brute_force_tiny():
+    rng = np.random.default_rng(1)
+    M, N, K, br, bk = 3, 2, 5, 2, 2
+    a, b = rng.normal(size=(M, K)), rng.normal(size=(N, K))
+    sA, sB = rng.uniform(0.5, 2, size=(2, 3)), rng.uniform(0.5, 2, size=(1, 3))
+    want = np.zeros((M, N))
+    for i, j, k in itertools.product(range(M), range(N), range(K)):
+        want[i, j] += a[i, k] * sA[i // br, k // bk] * b[j, k] * sB[j // br, k // bk]
+    assert np.allclose(BS.gemm_block_scaled(a, b, sA, sB, block=(br, bk)), want, rtol=1e-14, atol=1e-14)
+
+
+def test_unit_scales_are_the_plain_gemm():
+    M, N, K = 40, 24, 96
+    A = synthetic.e4m3_bytes(synthetic.draw("int:8", 31, M * K).reshape(M, K).astype(np.float32))
+    B = synthetic.e4m3_bytes(synthetic.draw("int:8", 32, N * K).reshape(N, K).astype(np.float32))
+    a, b = oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3")
+    for block in ((1, 32), (32, 32), (16, 16)):
+        br, bk = block
+        ones_a = np.ones((-(-M // br), -(-K // bk)))
+        ones_b = np.ones((-(-N // br), -(-K // bk)))
+        z, _ = oracle.gemm(A, B, "e4m3")
+        assert np.array_equal(BS.gemm_block_scaled(a, b, ones_a, ones_b, block), z)
+
+
+def test_uniform_scales_factor_out_and_one_tile_acts_locally():
+    rng = np.random.default_rng(2)
+    M, N, K = 33, 17, 70          # ragged against 32 x 32 tiles
+    a = rng.integers(-8, 9, size=(M, K)).astype(np.float64)
+    b = rng.integers(-8, 9, size=(N, K)).astype(np.float64)
+    shA, shB = (2, 3), (1, 3)
+    plain = a @ b.T
+    C = BS.gemm_block_scaled(a, b, np.full(shA, 4.0), np.full(shB, 0.25), block=(32, 32))
+    assert np.array_equal(C, plain)                # 4 * 0.25 = 1, exact on integers
+    sA = np.ones(shA)
+    sA[1, 2] = 8.0                                 # rows 32.., K 64..69
+    C = BS.gemm_block_scaled(a, b, sA, np.ones(shB), block=(32, 32))
+    part = a[32:, 64:] @ b[:, 64:].T
+    assert np.array_equal(C[:32], plain[:32])
+    assert np.array_equal(C[32:], plain[32:] + 7.0 * part)
+
+
+def test_scale_shapes_must_tile_the_operands():
+    a, b = np.zeros((5, 64)), np.zeros((3, 64))
+    with pytest.raises(ValueError):
+        BS.gemm_block_scaled(a, b, np.ones((5, 3)), np.ones((3, 2)), block=(1, 32))
