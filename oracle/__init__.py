@@ -64,6 +64,11 @@ def _load():
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_decode_array.restype = None
         lib.oracle_decode_array.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        lib.oracle_gemm_rows_bdec.restype = None
+        lib.oracle_gemm_rows_bdec.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                              ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_gemm_rows.restype = None
         lib.oracle_gemm_rows.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -101,11 +106,13 @@ def round_bf16(z: np.ndarray) -> np.ndarray:
 
 
 def gemm(A: np.ndarray, B: np.ndarray, dtype, alpha: float = 1.0, scales=None, bias=None,
-         relu: bool = False, rows=None, dtype_b=None):
+         relu: bool = False, rows=None, dtype_b=None, b_decoded=None):
     """z (FP64, unrounded, after the epilogue) and absdot = |alpha sA sB| * sum_k |a||b|.
 
     A: (M, K) codes of `dtype`, B: (N, K) codes of `dtype_b` (default: the same;
     the FP8 formats may be mixed).  rows: optional row indices to compute.
+    b_decoded: optional (N, K) FP64 array holding decode(B, dtype_b), for a caller
+    that computes many row samples of one B; the arithmetic is the same loop.
     Returns arrays of shape (len(rows) or M, N).
     """
     d = _dtype_code(dtype)
@@ -114,9 +121,13 @@ def gemm(A: np.ndarray, B: np.ndarray, dtype, alpha: float = 1.0, scales=None, b
         raise ValueError("BF16 pairs only with BF16")
     want = np.uint16 if d == BF16 else np.uint8
     A = np.ascontiguousarray(A, dtype=want)
-    B = np.ascontiguousarray(B, dtype=want)
     M, K = A.shape
-    N, K2 = B.shape
+    if b_decoded is None:
+        B = np.ascontiguousarray(B, dtype=want)
+        N, K2 = B.shape
+    else:
+        b_decoded = np.ascontiguousarray(b_decoded, dtype=np.float64)
+        N, K2 = b_decoded.shape
     assert K == K2
     sA, sB = (1.0, 1.0) if scales is None else (float(scales[0]), float(scales[1]))
     if rows is None:
@@ -125,10 +136,14 @@ def gemm(A: np.ndarray, B: np.ndarray, dtype, alpha: float = 1.0, scales=None, b
         rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
         nrows, rows_ptr = rows_arr.size, rows_arr.ctypes.data
     bias_arr = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    bias_ptr = None if bias_arr is None else bias_arr.ctypes.data
     z = np.empty((nrows, N), dtype=np.float64)
     ad = np.empty((nrows, N), dtype=np.float64)
-    _load().oracle_gemm_rows(M, N, K, d, db, A.ctypes.data, B.ctypes.data, rows_ptr, nrows,
-                             float(alpha), sA, sB,
-                             None if bias_arr is None else bias_arr.ctypes.data, int(bool(relu)),
-                             z.ctypes.data, ad.ctypes.data)
+    if b_decoded is None:
+        _load().oracle_gemm_rows(M, N, K, d, db, A.ctypes.data, B.ctypes.data, rows_ptr, nrows,
+                                 float(alpha), sA, sB, bias_ptr, int(bool(relu)), z.ctypes.data, ad.ctypes.data)
+    else:
+        _load().oracle_gemm_rows_bdec(N, K, d, A.ctypes.data, b_decoded.ctypes.data, rows_ptr, nrows,
+                                      float(alpha), sA, sB, bias_ptr, int(bool(relu)), z.ctypes.data,
+                                      ad.ctypes.data)
     return z, ad

@@ -128,23 +128,19 @@ uint16_t oracle_round_bf16(double x) {
 }
 
 /*
- * Rows rows[0..nrows) of the GEMM plus epilogue.  A holds dtype_a codes and B
- * dtype_b codes (the two FP8 formats may be mixed).  z_out and absdot_out are
- * nrows x N row-major (FP64).  absdot[r][j] = sum_k |alpha sA sB| |a_ik| |b_jk|,
- * the scale the error bound is quoted against.
- * rows == NULL means rows 0..nrows-1.
+ * Rows rows[0..nrows) of the GEMM plus epilogue, with B already decoded: Bd holds
+ * the exact FP64 values of B (N x K row-major), A holds dtype_a codes.  z_out and
+ * absdot_out are nrows x N row-major (FP64).  absdot[r][j] = sum_k |alpha sA sB|
+ * |a_ik| |b_jk|, the scale the error bound is quoted against.  rows == NULL means
+ * rows 0..nrows-1.  Every element is the same ascending-k loop whichever entry
+ * is called; this one lets a caller that computes many row samples of one B
+ * decode it once.
  */
-void oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int dtype_a, int dtype_b,
-                      const void *A, const void *B,
-                      const int64_t *rows, int64_t nrows,
-                      double alpha, double sA, double sB,
-                      const float *bias, int relu,
-                      double *z_out, double *absdot_out) {
-    (void)M;
-    /* exact decode of B once (N x K doubles); A rows decoded as used */
-    double *Bd = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
-    for (int64_t j = 0; j < N; ++j)
-        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode(dtype_b, B, j * K + k);
+void oracle_gemm_rows_bdec(int64_t N, int64_t K, int dtype_a, const void *A, const double *Bd,
+                           const int64_t *rows, int64_t nrows,
+                           double alpha, double sA, double sB,
+                           const float *bias, int relu,
+                           double *z_out, double *absdot_out) {
     const double scale = alpha * sA * sB;
 
 #pragma omp parallel for schedule(dynamic, 1)
@@ -168,5 +164,23 @@ void oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int dtype_a, int dtype_b,
         }
         free(Ad);
     }
+}
+
+/*
+ * The same with B given as dtype_b codes: B is decoded exactly (N x K doubles)
+ * and the rows are computed as above.  A holds dtype_a codes (the two FP8
+ * formats may be mixed).
+ */
+void oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int dtype_a, int dtype_b,
+                      const void *A, const void *B,
+                      const int64_t *rows, int64_t nrows,
+                      double alpha, double sA, double sB,
+                      const float *bias, int relu,
+                      double *z_out, double *absdot_out) {
+    (void)M;
+    double *Bd = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k) Bd[j * K + k] = decode(dtype_b, B, j * K + k);
+    oracle_gemm_rows_bdec(N, K, dtype_a, A, Bd, rows, nrows, alpha, sA, sB, bias, relu, z_out, absdot_out);
     free(Bd);
 }

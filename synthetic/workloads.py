@@ -28,6 +28,12 @@ WORKLOADS = {
     # 1920 x 1920 x 16384 BF16 -> FP32, U[-1,1], 225 tiles of 128x128, Stream-K with fixup
     "c4_bf16_streamk": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                             mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=1),
+    # the same problem with its 128x128 CTA tiles run as 2x1 CTA pairs (120 scheduled 256x128
+    # tiles), Stream-K, and the hybrid of data-parallel waves with a Stream-K tail
+    "c4_bf16_streamk_pairs": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
+                                  mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=2),
+    "c4_bf16_hybrid_pairs": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
+                                 mapping=("grouped_m", 8), schedule="streamk_hybrid", bn=128, cta_group=2),
     # the same problem, grouped-M G=8 persistent (the data-parallel comparison)
     "c4_bf16_persistent": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                                mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),

@@ -49,3 +49,34 @@ def test_oracle_step_numbers_rows_group_after_group(monkeypatch):
     for (z, _), (g, local) in zip(out, want_groups):
         zz, _ = oracle.gemm(inp[g].A, inp[g].B, "bf16", rows=np.array(local))
         assert np.array_equal(z, zz)
+
+
+def test_rotating_input_sets_exceed_l2_or_flush():
+    # large workloads rotate over sets that together hold at least 4x the L2; small ones flush
+    for name, w in bench.WORKLOADS.items():
+        sets = bench.input_sets(w)
+        if sets:
+            assert 2 <= sets <= bench.MAX_SETS
+            assert sets * bench.workload_bytes(w) >= 4 * bench.L2_BYTES
+        else:
+            assert bench.workload_bytes(w) * bench.MAX_SETS < 4 * bench.L2_BYTES
+    assert bench.input_sets(bench.WORKLOADS["c1_bf16_256"]) == 0
+    # FP8 8192^3: A and B one byte per element, D in BF16
+    assert bench.workload_bytes(bench.WORKLOADS["c3_e4m3_8192"]) == 2 * 8192 * 8192 + 2 * 8192 * 8192
+
+
+def test_config_is_the_same_for_both_arms():
+    # the reference arm and the GPU arm report one configuration, a function of the workload alone
+    a = bench.workload_config(bench.HEADLINE)
+    b = bench.workload_config(bench.HEADLINE)
+    assert a == b and a["M"] == a["N"] == a["K"] == 8192 and a["dtype"] == "e4m3"
+    assert bench.HEADLINE in bench.TARGET_PAIR and "c2x_bf16_8192" in bench.TARGET_PAIR
+
+
+def test_shard_rows_cover_the_problem():
+    w = bench.WORKLOADS["c3_e4m3_8192"]
+    for world in (1, 2, 3, 4, 8):
+        parts = [bench.shard_rows(w, world, r) for r in range(world)]
+        assert parts[0][0] == 0 and parts[-1][1] == w["M"]
+        assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
+        assert sum(bench.flops(p[2]) for p in parts) == bench.flops(w)

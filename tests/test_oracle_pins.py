@@ -191,6 +191,18 @@ def test_gemm_row_sample_equals_full():
     assert np.array_equal(zs, z[rows]) and np.array_equal(ads, ad[rows])
 
 
+@pytest.mark.parametrize("da,db", [("bf16", "bf16"), ("e4m3", "e5m2")])
+def test_gemm_with_predecoded_b_is_the_same_loop(da, db):
+    # the entry that takes B's decoded values runs the same ascending-k loop: bitwise equal
+    inp = synthetic.make_gemm_inputs(24, 40, 96, da if da == db else f"{da}_{db}", "normal", case=9,
+                                     bias_dist="normal")
+    rows = [3, 0, 23, 11]
+    kw = dict(alpha=0.75, scales=inp.scales, bias=inp.bias, relu=True, rows=rows, dtype_b=db)
+    z, ad = oracle.gemm(inp.A, inp.B, da, **kw)
+    z2, ad2 = oracle.gemm(inp.A, None, da, b_decoded=oracle.decode(inp.B, db), **kw)
+    assert np.array_equal(z, z2) and np.array_equal(ad, ad2)
+
+
 def test_epilogue_invariants():
     M, N, K = 20, 24, 40
     inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=9, bias_dist="normal")
