@@ -336,9 +336,11 @@ tst_status gemm_run_epi(tst_plan *plan, const void *A, const void *B, void *D,
  * memory, laid out as for gemm_run; args as in gemm_run_epi (DEVICE pointers, or
  * NULL when the plan's epilogue needs none).  No counterpart on the pages: the
  * host-level analogue of the kernel's overlap of loads with MMAs.  The call copies
- * B to a plan-owned device buffer, then A in row panels (a whole number of
- * scheduled tile rows each, `panels` of them, 0 = about 8, at most 64; a last
- * panel shorter than half the others joins the one before it); each
+ * B to a plan-owned device buffer, then A in row panels.  `panels` (0 = 8, at most
+ * 64) is the number of panels aimed for, an upper bound: every panel but the last is
+ * R = ceil(M / panels) rows rounded up to whole scheduled tile rows, so fewer panels
+ * may result, and a last panel shorter than R / 2 joins the one before it (which
+ * then holds up to 1.5 R rows); each
  * panel's GEMM runs on `stream` as soon as its rows have landed, and its rows of D
  * are copied back while later panels are still arriving.  Two plan-owned copy
  * streams carry the transfers, ordered after earlier work on `stream`, and
@@ -348,7 +350,9 @@ tst_status gemm_run_epi(tst_plan *plan, const void *A, const void *B, void *D,
  * copied synchronously.  The first call allocates the device buffers (M K + N K
  * input elements, M N outputs), the streams and one plan per panel height; later
  * calls reuse them (with the same `panels`).  amax, if set, covers all panels.
- * gemm_status_query reports the panels' device status.  Errors: INVALID_ARG (a
+ * gemm_status_query reports the first device status recorded by any panel of the
+ * call.  Fault-injection flags set on the plan (gemm_plan_set_debug) apply to the
+ * first panel only; its wait limit applies to every panel.  Errors: INVALID_ARG (a
  * NULL operand, panels outside 0..64), UNSUPPORTED (grouped plans), NO_DEVICE,
  * OOM, CUDA, and those of gemm_run_epi; after an error D is unspecified. */
 tst_status gemm_run_host(tst_plan *plan, const void *A_host, const void *B_host, void *D_host,
@@ -445,8 +449,9 @@ tst_status gemm_plan_get_info(const tst_plan *plan, tst_plan_info *info);
 tst_status gemm_work_items(const tst_plan *plan, int32_t cta, tst_work_item *items,
                            int64_t cap, int64_t *count);
 
-/* Device-side status of the last gemm_run on this plan: TST_OK, TST_ERR_TIMEOUT
- * or TST_ERR_DEVICE_CHECK.  Synchronises the stream of the last run first.
+/* Device-side status of the last gemm_run on this plan (of every panel of the
+ * last gemm_run_host): TST_OK, TST_ERR_TIMEOUT or TST_ERR_DEVICE_CHECK.
+ * Synchronises the stream of the last run first.
  * The status stays until the next gemm_run resets it.  If `detail` is not NULL
  * it receives the raw status word (code in bits 0-7, role in bits 8-15, CTA in
  * bits 16-31). */
@@ -503,17 +508,21 @@ tst_status gemm_plan_set_debug(tst_plan *plan, int32_t flags, void *trace_buf, i
  * keeps the partial tiles and locks in a file-scope device array of
  * TST_NOALLOC_SCRATCH_BYTES bytes, and builds its schedule on the stack.
  *
- * Computes the same C as gemm_plan_create + gemm_run with the same arguments
- * and tst_plan_options.cta_group = 1 (one CTA per tile; schedule must be
- * TST_STREAMK or TST_STREAMK_HYBRID; bn and num_ctas as in tst_plan_options,
- * 0 = choose).  A, B, C, bias, scales: caller-owned device
+ * Computes C = epilogue(A x B) as gemm_run does, within the same error bound:
+ * one CTA per 128 x bn tile, k-tiles of one 128-byte swizzle atom (bk = 64 BF16
+ * or 128 e4m3) issued by a single MMA thread, schedule TST_STREAMK or
+ * TST_STREAMK_HYBRID, bn and num_ctas as in tst_plan_options (bn 0 = 256 when
+ * the 128 x 256 tiles fill the SMs, else 128).  It is bit for bit the result of
+ * a plan made with cta_group = 1, the same bn and bk = 64 (BF16) / 128 (e4m3);
+ * the plan's defaults (two-atom k-tiles, the cost model's tile) may round
+ * differently in the last bits.  A, B, C, bias, scales: caller-owned device
  * pointers as for gemm_run.  device_status: optional device pointer to one
  * uint32 that receives the device-side status word (0 = OK, code in bits 0-7 as
  * in tst_status, e.g. 6 = a bounded wait ran out); NULL keeps it in the scratch
  * array, where it cannot be read.  The call enqueues a clear of the locks (and
  * of *device_status) plus one kernel launch on `stream` and returns.
  *
- * Scratch use: 256 bytes + 4 bytes per split tile (rounded up to 256) +
+ * Scratch use: 256 bytes + 8 bytes per split tile (rounded up to 256) +
  * 128 x bn x 4 bytes per split tile.  A problem that needs more than
  * TST_NOALLOC_SCRATCH_BYTES is rejected with TST_ERR_UNSUPPORTED before any GPU
  * work.  Every call, from any thread, shares the one array and leaves its last

@@ -110,3 +110,46 @@ def test_run_host_panel_counts_change_between_calls():
         tst.gemm_run_host(plan, Ah, Bh, Dh, panels=panels)
         assert tst.gemm_status_query(plan)[0] == tst.TST_OK, panels
         assert torch.equal(Dh, want), panels
+
+
+def test_run_host_reports_a_timeout_in_the_first_panel_only():
+    """Eight equal panels share one cached panel plan; a bounded-wait timeout injected into
+    the first panel alone must still be what the status query reports after the seven
+    panels that follow it ran cleanly.  The same plan then runs clean and exact."""
+    M, N, K = 2048, 512, 1024       # 8 panels of 256 rows: one panel height, one panel plan
+    A = synthetic.bf16_bits(synthetic.draw("int:8", 8160, M * K).reshape(M, K))
+    B = synthetic.bf16_bits(synthetic.draw("int:8", 8260, N * K).reshape(N, K))
+    plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent", out_dtype="f32",
+                                cta_group=2, bn=128)
+    Ah, Bh = _host(A), _host(B)
+    Dh = torch.full((M, N), float("nan")).pin_memory()
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOAD, None, 0, timeout_ns=20_000_000)
+    tst.gemm_run_host(plan, Ah, Bh, Dh, panels=8)
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_ERR_TIMEOUT, (st, hex(word))
+    # panels 1..7 ran without the fault: their rows are exact
+    want, _ = oracle.gemm(A, B, "bf16")
+    assert np.array_equal(Dh.numpy()[256:].astype(np.float64), want[256:])
+    tst.gemm_plan_set_debug(plan, 0, None, 0, timeout_ns=0)
+    tst.gemm_run_host(plan, Ah, Bh, Dh, panels=8)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    assert np.array_equal(Dh.numpy().astype(np.float64), want)
+
+
+def test_run_host_short_remainder_joins_the_last_panel():
+    """8 panels asked for on 2148 rows of CTA-pair tiles: panels of 512 rows leave 100
+    rows, which join the fourth panel (612 rows); every row against the oracle on random
+    normal inputs, within the element-wise bound."""
+    M, N, K = 2148, 520, 1024
+    inp = synthetic.make_gemm_inputs(M, N, K, "bf16", "normal", case=31)
+    plan = tst.gemm_plan_create(M, N, K, mapping=("grouped_m", 8), schedule="persistent", out_dtype="f32",
+                                cta_group=2, bn=128)
+    Dh = torch.full((M, N), float("nan")).pin_memory()
+    tst.gemm_run_host(plan, _host(inp.A), _host(inp.B), Dh, panels=8)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    z, ad = oracle.gemm(inp.A, inp.B, "bf16")
+    err = np.abs(Dh.numpy().astype(np.float64) - z)
+    assert (err <= 4e-3 * ad + 1e-6).all(), err.max()
+    Dd = torch.empty(M, N, device="cuda")
+    tst.gemm_run(plan, device_codes(inp.A), device_codes(inp.B), Dd)
+    assert torch.equal(Dh, Dd.cpu())       # the merged panel computes the same tiles

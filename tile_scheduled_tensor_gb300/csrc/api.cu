@@ -81,6 +81,7 @@ struct tst_plan {
   unsigned long long* d_status = nullptr;   // (run_id << 32) | status of that run
   unsigned long long* d_locks = nullptr;
   uint32_t run_id = 0;                      // id of the last launch (tags status and locks)
+  uint32_t status_floor = 0;                // first run id of the status window the query reads
   float* d_ws = nullptr;
   // debug
   int32_t debug_flags = 0;
@@ -756,8 +757,10 @@ tst_status gemm_run(tst_plan* p, const void* A, const void* B, void* C, const fl
 
 namespace {
 
+// continue_window: this launch extends the plan's status window (a later panel of one
+// gemm_run_host call on the same panel plan), so a code any of them records is kept
 tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_epilogue_args* ea,
-                  const int32_t* group_rows, void* stream_, bool keep_amax = false) {
+                  const int32_t* group_rows, void* stream_, bool keep_amax = false, bool continue_window = false) {
   if (p == nullptr || ea == nullptr) return TST_ERR_INVALID_ARG;
   // groups of different shapes bring their own operands (uploaded by gemm_grouped_array_run)
   const bool array_mode = !p->shapes_host.empty();
@@ -863,7 +866,9 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   // the status word and the Stream-K locks need no clearing: this launch's run id tags
   // what it writes, and values tagged with an earlier id never match (0 is never used)
   if (++p->run_id == 0) p->run_id = 1;
+  if (!continue_window || p->status_floor == 0) p->status_floor = p->run_id;
   kp.run_id = p->run_id;
+  kp.status_floor = p->status_floor;
   // amax starts at zero for every launch
   if (kp.ext.amax && !keep_amax && cudaMemsetAsync(kp.ext.amax, 0, sizeof(float), stream) != cudaSuccess)
     return TST_ERR_CUDA;
@@ -1144,13 +1149,24 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
          cudaEventRecord(ev[2 + q], h->s_in) == cudaSuccess;
   }
   if (!ok) return TST_ERR_CUDA;
-  // the panels' GEMMs on the caller's stream, each after its rows of A have landed
+  // the panels' GEMMs on the caller's stream, each after its rows of A have landed.  The
+  // first launch on each panel plan opens its status window and the later ones extend it,
+  // so a code recorded by any panel is reported.  The parent's fault-injection flags (a
+  // test hook) apply to the first panel only; its wait limit applies to every panel.
+  bool window_open[2] = {false, false};
+  const int32_t fault_flags = p->debug_flags & (TST_DEBUG_FAULT_SKIP_LOAD | TST_DEBUG_FAULT_SKIP_LOCK);
   for (int64_t q = 0; q < P; ++q) {
     const int64_t r0 = q * R;
     if (cudaStreamWaitEvent(s, ev[2 + q], 0) != cudaSuccess) return TST_ERR_CUDA;
     const tst_epilogue_args a = panel_args(r0);
-    const tst_status st = launch(plans[q], dA + r0 * K * elt, h->dB, dD + r0 * N * out_elt, &a, nullptr, s, q > 0);
+    const int slot = plans[q] == h->panel_plan[0] ? 0 : 1;
+    plans[q]->timeout_ns = p->timeout_ns;
+    plans[q]->debug_flags = q == 0 ? fault_flags : 0;
+    const tst_status st = launch(plans[q], dA + r0 * K * elt, h->dB, dD + r0 * N * out_elt, &a, nullptr, s, q > 0,
+                                 window_open[slot]);
+    plans[q]->debug_flags = 0;
     if (st != TST_OK) return st;
+    window_open[slot] = true;
     if (cudaEventRecord(ev[2 + P + q], s) != cudaSuccess) return TST_ERR_CUDA;
   }
   // outputs: each panel's D as soon as its GEMM is done
@@ -1208,8 +1224,11 @@ tst_status gemm_status_query(tst_plan* p, uint32_t* detail) {
   if (cudaStreamSynchronize(p->last_stream) != cudaSuccess) return TST_ERR_CUDA;
   unsigned long long tagged = 0;
   if (cudaMemcpy(&tagged, p->d_status, sizeof(tagged), cudaMemcpyDeviceToHost) != cudaSuccess) return TST_ERR_CUDA;
-  // a word tagged with another run id was left by an earlier launch: the last one recorded nothing
-  const uint32_t word = (tagged >> 32) == p->run_id ? static_cast<uint32_t>(tagged) : 0u;
+  // a word tagged outside the last status window was left by an earlier launch: the last
+  // launch (or run of launches) recorded nothing
+  const uint32_t tag = static_cast<uint32_t>(tagged >> 32);
+  const bool current = static_cast<uint32_t>(tag - p->status_floor) <= static_cast<uint32_t>(p->run_id - p->status_floor);
+  const uint32_t word = current ? static_cast<uint32_t>(tagged) : 0u;
   if (detail) *detail = word;
   switch (word & 0xFFu) {
     case 0: return TST_OK;

@@ -80,13 +80,18 @@ struct Ctx {
   int32_t unit;         // scheduling unit: the CTA (CG = 1) or the CTA pair (CG = 2)
 };
 
-// Record `code` in the status word unless this launch has recorded one already (a word
-// tagged with another launch's run id is stale and is replaced).
+// Record `code` in the status word unless a launch of the current status window (run ids
+// status_floor .. run_id) has recorded one already; a word tagged outside the window is
+// stale and is replaced.
 __device__ __forceinline__ void record_status(const KernelParams& p, uint32_t code, uint32_t role) {
   const unsigned long long mine = (static_cast<unsigned long long>(p.run_id) << 32) | code | (role << 8) |
                                   (static_cast<unsigned long long>(blockIdx.x) << 16);
+  auto in_window = [&](unsigned long long word) {
+    return static_cast<uint32_t>(static_cast<uint32_t>(word >> 32) - p.status_floor) <=
+           static_cast<uint32_t>(p.run_id - p.status_floor);
+  };
   unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(p.status);
-  while ((old >> 32) != p.run_id) {
+  while (!in_window(old)) {
     const unsigned long long seen = atomicCAS(p.status, old, mine);
     if (seen == old) break;
     old = seen;

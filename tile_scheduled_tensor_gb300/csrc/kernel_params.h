@@ -99,6 +99,9 @@ struct KernelParams {
   int32_t staging_offset;   // SK_TMA: byte offset of the staging buffers from the aligned shared base
   uint32_t run_id;          // tags the status word and the locks of this launch (never 0), so
                             // that values left by earlier launches need no clearing
+  uint32_t status_floor;    // the status word keeps a code recorded by any launch with a run id
+                            // in [status_floor, run_id] (a run of several launches on one plan);
+                            // status_floor == run_id for a single launch
 };
 
 // Tile configuration for a scheduled tile width BN, a CTA group of CG CTAs

@@ -227,6 +227,7 @@ extern "C" tst_status gemm_streamk_noalloc(int64_t M, int64_t N, int64_t K, tst_
   kp.sk_slots = 1;
   kp.timeout_ns = 10ull * 1000 * 1000 * 1000;
   kp.run_id = 1;   // the status word and the locks are cleared below for every call
+  kp.status_floor = 1;
 
   // ---- clear what must start at zero: the status word and the locks
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
