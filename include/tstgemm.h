@@ -151,6 +151,19 @@ typedef struct {
  *   amax = max over all (i, j) of |Y|                (when amax is set)
  *   D[i][j] = cast(d_scale * Y)
  *
+ * or, with block_scale (e4m3 D only, no d_scale), block scale factor generation
+ * ("H100 . Kernel Design", section 12.1, the block-scaling workflow; "H100 .
+ * WGMMA Part 2", section 11, one scale per 32 x 32 tile): D is cut into 32 x 32
+ * tiles (ragged at the right and bottom edges); tile (r, c) gets the power-of-two
+ * scale 2^E with E = floor(log2(max |Y| over the tile)) - 8 (8: the exponent of
+ * e4m3's largest power of two; E = 0 for an all-zero tile), and
+ *
+ *   D[i][j] = e4m3(Y / 2^E),  block_exp[r][c] = E
+ *
+ * rounded to nearest even and saturated to +-448, so D decodes back to Y within
+ * e4m3's precision as decode(D) * 2^E.  E is taken from the FP32 value of the
+ * tile maximum exactly.
+ *
  * Absent factors are 1 and absent terms 0.  activation: identity, ReLU
  * max(z, 0), GELU z * Phi(z) (Phi the standard normal CDF), SiLU z / (1 + e^-z).
  * All arithmetic is FP32.  Here C is the page's addend matrix; the result D is
@@ -173,6 +186,8 @@ typedef struct {
     int32_t amax;        /* 1: write max |Y| (before d_scale) to an FP32[1] */
     int32_t aux;         /* 1: also store Z (before the activation) to an M x N matrix */
     int32_t aux_dtype;   /* TST_OUT_F32 or TST_OUT_BF16 */
+    int32_t block_scale; /* 1: e4m3 D with one power-of-two scale per 32 x 32 tile (see above);
+                            needs out_dtype TST_OUT_E4M3 and no d_scale */
 } tst_epilogue_ex;
 
 /* Run-time operands of the extended epilogue: DEVICE pointers owned by the
@@ -188,6 +203,8 @@ typedef struct {
     const float *d_scale;   /* FP32[1] */
     float *amax;            /* FP32[1], written */
     void *aux;              /* M x N, aux_dtype, written */
+    int32_t *block_exp;     /* int32[ceil(M/32)][ceil(N/32)] row-major, written: the exponent E
+                               of each 32 x 32 tile's scale (block_scale); 4-byte aligned */
 } tst_epilogue_args;
 
 /* Optional plan settings.  Zero-initialise and set what you need. */
@@ -255,6 +272,16 @@ typedef struct {
                               the same either way.  TST_BOXES_2D: always 2-D; TST_BOXES_3D: 3-D
                               wherever possible; TST_BOXES_AUTO (default): 3-D for 128-column CTA
                               pair tiles, where it measured faster, else 2-D. */
+    int32_t cluster_n;     /* CTAs along N sharing A by TMA multicast ("H100 . cp.async.bulk"
+                              sections 8 and 11; "H100 . Kernel Design" section 10.1): 0 or 1 =
+                              none; 2 = clusters of two single CTAs computing side-by-side tiles
+                              of the same rows, each loading one of the k-tile's two atoms of A
+                              and multicasting it to both.  The scheduled tile is then 128 x 2 bn
+                              (the mapping and schedules act on it) and each CTA computes one
+                              128 x bn half.  Needs cta_group 1, two-atom k-tiles, the basic
+                              epilogue, one GEMM (not grouped), no HyTiS and no separate
+                              Stream-K reduction (TST_ERR_UNSUPPORTED otherwise).  The result is
+                              bit for bit that of the same plan without multicast. */
 } tst_plan_options;
 
 enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2, TST_SK_TMA = 3 };
@@ -282,6 +309,8 @@ typedef struct {
     int32_t sk_slots;          /* partial slots per split-tile half (separate reduction), else 1 */
     int32_t l2_hint;           /* the operand cache hint in use: TST_L2_NONE, _KEEP_A or _KEEP_B */
     int32_t box3d;             /* 1: one 3-D TMA box per operand and stage, 0: 2-D boxes per atom */
+    int32_t cluster_n;         /* CTAs along N sharing A by multicast (1 = none); the scheduled
+                                  tile is bm x (bn * cluster_n) and nt counts those */
 } tst_plan_info;
 
 typedef struct tst_plan tst_plan;

@@ -361,3 +361,37 @@ def test_run_host_argument_errors():
         tst.TST_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         tst.gemm_run_host(plan, A, B, [1], stream=0)
+
+
+def test_block_scale_plan_rules():
+    # block scale factor generation: e4m3 D only, in place of the tensor-wise output scale,
+    # one GEMM (not grouped), the GEMM's own epilogue (not the separate Stream-K reduction)
+    kw = dict(host_only=True, num_sms=152, block_scale=True)
+    p = tst.gemm_plan_create(512, 512, 256, out_dtype="e4m3", **kw)
+    assert p.info.M == 512
+    for bad, status in ((dict(out_dtype="bf16"), tst.TST_ERR_INVALID_ARG),
+                        (dict(out_dtype="e4m3", d_scale=True), tst.TST_ERR_INVALID_ARG),
+                        (dict(out_dtype="e4m3", schedule="streamk", sk_fixup="separate"), tst.TST_ERR_UNSUPPORTED)):
+        with pytest.raises(tst.TstError) as e:
+            tst.gemm_plan_create(512, 512, 256, **bad, **kw)
+        assert e.value.status == status, bad
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_grouped_plan_create(2, 512, 256, 256, out_dtype="e4m3", block_scale=True, host_only=True,
+                                     num_sms=152)
+    assert e.value.status == tst.TST_ERR_UNSUPPORTED
+
+
+def test_multicast_plan_rules():
+    # cluster_n = 2: clusters of two single CTAs along N (the scheduled tile 128 x 2 bn)
+    kw = dict(host_only=True, num_sms=152, cluster_n=2)
+    ok = tst.gemm_plan_create(1024, 1000, 1024, cta_group=1, bn=128, **kw)
+    assert ok.info.cluster_n == 2 and ok.info.ctas == 2 * ok.info.grid
+    assert (ok.info.mt, ok.info.nt) == (8, 4) and ok.info.bn == 128
+    for bad in (dict(cta_group=2), dict(cta_group=1, bk=64), dict(cta_group=1, schedule="hytis"),
+                dict(cta_group=1, schedule="streamk", sk_fixup="separate"), dict(cta_group=1, activation="gelu")):
+        with pytest.raises(tst.TstError) as e:
+            tst.gemm_plan_create(1024, 1024, 1024, bn=128, **bad, **kw)
+        assert e.value.status == tst.TST_ERR_UNSUPPORTED, bad
+    with pytest.raises(tst.TstError) as e:
+        tst.gemm_plan_create(1024, 1024, 1024, bn=128, cta_group=1, host_only=True, num_sms=152, cluster_n=3)
+    assert e.value.status == tst.TST_ERR_INVALID_ARG

@@ -98,31 +98,33 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      l2_hint="none", tma_boxes="auto", beta: float = 0.0, has_c: bool = False, c_dtype="f32",
                      bias_mode=None, activation=None,
                      row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
-                     amax: bool = False, aux: bool = False, aux_dtype="f32") -> Plan:
+                     amax: bool = False, aux: bool = False, aux_dtype="f32", block_scale: bool = False,
+                     cluster_n: int = 0) -> Plan:
     """Plan C = epilogue(A x B).  The basic epilogue is alpha, a column bias (has_bias),
     ReLU and the tensor-wise scales; any of beta/has_c, bias_mode='row', activation
-    'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux or out_dtype 'e4m3' selects
-    the extended one (gemm_plan_create_epi)."""
+    'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux, block_scale or out_dtype 'e4m3'
+    selects the extended one (gemm_plan_create_epi).  block_scale: an e4m3 D with one
+    power-of-two scale per 32 x 32 tile, whose exponents gemm_run writes to block_exp."""
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
                                   int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
                                   int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"), int(bool(pdl)),
                                   _enum(_L2, l2_hint, "l2_hint"),
-                                  _enum(_BOXES, tma_boxes, "tma_boxes"))
+                                  _enum(_BOXES, tma_boxes, "tma_boxes"), int(cluster_n))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \
         (TST_ACT_RELU if relu else TST_ACT_NONE)
     extended = bool(has_c or bmode == TST_BIAS_ROW or act in (TST_ACT_GELU, TST_ACT_SILU) or row_scale or
-                    col_scale or d_scale or amax or aux)
+                    col_scale or d_scale or amax or aux or block_scale)
     h = ctypes.c_void_p()
     if extended:
         epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), float(beta),
                                     int(bool(has_c)), _enum(_OUT, c_dtype, "c_dtype"), bmode, act,
                                     int(bool(use_scales)), int(bool(row_scale)), int(bool(col_scale)),
                                     int(bool(d_scale)), int(bool(amax)), int(bool(aux)),
-                                    _enum(_OUT, aux_dtype, "aux_dtype"))
+                                    _enum(_OUT, aux_dtype, "aux_dtype"), int(bool(block_scale)))
         _check(lib.gemm_plan_create_epi(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
                                         TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),
                                         ctypes.byref(epi), ctypes.byref(opts)), "gemm_plan_create_epi")
@@ -144,7 +146,8 @@ def gemm_grouped_plan_create(groups: int, M: int, N: int, K: int, dtype="bf16", 
                              col_scale: bool = False, d_scale: bool = False, amax: bool = False, aux: bool = False,
                              aux_dtype="f32", bn: int = 0, num_ctas: int = 0, host_only: bool = False,
                              num_sms: int = 0, timeout_ns: int = 0, cta_group: int = 0, stages: int = 0,
-                             bk: int = 0, pdl: bool = False, l2_hint="none", tma_boxes="auto") -> Plan:
+                             bk: int = 0, pdl: bool = False, l2_hint="none", tma_boxes="auto",
+                             block_scale: bool = False) -> Plan:
     """Plan `groups` GEMMs sharing N and K in one persistent launch: A holds the groups'
     rows one after another (at most M in all), B one N x K matrix per group; the row
     counts are given to gemm_grouped_run as a device int32 array."""
@@ -161,7 +164,7 @@ def gemm_grouped_plan_create(groups: int, M: int, N: int, K: int, dtype="bf16", 
     epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), float(beta), int(bool(has_c)),
                                 _enum(_OUT, c_dtype, "c_dtype"), bmode, act, int(bool(use_scales)),
                                 int(bool(row_scale)), int(bool(col_scale)), int(bool(d_scale)), int(bool(amax)),
-                                int(bool(aux)), _enum(_OUT, aux_dtype, "aux_dtype"))
+                                int(bool(aux)), _enum(_OUT, aux_dtype, "aux_dtype"), int(bool(block_scale)))
     h = ctypes.c_void_p()
     _check(lib.gemm_grouped_plan_create(ctypes.byref(h), int(groups), int(M), int(N), int(K),
                                         _enum(_DTYPES, dtype, "dtype"), TST_LAYOUT_A_ROW_B_NK, m, ctypes.byref(epi),
@@ -281,16 +284,17 @@ def _stream(stream):
 
 
 def gemm_run(plan: Plan, A, B, C, bias=None, scales=None, stream=None, c=None, row_scale=None, col_scale=None,
-             d_scale=None, amax=None, aux=None):
+             d_scale=None, amax=None, aux=None, block_exp=None):
     """Enqueue C = epilogue(A x B) on `stream` (default: torch's current stream).  The
     extended epilogue's operands (c: the addend of beta * C; row_scale, col_scale,
-    d_scale, amax, aux) go through gemm_run_epi."""
-    if all(x is None for x in (c, row_scale, col_scale, d_scale, amax, aux)):
+    d_scale, amax, aux; block_exp, int32 [ceil(M/32), ceil(N/32)] written by a
+    block-scaled e4m3 D) go through gemm_run_epi."""
+    if all(x is None for x in (c, row_scale, col_scale, d_scale, amax, aux, block_exp)):
         _check(lib.gemm_run(plan._h, _ptr(A), _ptr(B), _ptr(C), _ptr(bias), _ptr(scales), _stream(stream)),
                "gemm_run")
         return
     args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
-                                   _ptr(d_scale), _ptr(amax), _ptr(aux))
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux), _ptr(block_exp))
     _check(lib.gemm_run_epi(plan._h, _ptr(A), _ptr(B), _ptr(C), ctypes.byref(args), _stream(stream)),
            "gemm_run_epi")
 
@@ -304,12 +308,12 @@ def _host_ptr(x):
 
 
 def gemm_run_host(plan: Plan, A, B, D, panels: int = 0, stream=None, bias=None, scales=None, c=None,
-                  row_scale=None, col_scale=None, d_scale=None, amax=None, aux=None):
+                  row_scale=None, col_scale=None, d_scale=None, amax=None, aux=None, block_exp=None):
     """End to end on host tensors A, B, D (CPU, contiguous; pinned for the copies to
     overlap the computation): row panels of A stream in, each panel's GEMM runs as soon as
     it has landed, its rows of D stream back.  Epilogue operands are CUDA tensors."""
     args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
-                                   _ptr(d_scale), _ptr(amax), _ptr(aux))
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux), _ptr(block_exp))
     _check(lib.gemm_run_host(plan._h, _host_ptr(A), _host_ptr(B), _host_ptr(D), ctypes.byref(args), int(panels),
                              _stream(stream)), "gemm_run_host")
 

@@ -46,13 +46,13 @@ class tst_epilogue_ex(ctypes.Structure):
                 ("has_c", ctypes.c_int32), ("c_dtype", ctypes.c_int32), ("bias_mode", ctypes.c_int32),
                 ("activation", ctypes.c_int32), ("use_scales", ctypes.c_int32), ("row_scale", ctypes.c_int32),
                 ("col_scale", ctypes.c_int32), ("d_scale", ctypes.c_int32), ("amax", ctypes.c_int32),
-                ("aux", ctypes.c_int32), ("aux_dtype", ctypes.c_int32)]
+                ("aux", ctypes.c_int32), ("aux_dtype", ctypes.c_int32), ("block_scale", ctypes.c_int32)]
 
 
 class tst_epilogue_args(ctypes.Structure):
     _fields_ = [("c", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p), ("d_scale", ctypes.c_void_p),
-                ("amax", ctypes.c_void_p), ("aux", ctypes.c_void_p)]
+                ("amax", ctypes.c_void_p), ("aux", ctypes.c_void_p), ("block_exp", ctypes.c_void_p)]
 
 
 class tst_plan_options(ctypes.Structure):
@@ -60,7 +60,7 @@ class tst_plan_options(ctypes.Structure):
                 ("host_only", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_int64), ("stages", ctypes.c_int32), ("bk", ctypes.c_int32),
                 ("sk_groups", ctypes.c_int32), ("sk_fixup", ctypes.c_int32), ("pdl", ctypes.c_int32),
-                ("l2_hint", ctypes.c_int32), ("tma_boxes", ctypes.c_int32)]
+                ("l2_hint", ctypes.c_int32), ("tma_boxes", ctypes.c_int32), ("cluster_n", ctypes.c_int32)]
 
 
 class tst_plan_info(ctypes.Structure):
@@ -72,7 +72,7 @@ class tst_plan_info(ctypes.Structure):
                 ("max_items_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("cta_group", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("kernels_per_run", ctypes.c_int32), ("sk_slots", ctypes.c_int32),
-                ("l2_hint", ctypes.c_int32), ("box3d", ctypes.c_int32)]
+                ("l2_hint", ctypes.c_int32), ("box3d", ctypes.c_int32), ("cluster_n", ctypes.c_int32)]
 
 
 class tst_work_item(ctypes.Structure):

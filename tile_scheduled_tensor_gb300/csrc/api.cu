@@ -62,7 +62,8 @@ struct tst_plan {
   uint32_t fmt_ab = 0;         // FP8 operand formats for the instruction descriptor
   tst_plan_options opts{};
   int32_t bm = tst::kBlockM, bn = 128, bk = 64, stages = 0, smem_bytes = 0;
-  int32_t cg = 1;              // CTAs per scheduling unit (2 = CTA pair)
+  int32_t cg = 1;              // CTAs per scheduling unit along M (2 = CTA pair)
+  int32_t mc = 1;              // CTAs along N sharing A by multicast (the unit is cg x mc CTAs)
   int32_t sk_mode = 0;         // tst::SkFixup
   int32_t staging_offset = 0;  // SK_TMA staging buffers in shared memory
   int32_t sk_slots = 1;        // partial slots per split-tile half
@@ -261,7 +262,7 @@ int out_bytes(int32_t t) { return t == TST_OUT_F32 ? 4 : t == TST_OUT_BF16 ? 2 :
 bool needs_ext(const tst_epilogue_ex& e) {
   return e.out_dtype == TST_OUT_E4M3 || e.has_c || e.bias_mode == TST_BIAS_ROW ||
          (e.activation != TST_ACT_NONE && e.activation != TST_ACT_RELU) || e.row_scale || e.col_scale ||
-         e.d_scale || e.amax || e.aux;
+         e.d_scale || e.amax || e.aux || e.block_scale;
 }
 
 // FP8 operand formats of a dtype in the instruction descriptor: A bits 7-9, B bits 10-12,
@@ -293,6 +294,11 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if ((epi->has_c && !valid_in(epi->c_dtype)) || (epi->aux && !valid_in(epi->aux_dtype))) return TST_ERR_INVALID_ARG;
   if (epi->bias_mode < TST_BIAS_NONE || epi->bias_mode > TST_BIAS_ROW) return TST_ERR_INVALID_ARG;
   if (epi->activation < TST_ACT_NONE || epi->activation > TST_ACT_SILU) return TST_ERR_INVALID_ARG;
+  // block scale factor generation: an e4m3 D whose 32 x 32 tiles carry their own scale, in
+  // place of the tensor-wise output scale; one GEMM per launch, the GEMM's own epilogue
+  if (epi->block_scale != 0 && epi->block_scale != 1) return TST_ERR_INVALID_ARG;
+  if (epi->block_scale && (epi->out_dtype != TST_OUT_E4M3 || epi->d_scale)) return TST_ERR_INVALID_ARG;
+  if (epi->block_scale && (groups > 0 || (opts && opts->sk_fixup == TST_SK_SEPARATE))) return TST_ERR_UNSUPPORTED;
   if (layout != TST_LAYOUT_A_ROW_B_NK) return TST_ERR_UNSUPPORTED;
   tst_plan_options o{};
   if (opts) o = *opts;
@@ -349,6 +355,15 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     p->cg = o.cta_group != 0 ? o.cta_group : tc.cg;
   }
   p->bm = tst::kBlockM * p->cg;
+  // A multicast across two side-by-side single-CTA tiles: the multicast kernel instance
+  // covers the basic epilogue of one GEMM with two-atom k-tiles
+  if (o.cluster_n < 0 || o.cluster_n > 2) { delete p; return TST_ERR_INVALID_ARG; }
+  p->mc = o.cluster_n == 2 ? 2 : 1;
+  if (p->mc == 2 && (p->cg != 1 || p->ka != 2 || p->ext_on || groups > 0 || schedule == TST_HYTIS ||
+                     o.sk_fixup == TST_SK_SEPARATE)) {
+    delete p;
+    return TST_ERR_UNSUPPORTED;
+  }
   // one 3-D box per operand and stage: needs two atoms per k-tile and K (every group's K_g)
   // a whole number of 128-byte atoms; chosen by default for 128-column pair tiles only
   // (measured: +3 % there, 1-4 % slower on the other tile shapes)
@@ -358,7 +373,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     for (int32_t g = 0; g < groups; ++g)
       if ((static_cast<int64_t>(shapes[4 * g + 2]) * elt) % 128 != 0) p->box3d = false;
   const int64_t mt = ceil_div(M, p->bm);
-  const int64_t nt = ceil_div(N, p->bn);
+  const int64_t nt = ceil_div(N, p->bn * p->mc);   // scheduled tiles are bn x mc wide
   const int64_t kt = ceil_div(K, p->bk);
   // grouped: at most ceil(M / bm) + groups tile rows over all groups, whatever the split;
   // groups of different shapes: exactly the sum of their own grids
@@ -378,7 +393,8 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (!p->host_only) {
     // the extended epilogue has its own instance (two epilogue warpgroups, typed stores of D)
     const int kdt = dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3;
-    p->kernel = p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka) : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka);
+    p->kernel = p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka)
+                          : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka, p->mc);
     if (!p->kernel ||
         // the largest size any plan of this kernel asks for (the attribute is per kernel)
         cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tst::kSmemLimit) != cudaSuccess) {
@@ -388,19 +404,20 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     }
   }
 
-  // scheduling units that can be resident at once: one CTA per SM, or pairs
-  // of CTAs placed together as clusters of 2
+  // scheduling units that can be resident at once: one CTA per SM, or clusters of
+  // cg x mc CTAs placed together
+  const int csize = p->cg * p->mc;
   int64_t resident = p->num_sms;
-  if (p->cg == 2) {
-    resident = p->num_sms / 2;
+  if (csize > 1) {
+    resident = p->num_sms / csize;
     if (!p->host_only) {
       cudaLaunchConfig_t qc = {};
-      qc.gridDim = dim3(static_cast<unsigned>(2 * resident), 1, 1);
+      qc.gridDim = dim3(static_cast<unsigned>(csize * resident), 1, 1);
       qc.blockDim = dim3(tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
       qc.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
       cudaLaunchAttribute ca[1];
       ca[0].id = cudaLaunchAttributeClusterDimension;
-      ca[0].val.clusterDim.x = 2;
+      ca[0].val.clusterDim.x = csize;
       ca[0].val.clusterDim.y = 1;
       ca[0].val.clusterDim.z = 1;
       qc.attrs = ca;
@@ -424,7 +441,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   s.order = nullptr;
   s.rows = static_cast<int32_t>(M);
   s.bm = p->bm;
-  s.bn = p->bn;
+  s.bn = p->bn * p->mc;
   s.groups = groups;
   s.group_rows = nullptr;   // the run supplies the device array of group sizes
   s.group_b_rows = static_cast<int32_t>(N);
@@ -533,7 +550,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
 
   // plan-owned device memory: status word, then one lock and one 128 x bn FP32
   // partial tile per CTA-half of each split tile
-  const size_t slots = static_cast<size_t>(s.sk_tiles) * p->cg * p->sk_slots;
+  const size_t slots = static_cast<size_t>(s.sk_tiles) * p->cg * p->mc * p->sk_slots;
   const size_t status_bytes = 256;
   const size_t lock_bytes = ((slots * 8 + 255) / 256) * 256;
   const size_t ws_bytes = slots * tst::kBlockM * p->bn * sizeof(float);
@@ -691,7 +708,8 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->smem_bytes = p->smem_bytes;
   info->workspace_bytes = static_cast<int64_t>(p->dev_bytes);
   info->cta_group = p->cg;
-  info->ctas = p->sched.grid * p->cg;
+  info->ctas = p->sched.grid * p->cg * p->mc;
+  info->cluster_n = p->mc;
   info->kernels_per_run = (p->sk_mode == TST_SK_SEPARATE && p->sched.sk_tiles > 0) ? 2 : 1;
   info->sk_slots = p->sk_slots;
   info->l2_hint = p->opts.l2_hint;
@@ -732,7 +750,7 @@ tst_status gemm_plan_set_debug(tst_plan* p, int32_t flags, void* trace_buf, int6
     if (trace_buf == nullptr || cap < need) return TST_ERR_INVALID_ARG;
   }
   if (flags & TST_DEBUG_ROLE_CYCLES) {
-    const int64_t need = static_cast<int64_t>(p->sched.grid) * p->cg * tst::kStatSlots * 2;  // int32 units
+    const int64_t need = static_cast<int64_t>(p->sched.grid) * p->cg * p->mc * tst::kStatSlots * 2;  // int32 units
     if (trace_buf == nullptr || cap < need || (reinterpret_cast<uintptr_t>(trace_buf) & 7u)) return TST_ERR_INVALID_ARG;
   }
   p->debug_flags = flags;
@@ -773,8 +791,10 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   if ((has_bias && ea->bias == nullptr) || (e.use_scales && ea->scales == nullptr) ||
       (e.has_c && ea->c == nullptr) || (e.row_scale && ea->row_scale == nullptr) ||
       (e.col_scale && ea->col_scale == nullptr) || (e.d_scale && ea->d_scale == nullptr) ||
-      (e.amax && ea->amax == nullptr) || (e.aux && ea->aux == nullptr))
+      (e.amax && ea->amax == nullptr) || (e.aux && ea->aux == nullptr) ||
+      (e.block_scale && ea->block_exp == nullptr))
     return TST_ERR_INVALID_ARG;
+  if (e.block_scale && (reinterpret_cast<uintptr_t>(ea->block_exp) & 3u)) return TST_ERR_ALIGNMENT;
   if (!array_mode && (!aligned16(A) || !aligned16(B) || !aligned16(C))) return TST_ERR_ALIGNMENT;
   if ((has_bias && (reinterpret_cast<uintptr_t>(ea->bias) & 3u)) ||
       (e.use_scales && (reinterpret_cast<uintptr_t>(ea->scales) & 3u)))
@@ -793,7 +813,8 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   // 256 x bn tile between its two CTAs)
   const int box_k = p->bk / p->ka;
   if (!array_mode && A != p->tm_A) {
-    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, box_k, tst::kBlockM, p->box3d ? p->ka : 0))
+    // the multicast instance loads A by one 2-D box per atom (each CTA sends one atom)
+    if (!encode_operand(&p->tmap_a, A, p->dtype, p->M, p->K, box_k, tst::kBlockM, p->box3d && p->mc == 1 ? p->ka : 0))
       return TST_ERR_CUDA;
     p->tm_A = A;
   }
@@ -855,6 +876,8 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
     x.d_scale = e.d_scale ? ea->d_scale : nullptr;
     x.amax = e.amax ? ea->amax : nullptr;
     x.aux = e.aux ? ea->aux : nullptr;
+    x.block_exp = e.block_scale ? ea->block_exp : nullptr;
+    x.block_cols = static_cast<int32_t>(ceil_div(p->N, 32));
   }
   kp.debug_flags = p->debug_flags;
   kp.max_items = p->max_items;
@@ -874,16 +897,16 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
     return TST_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg * p->mc), 1, 1);
   cfg.blockDim = dim3(tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   unsigned na = 0;
-  if (p->cg == 2) {
-    // the two CTAs of a pair run as a cluster of 2 (co-scheduled on a pair of SMs)
+  if (p->cg * p->mc > 1) {
+    // a pair (and its multicast neighbour) run as one cluster, co-scheduled on neighbouring SMs
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.x = p->cg * p->mc;
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
@@ -973,7 +996,8 @@ tst_status gemm_grouped_array_plan_create(tst_plan** plan, int32_t groups, const
     return TST_ERR_INVALID_ARG;
   if (dtype < TST_BF16 || dtype > TST_E5M2_E4M3) return TST_ERR_INVALID_ARG;
   // only epilogue operations without per-element operands: each group has its own output
-  if (epi->bias_mode != TST_BIAS_NONE || epi->has_c || epi->row_scale || epi->col_scale || epi->aux)
+  if (epi->bias_mode != TST_BIAS_NONE || epi->has_c || epi->row_scale || epi->col_scale || epi->aux ||
+      epi->block_scale)
     return TST_ERR_UNSUPPORTED;
   const int elt = dtype == TST_BF16 ? 2 : 1;
   std::vector<int32_t> shapes(4 * static_cast<size_t>(groups), 0);
@@ -1122,6 +1146,7 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
     if (a.bias && e.bias_mode == TST_BIAS_ROW) a.bias += r0;
     if (a.row_scale) a.row_scale += r0;
     if (a.aux) a.aux = static_cast<char*>(a.aux) + r0 * N * (e.aux_dtype == TST_OUT_F32 ? 4 : 2);
+    if (a.block_exp) a.block_exp += (r0 / 32) * ceil_div(N, 32);   // panels start on 32-row tiles
     return a;
   };
   // every panel plan exists before anything is enqueued

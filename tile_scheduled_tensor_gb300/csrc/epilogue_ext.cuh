@@ -13,6 +13,13 @@
 //   e4m3 (round to nearest even, saturating to +-448: "H100 . WGMMA Part 2",
 //   section 10's clamping mode)                                       (step 7)
 //
+// or, for an e4m3 D with block scale factor generation (section 12.1's
+// block-scaling workflow; "H100 . WGMMA Part 2", section 11's 32 x 32 tiles): a
+// warp's 32-column chunk covers one 32 x 32 tile of D (its 32 lanes hold 32
+// consecutive rows), so the warp reduces the tile's max |Y|, derives the
+// power-of-two scale 2^E, E = floor(log2 max) - 8, from the FP32 bits, writes
+// e4m3(Y * 2^-E) and lane 0 records E.
+//
 // All arithmetic is FP32.  Row-major matrices (C, aux, D) use 16-byte vector
 // accesses when the chunk is whole and every row starts 16-byte aligned;
 // per-column FP32 vectors use 16-byte loads that every lane of a warp shares.
@@ -256,6 +263,80 @@ __device__ __forceinline__ float chunk_t(const EpiExt& e, const float* bias, flo
     for (int j = 0; j < W; ++j) y[j] *= d;
   }
   store_row_t<W, OUT>(D, row, N, col0, full, y);
+  return amax;
+}
+
+// E = floor(log2(m)) - 8 for the FP32 bit pattern of a non-negative maximum m (0 for an
+// all-zero tile; 0 for an infinite or NaN maximum, which finite inputs do not produce)
+__device__ __forceinline__ int32_t block_exponent(uint32_t m_bits) {
+  if (m_bits == 0u) return 0;
+  const int32_t field = static_cast<int32_t>(m_bits >> 23);
+  if (field >= 0xFF) return 0;
+  const int32_t fl = field > 0 ? field - 127 : (31 - __clz(m_bits & 0x7FFFFFu)) - 149;   // subnormal: mant * 2^-149
+  return fl - 8;
+}
+
+// y * 2^k exactly for the k a block scale needs (-119 <= k <= 157): one power-of-two
+// factor when it is a normal FP32 number, else two
+__device__ __forceinline__ float mul_pow2(float y, int32_t k) {
+  if (k >= -126 && k <= 127) return y * __int_as_float((k + 127) << 23);
+  const int32_t k1 = k / 2, k2 = k - k1;
+  return (y * __int_as_float((k1 + 127) << 23)) * __int_as_float((k2 + 127) << 23);
+}
+
+// One 32-column chunk of an e4m3 D with block scale factor generation.  All 32 lanes of
+// the warp call it with the same col0 and consecutive rows (lane 0's row a multiple of
+// 32): together they hold one 32 x 32 tile of D.  Lanes whose row is past M compute but
+// neither read nor write row data.  Returns the updated amax.
+template <int ACT>
+__device__ __forceinline__ float chunk_block_e4m3(const EpiExt& e, const float* bias, float s_row, float b_row,
+                                                  int32_t M, int32_t N, int32_t row, int32_t col0, const float* v,
+                                                  void* D, float amax) {
+  constexpr int W = 32;
+  const bool row_ok = row < M;
+  const bool full = col0 + W <= N;
+  float z[W];
+  if (e.col_scale) {
+    float cs[W];
+    load_vec<W>(e.col_scale, N, col0, full, cs);
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = (s_row * cs[j]) * v[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = s_row * v[j];
+  }
+  if (e.c_in != nullptr && row_ok) {
+    float c[W];
+    load_row<W>(e.c_type, e.c_in, row, N, col0, full, c);
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] = fmaf(e.beta, c[j], z[j]);
+  }
+  if (e.bias_mode == BIAS_COL) {
+    float b[W];
+    load_vec<W>(bias, N, col0, full, b);
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] += b[j];
+  } else if (e.bias_mode == BIAS_ROW) {
+#pragma unroll
+    for (int j = 0; j < W; ++j) z[j] += b_row;
+  }
+  if (e.aux != nullptr && row_ok) store_row<W>(e.aux_type, e.aux, row, N, col0, full, z);
+  float y[W];
+  float m = 0.0f;   // this lane's max |Y| over the tile's valid elements
+#pragma unroll
+  for (int j = 0; j < W; ++j) {
+    y[j] = activate_t<ACT>(z[j]);
+    if (row_ok && col0 + j < N) m = fmaxf(m, fabsf(y[j]));
+  }
+  if (e.amax != nullptr) amax = fmaxf(amax, m);
+  // non-negative FP32 values order like their bit patterns: the warp's max is the tile's
+  const int32_t E = block_exponent(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m)));
+#pragma unroll
+  for (int j = 0; j < W; ++j) y[j] = mul_pow2(y[j], -E);
+  if (row_ok) store_row_t<W, OUT_E4M3>(D, row, N, col0, full, y);
+  // a chunk past the last column (the rest of a ragged tile) is no tile of D
+  if ((threadIdx.x & 31) == 0 && row_ok && col0 < N)
+    e.block_exp[static_cast<int64_t>(row >> 5) * e.block_cols + (col0 >> 5)] = E;
   return amax;
 }
 

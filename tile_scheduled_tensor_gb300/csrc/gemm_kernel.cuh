@@ -72,12 +72,17 @@ struct SharedCtl {
   uint32_t pad;
 };
 
-// Per-CTA context shared by the roles.
+// Per-CTA context shared by the roles.  A scheduling unit is a cluster of CG x MC CTAs:
+// CG = 2 pairs two CTAs along M on one MMA (ranks 2i, 2i + 1), MC = 2 puts two of those
+// side by side along N, sharing A by multicast loads.
 struct Ctx {
   volatile uint32_t* abort;
-  uint32_t peer_abort;  // shared::cluster address of the peer's abort flag (pairs only)
-  uint32_t rank;        // 0 = leader / single CTA, 1 = peer
-  int32_t unit;         // scheduling unit: the CTA (CG = 1) or the CTA pair (CG = 2)
+  uint32_t abort_addr;  // shared address of this CTA's abort flag (mapped to the others' by mapa)
+  uint32_t rank;        // rank in the cluster; 0 = leader / single CTA
+  uint32_t rank_m;      // rank % CG: 0 = the pair's MMA issuer, 1 = its peer
+  uint32_t rank_n;      // rank / CG: which BN-column part of the scheduled tile
+  uint32_t csize;       // CTAs in the cluster (CG x MC)
+  int32_t unit;         // scheduling unit: the cluster
 };
 
 // Record `code` in the status word unless a launch of the current status window (run ids
@@ -101,7 +106,8 @@ __device__ __forceinline__ void record_status(const KernelParams& p, uint32_t co
 template <int CG>
 __device__ __forceinline__ void raise_error(const KernelParams& p, const Ctx& c, uint32_t code, uint32_t role) {
   *c.abort = 1u;
-  if (CG == 2) ptx::st_cluster_u32(c.peer_abort, 1u);
+  for (uint32_t r = 0; r < c.csize; ++r)   // every CTA of the cluster leaves its loops
+    if (r != c.rank) ptx::st_cluster_u32(ptx::mapa(c.abort_addr, r), 1u);
   record_status(p, code, role);
 }
 
@@ -173,17 +179,22 @@ __device__ __forceinline__ bool wait_lock_at_least(const KernelParams& p, const 
 }
 
 // ------------------------------------------------------------------ producer
-template <int BN, int DT, int CG, int KA>
+template <int BN, int DT, int CG, int KA, int MC>
 __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c, uint32_t smem_a, uint32_t smem_b,
                                              uint32_t bar_full, uint32_t bar_empty) {
   using Cfg = TileCfg<BN, CG, KA>;
   constexpr int BK_ATOM = DT == DT_BF16 ? 64 : 128;   // K elements per 128-byte swizzle atom
   constexpr int BK = BK_ATOM * KA;
-  constexpr int BM_UNIT = kBlockM * CG;   // rows of the scheduled tile
   constexpr int BN_CTA = BN / CG;         // B rows this CTA loads
+  // MC = 2: the two CTAs of the cluster compute side-by-side tiles of the same rows, so
+  // each loads one K atom of their common A tile and multicasts it to both
+  constexpr bool MCAST = MC > 1;
+  static_assert(!MCAST || (CG == 1 && KA == MC), "multicast: single CTAs, one atom of A per CTA");
+  const uint16_t mc_mask = static_cast<uint16_t>((1u << MC) - 1u);
   // pairs: both CTAs' loads complete on the leader's FULL barriers
-  const uint32_t full_target = CG == 2 ? ptx::mapa(bar_full, 0) : bar_full;
-  const bool leader = c.rank == 0;
+  const uint32_t full_target = CG == 2 ? ptx::mapa(bar_full, c.rank & ~1u) : bar_full;
+  const bool leader = c.rank == 0;          // the cluster's first CTA: trace and status records
+  const bool bar_owner = c.rank_m == 0;     // the CTA whose FULL barriers count this CTA's bytes
   int stage = 0;
   uint32_t phase = 0;
   uint32_t issued = 0, issued_parity = 0;  // per stage: a load was issued / parity of that phase
@@ -213,8 +224,9 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
     if ((w.flags & ITEM_CLAMPED) && leader)
       record_status(p, ST_DEVICE_CHECK, ROLE_PRODUCER);
     const bool narrow = (w.flags & ITEM_NARROW) != 0;   // half-width tile: half of B per stage
-    const int32_t m0 = w.row0 + static_cast<int32_t>(c.rank) * kBlockM;    // row of A
-    const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (narrow ? BN_CTA / 2 : BN_CTA);   // row of B
+    const int32_t m0 = w.row0 + static_cast<int32_t>(c.rank_m) * kBlockM;    // row of A
+    const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank_n) * BN +
+                       static_cast<int32_t>(c.rank_m) * (narrow ? BN_CTA / 2 : BN_CTA);   // row of B
     // groups of different shapes: the item's group has its own tensor maps (A at 2g, B at 2g + 1)
     const bool own_maps = p.sched.group_shapes != nullptr;
     const CUtensorMap* tmap_a = own_maps ? p.group_tmaps + 2 * w.group : &p.tmap_a;
@@ -228,7 +240,7 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
       const long long t0 = p.stats ? clock64() : 0;
       if (!wait_phase<CG>(p, c, bar_empty + 8 * stage, phase ^ 1u, ROLE_PRODUCER)) { ok = false; break; }
       if (p.stats) wait_empty += clock64() - t0;
-      if (leader) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * stage_bytes);
+      if (bar_owner) ptx::mbar_arrive_expect_tx(bar_full + 8 * stage, CG * stage_bytes);
       const bool skip = (p.debug_flags & DBG_SKIP_LOAD) && seq == 0 && kb == w.k_begin;
       if (!skip) {
         // a pair's loads complete on the leader's FULL barrier
@@ -247,7 +259,18 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
         };
         const uint32_t sa = smem_a + stage * Cfg::A_BYTES;
         const uint32_t sb = smem_b + stage * Cfg::B_BYTES;
-        if (KA > 1 && p.box3d) {
+        if constexpr (MCAST) {
+          // A: this CTA's atom column of the shared 128-row tile, into the same stage offset
+          // of both CTAs, counted on each one's FULL barrier; B: this CTA's own rows
+          ptx::tma_load_2d_mc(sa + c.rank_n * Cfg::A_SUB, tmap_a, bar_full + 8 * stage,
+                              kb * BK + static_cast<int32_t>(c.rank_n) * BK_ATOM, m0, mc_mask);
+          if (p.box3d) {
+            load3(sb, tmap_b, n0, kb * KA, pol_b);
+          } else {
+#pragma unroll
+            for (int a = 0; a < KA; ++a) load2(sb + a * Cfg::B_SUB, tmap_b, kb * BK + a * BK_ATOM, n0, pol_b);
+          }
+        } else if (KA > 1 && p.box3d) {
           // one 3-D box per operand: the KA atom columns land at KA consecutive sub-tiles,
           // the same image as KA 2-D boxes, in fewer requests.  A half-width B (HyTiS)
           // keeps its 2-D boxes at the full-width sub-tile stride.
@@ -274,10 +297,11 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
   // every load of this CTA is issued: a dependent grid may be scheduled
   if (p.pdl) ptx::griddep_launch_dependents();
   if (p.stats) p.stats[blockIdx.x * kStatSlots + STAT_PROD_WAIT_EMPTY] = wait_empty;
-  if (!ok && leader) {
+  if (!ok && bar_owner) {
     // aborting: wait (bounded) until the loads already issued have landed.  For a
     // pair the leader's FULL barrier counts both CTAs' bytes, and the peer stays
-    // alive at the final cluster barrier until the leader gets there.
+    // alive at the final cluster barrier until the leader gets there; with multicast
+    // each CTA's barrier also counts the atom its neighbour sends it.
     const uint64_t t0 = ptx::globaltimer();
     for (int s = 0; s < p.stages; ++s) {
       if (!(issued & (1u << s))) continue;
@@ -293,7 +317,7 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
 // Issuer `issuer` of Cfg::ISSUERS: with two issuers, issuer r issues the MMAs of
 // swizzle atom r of every k-tile into its own accumulator (columns r * BN of the
 // buffer); the epilogue adds the two.
-template <int BN, int DT, int CG, int KA>
+template <int BN, int DT, int CG, int KA, int MC>
 __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uint32_t tmem_base, uint32_t smem_a,
                                         uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty, uint32_t bar_tfull,
                                         uint32_t bar_tempty, uint32_t bar_drain, int issuer) {
@@ -349,8 +373,11 @@ __device__ __forceinline__ void run_mma(const KernelParams& p, const Ctx& c, uin
           else ptx::mma_f8(d_tmem, a_desc + off, b_desc + off_b, idesc, accumulate);
         }
       }
-      // stage free (in both CTAs of a pair) once these MMAs have read it
+      // stage free (in both CTAs of a pair) once these MMAs have read it; with multicast a
+      // CTA's stage is written by both CTAs of the cluster, so each one's EMPTY counts both
+      // CTAs' commits
       if (CG == 2) ptx::mma_commit_pair_mc(bar_empty + 8 * stage, 0x3);
+      else if (MC > 1) ptx::mma_commit_mc(bar_empty + 8 * stage, static_cast<uint16_t>((1u << MC) - 1u));
       else ptx::mma_commit(bar_empty + 8 * stage);
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
@@ -417,7 +444,7 @@ __device__ __forceinline__ void store_chunk(void* out, int32_t ncols, int32_t ro
 }
 
 // ACT and DOUT (activation and D's type) specialise the extended epilogue (OUT == OUT_EXT)
-template <int BN, int OUT, int CG, int KA, int ACT = ACT_NONE, int DOUT = OUT_F32>
+template <int BN, int OUT, int CG, int KA, int MC = 1, int ACT = ACT_NONE, int DOUT = OUT_F32>
 __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
                                              uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
   using Cfg = TileCfg<BN, CG, KA>;
@@ -435,7 +462,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   const int quad = warp & 3;                   // TMEM lane quadrant this warp may access
   const int row_in_tile = quad * 32 + lane;
   // pairs: arrive on the leader's TMEM_EMPTY barriers
-  const uint32_t tempty_target = CG == 2 ? ptx::mapa(bar_tempty, 0) : bar_tempty;
+  const uint32_t tempty_target = CG == 2 ? ptx::mapa(bar_tempty, c.rank & ~1u) : bar_tempty;
   // SK_TMA: this warpgroup's staging buffer for one 128 x 32 FP32 chunk ([column][row]), and
   // the thread that issues its bulk copies
   const bool tma_fixup = p.sk_mode == SK_TMA;
@@ -461,7 +488,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     // Stream-K slot of this CTA's half of the tile (valid when fixup); the separate
     // reduction gives every split of the half its own slot, indexed by the unit's
     // member number relative to the tile's first member
-    int32_t slot = (w.tile - p.sched.dp_tiles) * CG + static_cast<int32_t>(c.rank);
+    int32_t slot = (w.tile - p.sched.dp_tiles) * CG * MC + static_cast<int32_t>(c.rank);
     if (fixup && separate) {
       int32_t grp, m_first, m_last;
       int64_t t_lo, t_hi;
@@ -490,7 +517,8 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
     __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
     ptx::tc_fence_after();
 
-    const int32_t row = w.row0 + static_cast<int32_t>(c.rank) * kBlockM + row_in_tile;
+    const int32_t row = w.row0 + static_cast<int32_t>(c.rank_m) * kBlockM + row_in_tile;
+    const int32_t cta_col0 = w.col0 + static_cast<int32_t>(c.rank_n) * BN;   // this CTA's first column
     const uint32_t t_row =
         tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * BN * Cfg::ISSUERS);
     float* ws = fixup ? p.workspace + static_cast<int64_t>(slot) * (kBlockM * BN) : nullptr;
@@ -565,8 +593,15 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[32 * h + j] = __ldcg(wsc + j * kBlockM) + v[32 * h + j];
         }
-        const int32_t col0 = w.col0 + c32 * 32;
+        const int32_t col0 = cta_col0 + c32 * 32;
         if constexpr (EXT) {
+          if constexpr (DOUT == OUT_E4M3) {
+            if (p.ext.block_exp != nullptr) {   // the warp's chunk is one 32 x 32 tile of D
+              amax = epi::chunk_block_e4m3<ACT>(p.ext, p.bias, s_row, b_row, w.row_end, w.col_end, row, col0,
+                                                v + 32 * h, out, amax);
+              continue;
+            }
+          }
           amax = epi::chunk_t<32, ACT, DOUT>(p.ext, p.bias, s_row, b_row, w.row_end, w.col_end, row, col0,
                                              v + 32 * h, out, amax);
           continue;
@@ -634,9 +669,9 @@ template <int BN, int CG, int KA, int ACT>
 __device__ __forceinline__ void run_epilogue_ext_act(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
                                                      uint32_t bar_tfull, uint32_t bar_tempty, SharedCtl* ctl) {
   switch (p.ext.out_type) {
-    case OUT_BF16: run_epilogue<BN, OUT_EXT, CG, KA, ACT, OUT_BF16>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
-    case OUT_E4M3: run_epilogue<BN, OUT_EXT, CG, KA, ACT, OUT_E4M3>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
-    default: run_epilogue<BN, OUT_EXT, CG, KA, ACT, OUT_F32>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    case OUT_BF16: run_epilogue<BN, OUT_EXT, CG, KA, 1, ACT, OUT_BF16>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    case OUT_E4M3: run_epilogue<BN, OUT_EXT, CG, KA, 1, ACT, OUT_E4M3>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
+    default: run_epilogue<BN, OUT_EXT, CG, KA, 1, ACT, OUT_F32>(p, c, tmem_base, bar_tfull, bar_tempty, ctl); break;
   }
 }
 
@@ -652,10 +687,11 @@ __device__ __forceinline__ void run_epilogue_ext(const KernelParams& p, const Ct
 }
 
 // ------------------------------------------------------------------ kernel
-template <int BN, int DT, int OUT, int CG, int KA>
+template <int BN, int DT, int OUT, int CG, int KA, int MC = 1>
 __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EXT ? 2 : 1), 1)
     gemm_tcgen05_kernel(const __grid_constant__ KernelParams p) {
   using Cfg = TileCfg<BN, CG, KA>;
+  constexpr int CSIZE = CG * MC;   // CTAs per cluster (scheduling unit)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t smem_a = ptx::smem_addr(smem);
@@ -672,14 +708,17 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
 
   Ctx c;
   c.abort = &ctl->abort;
-  c.rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
-  c.peer_abort = CG == 2 ? ptx::mapa(ptx::smem_addr(&ctl->abort), c.rank ^ 1u) : 0u;
-  c.unit = static_cast<int32_t>(blockIdx.x) / CG;
+  c.abort_addr = ptx::smem_addr(&ctl->abort);
+  c.rank = CSIZE > 1 ? ptx::cluster_ctarank() : 0u;
+  c.rank_m = c.rank % CG;
+  c.rank_n = c.rank / CG;
+  c.csize = CSIZE;
+  c.unit = static_cast<int32_t>(blockIdx.x) / CSIZE;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::STAGES; ++s) {
       ptx::mbar_init(bar_full + 8 * s, 1);
-      ptx::mbar_init(bar_empty + 8 * s, Cfg::ISSUERS);   // one commit per MMA issuer
+      ptx::mbar_init(bar_empty + 8 * s, Cfg::ISSUERS * MC);   // one commit per MMA issuer of each CTA writing it
     }
     for (int b = 0; b < Cfg::NACC; ++b) {
       ptx::mbar_init(bar_tfull + 8 * b, Cfg::ISSUERS);
@@ -704,7 +743,7 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (CG == 2) ptx::cluster_sync();  // the peer's barriers exist before anyone signals them
+  if (CSIZE > 1) ptx::cluster_sync();  // the other CTAs' barriers exist before anyone signals them
   ptx::tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -718,7 +757,7 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
       work_begin(p.sched, c.unit, it);
       if (work_next(p.sched, it, w)) {
         constexpr int BK = (DT == DT_BF16 ? 64 : 128) * KA;
-        const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank) * (BN / CG);
+        const int32_t n0 = w.b_row0 + static_cast<int32_t>(c.rank_n) * BN + static_cast<int32_t>(c.rank_m) * (BN / CG);
         const int32_t kend = w.k_begin + (w.k_count < p.stages ? w.k_count : p.stages);
         for (int32_t kb = w.k_begin; kb < kend; ++kb) {
           if (p.box3d && KA > 1) ptx::tma_prefetch_l2_3d(&p.tmap_b, 0, n0, kb * KA);
@@ -731,24 +770,24 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
   }
 
   if (warp == 0) {
-    if (lane == 0) run_producer<BN, DT, CG, KA>(p, c, smem_a, smem_b, bar_full, bar_empty);
+    if (lane == 0) run_producer<BN, DT, CG, KA, MC>(p, c, smem_a, smem_b, bar_full, bar_empty);
   } else if (warp == 1 || (Cfg::DUAL && warp == 6)) {  // warp 6: second issuer of dual-issue tiles
     const int issuer = warp == 1 ? 0 : 1;
-    if (lane == 0 && c.rank == 0)
-      run_mma<BN, DT, CG, KA>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty,
-                              bar_drain + 8 * issuer, issuer);
+    if (lane == 0 && c.rank_m == 0)
+      run_mma<BN, DT, CG, KA, MC>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_tfull, bar_tempty,
+                                  bar_drain + 8 * issuer, issuer);
   } else if constexpr (OUT == OUT_EXT) {
     run_epilogue_ext<BN, CG, KA>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   } else {
-    run_epilogue<BN, OUT, CG, KA>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
+    run_epilogue<BN, OUT, CG, KA, MC>(p, c, tmem_base, bar_tfull, bar_tempty, ctl);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
   if (p.stats && threadIdx.x == 0) p.stats[blockIdx.x * kStatSlots + STAT_TOTAL] = clock64() - t_start;
-  // pairs: neither CTA leaves (nor frees TMEM) while the other may still signal
-  // its barriers or the leader's MMAs may still write its TMEM
-  if (CG == 2) ptx::cluster_sync();
+  // clusters: no CTA leaves (nor frees TMEM) while another may still signal its
+  // barriers, write its shared memory, or (pairs) the leader's MMAs its TMEM
+  if (CSIZE > 1) ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
@@ -757,10 +796,10 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
   }
 }
 
-template <int BN, int DT, int CG, int KA>
+template <int BN, int DT, int CG, int KA, int MC = 1>
 const void* select_kernel(int out_type) {
-  if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16, CG, KA>);
-  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32, CG, KA>);
+  if (out_type == OUT_BF16) return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_BF16, CG, KA, MC>);
+  return reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, DT, OUT_F32, CG, KA, MC>);
 }
 
 template <int BN, int DT, int CG, int KA>

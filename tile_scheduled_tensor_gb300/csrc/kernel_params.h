@@ -38,6 +38,9 @@ struct EpiExt {
   const float* d_scale;      // FP32[1] or null
   float* amax;               // FP32[1] or null
   void* aux;                 // M x N row-major (pre-activation Z), or null
+  int32_t* block_exp;        // block scale factor generation (e4m3 D): int32 exponent E of each
+                             // 32 x 32 tile of D, ceil(M / 32) x block_cols row-major, or null
+  int32_t block_cols;        // ceil(N / 32)
 };
 
 // device status word: code (bits 0-7) | role (8-15) | CTA (16-31)
@@ -150,6 +153,10 @@ const void* tst_kernel_bf16_cg2_ka2(int bn, int out_type);
 const void* tst_kernel_e4m3_cg1_ka2(int bn, int out_type);
 const void* tst_kernel_e4m3_cg2_ka2(int bn, int out_type);
 
+// clusters of two single CTAs along N sharing A by multicast (gemm_<dtype>_cg1_ka2_mc2.cu)
+const void* tst_kernel_bf16_cg1_ka2_mc2(int bn, int out_type);
+const void* tst_kernel_e4m3_cg1_ka2_mc2(int bn, int out_type);
+
 const void* tst_kernel_ext_bf16_cg1_ka1(int bn);
 const void* tst_kernel_ext_bf16_cg2_ka1(int bn);
 const void* tst_kernel_ext_e4m3_cg1_ka1(int bn);
@@ -169,7 +176,12 @@ inline const void* tst_kernel_ext(int dtype, int bn, int cg, int ka) {
   return cg == 2 ? tst_kernel_ext_e4m3_cg2_ka1(bn) : tst_kernel_ext_e4m3_cg1_ka1(bn);
 }
 
-inline const void* tst_kernel(int dtype, int bn, int out_type, int cg, int ka) {
+// mc = 2: the multicast instance (cg 1, ka 2 only), else the plain one
+inline const void* tst_kernel(int dtype, int bn, int out_type, int cg, int ka, int mc = 1) {
+  if (mc == 2) {
+    if (cg != 1 || ka != 2) return nullptr;
+    return dtype == tst::DT_BF16 ? tst_kernel_bf16_cg1_ka2_mc2(bn, out_type) : tst_kernel_e4m3_cg1_ka2_mc2(bn, out_type);
+  }
   if (ka == 2) {
     if (dtype == tst::DT_BF16)
       return cg == 2 ? tst_kernel_bf16_cg2_ka2(bn, out_type) : tst_kernel_bf16_cg1_ka2(bn, out_type);

@@ -434,6 +434,29 @@ __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_ma
       : "memory");
 }
 
+// TMA tile load whose data and completion are delivered to every CTA of ctaMask in this
+// cluster: the box lands at shared offset `dst` and its bytes are counted on the mbarrier
+// at offset `bar`, both taken relative to each destination CTA ("H100 . cp.async.bulk",
+// sections 8 and 11: one load feeds the CTAs of a cluster that need the same tile).
+// The tensor map addresses this GPU's own memory.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t c0,
+                                               int32_t c1, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+// single-CTA MMAs: arrive on the mbarrier at this shared offset in every CTA of ctaMask
+// once the MMAs issued so far by this thread complete
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
