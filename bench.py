@@ -52,6 +52,10 @@ DESCR = {
     "c2_bf16_4096": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 CTA tiles in 2x1 CTA pairs, grouped-M G=8, "
                     "persistent",
     "c2_bf16_4096_1cta": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 tiles, one CTA each, grouped-M G=8, persistent",
+    "c2_bf16_4096_mc": "BF16 GEMM 4096^3, N(0,1), BF16 out, 128x128 tiles, one CTA each, in clusters of two along N "
+                       "sharing A by TMA multicast, grouped-M G=8, persistent",
+    "c4_bf16_streamk_mc": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 128x128 tiles, one CTA each, in clusters "
+                          "of two along N sharing A by TMA multicast (120 scheduled 128x256 tiles), Stream-K",
     "c2x_bf16_8192": "BF16 GEMM 8192^3, N(0,1), BF16 out, grouped-M G=8, persistent",
     "c3_e4m3_8192": "FP8-e4m3 GEMM 8192^3, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, persistent",
     "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles of 128x128, one CTA each, "
@@ -83,7 +87,7 @@ MAX_SETS = 16             # more input sets than this: flush L2 before every lau
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
 
 
-PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint", "tma_boxes")
+PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint", "tma_boxes", "cluster_n")
 
 
 def extra_plan_options(w):
@@ -325,7 +329,8 @@ def workload_config(name, world=1, split="replicas"):
     cfg = {"workload": f"{name}: {DESCR[name]}", "M": w["M"], "N": w["N"], "K": w["K"], "dtype": w["dtype"],
            "out": w["out"], "mapping": f"{w['mapping'][0]}:{w['mapping'][1]}", "schedule": w["schedule"],
            "cta_tile": f"128x{w['bn']}" if w.get("bn") else "auto",
-           "scheduled_tile": f"{128 * w['cta_group']}x{w['bn']}" if w.get("bn") and w.get("cta_group") else "auto",
+           "scheduled_tile": (f"{128 * w['cta_group']}x{w['bn'] * w.get('cluster_n', 1)}"
+                              if w.get("bn") and w.get("cta_group") else "auto"),
            "cta_group": w.get("cta_group", 0), "accumulate": "fp32", "l2": l2_policy(w),
            "parallelism": (f"{world} independent problem(s), one per GPU" if split == "replicas"
                            else f"rows of one problem split over {world} GPU(s), B replicated")}
@@ -589,7 +594,7 @@ def band_model(plan, elt_bytes, K, l2_bytes=64 << 20):
     import tile_scheduled_tensor_gb300 as tst
     info = plan.info
     T, P = int(info.tiles), int(info.grid)
-    band = {"A": info.bm * K * elt_bytes, "B": info.bn * K * elt_bytes}
+    band = {"A": info.bm * K * elt_bytes, "B": info.bn * info.cluster_n * K * elt_bytes}
     lru, used, dram, per_wave = OrderedDict(), 0, 0, []
     for w0 in range(0, T, P):
         keys = set()

@@ -18,6 +18,9 @@ WORKLOADS = {
     # the same problem with one CTA per 128x128 tile (no pairing)
     "c2_bf16_4096_1cta": dict(M=4096, N=4096, K=4096, dtype="bf16", dist="normal", case=2, out="bf16",
                               mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),
+    # the same problem with single CTAs in clusters of two along N sharing A by TMA multicast
+    "c2_bf16_4096_mc": dict(M=4096, N=4096, K=4096, dtype="bf16", dist="normal", case=2, out="bf16",
+                            mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1, cluster_n=2),
     # 8192^3 BF16 -> BF16, N(0,1), grouped-M G=8, persistent (BF16 target size)
     "c2x_bf16_8192": dict(M=8192, N=8192, K=8192, dtype="bf16", dist="normal", case=2, out="bf16",
                           mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2),
@@ -34,6 +37,10 @@ WORKLOADS = {
                                   mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=2),
     "c4_bf16_hybrid_pairs": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                                  mapping=("grouped_m", 8), schedule="streamk_hybrid", bn=128, cta_group=2),
+    # the same problem with single CTAs in clusters of two along N that share A by TMA
+    # multicast (120 scheduled 128x256 tiles), Stream-K
+    "c4_bf16_streamk_mc": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
+                               mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=1, cluster_n=2),
     # the same problem, grouped-M G=8 persistent (the data-parallel comparison)
     "c4_bf16_persistent": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                                mapping=("grouped_m", 8), schedule="persistent", bn=128, cta_group=1),
