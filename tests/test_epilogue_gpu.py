@@ -134,13 +134,32 @@ def _bounds(e, acc, ad, act):
 
 
 def act_eval_error(act, Z, Y):
-    """Error of the kernel's FP32 evaluation of the activation at a given Z: a few roundings
-    for identity and ReLU; for GELU (Phi by Abramowitz & Stegun 26.2.17, absolute error
-    below 7.5e-8) and SiLU (fast exponential and divide) the implementations' measured
-    bounds, 2e-7 max(1, |z|) absolute plus 16 ulp relative."""
-    if act in (E.ACT_GELU, E.ACT_SILU):
-        return 16 * FP32_EPS * np.abs(Y) + 2e-7 * np.maximum(1.0, np.abs(Z))
-    return 8 * FP32_EPS * np.abs(Y)
+    """Error of the kernel's FP32 evaluation of the activation at a given Z, derived from
+    documented error bounds (u = 2^-23, the FP32 unit roundoff being u / 2):
+
+    * identity, ReLU: a few roundings, 8 u |y|.
+    * SiLU, computed as __fdividef(z, 1 + __expf(-z)).  The CUDA Programming Guide bounds
+      __expf(x) by 2 + floor(|1.173 x|) ulp and __fdividef by 2 ulp for divisors up to
+      2^126 (above it the result is 0).  With E = e^-z the exact result is z / (1 + E); the
+      computed one has relative error at most (2 + 1.173 |z|) u E / (1 + E) (the exponential
+      error, damped by E / (1 + E) = sigmoid(-z) in the sum) + u / 2 (the sum's rounding)
+      + 2 u (the divide), plus second order: the bound below takes (2 + 1.173 |z|) u
+      sigmoid(-z) + 4 u relative, and 1e-30 absolute for z below -87.3, where the result
+      is 0 and the exact one is below 1e-36.
+    * GELU, computed as z Phi(z) with Phi by Abramowitz & Stegun 26.2.17 (absolute error
+      below 7.5e-8 in exact arithmetic).  Its FP32 evaluation q = c e^(-u^2/2) P(t) has
+      relative error below (6 + 2 + 0.59 z^2 + 4) u: Horner's four fused steps on a
+      polynomial whose |terms| sum to at most 4.5 |P| (~6 u with the coefficients'
+      roundings), the divide and fma forming t, the exponential (2 + 1.173 z^2 / 2 ulp),
+      and the products; since q <= 1/2 and z^2 e^(-z^2/2) <= 0.74, the absolute error of
+      Phi is below 7.5e-8 + 8 u, doubled here for margin: |z| (7.5e-8 + 16 u) + u |y|."""
+    u = FP32_EPS
+    if act == E.ACT_SILU:
+        sig = 1.0 / (1.0 + np.exp(np.minimum(Z, 700.0)))      # sigmoid(-z)
+        return np.abs(Y) * ((2.0 + 1.173 * np.abs(Z)) * u * sig + 4.0 * u) + 1e-30
+    if act == E.ACT_GELU:
+        return np.abs(Z) * (7.5e-8 + 16.0 * u) + u * np.abs(Y)
+    return 8 * u * np.abs(Y)
 
 
 def _assert_bracket(got, want, tol, out, what):
