@@ -87,7 +87,8 @@ MAX_SETS = 16             # more input sets than this: flush L2 before every lau
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
 
 
-PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint", "tma_boxes", "cluster_n")
+PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint", "tma_boxes", "cluster_n",
+                    "epilogue_store")
 
 
 def extra_plan_options(w):

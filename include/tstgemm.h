@@ -282,7 +282,19 @@ typedef struct {
                               epilogue, one GEMM (not grouped), no HyTiS and no separate
                               Stream-K reduction (TST_ERR_UNSUPPORTED otherwise).  The result is
                               bit for bit that of the same plan without multicast. */
+    int32_t epilogue_store; /* how the basic epilogue writes D.  TST_STORE_TMA: each epilogue warp
+                              stages its 32 x 32 chunk of D in shared memory (swizzled) and one
+                              thread stores it with a bulk tensor copy ("H100 . Kernel Design"
+                              section 12.2's registers -> shared memory -> TMA store flow); needs an
+                              FP32 or BF16 D whose rows are multiples of 16 bytes, one GEMM, the
+                              basic epilogue and a fixup other than TMA (TST_ERR_UNSUPPORTED
+                              otherwise).  TST_STORE_DIRECT: 16-byte vector stores from registers.
+                              TST_STORE_AUTO (default): TMA stores where they apply and their
+                              staging fits beside a full ring, else direct.  Same results either
+                              way. */
 } tst_plan_options;
+
+enum { TST_STORE_AUTO = 0, TST_STORE_DIRECT = 1, TST_STORE_TMA = 2 };
 
 enum { TST_SK_DETERMINISTIC = 0, TST_SK_ATOMIC = 1, TST_SK_SEPARATE = 2, TST_SK_TMA = 3 };
 enum { TST_L2_NONE = 0, TST_L2_KEEP_A = 1, TST_L2_KEEP_B = 2, TST_L2_AUTO = 3 };
@@ -311,6 +323,7 @@ typedef struct {
     int32_t box3d;             /* 1: one 3-D TMA box per operand and stage, 0: 2-D boxes per atom */
     int32_t cluster_n;         /* CTAs along N sharing A by multicast (1 = none); the scheduled
                                   tile is bm x (bn * cluster_n) and nt counts those */
+    int32_t tma_store;         /* 1: D is stored through shared memory by TMA, 0: directly */
 } tst_plan_info;
 
 typedef struct tst_plan tst_plan;

@@ -395,3 +395,26 @@ def test_multicast_plan_rules():
     with pytest.raises(tst.TstError) as e:
         tst.gemm_plan_create(1024, 1024, 1024, bn=128, cta_group=1, host_only=True, num_sms=152, cluster_n=3)
     assert e.value.status == tst.TST_ERR_INVALID_ARG
+
+
+def test_tma_store_plan_rules():
+    kw = dict(host_only=True, num_sms=152, epilogue_store="tma")
+    for out in ("f32", "bf16"):
+        p = tst.gemm_plan_create(1000, 1000, 512, out_dtype=out, **kw)
+        assert p.info.tma_store == 1
+    # the default takes TMA stores where they apply, direct stores elsewhere
+    assert tst.gemm_plan_create(1000, 1000, 512, host_only=True, num_sms=152).info.tma_store == 1
+    assert tst.gemm_plan_create(1000, 1000, 512, host_only=True, num_sms=152,
+                                epilogue_store="direct").info.tma_store == 0
+    assert tst.gemm_plan_create(1000, 1000, 512, host_only=True, num_sms=152,
+                                out_dtype="e4m3").info.tma_store == 0
+    assert tst.gemm_plan_create(1000, 1001, 512, host_only=True, num_sms=152,
+                                out_dtype="bf16").info.tma_store == 0
+    for bad in (dict(out_dtype="e4m3"), dict(out_dtype="bf16", activation="gelu"),
+                dict(out_dtype="f32", schedule="streamk", sk_fixup="tma")):
+        with pytest.raises(tst.TstError) as e:
+            tst.gemm_plan_create(1000, 1000, 512, **bad, **kw)
+        assert e.value.status == tst.TST_ERR_UNSUPPORTED, bad
+    with pytest.raises(tst.TstError) as e:   # BF16 rows of 2002 bytes are not 16-byte multiples
+        tst.gemm_plan_create(1000, 1001, 512, out_dtype="bf16", **kw)
+    assert e.value.status == tst.TST_ERR_UNSUPPORTED

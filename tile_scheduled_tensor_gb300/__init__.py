@@ -38,6 +38,7 @@ _FIXUP = {"deterministic": TST_SK_DETERMINISTIC, "atomic": TST_SK_ATOMIC, "separ
 _L2 = {"none": _capi.TST_L2_NONE, "keep_a": _capi.TST_L2_KEEP_A, "keep_b": _capi.TST_L2_KEEP_B,
        "auto": _capi.TST_L2_AUTO}
 _BOXES = {"auto": _capi.TST_BOXES_AUTO, "2d": _capi.TST_BOXES_2D, "3d": _capi.TST_BOXES_3D}
+_STORE = {"auto": _capi.TST_STORE_AUTO, "direct": _capi.TST_STORE_DIRECT, "tma": _capi.TST_STORE_TMA}
 _SCHED = {"static": TST_STATIC, "persistent": TST_PERSISTENT, "streamk": TST_STREAMK,
           "streamk_hybrid": TST_STREAMK_HYBRID, "hytis": TST_HYTIS}
 
@@ -99,7 +100,7 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      bias_mode=None, activation=None,
                      row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
                      amax: bool = False, aux: bool = False, aux_dtype="f32", block_scale: bool = False,
-                     cluster_n: int = 0) -> Plan:
+                     cluster_n: int = 0, epilogue_store="auto") -> Plan:
     """Plan C = epilogue(A x B).  The basic epilogue is alpha, a column bias (has_bias),
     ReLU and the tensor-wise scales; any of beta/has_c, bias_mode='row', activation
     'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux, block_scale or out_dtype 'e4m3'
@@ -111,7 +112,8 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                                   int(num_sms), int(cta_group), int(timeout_ns), int(stages), int(bk),
                                   int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"), int(bool(pdl)),
                                   _enum(_L2, l2_hint, "l2_hint"),
-                                  _enum(_BOXES, tma_boxes, "tma_boxes"), int(cluster_n))
+                                  _enum(_BOXES, tma_boxes, "tma_boxes"), int(cluster_n),
+                                  _enum(_STORE, epilogue_store, "epilogue_store"))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \

@@ -30,6 +30,7 @@ TST_DEBUG_TRACE, TST_DEBUG_FAULT_SKIP_LOAD, TST_DEBUG_FAULT_SKIP_LOCK, TST_DEBUG
 TST_SK_DETERMINISTIC, TST_SK_ATOMIC, TST_SK_SEPARATE, TST_SK_TMA = 0, 1, 2, 3
 TST_L2_NONE, TST_L2_KEEP_A, TST_L2_KEEP_B, TST_L2_AUTO = 0, 1, 2, 3
 TST_BOXES_AUTO, TST_BOXES_2D, TST_BOXES_3D = 0, 1, 2
+TST_STORE_AUTO, TST_STORE_DIRECT, TST_STORE_TMA = 0, 1, 2
 
 
 class tst_mapping(ctypes.Structure):
@@ -60,7 +61,8 @@ class tst_plan_options(ctypes.Structure):
                 ("host_only", ctypes.c_int32), ("num_sms", ctypes.c_int32), ("cta_group", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_int64), ("stages", ctypes.c_int32), ("bk", ctypes.c_int32),
                 ("sk_groups", ctypes.c_int32), ("sk_fixup", ctypes.c_int32), ("pdl", ctypes.c_int32),
-                ("l2_hint", ctypes.c_int32), ("tma_boxes", ctypes.c_int32), ("cluster_n", ctypes.c_int32)]
+                ("l2_hint", ctypes.c_int32), ("tma_boxes", ctypes.c_int32), ("cluster_n", ctypes.c_int32),
+                ("epilogue_store", ctypes.c_int32)]
 
 
 class tst_plan_info(ctypes.Structure):
@@ -72,7 +74,8 @@ class tst_plan_info(ctypes.Structure):
                 ("max_items_per_cta", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("workspace_bytes", ctypes.c_int64), ("cta_group", ctypes.c_int32), ("ctas", ctypes.c_int32),
                 ("kernels_per_run", ctypes.c_int32), ("sk_slots", ctypes.c_int32),
-                ("l2_hint", ctypes.c_int32), ("box3d", ctypes.c_int32), ("cluster_n", ctypes.c_int32)]
+                ("l2_hint", ctypes.c_int32), ("box3d", ctypes.c_int32), ("cluster_n", ctypes.c_int32),
+                ("tma_store", ctypes.c_int32)]
 
 
 class tst_work_item(ctypes.Structure):

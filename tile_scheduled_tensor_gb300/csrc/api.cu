@@ -66,6 +66,8 @@ struct tst_plan {
   int32_t mc = 1;              // CTAs along N sharing A by multicast (the unit is cg x mc CTAs)
   int32_t sk_mode = 0;         // tst::SkFixup
   int32_t staging_offset = 0;  // SK_TMA staging buffers in shared memory
+  bool tma_store = false;      // the basic epilogue stores D by TMA from shared staging
+  int32_t store_offset = 0;    // ... at this offset of the aligned shared base
   int32_t sk_slots = 1;        // partial slots per split-tile half
   const void* reduce_kernel = nullptr;
   int32_t ka = 1;              // 128-byte swizzle atoms of K per pipeline stage
@@ -94,7 +96,8 @@ struct tst_plan {
   const void* kernel = nullptr;
   const void* tm_A = nullptr;
   const void* tm_B = nullptr;
-  CUtensorMap tmap_a{}, tmap_b{}, tmap_b_half{}, tmap_ws{};
+  const void* tm_C = nullptr;
+  CUtensorMap tmap_a{}, tmap_b{}, tmap_b_half{}, tmap_ws{}, tmap_c{};
   cudaStream_t last_stream = nullptr;
   bool ran = false;
   HostRun* host_run = nullptr;   // gemm_run_host state (created by its first call)
@@ -522,6 +525,28 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
     p->smem_bytes = smem;
     p->stages = std::min(p->stages, max_stages);   // stages whose A region holds the staging stay unused
   }
+  // TMA-store epilogue: two 32 x 32 chunks of D per epilogue warp, staged like the fixup's.
+  // Measured 1.3-2.4 % faster than direct stores on every listed workload, so the default
+  // takes it wherever it applies and its staging fits without taking ring stages.
+  if (o.epilogue_store < TST_STORE_AUTO || o.epilogue_store > TST_STORE_TMA) { delete p; return TST_ERR_INVALID_ARG; }
+  if (o.epilogue_store != TST_STORE_DIRECT) {
+    const int ob = out_bytes(epi->out_dtype);
+    const bool eligible = !p->ext_on && groups == 0 && epi->out_dtype != TST_OUT_E4M3 && (N * ob) % 16 == 0 &&
+                          !(p->sk_mode == TST_SK_TMA && s.sk_tiles > 0);
+    int offset = 0, smem = 0, max_stages = 0;
+    const bool fits = eligible && tst_staging(p->bn, p->cg, p->ka, tst_store_staging_bytes(ob), &offset, &smem,
+                                              &max_stages);
+    if (o.epilogue_store == TST_STORE_TMA && !fits) {
+      delete p;
+      return TST_ERR_UNSUPPORTED;
+    }
+    if (fits && (o.epilogue_store == TST_STORE_TMA || max_stages >= p->stages)) {
+      p->tma_store = true;
+      p->store_offset = offset;
+      p->smem_bytes = smem;
+      p->stages = std::min(p->stages, max_stages);
+    }
+  }
   // dependent launch and a grid whose CTAs wait on each other do not mix
   if (o.pdl && s.sk_tiles > 0 && p->sk_mode != TST_SK_SEPARATE) { delete p; return TST_ERR_UNSUPPORTED; }
   // separate reduction: as many partial slots per split tile as units can touch one tile
@@ -710,6 +735,7 @@ tst_status gemm_plan_get_info(const tst_plan* p, tst_plan_info* info) {
   info->cta_group = p->cg;
   info->ctas = p->sched.grid * p->cg * p->mc;
   info->cluster_n = p->mc;
+  info->tma_store = p->tma_store ? 1 : 0;
   info->kernels_per_run = (p->sk_mode == TST_SK_SEPARATE && p->sched.sk_tiles > 0) ? 2 : 1;
   info->sk_slots = p->sk_slots;
   info->l2_hint = p->opts.l2_hint;
@@ -828,6 +854,22 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
     p->tm_B = B;
   }
 
+  // the TMA-store epilogue's map of D: M x N, 32 x 32 boxes, swizzled to the staging layout
+  if (p->tma_store && C != p->tm_C) {
+    EncodeTiledFn fn = encode_fn();
+    const bool bf16 = e.out_dtype == TST_OUT_BF16;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p->N), static_cast<cuuint64_t>(p->M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(p->N) * (bf16 ? 2 : 4)};
+    cuuint32_t box[2] = {32, static_cast<cuuint32_t>(tst::kStoreChunkRows)};
+    cuuint32_t estr[2] = {1, 1};
+    if (!fn || fn(&p->tmap_c, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TST_ERR_CUDA;
+    p->tm_C = C;
+  }
+
   tst::KernelParams kp = {};
   kp.tmap_a = p->tmap_a;
   kp.tmap_b = p->tmap_b;
@@ -858,6 +900,9 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.use_scales = e.use_scales ? 1 : 0;
   kp.fmt_ab = p->fmt_ab;
   kp.staging_offset = p->staging_offset;
+  kp.tmap_c = p->tmap_c;
+  kp.tma_store = p->tma_store ? 1 : 0;
+  kp.store_offset = p->store_offset;
   kp.pdl = p->opts.pdl;
   kp.l2_hint = p->opts.l2_hint;
   kp.box3d = p->box3d ? 1 : 0;

@@ -443,6 +443,51 @@ __device__ __forceinline__ void store_chunk(void* out, int32_t ncols, int32_t ro
   }
 }
 
+// The TMA-store form of store_chunk: the warp writes its 32 x 32 chunk of D (lane = row) into
+// one of its two shared staging buffers, swizzled as the tensor map of D expects (64-byte
+// swizzle for BF16 rows of 64 bytes, 128-byte for FP32 rows of 128 bytes: 16-byte chunk q of
+// row r sits at q ^ ((r >> 1) & 3), resp. q ^ (r & 7), which spreads a store instruction's 32
+// lanes over all banks), and one lane stores the box with a bulk tensor copy.  Rows at or past
+// M and columns at or past N are clipped by the copy; a chunk that starts past either edge is
+// skipped.  The buffer is reused two chunks later, after its copy has finished reading it.
+template <int OUT>
+__device__ __forceinline__ void store_chunk_tma(const CUtensorMap* map, uint8_t* bufs, uint32_t& parity, int lane,
+                                                int32_t M, int32_t N, int32_t row_first, int32_t col0,
+                                                const float (&z)[32]) {
+  constexpr int EB = OUT == OUT_BF16 ? 2 : 4;
+  constexpr int CHUNK = kStoreChunkRows * 32 * EB;
+  if (col0 >= N || row_first >= M) return;
+  uint8_t* const buf = bufs + parity * CHUNK;
+  if (lane == 0) ptx::bulk_wait_read_1();   // the copy issued from this buffer two chunks ago
+  __syncwarp();
+  uint8_t* const rowp = buf + lane * 32 * EB;
+  if (OUT == OUT_BF16) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 pk;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 two = __floats2bfloat162_rn(z[8 * q + 2 * h], z[8 * q + 2 * h + 1]);
+        w[h] = *reinterpret_cast<uint32_t*>(&two);
+      }
+      *reinterpret_cast<uint4*>(rowp + ((q ^ ((lane >> 1) & 3)) << 4)) = pk;
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<float4*>(rowp + ((q ^ (lane & 7)) << 4)) =
+          make_float4(z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
+  }
+  ptx::fence_proxy_async_smem();   // the generic-proxy writes, before the async-proxy copy reads them
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(map, ptx::smem_addr(buf), col0, row_first);
+    ptx::bulk_commit();
+  }
+  parity ^= 1u;
+}
+
 // ACT and DOUT (activation and D's type) specialise the extended epilogue (OUT == OUT_EXT)
 template <int BN, int OUT, int CG, int KA, int MC = 1, int ACT = ACT_NONE, int DOUT = OUT_F32>
 __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
@@ -473,6 +518,10 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   float alpha = p.alpha;
   if (p.use_scales) alpha = alpha * __ldg(p.scales) * __ldg(p.scales + 1);
   const bool bias_vec = (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0 && (p.N & 3) == 0;
+  // TMA-store epilogue (basic path): this warp's two staging buffers of 32 x 32 outputs
+  constexpr int STORE_CHUNK = kStoreChunkRows * 32 * (OUT == OUT_BF16 ? 2 : 4);
+  uint8_t* const store_bufs = smem_base + p.store_offset + ew_idx * 2 * STORE_CHUNK;
+  uint32_t store_parity = 0;
 
   int acc = 0;
   uint32_t acc_phase = 0;
@@ -630,7 +679,11 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
 #pragma unroll
           for (int j = 0; j < 32; ++j) z[j] = fmaxf(z[j], 0.0f);
         }
-        store_chunk<OUT>(out, w.col_end, row, w.row_end, col0, z);
+        if (p.tma_store)
+          store_chunk_tma<OUT>(&p.tmap_c, store_bufs, store_parity, lane, w.row_end, w.col_end,
+                               row - lane, col0, z);
+        else
+          store_chunk<OUT>(out, w.col_end, row, w.row_end, col0, z);
       }
     }
     ptx::tc_fence_before();
@@ -656,6 +709,7 @@ __device__ __forceinline__ void run_epilogue(const KernelParams& p, const Ctx& c
   }
   // every epilogue thread leaves the loop in the same iteration, so each warp is whole here
   if (EXT) epi::amax_flush(p.ext, amax);
+  if (!EXT && p.tma_store && lane == 0) ptx::bulk_wait_all();   // this warp's stores of D have landed
   if (p.stats && ep == 0) {
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_WAIT_TFULL] = wait_tfull;
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_BUSY] = busy;
@@ -731,6 +785,7 @@ __global__ void __launch_bounds__(TileCfg<BN, CG, KA>::threads_for(OUT == OUT_EX
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&p.tmap_a);
     ptx::prefetch_tmap(&p.tmap_b);
+    if (p.tma_store) ptx::prefetch_tmap(&p.tmap_c);
   }
   if (warp == 1) {
     if (CG == 2) {

@@ -51,6 +51,7 @@ enum Role : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_
 // protocol with the partial tiles stored / added by TMA bulk copies from shared memory
 enum SkFixup : int32_t { SK_DETERMINISTIC = 0, SK_ATOMIC = 1, SK_SEPARATE = 2, SK_TMA = 3 };
 constexpr int kStagingBytes = kBlockM * 32 * 4;   // one 128 x 32 FP32 chunk per epilogue warpgroup
+constexpr int kStoreChunkRows = 32;                // TMA-store epilogue: a warp's 32 x 32 chunk of D
 
 enum DebugFlags : int32_t { DBG_TRACE = 1, DBG_SKIP_LOAD = 2, DBG_SKIP_LOCK = 4, DBG_ROLE_CYCLES = 8 };
 
@@ -100,6 +101,10 @@ struct KernelParams {
   int32_t box3d;            // A and B maps are 3-D (atom elements, rows, atoms): one box per operand
                             // and stage brings all KA atom columns (HyTiS half-width B stays 2-D)
   int32_t staging_offset;   // SK_TMA: byte offset of the staging buffers from the aligned shared base
+  CUtensorMap tmap_c;       // tma_store: D as an M x N tensor, 32 x 32 boxes, 64-byte (BF16) or
+                            // 128-byte (FP32) swizzle
+  int32_t tma_store;        // 1: the basic epilogue stores D through shared memory and TMA
+  int32_t store_offset;     // tma_store: byte offset of the store staging from the aligned shared base
   uint32_t run_id;          // tags the status word and the locks of this launch (never 0), so
                             // that values left by earlier launches need no clearing
   uint32_t status_floor;    // the status word keeps a code recorded by any launch with a run id
@@ -139,6 +144,7 @@ struct TileCfg {
   // SK_TMA staging: one kStagingBytes buffer per epilogue warpgroup after the control block
   static constexpr int STAGING_OFFSET = ((MISC_OFFSET + 16 + 1023) / 1024) * 1024;
   static constexpr int smem_bytes_tma(int ew) { return 1024 + STAGING_OFFSET + ew * kStagingBytes; }
+  static constexpr int smem_bytes_staging(int bytes) { return 1024 + STAGING_OFFSET + bytes; }
 };
 
 }  // namespace tst
@@ -205,37 +211,47 @@ inline int tst_cfg(int bn, int cg, int ka, bool smem) {
 
 inline int tst_kernel_smem_bytes(int bn, int cg, int ka) { return tst_cfg(bn, cg, ka, true); }
 
-// Where the SK_TMA staging buffers (one per epilogue warpgroup) go: past the control
-// block when shared memory has room, else in the A regions of the ring's last stages,
-// which the plan then leaves unused.  Returns false when neither fits.
+// Where `bytes` of epilogue staging go (the SK_TMA fixup's chunks, one 128 x 32 FP32 buffer
+// per epilogue warpgroup; or the TMA-store epilogue's two 32 x 32 buffers per epilogue warp):
+// past the control block when shared memory has room, else in the A regions of the ring's
+// last stages, which the plan then leaves unused.  Both places are 1024-byte aligned.
+// Returns false when neither fits.
 template <int BN, int CG, int KA>
-inline bool tst_tma_staging_cfg(int ew, int* offset, int* smem_bytes, int* max_stages) {
+inline bool tst_staging_cfg(int bytes, int* offset, int* smem_bytes, int* max_stages) {
   using Cfg = tst::TileCfg<BN, CG, KA>;
-  if (Cfg::smem_bytes_tma(ew) <= tst::kSmemLimit) {
+  if (Cfg::smem_bytes_staging(bytes) <= tst::kSmemLimit) {
     *offset = Cfg::STAGING_OFFSET;
-    *smem_bytes = Cfg::smem_bytes_tma(ew);
+    *smem_bytes = Cfg::smem_bytes_staging(bytes);
     *max_stages = Cfg::STAGES;
     return true;
   }
-  const int need = (ew * tst::kStagingBytes + Cfg::A_BYTES - 1) / Cfg::A_BYTES;
+  const int need = (bytes + Cfg::A_BYTES - 1) / Cfg::A_BYTES;
   *offset = (Cfg::STAGES - need) * Cfg::A_BYTES;
   *smem_bytes = Cfg::SMEM_BYTES;
   *max_stages = Cfg::STAGES - need;
   return *max_stages >= 2;
 }
 
-inline bool tst_tma_staging(int bn, int cg, int ka, int ew, int* offset, int* smem_bytes, int* max_stages) {
+inline bool tst_staging(int bn, int cg, int ka, int bytes, int* offset, int* smem_bytes, int* max_stages) {
   if (bn == 256) {
-    if (cg == 2) return ka == 2 ? tst_tma_staging_cfg<256, 2, 2>(ew, offset, smem_bytes, max_stages)
-                                : tst_tma_staging_cfg<256, 2, 1>(ew, offset, smem_bytes, max_stages);
-    return ka == 2 ? tst_tma_staging_cfg<256, 1, 2>(ew, offset, smem_bytes, max_stages)
-                   : tst_tma_staging_cfg<256, 1, 1>(ew, offset, smem_bytes, max_stages);
+    if (cg == 2) return ka == 2 ? tst_staging_cfg<256, 2, 2>(bytes, offset, smem_bytes, max_stages)
+                                : tst_staging_cfg<256, 2, 1>(bytes, offset, smem_bytes, max_stages);
+    return ka == 2 ? tst_staging_cfg<256, 1, 2>(bytes, offset, smem_bytes, max_stages)
+                   : tst_staging_cfg<256, 1, 1>(bytes, offset, smem_bytes, max_stages);
   }
-  if (cg == 2) return ka == 2 ? tst_tma_staging_cfg<128, 2, 2>(ew, offset, smem_bytes, max_stages)
-                              : tst_tma_staging_cfg<128, 2, 1>(ew, offset, smem_bytes, max_stages);
-  return ka == 2 ? tst_tma_staging_cfg<128, 1, 2>(ew, offset, smem_bytes, max_stages)
-                 : tst_tma_staging_cfg<128, 1, 1>(ew, offset, smem_bytes, max_stages);
+  if (cg == 2) return ka == 2 ? tst_staging_cfg<128, 2, 2>(bytes, offset, smem_bytes, max_stages)
+                              : tst_staging_cfg<128, 2, 1>(bytes, offset, smem_bytes, max_stages);
+  return ka == 2 ? tst_staging_cfg<128, 1, 2>(bytes, offset, smem_bytes, max_stages)
+                 : tst_staging_cfg<128, 1, 1>(bytes, offset, smem_bytes, max_stages);
 }
+
+// the SK_TMA fixup's staging: one 128 x 32 FP32 chunk per epilogue warpgroup
+inline bool tst_tma_staging(int bn, int cg, int ka, int ew, int* offset, int* smem_bytes, int* max_stages) {
+  return tst_staging(bn, cg, ka, ew * tst::kStagingBytes, offset, smem_bytes, max_stages);
+}
+
+// the TMA-store epilogue's staging: two 32 x 32 chunks of D per epilogue warp (4 warps)
+inline int tst_store_staging_bytes(int out_bytes) { return 4 * 2 * tst::kStoreChunkRows * 32 * out_bytes; }
 namespace tst {
 // Separate-reduction pass of Stream-K (streamk_reduce.cu): sums each split
 // tile's partial slots in K order and applies the epilogue.
