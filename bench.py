@@ -61,7 +61,7 @@ DESCR = {
     "c4_bf16_streamk": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles of 128x128, one CTA each, "
                        "Stream-K with fixup",
     "c4_bf16_streamk_pairs": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 128x128 CTA tiles in 2x1 CTA pairs "
-                             "(120 scheduled 256x128 tiles), Stream-K with fixup",
+                             "(120 scheduled 256x128 tiles), Stream-K with fixup in 4 groups",
     "c4_bf16_hybrid_pairs": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 128x128 CTA tiles in 2x1 CTA pairs, "
                             "data-parallel waves + Stream-K tail",
     "c4_bf16_persistent": "BF16 GEMM 1920x1920x16384, U[-1,1], FP32 out, 225 tiles of 128x128, one CTA each, "
@@ -87,8 +87,8 @@ MAX_SETS = 16             # more input sets than this: flush L2 before every lau
 KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
 
 
-PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "l2_hint", "tma_boxes", "cluster_n",
-                    "epilogue_store")
+PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "sk_fixup", "l2_hint", "tma_boxes",
+                    "cluster_n", "epilogue_store", "l2_prefetch")
 
 
 def extra_plan_options(w):

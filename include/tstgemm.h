@@ -292,6 +292,11 @@ typedef struct {
                               TST_STORE_AUTO (default): TMA stores where they apply and their
                               staging fits beside a full ring, else direct.  Same results either
                               way. */
+    int32_t l2_prefetch;   /* 0 = off; d > 0: with the loads of k-tile kb the producer also asks TMA
+                              to bring k-tile kb + d of the same work item into L2 (a prefetch:
+                              no shared memory, no barrier, never a fault; "H100 . cp.async.bulk"
+                              section 6's L2 prefetch), so the ring's loads more often hit L2.
+                              At most 16.  Same results either way. */
 } tst_plan_options;
 
 enum { TST_STORE_AUTO = 0, TST_STORE_DIRECT = 1, TST_STORE_TMA = 2 };

@@ -32,9 +32,10 @@ WORKLOADS = {
     "c4_bf16_streamk": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                             mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=1),
     # the same problem with its 128x128 CTA tiles run as 2x1 CTA pairs (120 scheduled 256x128
-    # tiles), Stream-K, and the hybrid of data-parallel waves with a Stream-K tail
+    # tiles), Stream-K in 4 groups (the split tiles dealt to groups for L2 locality), and the
+    # hybrid of data-parallel waves with a Stream-K tail
     "c4_bf16_streamk_pairs": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
-                                  mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=2),
+                                  mapping=("grouped_m", 8), schedule="streamk", bn=128, cta_group=2, sk_groups=4),
     "c4_bf16_hybrid_pairs": dict(M=1920, N=1920, K=16384, dtype="bf16", dist="uniform", case=4, out="f32",
                                  mapping=("grouped_m", 8), schedule="streamk_hybrid", bn=128, cta_group=2),
     # the same problem with single CTAs in clusters of two along N that share A by TMA

@@ -59,3 +59,29 @@ def test_hinted_grouped_array_equals_plain():
             assert torch.equal(res["keep_a"][g], res["none"][g])
             z, _ = oracle.gemm(As[g], Bs[g], "bf16")
             assert np.array_equal(host_values(res["none"][g]), z), g
+
+
+@pytest.mark.parametrize("dtype,cg,bn,schedule,extra", [
+    ("bf16", 2, 128, "persistent", {}),                      # 3-D boxes (128-column pairs)
+    ("e4m3", 2, 256, "persistent", {}),                      # 2-D boxes
+    ("bf16", 1, 128, "streamk", {"cluster_n": 2}),           # multicast: each CTA prefetches its own atom
+    ("bf16", 1, 128, "hytis", {}),                           # half-width tiles
+])
+def test_l2_prefetch_changes_no_result(dtype, cg, bn, schedule, extra):
+    # prefetching k-tiles into L2 ahead of their loads is a hint: the same bits, the oracle's values
+    M, N, K = 1000, 776, 2048
+    enc = synthetic.bf16_bits if dtype == "bf16" else (lambda x: synthetic.e4m3_bytes(x.astype(np.float32)))
+    Ah = enc(synthetic.draw("int:8", 7500, M * K).reshape(M, K))
+    Bh = enc(synthetic.draw("int:8", 7501, N * K).reshape(N, K))
+    A, B = device_codes(Ah), device_codes(Bh)
+    outs = {}
+    for d in (0, 1, 4):
+        plan = tst.gemm_plan_create(M, N, K, dtype=dtype, mapping=("grouped_m", 4), schedule=schedule,
+                                    out_dtype="f32", cta_group=cg, bn=bn, l2_prefetch=d, **extra)
+        D = torch.full((M, N), float("nan"), device="cuda")
+        tst.gemm_run(plan, A, B, D)
+        assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+        outs[d] = D
+    assert torch.equal(outs[1], outs[0]) and torch.equal(outs[4], outs[0])
+    want, _ = oracle.gemm(Ah, Bh, dtype)
+    assert np.array_equal(host_values(outs[4]), want)

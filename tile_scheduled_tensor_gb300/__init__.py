@@ -100,7 +100,7 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      bias_mode=None, activation=None,
                      row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
                      amax: bool = False, aux: bool = False, aux_dtype="f32", block_scale: bool = False,
-                     cluster_n: int = 0, epilogue_store="auto") -> Plan:
+                     cluster_n: int = 0, epilogue_store="auto", l2_prefetch: int = 0) -> Plan:
     """Plan C = epilogue(A x B).  The basic epilogue is alpha, a column bias (has_bias),
     ReLU and the tensor-wise scales; any of beta/has_c, bias_mode='row', activation
     'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux, block_scale or out_dtype 'e4m3'
@@ -113,7 +113,7 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                                   int(sk_groups), _enum(_FIXUP, sk_fixup, "sk_fixup"), int(bool(pdl)),
                                   _enum(_L2, l2_hint, "l2_hint"),
                                   _enum(_BOXES, tma_boxes, "tma_boxes"), int(cluster_n),
-                                  _enum(_STORE, epilogue_store, "epilogue_store"))
+                                  _enum(_STORE, epilogue_store, "epilogue_store"), int(l2_prefetch))
     bmode = _enum(_BIAS, bias_mode, "bias_mode") if bias_mode is not None else \
         (TST_BIAS_COL if has_bias else TST_BIAS_NONE)
     act = _enum(_ACT, activation, "activation") if activation is not None else \

@@ -62,7 +62,7 @@ class tst_plan_options(ctypes.Structure):
                 ("timeout_ns", ctypes.c_int64), ("stages", ctypes.c_int32), ("bk", ctypes.c_int32),
                 ("sk_groups", ctypes.c_int32), ("sk_fixup", ctypes.c_int32), ("pdl", ctypes.c_int32),
                 ("l2_hint", ctypes.c_int32), ("tma_boxes", ctypes.c_int32), ("cluster_n", ctypes.c_int32),
-                ("epilogue_store", ctypes.c_int32)]
+                ("epilogue_store", ctypes.c_int32), ("l2_prefetch", ctypes.c_int32)]
 
 
 class tst_plan_info(ctypes.Structure):

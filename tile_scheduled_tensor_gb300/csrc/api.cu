@@ -308,6 +308,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (o.bn != 0 && o.bn != 128 && o.bn != 256) return TST_ERR_UNSUPPORTED;
   if (o.num_ctas < 0 || o.num_sms < 0 || o.timeout_ns < 0 || o.pdl < 0 || o.pdl > 1) return TST_ERR_INVALID_ARG;
   if (o.l2_hint < TST_L2_NONE || o.l2_hint > TST_L2_AUTO) return TST_ERR_INVALID_ARG;
+  if (o.l2_prefetch < 0 || o.l2_prefetch > 16) return TST_ERR_INVALID_ARG;
   if (o.l2_hint == TST_L2_AUTO)   // keep the operand whose band the mapping's strips re-read
     o.l2_hint = (mapping.kind == TST_MAP_LINEAR_MFAST || mapping.kind == TST_MAP_GROUPED_N) ? TST_L2_KEEP_B
                                                                                             : TST_L2_KEEP_A;
@@ -905,6 +906,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.store_offset = p->store_offset;
   kp.pdl = p->opts.pdl;
   kp.l2_hint = p->opts.l2_hint;
+  kp.l2_prefetch = p->opts.l2_prefetch;
   kp.box3d = p->box3d ? 1 : 0;
   if (p->ext_on) {
     tst::EpiExt& x = kp.ext;

@@ -288,6 +288,24 @@ __device__ __forceinline__ void run_producer(const KernelParams& p, const Ctx& c
           }
         }
       }
+      // L2 prefetch of the k-tile `l2_prefetch` ahead in this item: the same boxes this CTA
+      // will load then, brought into L2 now so that load hits
+      if (p.l2_prefetch > 0 && !skip) {
+        const int32_t kp = kb + p.l2_prefetch;
+        if (kp < w.k_begin + w.k_count) {
+          if (KA > 1 && p.box3d && !MCAST) {
+            ptx::tma_prefetch_l2_3d(tmap_a, 0, m0, kp * KA);
+            if (!narrow) ptx::tma_prefetch_l2_3d(tmap_b, 0, n0, kp * KA);
+          } else {
+#pragma unroll
+            for (int a = 0; a < KA; ++a) {
+              if (!MCAST || a == static_cast<int>(c.rank_n)) ptx::tma_prefetch_l2_2d(tmap_a, kp * BK + a * BK_ATOM, m0);
+              if (!(KA > 1 && p.box3d && !narrow)) ptx::tma_prefetch_l2_2d(tmap_b, kp * BK + a * BK_ATOM, n0);
+            }
+            if (KA > 1 && p.box3d && !narrow) ptx::tma_prefetch_l2_3d(tmap_b, 0, n0, kp * KA);
+          }
+        }
+      }
       issued |= 1u << stage;
       issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }

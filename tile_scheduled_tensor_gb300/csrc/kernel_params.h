@@ -98,6 +98,7 @@ struct KernelParams {
   EpiExt ext;               // extended epilogue (ext.on == 0: the basic one above)
   int32_t pdl;              // launched as a programmatic dependent: wait before global accesses
   int32_t l2_hint;          // operand loads' L2 policy: 0 none, 1 A evict_last / B normal, 2 the reverse
+  int32_t l2_prefetch;      // 0, or the distance in k-tiles of the L2 prefetch issued with each load
   int32_t box3d;            // A and B maps are 3-D (atom elements, rows, atoms): one box per operand
                             // and stage brings all KA atom columns (HyTiS half-width B stays 2-D)
   int32_t staging_offset;   // SK_TMA: byte offset of the staging buffers from the aligned shared base
