@@ -36,6 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from synthetic import make_addend, make_gemm_inputs, make_group_rows, make_group_shapes, operand_types  # noqa: E402
+from synthetic import splitmix64 as synthetic_splitmix  # noqa: E402
 from synthetic.workloads import WORKLOADS  # noqa: E402
 
 METRIC = "GEMM TFLOPS (2MNK/s) BF16 & FP8 at 1 GB300; % of dense tensor-core peak"
@@ -45,7 +46,8 @@ HEADLINE = "c3_e4m3_8192"
 TARGET_PAIR = ("c3_e4m3_8192", "c2x_bf16_8192")
 EXTRA = ["c2x_bf16_8192", "c2_bf16_4096", "c2_bf16_4096_1cta", "c1_bf16_256", "c4_bf16_streamk_pairs",
          "c4_bf16_streamk", "c4_bf16_hybrid_pairs", "c4_bf16_persistent", "c4_bf16_hybrid", "c4_bf16_hytis",
-         "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "g1_bf16_grouped",
+         "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "c3b_e4m3_8192_blk32",
+         "c3b_e4m3_8192_blk1x128", "g1_bf16_grouped",
          "g2_bf16_grouped_shapes"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
@@ -75,6 +77,10 @@ DESCR = {
                             "C a BF16 N(0,1) addend, grouped-M G=8",
     "c3m_e4m3_e5m2_8192": "FP8 GEMM 8192^3, A e4m3 x B e5m2, N(0,1) tensor-wise scales, BF16 out, grouped-N G=16, "
                           "persistent",
+    "c3b_e4m3_8192_blk32": "FP8-e4m3 GEMM 8192^3 with block-scaled operands (one power-of-two FP32 scale per 32x32 "
+                           "tile of A and of B), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
+    "c3b_e4m3_8192_blk1x128": "FP8-e4m3 GEMM 8192^3 with block-scaled operands (one power-of-two FP32 scale per "
+                              "1x128 tile: per row and 128 K), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
     "g2_bf16_grouped_shapes": "grouped BF16 GEMM over 12 problems of different shapes (seeded M_g in [256, 4096], "
                               "N_g, K_g in {1024..8192}; 0.68 TFLOP), each with its own A, B, D; BF16 out, "
                               "grouped-M G=8 inside each group, one persistent launch",
@@ -88,7 +94,7 @@ KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h
 
 
 PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "sk_fixup", "l2_hint", "tma_boxes",
-                    "cluster_n", "epilogue_store", "l2_prefetch")
+                    "cluster_n", "epilogue_store", "l2_prefetch", "ab_block")
 
 
 def extra_plan_options(w):
@@ -159,6 +165,17 @@ def oracle_step(w, inp, rows, addend=None, b_decoded=None):
                                           rows=rows[sel], dtype_b=fb)
         return z, ad
     epi = w.get("epi")
+    if "ab_block" in w:
+        # block-scaled operands: the oracle's block expansion on the sampled rows, then the
+        # tensor-wise scales and alpha (the basic epilogue)
+        from oracle import blockscale as BS
+        br, bk = w["ab_block"]
+        sa, sb = block_scales(w)
+        rows = np.asarray(rows, dtype=np.int64)
+        a = oracle.decode(inp.A[rows], fa) * np.repeat(sa[rows // br].astype(np.float64), bk, axis=1)[:, :w["K"]]
+        b = (b_decoded if b_decoded is not None else oracle.decode(inp.B, fb)) * BS.expand(sb, w["N"], w["K"], br, bk)
+        s = w.get("alpha", 1.0) * (float(inp.scales[0]) * float(inp.scales[1]) if inp.scales is not None else 1.0)
+        return s * (a @ b.T), s * (np.abs(a) @ np.abs(b).T)
     if epi is None:
         return oracle.gemm(inp.A, inp.B, fa, alpha=w.get("alpha", 1.0), scales=inp.scales, bias=inp.bias,
                            relu=w.get("relu", False), rows=rows, dtype_b=fb, b_decoded=b_decoded)
@@ -186,6 +203,18 @@ def oracle_rows_per_step(cores):
     """Rows per oracle call: four per host thread, so the OpenMP loop over rows keeps every
     core busy."""
     return 4 * max(1, cores)
+
+
+def block_scales(w):
+    """Seeded power-of-two block scales (2^-3 .. 2^3) of A and B for a workload with
+    block-scaled operands: ceil(rows / br) x ceil(K / bk) FP32 each."""
+    br, bk = w["ab_block"]
+    out = []
+    for rows, seed in ((w["M"], 9800), (w["N"], 9900)):
+        shape = (-(-rows // br), -(-w["K"] // bk))
+        e = (synthetic_splitmix(seed + w["case"], shape[0] * shape[1]) % np.uint64(7)).astype(np.int64) - 3
+        out.append((2.0 ** e).astype(np.float32).reshape(shape))
+    return out
 
 
 def make_inputs_for(w):
@@ -261,6 +290,10 @@ def setup_workload(w, tst, torch, row_block=None):
         host["c"] = torch.from_numpy(arr.view(np.int16) if arr.dtype == np.uint16 else arr).pin_memory()
     if "d_scale" in epi:
         host["d_scale"] = torch.tensor([epi["d_scale"]], dtype=torch.float32).pin_memory()
+    if "ab_block" in w:
+        sa, sb = block_scales(w)
+        host["a_block_scales"] = torch.from_numpy(sa).pin_memory()
+        host["b_block_scales"] = torch.from_numpy(sb).pin_memory()
     dev = {k: v.cuda() for k, v in host.items()}
     if epi.get("amax"):
         dev["amax"] = torch.zeros(4, dtype=torch.float32, device="cuda")
@@ -272,7 +305,8 @@ def setup_workload(w, tst, torch, row_block=None):
 def run_args(dev):
     """Keyword arguments of gemm_run for the device operands of setup_workload."""
     return dict(bias=dev.get("bias"), scales=dev.get("scales"), c=dev.get("c"), d_scale=dev.get("d_scale"),
-                amax=dev.get("amax"))
+                amax=dev.get("amax"), a_block_scales=dev.get("a_block_scales"),
+                b_block_scales=dev.get("b_block_scales"))
 
 
 def run_once(tst, plan, dev, C, stream=None):

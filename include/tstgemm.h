@@ -188,6 +188,20 @@ typedef struct {
     int32_t aux_dtype;   /* TST_OUT_F32 or TST_OUT_BF16 */
     int32_t block_scale; /* 1: e4m3 D with one power-of-two scale per 32 x 32 tile (see above);
                             needs out_dtype TST_OUT_E4M3 and no d_scale */
+    int32_t ab_block_rows; /* block-scaled FP8 operands ("H100 . WGMMA Part 2" section 11): with
+                            ab_block_k > 0, A and B carry one FP32 scale per ab_block_rows x
+                            ab_block_k tile of (rows x K) and
+                              Acc[i][j] = sum_k a_ik sA[i / br][k / bk] * b_jk sB[j / br][k / bk]
+                            (br = ab_block_rows >= 1, bk = ab_block_k in {32, 64, 128}; e.g.
+                            32 x 32 tiles, or 1 x 32 for one scale per 32 K of a row).  The
+                            tensor core sums each k-block of bk into a fresh partial and the
+                            epilogue warps add (sA * sB) * partial in FP32 (the page's section
+                            15.3 multi-stage accumulation).  Needs FP8 operands, FP32 or BF16 D,
+                            alpha / tensor-wise scales / column bias / ReLU only, the static or
+                            persistent schedule, single CTAs with 128-column tiles and one-atom
+                            k-tiles (bn, cta_group, bk 0 or those values; TST_ERR_UNSUPPORTED
+                            otherwise). */
+    int32_t ab_block_k;
 } tst_epilogue_ex;
 
 /* Run-time operands of the extended epilogue: DEVICE pointers owned by the
@@ -205,6 +219,8 @@ typedef struct {
     void *aux;              /* M x N, aux_dtype, written */
     int32_t *block_exp;     /* int32[ceil(M/32)][ceil(N/32)] row-major, written: the exponent E
                                of each 32 x 32 tile's scale (block_scale); 4-byte aligned */
+    const float *a_block_scales; /* FP32[ceil(M/br)][ceil(K/bk)] row-major (block-scaled operands) */
+    const float *b_block_scales; /* FP32[ceil(N/br)][ceil(K/bk)] row-major */
 } tst_epilogue_args;
 
 /* Optional plan settings.  Zero-initialise and set what you need. */

@@ -80,3 +80,19 @@ def test_shard_rows_cover_the_problem():
         assert parts[0][0] == 0 and parts[-1][1] == w["M"]
         assert all(a[1] == b[0] for a, b in zip(parts, parts[1:]))
         assert sum(bench.flops(p[2]) for p in parts) == bench.flops(w)
+
+
+def test_block_scaled_oracle_step_is_the_oracle_on_sampled_rows():
+    # the benchmark's row-sampled oracle step for block-scaled operands equals the oracle's
+    # block-scaled product (with the tensor-wise scales and alpha) on those rows
+    from oracle import blockscale as BS
+    w = dict(M=70, N=40, K=96, dtype="e4m3", dist="normal", case=5, out="f32", mapping=("grouped_n", 2),
+             schedule="persistent", bn=128, cta_group=1, use_scales=True, ab_block=(32, 32), alpha=0.5)
+    inp = bench.make_inputs_for(w)
+    sa, sb = bench.block_scales(w)
+    full = BS.gemm_block_scaled(oracle.decode(inp.A, "e4m3"), oracle.decode(inp.B, "e4m3"), sa, sb, (32, 32))
+    full = full * 0.5 * float(inp.scales[0]) * float(inp.scales[1])
+    rows = np.array([0, 31, 32, 69, 5])
+    z, _ = bench.oracle_step(w, inp, rows)
+    assert np.allclose(z, full[rows], rtol=1e-13, atol=1e-13)
+    assert sa.shape == (3, 3) and sb.shape == (2, 3) and set(np.unique(np.log2(sa))) <= set(range(-3, 4))

@@ -1,0 +1,97 @@
+"""GPU parity of block-scaled FP8 operands (plan option ab_block = (br, bk): one FP32 scale
+per br x bk tile of A and of B) against the oracle's gemm_block_scaled.
+
+Exact where every value is exactly representable: small-integer e4m3 codes, power-of-two
+scales and sums below 2^24 make each k-block partial, its scaled product and the running
+FP32 sum exact, so the kernel and the FP64 oracle agree bit for bit (a BF16 D is then the
+oracle's round-to-nearest-even of the exact value).  Random normal inputs with scales
+that are not powers of two stay within 4e-3 of sum_k |a sA| |b sB| (+ 1e-6).  Tilings:
+the page's 32 x 32 tiles, the microscaling 1 x 32, and coarser 1 x 128, 128 x 128,
+32 x 64; ragged M, N and K against the tiles and the k-blocks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+import tile_scheduled_tensor_gb300 as tst
+from oracle import blockscale as BS
+
+from gemm_check import device_codes, host_values
+
+pytestmark = pytest.mark.gpu
+
+
+def _scales(seed, rows, K, br, bk, pow2=True):
+    shape = (-(-rows // br), -(-K // bk))
+    if pow2:
+        e = (synthetic.splitmix64(seed, shape[0] * shape[1]) % np.uint64(7)).astype(np.int64) - 3
+        return (2.0 ** e).reshape(shape).astype(np.float32)
+    return (0.5 + 1.5 * synthetic.uniform01(seed, shape[0] * shape[1])).reshape(shape).astype(np.float32)
+
+
+def _run(M, N, K, br, bk, out, schedule="persistent", mapping=("grouped_m", 4), dtype="e4m3", dist="int:4",
+         pow2=True, alpha=1.0, bias=False, relu=False, seed=0):
+    xa = synthetic.draw(dist, 9600 + seed, M * K).reshape(M, K).astype(np.float32)
+    xb = synthetic.draw(dist, 9700 + seed, N * K).reshape(N, K).astype(np.float32)
+    fa, fb = synthetic.operand_types(dtype)
+    enc = {"e4m3": synthetic.e4m3_bytes, "e5m2": synthetic.e5m2_bytes}
+    A, B = enc[fa](xa), enc[fb](xb)
+    sA, sB = _scales(9800 + seed, M, K, br, bk, pow2), _scales(9900 + seed, N, K, br, bk, pow2)
+    bv = synthetic.draw("int:4", 9950 + seed, N).astype(np.float32) if bias else None
+    plan = tst.gemm_plan_create(M, N, K, dtype=dtype, mapping=mapping, schedule=schedule, out_dtype=out,
+                                alpha=alpha, has_bias=bias, relu=relu, ab_block=(br, bk))
+    assert plan.info.bn == 128 and plan.info.cta_group == 1 and plan.info.bk == 128
+    D = torch.full((M, N), float("nan"), dtype=torch.float32 if out == "f32" else torch.bfloat16, device="cuda")
+    tst.gemm_run(plan, device_codes(A), device_codes(B), D, bias=torch.from_numpy(bv).cuda() if bias else None,
+                 a_block_scales=torch.from_numpy(sA).cuda(), b_block_scales=torch.from_numpy(sB).cuda())
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_OK, (tst.gemm_status_string(st), hex(word))
+    a, b = oracle.decode(A, fa), oracle.decode(B, fb)
+    acc = BS.gemm_block_scaled(a, b, sA, sB, (br, bk))
+    absacc = BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, (br, bk))
+    z = alpha * acc + (bv.astype(np.float64)[None, :] if bias else 0.0)
+    if relu:
+        z = np.maximum(z, 0.0)
+    return host_values(D), z, abs(alpha) * absacc
+
+
+@pytest.mark.parametrize("br,bk", [(32, 32), (1, 32), (1, 128), (128, 128), (32, 64)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_block_scaled_small_integers_exact(br, bk, out):
+    # 400 = 3 x 128 + 16 rows, 328 = 2 x 128 + 72 columns, K = 1040 = 8 k-tiles + 16 (ragged k-block)
+    got, z, _ = _run(400, 328, 1040, br, bk, out, alpha=0.5, bias=True, relu=(out == "bf16"), seed=br + bk)
+    want = z if out == "f32" else oracle.decode(oracle.round_bf16(z), "bf16")
+    assert np.abs(z).max() < 2 ** 22
+    assert np.array_equal(got, want), np.argwhere(got != want)[:5]
+
+
+@pytest.mark.parametrize("schedule,mapping", [("static", ("linear_nfast", 1)), ("persistent", ("grouped_n", 2)),
+                                              ("persistent", ("morton", 1))])
+def test_block_scaled_schedules_and_formats_exact(schedule, mapping):
+    for dtype in ("e4m3", "e4m3_e5m2"):
+        got, z, _ = _run(1024, 640, 2048, 32, 32, "f32", schedule=schedule, mapping=mapping, dtype=dtype, seed=7)
+        assert np.array_equal(got, z), dtype
+
+
+@pytest.mark.parametrize("br,bk", [(32, 32), (1, 32), (128, 128)])
+def test_block_scaled_random_within_bound(br, bk):
+    got, z, absz = _run(777, 520, 3072, br, bk, "f32", dist="normal", pow2=False, seed=11)
+    err = np.abs(got - z)
+    bound = 4e-3 * absz + 1e-6
+    assert (err <= bound).all(), float((err / bound).max())
+
+
+def test_block_scaled_unit_scales_are_the_plain_fp8_gemm():
+    # with every block scale 1 the result is the plain e4m3 GEMM (exact on small integers)
+    M, N, K = 512, 384, 1024
+    A = synthetic.e4m3_bytes(synthetic.draw("int:8", 9601, M * K).reshape(M, K).astype(np.float32))
+    B = synthetic.e4m3_bytes(synthetic.draw("int:8", 9602, N * K).reshape(N, K).astype(np.float32))
+    ones = torch.ones(M // 32, K // 32, device="cuda"), torch.ones(N // 32, K // 32, device="cuda")
+    plan = tst.gemm_plan_create(M, N, K, dtype="e4m3", mapping=("grouped_m", 8), schedule="persistent",
+                                out_dtype="f32", ab_block=(32, 32))
+    D = torch.empty(M, N, device="cuda")
+    tst.gemm_run(plan, device_codes(A), device_codes(B), D, a_block_scales=ones[0], b_block_scales=ones[1])
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    z, _ = oracle.gemm(A, B, "e4m3")
+    assert np.array_equal(host_values(D), z)

@@ -418,3 +418,22 @@ def test_tma_store_plan_rules():
     with pytest.raises(tst.TstError) as e:   # BF16 rows of 2002 bytes are not 16-byte multiples
         tst.gemm_plan_create(1000, 1001, 512, out_dtype="bf16", **kw)
     assert e.value.status == tst.TST_ERR_UNSUPPORTED
+
+
+def test_block_scaled_operand_plan_rules():
+    kw = dict(host_only=True, num_sms=152)
+    p = tst.gemm_plan_create(1000, 1000, 1024, dtype="e4m3", schedule="persistent", ab_block=(32, 32), **kw)
+    assert (p.info.bn, p.info.cta_group, p.info.bk, p.info.tma_store) == (128, 1, 128, 0)
+    for bad, status in ((dict(dtype="bf16"), tst.TST_ERR_UNSUPPORTED),
+                        (dict(dtype="e4m3", schedule="streamk"), tst.TST_ERR_UNSUPPORTED),
+                        (dict(dtype="e4m3", cta_group=2), tst.TST_ERR_UNSUPPORTED),
+                        (dict(dtype="e4m3", bn=256), tst.TST_ERR_UNSUPPORTED),
+                        (dict(dtype="e4m3", activation="gelu"), tst.TST_ERR_UNSUPPORTED),
+                        (dict(dtype="e4m3", out_dtype="e4m3"), tst.TST_ERR_UNSUPPORTED),
+                        (dict(dtype="e4m3", ab_block=(32, 48)), tst.TST_ERR_INVALID_ARG),
+                        (dict(dtype="e4m3", ab_block=(0, 32)), tst.TST_ERR_INVALID_ARG)):
+        args = dict(schedule="persistent", ab_block=(32, 32))
+        args.update(bad)
+        with pytest.raises(tst.TstError) as e:
+            tst.gemm_plan_create(1000, 1000, 1024, **args, **kw)
+        assert e.value.status == status, bad

@@ -100,12 +100,14 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
                      bias_mode=None, activation=None,
                      row_scale: bool = False, col_scale: bool = False, d_scale: bool = False,
                      amax: bool = False, aux: bool = False, aux_dtype="f32", block_scale: bool = False,
-                     cluster_n: int = 0, epilogue_store="auto", l2_prefetch: int = 0) -> Plan:
+                     cluster_n: int = 0, epilogue_store="auto", l2_prefetch: int = 0, ab_block=None) -> Plan:
     """Plan C = epilogue(A x B).  The basic epilogue is alpha, a column bias (has_bias),
     ReLU and the tensor-wise scales; any of beta/has_c, bias_mode='row', activation
     'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux, block_scale or out_dtype 'e4m3'
     selects the extended one (gemm_plan_create_epi).  block_scale: an e4m3 D with one
-    power-of-two scale per 32 x 32 tile, whose exponents gemm_run writes to block_exp."""
+    power-of-two scale per 32 x 32 tile, whose exponents gemm_run writes to block_exp.
+    ab_block=(br, bk): block-scaled FP8 operands, one scale per br x bk tile of A and of B
+    (gemm_run's a_block_scales, b_block_scales)."""
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
@@ -121,12 +123,13 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
     extended = bool(has_c or bmode == TST_BIAS_ROW or act in (TST_ACT_GELU, TST_ACT_SILU) or row_scale or
                     col_scale or d_scale or amax or aux or block_scale)
     h = ctypes.c_void_p()
-    if extended:
+    br, bk = ab_block if ab_block is not None else (0, 0)
+    if extended or ab_block is not None:
         epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), float(beta),
                                     int(bool(has_c)), _enum(_OUT, c_dtype, "c_dtype"), bmode, act,
                                     int(bool(use_scales)), int(bool(row_scale)), int(bool(col_scale)),
                                     int(bool(d_scale)), int(bool(amax)), int(bool(aux)),
-                                    _enum(_OUT, aux_dtype, "aux_dtype"), int(bool(block_scale)))
+                                    _enum(_OUT, aux_dtype, "aux_dtype"), int(bool(block_scale)), int(br), int(bk))
         _check(lib.gemm_plan_create_epi(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
                                         TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),
                                         ctypes.byref(epi), ctypes.byref(opts)), "gemm_plan_create_epi")
@@ -286,17 +289,19 @@ def _stream(stream):
 
 
 def gemm_run(plan: Plan, A, B, C, bias=None, scales=None, stream=None, c=None, row_scale=None, col_scale=None,
-             d_scale=None, amax=None, aux=None, block_exp=None):
+             d_scale=None, amax=None, aux=None, block_exp=None, a_block_scales=None, b_block_scales=None):
     """Enqueue C = epilogue(A x B) on `stream` (default: torch's current stream).  The
     extended epilogue's operands (c: the addend of beta * C; row_scale, col_scale,
     d_scale, amax, aux; block_exp, int32 [ceil(M/32), ceil(N/32)] written by a
     block-scaled e4m3 D) go through gemm_run_epi."""
-    if all(x is None for x in (c, row_scale, col_scale, d_scale, amax, aux, block_exp)):
+    if all(x is None for x in (c, row_scale, col_scale, d_scale, amax, aux, block_exp, a_block_scales,
+                               b_block_scales)):
         _check(lib.gemm_run(plan._h, _ptr(A), _ptr(B), _ptr(C), _ptr(bias), _ptr(scales), _stream(stream)),
                "gemm_run")
         return
     args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
-                                   _ptr(d_scale), _ptr(amax), _ptr(aux), _ptr(block_exp))
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux), _ptr(block_exp), _ptr(a_block_scales),
+                                   _ptr(b_block_scales))
     _check(lib.gemm_run_epi(plan._h, _ptr(A), _ptr(B), _ptr(C), ctypes.byref(args), _stream(stream)),
            "gemm_run_epi")
 
@@ -310,12 +315,14 @@ def _host_ptr(x):
 
 
 def gemm_run_host(plan: Plan, A, B, D, panels: int = 0, stream=None, bias=None, scales=None, c=None,
-                  row_scale=None, col_scale=None, d_scale=None, amax=None, aux=None, block_exp=None):
+                  row_scale=None, col_scale=None, d_scale=None, amax=None, aux=None, block_exp=None,
+                  a_block_scales=None, b_block_scales=None):
     """End to end on host tensors A, B, D (CPU, contiguous; pinned for the copies to
     overlap the computation): row panels of A stream in, each panel's GEMM runs as soon as
     it has landed, its rows of D stream back.  Epilogue operands are CUDA tensors."""
     args = _capi.tst_epilogue_args(_ptr(c), _ptr(bias), _ptr(scales), _ptr(row_scale), _ptr(col_scale),
-                                   _ptr(d_scale), _ptr(amax), _ptr(aux), _ptr(block_exp))
+                                   _ptr(d_scale), _ptr(amax), _ptr(aux), _ptr(block_exp), _ptr(a_block_scales),
+                                   _ptr(b_block_scales))
     _check(lib.gemm_run_host(plan._h, _host_ptr(A), _host_ptr(B), _host_ptr(D), ctypes.byref(args), int(panels),
                              _stream(stream)), "gemm_run_host")
 

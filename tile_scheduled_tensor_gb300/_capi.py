@@ -47,13 +47,15 @@ class tst_epilogue_ex(ctypes.Structure):
                 ("has_c", ctypes.c_int32), ("c_dtype", ctypes.c_int32), ("bias_mode", ctypes.c_int32),
                 ("activation", ctypes.c_int32), ("use_scales", ctypes.c_int32), ("row_scale", ctypes.c_int32),
                 ("col_scale", ctypes.c_int32), ("d_scale", ctypes.c_int32), ("amax", ctypes.c_int32),
-                ("aux", ctypes.c_int32), ("aux_dtype", ctypes.c_int32), ("block_scale", ctypes.c_int32)]
+                ("aux", ctypes.c_int32), ("aux_dtype", ctypes.c_int32), ("block_scale", ctypes.c_int32),
+                ("ab_block_rows", ctypes.c_int32), ("ab_block_k", ctypes.c_int32)]
 
 
 class tst_epilogue_args(ctypes.Structure):
     _fields_ = [("c", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("scales", ctypes.c_void_p),
                 ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p), ("d_scale", ctypes.c_void_p),
-                ("amax", ctypes.c_void_p), ("aux", ctypes.c_void_p), ("block_exp", ctypes.c_void_p)]
+                ("amax", ctypes.c_void_p), ("aux", ctypes.c_void_p), ("block_exp", ctypes.c_void_p),
+                ("a_block_scales", ctypes.c_void_p), ("b_block_scales", ctypes.c_void_p)]
 
 
 class tst_plan_options(ctypes.Structure):

@@ -20,7 +20,7 @@ LIB = os.path.join(PKG, "libtstgemm.so")
 SOURCES = (["api.cu", "noalloc.cu", "streamk_reduce.cu"] +
            [f"gemm_{kind}{dt}_cg{cg}_ka{ka}.cu" for kind in ("", "ext_") for dt in ("bf16", "e4m3") for cg in (1, 2)
             for ka in (1, 2)] +
-           [f"gemm_{dt}_cg1_ka2_mc2.cu" for dt in ("bf16", "e4m3")])
+           [f"gemm_{dt}_cg1_ka2_mc2.cu" for dt in ("bf16", "e4m3")] + ["gemm_bs.cu"])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-diag-suppress", "177", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -66,6 +66,7 @@ struct tst_plan {
   int32_t mc = 1;              // CTAs along N sharing A by multicast (the unit is cg x mc CTAs)
   int32_t sk_mode = 0;         // tst::SkFixup
   int32_t staging_offset = 0;  // SK_TMA staging buffers in shared memory
+  bool bs = false;             // block-scaled FP8 operands (gemm_bs_kernel)
   bool tma_store = false;      // the basic epilogue stores D by TMA from shared staging
   int32_t store_offset = 0;    // ... at this offset of the aligned shared base
   int32_t sk_slots = 1;        // partial slots per split-tile half
@@ -305,6 +306,22 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (layout != TST_LAYOUT_A_ROW_B_NK) return TST_ERR_UNSUPPORTED;
   tst_plan_options o{};
   if (opts) o = *opts;
+  // block-scaled FP8 operands: their own kernel, single CTAs with 128 x 128 tiles and one-atom
+  // k-tiles, the basic epilogue, whole tiles (static or persistent)
+  const bool bs = epi->ab_block_k != 0;
+  if (bs) {
+    if (epi->ab_block_k != 32 && epi->ab_block_k != 64 && epi->ab_block_k != 128) return TST_ERR_INVALID_ARG;
+    if (epi->ab_block_rows < 1) return TST_ERR_INVALID_ARG;
+    if (dtype == TST_BF16 || needs_ext(*epi) || groups > 0 || (schedule != TST_STATIC && schedule != TST_PERSISTENT) ||
+        (o.bn != 0 && o.bn != 128) || (o.cta_group != 0 && o.cta_group != 1) || (o.bk != 0 && o.bk != 128) ||
+        o.cluster_n == 2 || o.pdl || o.epilogue_store == TST_STORE_TMA || o.l2_prefetch)
+      return TST_ERR_UNSUPPORTED;
+    o.bn = 128;
+    o.cta_group = 1;
+    o.bk = 128;
+    o.tma_boxes = TST_BOXES_2D;
+    o.epilogue_store = TST_STORE_DIRECT;
+  }
   if (o.bn != 0 && o.bn != 128 && o.bn != 256) return TST_ERR_UNSUPPORTED;
   if (o.num_ctas < 0 || o.num_sms < 0 || o.timeout_ns < 0 || o.pdl < 0 || o.pdl > 1) return TST_ERR_INVALID_ARG;
   if (o.l2_hint < TST_L2_NONE || o.l2_hint > TST_L2_AUTO) return TST_ERR_INVALID_ARG;
@@ -324,6 +341,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   p->b_rows = groups > 0 ? static_cast<int64_t>(groups) * N : N;
   p->fmt_ab = dtype == TST_BF16 ? 0u : fp8_formats(dtype);
   p->host_only = o.host_only != 0;
+  p->bs = bs;
   if (o.timeout_ns > 0) p->timeout_ns = static_cast<uint64_t>(o.timeout_ns);
 
   // device properties
@@ -397,8 +415,9 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (!p->host_only) {
     // the extended epilogue has its own instance (two epilogue warpgroups, typed stores of D)
     const int kdt = dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3;
-    p->kernel = p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka)
-                          : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka, p->mc);
+    p->kernel = p->bs       ? tst_bs_kernel(kernel_out(*p))
+                : p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka)
+                            : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka, p->mc);
     if (!p->kernel ||
         // the largest size any plan of this kernel asks for (the attribute is per kernel)
         cudaFuncSetAttribute(p->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tst::kSmemLimit) != cudaSuccess) {
@@ -819,8 +838,12 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
       (e.has_c && ea->c == nullptr) || (e.row_scale && ea->row_scale == nullptr) ||
       (e.col_scale && ea->col_scale == nullptr) || (e.d_scale && ea->d_scale == nullptr) ||
       (e.amax && ea->amax == nullptr) || (e.aux && ea->aux == nullptr) ||
-      (e.block_scale && ea->block_exp == nullptr))
+      (e.block_scale && ea->block_exp == nullptr) ||
+      (p->bs && (ea->a_block_scales == nullptr || ea->b_block_scales == nullptr)))
     return TST_ERR_INVALID_ARG;
+  if (p->bs && ((reinterpret_cast<uintptr_t>(ea->a_block_scales) & 3u) ||
+                (reinterpret_cast<uintptr_t>(ea->b_block_scales) & 3u)))
+    return TST_ERR_ALIGNMENT;
   if (e.block_scale && (reinterpret_cast<uintptr_t>(ea->block_exp) & 3u)) return TST_ERR_ALIGNMENT;
   if (!array_mode && (!aligned16(A) || !aligned16(B) || !aligned16(C))) return TST_ERR_ALIGNMENT;
   if ((has_bias && (reinterpret_cast<uintptr_t>(ea->bias) & 3u)) ||
@@ -907,6 +930,13 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
   kp.pdl = p->opts.pdl;
   kp.l2_hint = p->opts.l2_hint;
   kp.l2_prefetch = p->opts.l2_prefetch;
+  if (p->bs) {
+    kp.bs_a = ea->a_block_scales;
+    kp.bs_b = ea->b_block_scales;
+    kp.bs_rows = e.ab_block_rows;
+    kp.bs_k = e.ab_block_k;
+    kp.bs_kblocks = static_cast<int32_t>(ceil_div(p->K, e.ab_block_k));
+  }
   kp.box3d = p->box3d ? 1 : 0;
   if (p->ext_on) {
     tst::EpiExt& x = kp.ext;
@@ -945,7 +975,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p->sched.grid * p->cg * p->mc), 1, 1);
-  cfg.blockDim = dim3(tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
+  cfg.blockDim = dim3(p->bs ? kBsThreads : tst_kernel_threads(p->bn, p->ka, p->ext_on), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(p->smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -1130,6 +1160,8 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
   // a last panel shorter than half a panel joins the one before it (a GEMM of a few rows
   // costs nearly a full panel's time); the panels keep at most two heights
   if (P > 1 && M - (P - 1) * R < R / 2) --P;
+  // block-scaled operands: every panel must start on a row block of A's scales
+  if (p->bs && R % e.ab_block_rows != 0 && P > 1) return TST_ERR_UNSUPPORTED;
 
   HostRun* h = p->host_run;
   if (h == nullptr) {
@@ -1194,6 +1226,7 @@ tst_status gemm_run_host(tst_plan* p, const void* A, const void* B, void* D, con
     if (a.row_scale) a.row_scale += r0;
     if (a.aux) a.aux = static_cast<char*>(a.aux) + r0 * N * (e.aux_dtype == TST_OUT_F32 ? 4 : 2);
     if (a.block_exp) a.block_exp += (r0 / 32) * ceil_div(N, 32);   // panels start on 32-row tiles
+    if (a.a_block_scales) a.a_block_scales += (r0 / e.ab_block_rows) * ceil_div(K, e.ab_block_k);
     return a;
   };
   // every panel plan exists before anything is enqueued

@@ -99,6 +99,11 @@ struct KernelParams {
   int32_t pdl;              // launched as a programmatic dependent: wait before global accesses
   int32_t l2_hint;          // operand loads' L2 policy: 0 none, 1 A evict_last / B normal, 2 the reverse
   int32_t l2_prefetch;      // 0, or the distance in k-tiles of the L2 prefetch issued with each load
+  // block-scaled operands (gemm_bs_kernel): one FP32 scale per bs_rows x bs_k tile of A
+  // (ceil(M / bs_rows) x bs_kblocks, row-major) and of B (ceil(N / bs_rows) x bs_kblocks)
+  const float* bs_a;
+  const float* bs_b;
+  int32_t bs_rows, bs_k, bs_kblocks;
   int32_t box3d;            // A and B maps are 3-D (atom elements, rows, atoms): one box per operand
                             // and stage brings all KA atom columns (HyTiS half-width B stays 2-D)
   int32_t staging_offset;   // SK_TMA: byte offset of the staging buffers from the aligned shared base
@@ -272,6 +277,11 @@ constexpr int kReduceThreads = 256;
 constexpr int kReduceRows = 16;  // rows of a 128-row tile half per CTA
 }  // namespace tst
 const void* tst_reduce_kernel(int out_type);
+
+// Block-scaled operands (gemm_bs.cu): FP8 operands, single CTAs, 128-column tiles, one-atom
+// k-tiles; warps 2-9 accumulate the scaled k-block partials (320 threads).
+constexpr int kBsThreads = 320;
+const void* tst_bs_kernel(int out_type);
 
 inline int tst_kernel_threads(int bn, int ka, bool ext = false) {
   return ((bn == 128 && ka == 2) ? tst::kThreadsDual : tst::kThreads) + (ext ? 128 : 0);
