@@ -47,7 +47,7 @@ TARGET_PAIR = ("c3_e4m3_8192", "c2x_bf16_8192")
 EXTRA = ["c2x_bf16_8192", "c2_bf16_4096", "c2_bf16_4096_1cta", "c1_bf16_256", "c4_bf16_streamk_pairs",
          "c4_bf16_streamk", "c4_bf16_hybrid_pairs", "c4_bf16_persistent", "c4_bf16_hybrid", "c4_bf16_hytis",
          "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "c3b_e4m3_8192_blk32",
-         "c3b_e4m3_8192_blk1x128", "g1_bf16_grouped",
+         "c3b_e4m3_8192_blk1x128", "c3b_e4m3_8192_blk128", "g1_bf16_grouped",
          "g2_bf16_grouped_shapes"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
@@ -81,6 +81,8 @@ DESCR = {
                            "tile of A and of B), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
     "c3b_e4m3_8192_blk1x128": "FP8-e4m3 GEMM 8192^3 with block-scaled operands (one power-of-two FP32 scale per "
                               "1x128 tile: per row and 128 K), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
+    "c3b_e4m3_8192_blk128": "FP8-e4m3 GEMM 8192^3 with block-scaled operands (one power-of-two FP32 scale per "
+                            "128x128 tile), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
     "g2_bf16_grouped_shapes": "grouped BF16 GEMM over 12 problems of different shapes (seeded M_g in [256, 4096], "
                               "N_g, K_g in {1024..8192}; 0.68 TFLOP), each with its own A, B, D; BF16 out, "
                               "grouped-M G=8 inside each group, one persistent launch",

@@ -72,7 +72,7 @@ WORKLOADS = {
                                    mapping=("grouped_m", 8), schedule="persistent", bn=256, cta_group=2,
                                    shape_groups=12),
     # 8192^3 e4m3 with block-scaled operands (one power-of-two FP32 scale per 32 x 32 tile of A
-    # and of B; and per 1 x 128, one per 128 K of a row): 128x128 single-CTA tiles, one-atom
+    # and of B; per 1 x 128, one per 128 K of a row; per 128 x 128 tile): 128x128 single-CTA tiles, one-atom
     # k-tiles, grouped-N G=16, persistent
     "c3b_e4m3_8192_blk32": dict(M=8192, N=8192, K=8192, dtype="e4m3", dist="normal", case=3, out="bf16",
                                 mapping=("grouped_n", 16), schedule="persistent", bn=128, cta_group=1,
@@ -80,6 +80,9 @@ WORKLOADS = {
     "c3b_e4m3_8192_blk1x128": dict(M=8192, N=8192, K=8192, dtype="e4m3", dist="normal", case=3, out="bf16",
                                    mapping=("grouped_n", 16), schedule="persistent", bn=128, cta_group=1,
                                    use_scales=True, ab_block=(1, 128)),
+    "c3b_e4m3_8192_blk128": dict(M=8192, N=8192, K=8192, dtype="e4m3", dist="normal", case=3, out="bf16",
+                                 mapping=("grouped_n", 16), schedule="persistent", bn=128, cta_group=1,
+                                 use_scales=True, ab_block=(128, 128)),
     # 8192^3 with mixed FP8 formats: A e4m3, B e5m2 (tensor-wise scales) -> BF16, grouped-N G=16
     "c3m_e4m3_e5m2_8192": dict(M=8192, N=8192, K=8192, dtype="e4m3_e5m2", dist="normal", case=3, out="bf16",
                                mapping=("grouped_n", 16), schedule="persistent", bn=256, cta_group=2,

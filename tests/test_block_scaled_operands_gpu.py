@@ -95,3 +95,47 @@ def test_block_scaled_unit_scales_are_the_plain_fp8_gemm():
     assert tst.gemm_status_query(plan)[0] == tst.TST_OK
     z, _ = oracle.gemm(A, B, "e4m3")
     assert np.array_equal(host_values(D), z)
+
+
+def test_block_scaled_four_stage_ring_and_many_items_exact():
+    # the smallest ring the two MMA issuers allow, an odd k-tile count (a lone last k-block
+    # per item) and several work items per CTA
+    M, N, K = 1536, 1280, 1152
+    xa = synthetic.draw("int:4", 9611, M * K).reshape(M, K).astype(np.float32)
+    xb = synthetic.draw("int:4", 9612, N * K).reshape(N, K).astype(np.float32)
+    A, B = synthetic.e4m3_bytes(xa), synthetic.e4m3_bytes(xb)
+    for br, bk in ((1, 128), (32, 64), (32, 32)):
+        sA, sB = _scales(9613, M, K, br, bk), _scales(9614, N, K, br, bk)
+        plan = tst.gemm_plan_create(M, N, K, dtype="e4m3", mapping=("grouped_m", 4), schedule="persistent",
+                                    out_dtype="f32", ab_block=(br, bk), stages=4, num_ctas=19)
+        assert plan.info.stages == 4
+        D = torch.full((M, N), float("nan"), device="cuda")
+        tst.gemm_run(plan, device_codes(A), device_codes(B), D, a_block_scales=torch.from_numpy(sA).cuda(),
+                     b_block_scales=torch.from_numpy(sB).cuda())
+        assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+        want = BS.gemm_block_scaled(oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3"), sA, sB, (br, bk))
+        assert np.array_equal(host_values(D), want), (br, bk)
+
+
+def test_block_scaled_timeout_on_missing_load_reports_and_recovers():
+    # the producer skips one load (host-set debug flag): an MMA issuer's bounded wait runs
+    # out, the kernel ends with TST_ERR_TIMEOUT (the accumulating warps finish their walk
+    # of the windows without waiting on the issuers), and the plan then runs clean
+    M, N, K = 512, 512, 1024
+    xa = synthetic.draw("int:4", 9621, M * K).reshape(M, K).astype(np.float32)
+    xb = synthetic.draw("int:4", 9622, N * K).reshape(N, K).astype(np.float32)
+    A, B = synthetic.e4m3_bytes(xa), synthetic.e4m3_bytes(xb)
+    sA, sB = _scales(9623, M, K, 32, 32), _scales(9624, N, K, 32, 32)
+    plan = tst.gemm_plan_create(M, N, K, dtype="e4m3", mapping=("grouped_m", 4), schedule="persistent",
+                                out_dtype="f32", ab_block=(32, 32))
+    ops = dict(a_block_scales=torch.from_numpy(sA).cuda(), b_block_scales=torch.from_numpy(sB).cuda())
+    tst.gemm_plan_set_debug(plan, tst.TST_DEBUG_FAULT_SKIP_LOAD, None, 0, timeout_ns=20_000_000)
+    D = torch.zeros(M, N, device="cuda")
+    tst.gemm_run(plan, device_codes(A), device_codes(B), D, **ops)
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_ERR_TIMEOUT, (st, hex(word))
+    tst.gemm_plan_set_debug(plan, 0, None, 0)
+    tst.gemm_run(plan, device_codes(A), device_codes(B), D, **ops)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    want = BS.gemm_block_scaled(oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3"), sA, sB, (32, 32))
+    assert np.array_equal(host_values(D), want)

@@ -407,15 +407,18 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   }
   if (T >= (int64_t(1) << 30) || T * kt >= (int64_t(1) << 62)) { delete p; return TST_ERR_INVALID_ARG; }
   p->stages = tst_kernel_stages(p->bn, p->cg, p->ka);
+  if (p->bs) p->stages -= 1;   // the last stage's A slot holds the block-scaled kernel's scale windows
   if (o.stages != 0) {
-    if (o.stages < 2 || o.stages > p->stages) { delete p; return TST_ERR_UNSUPPORTED; }
+    // block-scaled: an MMA issuer skips up to three k-tiles that the other one reads, so
+    // its parity waits on a stage stay unambiguous only with four stages or more
+    if (o.stages < (p->bs ? 4 : 2) || o.stages > p->stages) { delete p; return TST_ERR_UNSUPPORTED; }
     p->stages = o.stages;
   }
   p->smem_bytes = tst_kernel_smem_bytes(p->bn, p->cg, p->ka);
   if (!p->host_only) {
     // the extended epilogue has its own instance (two epilogue warpgroups, typed stores of D)
     const int kdt = dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3;
-    p->kernel = p->bs       ? tst_bs_kernel(kernel_out(*p))
+    p->kernel = p->bs       ? tst_bs_kernel(kernel_out(*p), epi->ab_block_rows % 32 != 0)
                 : p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka)
                             : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka, p->mc);
     if (!p->kernel ||

@@ -11,20 +11,23 @@
 // K = 32) into a fresh partial in Tensor Memory, and the epilogue warps multiply every
 // partial by its two block scales and add it to an FP32 sum held in registers.
 //
-// Roles, 320 threads, one CTA per SM, single CTAs with 128 x 128 tiles and one-atom
+// Roles, 352 threads, one CTA per SM, single CTAs with 128 x 128 tiles and one-atom
 // k-tiles (128 e4m3 / e5m2 of K per stage):
 //   warp 0      the TMA producer of the plain kernel (run_producer).
-//   warp 1      MMA issuer: per k-block, wait until partial buffer pb is free
-//               (PEMPTY[pb]), issue its MMAs into TMEM columns pb * 128 (the first one
-//               overwriting), commit -> PFULL[pb]; after each stage, commit -> EMPTY[s].
-//               Four partial buffers fill the 512 TMEM columns, so the MMAs of the next
-//               k-blocks run while the epilogue warps read the last ones.
+//   warps 1, 10 MMA issuers 0 and 1, taking alternate pairs of k-blocks: wait until the
+//               issuer's partial slot (two 128-column buffers) is free (PEMPTY[r]), issue
+//               each k-block's MMAs into its buffer (the first one overwriting), commit ->
+//               PFULL[r]; commit -> EMPTY[s] after the last MMA reading stage s.  The two
+//               slots fill the 512 TMEM columns, so one pair's MMAs run while the epilogue
+//               warps read the other's partials.
 //   warps 2-9   two warpgroups, each taking 64 of the tile's 128 columns (a warp reads the
-//               TMEM lanes of its quadrant, 32 rows): two k-blocks at a time, wait
-//               PFULL of both buffers, load both partials (one wait for the two loads), add
-//               (sA * sB) * partial to the sum and release them (PEMPTY counts the 8
-//               warps); after the work item's last k-block, apply alpha, the column bias
-//               and ReLU, cast and store.
+//               TMEM lanes of its quadrant, 32 rows): a pair of k-blocks at a time, wait
+//               PFULL of its slot, load the two partials one after the other, add
+//               (sA * sB) * partial to the sum with packed FP32 pairs and release them
+//               (PEMPTY counts the 8 warps); after the work item's last k-block, apply
+//               alpha, the column bias and ReLU, cast and store.  The same warps copy the
+//               scales into shared memory a window of k-blocks ahead (cp.async), so no
+//               scale load waits on the critical path.
 // The schedules are the static and persistent ones (whole tiles; each work item starts
 // at k = 0).  Every wait is bounded as in the plain kernel.
 #pragma once
@@ -32,61 +35,88 @@
 
 namespace tst {
 
-constexpr int kBsBuffers = 4;   // k-block partials in TMEM, 128 columns each
+constexpr int kBsBuffers = 4;   // k-block partials in TMEM, 128 columns each (two slots of two)
+constexpr int kBsPairSlots = 2;    // partial slots (pairs of buffers), one per MMA issuer
 constexpr int kBsWarps = 8;     // the accumulating (epilogue) warps, 2-9
 
-template <int DT>
-__device__ __forceinline__ void run_mma_bs(const KernelParams& p, const Ctx& c, uint32_t tmem_base, uint32_t smem_a,
-                                           uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty,
+// MMA issuer r (0 or 1) of the pairs of k-blocks: pair q of this CTA (counted over its
+// work items; an item's k-blocks pair up from its first, an odd last one alone) goes to
+// slot q & 1, whose two partial buffers are TMEM columns (2 (q & 1) + {0, 1}) * 128, and
+// is issued by issuer q & 1, which alone waits PEMPTY and commits PFULL of that slot.  Two
+// issuers, because one thread issues MMAs, commits and waits about as fast as the tensor
+// core computes a 128 x 128 x 32 MMA: each overlaps its handshakes with the other's MMAs.
+// An issuer waits FULL of each operand stage its k-blocks read and commits EMPTY after
+// the last of them (with 32-wide k-blocks the two pairs of a k-tile go to both issuers,
+// so the plan's EMPTY barriers count two commits).  PB = bk / 32 MMAs per k-block.
+template <int PB>
+__device__ __forceinline__ void run_mma_bs(const KernelParams& p, const Ctx& c, int r, uint32_t tmem_base,
+                                           uint32_t smem_a, uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty,
                                            uint32_t bar_pfull, uint32_t bar_pempty, uint32_t bar_drain) {
   using Cfg = TileCfg<128, 1, 1>;
+  constexpr int PER_ATOM = 4 / PB;   // k-blocks per k-tile (one 128-element atom)
   const uint32_t idesc = ptx::make_idesc(0u, kBlockM, 128) | p.fmt_ab;
-  const int per_block = p.bs_k / 32;   // MMAs of K = 32 per k-block
-  int stage = 0, pb = 0;
-  uint32_t phase = 0, pphase = 0;
-  bool ok = true;
   const uint64_t a_desc0 = ptx::sw128_kmajor_desc(smem_a);
   const uint64_t b_desc0 = ptx::sw128_kmajor_desc(smem_b);
+  int32_t kt_item = 0;   // k-tiles of this CTA before the current item
+  int32_t kt_cur = 0;    // the k-tile (stage, phase) describe
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t q0 = 0;       // pairs of this CTA before the current item
+  bool ok = true;
+  long long wait_full = 0, wait_pempty = 0, kblocks = 0;   // role-cycle counters (debug)
+  const bool stats = p.stats != nullptr && r == 0;
   WorkIter it;
   work_begin(p.sched, c.unit, it);
   WorkItem w;
-  long long wait_full = 0, wait_pempty = 0, kblocks = 0;   // role-cycle counters (debug)
   while (ok && work_next(p.sched, it, w)) {
-    int kk = 0;   // MMA index inside the work item
-    for (int32_t i = 0; i < w.k_count; ++i) {
-      const long long t0 = p.stats ? clock64() : 0;
-      if (!wait_phase<1>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
-      if (p.stats) wait_full += clock64() - t0;
-      const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
-      const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
+    const int nkb = w.k_count * PER_ATOM;
+    const int npairs = (nkb + 1) >> 1;
+    for (int i = static_cast<int>((q0 + static_cast<uint32_t>(r)) & 1u); i < npairs; i += 2) {
+      const uint32_t use = (q0 + static_cast<uint32_t>(i)) >> 1;   // earlier uses of slot r
+      const long long t1 = stats ? clock64() : 0;
+      if (!wait_phase<1>(p, c, bar_pempty + 8 * r, (use & 1u) ^ 1u, ROLE_MMA)) { ok = false; break; }
+      if (stats) wait_pempty += clock64() - t1;
+      ptx::tc_fence_after();
+      const int j0 = 2 * i;
+      const int j1 = j0 + 2 < nkb ? j0 + 2 : nkb;
+      for (int j = j0; j < j1; ++j) {
+        const int jin = j % PER_ATOM;   // k-block inside its k-tile
+        if (j == j0 || jin == 0) {      // this issuer's first k-block of a k-tile: its stage
+          const int32_t kt = kt_item + j / PER_ATOM;
+          while (kt_cur < kt) {
+            ++kt_cur;
+            if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+          }
+          const long long t0 = stats ? clock64() : 0;
+          if (!wait_phase<1>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
+          if (stats) wait_full += clock64() - t0;
+        }
+        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
+        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
+        const uint32_t d = tmem_base + static_cast<uint32_t>((2 * r + (j - j0)) * 128);
 #pragma unroll
-      for (int k = 0; k < 4; ++k, ++kk) {
-        const int pos = kk % per_block;
-        if (pos == 0) {   // a new k-block: its partial buffer must have been read
-          const long long t1 = p.stats ? clock64() : 0;
-          if (!wait_phase<1>(p, c, bar_pempty + 8 * pb, pphase ^ 1u, ROLE_MMA)) { ok = false; break; }
-          if (p.stats) { wait_pempty += clock64() - t1; ++kblocks; }
-          ptx::tc_fence_after();
+        for (int pos = 0; pos < PB; ++pos) {
+          // 32 bytes of K per MMA inside the 128-byte atom; the first MMA overwrites
+          const uint64_t off = static_cast<uint64_t>((jin * PB + pos) * 2);
+          ptx::mma_f8(d, a_desc + off, b_desc + off, idesc, pos != 0);
         }
-        // 32 bytes of K per MMA inside the 128-byte atom
-        const uint64_t off = static_cast<uint64_t>(k * 2);
-        ptx::mma_f8(tmem_base + static_cast<uint32_t>(pb * 128), a_desc + off, b_desc + off, idesc, pos != 0);
-        if (pos == per_block - 1) {
-          ptx::mma_commit(bar_pfull + 8 * pb);
-          if (++pb == kBsBuffers) { pb = 0; pphase ^= 1u; }
-        }
+        if (stats) ++kblocks;
+        // the stage is free once this issuer's MMAs reading it have completed
+        if (j == j1 - 1 || jin == PER_ATOM - 1) ptx::mma_commit(bar_empty + 8 * stage);
       }
       if (!ok) break;
-      ptx::mma_commit(bar_empty + 8 * stage);   // the stage is free once these MMAs have read it
-      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+      ptx::mma_commit(bar_pfull + 8 * r);
     }
+    q0 += static_cast<uint32_t>(npairs);
+    kt_item += w.k_count;
   }
-  if (p.stats) {
+  if (stats) {
     p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_FULL] = wait_full;
-    p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_TEMPTY] = wait_pempty;   // partial buffers
-    p.stats[blockIdx.x * kStatSlots + STAT_KBLOCKS] = kblocks;               // k-blocks
+    p.stats[blockIdx.x * kStatSlots + STAT_MMA_WAIT_TEMPTY] = wait_pempty;   // partial slots
+    p.stats[blockIdx.x * kStatSlots + STAT_KBLOCKS] = kblocks * 2;           // k-blocks (both issuers)
   }
-  // every MMA issued above completes before TMEM can be released
+  // every MMA this issuer issued completes before TMEM can be released (the drain barrier
+  // counts both issuers' commits)
   ptx::mma_commit(bar_drain);
   const uint64_t t0 = ptx::globaltimer();
   while (!ptx::mbar_try_wait(bar_drain, 0)) {
@@ -97,125 +127,166 @@ __device__ __forceinline__ void run_mma_bs(const KernelParams& p, const Ctx& c, 
   }
 }
 
-// Row of B's scales for column `col` (clamped into the matrix: columns past N carry zero
-// partials and need only some finite scale)
-__device__ __forceinline__ int32_t bs_col_row(const KernelParams& p, int32_t col) {
-  col = col < p.N ? col : p.N - 1;
-  return p.bs_rows == 1 ? col : col / p.bs_rows;
+// Scale windows: the epilogue warps copy the scales of kBsWindow consecutive k-blocks
+// of a work item into shared memory ahead of use, laid out per k-block as 128 row scales
+// of A (rows of the tile) then 128 column scales of B (columns of the tile), so a warp
+// reads its rows' scales conflict-free and its columns' scales by broadcast.  Two window
+// buffers alternate in the A slot of the ring's last stage (the plan leaves it out of
+// the ring); window g + 1 is copied while window g is in use, across work items too.
+constexpr int kBsWindow = 8;                      // k-blocks per window (even)
+constexpr int kBsScalesPerKb = 256;                     // scales per k-block in a window
+constexpr int kBsWindowBytes = kBsWindow * kBsScalesPerKb * 4;
+constexpr uint32_t kBsBarrier = 1;                // named barrier of the accumulating warps
+
+// Copy the scales of k-blocks kb0 .. kb0 + kBsWindow - 1 of item w into the window at
+// shared address dst; accumulating thread e (0-255) copies slot e of each k-block.
+__device__ __forceinline__ void bs_stage_window(const KernelParams& p, const WorkItem& w, int32_t kb0, uint32_t dst,
+                                                int e) {
+  const bool is_a = e < 128;
+  const int32_t lim = is_a ? p.M : p.N;
+  int32_t idx = is_a ? w.row0 + e : w.col0 + (e - 128);
+  idx = idx < lim ? idx : lim - 1;   // rows and columns past the matrix carry zero partials
+  const float* src = (is_a ? p.bs_a : p.bs_b) + static_cast<int64_t>(idx / p.bs_rows) * p.bs_kblocks;
+#pragma unroll
+  for (int i = 0; i < kBsWindow; ++i) {
+    int32_t kb = kb0 + i;
+    kb = kb < p.bs_kblocks ? kb : p.bs_kblocks - 1;   // k-blocks past K hold zero partials
+    ptx::cp_async_4(dst + static_cast<uint32_t>((i * kBsScalesPerKb + e) * 4), src + kb);
+  }
+  ptx::cp_async_commit();
 }
 
-// Fold the partials of k-blocks kb0 and kb1 (v[0..31] and v[32..63], columns col0 ..
-// col0 + 31 of this thread's row) into r[0..31].  `b_row` >= 0: the 32 columns share that
-// row of B's scales; else each column has its own.
-__device__ __forceinline__ void bs_fold(const KernelParams& p, float s_a0, float s_a1, int32_t kb0, int32_t kb1,
-                                        int32_t b_row, int32_t col0, const float (&v)[64], float* r) {
-  if (b_row >= 0) {
-    const float* sb = p.bs_b + static_cast<int64_t>(b_row) * p.bs_kblocks;
-    const float s0 = s_a0 * __ldg(sb + kb0), s1 = s_a1 * __ldg(sb + kb1);
+// r[q] += s * v[q] for q = 0 .. 31 (one k-block's partials of a 32-column chunk), two
+// columns per packed FMA, each lane fused and rounded like fmaf.
+__device__ __forceinline__ void bs_fold_shared(float s, const float (&v)[32], float* r) {
 #pragma unroll
-    for (int q = 0; q < 32; ++q) r[q] = fmaf(s1, v[32 + q], fmaf(s0, v[q], r[q]));
-  } else {
+  for (int q = 0; q < 32; q += 2) ptx::fma_f32x2(r[q], r[q + 1], s, s, v[q], v[q + 1]);
+}
+
+// The same with one scale of B per column: r[q] += (sa * sb[q]) * v[q] (sb in the window,
+// 16-byte aligned, read by broadcast four at a time).
+__device__ __forceinline__ void bs_fold_columns(float sa, const float* sb, const float (&v)[32], float* r) {
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      const float* sb = p.bs_b + static_cast<int64_t>(bs_col_row(p, col0 + q)) * p.bs_kblocks;
-      r[q] = fmaf(s_a1 * __ldg(sb + kb1), v[32 + q], fmaf(s_a0 * __ldg(sb + kb0), v[q], r[q]));
-    }
+  for (int q = 0; q < 32; q += 4) {
+    const float4 b = *reinterpret_cast<const float4*>(sb + q);
+    float t0, t1, t2, t3;
+    ptx::mul_f32x2(t0, t1, sa, sa, b.x, b.y);
+    ptx::mul_f32x2(t2, t3, sa, sa, b.z, b.w);
+    ptx::fma_f32x2(r[q], r[q + 1], t0, t1, v[q], v[q + 1]);
+    ptx::fma_f32x2(r[q + 2], r[q + 3], t2, t3, v[q + 2], v[q + 3]);
   }
 }
 
-template <int OUT>
+// PER_COL: B's scale rows change inside a 32-column chunk (br not a multiple of 32), so
+// every column takes its own scale; else one per chunk.
+template <int OUT, bool PER_COL>
 __device__ __forceinline__ void run_epilogue_bs(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
-                                                uint32_t bar_pfull, uint32_t bar_pempty) {
+                                                uint32_t bar_pfull, uint32_t bar_pempty, uint32_t win_smem,
+                                                const float* win_ptr) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int e = threadIdx.x - 64;         // 0-255 among the accumulating warps
   const int group = (warp - 2) >> 2;      // which 64 columns of the tile
   const int quad = warp & 3;              // TMEM lane quadrant this warp may access
   const int row_in_tile = quad * 32 + lane;
   const int per_atom = 128 / p.bs_k;      // k-blocks per k-tile
+  const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
   float alpha = p.alpha;
   if (p.use_scales) alpha = alpha * __ldg(p.scales) * __ldg(p.scales + 1);
-  int pb = 0;
-  uint32_t pphase = 0;
+  uint32_t q = 0;   // pairs of k-blocks of this CTA so far: pair q uses slot q & 1
   WorkIter it;
   work_begin(p.sched, c.unit, it);
-  WorkItem w;
+  WorkItem w, wn;
   bool ok = true;
   const bool stat_thread = p.stats != nullptr && threadIdx.x == 64;   // warp 2, lane 0
   long long wait_pfull = 0, busy = 0, items = 0;
-  // lane 0 waits (bounded) for partial buffer b and the warp follows its verdict
+  // lane 0 waits (bounded) for partial slot b and the warp follows its verdict
   auto wait_partial = [&](int b, uint32_t par) {
     bool got = true;
     if (lane == 0) got = wait_phase<1>(p, c, bar_pfull + 8 * b, par, ROLE_EPILOGUE);
     return __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
   };
-  while (ok && work_next_warp(p.sched, it, w)) {
+  // Every accumulating warp walks the same items and windows and meets the same barriers:
+  // after a failed wait a warp keeps walking (skipping the work), so none is left waiting
+  // at a barrier for a warp that has left.
+  bool have = work_next(p.sched, it, w);
+  uint32_t g = 0;   // windows begun so far: window g uses buffer g & 1
+  if (have) bs_stage_window(p, w, 0, win_smem, e);
+  while (have) {
+    const bool have_next = work_next(p.sched, it, wn);
     const int32_t row = w.row0 + row_in_tile;
     const int32_t col_base = w.col0 + group * 64;
-    // rows past M carry zero partials: any finite scale row will do
-    const float* sa = p.bs_a + static_cast<int64_t>((row < p.M ? row : p.M - 1) / p.bs_rows) * p.bs_kblocks;
-    // the row of B's scales of each 32-column half, when the half shares one (computed once
-    // per item); -1 when its columns have rows of their own
-    const bool one_b = (col_base / p.bs_rows) == ((col_base + 63) / p.bs_rows);
-    const bool halves_shared = one_b || (p.bs_rows & 31) == 0;
-    const int32_t b_row0 = halves_shared ? bs_col_row(p, col_base) : -1;
-    const int32_t b_row1 = halves_shared ? bs_col_row(p, col_base + 32) : -1;
     float r[64];
 #pragma unroll
     for (int j = 0; j < 64; ++j) r[j] = 0.0f;
     const int nkb = w.k_count * per_atom;
-    // two k-blocks per step (buffers pb and pb + 1, the MMAs filling the other two
-    // meanwhile): both partials' loads in flight before one wait; an odd last k-block
-    // pairs with itself at a zero weight
-    for (int j = 0; j < nkb; j += 2) {
-      const bool pair = j + 1 < nkb;
-      const int pb1 = pair ? (pb + 1 == kBsBuffers ? 0 : pb + 1) : pb;
-      const uint32_t par1 = pair && pb1 == 0 ? (pphase ^ 1u) : pphase;
-      const long long t0 = stat_thread ? clock64() : 0;
-      if (!wait_partial(pb, pphase) || (pair && !wait_partial(pb1, par1))) { ok = false; break; }
-      const long long t1 = stat_thread ? clock64() : 0;
-      if (stat_thread) wait_pfull += t1 - t0;
-      ptx::tc_fence_after();
-      // k-blocks past K (the zero-filled rest of the last k-tile) reuse the last scale
-      const int32_t kb0 = j < p.bs_kblocks ? j : p.bs_kblocks - 1;
-      const int32_t kb1 = j + 1 < p.bs_kblocks ? j + 1 : p.bs_kblocks - 1;
-      const float s_a0 = __ldg(sa + kb0);
-      const float s_a1 = pair ? __ldg(sa + kb1) : 0.0f;
-      const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int nwin = (nkb + kBsWindow - 1) / kBsWindow;
+    for (int wi = 0; wi < nwin; ++wi, ++g) {
+      ptx::cp_async_wait_all();
+      ptx::named_bar_sync(kBsBarrier, 256);   // window g is in place; window g - 1 is read
+      const uint32_t next_buf = win_smem + ((g + 1) & 1u) * kBsWindowBytes;
+      if (wi + 1 < nwin) bs_stage_window(p, w, (wi + 1) * kBsWindow, next_buf, e);
+      else if (have_next) bs_stage_window(p, wn, 0, next_buf, e);
+      const float* win = win_ptr + (g & 1u) * (kBsWindowBytes / 4);
+      const int jend = nkb < (wi + 1) * kBsWindow ? nkb : (wi + 1) * kBsWindow;
+      // a pair of k-blocks per step (one slot: two partial buffers, the other slot filling
+      // meanwhile); an odd last k-block alone
+      for (int j = wi * kBsWindow; ok && j < jend; j += 2, ++q) {
+        const bool pair = j + 1 < jend;
+        const int slot = static_cast<int>(q & 1u);
+        const int pb = 2 * slot, pb1 = 2 * slot + 1;
+        const long long t0 = stat_thread ? clock64() : 0;
+        if (!wait_partial(slot, (q >> 1) & 1u)) { ok = false; break; }
+        const long long t1 = stat_thread ? clock64() : 0;
+        if (stat_thread) wait_pfull += t1 - t0;
+        ptx::tc_fence_after();
+        const float* s0 = win + (j - wi * kBsWindow) * kBsScalesPerKb;
+        const float* s1 = s0 + kBsScalesPerKb;
+        const float sa0 = s0[row_in_tile];
+        const float sa1 = pair ? s1[row_in_tile] : 0.0f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t col = static_cast<uint32_t>(group * 64 + h * 32);
+          const int cs = 128 + group * 64 + h * 32;   // this chunk's column scales in the window
+          // one k-block's 32 columns per TMEM load (the pair's partials one after the other
+          // keep the live registers under the cap of 11 warps per CTA)
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (k == 1 && !pair) break;
+            const float* sk = k == 0 ? s0 : s1;
+            float v[32];
+            ptx::tmem_load_32cols(tmem_base + lane_off + static_cast<uint32_t>((k == 0 ? pb : pb1) * 128) + col, v);
+            if (PER_COL) bs_fold_columns(k == 0 ? sa0 : sa1, sk + cs, v, r + 32 * h);
+            else bs_fold_shared((k == 0 ? sa0 : sa1) * sk[cs], v, r + 32 * h);
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar_pempty + 8 * slot);   // the partials are in registers
+        if (stat_thread) busy += clock64() - t1;
+      }
+    }
+    if (ok) {
+      // the basic epilogue on the block-scaled sum: alpha, column bias, ReLU, cast, store
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint32_t col = static_cast<uint32_t>(group * 64 + h * 32);
-        float v[64];
-        ptx::tmem_load_2x32(tmem_base + lane_off + static_cast<uint32_t>(pb * 128) + col,
-                            tmem_base + lane_off + static_cast<uint32_t>(pb1 * 128) + col, v);
-        bs_fold(p, s_a0, s_a1, kb0, kb1, h == 0 ? b_row0 : b_row1, col_base + 32 * h, v, r + 32 * h);
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {   // the partials are in registers
-        ptx::mbar_arrive(bar_pempty + 8 * pb);
-        if (pair) ptx::mbar_arrive(bar_pempty + 8 * pb1);
-      }
-      if (stat_thread) busy += clock64() - t1;
-      for (int step = 0; step < (pair ? 2 : 1); ++step)
-        if (++pb == kBsBuffers) { pb = 0; pphase ^= 1u; }
-    }
-    if (!ok) break;
-    // the basic epilogue on the block-scaled sum: alpha, column bias, ReLU, cast, store
+        const int32_t col0 = col_base + h * 32;
+        float z[32];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int32_t col0 = col_base + h * 32;
-      float z[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int32_t col = col0 + q;
-        const float b = (p.has_bias && col < w.col_end) ? __ldg(p.bias + col) : 0.0f;
-        z[q] = fmaf(alpha, r[32 * h + q], b);
-        if (p.relu) z[q] = fmaxf(z[q], 0.0f);
+        for (int q = 0; q < 32; ++q) {
+          const int32_t col = col0 + q;
+          const float b = (p.has_bias && col < w.col_end) ? __ldg(p.bias + col) : 0.0f;
+          z[q] = fmaf(alpha, r[32 * h + q], b);
+          if (p.relu) z[q] = fmaxf(z[q], 0.0f);
+        }
+        store_chunk<OUT>(p.C, w.col_end, row, w.row_end, col0, z);
       }
-      store_chunk<OUT>(p.C, w.col_end, row, w.row_end, col0, z);
+      items += 1;
     }
-    items += 1;
+    w = wn;
+    have = have_next;
   }
+  ptx::cp_async_wait_all();
   if (stat_thread) {
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_WAIT_TFULL] = wait_pfull;   // waits for partials
     p.stats[blockIdx.x * kStatSlots + STAT_EPI_BUSY] = busy;               // loading and folding them
@@ -223,10 +294,11 @@ __device__ __forceinline__ void run_epilogue_bs(const KernelParams& p, const Ctx
   }
 }
 
-template <int DT, int OUT>
+template <int DT, int OUT, bool PER_COL>
 __global__ void __launch_bounds__(kBsThreads, 1) gemm_bs_kernel(const __grid_constant__ KernelParams p) {
   using Cfg = TileCfg<128, 1, 1>;
   static_assert(Cfg::NACC == kBsBuffers, "the partial buffers use the accumulator barriers' slots");
+  static_assert(2 * kBsWindowBytes <= Cfg::A_BYTES, "two scale windows fit one stage's A slot");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t smem_a = ptx::smem_addr(smem);
@@ -236,6 +308,8 @@ __global__ void __launch_bounds__(kBsThreads, 1) gemm_bs_kernel(const __grid_con
   const uint32_t bar_pfull = bar_empty + 8 * Cfg::STAGES;
   const uint32_t bar_pempty = bar_pfull + 8 * kBsBuffers;
   const uint32_t bar_drain = bar_pempty + 8 * kBsBuffers;
+  // the scale windows: the A slot of the ring's last stage (p.stages < Cfg::STAGES)
+  uint8_t* win = smem + (Cfg::STAGES - 1) * Cfg::A_BYTES;
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + Cfg::MISC_OFFSET);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -251,15 +325,17 @@ __global__ void __launch_bounds__(kBsThreads, 1) gemm_bs_kernel(const __grid_con
   c.unit = static_cast<int32_t>(blockIdx.x);
 
   if (threadIdx.x == 0) {
+    // with 32-wide k-blocks both issuers read every stage (one pair each)
+    const uint32_t readers = p.bs_k == 32 ? 2u : 1u;
     for (int s = 0; s < Cfg::STAGES; ++s) {
       ptx::mbar_init(bar_full + 8 * s, 1);
-      ptx::mbar_init(bar_empty + 8 * s, 1);
+      ptx::mbar_init(bar_empty + 8 * s, readers);
     }
-    for (int b = 0; b < kBsBuffers; ++b) {
+    for (int b = 0; b < kBsPairSlots; ++b) {
       ptx::mbar_init(bar_pfull + 8 * b, 1);
       ptx::mbar_init(bar_pempty + 8 * b, kBsWarps);
     }
-    ptx::mbar_init(bar_drain, 1);
+    ptx::mbar_init(bar_drain, 2);
     ctl->abort = 0;
     ctl->ep_ok = 0;
     ptx::fence_mbar_init();
@@ -277,11 +353,19 @@ __global__ void __launch_bounds__(kBsThreads, 1) gemm_bs_kernel(const __grid_con
 
   if (warp == 0) {
     if (lane == 0) run_producer<128, DT, 1, 1, 1>(p, c, smem_a, smem_b, bar_full, bar_empty);
-  } else if (warp == 1) {
-    if (lane == 0)
-      run_mma_bs<DT>(p, c, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_pfull, bar_pempty, bar_drain);
+  } else if (warp == 1 || warp == 10) {
+    if (lane == 0) {
+      const int r = warp == 1 ? 0 : 1;
+      if (p.bs_k == 32)
+        run_mma_bs<1>(p, c, r, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_pfull, bar_pempty, bar_drain);
+      else if (p.bs_k == 64)
+        run_mma_bs<2>(p, c, r, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_pfull, bar_pempty, bar_drain);
+      else
+        run_mma_bs<4>(p, c, r, tmem_base, smem_a, smem_b, bar_full, bar_empty, bar_pfull, bar_pempty, bar_drain);
+    }
   } else {
-    run_epilogue_bs<OUT>(p, c, tmem_base, bar_pfull, bar_pempty);
+    run_epilogue_bs<OUT, PER_COL>(p, c, tmem_base, bar_pfull, bar_pempty, ptx::smem_addr(win),
+                                  reinterpret_cast<const float*>(win));
   }
 
   ptx::tc_fence_before();

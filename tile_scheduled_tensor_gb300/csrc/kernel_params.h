@@ -279,9 +279,12 @@ constexpr int kReduceRows = 16;  // rows of a 128-row tile half per CTA
 const void* tst_reduce_kernel(int out_type);
 
 // Block-scaled operands (gemm_bs.cu): FP8 operands, single CTAs, 128-column tiles, one-atom
-// k-tiles; warps 2-9 accumulate the scaled k-block partials (320 threads).
-constexpr int kBsThreads = 320;
-const void* tst_bs_kernel(int out_type);
+// k-tiles; warps 1 and 10 issue the MMAs, warps 2-9 accumulate the scaled k-block partials
+// (352 threads).  per_col: one
+// scale of B per column (block rows not a multiple of 32).  The ring's last stage holds the
+// scale windows, so a plan runs at most (the tile's stages - 1) stages.
+constexpr int kBsThreads = 352;
+const void* tst_bs_kernel(int out_type, bool per_col);
 
 inline int tst_kernel_threads(int bn, int ka, bool ext = false) {
   return ((bn == 128 && ka == 2) ? tst::kThreadsDual : tst::kThreads) + (ext ? 128 : 0);

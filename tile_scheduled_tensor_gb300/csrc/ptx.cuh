@@ -321,6 +321,38 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Asynchronous 4-byte copy global -> shared (the Ampere-style cp.async, outside the
+// bulk/TMA proxy): complete after cp_async_wait_all, visible to other threads after a
+// barrier that follows it.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Packed FP32 pairs (sm_100 and later): each lane is the plain round-to-nearest FP32
+// operation, so the results equal fmaf / __fmul_rn lane by lane; one instruction for two.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+// (d0, d1) += (a0, a1) * (b0, b1), fused, round to nearest
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f32x2(a0, a1)), "l"(f32x2(b0, b1)), "l"(f32x2(d0, d1)));
+  f32x2_split(d, d0, d1);
+}
+// (d0, d1) = (a0, a1) * (b0, b1), round to nearest
+__device__ __forceinline__ void mul_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f32x2(a0, a1)), "l"(f32x2(b0, b1)));
+  f32x2_split(d, d0, d1);
+}
+
 }  // namespace ptx
 }  // namespace tst
 
