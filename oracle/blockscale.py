@@ -32,13 +32,21 @@ def expand(s: np.ndarray, rows: int, K: int, br: int, bk: int) -> np.ndarray:
     return np.repeat(np.repeat(s, br, axis=0), bk, axis=1)[:rows, :K]
 
 
-def gemm_block_scaled(a: np.ndarray, b: np.ndarray, sA: np.ndarray, sB: np.ndarray, block=(1, 32)):
+def gemm_block_scaled(a: np.ndarray, b: np.ndarray, sA: np.ndarray, sB: np.ndarray, block=(1, 32), rows=None):
     """C (M x N, FP64) from decoded operands a (M x K) and b (N x K) and their tile
-    scales sA (ceil(M / br) x ceil(K / bk)) and sB (ceil(N / br) x ceil(K / bk))."""
+    scales sA (ceil(M / br) x ceil(K / bk)) and sB (ceil(N / br) x ceil(K / bk)).
+    rows: only these rows of C (the same definition evaluated for a subset of i)."""
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     br, bk = block
     (M, K), (N, K2) = a.shape, b.shape
     if K != K2:
         raise ValueError("A and B disagree on K")
-    return (a * expand(sA, M, K, br, bk)) @ (b * expand(sB, N, K, br, bk)).T
+    if rows is None:
+        return (a * expand(sA, M, K, br, bk)) @ (b * expand(sB, N, K, br, bk)).T
+    rows = np.asarray(rows, dtype=np.int64)
+    s = np.asarray(sA, dtype=np.float64)
+    if s.shape != (-(-M // br), -(-K // bk)):
+        raise ValueError(f"scale shape {s.shape} does not tile {M} x {K} by {br} x {bk}")
+    sa_rows = np.repeat(s[rows // br], bk, axis=1)[:, :K]
+    return (a[rows] * sa_rows) @ (b * expand(sB, N, K, br, bk)).T

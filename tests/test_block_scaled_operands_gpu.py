@@ -17,7 +17,8 @@ import synthetic
 import tile_scheduled_tensor_gb300 as tst
 from oracle import blockscale as BS
 
-from gemm_check import device_codes, host_values
+from gemm_check import assert_close, device_codes, host_values, make_inputs, plan_for, sample_rows, to_device
+from synthetic.workloads import WORKLOADS
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +140,26 @@ def test_block_scaled_timeout_on_missing_load_reports_and_recovers():
     assert tst.gemm_status_query(plan)[0] == tst.TST_OK
     want = BS.gemm_block_scaled(oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3"), sA, sB, (32, 32))
     assert np.array_equal(host_values(D), want)
+
+
+@pytest.mark.parametrize("name", ["c3b_e4m3_8192_blk32", "c3b_e4m3_8192_blk1x128", "c3b_e4m3_8192_blk128"])
+def test_block_scaled_workload_full_size_sampled_rows(name):
+    # the benchmark's 8192^3 workload in the benchmark's plan, with its seeded power-of-two
+    # block scales and tensor-wise scales: sampled rows against the oracle within the bound
+    import bench
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    sA, sB = bench.block_scales(w)
+    plan = plan_for(w, ab_block=w["ab_block"])
+    A, B, _, scales = to_device(inp)
+    C = torch.empty(w["M"], w["N"], dtype=torch.bfloat16, device="cuda")
+    tst.gemm_run(plan, A, B, C, scales=scales, a_block_scales=torch.from_numpy(sA).cuda(),
+                 b_block_scales=torch.from_numpy(sB).cuda())
+    st, word = tst.gemm_status_query(plan)
+    assert st == tst.TST_OK, (tst.gemm_status_string(st), hex(word))
+    rows = sample_rows(w["M"], count=12)
+    a, b = oracle.decode(inp.A, "e4m3"), oracle.decode(inp.B, "e4m3")
+    s = w.get("alpha", 1.0) * float(inp.scales[0]) * float(inp.scales[1])
+    z = s * BS.gemm_block_scaled(a, b, sA, sB, w["ab_block"], rows=rows)
+    ad = abs(s) * BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, w["ab_block"], rows=rows)
+    assert_close(host_values(C)[rows], z, ad, "bf16", name)

@@ -56,3 +56,26 @@ def test_scale_shapes_must_tile_the_operands():
     a, b = np.zeros((5, 64)), np.zeros((3, 64))
     with pytest.raises(ValueError):
         BS.gemm_block_scaled(a, b, np.ones((5, 3)), np.ones((3, 2)), block=(1, 32))
+
+
+def test_row_subset_equals_the_full_result_rows():
+    # the rows option evaluates the same definition for a subset of C's rows, ragged row
+    # blocks included: exactly the full result's rows where the arithmetic is exact (small
+    # integers, power-of-two scales), and within FP64 rounding otherwise (the library matrix
+    # product sums in an order that depends on the shapes)
+    rng = np.random.default_rng(3)
+    M, N, K = 70, 20, 96
+    rows = np.array([0, 1, 31, 32, 33, 63, 64, 69])
+    for br, bk in ((1, 32), (32, 32), (16, 64)):
+        shA, shB = (-(-M // br), -(-K // bk)), (-(-N // br), -(-K // bk))
+        a = rng.integers(-8, 9, size=(M, K)).astype(np.float64)
+        b = rng.integers(-8, 9, size=(N, K)).astype(np.float64)
+        sA, sB = 2.0 ** rng.integers(-3, 4, size=shA), 2.0 ** rng.integers(-3, 4, size=shB)
+        full = BS.gemm_block_scaled(a, b, sA, sB, (br, bk))
+        assert np.array_equal(BS.gemm_block_scaled(a, b, sA, sB, (br, bk), rows=rows), full[rows])
+        a, b = rng.normal(size=(M, K)), rng.normal(size=(N, K))
+        sA, sB = rng.uniform(0.5, 2, size=shA), rng.uniform(0.5, 2, size=shB)
+        full = BS.gemm_block_scaled(a, b, sA, sB, (br, bk))
+        assert np.allclose(BS.gemm_block_scaled(a, b, sA, sB, (br, bk), rows=rows), full[rows], rtol=1e-13, atol=1e-13)
+    with pytest.raises(ValueError):
+        BS.gemm_block_scaled(a, b, np.ones((2, 3)), np.ones((1, 3)), (1, 32), rows=[0])
