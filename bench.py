@@ -305,10 +305,14 @@ def setup_workload(w, tst, torch, row_block=None):
 
 
 def run_args(dev):
-    """Keyword arguments of gemm_run for the device operands of setup_workload."""
-    return dict(bias=dev.get("bias"), scales=dev.get("scales"), c=dev.get("c"), d_scale=dev.get("d_scale"),
-                amax=dev.get("amax"), a_block_scales=dev.get("a_block_scales"),
-                b_block_scales=dev.get("b_block_scales"))
+    """Keyword arguments of gemm_run (or gemm_grouped_run) for the device operands of
+    setup_workload; the block scales only for a workload that has them (gemm_run alone takes
+    block-scaled operands)."""
+    kw = dict(bias=dev.get("bias"), scales=dev.get("scales"), c=dev.get("c"), d_scale=dev.get("d_scale"),
+              amax=dev.get("amax"))
+    if "a_block_scales" in dev:
+        kw.update(a_block_scales=dev["a_block_scales"], b_block_scales=dev["b_block_scales"])
+    return kw
 
 
 def run_once(tst, plan, dev, C, stream=None):

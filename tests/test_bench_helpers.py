@@ -96,3 +96,17 @@ def test_block_scaled_oracle_step_is_the_oracle_on_sampled_rows():
     z, _ = bench.oracle_step(w, inp, rows)
     assert np.allclose(z, full[rows], rtol=1e-13, atol=1e-13)
     assert sa.shape == (3, 3) and sb.shape == (2, 3) and set(np.unique(np.log2(sa))) <= set(range(-3, 4))
+
+
+def test_run_args_match_the_entry_points_signatures():
+    # every keyword run_args passes is a parameter of the entry point run_once calls: the
+    # grouped run takes no block-scaled operands, so a workload without them passes none
+    import inspect
+    import tile_scheduled_tensor_gb300 as tst
+    plain = bench.run_args({"bias": 1, "scales": 2})
+    assert "a_block_scales" not in plain and "b_block_scales" not in plain
+    assert set(plain) <= set(inspect.signature(tst.gemm_grouped_run).parameters)
+    assert set(plain) <= set(inspect.signature(tst.gemm_run).parameters)
+    scaled = bench.run_args({"a_block_scales": 3, "b_block_scales": 4})
+    assert (scaled["a_block_scales"], scaled["b_block_scales"]) == (3, 4)
+    assert set(scaled) <= set(inspect.signature(tst.gemm_run).parameters)
