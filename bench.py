@@ -92,7 +92,8 @@ DESCR = {
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 128 << 20      # GB300's L2 (126.5 MiB), rounded up
 MAX_SETS = 16             # more input sets than this: flush L2 before every launch instead
-KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh",
+                  "gemm_blockscale.cuh", "gemm_bs.cu"]
 
 
 PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "sk_fixup", "l2_hint", "tma_boxes",
@@ -333,7 +334,8 @@ def elt_bytes(kind):
 
 def workload_bytes(w):
     """Bytes one launch of workload w reads and writes at least once: A, B, the output (and
-    the epilogue's addend matrix), from the shapes alone."""
+    the epilogue's addend matrix, or the block scales of block-scaled operands), from the
+    shapes alone."""
     fa, fb = operand_types(w["dtype"])
     out = elt_bytes(w["out"])
     shapes = group_shapes(w)
@@ -344,6 +346,9 @@ def workload_bytes(w):
     epi = w.get("epi") or {}
     if "c_dtype" in epi:
         total += w["M"] * w["N"] * elt_bytes(epi["c_dtype"])
+    if "ab_block" in w:   # one FP32 scale per br x bk tile of A and of B
+        br, bk = w["ab_block"]
+        total += (-(-w["M"] // br) + -(-w["N"] // br)) * -(-w["K"] // bk) * 4
     return total
 
 
