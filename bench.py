@@ -92,8 +92,9 @@ DESCR = {
 L2_FLUSH_BYTES = 512 << 20
 L2_BYTES = 128 << 20      # GB300's L2 (126.5 MiB), rounded up
 MAX_SETS = 16             # more input sets than this: flush L2 before every launch instead
-KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh",
-                  "gemm_blockscale.cuh", "gemm_bs.cu"]
+KERNEL_SOURCES = ["gemm_kernel.cuh", "ptx.cuh", "kernel_params.h", "tile_sched.h", "epilogue_ext.cuh"]
+# the block-scaled kernel reuses the plain kernel's producer and helpers
+BS_KERNEL_SOURCES = KERNEL_SOURCES + ["gemm_blockscale.cuh", "gemm_bs.cu"]
 
 
 PLAN_OPTION_KEYS = ("sk_groups", "bk", "stages", "num_ctas", "sk_forward", "sk_fixup", "l2_hint", "tma_boxes",
@@ -414,12 +415,13 @@ def aggregate(flops_per_rank: float, local_ms: float, world: int, max_reduce):
     return job_throughput(world * flops_per_rank, local_ms, max_reduce)
 
 
-def kernel_hash():
-    """Hash of the kernel sources' code (comments and blank space removed, so that a
-    comment edit does not invalidate a capture taken on the same code)."""
+def kernel_hash(sources=None):
+    """Hash of a kernel's sources' code (comments and blank space removed, so that a
+    comment edit does not invalidate a capture taken on the same code); the plain GEMM
+    kernel's sources by default."""
     import re
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, "tile_scheduled_tensor_gb300", "csrc", f)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -445,7 +447,8 @@ def dram_traffic(name):
     with open(path) as f:
         d = json.load(f)
     e = d.get(name)
-    if not e or e.get("kernel_hash") != kernel_hash():
+    sources = BS_KERNEL_SOURCES if "ab_block" in WORKLOADS.get(name, {}) else KERNEL_SOURCES
+    if not e or e.get("kernel_hash") != kernel_hash(sources):
         return None
     return e.get("bytes_per_launch")
 
@@ -1160,6 +1163,7 @@ def main():
             "clocks": head["clocks"],
             "workloads": extra,
             "kernel_hash": kernel_hash(),
+            "bs_kernel_hash": kernel_hash(BS_KERNEL_SOURCES),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
