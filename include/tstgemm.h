@@ -199,7 +199,7 @@ typedef struct {
                             15.3 multi-stage accumulation).  Needs FP8 operands, FP32 or BF16 D,
                             alpha / tensor-wise scales / column bias / ReLU only, the static or
                             persistent schedule, single CTAs with 128-column tiles and one-atom
-                            k-tiles (bn, cta_group, bk 0 or those values), stages 0 or 4 to 6
+                            k-tiles (bn, cta_group, bk 0 or those values), stages 0 or 2 to 6
                             (the ring's seventh stage holds the staged scales); else
                             TST_ERR_UNSUPPORTED. */
     int32_t ab_block_k;

@@ -98,9 +98,9 @@ def test_block_scaled_unit_scales_are_the_plain_fp8_gemm():
     assert np.array_equal(host_values(D), z)
 
 
-def test_block_scaled_four_stage_ring_and_many_items_exact():
-    # the smallest ring the two MMA issuers allow, an odd k-tile count (a lone last k-block
-    # per item) and several work items per CTA
+def test_block_scaled_two_stage_ring_and_many_items_exact():
+    # the smallest ring, an odd k-tile count (a lone last k-block per item, which flips the
+    # issuers' roles in the next item's pairs) and several work items per CTA
     M, N, K = 1536, 1280, 1152
     xa = synthetic.draw("int:4", 9611, M * K).reshape(M, K).astype(np.float32)
     xb = synthetic.draw("int:4", 9612, N * K).reshape(N, K).astype(np.float32)
@@ -108,8 +108,8 @@ def test_block_scaled_four_stage_ring_and_many_items_exact():
     for br, bk in ((1, 128), (32, 64), (32, 32)):
         sA, sB = _scales(9613, M, K, br, bk), _scales(9614, N, K, br, bk)
         plan = tst.gemm_plan_create(M, N, K, dtype="e4m3", mapping=("grouped_m", 4), schedule="persistent",
-                                    out_dtype="f32", ab_block=(br, bk), stages=4, num_ctas=19)
-        assert plan.info.stages == 4
+                                    out_dtype="f32", ab_block=(br, bk), stages=2, num_ctas=19)
+        assert plan.info.stages == 2
         D = torch.full((M, N), float("nan"), device="cuda")
         tst.gemm_run(plan, device_codes(A), device_codes(B), D, a_block_scales=torch.from_numpy(sA).cuda(),
                      b_block_scales=torch.from_numpy(sB).cuda())
@@ -163,3 +163,22 @@ def test_block_scaled_workload_full_size_sampled_rows(name):
     z = s * BS.gemm_block_scaled(a, b, sA, sB, w["ab_block"], rows=rows)
     ad = abs(s) * BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, w["ab_block"], rows=rows)
     assert_close(host_values(C)[rows], z, ad, "bf16", name)
+
+
+def test_block_scaled_single_k_tile_items_exact():
+    # K = 128 at 128-wide k-blocks: every work item is one lone k-block, so the issuers take
+    # alternate items; a two-stage ring; exact on small integers
+    M, N, K = 1024, 896, 128
+    xa = synthetic.draw("int:4", 9631, M * K).reshape(M, K).astype(np.float32)
+    xb = synthetic.draw("int:4", 9632, N * K).reshape(N, K).astype(np.float32)
+    A, B = synthetic.e4m3_bytes(xa), synthetic.e4m3_bytes(xb)
+    for br in (1, 128):
+        sA, sB = _scales(9633, M, K, br, 128), _scales(9634, N, K, br, 128)
+        plan = tst.gemm_plan_create(M, N, K, dtype="e4m3", mapping=("grouped_m", 2), schedule="persistent",
+                                    out_dtype="f32", ab_block=(br, 128), stages=2, num_ctas=7)
+        D = torch.full((M, N), float("nan"), device="cuda")
+        tst.gemm_run(plan, device_codes(A), device_codes(B), D, a_block_scales=torch.from_numpy(sA).cuda(),
+                     b_block_scales=torch.from_numpy(sB).cuda())
+        assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+        want = BS.gemm_block_scaled(oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3"), sA, sB, (br, 128))
+        assert np.array_equal(host_values(D), want), br

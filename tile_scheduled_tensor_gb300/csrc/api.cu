@@ -409,9 +409,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   p->stages = tst_kernel_stages(p->bn, p->cg, p->ka);
   if (p->bs) p->stages -= 1;   // the last stage's A slot holds the block-scaled kernel's scale windows
   if (o.stages != 0) {
-    // block-scaled: an MMA issuer skips up to three k-tiles that the other one reads, so
-    // its parity waits on a stage stay unambiguous only with four stages or more
-    if (o.stages < (p->bs ? 4 : 2) || o.stages > p->stages) { delete p; return TST_ERR_UNSUPPORTED; }
+    if (o.stages < 2 || o.stages > p->stages) { delete p; return TST_ERR_UNSUPPORTED; }
     p->stages = o.stages;
   }
   p->smem_bytes = tst_kernel_smem_bytes(p->bn, p->cg, p->ka);

@@ -14,12 +14,13 @@
 // Roles, 352 threads, one CTA per SM, single CTAs with 128 x 128 tiles and one-atom
 // k-tiles (128 e4m3 / e5m2 of K per stage):
 //   warp 0      the TMA producer of the plain kernel (run_producer).
-//   warps 1, 10 MMA issuers 0 and 1, taking alternate pairs of k-blocks: wait until the
-//               issuer's partial slot (two 128-column buffers) is free (PEMPTY[r]), issue
-//               each k-block's MMAs into its buffer (the first one overwriting), commit ->
-//               PFULL[r]; commit -> EMPTY[s] after the last MMA reading stage s.  The two
-//               slots fill the 512 TMEM columns, so one pair's MMAs run while the epilogue
-//               warps read the other's partials.
+//   warps 1, 10 MMA issuers 0 and 1, taking alternate k-blocks: for each pair of k-blocks
+//               wait until its partial slot (two 128-column buffers) is free (PEMPTY),
+//               issue the issuer's k-block of the pair into its buffer (the first MMA
+//               overwriting), commit -> PFULL (counting both issuers); commit -> EMPTY[s]
+//               after the last MMA reading stage s.  The two slots fill the 512 TMEM
+//               columns, so one pair's MMAs run while the epilogue warps read the other's
+//               partials.
 //   warps 2-9   two warpgroups, each taking 64 of the tile's 128 columns (a warp reads the
 //               TMEM lanes of its quadrant, 32 rows): a pair of k-blocks at a time, wait
 //               PFULL of its slot, load the two partials one after the other, add
@@ -36,18 +37,22 @@
 namespace tst {
 
 constexpr int kBsBuffers = 4;   // k-block partials in TMEM, 128 columns each (two slots of two)
-constexpr int kBsPairSlots = 2;    // partial slots (pairs of buffers), one per MMA issuer
+constexpr int kBsPairSlots = 2; // partial slots (pairs of buffers)
 constexpr int kBsWarps = 8;     // the accumulating (epilogue) warps, 2-9
 
-// MMA issuer r (0 or 1) of the pairs of k-blocks: pair q of this CTA (counted over its
-// work items; an item's k-blocks pair up from its first, an odd last one alone) goes to
-// slot q & 1, whose two partial buffers are TMEM columns (2 (q & 1) + {0, 1}) * 128, and
-// is issued by issuer q & 1, which alone waits PEMPTY and commits PFULL of that slot.  Two
-// issuers, because one thread issues MMAs, commits and waits about as fast as the tensor
-// core computes a 128 x 128 x 32 MMA: each overlaps its handshakes with the other's MMAs.
-// An issuer waits FULL of each operand stage its k-blocks read and commits EMPTY after
-// the last of them (with 32-wide k-blocks the two pairs of a k-tile go to both issuers,
-// so the plan's EMPTY barriers count two commits).  PB = bk / 32 MMAs per k-block.
+// MMA issuer r (0 or 1).  The k-blocks of each work item pair up from its first (an odd
+// last one alone); pair q of this CTA (counted over its items) uses slot q & 1, whose two
+// partial buffers are TMEM columns (2 (q & 1) + {0, 1}) * 128.  Both issuers work on every
+// pair: issuer r issues the k-blocks whose index over all of this CTA's items has parity
+// r (so each issuer takes every other k-block, across items too), each into the buffer of
+// its position in the pair, after waiting PEMPTY of the slot; each commits PFULL of the
+// slot (counting two), or only arrives on it when the pair is a lone k-block of the other
+// issuer.  Two issuers, because one thread issues an MMA about as fast as the tensor core
+// computes a 128 x 128 x 32 one: a pair's MMAs are issued by both at once.  An issuer waits
+// FULL of each operand stage its k-blocks read and commits EMPTY after the last of them
+// (below 128-wide k-blocks both issuers read every stage, so the plan's EMPTY barriers then
+// count two commits).  Every other k-block keeps an issuer's FULL waits at most two k-tiles
+// apart, so a ring of two stages keeps them unambiguous.  PB = bk / 32 MMAs per k-block.
 template <int PB>
 __device__ __forceinline__ void run_mma_bs(const KernelParams& p, const Ctx& c, int r, uint32_t tmem_base,
                                            uint32_t smem_a, uint32_t smem_b, uint32_t bar_full, uint32_t bar_empty,
@@ -62,6 +67,7 @@ __device__ __forceinline__ void run_mma_bs(const KernelParams& p, const Ctx& c, 
   int stage = 0;
   uint32_t phase = 0;
   uint32_t q0 = 0;       // pairs of this CTA before the current item
+  uint32_t kb0 = 0;      // k-blocks of this CTA before the current item
   bool ok = true;
   long long wait_full = 0, wait_pempty = 0, kblocks = 0;   // role-cycle counters (debug)
   const bool stats = p.stats != nullptr && r == 0;
@@ -71,43 +77,47 @@ __device__ __forceinline__ void run_mma_bs(const KernelParams& p, const Ctx& c, 
   while (ok && work_next(p.sched, it, w)) {
     const int nkb = w.k_count * PER_ATOM;
     const int npairs = (nkb + 1) >> 1;
-    for (int i = static_cast<int>((q0 + static_cast<uint32_t>(r)) & 1u); i < npairs; i += 2) {
-      const uint32_t use = (q0 + static_cast<uint32_t>(i)) >> 1;   // earlier uses of slot r
+    // this issuer's k-blocks of the item: j = first, first + 2, ...
+    const int first = static_cast<int>((kb0 + static_cast<uint32_t>(r)) & 1u);
+    for (int i = 0; i < npairs; ++i) {
+      const uint32_t q = q0 + static_cast<uint32_t>(i);
+      const int slot = static_cast<int>(q & 1u);
       const long long t1 = stats ? clock64() : 0;
-      if (!wait_phase<1>(p, c, bar_pempty + 8 * r, (use & 1u) ^ 1u, ROLE_MMA)) { ok = false; break; }
+      if (!wait_phase<1>(p, c, bar_pempty + 8 * slot, ((q >> 1) & 1u) ^ 1u, ROLE_MMA)) { ok = false; break; }
       if (stats) wait_pempty += clock64() - t1;
       ptx::tc_fence_after();
-      const int j0 = 2 * i;
-      const int j1 = j0 + 2 < nkb ? j0 + 2 : nkb;
-      for (int j = j0; j < j1; ++j) {
-        const int jin = j % PER_ATOM;   // k-block inside its k-tile
-        if (j == j0 || jin == 0) {      // this issuer's first k-block of a k-tile: its stage
-          const int32_t kt = kt_item + j / PER_ATOM;
-          while (kt_cur < kt) {
-            ++kt_cur;
-            if (++stage == p.stages) { stage = 0; phase ^= 1u; }
-          }
-          const long long t0 = stats ? clock64() : 0;
-          if (!wait_phase<1>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
-          if (stats) wait_full += clock64() - t0;
-        }
-        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
-        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
-        const uint32_t d = tmem_base + static_cast<uint32_t>((2 * r + (j - j0)) * 128);
-#pragma unroll
-        for (int pos = 0; pos < PB; ++pos) {
-          // 32 bytes of K per MMA inside the 128-byte atom; the first MMA overwrites
-          const uint64_t off = static_cast<uint64_t>((jin * PB + pos) * 2);
-          ptx::mma_f8(d, a_desc + off, b_desc + off, idesc, pos != 0);
-        }
-        if (stats) ++kblocks;
-        // the stage is free once this issuer's MMAs reading it have completed
-        if (j == j1 - 1 || jin == PER_ATOM - 1) ptx::mma_commit(bar_empty + 8 * stage);
+      const int j = 2 * i + first;   // this issuer's k-block of the pair, if the pair has it
+      if (j >= nkb) {                // a lone last k-block of the other issuer
+        ptx::mbar_arrive(bar_pfull + 8 * slot);
+        continue;
       }
-      if (!ok) break;
-      ptx::mma_commit(bar_pfull + 8 * r);
+      const int jin = j % PER_ATOM;   // k-block inside its k-tile
+      if (jin < 2 || PER_ATOM == 1) {  // this issuer's first k-block of a k-tile: its stage
+        const int32_t kt = kt_item + j / PER_ATOM;
+        while (kt_cur < kt) {
+          ++kt_cur;
+          if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+        }
+        const long long t0 = stats ? clock64() : 0;
+        if (!wait_phase<1>(p, c, bar_full + 8 * stage, phase, ROLE_MMA)) { ok = false; break; }
+        if (stats) wait_full += clock64() - t0;
+      }
+      const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
+      const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
+      const uint32_t d = tmem_base + static_cast<uint32_t>((2 * slot + (j - 2 * i)) * 128);
+#pragma unroll
+      for (int pos = 0; pos < PB; ++pos) {
+        // 32 bytes of K per MMA inside the 128-byte atom; the first MMA overwrites
+        const uint64_t off = static_cast<uint64_t>((jin * PB + pos) * 2);
+        ptx::mma_f8(d, a_desc + off, b_desc + off, idesc, pos != 0);
+      }
+      if (stats) ++kblocks;
+      // the stage is free once this issuer's MMAs reading it have completed
+      if (jin + 2 >= PER_ATOM || j + 2 >= nkb) ptx::mma_commit(bar_empty + 8 * stage);
+      ptx::mma_commit(bar_pfull + 8 * slot);
     }
     q0 += static_cast<uint32_t>(npairs);
+    kb0 += static_cast<uint32_t>(nkb);
     kt_item += w.k_count;
   }
   if (stats) {
@@ -256,13 +266,16 @@ __device__ __forceinline__ void run_epilogue_bs(const KernelParams& p, const Ctx
             const float* sk = k == 0 ? s0 : s1;
             float v[32];
             ptx::tmem_load_32cols(tmem_base + lane_off + static_cast<uint32_t>((k == 0 ? pb : pb1) * 128) + col, v);
+            if (h == 1 && (k == 1 || !pair)) {
+              // the slot's last partial is in registers: release the slot before folding it
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(bar_pempty + 8 * slot);
+            }
             if (PER_COL) bs_fold_columns(k == 0 ? sa0 : sa1, sk + cs, v, r + 32 * h);
             else bs_fold_shared((k == 0 ? sa0 : sa1) * sk[cs], v, r + 32 * h);
           }
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar_pempty + 8 * slot);   // the partials are in registers
         if (stat_thread) busy += clock64() - t1;
       }
     }
@@ -325,14 +338,14 @@ __global__ void __launch_bounds__(kBsThreads, 1) gemm_bs_kernel(const __grid_con
   c.unit = static_cast<int32_t>(blockIdx.x);
 
   if (threadIdx.x == 0) {
-    // with 32-wide k-blocks both issuers read every stage (one pair each)
-    const uint32_t readers = p.bs_k == 32 ? 2u : 1u;
+    // below 128-wide k-blocks both issuers read every stage
+    const uint32_t readers = p.bs_k == 128 ? 1u : 2u;
     for (int s = 0; s < Cfg::STAGES; ++s) {
       ptx::mbar_init(bar_full + 8 * s, 1);
       ptx::mbar_init(bar_empty + 8 * s, readers);
     }
     for (int b = 0; b < kBsPairSlots; ++b) {
-      ptx::mbar_init(bar_pfull + 8 * b, 1);
+      ptx::mbar_init(bar_pfull + 8 * b, 2);   // both issuers
       ptx::mbar_init(bar_pempty + 8 * b, kBsWarps);
     }
     ptx::mbar_init(bar_drain, 2);
