@@ -18,6 +18,12 @@ br = 1, bk = 32 is the microscaling layout (one scale per 32 consecutive K eleme
 a row); br = bk = 32 the page's 32 x 32 tiles.  The scales are FP64 values here (the
 formats' power-of-two scales are a special case).  The sum is taken in FP64 by a
 matrix product of the scaled, decoded operands.
+
+The page gives one tile shape per matrix; the two operands may take different ones
+(reading: B's tiles may have their own row count br_b, sharing bk, so that k-block
+boundaries coincide), e.g. 1 x 128 tiles of A with 128 x 128 tiles of B:
+
+    C[i][j] = sum_k  dec(A[i][k]) sA[i // br][k // bk] * dec(B[j][k]) sB[j // br_b][k // bk].
 """
 from __future__ import annotations
 
@@ -32,21 +38,24 @@ def expand(s: np.ndarray, rows: int, K: int, br: int, bk: int) -> np.ndarray:
     return np.repeat(np.repeat(s, br, axis=0), bk, axis=1)[:rows, :K]
 
 
-def gemm_block_scaled(a: np.ndarray, b: np.ndarray, sA: np.ndarray, sB: np.ndarray, block=(1, 32), rows=None):
+def gemm_block_scaled(a: np.ndarray, b: np.ndarray, sA: np.ndarray, sB: np.ndarray, block=(1, 32), rows=None,
+                      block_rows_b=None):
     """C (M x N, FP64) from decoded operands a (M x K) and b (N x K) and their tile
-    scales sA (ceil(M / br) x ceil(K / bk)) and sB (ceil(N / br) x ceil(K / bk)).
-    rows: only these rows of C (the same definition evaluated for a subset of i)."""
+    scales sA (ceil(M / br) x ceil(K / bk)) and sB (ceil(N / br_b) x ceil(K / bk)),
+    br_b = block_rows_b (default br).  rows: only these rows of C (the same definition
+    evaluated for a subset of i)."""
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     br, bk = block
+    br_b = br if block_rows_b is None else block_rows_b
     (M, K), (N, K2) = a.shape, b.shape
     if K != K2:
         raise ValueError("A and B disagree on K")
     if rows is None:
-        return (a * expand(sA, M, K, br, bk)) @ (b * expand(sB, N, K, br, bk)).T
+        return (a * expand(sA, M, K, br, bk)) @ (b * expand(sB, N, K, br_b, bk)).T
     rows = np.asarray(rows, dtype=np.int64)
     s = np.asarray(sA, dtype=np.float64)
     if s.shape != (-(-M // br), -(-K // bk)):
         raise ValueError(f"scale shape {s.shape} does not tile {M} x {K} by {br} x {bk}")
     sa_rows = np.repeat(s[rows // br], bk, axis=1)[:, :K]
-    return (a[rows] * sa_rows) @ (b * expand(sB, N, K, br, bk)).T
+    return (a[rows] * sa_rows) @ (b * expand(sB, N, K, br_b, bk)).T

@@ -79,3 +79,24 @@ def test_row_subset_equals_the_full_result_rows():
         assert np.allclose(BS.gemm_block_scaled(a, b, sA, sB, (br, bk), rows=rows), full[rows], rtol=1e-13, atol=1e-13)
     with pytest.raises(ValueError):
         BS.gemm_block_scaled(a, b, np.ones((2, 3)), np.ones((1, 3)), (1, 32), rows=[0])
+
+
+def test_brute_force_tiny_with_separate_row_blocks_for_b():
+    rng = np.random.default_rng(4)
+    M, N, K, br, br_b, bk = 3, 5, 6, 1, 4, 4
+    a, b = rng.normal(size=(M, K)), rng.normal(size=(N, K))
+    sA, sB = rng.uniform(0.5, 2, size=(3, 2)), rng.uniform(0.5, 2, size=(2, 2))
+    want = np.zeros((M, N))
+    for i, j, k in itertools.product(range(M), range(N), range(K)):
+        want[i, j] += a[i, k] * sA[i // br, k // bk] * b[j, k] * sB[j // br_b, k // bk]
+    got = BS.gemm_block_scaled(a, b, sA, sB, block=(br, bk), block_rows_b=br_b)
+    assert np.allclose(got, want, rtol=1e-14, atol=1e-14)
+    rows = np.array([0, 2])
+    assert np.allclose(BS.gemm_block_scaled(a, b, sA, sB, (br, bk), rows=rows, block_rows_b=br_b), want[rows],
+                       rtol=1e-14, atol=1e-14)
+    # B's row blocks equal to A's: the one-shape form
+    sB2 = rng.uniform(0.5, 2, size=(5, 2))
+    assert np.array_equal(BS.gemm_block_scaled(a, b, sA, sB2, (1, bk), block_rows_b=1),
+                          BS.gemm_block_scaled(a, b, sA, sB2, (1, bk)))
+    with pytest.raises(ValueError):   # sB must tile B by br_b
+        BS.gemm_block_scaled(a, b, sA, sB, block=(br, bk))
