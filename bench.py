@@ -47,7 +47,7 @@ TARGET_PAIR = ("c3_e4m3_8192", "c2x_bf16_8192")
 EXTRA = ["c2x_bf16_8192", "c2_bf16_4096", "c2_bf16_4096_1cta", "c1_bf16_256", "c4_bf16_streamk_pairs",
          "c4_bf16_streamk", "c4_bf16_hybrid_pairs", "c4_bf16_persistent", "c4_bf16_hybrid", "c4_bf16_hytis",
          "c5_bf16_epilogue", "c6_bf16_fp8_epilogue", "c3m_e4m3_e5m2_8192", "c3b_e4m3_8192_blk32",
-         "c3b_e4m3_8192_blk1x128", "c3b_e4m3_8192_blk128", "g1_bf16_grouped",
+         "c3b_e4m3_8192_blk1x128", "c3b_e4m3_8192_blk128", "c3b_e4m3_8192_blk1x128_b128", "g1_bf16_grouped",
          "g2_bf16_grouped_shapes"]
 DESCR = {
     "c1_bf16_256": "BF16 GEMM 256^3, U[-1,1], FP32 out, linear N-fast, static",
@@ -83,6 +83,9 @@ DESCR = {
                               "1x128 tile: per row and 128 K), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
     "c3b_e4m3_8192_blk128": "FP8-e4m3 GEMM 8192^3 with block-scaled operands (one power-of-two FP32 scale per "
                             "128x128 tile), BF16 out, 128x128 tiles, grouped-N G=16, persistent",
+    "c3b_e4m3_8192_blk1x128_b128": "FP8-e4m3 GEMM 8192^3 with block-scaled operands (one power-of-two FP32 scale "
+                                   "per 1x128 tile of A and per 128x128 tile of B), BF16 out, 128x128 tiles, "
+                                   "grouped-N G=16, persistent",
     "g2_bf16_grouped_shapes": "grouped BF16 GEMM over 12 problems of different shapes (seeded M_g in [256, 4096], "
                               "N_g, K_g in {1024..8192}; 0.68 TFLOP), each with its own A, B, D; BF16 out, "
                               "grouped-M G=8 inside each group, one persistent launch",
@@ -173,11 +176,11 @@ def oracle_step(w, inp, rows, addend=None, b_decoded=None):
         # block-scaled operands: the oracle's block expansion on the sampled rows, then the
         # tensor-wise scales and alpha (the basic epilogue)
         from oracle import blockscale as BS
-        br, bk = w["ab_block"]
+        br, bk, br_b = ab_shape(w)
         sa, sb = block_scales(w)
         rows = np.asarray(rows, dtype=np.int64)
         a = oracle.decode(inp.A[rows], fa) * np.repeat(sa[rows // br].astype(np.float64), bk, axis=1)[:, :w["K"]]
-        b = (b_decoded if b_decoded is not None else oracle.decode(inp.B, fb)) * BS.expand(sb, w["N"], w["K"], br, bk)
+        b = (b_decoded if b_decoded is not None else oracle.decode(inp.B, fb)) * BS.expand(sb, w["N"], w["K"], br_b, bk)
         s = w.get("alpha", 1.0) * (float(inp.scales[0]) * float(inp.scales[1]) if inp.scales is not None else 1.0)
         return s * (a @ b.T), s * (np.abs(a) @ np.abs(b).T)
     if epi is None:
@@ -209,13 +212,21 @@ def oracle_rows_per_step(cores):
     return 4 * max(1, cores)
 
 
+def ab_shape(w):
+    """(br, bk, br_b) of a workload with block-scaled operands: A's tile rows, the shared
+    k-block, B's tile rows (A's unless the workload gives its own)."""
+    t = tuple(w["ab_block"])
+    return (t[0], t[1], t[2] if len(t) > 2 and t[2] else t[0])
+
+
 def block_scales(w):
     """Seeded power-of-two block scales (2^-3 .. 2^3) of A and B for a workload with
-    block-scaled operands: ceil(rows / br) x ceil(K / bk) FP32 each."""
-    br, bk = w["ab_block"]
+    block-scaled operands: ceil(M / br) x ceil(K / bk) and ceil(N / br_b) x ceil(K / bk)
+    FP32."""
+    br, bk, br_b = ab_shape(w)
     out = []
-    for rows, seed in ((w["M"], 9800), (w["N"], 9900)):
-        shape = (-(-rows // br), -(-w["K"] // bk))
+    for rows, r_blk, seed in ((w["M"], br, 9800), (w["N"], br_b, 9900)):
+        shape = (-(-rows // r_blk), -(-w["K"] // bk))
         e = (synthetic_splitmix(seed + w["case"], shape[0] * shape[1]) % np.uint64(7)).astype(np.int64) - 3
         out.append((2.0 ** e).astype(np.float32).reshape(shape))
     return out
@@ -347,9 +358,9 @@ def workload_bytes(w):
     epi = w.get("epi") or {}
     if "c_dtype" in epi:
         total += w["M"] * w["N"] * elt_bytes(epi["c_dtype"])
-    if "ab_block" in w:   # one FP32 scale per br x bk tile of A and of B
-        br, bk = w["ab_block"]
-        total += (-(-w["M"] // br) + -(-w["N"] // br)) * -(-w["K"] // bk) * 4
+    if "ab_block" in w:   # one FP32 scale per br x bk tile of A and per br_b x bk tile of B
+        br, bk, br_b = ab_shape(w)
+        total += (-(-w["M"] // br) + -(-w["N"] // br_b)) * -(-w["K"] // bk) * 4
     return total
 
 

@@ -189,11 +189,15 @@ typedef struct {
     int32_t block_scale; /* 1: e4m3 D with one power-of-two scale per 32 x 32 tile (see above);
                             needs out_dtype TST_OUT_E4M3 and no d_scale */
     int32_t ab_block_rows; /* block-scaled FP8 operands ("H100 . WGMMA Part 2" section 11): with
-                            ab_block_k > 0, A and B carry one FP32 scale per ab_block_rows x
-                            ab_block_k tile of (rows x K) and
-                              Acc[i][j] = sum_k a_ik sA[i / br][k / bk] * b_jk sB[j / br][k / bk]
-                            (br = ab_block_rows >= 1, bk = ab_block_k in {32, 64, 128}; e.g.
-                            32 x 32 tiles, or 1 x 32 for one scale per 32 K of a row).  The
+                            ab_block_k > 0, A carries one FP32 scale per ab_block_rows x
+                            ab_block_k tile of (rows x K), B one per ab_block_rows_b x
+                            ab_block_k tile, and
+                              Acc[i][j] = sum_k a_ik sA[i / br][k / bk] * b_jk sB[j / br_b][k / bk]
+                            (br = ab_block_rows >= 1, br_b = ab_block_rows_b, 0 meaning br,
+                            bk = ab_block_k in {32, 64, 128}; e.g. 32 x 32 tiles, 1 x 32 for one
+                            scale per 32 K of a row, or 1 x 128 tiles of A with 128 x 128 of B;
+                            sA is ceil(M / br) x ceil(K / bk), sB ceil(N / br_b) x ceil(K / bk),
+                            row-major FP32).  The
                             tensor core sums each k-block of bk into a fresh partial and the
                             epilogue warps add (sA * sB) * partial in FP32 (the page's section
                             15.3 multi-stage accumulation).  Needs FP8 operands, FP32 or BF16 D,
@@ -203,6 +207,7 @@ typedef struct {
                             (the ring's seventh stage holds the staged scales); else
                             TST_ERR_UNSUPPORTED. */
     int32_t ab_block_k;
+    int32_t ab_block_rows_b; /* rows of B's scale tiles (0: ab_block_rows; else >= 1) */
 } tst_epilogue_ex;
 
 /* Run-time operands of the extended epilogue: DEVICE pointers owned by the

@@ -83,6 +83,10 @@ WORKLOADS = {
     "c3b_e4m3_8192_blk128": dict(M=8192, N=8192, K=8192, dtype="e4m3", dist="normal", case=3, out="bf16",
                                  mapping=("grouped_n", 16), schedule="persistent", bn=128, cta_group=1,
                                  use_scales=True, ab_block=(128, 128)),
+    # the same with 1 x 128 tiles of A (a row's 128 K) and 128 x 128 tiles of B: (br, bk, br_b)
+    "c3b_e4m3_8192_blk1x128_b128": dict(M=8192, N=8192, K=8192, dtype="e4m3", dist="normal", case=3, out="bf16",
+                                        mapping=("grouped_n", 16), schedule="persistent", bn=128, cta_group=1,
+                                        use_scales=True, ab_block=(1, 128, 128)),
     # 8192^3 with mixed FP8 formats: A e4m3, B e5m2 (tensor-wise scales) -> BF16, grouped-N G=16
     "c3m_e4m3_e5m2_8192": dict(M=8192, N=8192, K=8192, dtype="e4m3_e5m2", dist="normal", case=3, out="bf16",
                                mapping=("grouped_n", 16), schedule="persistent", bn=256, cta_group=2,

@@ -110,3 +110,11 @@ def test_run_args_match_the_entry_points_signatures():
     scaled = bench.run_args({"a_block_scales": 3, "b_block_scales": 4})
     assert (scaled["a_block_scales"], scaled["b_block_scales"]) == (3, 4)
     assert set(scaled) <= set(inspect.signature(tst.gemm_run).parameters)
+
+
+def test_block_scale_shapes_with_separate_b_tiles():
+    w = dict(M=300, N=200, K=1000, case=3, ab_block=(1, 128, 64))
+    assert bench.ab_shape(w) == (1, 128, 64)
+    assert bench.ab_shape(dict(w, ab_block=(32, 64))) == (32, 64, 32)
+    sa, sb = bench.block_scales(w)
+    assert sa.shape == (300, 8) and sb.shape == (4, 8)

@@ -32,16 +32,17 @@ def _scales(seed, rows, K, br, bk, pow2=True):
 
 
 def _run(M, N, K, br, bk, out, schedule="persistent", mapping=("grouped_m", 4), dtype="e4m3", dist="int:4",
-         pow2=True, alpha=1.0, bias=False, relu=False, seed=0):
+         pow2=True, alpha=1.0, bias=False, relu=False, seed=0, br_b=None):
     xa = synthetic.draw(dist, 9600 + seed, M * K).reshape(M, K).astype(np.float32)
     xb = synthetic.draw(dist, 9700 + seed, N * K).reshape(N, K).astype(np.float32)
     fa, fb = synthetic.operand_types(dtype)
     enc = {"e4m3": synthetic.e4m3_bytes, "e5m2": synthetic.e5m2_bytes}
     A, B = enc[fa](xa), enc[fb](xb)
-    sA, sB = _scales(9800 + seed, M, K, br, bk, pow2), _scales(9900 + seed, N, K, br, bk, pow2)
+    sA, sB = _scales(9800 + seed, M, K, br, bk, pow2), _scales(9900 + seed, N, K, br_b or br, bk, pow2)
     bv = synthetic.draw("int:4", 9950 + seed, N).astype(np.float32) if bias else None
     plan = tst.gemm_plan_create(M, N, K, dtype=dtype, mapping=mapping, schedule=schedule, out_dtype=out,
-                                alpha=alpha, has_bias=bias, relu=relu, ab_block=(br, bk))
+                                alpha=alpha, has_bias=bias, relu=relu,
+                                ab_block=(br, bk) if br_b is None else (br, bk, br_b))
     assert plan.info.bn == 128 and plan.info.cta_group == 1 and plan.info.bk == 128
     D = torch.full((M, N), float("nan"), dtype=torch.float32 if out == "f32" else torch.bfloat16, device="cuda")
     tst.gemm_run(plan, device_codes(A), device_codes(B), D, bias=torch.from_numpy(bv).cuda() if bias else None,
@@ -49,8 +50,8 @@ def _run(M, N, K, br, bk, out, schedule="persistent", mapping=("grouped_m", 4), 
     st, word = tst.gemm_status_query(plan)
     assert st == tst.TST_OK, (tst.gemm_status_string(st), hex(word))
     a, b = oracle.decode(A, fa), oracle.decode(B, fb)
-    acc = BS.gemm_block_scaled(a, b, sA, sB, (br, bk))
-    absacc = BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, (br, bk))
+    acc = BS.gemm_block_scaled(a, b, sA, sB, (br, bk), block_rows_b=br_b)
+    absacc = BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, (br, bk), block_rows_b=br_b)
     z = alpha * acc + (bv.astype(np.float64)[None, :] if bias else 0.0)
     if relu:
         z = np.maximum(z, 0.0)
@@ -65,6 +66,15 @@ def test_block_scaled_small_integers_exact(br, bk, out):
     want = z if out == "f32" else oracle.decode(oracle.round_bf16(z), "bf16")
     assert np.abs(z).max() < 2 ** 22
     assert np.array_equal(got, want), np.argwhere(got != want)[:5]
+
+
+@pytest.mark.parametrize("br,bk,br_b", [(1, 128, 128), (32, 32, 128), (128, 64, 1), (1, 32, 32), (64, 128, 3)])
+def test_block_scaled_separate_b_tiles_exact(br, bk, br_b):
+    # B's scale tiles with their own row count: shared per 32-column chunk (br_b a multiple of
+    # 32) or per column, whatever A's tiles are; ragged in M, N and K
+    got, z, _ = _run(400, 328, 1040, br, bk, "f32", alpha=0.5, bias=True, seed=br + bk + br_b, br_b=br_b)
+    assert np.abs(z).max() < 2 ** 22
+    assert np.array_equal(got, z), np.argwhere(got != z)[:5]
 
 
 @pytest.mark.parametrize("schedule,mapping", [("static", ("linear_nfast", 1)), ("persistent", ("grouped_n", 2)),
@@ -142,7 +152,8 @@ def test_block_scaled_timeout_on_missing_load_reports_and_recovers():
     assert np.array_equal(host_values(D), want)
 
 
-@pytest.mark.parametrize("name", ["c3b_e4m3_8192_blk32", "c3b_e4m3_8192_blk1x128", "c3b_e4m3_8192_blk128"])
+@pytest.mark.parametrize("name", ["c3b_e4m3_8192_blk32", "c3b_e4m3_8192_blk1x128", "c3b_e4m3_8192_blk128",
+                                  "c3b_e4m3_8192_blk1x128_b128"])
 def test_block_scaled_workload_full_size_sampled_rows(name):
     # the benchmark's 8192^3 workload in the benchmark's plan, with its seeded power-of-two
     # block scales and tensor-wise scales: sampled rows against the oracle within the bound
@@ -160,8 +171,9 @@ def test_block_scaled_workload_full_size_sampled_rows(name):
     rows = sample_rows(w["M"], count=12)
     a, b = oracle.decode(inp.A, "e4m3"), oracle.decode(inp.B, "e4m3")
     s = w.get("alpha", 1.0) * float(inp.scales[0]) * float(inp.scales[1])
-    z = s * BS.gemm_block_scaled(a, b, sA, sB, w["ab_block"], rows=rows)
-    ad = abs(s) * BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, w["ab_block"], rows=rows)
+    br, bk, br_b = bench.ab_shape(w)
+    z = s * BS.gemm_block_scaled(a, b, sA, sB, (br, bk), rows=rows, block_rows_b=br_b)
+    ad = abs(s) * BS.gemm_block_scaled(np.abs(a), np.abs(b), sA, sB, (br, bk), rows=rows, block_rows_b=br_b)
     assert_close(host_values(C)[rows], z, ad, "bf16", name)
 
 

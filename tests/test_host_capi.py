@@ -426,6 +426,10 @@ def test_block_scaled_operand_plan_rules():
     assert (p.info.bn, p.info.cta_group, p.info.bk, p.info.tma_store, p.info.stages) == (128, 1, 128, 0, 6)
     assert tst.gemm_plan_create(1000, 1000, 1024, dtype="e4m3", schedule="persistent", ab_block=(1, 128), stages=2,
                                 **kw).info.stages == 2
+    # B's own tile rows (0: A's)
+    for ab in ((1, 128, 128), (1, 128, 0), (32, 64, 7)):
+        assert tst.gemm_plan_create(1000, 1000, 1024, dtype="e4m3", schedule="persistent", ab_block=ab,
+                                    **kw).info.bn == 128
     for bad, status in ((dict(dtype="bf16"), tst.TST_ERR_UNSUPPORTED),
                         (dict(dtype="e4m3", stages=7), tst.TST_ERR_UNSUPPORTED),   # the scales' stage
                         (dict(dtype="e4m3", schedule="streamk"), tst.TST_ERR_UNSUPPORTED),
@@ -434,7 +438,8 @@ def test_block_scaled_operand_plan_rules():
                         (dict(dtype="e4m3", activation="gelu"), tst.TST_ERR_UNSUPPORTED),
                         (dict(dtype="e4m3", out_dtype="e4m3"), tst.TST_ERR_UNSUPPORTED),
                         (dict(dtype="e4m3", ab_block=(32, 48)), tst.TST_ERR_INVALID_ARG),
-                        (dict(dtype="e4m3", ab_block=(0, 32)), tst.TST_ERR_INVALID_ARG)):
+                        (dict(dtype="e4m3", ab_block=(0, 32)), tst.TST_ERR_INVALID_ARG),
+                        (dict(dtype="e4m3", ab_block=(1, 128, -1)), tst.TST_ERR_INVALID_ARG)):
         args = dict(schedule="persistent", ab_block=(32, 32))
         args.update(bad)
         with pytest.raises(tst.TstError) as e:

@@ -123,13 +123,14 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
     extended = bool(has_c or bmode == TST_BIAS_ROW or act in (TST_ACT_GELU, TST_ACT_SILU) or row_scale or
                     col_scale or d_scale or amax or aux or block_scale)
     h = ctypes.c_void_p()
-    br, bk = ab_block if ab_block is not None else (0, 0)
+    br, bk, br_b = (tuple(ab_block) + (0,))[:3] if ab_block is not None else (0, 0, 0)
     if extended or ab_block is not None:
         epi = _capi.tst_epilogue_ex(_enum(_OUT, out_dtype, "out_dtype"), float(alpha), float(beta),
                                     int(bool(has_c)), _enum(_OUT, c_dtype, "c_dtype"), bmode, act,
                                     int(bool(use_scales)), int(bool(row_scale)), int(bool(col_scale)),
                                     int(bool(d_scale)), int(bool(amax)), int(bool(aux)),
-                                    _enum(_OUT, aux_dtype, "aux_dtype"), int(bool(block_scale)), int(br), int(bk))
+                                    _enum(_OUT, aux_dtype, "aux_dtype"), int(bool(block_scale)), int(br), int(bk),
+                                    int(br_b))
         _check(lib.gemm_plan_create_epi(ctypes.byref(h), int(M), int(N), int(K), _enum(_DTYPES, dtype, "dtype"),
                                         TST_LAYOUT_A_ROW_B_NK, m, _enum(_SCHED, schedule, "schedule"),
                                         ctypes.byref(epi), ctypes.byref(opts)), "gemm_plan_create_epi")

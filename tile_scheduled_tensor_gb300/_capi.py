@@ -48,7 +48,8 @@ class tst_epilogue_ex(ctypes.Structure):
                 ("activation", ctypes.c_int32), ("use_scales", ctypes.c_int32), ("row_scale", ctypes.c_int32),
                 ("col_scale", ctypes.c_int32), ("d_scale", ctypes.c_int32), ("amax", ctypes.c_int32),
                 ("aux", ctypes.c_int32), ("aux_dtype", ctypes.c_int32), ("block_scale", ctypes.c_int32),
-                ("ab_block_rows", ctypes.c_int32), ("ab_block_k", ctypes.c_int32)]
+                ("ab_block_rows", ctypes.c_int32), ("ab_block_k", ctypes.c_int32),
+                ("ab_block_rows_b", ctypes.c_int32)]
 
 
 class tst_epilogue_args(ctypes.Structure):

@@ -263,6 +263,9 @@ bool valid_in(int32_t t) { return t == TST_OUT_F32 || t == TST_OUT_BF16; }
 int out_bytes(int32_t t) { return t == TST_OUT_F32 ? 4 : t == TST_OUT_BF16 ? 2 : 1; }
 
 // whether the epilogue needs more than the basic alpha / column bias / ReLU / scales path
+// rows of B's scale tiles of a block-scaled plan (0 in the options: A's)
+int32_t bs_rows_b(const tst_epilogue_ex& e) { return e.ab_block_rows_b > 0 ? e.ab_block_rows_b : e.ab_block_rows; }
+
 bool needs_ext(const tst_epilogue_ex& e) {
   return e.out_dtype == TST_OUT_E4M3 || e.has_c || e.bias_mode == TST_BIAS_ROW ||
          (e.activation != TST_ACT_NONE && e.activation != TST_ACT_RELU) || e.row_scale || e.col_scale ||
@@ -311,7 +314,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   const bool bs = epi->ab_block_k != 0;
   if (bs) {
     if (epi->ab_block_k != 32 && epi->ab_block_k != 64 && epi->ab_block_k != 128) return TST_ERR_INVALID_ARG;
-    if (epi->ab_block_rows < 1) return TST_ERR_INVALID_ARG;
+    if (epi->ab_block_rows < 1 || epi->ab_block_rows_b < 0) return TST_ERR_INVALID_ARG;
     if (dtype == TST_BF16 || needs_ext(*epi) || groups > 0 || (schedule != TST_STATIC && schedule != TST_PERSISTENT) ||
         (o.bn != 0 && o.bn != 128) || (o.cta_group != 0 && o.cta_group != 1) || (o.bk != 0 && o.bk != 128) ||
         o.cluster_n == 2 || o.pdl || o.epilogue_store == TST_STORE_TMA || o.l2_prefetch)
@@ -416,7 +419,7 @@ tst_status create_plan(tst_plan** out, int64_t M, int64_t N, int64_t K, tst_dtyp
   if (!p->host_only) {
     // the extended epilogue has its own instance (two epilogue warpgroups, typed stores of D)
     const int kdt = dtype == TST_BF16 ? tst::DT_BF16 : tst::DT_E4M3;
-    p->kernel = p->bs       ? tst_bs_kernel(kernel_out(*p), epi->ab_block_rows % 32 != 0)
+    p->kernel = p->bs       ? tst_bs_kernel(kernel_out(*p), bs_rows_b(*epi) % 32 != 0)
                 : p->ext_on ? tst_kernel_ext(kdt, p->bn, p->cg, p->ka)
                             : tst_kernel(kdt, p->bn, kernel_out(*p), p->cg, p->ka, p->mc);
     if (!p->kernel ||
@@ -935,6 +938,7 @@ tst_status launch(tst_plan* p, const void* A, const void* B, void* C, const tst_
     kp.bs_a = ea->a_block_scales;
     kp.bs_b = ea->b_block_scales;
     kp.bs_rows = e.ab_block_rows;
+    kp.bs_rows_b = bs_rows_b(e);
     kp.bs_k = e.ab_block_k;
     kp.bs_kblocks = static_cast<int32_t>(ceil_div(p->K, e.ab_block_k));
   }

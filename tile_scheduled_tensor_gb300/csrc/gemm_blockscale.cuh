@@ -1,6 +1,6 @@
 // Block-scaled FP8 GEMM for sm_103a: one FP32 scale per small tile of each operand.
 //
-//   C[i][j] = epilogue( sum_k a_ik sA[i / br][k / bk] * b_jk sB[j / br][k / bk] )
+//   C[i][j] = epilogue( sum_k a_ik sA[i / br][k / bk] * b_jk sB[j / br_b][k / bk] )
 //
 // Block-wise scaling ("H100 . WGMMA Part 2", section 11: one scale per small tile of the
 // matrix, e.g. 32 x 32, besides the tensor-wise and vector-wise forms) makes the scale
@@ -156,7 +156,7 @@ __device__ __forceinline__ void bs_stage_window(const KernelParams& p, const Wor
   const int32_t lim = is_a ? p.M : p.N;
   int32_t idx = is_a ? w.row0 + e : w.col0 + (e - 128);
   idx = idx < lim ? idx : lim - 1;   // rows and columns past the matrix carry zero partials
-  const float* src = (is_a ? p.bs_a : p.bs_b) + static_cast<int64_t>(idx / p.bs_rows) * p.bs_kblocks;
+  const float* src = (is_a ? p.bs_a : p.bs_b) + static_cast<int64_t>(idx / (is_a ? p.bs_rows : p.bs_rows_b)) * p.bs_kblocks;
 #pragma unroll
   for (int i = 0; i < kBsWindow; ++i) {
     int32_t kb = kb0 + i;
@@ -187,8 +187,8 @@ __device__ __forceinline__ void bs_fold_columns(float sa, const float* sb, const
   }
 }
 
-// PER_COL: B's scale rows change inside a 32-column chunk (br not a multiple of 32), so
-// every column takes its own scale; else one per chunk.
+// PER_COL: B's scale rows change inside a 32-column chunk (B's tile rows not a multiple of
+// 32), so every column takes its own scale; else one per chunk.
 template <int OUT, bool PER_COL>
 __device__ __forceinline__ void run_epilogue_bs(const KernelParams& p, const Ctx& c, uint32_t tmem_base,
                                                 uint32_t bar_pfull, uint32_t bar_pempty, uint32_t win_smem,

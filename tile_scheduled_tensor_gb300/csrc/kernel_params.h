@@ -100,10 +100,12 @@ struct KernelParams {
   int32_t l2_hint;          // operand loads' L2 policy: 0 none, 1 A evict_last / B normal, 2 the reverse
   int32_t l2_prefetch;      // 0, or the distance in k-tiles of the L2 prefetch issued with each load
   // block-scaled operands (gemm_bs_kernel): one FP32 scale per bs_rows x bs_k tile of A
-  // (ceil(M / bs_rows) x bs_kblocks, row-major) and of B (ceil(N / bs_rows) x bs_kblocks)
+  // (ceil(M / bs_rows) x bs_kblocks, row-major) and per bs_rows_b x bs_k tile of B
+  // (ceil(N / bs_rows_b) x bs_kblocks)
   const float* bs_a;
   const float* bs_b;
   int32_t bs_rows, bs_k, bs_kblocks;
+  int32_t bs_rows_b;
   int32_t box3d;            // A and B maps are 3-D (atom elements, rows, atoms): one box per operand
                             // and stage brings all KA atom columns (HyTiS half-width B stays 2-D)
   int32_t staging_offset;   // SK_TMA: byte offset of the staging buffers from the aligned shared base
