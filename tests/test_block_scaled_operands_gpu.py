@@ -1,5 +1,6 @@
 """GPU parity of block-scaled FP8 operands (plan option ab_block = (br, bk): one FP32 scale
-per br x bk tile of A and of B) against the oracle's gemm_block_scaled.
+per br x bk tile of A and of B; (br, bk, br_b): B's tiles of br_b rows) against the oracle's
+gemm_block_scaled.
 
 Exact where every value is exactly representable: small-integer e4m3 codes, power-of-two
 scales and sums below 2^24 make each k-block partial, its scaled product and the running
@@ -7,7 +8,8 @@ FP32 sum exact, so the kernel and the FP64 oracle agree bit for bit (a BF16 D is
 oracle's round-to-nearest-even of the exact value).  Random normal inputs with scales
 that are not powers of two stay within 4e-3 of sum_k |a sA| |b sB| (+ 1e-6).  Tilings:
 the page's 32 x 32 tiles, the microscaling 1 x 32, and coarser 1 x 128, 128 x 128,
-32 x 64; ragged M, N and K against the tiles and the k-blocks."""
+32 x 64, and mixed ones (1 x 128 tiles of A with 128 x 128 of B, per-column B scales under
+shared A scales); ragged M, N and K against the tiles and the k-blocks."""
 import numpy as np
 import pytest
 import torch
