@@ -106,8 +106,9 @@ def gemm_plan_create(M: int, N: int, K: int, dtype="bf16", mapping=("linear_nfas
     'gelu'/'silu', row_scale, col_scale, d_scale, amax, aux, block_scale or out_dtype 'e4m3'
     selects the extended one (gemm_plan_create_epi).  block_scale: an e4m3 D with one
     power-of-two scale per 32 x 32 tile, whose exponents gemm_run writes to block_exp.
-    ab_block=(br, bk): block-scaled FP8 operands, one scale per br x bk tile of A and of B
-    (gemm_run's a_block_scales, b_block_scales)."""
+    ab_block=(br, bk): block-scaled FP8 operands, one scale per br x bk tile of A and of B;
+    (br, bk, br_b): B's tiles of br_b rows (gemm_run's a_block_scales, ceil(M / br) x
+    ceil(K / bk), and b_block_scales, ceil(N / br_b) x ceil(K / bk), FP32 row-major)."""
     kind, group = mapping if isinstance(mapping, (tuple, list)) else (mapping, 1)
     m = _capi.tst_mapping(_enum(_MAPS, kind, "mapping"), int(group))
     opts = _capi.tst_plan_options(int(bn), int(num_ctas), int(bool(sk_forward)), int(bool(host_only)),
