@@ -196,3 +196,29 @@ def test_block_scaled_single_k_tile_items_exact():
         assert tst.gemm_status_query(plan)[0] == tst.TST_OK
         want = BS.gemm_block_scaled(oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3"), sA, sB, (br, 128))
         assert np.array_equal(host_values(D), want), br
+
+
+@pytest.mark.parametrize("ab", [(32, 32), (1, 128, 128)])
+def test_block_scaled_host_buffers_equal_the_device_run(ab):
+    # gemm_run_host: B, then A in row panels, each panel's GEMM with its own rows of A's
+    # scales (B's scales whole); bit for bit the device run, and exact against the oracle
+    M, N, K = 1100, 384, 1024
+    br, bk, br_b = (tuple(ab) + (None,))[:3]
+    xa = synthetic.draw("int:4", 9641, M * K).reshape(M, K).astype(np.float32)
+    xb = synthetic.draw("int:4", 9642, N * K).reshape(N, K).astype(np.float32)
+    A, B = synthetic.e4m3_bytes(xa), synthetic.e4m3_bytes(xb)
+    sA, sB = _scales(9643, M, K, br, bk), _scales(9644, N, K, br_b or br, bk)
+    plan = tst.gemm_plan_create(M, N, K, dtype="e4m3", mapping=("grouped_m", 4), schedule="persistent",
+                                out_dtype="f32", ab_block=ab)
+    ops = dict(a_block_scales=torch.from_numpy(sA).cuda(), b_block_scales=torch.from_numpy(sB).cuda())
+    D_dev = torch.full((M, N), float("nan"), device="cuda")
+    tst.gemm_run(plan, device_codes(A), device_codes(B), D_dev, **ops)
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    Dh = torch.full((M, N), float("nan")).pin_memory()
+    tst.gemm_run_host(plan, torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), Dh, panels=4, **ops)
+    torch.cuda.synchronize()
+    assert tst.gemm_status_query(plan)[0] == tst.TST_OK
+    assert torch.equal(Dh, D_dev.cpu())
+    want = BS.gemm_block_scaled(oracle.decode(A, "e4m3"), oracle.decode(B, "e4m3"), sA, sB, (br, bk),
+                                block_rows_b=br_b)
+    assert np.array_equal(Dh.numpy(), want)
